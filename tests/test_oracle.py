@@ -1,0 +1,464 @@
+"""Pins for the CPU oracle, independent of the oracle itself.
+
+Each test checks the oracle against something the pages or mathematics fix:
+published known-answer vectors, printed numbers, library routines that the
+definition reduces to (torch's TransformerDecoderLayer / layer_norm / gelu /
+scaled_dot_product_attention / bf16 cast, all in float64), closed forms and
+exact invariants of the method (speculative greedy == autoregressive greedy).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import synth
+from oracle import model as M
+from oracle import philox
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+# A small shape that keeps the oracle fast while exercising every code path.
+SMALL = synth.ModelShape("small", 3, 128, 2, 512, vocab=1000, max_pos=96,
+                         hist_layers=(0, 2), dtype="f32")
+
+
+def _load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+@pytest.fixture(scope="module")
+def small():
+    tw = synth.target_weights(SMALL, 11)
+    dw = synth.drafter_weights(SMALL, 11, tw)
+    orc = M.Oracle(SMALL, tw, dw)
+    A = synth.encoder_states(SMALL, 11, 0, frames=60)
+    return orc, tw, dw, A
+
+
+# ---------------------------------------------------------------- Philox
+
+def test_philox_known_answers():
+    for v in _load("philox4x32_10_kat.json")["vectors"]:
+        ctr = [int(x, 16) for x in v["ctr"]]
+        key = [int(x, 16) for x in v["key"]]
+        out = philox.philox4x32_10(ctr, key)
+        assert ["%08x" % w for w in out] == v["out"]
+
+
+def test_philox_uniform_range_and_mean():
+    u = np.array([philox.uniform(7, s, r, j, 1) for s in range(4) for r in range(50) for j in range(10)])
+    assert u.min() >= 0.0 and u.max() < 1.0
+    assert abs(u.mean() - 0.5) < 4 * math.sqrt(1 / 12 / u.size)
+
+
+# ---------------------------------------------------------------- numerics
+
+def test_round_bf16_matches_torch_cast():
+    x = np.random.default_rng(0).standard_normal(10000) * 3
+    x = np.concatenate([x, [0.0, -0.0, 1.0, 1.00390625, 1.01171875, 65504.0, 1e-30]])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(M.round_bf16(x), ref)
+
+
+def test_layer_norm_and_gelu_match_torch():
+    g = np.random.default_rng(1)
+    x = g.standard_normal((7, 96))
+    w, b = g.standard_normal(96), g.standard_normal(96)
+    ref = F.layer_norm(torch.from_numpy(x), (96,), torch.from_numpy(w), torch.from_numpy(b), eps=1e-5)
+    np.testing.assert_allclose(M.layer_norm(x, w, b), ref.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(M.gelu(x), F.gelu(torch.from_numpy(x)).numpy(), rtol=0, atol=1e-14)
+
+
+def test_mha_matches_sdpa_and_softmax_sums_to_one():
+    g = np.random.default_rng(2)
+    q, k, v = g.standard_normal((5, 128)), g.standard_normal((9, 128)), g.standard_normal((9, 128))
+    mask = np.tril(np.ones((5, 9), dtype=bool), k=4)
+    o = M.mha(q, k, v, 2, mask)
+    th = lambda a: torch.from_numpy(a).reshape(a.shape[0], 2, 64).transpose(0, 1)
+    ref = F.scaled_dot_product_attention(th(q), th(k), th(v), attn_mask=torch.from_numpy(mask))
+    np.testing.assert_allclose(o, ref.transpose(0, 1).reshape(5, 128).numpy(), atol=1e-12)
+    p = M.softmax(g.standard_normal((4, 1000)) * 10)
+    np.testing.assert_allclose(p.sum(-1), 1.0, atol=1e-12)
+
+
+def test_rope_closed_form_and_relative_position():
+    dh, H = 64, 2
+    th = M.rope_theta(dh)
+    # theta_i = 10000^(-2i/64): theta_0 = 1, theta_16 = 10000^-0.5 = 0.01
+    assert th[0] == np.float32(1.0) and abs(th[16] - 0.01) < 1e-9
+    for p in (0, 1, 7, 300):
+        for i in (0, 5, 31):
+            e = np.zeros((1, H * dh))
+            e[0, 2 * i] = 1.0
+            r = M.rope(e, np.array([p]), H)
+            ang = float(np.float32(np.float32(p) * th[i]))
+            expect = np.zeros(H * dh)
+            expect[2 * i], expect[2 * i + 1] = math.cos(ang), math.sin(ang)
+            np.testing.assert_allclose(r[0], expect, atol=1e-15)
+    g = np.random.default_rng(3)
+    q, k = g.standard_normal((1, H * dh)), g.standard_normal((1, H * dh))
+    d1 = (M.rope(q, [40], H) * M.rope(k, [13], H)).sum()
+    d2 = (M.rope(q, [140], H) * M.rope(k, [113], H)).sum()
+    assert abs(d1 - d2) < 1e-4 * (abs(d1) + 1)
+    np.testing.assert_allclose(np.linalg.norm(M.rope(q, [77], H)), np.linalg.norm(q), rtol=1e-12)
+
+
+# ---------------------------------------------------------------- target decoder
+
+def _torch_decoder(shape, tw, l):
+    d, f = shape.d_model, shape.d_ff
+    lay = torch.nn.TransformerDecoderLayer(d, shape.n_heads, f, dropout=0.0, activation="gelu",
+                                           batch_first=True, norm_first=True, dtype=torch.float64)
+    T = lambda n: torch.from_numpy(np.asarray(tw[f"layers.{l}.{n}"], dtype=np.float64))
+    z = torch.zeros(d, dtype=torch.float64)
+    with torch.no_grad():
+        lay.self_attn.in_proj_weight.copy_(T("w_qkv"))
+        lay.self_attn.in_proj_bias.copy_(torch.cat([T("b_q"), z, T("b_v")]))
+        lay.self_attn.out_proj.weight.copy_(T("w_o"))
+        lay.self_attn.out_proj.bias.copy_(T("b_o"))
+        lay.multihead_attn.in_proj_weight.copy_(torch.cat([T("w_qc"), T("w_kvc")]))
+        lay.multihead_attn.in_proj_bias.copy_(torch.cat([T("b_qc"), z, T("b_vc")]))
+        lay.multihead_attn.out_proj.weight.copy_(T("w_oc"))
+        lay.multihead_attn.out_proj.bias.copy_(T("b_oc"))
+        lay.linear1.weight.copy_(T("w_fc1")); lay.linear1.bias.copy_(T("b_fc1"))
+        lay.linear2.weight.copy_(T("w_fc2")); lay.linear2.bias.copy_(T("b_fc2"))
+        for i in (1, 2, 3):
+            getattr(lay, f"norm{i}").weight.copy_(T(f"ln{i}_g"))
+            getattr(lay, f"norm{i}").bias.copy_(T(f"ln{i}_b"))
+    return lay.eval()
+
+
+def test_full_forward_matches_torch_decoder_stack(small):
+    """The whole target forward (embeddings, every layer, final LN, tied head)
+    reduces to torch's pre-LN TransformerDecoderLayer stack."""
+    orc, tw, _, A = small
+    req = orc.new_request(A)
+    toks = [5, 17, 999, 0, 42, 42, 7]
+    logits, hist = orc.forward_full(req, toks)
+    E = torch.from_numpy(tw["tok_emb"].astype(np.float64))
+    x = (E[toks] + torch.from_numpy(tw["pos_emb"].astype(np.float64))[: len(toks)])[None]
+    mem = torch.from_numpy(A.astype(np.float64))[None]
+    causal = torch.nn.Transformer.generate_square_subsequent_mask(len(toks), dtype=torch.float64)
+    hs = []
+    with torch.no_grad():
+        for l in range(SMALL.n_layers):
+            x = _torch_decoder(SMALL, tw, l)(x, mem, tgt_mask=causal)
+            if l in SMALL.hist_layers:
+                hs.append(x[0].numpy())
+        hf = F.layer_norm(x[0], (SMALL.d_model,), torch.from_numpy(tw["lnf_g"].astype(np.float64)),
+                          torch.from_numpy(tw["lnf_b"].astype(np.float64)))
+        ref = (hf @ E.T).numpy()
+    np.testing.assert_allclose(logits, ref, rtol=0, atol=1e-9)
+    np.testing.assert_allclose(hist, np.stack(hs, 1), atol=1e-10)
+
+
+def test_cached_verify_equals_full_forward(small):
+    orc, _, _, A = small
+    toks = [3, 1, 4, 1, 5, 9, 2, 6, 5, 3, 5, 8]
+    full, fh = orc.forward_full(orc.new_request(A), toks)
+    req = orc.new_request(A)
+    got = []
+    for blk in ([0, 4], [4, 5], [5, 9], [9, 12]):
+        got.append(orc.verify(req, toks[blk[0]:blk[1]]))
+        req.L = blk[1]
+    np.testing.assert_allclose(np.concatenate(got), full, atol=1e-10)
+    np.testing.assert_allclose(req.hist[:12], fh, atol=1e-10)
+
+
+def test_causal_and_frame_mask_invariants(small):
+    orc, _, _, A = small
+    r1, r2 = orc.new_request(A, frames=40), orc.new_request(A, frames=40)
+    b1, b2 = [1, 2, 3, 4, 5, 6], [1, 2, 3, 77, 88, 99]
+    l1, l2 = orc.verify(r1, b1), orc.verify(r2, b2)
+    np.testing.assert_array_equal(l1[:3], l2[:3])         # later block tokens do not leak back
+    assert np.abs(l1[3:] - l2[3:]).max() > 1e-3
+    A2 = A.copy(); A2[40:] = 1e3                            # frames beyond F are never read
+    r3 = orc.new_request(A2, frames=40)
+    np.testing.assert_array_equal(orc.verify(r3, b1), l1)
+
+
+def test_bf16_mode_tracks_fp32(small):
+    orc, tw, dw, A = small
+    ob = M.Oracle(SMALL, tw, dw, bf16=True)
+    toks = [1, 2, 3, 4, 5]
+    a, _ = orc.forward_full(orc.new_request(A), toks)
+    b, _ = ob.forward_full(ob.new_request(A), toks)
+    rel = np.abs(a - b).max() / np.abs(a).max()
+    assert 1e-5 < rel < 3e-2
+
+
+# ---------------------------------------------------------------- drafter
+
+def test_drafter_layer_reduces_to_torch_decoder_layer(small):
+    """At RoPE position 0 (identity rotation) the drafter layer is a pre-LN
+    decoder layer whose self-attention keys/values are [history ; LN1(block)]
+    through the same projections, with no mask — torch's MHA with
+    key = value = concat(h_hist, LN1(x))."""
+    orc, tw, dw, A = small
+    req = orc.new_request(A)
+    g = np.random.default_rng(4)
+    x = g.standard_normal((9, SMALL.d_model))
+    h_hist = g.standard_normal((5, SMALL.d_model))
+    got = orc.drafter_layer(x, 1, np.zeros(9, int), h_hist, np.zeros(5, int), req.dck[1], req.dcv[1])
+    lay = _torch_decoder(SMALL, dw, 1)
+    X, Hh = torch.from_numpy(x)[None], torch.from_numpy(h_hist)[None]
+    with torch.no_grad():
+        h = lay.norm1(X)
+        kv = torch.cat([Hh, h], dim=1)
+        y = X + lay.self_attn(h, kv, kv, need_weights=False)[0]
+        y = y + lay.multihead_attn(lay.norm2(y), torch.from_numpy(A.astype(np.float64))[None],
+                                   torch.from_numpy(A.astype(np.float64))[None], need_weights=False)[0]
+        y = y + lay.linear2(F.gelu(lay.linear1(lay.norm3(y))))
+    np.testing.assert_allclose(got, y[0].numpy(), atol=1e-10)
+
+
+def test_history_fusion_special_case(small):
+    """With W_f = [I, 0] the fused history is LN_h of the first history
+    layer's residual stream."""
+    orc, tw, dw, A = small
+    d = SMALL.d_model
+    dw2 = dict(dw)
+    dw2["fuse_w"] = np.concatenate([np.eye(d), np.zeros((d, d))], axis=1).astype(np.float32)
+    o2 = M.Oracle(SMALL, tw, dw2)
+    resid = np.random.default_rng(5).standard_normal((4, 2, d))
+    ref = F.layer_norm(torch.from_numpy(resid[:, 0]), (d,), torch.from_numpy(dw["lnh_g"].astype(np.float64)),
+                       torch.from_numpy(dw["lnh_b"].astype(np.float64))).numpy()
+    np.testing.assert_allclose(o2.history_features(resid), ref, atol=1e-12)
+
+
+def test_drafter_history_mask_and_block_symmetry(small):
+    orc, _, _, A = small
+    req = orc.new_request(A)
+    orc.verify(req, [1, 2, 3, 4, 5, 6])
+    req.L = 4
+    z1 = orc.draft_logits(req, 9)
+    req.hist[4:] = 123.0                                   # at/after the anchor: never read
+    z2 = orc.draft_logits(req, 9)
+    np.testing.assert_array_equal(z1, z2)
+    assert z1.shape == (SMALL.K, SMALL.vocab)
+    # the mask rows only differ by their RoPE positions: they must not all agree
+    assert np.abs(z1[0] - z1[-1]).max() > 1e-6
+
+
+def test_drafter_parameter_counts_match_paper():
+    """Whisper-Flash §3.2 / Table 3: 60.7M trainable parameters with audio and
+    history, 47.5M without direct audio, 52.5M without the target history."""
+    gold = _load("paper_numbers.json")["drafter_params_millions"]
+    s = synth.LARGE_V3
+    sizes = dict((n, int(np.prod(sh))) for n, sh in synth.drafter_tensor_shapes(s))
+    full = sum(sizes.values())
+    cross = sum(v for n, v in sizes.items()
+                if any(n.endswith(k) for k in ("w_qc", "w_kvc", "w_oc", "b_qc", "b_vc", "b_oc", "ln2_g", "ln2_b")))
+    hist = sizes["fuse_w"] + sizes["lnh_g"] + sizes["lnh_b"]
+    tol = gold["printed_precision"]
+    assert abs(full / 1e6 - gold["audio_and_history"]) < tol
+    assert abs((full - cross) / 1e6 - gold["without_audio"]) < gold["tolerance_without_audio"]
+    assert abs((full - hist) / 1e6 - gold["without_history"]) < tol
+    shp = _load("paper_numbers.json")["whisper_large_v3_shape"]
+    assert list(s.hist_layers) == shp["hist_layers"] and s.n_layers == shp["n_layers"]
+    assert s.n_hist * s.d_model == shp["concat_width"]
+
+
+# ---------------------------------------------------------------- acceptance
+
+def test_figure1_worked_example():
+    ex = _load("paper_numbers.json")["figure1_worked_example"]
+    words = sorted(set(ex["candidates"]) | set(ex["target_argmax"]))
+    ids = {w: i for i, w in enumerate(words)}
+    block = [ids["the"]] + [ids[w] for w in ex["candidates"]]
+    g = [ids[w] for w in ex["target_argmax"]]
+    acc = M.accept_greedy(block, 8, g, budget=100, eos=10 ** 6)
+    assert acc.a == ex["accepted"]
+    assert acc.emitted == [ids[w] for w in ex["emitted"]]
+    assert acc.next_anchor == ids[ex["next_anchor"]]
+
+
+def test_accept_eos_budget_and_bonus():
+    eos = 9
+    acc = M.accept_greedy([1, 2, eos, 4], 3, [2, eos, 4, 5], budget=50, eos=eos)
+    assert acc.a == 2 and acc.emitted == [2, eos] and acc.done          # no bonus after EOS
+    acc = M.accept_greedy([1, 2, 3], 2, [2, 3, 7], budget=50, eos=eos)
+    assert acc.a == 2 and acc.emitted == [2, 3, 7] and not acc.done      # bonus
+    acc = M.accept_greedy([1, 2, 3], 2, [2, eos, 7], budget=50, eos=eos)
+    assert acc.emitted == [2, eos] and acc.done                          # EOS correction
+    acc = M.accept_greedy([1, 2, 3], 2, [2, 3, 7], budget=3, eos=eos)
+    assert acc.done and len(acc.emitted) == 3                            # budget used up
+
+
+@pytest.fixture(scope="module")
+def small_prompted():
+    s = synth.ModelShape("small", 3, 128, 2, 512, vocab=1000, max_pos=96, hist_layers=(0, 2),
+                         dtype="f32", eos_id=999, prompt=(990, 991, 992, 993))
+    tw = synth.target_weights(s, 12)
+    dw = synth.drafter_weights(s, 12, tw)
+    return s, M.Oracle(s, tw, dw), synth.encoder_states(s, 12, 0, frames=50)
+
+
+def test_speculative_equals_ar_for_all_draft_kinds(small_prompted):
+    s, orc, A = small_prompted
+    budget = 25
+    ar = M.greedy_plain(orc, orc.new_request(A), budget)
+    traj = list(s.prompt) + ar.tokens
+    perfect = lambda req, a, t, n: [traj[t + j] if t + j < len(traj) else 0 for j in range(1, n + 1)]
+    wrong = lambda req, a, t, n: [(traj[t + j] + 1) % s.vocab if t + j < len(traj) else 0 for j in range(1, n + 1)]
+    plan = synth.corruption_plan(1, s.max_pos, s.K, synth.corruption_p_const(s.K, 0.3), s.vocab, 3)
+    corrupt = M.corrupted_proposer(traj, plan.mask[0], plan.tok[0])
+    for prop, tau in ((perfect, None), (wrong, 1.0), (corrupt, None), (M.drafter_proposer(orc), None)):
+        sp = M.speculative_greedy(orc, orc.new_request(A), budget, prop)
+        assert sp.tokens == ar.tokens
+        met = M.acceptance_metrics(sp, s.K)
+        if tau is not None:
+            assert met["tau"] == tau
+        # emitted per round = a + 1 (no EOS here): tau = 1 + mean a
+        assert abs(met["tau"] - (1 + met["mean_a"])) < 1e-12
+    sp = M.speculative_greedy(orc, orc.new_request(A), budget, perfect)
+    assert sp.accepted[:2] == [s.K, s.K]          # perfect drafts: K+1 tokens per call
+    assert 1 + sum(sp.emitted) == budget          # prefill emits the first token
+
+
+def test_rollback_keeps_L_plus_1_plus_a(small_prompted):
+    s, orc, A = small_prompted
+    ar = M.greedy_cached(orc, orc.new_request(A), 10)
+    req = orc.new_request(A)
+    acc, _ = M.prefill(orc, req, 50)
+    assert req.L == len(s.prompt) and acc.next_anchor == ar.tokens[0]
+    L0 = req.L
+    block = [ar.tokens[0], ar.tokens[1], ar.tokens[2], (ar.tokens[3] + 1) % s.vocab]
+    lg = orc.verify(req, block)
+    g = [M.argmax_lowest(z) for z in lg]
+    acc2 = M.accept_greedy(block, 3, g, 50, s.eos_id)
+    assert acc2.a == 2 and acc2.emitted == ar.tokens[1:4]
+    req.L += 1 + acc2.a
+    assert req.L == L0 + 3
+    # re-verifying from the rolled-back cache reproduces the accepted rows
+    r2 = orc.new_request(A)
+    M.prefill(orc, r2, 50)
+    lg3 = orc.verify(r2, block[:3])
+    np.testing.assert_allclose(lg3, lg[:3], atol=1e-10)
+    # the next round starts at L0 + 3 and overwrites the rejected position
+    lg4 = orc.verify(req, [acc2.next_anchor])
+    assert M.argmax_lowest(lg4[0]) == ar.tokens[4]
+
+
+def test_budget_limits_candidates(small_prompted):
+    s, orc, A = small_prompted
+    seen = []
+    def prop(req, a, t, n):
+        seen.append(n)
+        return [0] * n
+    sp = M.speculative_greedy(orc, orc.new_request(A), 5, prop)
+    assert len(sp.tokens) == 5
+    R = 4
+    for n in seen:                                 # n_prop = min(K, R-1)
+        assert n == min(s.K, R - 1)
+        R -= 1
+
+
+def test_synthetic_acceptance_closed_form(small_prompted):
+    """E[a] = sum_k prod_{j<=k} (1 - p_j) for independently corrupted drafts
+    of the target's own trajectory (K = 8, p = 0.2: 3.329)."""
+    s, orc, A = small_prompted
+    budget = 90
+    ar = M.greedy_cached(orc, orc.new_request(A), budget)
+    traj = list(s.prompt) + ar.tokens
+    pj = synth.corruption_p_const(s.K, 0.2)
+    expect = sum(np.prod(1 - pj[:k]) for k in range(1, s.K + 1))
+    assert abs(expect - 3.329) < 1e-3
+    full_a = []
+    for seed in range(6):
+        plan = synth.corruption_plan(1, s.max_pos, s.K, pj, s.vocab, 100 + seed)
+        sp = M.speculative_greedy(orc, orc.new_request(A), budget,
+                                  M.corrupted_proposer(traj, plan.mask[0], plan.tok[0]))
+        assert sp.tokens == ar.tokens
+        full_a += [a for a, n in zip(sp.accepted, sp.proposed) if n == s.K]
+    full_a = np.array(full_a)
+    se = full_a.std() / math.sqrt(len(full_a))
+    assert abs(full_a.mean() - expect) < 4 * se + 0.05, (full_a.mean(), expect, se)
+
+
+def test_paper_metric_identities():
+    g = _load("paper_numbers.json")
+    K = g["table_a4_identity_a_equals_alpha_K"]["K"]
+    for r in g["table_a4_identity_a_equals_alpha_K"]["rows"]:
+        assert abs(r["alpha"] * K - r["a"]) < g["table_a4_identity_a_equals_alpha_K"]["printed_precision"]
+    for r in g["table_a5_tau_bound"]["rows"]:
+        assert r["tau"] <= 1 + r["alpha"] * r["K"] + 1e-9
+
+
+# ---------------------------------------------------------------- rejection rule
+
+def _grid_uniform(n):
+    return (np.arange(n) + 0.5) / n
+
+
+def test_rejection_rule_preserves_target_distribution_exactly():
+    """Quadrature over the acceptance and residual uniforms: the first
+    emitted token's distribution equals p (Leviathan et al. / Chen et al.,
+    as used in Whisper-Flash §3.1)."""
+    V, T = 7, 0.7
+    g = np.random.default_rng(8)
+    zp, zq = g.standard_normal(V) * 2, g.standard_normal(V) * 2
+    p = M.probs_fp32(zp, T).astype(np.float64)
+    q = M.probs_fp32(zq, T).astype(np.float64)
+    N = 4000
+    grid = _grid_uniform(N)
+    dist = np.zeros(V)
+    for y in range(V):
+        for u in grid[::8]:
+            for u2 in grid[::40]:
+                uni = lambda j, purpose, u=u, u2=u2: u if purpose == philox.PURPOSE_ACCEPT else u2
+                acc, _ = M.accept_sampling([0, y], 1, [zp, zp], [zq], T, 0, 0, 0, 10, eos=10 ** 6, uniform=uni)
+                dist[acc.emitted[0]] += q[y]
+    dist /= len(grid[::8]) * len(grid[::40])
+    np.testing.assert_allclose(dist, p, atol=3e-3)
+
+
+def test_rejection_rule_special_cases():
+    V, T = 50, 1.0
+    g = np.random.default_rng(9)
+    z = g.standard_normal(V)
+    # q == p: always accepted
+    for rnd in range(40):
+        acc, _ = M.accept_sampling([0, 3, 4], 2, [z, z, z], [z, z], T, 5, 0, rnd, 10, 10 ** 6)
+        assert acc.a == 2
+    # p(y) == 0 (suppressed): never accepted
+    for rnd in range(40):
+        acc, _ = M.accept_sampling([0, 3], 1, [z, z], [z], T, 5, 0, rnd, 10, 10 ** 6, suppress=[3])
+        assert acc.a == 0 and acc.emitted[0] != 3
+    # disjoint supports: the residual is p itself
+    zp = np.full(V, -np.inf); zp[:10] = g.standard_normal(10)
+    zq = np.full(V, -np.inf); zq[20:] = g.standard_normal(30)
+    p = M.probs_fp32(zp, T)
+    for rnd in range(40):
+        acc, det = M.accept_sampling([0, 25], 1, [zp, zp], [zq], T, 5, 0, rnd, 10, 10 ** 6)
+        assert acc.a == 0
+        assert det[-1][0] == "residual" and det[-1][3] == M.sample_inverse_cdf(p, det[-1][2])
+    # T -> 0 reduces to greedy verification
+    zt, zd = g.standard_normal(V), g.standard_normal(V)
+    acc, _ = M.accept_sampling([0, int(np.argmax(zt))], 1, [zt, zt], [zd], 1e-4, 5, 0, 0, 10, 10 ** 6)
+    assert acc.a == 1
+    y = (int(np.argmax(zt)) + 1) % V
+    acc, _ = M.accept_sampling([0, y], 1, [zt, zt], [zd], 1e-4, 5, 0, 0, 10, 10 ** 6)
+    assert acc.a == 0 and acc.emitted == [int(np.argmax(zt))]
+
+
+def test_first_token_chi_square_montecarlo():
+    """Monte Carlo over Philox streams: first emitted token ~ p."""
+    V, T = 20, 0.7
+    g = np.random.default_rng(10)
+    zp = g.standard_normal(V)
+    zq = zp + g.standard_normal(V)
+    p = M.probs_fp32(zp, T).astype(np.float64)
+    n = 6000
+    counts = np.zeros(V)
+    for r in range(n):
+        y = M.sample_draft(zq, T, 7, 0, r, 1)
+        acc, _ = M.accept_sampling([0, y], 1, [zp, zp], [zq], T, 7, 0, r, 10, 10 ** 6)
+        counts[acc.emitted[0]] += 1
+    chi2 = ((counts - n * p) ** 2 / (n * p)).sum()
+    assert chi2 < 43.8   # chi-square 99.9% quantile, 19 dof
