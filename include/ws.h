@@ -1,0 +1,239 @@
+/*
+ * ws.h — C ABI of the speculative Whisper decoding library (libws.so).
+ *
+ * The library implements the data-parallel hot path of Whisper-Flash
+ * ("Whisper-Flash: Acoustically Conditioned Parallel Drafting for Faster
+ * Whisper Decoding", arXiv 2609.32869): a two-layer parallel drafter fills
+ * K mask positions after the latest token (§3.2, Eq. 2), the frozen target
+ * decoder verifies the K+1-token block in one causal pass and keeps the
+ * longest prefix matching its own greedy argmax, or applies the rejection
+ * rule when sampling (§3.1), and the KV cache is rolled back by length
+ * (Appendix A.1).
+ *
+ * Conventions for every entry point
+ *   - All pointers are DEVICE pointers unless the comment says "host".  The
+ *     caller allocates every buffer (workspace, weights, inputs, outputs)
+ *     and keeps it alive while work that uses it is in flight.  The library
+ *     never allocates device memory and never synchronises the stream
+ *     (except ws_load_weights, which finishes its copies before returning).
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL
+ *     is the legacy default stream).  Launch sequences are CUDA-graph
+ *     capturable once the context exists.
+ *   - Return value: WS_OK (0) or a negative WS_E* code.  Argument errors are
+ *     detected on the host before anything is enqueued; ws_last_error()
+ *     gives a one-line description.  No call aborts or throws.
+ *   - Device-side invariant violations (a position at or beyond max_pos, a
+ *     token id outside the vocabulary) skip the offending access and set a
+ *     device status word; ws_status() reads and clears it.
+ *   - "Request slots" are integers in [0, max_batch); a call works on the
+ *     slots listed in `req_ids` (device int32[n_req]), in that order.
+ *     Distinct entries are required.
+ *   - Row-major layouts; "[n, H]" means n rows of H elements.
+ *   - Model dtype: WS_F32 (float) or WS_BF16 (bfloat16, fp32 accumulation,
+ *     fp32 residual stream and logits).
+ */
+#ifndef WS_H_
+#define WS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ws_ctx ws_ctx;   /* opaque; owns no PyTorch objects */
+typedef void* ws_stream;        /* cudaStream_t */
+
+enum {
+  WS_OK = 0,
+  WS_EINVAL = -1,        /* bad argument (null pointer, size, mode) */
+  WS_ENOSPACE = -2,      /* workspace smaller than ws_query_workspace() */
+  WS_EPOS = -3,          /* a block would pass the decoder context max_pos */
+  WS_ECUDA = -4,         /* a CUDA runtime / driver call failed */
+  WS_EDEVICE = -5,       /* device status word was set (see ws_status) */
+  WS_EUNSUPPORTED = -6   /* shape or option this build does not implement */
+};
+
+enum { WS_F32 = 0, WS_BF16 = 1 };
+
+/* GEMM engine: both compute every output element with a K order that does
+ * not depend on the number of rows, so block verification and one-token
+ * decoding give bit-identical rows.  A context uses one engine throughout. */
+enum { WS_GEMM_AUTO = 0, WS_GEMM_SIMT = 1, WS_GEMM_TC = 2 };
+
+/* Model description.  Shapes of Whisper large-v3: 32 / 1280 / 20 / 5120 /
+ * 51866 / 448 (Whisper-Flash §1, Appendix A.2). */
+typedef struct {
+  int32_t n_layers;        /* target decoder layers */
+  int32_t d_model;         /* width d; multiple of 128 */
+  int32_t n_heads;         /* d_model / n_heads must be 64 */
+  int32_t d_ff;            /* FFN width; multiple of 128 */
+  int32_t vocab;           /* V */
+  int32_t max_pos;         /* decoder context (learned positions), <= 448 */
+  int32_t drafter_layers;  /* 0 (no drafter) or 2 */
+  int32_t n_hist;          /* history layers (1..8) */
+  int32_t hist_layers[8];  /* zero-based target layers whose residual streams feed the drafter */
+  int32_t K;               /* mask positions per draft block, <= 15 */
+  int32_t dtype;           /* WS_F32 or WS_BF16 */
+  int32_t max_batch;       /* request slots */
+  int32_t max_frames;      /* encoder frames per request, <= 1500 */
+  int32_t max_block;       /* largest verify block height H (>= K+1, >= prompt length), <= 16 */
+  int32_t eos_id;          /* end-of-transcript token id */
+  int32_t gemm;            /* WS_GEMM_* */
+} ws_model_desc;
+
+/* Bytes of device workspace the context needs (weights copy, caches,
+ * activations, scratch).  0 if the description is invalid. */
+size_t ws_query_workspace(const ws_model_desc* desc);
+
+/* Create a context inside `workspace` (device, >= ws_query_workspace bytes,
+ * 256-byte aligned) and copy the weight blobs into it.  Blobs may be host or
+ * device memory, in the model dtype, laid out as:
+ *   target : tok_emb[V,d] pos_emb[max_pos,d] layer*n_layers lnf_g[d] lnf_b[d]
+ *   drafter: fuse_w[d, n_hist*d] lnh_g[d] lnh_b[d] mask_emb[d] lnf_g[d] lnf_b[d]
+ *            layer*drafter_layers            (NULL when drafter_layers == 0)
+ *   layer  : w_qkv[3d,d] w_o[d,d] w_qc[d,d] w_kvc[2d,d] w_oc[d,d]
+ *            w_fc1[f,d] w_fc2[d,f] b_q b_v b_o b_qc b_vc b_oc [d]
+ *            b_fc1[f] b_fc2[d] ln1_g ln1_b ln2_g ln2_b ln3_g ln3_b [d]
+ * Matrices are [out, in] (y = x W^T + b); keys have no bias (Whisper).
+ * The context state lives in the workspace; the host-side handle is freed
+ * by ws_free.  Synchronises `stream` before returning. */
+int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace,
+                    size_t workspace_bytes, const void* target_blob,
+                    const void* drafter_blob, ws_stream stream);
+
+/* Reset request slots: target cache length L = 0, drafter history empty. */
+int ws_reset(ws_ctx* ctx, int n_req, const int32_t* req_ids, ws_stream stream);
+
+/* Per-request acoustic K/V (Whisper-Flash Appendix A.5: every request
+ * refreshes the acoustic key/value projections of target and drafter; they
+ * are written once and only read afterwards).  For every target layer and
+ * every drafter layer: K_c = A W_k^T, V_c = A W_v^T + b_v.
+ *   enc          [sum_i F_i, d] model dtype, requests packed back to back
+ *   cu_frames    [n_req+1] int32 prefix sums of F_i (cu_frames[0] = 0)
+ *   valid_frames [n_req] int32 frames that attention may see (<= F_i), or
+ *                NULL (= F_i).  Frames at or beyond it are excluded from the
+ *                softmax (padding), not zero-filled.
+ *   max_frames_call  host int, max_i F_i (sizes the launch; <= max_frames) */
+int ws_cross_kv(ws_ctx* ctx, int n_req, const int32_t* req_ids, const void* enc,
+                const int32_t* cu_frames, const int32_t* valid_frames,
+                int max_frames_call, ws_stream stream);
+
+/* Block verification (Whisper-Flash §3.1): one causal target pass over
+ * block[i, 0:block_len[i]] at positions L..L+block_len-1 of each request.
+ * Row j attends to cache positions 0..L+j.  The block's K/V are written into
+ * the paged cache (they become valid only when ws_accept advances L), and
+ * the residual streams after the history layers are kept for the drafter.
+ *   H          host int, row stride of block/target/logits (1..max_block)
+ *   block      [n_req, H] int32 token ids (column 0 = the anchor)
+ *   block_len  [n_req] int32 in 0..H (0 = request idle this call)
+ *   target     [n_req, H] int32 out: greedy argmax of each row (Eq. 1,
+ *              ties to the lowest id); -1 for rows >= block_len
+ *   logits     [n_req, H, V] float out, or NULL (needed for sampling)
+ * Prefill is a verify of the prompt with L = 0 (Appendix A.1). */
+int ws_verify(ws_ctx* ctx, int n_req, const int32_t* req_ids, int H,
+              const int32_t* block, const int32_t* block_len, int32_t* target,
+              float* logits, ws_stream stream);
+
+/* Parallel drafting (Whisper-Flash §3.2, Eq. 2, Appendix A.2).  First folds
+ * the rows left by the last ws_verify into the drafter history (fusion
+ * projection of the n_hist residual streams, LN, per-layer K/V with RoPE at
+ * their absolute positions), then runs the drafter on
+ * X_t = [Emb(anchor), m, ..., m] at RoPE positions t..t+K, t = L.
+ *   block      [n_req, K+1] int32 in/out: column 0 (anchor) is read,
+ *              columns 1..K receive the proposals
+ *   temperature  0 = greedy proposals (argmax); > 0 = each mask row sampled
+ *              independently from softmax(z/T) (Appendix A.4) with Philox
+ *              counter (slot, round, j, 0)
+ *   q_logits   [n_req, K, V] float out (draft logits), or NULL (greedy) */
+int ws_draft(ws_ctx* ctx, int n_req, const int32_t* req_ids, int32_t* block,
+             float temperature, uint64_t seed, uint64_t round, float* q_logits,
+             ws_stream stream);
+
+enum { WS_ACCEPT_GREEDY = 0, WS_ACCEPT_SAMPLE = 1, WS_ACCEPT_FORCED = 2 };
+
+/* Inputs and outputs of ws_accept (all device int32 unless noted). */
+typedef struct {
+  int32_t mode;              /* WS_ACCEPT_* */
+  int32_t H;                 /* row stride of block / target / p_logits */
+  const int32_t* block;      /* [n, H] the verified block */
+  const int32_t* block_len;  /* [n] 1 + proposals; 0 = idle */
+  const int32_t* target;     /* [n, H] target argmax per row (GREEDY, FORCED) */
+  const float* p_logits;     /* [n, H, V] target logits (SAMPLE) */
+  const float* q_logits;     /* [n, K, V] draft logits (SAMPLE) */
+  float temperature;         /* SAMPLE */
+  uint64_t seed, round;      /* Philox key and round (SAMPLE) */
+  int32_t* budget;           /* [n] in/out output tokens left R */
+  int32_t* done;             /* [n] in/out; done requests are skipped */
+  int32_t* n_acc;            /* [n] out accepted candidates a */
+  int32_t* n_emit;           /* [n] out tokens emitted this call */
+  int32_t* next_block;       /* [n, Hn] out: column 0 = next anchor */
+  int32_t next_stride;       /* Hn (>= 1) */
+  int32_t* next_len;         /* [n] out: 1 + min(K, R-1) for the next block, 0 when done */
+  int32_t* transcript;       /* [n, tcap] emitted tokens appended, or NULL */
+  int32_t* out_len;          /* [n] in/out transcript length (required with transcript) */
+  int32_t tcap;
+  int32_t* n_done;           /* [1] +1 per request that finishes here, or NULL */
+} ws_accept_args;
+
+/* Acceptance and rollback (Whisper-Flash §3.1, Appendix A.1, A.4).
+ * GREEDY: a = longest prefix of candidates equal to the target's argmax at
+ *   the previous row; emit them plus the target's token at the first
+ *   disagreement (or the bonus after all agree); an accepted EOS ends the
+ *   transcript with no bonus.
+ * SAMPLE: candidate j accepted iff u_j * q_j(y_j) < p_j(y_j) (FP32), u_j
+ *   from Philox (slot, round, j, 1); at the first rejection a token is drawn
+ *   from the normalised (p_j - q_j)_+ (or p_j when that is empty), after a
+ *   full accept the bonus is drawn from row n_prop — counter (slot, round,
+ *   j, 2), inverse CDF in ascending id order.  Same temperature and token
+ *   suppression as the drafter.
+ * FORCED: all block tokens are given (prompt prefill); emits the argmax of
+ *   the last row.
+ * Then L <- L + 1 + a (the old anchor plus the accepted candidates), R -= n_emit,
+ * done when EOS was emitted or R == 0. */
+int ws_accept(ws_ctx* ctx, int n_req, const int32_t* req_ids,
+              const ws_accept_args* args, ws_stream stream);
+
+/* Synthetic proposals from a reference trajectory (a workload generator,
+ * not part of the method): for the anchor at t = L, candidate j (1..K) is
+ * ctok[i, t, j-1] when cmask[i, t, j-1] != 0, else traj[i, t+j].
+ *   block  [n, K+1] in/out (columns 1..K written)
+ *   traj   [n, tlen] int32 (prompt + transcript, absolute positions)
+ *   cmask  [n, max_pos, K] uint8; ctok [n, max_pos, K] int32 */
+int ws_draft_synthetic(ws_ctx* ctx, int n_req, const int32_t* req_ids, int32_t* block,
+                       const int32_t* traj, int tlen, const uint8_t* cmask,
+                       const int32_t* ctok, ws_stream stream);
+
+/* Sample rows of given logits with the drafter's sampler: out[i, r] ~
+ * softmax(logits[i, r, :] / T) using Philox counter (slot, round, r+1, 0).
+ *   logits [n, rows, V] float; out [n, rows] int32 (row stride `rows`). */
+int ws_sample(ws_ctx* ctx, int n_req, const int32_t* req_ids, const float* logits,
+              int rows, float temperature, uint64_t seed, uint64_t round,
+              int32_t* out, ws_stream stream);
+
+/* Token suppression shared by draft and target logits (Appendix A.4):
+ * mask [ceil(V/32)] uint32 device bitmask (bit set = id suppressed), or NULL
+ * to clear.  The pointer is kept; the buffer must outlive the context. */
+int ws_set_suppress(ws_ctx* ctx, const uint32_t* mask);
+
+/* Copy the target cache lengths L of the listed slots into out [n] int32. */
+int ws_get_lengths(ws_ctx* ctx, int n_req, const int32_t* req_ids, int32_t* out,
+                   ws_stream stream);
+
+/* Synchronise `stream`, return and clear the device status word (0 = ok). */
+int ws_status(ws_ctx* ctx, ws_stream stream, int32_t* host_status);
+
+/* Name of the GEMM engine in use ("simt" or "tcgen05"). */
+const char* ws_gemm_engine(const ws_ctx* ctx);
+
+/* Last error message for ctx (or for the calling thread when ctx is NULL). */
+const char* ws_last_error(const ws_ctx* ctx);
+
+/* Destroy the host handle (the workspace stays owned by the caller). */
+void ws_free(ws_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WS_H_ */

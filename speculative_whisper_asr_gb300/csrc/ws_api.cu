@@ -1,0 +1,599 @@
+// C ABI of libws: context, workspace layout and the host-side orchestration
+// of the decoding path (include/ws.h documents every entry point).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "ws_internal.cuh"
+
+struct LayerW {
+  const void *w_qkv, *w_o, *w_qc, *w_kvc, *w_oc, *w_fc1, *w_fc2;
+  const void *b_q, *b_v, *b_o, *b_qc, *b_vc, *b_oc, *b_fc1, *b_fc2;
+  const void *ln1_g, *ln1_b, *ln2_g, *ln2_b, *ln3_g, *ln3_b;
+};
+
+struct ws_ctx {
+  ws_model_desc d;
+  int es = 4;                   // element size of the model dtype
+  int heads = 0, ppr = 0, n_pages = 0, n_xl = 0, max_split = 0;
+  char* ws = nullptr;
+  size_t ws_bytes = 0;
+  const void *tok_emb = nullptr, *pos_emb = nullptr, *lnf_g = nullptr, *lnf_b = nullptr;
+  const void *fuse_w = nullptr, *lnh_g = nullptr, *lnh_b = nullptr, *mask_emb = nullptr;
+  const void *dlnf_g = nullptr, *dlnf_b = nullptr;
+  std::vector<LayerW> tl, dl;
+  char* kv = nullptr;  size_t kv_layer_bytes = 0;     // target self KV pool
+  char* hkv = nullptr;                                // drafter history KV pool
+  void* xkv = nullptr; size_t x_slot_elems = 0, x_layer_elems = 0;
+  int32_t* ptab = nullptr;
+  float* rope = nullptr;
+  int32_t *L = nullptr, *Fc = nullptr, *Fv = nullptr, *pend_start = nullptr, *pend_n = nullptr, *status = nullptr;
+  float* x = nullptr;
+  void *h = nullptr, *q = nullptr, *ao = nullptr, *ffn = nullptr, *kb = nullptr, *vb = nullptr;
+  float* hist = nullptr;
+  unsigned long long* amax = nullptr;
+  float* part = nullptr;
+  void* feat = nullptr; float* hpre = nullptr; void* hh = nullptr;
+  int pending_H = 0;
+  int max_fc = 0;
+  const uint32_t* suppress = nullptr;
+  int engine = WS_GEMM_SIMT;
+  bool pdl = true;              // programmatic dependent launch allowed
+  bool cur_pdl = false;         // PDL for the call in progress (never on the legacy stream)
+  std::string err;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(ws_ctx* c, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (c) c->err = buf; else g_err = buf;
+  return code;
+}
+
+#define CK(x)                                                                                   \
+  do {                                                                                          \
+    cudaError_t e_ = (x);                                                                       \
+    if (e_ != cudaSuccess) return fail(c, WS_ECUDA, "%s: %s", #x, cudaGetErrorString(e_));      \
+  } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Element counts of the blobs (see ws.h).
+size_t layer_elems(const ws_model_desc& d) {
+  size_t D = d.d_model, F = d.d_ff;
+  return 3 * D * D + D * D + D * D + 2 * D * D + D * D + F * D + D * F + 6 * D + F + D + 6 * D;
+}
+size_t target_elems(const ws_model_desc& d) {
+  return (size_t)d.vocab * d.d_model + (size_t)d.max_pos * d.d_model + d.n_layers * layer_elems(d) + 2 * d.d_model;
+}
+size_t drafter_elems(const ws_model_desc& d) {
+  if (d.drafter_layers == 0) return 0;
+  size_t D = d.d_model;
+  return D * (d.n_hist * D) + 5 * D + d.drafter_layers * layer_elems(d);
+}
+
+// Workspace layout: a bump allocator over the caller's buffer.
+struct Layout {
+  size_t off = 0;
+  size_t take(size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; }
+};
+
+struct Plan {
+  size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
+  size_t kv_layer_bytes, total;
+  int heads, ppr, n_pages, n_xl, max_split;
+};
+
+const char* check_desc(const ws_model_desc* d) {
+  if (!d) return "null model description";
+  if (d->dtype != WS_F32 && d->dtype != WS_BF16) return "dtype must be WS_F32 or WS_BF16";
+  if (d->n_layers < 1 || d->n_layers > 256) return "n_layers out of range";
+  if (d->d_model < 128 || d->d_model % 128 != 0 || d->d_model > 2048) return "d_model must be a multiple of 128, <= 2048";
+  if (d->n_heads < 1 || d->d_model / d->n_heads != WS_DH || d->d_model % d->n_heads) return "d_model / n_heads must be 64";
+  if (d->d_ff < 128 || d->d_ff % 128 != 0) return "d_ff must be a multiple of 128";
+  if (d->vocab < 2 || d->vocab % 2 != 0) return "vocab must be even and >= 2";
+  if (d->max_pos < 1 || d->max_pos > 4096) return "max_pos out of range";
+  if (d->drafter_layers < 0 || d->drafter_layers > 8) return "drafter_layers out of range";
+  if (d->K < 1 || d->K > 15) return "K must be 1..15";
+  if (d->max_block < d->K + 1 || d->max_block > 16) return "max_block must be in K+1..16";
+  if (d->max_batch < 1 || d->max_batch > 4096) return "max_batch out of range";
+  if (d->max_frames < 1 || d->max_frames > 4096) return "max_frames out of range";
+  if (d->eos_id < 0 || d->eos_id >= d->vocab) return "eos_id outside the vocabulary";
+  if (d->gemm < WS_GEMM_AUTO || d->gemm > WS_GEMM_TC) return "unknown gemm engine";
+  if (d->drafter_layers > 0) {
+    if (d->n_hist < 1 || d->n_hist > 8) return "n_hist must be 1..8";
+    for (int i = 0; i < d->n_hist; ++i)
+      if (d->hist_layers[i] < 0 || d->hist_layers[i] >= d->n_layers) return "history layer out of range";
+  }
+  return nullptr;
+}
+
+Plan make_plan(const ws_model_desc& d) {
+  Plan p;
+  Layout lay;
+  const size_t es = d.dtype == WS_BF16 ? 2 : 4;
+  const size_t D = d.d_model;
+  p.heads = d.n_heads;
+  p.ppr = (d.max_pos + WS_PAGE - 1) / WS_PAGE;
+  p.n_pages = d.max_batch * p.ppr;
+  p.n_xl = d.n_layers + d.drafter_layers;
+  p.max_split = (d.max_frames + WS_XCHUNK - 1) / WS_XCHUNK;
+  const size_t M = (size_t)d.max_batch * d.max_block;
+  p.tblob = lay.take(target_elems(d) * es);
+  p.dblob = lay.take(drafter_elems(d) * es);
+  p.kv_layer_bytes = (size_t)p.n_pages * 2 * d.n_heads * WS_PAGE * WS_DH * es;
+  p.kv = lay.take(p.kv_layer_bytes * d.n_layers);
+  p.hkv = lay.take(p.kv_layer_bytes * d.drafter_layers);
+  p.xkv = lay.take((size_t)d.max_batch * p.n_xl * 2 * D * d.max_frames * es);
+  p.ptab = lay.take((size_t)p.n_pages * 4);
+  p.rope = lay.take((size_t)d.max_pos * WS_DH * 4);
+  p.state = lay.take((size_t)d.max_batch * 5 * 4 + 256);
+  p.x = lay.take(M * D * 4);
+  p.h = lay.take(M * D * es);
+  p.q = lay.take(M * D * es);
+  p.ao = lay.take(M * D * es);
+  p.ffn = lay.take(M * d.d_ff * es);
+  p.kb = lay.take(M * D * es);
+  p.vb = lay.take(M * D * es);
+  const int nh = d.drafter_layers > 0 ? d.n_hist : 0;
+  p.hist = lay.take((size_t)d.max_batch * d.max_block * nh * D * 4);
+  p.amax = lay.take(M * 8);
+  p.part = lay.take(M * d.n_heads * p.max_split * (WS_DH + 2) * 4);
+  p.feat = lay.take(M * nh * D * es);
+  p.hpre = lay.take(M * D * 4);
+  p.hh = lay.take(M * D * es);
+  p.total = lay.off;
+  return p;
+}
+
+void bind_layer(LayerW& w, const char*& p, const ws_model_desc& d, size_t es) {
+  const size_t D = d.d_model, F = d.d_ff;
+  auto take = [&](size_t n) { const void* r = p; p += n * es; return r; };
+  w.w_qkv = take(3 * D * D); w.w_o = take(D * D); w.w_qc = take(D * D); w.w_kvc = take(2 * D * D);
+  w.w_oc = take(D * D); w.w_fc1 = take(F * D); w.w_fc2 = take(D * F);
+  w.b_q = take(D); w.b_v = take(D); w.b_o = take(D); w.b_qc = take(D); w.b_vc = take(D); w.b_oc = take(D);
+  w.b_fc1 = take(F); w.b_fc2 = take(D);
+  w.ln1_g = take(D); w.ln1_b = take(D); w.ln2_g = take(D); w.ln2_b = take(D); w.ln3_g = take(D); w.ln3_b = take(D);
+}
+
+KVPool pool(ws_ctx* c, char* base, int layer) {
+  KVPool k;
+  k.base = base + (size_t)layer * c->kv_layer_bytes;
+  k.ptab = c->ptab;
+  k.ppr = c->ppr;
+  k.n_heads = c->heads;
+  return k;
+}
+
+XKV xkv_of(ws_ctx* c) {
+  XKV x;
+  x.base = c->xkv;
+  x.slot_stride = c->x_slot_elems;
+  x.layer_stride = c->x_layer_elems;
+  x.max_frames = c->d.max_frames;
+  x.n_heads = c->heads;
+  return x;
+}
+
+Epi epi0(ws_ctx* c, int kind) {
+  Epi e;
+  memset(&e, 0, sizeof e);
+  e.kind = kind;
+  e.d = c->d.d_model;
+  e.status = c->status;
+  e.rope = c->rope;
+  e.suppress = c->suppress;
+  e.max_block = c->d.max_block;
+  return e;
+}
+
+template <typename T>
+cudaError_t gemm(ws_ctx* c, const void* X, int ldx, const void* W, int M, int N, int K, const Epi& e,
+                 cudaStream_t s, int batch = 1) {
+  GemmShape g;
+  g.X = X; g.ldx = ldx; g.W = W; g.ldw = K; g.M = M; g.N = N; g.K = K; g.batch = batch;
+  return launch_gemm_simt<T>(g, e, s, c->cur_pdl);
+}
+
+template <typename T>
+cudaError_t layernorm(ws_ctx* c, int M, const float* x, const void* g, const void* b, void* y,
+                      cudaStream_t s, int group_skip = 0) {
+  const int D = c->d.d_model;
+  return launch_layernorm<T>(M, D, x, D, (const T*)g, (const T*)b, (T*)y, D, group_skip, s, c->cur_pdl);
+}
+
+bool is_hist_layer(const ws_model_desc& d, int l, int& idx) {
+  if (d.drafter_layers == 0) return false;
+  for (int i = 0; i < d.n_hist; ++i)
+    if (d.hist_layers[i] == l) { idx = i; return true; }
+  return false;
+}
+
+// --------------------------------------------------------------------------- verify
+template <typename T>
+int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* block, const int32_t* blen,
+                int32_t* target, float* logits, cudaStream_t s) {
+  const ws_model_desc& d = c->d;
+  const int D = d.d_model, M = n * H;
+  const bool pdl = c->cur_pdl;
+  RowMap rm;
+  rm.mode = ROW_VERIFY; rm.H = H; rm.max_pos = d.max_pos; rm.req_ids = req; rm.L = c->L;
+  rm.block_len = blen; rm.pend_start = c->pend_start; rm.pend_n = c->pend_n;
+  CK(launch_embed_target<T>(n, H, rm, block, (const T*)c->tok_emb, (const T*)c->pos_emb, D, d.vocab, c->x,
+                            c->pend_start, c->pend_n, c->status, s, pdl));
+  const int n_split = c->max_fc > 0 ? (c->max_fc + WS_XCHUNK - 1) / WS_XCHUNK : 1;
+  for (int l = 0; l < d.n_layers; ++l) {
+    const LayerW& w = c->tl[l];
+    CK(layernorm<T>(c, M, c->x, w.ln1_g, w.ln1_b, c->h, s));
+    Epi e = epi0(c, EPI_QKV);
+    e.bias = w.b_q; e.bias2 = w.b_v; e.out = c->q; e.rm = rm; e.kv = pool(c, c->kv, l);
+    CK(gemm<T>(c, c->h, D, w.w_qkv, M, 3 * D, D, e, s));
+    CK(launch_self_attn<T>(n, H, rm, (const T*)c->q, pool(c, c->kv, l), (T*)c->ao, c->heads, s, pdl));
+    e = epi0(c, EPI_RESID);
+    e.bias = w.b_o; e.resid = c->x; e.ldr = D;
+    CK(gemm<T>(c, c->ao, D, w.w_o, M, D, D, e, s));
+    CK(layernorm<T>(c, M, c->x, w.ln2_g, w.ln2_b, c->h, s));
+    e = epi0(c, EPI_STORE);
+    e.bias = w.b_qc; e.out = c->q; e.ldo = D;
+    CK(gemm<T>(c, c->h, D, w.w_qc, M, D, D, e, s));
+    CK(launch_cross_attn<T>(n, H, req, c->Fv, (const T*)c->q, xkv_of(c), l, c->part, (T*)c->ao, c->heads, n_split,
+                            s, pdl));
+    e = epi0(c, EPI_RESID);
+    e.bias = w.b_oc; e.resid = c->x; e.ldr = D;
+    CK(gemm<T>(c, c->ao, D, w.w_oc, M, D, D, e, s));
+    CK(layernorm<T>(c, M, c->x, w.ln3_g, w.ln3_b, c->h, s));
+    e = epi0(c, EPI_GELU);
+    e.bias = w.b_fc1; e.out = c->ffn; e.ldo = d.d_ff;
+    CK(gemm<T>(c, c->h, D, w.w_fc1, M, d.d_ff, D, e, s));
+    e = epi0(c, EPI_RESID);
+    e.bias = w.b_fc2; e.resid = c->x; e.ldr = D;
+    int hidx;
+    if (is_hist_layer(d, l, hidx)) {
+      e.hist = c->hist; e.hist_idx = hidx; e.n_hist = d.n_hist; e.rm = rm;
+    }
+    CK(gemm<T>(c, c->ffn, d.d_ff, w.w_fc2, M, D, d.d_ff, e, s));
+  }
+  CK(layernorm<T>(c, M, c->x, c->lnf_g, c->lnf_b, c->h, s));
+  CK(launch_argmax_init(M, c->amax, s, pdl));
+  Epi e = epi0(c, EPI_LOGITS);
+  e.logits = logits; e.ldl = d.vocab; e.amax = c->amax;
+  CK(gemm<T>(c, c->h, D, c->tok_emb, M, d.vocab, D, e, s));
+  CK(launch_argmax_finalize(n, H, blen, c->amax, target, H, 0, s, pdl));
+  if (d.drafter_layers > 0) c->pending_H = H > c->pending_H ? H : c->pending_H;
+  return WS_OK;
+}
+
+// --------------------------------------------------------------------------- draft
+template <typename T>
+int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp, uint64_t seed, uint64_t rnd,
+               float* q_logits, cudaStream_t s) {
+  const ws_model_desc& d = c->d;
+  const int D = d.d_model, K = d.K, K1 = K + 1;
+  const bool pdl = c->cur_pdl;
+  // 1) fold the rows of the last verify into the drafter history
+  const int Hp = c->pending_H;
+  if (Hp > 0) {
+    const int Mh = n * Hp, W = d.n_hist * D;
+    CK(launch_hist_gather<T>(n, Hp, req, c->pend_n, c->hist, d.max_block, d.n_hist, D, (T*)c->feat, s, pdl));
+    Epi e = epi0(c, EPI_F32);
+    e.out = c->hpre; e.ldo = D;
+    CK(gemm<T>(c, c->feat, W, c->fuse_w, Mh, D, W, e, s));
+    CK(layernorm<T>(c, Mh, c->hpre, c->lnh_g, c->lnh_b, c->hh, s));
+    RowMap rh;
+    rh.mode = ROW_HIST; rh.H = Hp; rh.max_pos = d.max_pos; rh.req_ids = req; rh.L = c->L;
+    rh.block_len = nullptr; rh.pend_start = c->pend_start; rh.pend_n = c->pend_n;
+    for (int l = 0; l < d.drafter_layers; ++l) {
+      const LayerW& w = c->dl[l];
+      Epi eh = epi0(c, EPI_HISTKV);
+      eh.bias2 = w.b_v; eh.rm = rh; eh.kv = pool(c, c->hkv, l);
+      const char* wkv = (const char*)w.w_qkv + (size_t)D * D * c->es;   // rows k | v of w_qkv
+      CK(gemm<T>(c, c->hh, D, wkv, Mh, 2 * D, D, eh, s));
+    }
+  }
+  // 2) the block X_t = [Emb(anchor), m, ..., m] through the drafter layers
+  const int M = n * K1;
+  RowMap rd;
+  rd.mode = ROW_DRAFT; rd.H = K1; rd.max_pos = d.max_pos; rd.req_ids = req; rd.L = c->L;
+  rd.block_len = nullptr; rd.pend_start = c->pend_start; rd.pend_n = c->pend_n;
+  CK(launch_embed_draft<T>(n, K1, req, block, (const T*)c->tok_emb, (const T*)c->mask_emb, D, d.vocab, c->x,
+                           c->pend_n, c->status, s, pdl));
+  const int n_split = c->max_fc > 0 ? (c->max_fc + WS_XCHUNK - 1) / WS_XCHUNK : 1;
+  for (int l = 0; l < d.drafter_layers; ++l) {
+    const LayerW& w = c->dl[l];
+    CK(layernorm<T>(c, M, c->x, w.ln1_g, w.ln1_b, c->h, s));
+    Epi e = epi0(c, EPI_QKV_DRAFT);
+    e.bias = w.b_q; e.bias2 = w.b_v; e.out = c->q; e.kout = c->kb; e.vout = c->vb; e.rm = rd;
+    CK(gemm<T>(c, c->h, D, w.w_qkv, M, 3 * D, D, e, s));
+    CK(launch_draft_attn<T>(n, K1, req, c->L, (const T*)c->q, (const T*)c->kb, (const T*)c->vb,
+                            pool(c, c->hkv, l), (T*)c->ao, c->heads, d.max_pos, s, pdl));
+    e = epi0(c, EPI_RESID);
+    e.bias = w.b_o; e.resid = c->x; e.ldr = D;
+    CK(gemm<T>(c, c->ao, D, w.w_o, M, D, D, e, s));
+    CK(layernorm<T>(c, M, c->x, w.ln2_g, w.ln2_b, c->h, s));
+    e = epi0(c, EPI_STORE);
+    e.bias = w.b_qc; e.out = c->q; e.ldo = D;
+    CK(gemm<T>(c, c->h, D, w.w_qc, M, D, D, e, s));
+    CK(launch_cross_attn<T>(n, K1, req, c->Fv, (const T*)c->q, xkv_of(c), d.n_layers + l, c->part, (T*)c->ao,
+                            c->heads, n_split, s, pdl));
+    e = epi0(c, EPI_RESID);
+    e.bias = w.b_oc; e.resid = c->x; e.ldr = D;
+    CK(gemm<T>(c, c->ao, D, w.w_oc, M, D, D, e, s));
+    CK(layernorm<T>(c, M, c->x, w.ln3_g, w.ln3_b, c->h, s));
+    e = epi0(c, EPI_GELU);
+    e.bias = w.b_fc1; e.out = c->ffn; e.ldo = d.d_ff;
+    CK(gemm<T>(c, c->h, D, w.w_fc1, M, d.d_ff, D, e, s));
+    e = epi0(c, EPI_RESID);
+    e.bias = w.b_fc2; e.resid = c->x; e.ldr = D;
+    CK(gemm<T>(c, c->ffn, d.d_ff, w.w_fc2, M, D, d.d_ff, e, s));
+  }
+  // 3) final LN on the K mask rows, shared LM head, argmax or sampling
+  const int Mk = n * K;
+  CK(layernorm<T>(c, Mk, c->x, c->dlnf_g, c->dlnf_b, c->h, s, K1));
+  Epi e = epi0(c, EPI_LOGITS);
+  e.logits = q_logits; e.ldl = d.vocab;
+  if (temp <= 0.0f) {
+    CK(launch_argmax_init(Mk, c->amax, s, pdl));
+    e.amax = c->amax;
+    CK(gemm<T>(c, c->h, D, c->tok_emb, Mk, d.vocab, D, e, s));
+    CK(launch_argmax_finalize(n, K, nullptr, c->amax, block, K1, 1, s, pdl));
+  } else {
+    CK(gemm<T>(c, c->h, D, c->tok_emb, Mk, d.vocab, D, e, s));
+    CK(launch_sample_rows(n, K, req, q_logits, d.vocab, d.vocab, temp, seed, rnd, c->suppress, block, K1, 1, s,
+                          pdl));
+  }
+  return WS_OK;
+}
+
+// --------------------------------------------------------------------------- cross K/V
+template <typename T>
+int cross_kv_impl(ws_ctx* c, int n, const int32_t* req, const void* enc, const int32_t* cu, const int32_t* valid,
+                  int maxF, cudaStream_t s) {
+  const ws_model_desc& d = c->d;
+  const int D = d.d_model;
+  CK(launch_set_frames(n, req, cu, valid, d.max_frames, c->Fc, c->Fv, c->status, s));
+  for (int l = 0; l < c->n_xl; ++l) {
+    const LayerW& w = l < d.n_layers ? c->tl[l] : c->dl[l - d.n_layers];
+    Epi e = epi0(c, EPI_CROSSKV);
+    e.bias2 = w.b_vc; e.xkv = xkv_of(c); e.xlayer = l; e.cu_frames = cu; e.req_ids = req;
+    CK(gemm<T>(c, enc, D, w.w_kvc, maxF, 2 * D, D, e, s, n));
+  }
+  if (maxF > c->max_fc) c->max_fc = maxF;
+  return WS_OK;
+}
+
+int check_common(ws_ctx* c, int n, const int32_t* req, ws_stream stream = nullptr) {
+  if (!c) return fail(nullptr, WS_EINVAL, "null context");
+  // PDL only on created streams; the legacy default stream serialises plainly
+  c->cur_pdl = c->pdl && stream != nullptr && (cudaStream_t)stream != cudaStreamLegacy &&
+               (cudaStream_t)stream != cudaStreamPerThread;
+  if (n < 0 || n > c->d.max_batch) return fail(c, WS_EINVAL, "n_req %d outside 0..max_batch (%d)", n, c->d.max_batch);
+  if (n > 0 && !req) return fail(c, WS_EINVAL, "null req_ids");
+  return WS_OK;
+}
+
+}  // namespace
+
+// =========================================================================== C ABI
+extern "C" {
+
+size_t ws_query_workspace(const ws_model_desc* desc) {
+  if (check_desc(desc)) return 0;
+  return make_plan(*desc).total;
+}
+
+int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, size_t workspace_bytes,
+                    const void* target_blob, const void* drafter_blob, ws_stream stream) {
+  ws_ctx* c = nullptr;
+  if (!out) return fail(nullptr, WS_EINVAL, "null output handle");
+  *out = nullptr;
+  if (const char* why = check_desc(desc)) return fail(nullptr, WS_EINVAL, "%s", why);
+  if (!workspace || ((uintptr_t)workspace & 255)) return fail(nullptr, WS_EINVAL, "workspace null or not 256-byte aligned");
+  if (!target_blob) return fail(nullptr, WS_EINVAL, "null target blob");
+  if (desc->drafter_layers > 0 && !drafter_blob) return fail(nullptr, WS_EINVAL, "null drafter blob");
+  Plan p = make_plan(*desc);
+  if (workspace_bytes < p.total)
+    return fail(nullptr, WS_ENOSPACE, "workspace %zu bytes < required %zu", workspace_bytes, p.total);
+  if (desc->gemm == WS_GEMM_TC && !tc_engine_available())
+    return fail(nullptr, WS_EUNSUPPORTED, "tcgen05 GEMM engine not built");
+
+  c = new ws_ctx();
+  c->d = *desc;
+  c->es = desc->dtype == WS_BF16 ? 2 : 4;
+  c->heads = p.heads; c->ppr = p.ppr; c->n_pages = p.n_pages; c->n_xl = p.n_xl; c->max_split = p.max_split;
+  c->ws = (char*)workspace; c->ws_bytes = workspace_bytes;
+  c->engine = (desc->gemm == WS_GEMM_TC || (desc->gemm == WS_GEMM_AUTO && desc->dtype == WS_BF16 &&
+                                            tc_engine_available())) ? WS_GEMM_TC : WS_GEMM_SIMT;
+  char* b = c->ws;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t tb = target_elems(*desc) * c->es, db = drafter_elems(*desc) * c->es;
+  auto cleanup = [&](int code) { delete c; return code; };
+  cudaError_t e = cudaMemcpyAsync(b + p.tblob, target_blob, tb, cudaMemcpyDefault, s);
+  if (e == cudaSuccess && db) e = cudaMemcpyAsync(b + p.dblob, drafter_blob, db, cudaMemcpyDefault, s);
+  if (e != cudaSuccess) { fail(nullptr, WS_ECUDA, "weight copy: %s", cudaGetErrorString(e)); return cleanup(WS_ECUDA); }
+
+  const char* tp = b + p.tblob;
+  const size_t D = desc->d_model;
+  c->tok_emb = tp; tp += (size_t)desc->vocab * D * c->es;
+  c->pos_emb = tp; tp += (size_t)desc->max_pos * D * c->es;
+  c->tl.resize(desc->n_layers);
+  for (auto& w : c->tl) bind_layer(w, tp, *desc, c->es);
+  c->lnf_g = tp; tp += D * c->es;
+  c->lnf_b = tp;
+  if (desc->drafter_layers > 0) {
+    const char* dp = b + p.dblob;
+    c->fuse_w = dp; dp += D * desc->n_hist * D * c->es;
+    c->lnh_g = dp; dp += D * c->es;
+    c->lnh_b = dp; dp += D * c->es;
+    c->mask_emb = dp; dp += D * c->es;
+    c->dlnf_g = dp; dp += D * c->es;
+    c->dlnf_b = dp; dp += D * c->es;
+    c->dl.resize(desc->drafter_layers);
+    for (auto& w : c->dl) bind_layer(w, dp, *desc, c->es);
+  }
+  c->kv = b + p.kv; c->kv_layer_bytes = p.kv_layer_bytes;
+  c->hkv = b + p.hkv;
+  c->xkv = b + p.xkv;
+  c->x_layer_elems = 2 * D * desc->max_frames;
+  c->x_slot_elems = c->x_layer_elems * p.n_xl;
+  c->ptab = (int32_t*)(b + p.ptab);
+  c->rope = (float*)(b + p.rope);
+  int32_t* st = (int32_t*)(b + p.state);
+  c->L = st; c->Fc = st + desc->max_batch; c->Fv = st + 2 * desc->max_batch;
+  c->pend_start = st + 3 * desc->max_batch; c->pend_n = st + 4 * desc->max_batch;
+  c->status = st + 5 * desc->max_batch;
+  c->x = (float*)(b + p.x); c->h = b + p.h; c->q = b + p.q; c->ao = b + p.ao; c->ffn = b + p.ffn;
+  c->kb = b + p.kb; c->vb = b + p.vb; c->hist = (float*)(b + p.hist);
+  c->amax = (unsigned long long*)(b + p.amax); c->part = (float*)(b + p.part);
+  c->feat = b + p.feat; c->hpre = (float*)(b + p.hpre); c->hh = b + p.hh;
+
+  std::vector<int32_t> pt(p.n_pages);
+  for (int i = 0; i < p.n_pages; ++i) pt[i] = i;   // each slot owns its own pages
+  e = cudaMemcpyAsync(c->ptab, pt.data(), pt.size() * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st, 0, (size_t)desc->max_batch * 5 * 4 + 256, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->hist, 0, (size_t)desc->max_batch * desc->max_block *
+                                                        (desc->drafter_layers ? desc->n_hist : 0) * D * 4, s);
+  if (e == cudaSuccess) e = launch_rope_table(c->rope, desc->max_pos, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) { fail(nullptr, WS_ECUDA, "context init: %s", cudaGetErrorString(e)); return cleanup(WS_ECUDA); }
+  *out = c;
+  return WS_OK;
+}
+
+int ws_reset(ws_ctx* c, int n, const int32_t* req, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  CK(launch_reset(n, req, c->L, c->pend_n, (cudaStream_t)stream));
+  return WS_OK;
+}
+
+int ws_cross_kv(ws_ctx* c, int n, const int32_t* req, const void* enc, const int32_t* cu, const int32_t* valid,
+                int maxF, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (!enc || !cu) return fail(c, WS_EINVAL, "null encoder states or cu_frames");
+  if (maxF < 1 || maxF > c->d.max_frames) return fail(c, WS_EINVAL, "max_frames_call %d outside 1..%d", maxF, c->d.max_frames);
+  cudaStream_t s = (cudaStream_t)stream;
+  return c->d.dtype == WS_BF16 ? cross_kv_impl<bf16>(c, n, req, enc, cu, valid, maxF, s)
+                               : cross_kv_impl<float>(c, n, req, enc, cu, valid, maxF, s);
+}
+
+int ws_verify(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* block, const int32_t* blen,
+              int32_t* target, float* logits, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (H < 1 || H > c->d.max_block) return fail(c, WS_EINVAL, "H %d outside 1..max_block (%d)", H, c->d.max_block);
+  if (!block || !blen || !target) return fail(c, WS_EINVAL, "null block, block_len or target");
+  cudaStream_t s = (cudaStream_t)stream;
+  return c->d.dtype == WS_BF16 ? verify_impl<bf16>(c, n, req, H, block, blen, target, logits, s)
+                               : verify_impl<float>(c, n, req, H, block, blen, target, logits, s);
+}
+
+int ws_draft(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temperature, uint64_t seed, uint64_t round,
+             float* q_logits, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (c->d.drafter_layers == 0) return fail(c, WS_EUNSUPPORTED, "context has no drafter");
+  if (!block) return fail(c, WS_EINVAL, "null block");
+  if (!(temperature >= 0.0f)) return fail(c, WS_EINVAL, "temperature must be >= 0");
+  if (temperature > 0.0f && !q_logits) return fail(c, WS_EINVAL, "sampling needs q_logits");
+  cudaStream_t s = (cudaStream_t)stream;
+  return c->d.dtype == WS_BF16 ? draft_impl<bf16>(c, n, req, block, temperature, seed, round, q_logits, s)
+                               : draft_impl<float>(c, n, req, block, temperature, seed, round, q_logits, s);
+}
+
+int ws_accept(ws_ctx* c, int n, const int32_t* req, const ws_accept_args* a, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (!a) return fail(c, WS_EINVAL, "null accept args");
+  if (n == 0) return WS_OK;
+  if (a->mode < WS_ACCEPT_GREEDY || a->mode > WS_ACCEPT_FORCED) return fail(c, WS_EINVAL, "unknown accept mode");
+  if (a->H < 1 || a->H > c->d.max_block) return fail(c, WS_EINVAL, "H outside 1..max_block");
+  if (!a->block || !a->block_len || !a->budget || !a->done || !a->n_acc || !a->n_emit || !a->next_block ||
+      !a->next_len)
+    return fail(c, WS_EINVAL, "null required accept array");
+  if (a->next_stride < 1) return fail(c, WS_EINVAL, "next_stride must be >= 1");
+  if (a->mode != WS_ACCEPT_SAMPLE && !a->target) return fail(c, WS_EINVAL, "greedy/forced acceptance needs target");
+  if (a->mode == WS_ACCEPT_SAMPLE) {
+    if (!a->p_logits || !a->q_logits) return fail(c, WS_EINVAL, "sampling acceptance needs p_logits and q_logits");
+    if (!(a->temperature > 0.0f)) return fail(c, WS_EINVAL, "sampling acceptance needs temperature > 0");
+  }
+  if (a->transcript && (!a->out_len || a->tcap < 1)) return fail(c, WS_EINVAL, "transcript needs out_len and tcap");
+  AcceptParams p;
+  p.a = *a;
+  p.req_ids = req;
+  p.L = c->L;
+  p.K = c->d.K;
+  p.V = c->d.vocab;
+  p.eos = c->d.eos_id;
+  p.suppress = c->suppress;
+  p.status = c->status;
+  CK(launch_accept(n, p, (cudaStream_t)stream, c->cur_pdl));
+  return WS_OK;
+}
+
+int ws_draft_synthetic(ws_ctx* c, int n, const int32_t* req, int32_t* block, const int32_t* traj, int tlen,
+                       const uint8_t* cmask, const int32_t* ctok, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (!block || !traj || !cmask || !ctok || tlen < 1) return fail(c, WS_EINVAL, "null synthetic-draft input");
+  CK(launch_draft_synth(n, c->d.K, req, c->L, block, traj, tlen, cmask, ctok, c->d.max_pos, (cudaStream_t)stream,
+                        c->cur_pdl));
+  return WS_OK;
+}
+
+int ws_sample(ws_ctx* c, int n, const int32_t* req, const float* logits, int rows, float temperature, uint64_t seed,
+              uint64_t round, int32_t* out, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (!logits || !out || rows < 1) return fail(c, WS_EINVAL, "null logits/out or rows < 1");
+  if (!(temperature > 0.0f)) return fail(c, WS_EINVAL, "temperature must be > 0");
+  CK(launch_sample_rows(n, rows, req, logits, c->d.vocab, c->d.vocab, temperature, seed, round, c->suppress, out,
+                        rows, 0, (cudaStream_t)stream, c->cur_pdl));
+  return WS_OK;
+}
+
+int ws_set_suppress(ws_ctx* c, const uint32_t* mask) {
+  if (!c) return fail(nullptr, WS_EINVAL, "null context");
+  c->suppress = mask;
+  return WS_OK;
+}
+
+int ws_get_lengths(ws_ctx* c, int n, const int32_t* req, int32_t* out, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (!out) return fail(c, WS_EINVAL, "null output");
+  CK(launch_get_lengths(n, req, c->L, out, (cudaStream_t)stream));
+  return WS_OK;
+}
+
+int ws_status(ws_ctx* c, ws_stream stream, int32_t* host_status) {
+  if (!c) return fail(nullptr, WS_EINVAL, "null context");
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t v = 0;
+  CK(cudaMemcpyAsync(&v, c->status, 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  CK(cudaMemsetAsync(c->status, 0, 4, s));
+  CK(cudaStreamSynchronize(s));
+  if (host_status) *host_status = v;
+  if (v) return fail(c, WS_EDEVICE, "device status 0x%x (1 = position >= max_pos, 2 = token id, 4 = frames)", v);
+  return WS_OK;
+}
+
+const char* ws_gemm_engine(const ws_ctx* c) {
+  if (!c) return "none";
+  return c->engine == WS_GEMM_TC ? "tcgen05" : "simt";
+}
+
+const char* ws_last_error(const ws_ctx* c) { return c ? c->err.c_str() : g_err.c_str(); }
+
+void ws_free(ws_ctx* c) { delete c; }
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+// GEMM epilogues: what happens to an fp32 accumulator pair (row r, features
+// n and n+1).  Shared by the SIMT and the tcgen05 GEMM engines so both store
+// identical results for identical accumulators.
+#pragma once
+#include "ws_internal.cuh"
+
+template <typename T>
+__device__ __forceinline__ float bias_at(const void* b, int n) {
+  return b ? to_f<T>(reinterpret_cast<const T*>(b)[n]) : 0.0f;
+}
+
+// RoPE (RoFormer, interleaved pairs): rotate (y0, y1) = features (n, n+1) of
+// a head by the angle of pair (n % 64) / 2 at absolute position pos.
+__device__ __forceinline__ void rope_pair(const float* tab, int pos, int n, float& y0, float& y1) {
+  const float* cs = tab + ((size_t)pos * (WS_DH / 2) + (n % WS_DH) / 2) * 2;
+  float c = cs[0], s = cs[1];
+  float a = y0, b = y1;
+  y0 = a * c - b * s;
+  y1 = a * s + b * c;
+}
+
+// n is even; features n and n+1 are both < N.  `z` is the batch index
+// (request) for CROSSKV, whose rows are frame indices of that request.
+template <typename T>
+__device__ __forceinline__ void epi_pair(const Epi& e, int r, int n, float y0, float y1, int z) {
+  switch (e.kind) {
+    case EPI_STORE:
+    case EPI_GELU: {
+      float v0 = y0 + bias_at<T>(e.bias, n), v1 = y1 + bias_at<T>(e.bias, n + 1);
+      if (e.kind == EPI_GELU) { v0 = gelu_erf(v0); v1 = gelu_erf(v1); }
+      T* o = reinterpret_cast<T*>(e.out) + (size_t)r * e.ldo + n;
+      o[0] = from_f<T>(v0); o[1] = from_f<T>(v1);
+      break;
+    }
+    case EPI_F32: {
+      float* o = reinterpret_cast<float*>(e.out) + (size_t)r * e.ldo + n;
+      o[0] = y0 + bias_at<T>(e.bias, n); o[1] = y1 + bias_at<T>(e.bias, n + 1);
+      break;
+    }
+    case EPI_RESID: {
+      float* x = e.resid + (size_t)r * e.ldr + n;
+      float v0 = x[0] + (y0 + bias_at<T>(e.bias, n));
+      float v1 = x[1] + (y1 + bias_at<T>(e.bias, n + 1));
+      x[0] = v0; x[1] = v1;
+      if (e.hist) {
+        int slot, j, pos;
+        row_info(e.rm, r, slot, j, pos);
+        float* h = e.hist + (((size_t)slot * e.max_block + j) * e.n_hist + e.hist_idx) * e.d + n;
+        h[0] = v0; h[1] = v1;
+      }
+      break;
+    }
+    case EPI_QKV:
+    case EPI_QKV_DRAFT: {
+      int part = n / e.d, nn = n - part * e.d;
+      int slot, j, pos;
+      bool valid = row_info(e.rm, r, slot, j, pos);
+      if (part == 0) {
+        y0 += bias_at<T>(e.bias, nn); y1 += bias_at<T>(e.bias, nn + 1);
+        if (e.kind == EPI_QKV_DRAFT) rope_pair(e.rope, min(pos, e.rm.max_pos - 1), nn, y0, y1);
+        T* o = reinterpret_cast<T*>(e.out) + (size_t)r * e.d + nn;
+        o[0] = from_f<T>(y0); o[1] = from_f<T>(y1);
+      } else {
+        if (part == 2) { y0 += bias_at<T>(e.bias2, nn); y1 += bias_at<T>(e.bias2, nn + 1); }
+        if (e.kind == EPI_QKV_DRAFT) {
+          if (part == 1) rope_pair(e.rope, min(pos, e.rm.max_pos - 1), nn, y0, y1);
+          T* o = reinterpret_cast<T*>(part == 1 ? e.kout : e.vout) + (size_t)r * e.d + nn;
+          o[0] = from_f<T>(y0); o[1] = from_f<T>(y1);
+        } else if (valid) {
+          T* o = kv_ptr<T>(e.kv, slot, pos, part - 1, nn / WS_DH) + (nn % WS_DH);
+          o[0] = from_f<T>(y0); o[1] = from_f<T>(y1);
+        }
+      }
+      break;
+    }
+    case EPI_HISTKV: {
+      int part = n / e.d, nn = n - part * e.d;
+      int slot, j, pos;
+      if (!row_info(e.rm, r, slot, j, pos)) break;
+      if (part == 0) rope_pair(e.rope, pos, nn, y0, y1);
+      else { y0 += bias_at<T>(e.bias2, nn); y1 += bias_at<T>(e.bias2, nn + 1); }
+      T* o = kv_ptr<T>(e.kv, slot, pos, part, nn / WS_DH) + (nn % WS_DH);
+      o[0] = from_f<T>(y0); o[1] = from_f<T>(y1);
+      break;
+    }
+    case EPI_CROSSKV: {
+      int part = n / e.d, nn = n - part * e.d;
+      if (part == 1) { y0 += bias_at<T>(e.bias2, nn); y1 += bias_at<T>(e.bias2, nn + 1); }
+      int slot = e.req_ids[z];
+      T* o = xkv_ptr<T>(e.xkv, slot, e.xlayer, part, nn / WS_DH, r) + (nn % WS_DH);
+      o[0] = from_f<T>(y0); o[1] = from_f<T>(y1);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+// LM head value of one logit: suppressed ids become -inf (Whisper-Flash
+// Appendix A.4: draft and target logits get the same token suppression).
+__device__ __forceinline__ float epi_logit(const Epi& e, int n, float y) {
+  if (e.suppress && ((e.suppress[n >> 5] >> (n & 31)) & 1u)) return -INFINITY;
+  return y;
+}

@@ -1,0 +1,250 @@
+// Internal declarations shared by the CUDA translation units of libws.
+// Nothing here is part of the public ABI (include/ws.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/ws.h"
+
+typedef __nv_bfloat16 bf16;
+
+#define WS_DH 64          // head width (Whisper: d_model / n_heads = 64)
+#define WS_PAGE 64        // tokens per KV-cache page
+#define WS_XCHUNK 128     // encoder frames per cross-attention split
+#define WS_MAX_SPLIT 12   // ceil(1500 / WS_XCHUNK)
+
+// Device status bits (ws_status).
+#define WS_ST_POS 1       // a position at or beyond max_pos was requested
+#define WS_ST_TOKEN 2     // a token id outside [0, V) was seen
+#define WS_ST_FRAMES 4    // frame counts inconsistent with max_frames
+
+// ------------------------------------------------------------------ conversions
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<bf16>(bf16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float gelu_erf(float x) {
+  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+// Total order on floats as unsigned ints (larger float -> larger key).
+__device__ __forceinline__ uint32_t f32_order(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// Argmax key: value first, then the LOWEST id wins ties.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int id) {
+  return ((unsigned long long)f32_order(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
+}
+__device__ __forceinline__ int argmax_key_id(unsigned long long k) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+}
+
+// ------------------------------------------------------------------ Philox4x32-10
+// Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
+// (SC'11): 10 rounds of the Philox S-box with the published multipliers and
+// Weyl key increments.
+struct Philox4 { uint32_t x[4]; };
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    k0 += 0x9E3779B9u; k1 += 0xBB67AE85u;
+  }
+  Philox4 o; o.x[0] = c0; o.x[1] = c1; o.x[2] = c2; o.x[3] = c3;
+  return o;
+}
+// The method's uniform in [0,1): counter (slot, round, j, purpose), key = seed.
+__device__ __forceinline__ float ws_uniform(uint64_t seed, uint32_t slot, uint64_t rnd, uint32_t j,
+                                            uint32_t purpose) {
+  Philox4 o = philox4x32_10(slot, (uint32_t)rnd, j, purpose, (uint32_t)seed, (uint32_t)(seed >> 32));
+  return (float)(o.x[0] >> 8) * (1.0f / 16777216.0f);
+}
+
+// ------------------------------------------------------------------ warp / block reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ------------------------------------------------------------------ PDL
+// Programmatic dependent launch: a kernel may start while its predecessor on
+// the stream drains; it must wait before touching the predecessor's outputs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ------------------------------------------------------------------ row maps
+// How a row of an activation matrix maps to (request slot, block row j,
+// absolute position).  Rows are laid out request-major: r = i * H + j.
+enum RowMode { ROW_VERIFY = 0, ROW_DRAFT = 1, ROW_HIST = 2, ROW_PLAIN = 3 };
+struct RowMap {
+  int mode;
+  int H;                       // rows per request in this call
+  int max_pos;
+  const int32_t* req_ids;      // [n]
+  const int32_t* L;            // [max_batch] cache lengths (ctx state)
+  const int32_t* block_len;    // [n] (ROW_VERIFY)
+  const int32_t* pend_start;   // [max_batch] (ROW_HIST)
+  const int32_t* pend_n;       // [max_batch] (ROW_HIST)
+};
+// Returns true when the row holds a real token whose K/V may be written.
+__device__ __forceinline__ bool row_info(const RowMap& m, int r, int& slot, int& j, int& pos) {
+  int i = r / m.H;
+  j = r - i * m.H;
+  slot = m.req_ids[i];
+  bool valid;
+  if (m.mode == ROW_HIST) {
+    pos = m.pend_start[slot] + j;
+    valid = j < m.pend_n[slot];
+  } else {
+    pos = m.L[slot] + j;
+    valid = (m.mode == ROW_VERIFY) ? (j < m.block_len[i]) : true;
+  }
+  return valid && pos < m.max_pos;
+}
+
+// ------------------------------------------------------------------ KV layouts
+// Self / history KV pool of one layer: [n_pages][2 (K,V)][heads][WS_PAGE][64].
+// Page of (slot, pos) = ptab[slot * ppr + pos / WS_PAGE].
+struct KVPool {
+  void* base;                  // this layer's pool
+  const int32_t* ptab;
+  int ppr;                     // pages per request
+  int n_heads;
+};
+template <typename T>
+__device__ __forceinline__ T* kv_ptr(const KVPool& p, int slot, int pos, int kv, int head) {
+  int page = p.ptab[slot * p.ppr + pos / WS_PAGE];
+  size_t off = (((size_t)page * 2 + kv) * p.n_heads + head) * (WS_PAGE * WS_DH) + (size_t)(pos % WS_PAGE) * WS_DH;
+  return reinterpret_cast<T*>(p.base) + off;
+}
+
+// Cross (acoustic) K/V of one request and one layer: [2][heads][max_frames][64].
+struct XKV {
+  void* base;                  // slot 0, layer 0
+  size_t slot_stride;          // elements between slots
+  size_t layer_stride;         // elements between layers (= 2 * heads * max_frames * 64)
+  int max_frames;
+  int n_heads;
+};
+template <typename T>
+__device__ __forceinline__ T* xkv_ptr(const XKV& x, int slot, int layer, int kv, int head, int frame) {
+  return reinterpret_cast<T*>(x.base) + (size_t)slot * x.slot_stride + (size_t)layer * x.layer_stride +
+         ((size_t)kv * x.n_heads + head) * ((size_t)x.max_frames * WS_DH) + (size_t)frame * WS_DH;
+}
+
+// ------------------------------------------------------------------ GEMM epilogues
+enum EpiKind {
+  EPI_STORE = 0,    // out[r, n] = act(y + b)
+  EPI_GELU = 1,     // out[r, n] = act(gelu(y + b))
+  EPI_F32 = 2,      // outf[r, n] = y + b
+  EPI_RESID = 3,    // resid[r, n] += y + b  (+ optional history copy)
+  EPI_QKV = 4,      // target self-attention: q -> qout, k/v -> paged cache
+  EPI_QKV_DRAFT = 5,// drafter block: RoPE(q) -> qout, RoPE(k) -> kout, v -> vout
+  EPI_HISTKV = 6,   // drafter history: RoPE(k), v + b -> history cache
+  EPI_CROSSKV = 7,  // acoustic K/V -> per-request slabs
+  EPI_LOGITS = 8    // logits (+ suppression) -> optional store + argmax keys
+};
+
+struct Epi {
+  int kind;
+  int d;                        // model width (QKV splits)
+  const void* bias;             // [N] model dtype or NULL (QKV: b_q)
+  const void* bias2;            // QKV: b_v ; HISTKV: b_v
+  void* out; int ldo;           // model-dtype or f32 output
+  float* resid; int ldr;
+  // history copy of the updated residual (verify, history layers):
+  // hist[(slot * max_block + j) * n_hist + hidx][n]
+  float* hist; int hist_idx; int n_hist; int max_block;
+  RowMap rm;
+  KVPool kv;                    // QKV / HISTKV target
+  void* kout; void* vout;       // QKV_DRAFT
+  const float* rope;            // [max_pos][32][2] (cos, sin) or NULL
+  XKV xkv; int xlayer;          // CROSSKV
+  const int32_t* cu_frames;     // CROSSKV: [n+1]
+  const int32_t* req_ids;       // CROSSKV
+  float* logits; long long ldl; // LOGITS
+  unsigned long long* amax;     // LOGITS: [M] argmax keys
+  const uint32_t* suppress;     // LOGITS
+  int32_t* status;
+};
+
+// ------------------------------------------------------------------ launchers
+// Implemented in ws_gemm_simt.cu / ws_gemm_tc.cu / ws_kernels.cu / ws_attn.cu.
+struct GemmShape {
+  const void* X; int ldx;       // [M, K] activations, model dtype
+  const void* W; int ldw;       // [N, K] weights, model dtype
+  int M, N, K;
+  int batch;                    // grid.z repeats (CROSSKV: n_req), row offset by cu_frames
+};
+
+template <typename T> cudaError_t launch_gemm_simt(const GemmShape& g, const Epi& e, cudaStream_t s, bool pdl);
+
+struct TcGemm;  // tcgen05 engine state (ws_gemm_tc.cu)
+bool tc_engine_available();
+
+template <typename T>
+cudaError_t launch_layernorm(int M, int d, const float* x, int ldx, const T* g, const T* b, T* y, int ldy,
+                             int group_skip, cudaStream_t s, bool pdl);
+template <typename T>
+cudaError_t launch_embed_target(int n, int H, const RowMap& rm, const int32_t* block, const T* E,
+                                const T* P, int d, int V, float* x, int32_t* pend_start, int32_t* pend_n,
+                                int32_t* status, cudaStream_t s, bool pdl);
+template <typename T>
+cudaError_t launch_embed_draft(int n, int K1, const int32_t* req_ids, const int32_t* block, const T* E,
+                               const T* m, int d, int V, float* x, int32_t* pend_n, int32_t* status,
+                               cudaStream_t s, bool pdl);
+cudaError_t launch_argmax_init(int M, unsigned long long* keys, cudaStream_t s, bool pdl);
+cudaError_t launch_argmax_finalize(int n, int H, const int32_t* block_len, const unsigned long long* keys,
+                                   int32_t* out, int out_stride, int out_col0, cudaStream_t s, bool pdl);
+template <typename T>
+cudaError_t launch_hist_gather(int n, int Hp, const int32_t* req_ids, const int32_t* pend_n,
+                               const float* hist, int max_block, int n_hist, int d, T* feat,
+                               cudaStream_t s, bool pdl);
+template <typename T>
+cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const KVPool& kv, T* O,
+                             int n_heads, cudaStream_t s, bool pdl);
+template <typename T>
+cudaError_t launch_draft_attn(int n, int K1, const int32_t* req_ids, const int32_t* L, const T* Q,
+                              const T* Kb, const T* Vb, const KVPool& hkv, T* O, int n_heads,
+                              int max_pos, cudaStream_t s, bool pdl);
+template <typename T>
+cudaError_t launch_cross_attn(int n, int H, const int32_t* req_ids, const int32_t* Fv, const T* Q,
+                              const XKV& x, int layer, float* part, T* O, int n_heads, int n_split,
+                              cudaStream_t s, bool pdl);
+cudaError_t launch_rope_table(float* tab, int max_pos, cudaStream_t s);
+cudaError_t launch_set_frames(int n, const int32_t* req_ids, const int32_t* cu, const int32_t* valid,
+                              int max_frames, int32_t* Fc, int32_t* Fv, int32_t* status, cudaStream_t s);
+cudaError_t launch_reset(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n, cudaStream_t s);
+cudaError_t launch_sample_rows(int n, int rows, const int32_t* req_ids, const float* logits, long long row_stride,
+                               int V, float T, uint64_t seed, uint64_t rnd, const uint32_t* suppress,
+                               int32_t* out, int out_stride, int out_col0, cudaStream_t s, bool pdl);
+struct AcceptParams {
+  ws_accept_args a;
+  const int32_t* req_ids;
+  int32_t* L;
+  int K, V, eos;
+  const uint32_t* suppress;
+  int32_t* status;
+};
+cudaError_t launch_accept(int n, const AcceptParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_draft_synth(int n, int K, const int32_t* req_ids, const int32_t* L, int32_t* block,
+                               const int32_t* traj, int tlen, const uint8_t* cmask, const int32_t* ctok,
+                               int max_pos, cudaStream_t s, bool pdl);
+cudaError_t launch_get_lengths(int n, const int32_t* req_ids, const int32_t* L, int32_t* out, cudaStream_t s);

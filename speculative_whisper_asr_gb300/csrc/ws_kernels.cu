@@ -1,0 +1,540 @@
+// Element-wise and per-request kernels of the decoding path: embeddings,
+// layer norm, argmax bookkeeping, history gather, sampling, acceptance.
+#include "ws_internal.cuh"
+
+namespace {
+
+cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                            cudaLaunchAttribute* at) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cfg;
+}
+
+// Block-wide fixed-order reductions (blockDim.x == 256 or 128).
+template <int NT>
+__device__ float block_sum(float v, float* sh) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) t += sh[i];
+  return t;
+}
+template <int NT>
+__device__ float block_max(float v, float* sh) {
+  v = warp_max(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  float t = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) t = fmaxf(t, sh[i]);
+  return t;
+}
+
+// ------------------------------------------------------------------ embeddings
+// Target rows: x = E[token] + P[position] (token + learned position embedding).
+template <typename T>
+__global__ void embed_target_kernel(RowMap rm, const int32_t* block, const T* E, const T* P, int d, int V,
+                                    float* x, int32_t* pend_start, int32_t* pend_n, int32_t* status) {
+  pdl_wait();
+  const int r = blockIdx.x;
+  int slot, j, pos;
+  bool valid = row_info(rm, r, slot, j, pos);
+  const int i = r / rm.H;
+  int tok = block[r];
+  bool in_block = j < rm.block_len[i];
+  if (in_block && pos >= rm.max_pos && threadIdx.x == 0) atomicOr(status, WS_ST_POS);
+  if (!valid) { tok = 0; pos = min(pos, rm.max_pos - 1); }
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) atomicOr(status, WS_ST_TOKEN);
+    tok = 0;
+  }
+  if (j == 0 && threadIdx.x == 0) {
+    pend_start[slot] = rm.L[slot];
+    pend_n[slot] = rm.block_len[i];
+  }
+  pdl_trigger();
+  const T* e = E + (size_t)tok * d;
+  const T* p = P + (size_t)pos * d;
+  for (int n = threadIdx.x; n < d; n += blockDim.x) x[(size_t)r * d + n] = to_f<T>(e[n]) + to_f<T>(p[n]);
+}
+
+// Drafter rows: X_t = [Emb(anchor), m, ..., m] (Whisper-Flash Eq. 2); no
+// absolute position embedding (positions enter through RoPE).
+template <typename T>
+__global__ void embed_draft_kernel(int K1, const int32_t* req_ids, const int32_t* block, const T* E, const T* m,
+                                   int d, int V, float* x, int32_t* pend_n, int32_t* status) {
+  pdl_wait();
+  const int r = blockIdx.x, i = r / K1, j = r - i * K1;
+  const T* src = m;
+  if (j == 0) {
+    int tok = block[(size_t)i * K1];
+    if (tok < 0 || tok >= V) {
+      if (threadIdx.x == 0) atomicOr(status, WS_ST_TOKEN);
+      tok = 0;
+    }
+    src = E + (size_t)tok * d;
+    if (threadIdx.x == 0) pend_n[req_ids[i]] = 0;   // history rows are folded in by now
+  }
+  pdl_trigger();
+  for (int n = threadIdx.x; n < d; n += blockDim.x) x[(size_t)r * d + n] = to_f<T>(src[n]);
+}
+
+// ------------------------------------------------------------------ layer norm
+// y = (x - mean) / sqrt(var + 1e-5) * g + b over each row, fp32 statistics.
+// group_skip > 0: output row o reads input row (o / (G-1)) * G + o % (G-1) + 1
+// (drops row 0 of every group of G rows: the drafter's anchor row).
+template <typename T>
+__global__ void __launch_bounds__(128) layernorm_kernel(int d, const float* x, int ldx, const T* g, const T* b,
+                                                        T* y, int ldy, int group_skip) {
+  __shared__ float sh[4];
+  pdl_wait();
+  const int o = blockIdx.x;
+  int src = o;
+  if (group_skip > 0) {
+    int G1 = group_skip - 1;
+    src = (o / G1) * group_skip + (o % G1) + 1;
+  }
+  const float* xr = x + (size_t)src * ldx;
+  float v[16];
+  float s = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    int n = threadIdx.x + u * 128;
+    v[u] = n < d ? xr[n] : 0.0f;
+    s += v[u];
+  }
+  const float mean = block_sum<128>(s, sh) / (float)d;
+  float q = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    int n = threadIdx.x + u * 128;
+    float c = n < d ? v[u] - mean : 0.0f;
+    q += c * c;
+  }
+  const float var = block_sum<128>(q, sh) / (float)d;
+  const float rstd = rsqrtf(var + 1e-5f);
+  pdl_trigger();
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    int n = threadIdx.x + u * 128;
+    if (n < d) y[(size_t)o * ldy + n] = from_f<T>((v[u] - mean) * rstd * to_f<T>(g[n]) + to_f<T>(b[n]));
+  }
+}
+
+// ------------------------------------------------------------------ argmax
+__global__ void argmax_init_kernel(int M, unsigned long long* keys) {
+  pdl_wait();
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < M) keys[i] = 0ull;
+  pdl_trigger();
+}
+
+// keys [n*H] -> out[i*stride + col0 + j]; rows j >= block_len[i] get -1.
+__global__ void argmax_finalize_kernel(int n, int H, const int32_t* block_len, const unsigned long long* keys,
+                                       int32_t* out, int stride, int col0) {
+  pdl_wait();
+  int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r < n * H) {
+    int i = r / H, j = r - i * H;
+    bool valid = block_len ? (j < block_len[i]) : true;
+    out[(size_t)i * stride + col0 + j] = valid ? argmax_key_id(keys[r]) : -1;
+  }
+  pdl_trigger();
+}
+
+// ------------------------------------------------------------------ history gather
+// feat[i*Hp + j] = concat_h resid_h(slot, j) for pending rows (else zeros);
+// the concatenated residual streams are the fusion projection's input.
+template <typename T>
+__global__ void hist_gather_kernel(int Hp, const int32_t* req_ids, const int32_t* pend_n, const float* hist,
+                                   int max_block, int n_hist, int d, T* feat) {
+  pdl_wait();
+  const int r = blockIdx.x, i = r / Hp, j = r - i * Hp;
+  const int slot = req_ids[i];
+  const bool valid = j < pend_n[slot];
+  const int w = n_hist * d;
+  const float* src = hist + ((size_t)slot * max_block + j) * w;
+  pdl_trigger();
+  for (int c = threadIdx.x; c < w; c += blockDim.x) feat[(size_t)r * w + c] = from_f<T>(valid ? src[c] : 0.0f);
+}
+
+// ------------------------------------------------------------------ RoPE table
+// tab[pos][i] = (cos, sin)(fp32(pos * theta_i)), theta_i = fp32(10000^(-2i/64)):
+// base 10,000 and FP32 phases (Whisper-Flash Appendix A.2).  The cos/sin of the
+// fp32 phase are evaluated in double and rounded once.
+__global__ void rope_table_kernel(float* tab, int max_pos) {
+  int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= max_pos * (WS_DH / 2)) return;
+  int pos = idx / (WS_DH / 2), i = idx % (WS_DH / 2);
+  float theta = (float)pow(10000.0, -2.0 * (double)i / (double)WS_DH);
+  float ang = (float)pos * theta;
+  tab[idx * 2 + 0] = (float)cos((double)ang);
+  tab[idx * 2 + 1] = (float)sin((double)ang);
+}
+
+// ------------------------------------------------------------------ request state
+__global__ void set_frames_kernel(int n, const int32_t* req_ids, const int32_t* cu, const int32_t* valid,
+                                  int max_frames, int32_t* Fc, int32_t* Fv, int32_t* status) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  int F = cu[i + 1] - cu[i];
+  int v = valid ? valid[i] : F;
+  if (F < 0 || F > max_frames || v < 0 || v > F) {
+    atomicOr(status, WS_ST_FRAMES);
+    F = max(0, min(F, max_frames));
+    v = max(0, min(v, F));
+  }
+  Fc[req_ids[i]] = F;
+  Fv[req_ids[i]] = v;
+}
+
+__global__ void reset_kernel(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) { L[req_ids[i]] = 0; pend_n[req_ids[i]] = 0; }
+}
+
+__global__ void get_lengths_kernel(int n, const int32_t* req_ids, const int32_t* L, int32_t* out) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = L[req_ids[i]];
+}
+
+// ------------------------------------------------------------------ sampling helpers
+constexpr int SNT = 256;   // threads of the sampling / acceptance CTAs
+
+__device__ __forceinline__ bool suppressed(const uint32_t* sup, int v) {
+  return sup && ((sup[v >> 5] >> (v & 31)) & 1u);
+}
+// Scaled logit z/T (suppressed ids -> -inf).
+__device__ __forceinline__ float scaled(const float* z, int v, float T, const uint32_t* sup) {
+  return suppressed(sup, v) ? -INFINITY : z[v] / T;
+}
+
+struct RowStat { float m, S; };
+// max and sum of exp(z/T - max) over a row (FP32, fixed order per thread chunk).
+__device__ RowStat row_stat(const float* z, int V, float T, const uint32_t* sup, float* sh) {
+  float m = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += SNT) m = fmaxf(m, scaled(z, v, T, sup));
+  m = block_max<SNT>(m, sh);
+  float s = 0.0f;
+  for (int v = threadIdx.x; v < V; v += SNT) s += expf(scaled(z, v, T, sup) - m);
+  s = block_sum<SNT>(s, sh);
+  RowStat r; r.m = m; r.S = s;
+  return r;
+}
+
+// Inverse CDF over non-negative weights w(v), v = 0..V-1 in ascending id
+// order: the smallest v whose running sum exceeds u * sum(w).  Each thread
+// owns a contiguous chunk; chunk sums are prefixed in thread order.
+template <class WF>
+__device__ int block_inverse_cdf(WF w, int V, float u, float* sh /* >= SNT + 8 floats */) {
+  __shared__ int found;
+  const int C = (V + SNT - 1) / SNT;
+  const int lo = threadIdx.x * C, hi = min(V, lo + C);
+  float s = 0.0f;
+  for (int v = lo; v < hi; ++v) s += w(v);
+  __syncthreads();
+  sh[threadIdx.x] = s;
+  if (threadIdx.x == 0) found = -1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float run = 0.0f;
+    for (int t = 0; t < SNT; ++t) { float c = sh[t]; sh[t] = run; run += c; }
+    sh[SNT] = run;
+  }
+  __syncthreads();
+  const float total = sh[SNT];
+  const float target = u * total;
+  const float pre = sh[threadIdx.x];
+  const float nxt = threadIdx.x + 1 < SNT ? sh[threadIdx.x + 1] : total;
+  if (s > 0.0f && pre <= target && target < nxt) {
+    float run = pre;
+    int tok = -1, last = -1;
+    for (int v = lo; v < hi; ++v) {
+      float wv = w(v);
+      if (wv > 0.0f) last = v;
+      run += wv;
+      if (run > target) { tok = v; break; }
+    }
+    atomicMax(&found, tok >= 0 ? tok : last);
+  }
+  __syncthreads();
+  if (found < 0) {   // rounding pushed the target past the end: last id with weight
+    if (threadIdx.x == 0) {
+      for (int v = V - 1; v >= 0; --v) if (w(v) > 0.0f) { found = v; break; }
+      if (found < 0) found = 0;
+    }
+    __syncthreads();
+  }
+  int res = found;
+  __syncthreads();
+  return res;
+}
+
+// One sampled token per (request, row): softmax(z / T) via inverse CDF with
+// Philox counter (slot, round, row + 1, 0) — the drafter's sampler.
+__global__ void __launch_bounds__(SNT) sample_rows_kernel(int rows, const int32_t* req_ids, const float* logits,
+                                                          long long row_stride, int V, float T, uint64_t seed,
+                                                          uint64_t rnd, const uint32_t* sup, int32_t* out,
+                                                          int out_stride, int out_col0) {
+  __shared__ float sh[SNT + 8];
+  pdl_wait();
+  const int i = blockIdx.x / rows, r = blockIdx.x - i * rows;
+  const int slot = req_ids[i];
+  const float* z = logits + ((long long)i * rows + r) * row_stride;
+  RowStat st = row_stat(z, V, T, sup, sh);
+  const float u = ws_uniform(seed, (uint32_t)slot, rnd, (uint32_t)(r + 1), 0u);
+  int tok = block_inverse_cdf([&](int v) { return expf(scaled(z, v, T, sup) - st.m); }, V, u, sh);
+  pdl_trigger();
+  if (threadIdx.x == 0) out[(size_t)i * out_stride + out_col0 + r] = tok;
+}
+
+// ------------------------------------------------------------------ acceptance
+// One CTA per request.  Whisper-Flash §3.1 / Appendix A.1 / A.4.
+__global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
+  __shared__ float sh[SNT + 8];
+  __shared__ int s_emit[17];
+  __shared__ int s_ne, s_a, s_stop;
+  pdl_wait();
+  const ws_accept_args& A = P.a;
+  const int i = blockIdx.x;
+  const int slot = P.req_ids[i];
+  const int blen = A.block_len[i];
+  const bool was_done = A.done[i] != 0;
+  int R = A.budget[i];
+  if (was_done || blen <= 0 || R <= 0) {
+    if (threadIdx.x == 0) {
+      A.n_acc[i] = 0;
+      A.n_emit[i] = 0;
+      A.next_len[i] = 0;
+      A.next_block[(size_t)i * A.next_stride] = A.block[(size_t)i * A.H];
+      if (!was_done && (blen <= 0 || R <= 0)) {
+        // an idle request with no budget left is finished
+        if (R <= 0) { A.done[i] = 1; if (A.n_done) atomicAdd(A.n_done, 1); }
+      }
+    }
+    return;
+  }
+  const int32_t* blk = A.block + (size_t)i * A.H;
+  // at most R-1 candidates (Appendix A.1); a forced block is taken whole
+  int n_prop = A.mode == WS_ACCEPT_FORCED ? blen - 1 : min(blen - 1, max(R - 1, 0));
+  n_prop = min(n_prop, A.H - 1);                       // the block holds H tokens
+  if (A.mode == WS_ACCEPT_SAMPLE) n_prop = min(n_prop, P.K);   // q rows exist for K candidates
+  if (threadIdx.x == 0) { s_ne = 0; s_a = 0; s_stop = 0; }
+  __syncthreads();
+
+  if (A.mode == WS_ACCEPT_GREEDY || A.mode == WS_ACCEPT_FORCED) {
+    if (threadIdx.x == 0) {
+      const int32_t* g = A.target + (size_t)i * A.H;
+      int a = 0, ne = 0;
+      bool eos_hit = false;
+      if (A.mode == WS_ACCEPT_FORCED) {
+        a = n_prop;
+      } else {
+        for (int j = 1; j <= n_prop; ++j) {
+          if (blk[j] != g[j - 1]) break;
+          ++a;
+          s_emit[ne++] = blk[j];
+          if (blk[j] == P.eos) { eos_hit = true; break; }
+        }
+      }
+      if (!eos_hit) s_emit[ne++] = g[a];
+      s_a = a;
+      s_ne = ne;
+    }
+    __syncthreads();
+  } else {
+    // Rejection rule: accept y_j iff u_j * q_j(y_j) < p_j(y_j) (FP32).
+    const float T = A.temperature;
+    for (int j = 1; j <= n_prop; ++j) {
+      const int y = blk[j];
+      const float* zp = A.p_logits + ((long long)i * A.H + (j - 1)) * P.V;
+      const float* zq = A.q_logits + ((long long)i * P.K + (j - 1)) * P.V;
+      RowStat sp = row_stat(zp, P.V, T, P.suppress, sh);
+      RowStat sq = row_stat(zq, P.V, T, P.suppress, sh);
+      const bool yok = y >= 0 && y < P.V;
+      const float py = yok ? expf(scaled(zp, y, T, P.suppress) - sp.m) / sp.S : 0.0f;
+      const float qy = yok ? expf(scaled(zq, y, T, P.suppress) - sq.m) / sq.S : 0.0f;
+      const float u = ws_uniform(A.seed, (uint32_t)slot, A.round, (uint32_t)j, 1u);
+      if (u * qy < py) {
+        if (threadIdx.x == 0) { s_emit[s_ne++] = y; s_a = j; if (y == P.eos) s_stop = 1; }
+        __syncthreads();
+        if (s_stop) break;
+        continue;
+      }
+      // residual (p - q)_+, normalised implicitly by the inverse CDF; p when empty
+      auto resid = [&](int v) {
+        float pv = expf(scaled(zp, v, T, P.suppress) - sp.m) / sp.S;
+        float qv = expf(scaled(zq, v, T, P.suppress) - sq.m) / sq.S;
+        return fmaxf(pv - qv, 0.0f);
+      };
+      float rs = 0.0f;
+      for (int v = threadIdx.x; v < P.V; v += SNT) rs += resid(v);
+      rs = block_sum<SNT>(rs, sh);
+      const float u2 = ws_uniform(A.seed, (uint32_t)slot, A.round, (uint32_t)j, 2u);
+      int tok;
+      if (rs > 0.0f) tok = block_inverse_cdf(resid, P.V, u2, sh);
+      else tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m); }, P.V, u2, sh);
+      if (threadIdx.x == 0) { s_emit[s_ne++] = tok; s_stop = 2; }
+      __syncthreads();
+      break;
+    }
+    __syncthreads();
+    if (s_stop == 0) {   // every candidate accepted: bonus from the target row n_prop
+      const float* zp = A.p_logits + ((long long)i * A.H + n_prop) * P.V;
+      RowStat sp = row_stat(zp, P.V, T, P.suppress, sh);
+      const float u2 = ws_uniform(A.seed, (uint32_t)slot, A.round, (uint32_t)(n_prop + 1), 2u);
+      int tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m); }, P.V, u2, sh);
+      if (threadIdx.x == 0) s_emit[s_ne++] = tok;
+    }
+    __syncthreads();
+  }
+
+  if (threadIdx.x == 0) {
+    const int a = s_a, ne = s_ne;
+    P.L[slot] += 1 + a;                 // rollback by length: keep the anchor + a candidates
+    R -= ne;
+    const int last = s_emit[ne - 1];
+    const bool done = (last == P.eos) || R <= 0;
+    A.budget[i] = R;
+    A.n_acc[i] = a;
+    A.n_emit[i] = ne;
+    A.next_block[(size_t)i * A.next_stride] = last;
+    A.next_len[i] = done ? 0 : 1 + min(P.K, R - 1);
+    if (A.transcript) {
+      int ol = A.out_len[i];
+      for (int k = 0; k < ne; ++k)
+        if (ol < A.tcap) A.transcript[(size_t)i * A.tcap + ol++] = s_emit[k];
+      A.out_len[i] = ol;
+    }
+    if (done) {
+      A.done[i] = 1;
+      if (A.n_done) atomicAdd(A.n_done, 1);
+    }
+  }
+  pdl_trigger();
+}
+
+// ------------------------------------------------------------------ synthetic drafts
+__global__ void draft_synth_kernel(int K, const int32_t* req_ids, const int32_t* L, int32_t* block,
+                                   const int32_t* traj, int tlen, const uint8_t* cmask, const int32_t* ctok,
+                                   int max_pos) {
+  pdl_wait();
+  const int i = blockIdx.x, j = threadIdx.x + 1;
+  if (j > K) return;
+  const int t = min(L[req_ids[i]], max_pos - 1);
+  const size_t c = ((size_t)i * max_pos + t) * K + (j - 1);
+  int tok;
+  if (cmask[c] || t + j >= tlen) tok = ctok[c];
+  else tok = traj[(size_t)i * tlen + t + j];
+  block[(size_t)i * (K + 1) + j] = tok;
+  pdl_trigger();
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+template <typename T>
+cudaError_t launch_embed_target(int n, int H, const RowMap& rm, const int32_t* block, const T* E, const T* P,
+                                int d, int V, float* x, int32_t* pend_start, int32_t* pend_n, int32_t* status,
+                                cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(n * H), dim3(128), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, embed_target_kernel<T>, rm, block, E, P, d, V, x, pend_start, pend_n, status);
+}
+template <typename T>
+cudaError_t launch_embed_draft(int n, int K1, const int32_t* req_ids, const int32_t* block, const T* E, const T* m,
+                               int d, int V, float* x, int32_t* pend_n, int32_t* status, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(n * K1), dim3(128), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, embed_draft_kernel<T>, K1, req_ids, block, E, m, d, V, x, pend_n, status);
+}
+template <typename T>
+cudaError_t launch_layernorm(int M, int d, const float* x, int ldx, const T* g, const T* b, T* y, int ldy,
+                             int group_skip, cudaStream_t s, bool pdl) {
+  if (M <= 0) return cudaSuccess;
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(128), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, layernorm_kernel<T>, d, x, ldx, g, b, y, ldy, group_skip);
+}
+cudaError_t launch_argmax_init(int M, unsigned long long* keys, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3((M + 255) / 256), dim3(256), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, argmax_init_kernel, M, keys);
+}
+cudaError_t launch_argmax_finalize(int n, int H, const int32_t* block_len, const unsigned long long* keys,
+                                   int32_t* out, int out_stride, int out_col0, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3((n * H + 255) / 256), dim3(256), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, argmax_finalize_kernel, n, H, block_len, keys, out, out_stride, out_col0);
+}
+template <typename T>
+cudaError_t launch_hist_gather(int n, int Hp, const int32_t* req_ids, const int32_t* pend_n, const float* hist,
+                               int max_block, int n_hist, int d, T* feat, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(n * Hp), dim3(256), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, hist_gather_kernel<T>, Hp, req_ids, pend_n, hist, max_block, n_hist, d, feat);
+}
+cudaError_t launch_rope_table(float* tab, int max_pos, cudaStream_t s) {
+  int n = max_pos * (WS_DH / 2);
+  rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(tab, max_pos);
+  return cudaGetLastError();
+}
+cudaError_t launch_set_frames(int n, const int32_t* req_ids, const int32_t* cu, const int32_t* valid,
+                              int max_frames, int32_t* Fc, int32_t* Fv, int32_t* status, cudaStream_t s) {
+  set_frames_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, cu, valid, max_frames, Fc, Fv, status);
+  return cudaGetLastError();
+}
+cudaError_t launch_reset(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n, cudaStream_t s) {
+  reset_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, L, pend_n);
+  return cudaGetLastError();
+}
+cudaError_t launch_get_lengths(int n, const int32_t* req_ids, const int32_t* L, int32_t* out, cudaStream_t s) {
+  get_lengths_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, L, out);
+  return cudaGetLastError();
+}
+cudaError_t launch_sample_rows(int n, int rows, const int32_t* req_ids, const float* logits, long long row_stride,
+                               int V, float T, uint64_t seed, uint64_t rnd, const uint32_t* suppress, int32_t* out,
+                               int out_stride, int out_col0, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(n * rows), dim3(SNT), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, sample_rows_kernel, rows, req_ids, logits, row_stride, V, T, seed, rnd,
+                            suppress, out, out_stride, out_col0);
+}
+cudaError_t launch_accept(int n, const AcceptParams& p, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(n), dim3(SNT), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, accept_kernel, p);
+}
+cudaError_t launch_draft_synth(int n, int K, const int32_t* req_ids, const int32_t* L, int32_t* block,
+                               const int32_t* traj, int tlen, const uint8_t* cmask, const int32_t* ctok, int max_pos,
+                               cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(n), dim3(32), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, draft_synth_kernel, K, req_ids, L, block, traj, tlen, cmask, ctok, max_pos);
+}
+
+#define INST(T)                                                                                                     \
+  template cudaError_t launch_embed_target<T>(int, int, const RowMap&, const int32_t*, const T*, const T*, int, int, \
+                                              float*, int32_t*, int32_t*, int32_t*, cudaStream_t, bool);             \
+  template cudaError_t launch_embed_draft<T>(int, int, const int32_t*, const int32_t*, const T*, const T*, int, int, \
+                                             float*, int32_t*, int32_t*, cudaStream_t, bool);                        \
+  template cudaError_t launch_layernorm<T>(int, int, const float*, int, const T*, const T*, T*, int, int,           \
+                                           cudaStream_t, bool);                                                      \
+  template cudaError_t launch_hist_gather<T>(int, int, const int32_t*, const int32_t*, const float*, int, int, int, \
+                                             T*, cudaStream_t, bool);
+INST(float)
+INST(bf16)

@@ -1,0 +1,239 @@
+"""Host driver for libws: device buffers (PyTorch), weight upload and the
+propose / verify / accept loop.  Every step of the decoding path runs in the
+library's CUDA kernels; this module only allocates memory, marshals
+arguments and decides when the loop stops.
+
+Loop (Whisper-Flash §3.1, Appendix A.1):
+  prefill   : ws_verify(prompt) + ws_accept(FORCED) -> first anchor
+  each round: ws_draft (or ws_draft_synthetic) -> ws_verify(K+1 rows)
+              -> ws_accept (greedy or rejection rule) -> next anchor
+  AR greedy : ws_verify(1 row) + ws_accept with no proposals
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import synth
+from . import binding as B
+
+
+def _ptr(t):
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+@dataclass
+class RunStats:
+    rounds: int = 0
+    proposed: int = 0
+    accepted: int = 0
+    emitted: int = 0
+    per_round_acc: list = field(default_factory=list)
+
+
+class Decoder:
+    """One libws context on the current CUDA device."""
+
+    def __init__(self, shape: synth.ModelShape, target: dict, drafter: dict | None, max_batch: int,
+                 max_frames: int = 1500, gemm: int = B.WS_GEMM_AUTO, max_block: int | None = None):
+        if not torch.cuda.is_available():
+            raise RuntimeError("libws needs a CUDA device")
+        self.s = shape
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        self.max_batch = max_batch
+        self.max_frames = max_frames
+        self.K = shape.K
+        self.V = shape.vocab
+        self.dtype = B.WS_BF16 if shape.dtype == "bf16" else B.WS_F32
+        self.tdtype = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+        dl = shape.drafter_layers if drafter is not None else 0
+        self.max_block = max_block or max(shape.K + 1, len(shape.prompt))
+        self.desc = B.make_desc(shape.n_layers, shape.d_model, shape.n_heads, shape.d_ff, shape.vocab,
+                                shape.max_pos, dl, shape.hist_layers, shape.K, self.dtype, max_batch, max_frames,
+                                self.max_block, shape.eos_id, gemm)
+        nbytes = B.ws_query_workspace(self.desc)
+        if nbytes == 0:
+            raise ValueError("invalid model description")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+        tblob = self._blob(target, synth.target_tensor_shapes(shape))
+        dblob = self._blob(drafter, synth.drafter_tensor_shapes(shape)) if dl else None
+        self.ctx = B.ws_load_weights(self.desc, self.workspace.data_ptr(), nbytes, tblob.data_ptr(),
+                                     _ptr(dblob), _stream())
+        del tblob, dblob
+        self.engine = B.ws_gemm_engine(self.ctx)
+
+    def __del__(self):
+        ctx = getattr(self, "ctx", None)
+        if ctx:
+            B.ws_free(ctx)
+            self.ctx = None
+
+    def _blob(self, tensors, order):
+        flat = synth.encode_blob(synth.pack_blob(tensors, order), self.s.dtype)
+        t = torch.from_numpy(flat)
+        if self.s.dtype == "bf16":
+            t = t.view(torch.int16)
+        return t.to(self.dev)
+
+    def enc_tensor(self, A: np.ndarray) -> torch.Tensor:
+        """Encoder states (already in the model's value set) as a device tensor."""
+        if self.s.dtype == "bf16":
+            return torch.from_numpy(synth.bf16_bits(A)).view(torch.int16).to(self.dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(A, dtype=np.float32)).to(self.dev)
+
+    # ------------------------------------------------------------------ raw calls
+    def slots(self, ids) -> torch.Tensor:
+        return torch.as_tensor(np.asarray(ids, dtype=np.int32), device=self.dev)
+
+    def reset(self, req):
+        B.ws_reset(self.ctx, req.numel(), req.data_ptr(), _stream())
+
+    def cross_kv(self, req, enc_packed: torch.Tensor, frames, valid=None):
+        frames = np.asarray(frames, dtype=np.int32)
+        cu = torch.as_tensor(np.concatenate([[0], np.cumsum(frames)]).astype(np.int32), device=self.dev)
+        vt = None if valid is None else torch.as_tensor(np.asarray(valid, dtype=np.int32), device=self.dev)
+        B.ws_cross_kv(self.ctx, req.numel(), req.data_ptr(), enc_packed.data_ptr(), cu.data_ptr(), _ptr(vt),
+                      int(frames.max()), _stream())
+        return cu, vt
+
+    def verify(self, req, block, block_len, target, logits=None):
+        n, H = block.shape
+        B.ws_verify(self.ctx, n, req.data_ptr(), H, block.data_ptr(), block_len.data_ptr(), target.data_ptr(),
+                    _ptr(logits), _stream())
+
+    def draft(self, req, block, temperature=0.0, seed=0, rnd=0, q_logits=None):
+        B.ws_draft(self.ctx, req.numel(), req.data_ptr(), block.data_ptr(), float(temperature), seed, rnd,
+                   _ptr(q_logits), _stream())
+
+    def sample(self, req, logits, temperature, seed, rnd, out):
+        n, rows = out.shape
+        B.ws_sample(self.ctx, n, req.data_ptr(), logits.data_ptr(), rows, float(temperature), seed, rnd,
+                    out.data_ptr(), _stream())
+
+    def lengths(self, req) -> np.ndarray:
+        out = torch.empty(req.numel(), dtype=torch.int32, device=self.dev)
+        B.ws_get_lengths(self.ctx, req.numel(), req.data_ptr(), out.data_ptr(), _stream())
+        return out.cpu().numpy()
+
+    def status(self) -> int:
+        return B.ws_status(self.ctx, _stream())
+
+    # ------------------------------------------------------------------ batch state
+    def new_batch(self, req, budgets, tcap: int | None = None, sampling: bool = False) -> "Batch":
+        return Batch(self, req, budgets, tcap or self.s.max_pos, sampling)
+
+
+class Batch:
+    """Device arrays of one decoding batch (request slots `req`)."""
+
+    def __init__(self, dec: Decoder, req: torch.Tensor, budgets, tcap: int, sampling: bool):
+        self.dec = dec
+        self.req = req
+        n = req.numel()
+        self.n = n
+        dev, K = dec.dev, dec.K
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.block = torch.zeros(n, K + 1, **i32)
+        self.blen = torch.zeros(n, **i32)
+        self.target = torch.zeros(n, K + 1, **i32)
+        self.block1 = torch.zeros(n, 1, **i32)
+        self.target1 = torch.zeros(n, 1, **i32)
+        self.prompt = torch.as_tensor(np.tile(np.asarray(dec.s.prompt, dtype=np.int32), (n, 1)), device=dev)
+        self.plen = torch.full((n,), len(dec.s.prompt), **i32)
+        self.ptarget = torch.zeros(n, len(dec.s.prompt), **i32)
+        self.budget = torch.as_tensor(np.asarray(budgets, dtype=np.int32), device=dev).clone()
+        self.done = torch.zeros(n, **i32)
+        self.n_acc = torch.zeros(n, **i32)
+        self.n_emit = torch.zeros(n, **i32)
+        self.transcript = torch.full((n, tcap), -1, **i32)
+        self.out_len = torch.zeros(n, **i32)
+        self.n_done = torch.zeros(1, **i32)
+        self.tcap = tcap
+        self.acc_sum = torch.zeros(n, dtype=torch.int64, device=dev)
+        self.prop_sum = torch.zeros(n, dtype=torch.int64, device=dev)
+        self.p_logits = self.q_logits = self.p_logits1 = None
+        if sampling:
+            self.p_logits = torch.empty(n, K + 1, dec.V, dtype=torch.float32, device=dev)
+            self.q_logits = torch.empty(n, K, dec.V, dtype=torch.float32, device=dev)
+        self.host_done = torch.zeros(1, dtype=torch.int32).pin_memory()
+
+    def _args(self, mode, H, block, blen, target, next_block, next_len, p_logits=None, q_logits=None,
+              temperature=0.0, seed=0, rnd=0) -> B.AcceptArgs:
+        a = B.AcceptArgs()
+        a.mode, a.H = mode, H
+        a.block, a.block_len, a.target = block.data_ptr(), blen.data_ptr(), _ptr(target)
+        a.p_logits, a.q_logits = _ptr(p_logits), _ptr(q_logits)
+        a.temperature, a.seed, a.round = float(temperature), int(seed), int(rnd)
+        a.budget, a.done, a.n_acc, a.n_emit = (self.budget.data_ptr(), self.done.data_ptr(),
+                                               self.n_acc.data_ptr(), self.n_emit.data_ptr())
+        a.next_block, a.next_stride, a.next_len = next_block.data_ptr(), next_block.shape[1], next_len.data_ptr()
+        a.transcript, a.out_len, a.tcap = self.transcript.data_ptr(), self.out_len.data_ptr(), self.tcap
+        a.n_done = self.n_done.data_ptr()
+        return a
+
+    def prefill(self, ar: bool = False):
+        """Prompt pass: emits the first transcript token (the first anchor)."""
+        d = self.dec
+        d.reset(self.req)
+        d.verify(self.req, self.prompt, self.plen, self.ptarget)
+        nb = self.block1 if ar else self.block
+        a = self._args(B.WS_ACCEPT_FORCED, self.prompt.shape[1], self.prompt, self.plen, self.ptarget, nb,
+                       self.blen)
+        B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
+
+    def ar_step(self):
+        d = self.dec
+        d.verify(self.req, self.block1, self.blen, self.target1)
+        a = self._args(B.WS_ACCEPT_GREEDY, 1, self.block1, self.blen, self.target1, self.block1, self.blen)
+        B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
+
+    def spec_step(self, rnd: int, synthetic=None, temperature: float = 0.0, seed: int = 0, run_drafter=True):
+        """One propose / verify / accept round.  `synthetic` = (traj, tlen, cmask, ctok) device tensors."""
+        d = self.dec
+        sampling = temperature > 0.0
+        if run_drafter:
+            d.draft(self.req, self.block, temperature, seed, rnd, self.q_logits if sampling else None)
+        if synthetic is not None:
+            traj, cmask, ctok = synthetic
+            B.ws_draft_synthetic(d.ctx, self.n, self.req.data_ptr(), self.block.data_ptr(), traj.data_ptr(),
+                                 traj.shape[1], cmask.data_ptr(), ctok.data_ptr(), _stream())
+        d.verify(self.req, self.block, self.blen, self.target, self.p_logits if sampling else None)
+        mode = B.WS_ACCEPT_SAMPLE if sampling else B.WS_ACCEPT_GREEDY
+        a = self._args(mode, d.K + 1, self.block, self.blen, self.target, self.block, self.blen,
+                       self.p_logits, self.q_logits, temperature, seed, rnd)
+        B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
+
+    def poll_done(self) -> int:
+        self.host_done.copy_(self.n_done, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return int(self.host_done.item())
+
+    def transcripts(self):
+        t = self.transcript.cpu().numpy()
+        n = self.out_len.cpu().numpy()
+        return [list(map(int, t[i, :n[i]])) for i in range(self.n)]
+
+
+def run_ar(dec: Decoder, batch: Batch, max_rounds: int = 100000) -> int:
+    batch.prefill(ar=True)
+    rounds = 0
+    while batch.poll_done() < batch.n and rounds < max_rounds:
+        batch.ar_step()
+        rounds += 1
+    return rounds
+
+
+def run_spec(dec: Decoder, batch: Batch, synthetic=None, temperature=0.0, seed=0, max_rounds=100000,
+             run_drafter=True) -> int:
+    batch.prefill()
+    rounds = 0
+    while batch.poll_done() < batch.n and rounds < max_rounds:
+        batch.spec_step(rounds + 1, synthetic, temperature, seed, run_drafter)
+        rounds += 1
+    return rounds

@@ -1,0 +1,45 @@
+"""Shared helpers for the GPU parity tests (CUDA path vs the CPU oracle)."""
+import numpy as np
+import torch
+
+import synth
+from oracle import model as M
+
+MARGIN = 1e-3     # near-tie rule: a token may differ where the oracle's top-2 margin is below this
+
+
+def logits_close(gpu: np.ndarray, ora: np.ndarray, tol: float):
+    """Per row: max |g - o| <= tol * max(max |o|, 1).  Returns the worst ratio."""
+    gpu = np.asarray(gpu, dtype=np.float64).reshape(-1, ora.shape[-1])
+    ora = np.asarray(ora, dtype=np.float64).reshape(-1, ora.shape[-1])
+    worst = 0.0
+    for g, o in zip(gpu, ora):
+        err = np.abs(g - o).max()
+        scale = max(np.abs(o).max(), 1.0)
+        worst = max(worst, err / scale)
+    assert worst <= tol, f"logits differ: {worst:.3e} > {tol:.1e}"
+    return worst
+
+
+def tokens_match(gpu: list, ora: list, margins: list):
+    """Exact token equality, except that at the first difference the oracle's
+    top-2 margin must be below MARGIN (there the comparison stops)."""
+    for i, (g, o) in enumerate(zip(gpu, ora)):
+        if g != o:
+            assert margins[i] < MARGIN, f"token {i}: gpu {g} != oracle {o} with margin {margins[i]:.3e}"
+            return i
+    assert len(gpu) == len(ora), (len(gpu), len(ora))
+    return len(gpu)
+
+
+def small_shape(dtype="f32", **kw):
+    """Multi-tile shape with ragged tails: vocab 1000 is not a multiple of the
+    64-feature GEMM tile, 4 heads, FFN 512."""
+    args = dict(name="small", n_layers=3, d_model=256, n_heads=4, d_ff=512, vocab=1000, max_pos=96,
+                hist_layers=(0, 2), dtype=dtype, eos_id=999, prompt=(990, 991, 992, 993))
+    args.update(kw)
+    return synth.ModelShape(**args)
+
+
+def dev_i32(a, dev="cuda"):
+    return torch.as_tensor(np.asarray(a, dtype=np.int32), device=dev)
