@@ -1,0 +1,361 @@
+"""Benchmark: accepted decoder tokens/s of speculative Whisper decoding.
+
+One step = the whole decoding path over one batch of synthetic requests:
+per-request acoustic K/V (ws_cross_kv), prompt prefill, then propose /
+verify / accept rounds (ws_draft with the two-layer parallel drafter,
+synthetic proposals from the target's own greedy trajectory, ws_verify,
+ws_accept) until every transcript is finished.
+
+Default workload: Whisper-large-v3-shaped decoder, bf16, batch 1, 224-token
+transcripts, K = 8, proposals corrupted independently with p = 0.2.
+Weights are random N(0, 0.02), encoder states N(0, 1) (seeded).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  --impl reference  times the CPU oracle (the reference arm) on a bounded
+                    sample of the same workload.
+Under torchrun (N > 1) every rank decodes its own batch (weak scaling); the
+time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "accepted decoder tokens/s at batch 1/16/96; verify-step HBM GB/s vs peak"
+SEED = 1
+BUDGET = 224
+P_CORRUPT = 0.2
+
+
+def workload(batch: int):
+    return {"workload": f"whisper-large-v3-shaped decoder, bf16, batch {batch}, {BUDGET}-token transcripts, "
+                        f"K=8, 2-layer parallel drafter run + synthetic proposals (p={P_CORRUPT}), "
+                        f"1500-frame encoder states",
+            "global_batch": batch, "seq_len": BUDGET, "K": 8, "frames": 1500,
+            "l2": "no flush: every step streams 1.6 GB of weights + 0.25 GB/request of acoustic K/V (> 129 MB L2)"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+def verify_bytes(s: synth.ModelShape, n_req: int, H: int, L_mean: float, frames: int = 1500) -> float:
+    """Bytes one ws_verify must move at least: every weight once (layers +
+    tied LM head), each request's acoustic K/V for every layer, its self K/V
+    up to the block, plus the logits-free outputs (negligible)."""
+    d, f, nl = s.d_model, s.d_ff, s.n_layers
+    es = 2
+    w_layer = (3 * d * d + d * d + d * d + d * d + d * f + f * d) * es   # w_kvc is only read by ws_cross_kv
+    weights = nl * w_layer + s.vocab * d * es
+    xkv = n_req * nl * 2 * frames * d * es
+    skv = n_req * nl * 2 * (L_mean + H) * d * es
+    return float(weights + xkv + skv)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index: int):
+        self.idx = dev_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, rank: int, world: int):
+    import torch
+    from speculative_whisper_asr_gb300 import binding as B
+    from speculative_whisper_asr_gb300 import runtime as R
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    s = synth.LARGE_V3
+    n = args.batch
+    tw = synth.target_weights(s, SEED)
+    dw = synth.drafter_weights(s, SEED, tw)
+    dec = R.Decoder(s, tw, dw, max_batch=n, max_frames=1500)
+    del tw, dw
+    req = dec.slots(list(range(n)))
+    As = [synth.encoder_states(s, SEED, rank * n + i) for i in range(n)]
+    host_enc = torch.from_numpy(np.concatenate([synth.bf16_bits(a) for a in As])).view(torch.int16)
+    host_enc = host_enc.pin_memory()
+    enc = host_enc.to(dev).view(torch.bfloat16)
+    frames = [1500] * n
+    cu, _ = dec.cross_kv(req, enc, frames)
+
+    # reference trajectory (target's own greedy output), then the corruption plan
+    b_ar = dec.new_batch(req, [BUDGET] * n)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    R.run_ar(dec, b_ar)
+    torch.cuda.synchronize()
+    ar_time = time.perf_counter() - t0
+    ar = b_ar.transcripts()
+    traj = np.full((n, s.max_pos), 0, dtype=np.int32)
+    for i in range(n):
+        t = list(s.prompt) + ar[i]
+        traj[i, :len(t)] = t
+    plan = synth.corruption_plan(n, s.max_pos, s.K, synth.corruption_p_const(s.K, P_CORRUPT), s.vocab,
+                                 SEED + 100 + rank)
+    syn = (torch.as_tensor(traj, device=dev), torch.as_tensor(plan.mask, device=dev),
+           torch.as_tensor(plan.tok, device=dev))
+
+    batch = dec.new_batch(req, [BUDGET] * n)
+    budgets = torch.full((n,), BUDGET, dtype=torch.int32, device=dev)
+    ev_v = []
+
+    def step(record=False, e2e=False):
+        """One pass of the whole path; returns tokens emitted."""
+        if e2e:
+            enc.view(torch.int16).copy_(host_enc, non_blocking=True)
+        B.ws_cross_kv(dec.ctx, n, req.data_ptr(), enc.data_ptr(), cu.data_ptr(), None, 1500, 1500 * n,
+                      stream.cuda_stream)
+        batch.budget.copy_(budgets)
+        batch.done.zero_(); batch.out_len.zero_(); batch.n_done.zero_()
+        batch.prefill()
+        rnd = 0
+        while batch.poll_done() < n:
+            rnd += 1
+            dec.draft(req, batch.block, 0.0, 0, rnd, None)
+            B.ws_draft_synthetic(dec.ctx, n, req.data_ptr(), batch.block.data_ptr(), syn[0].data_ptr(),
+                                 syn[0].shape[1], syn[1].data_ptr(), syn[2].data_ptr(), stream.cuda_stream)
+            if record:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            dec.verify(req, batch.block, batch.blen, batch.target)
+            if record:
+                e1.record(stream)
+                ev_v.append((e0, e1))
+            a = batch._args(B.WS_ACCEPT_GREEDY, s.K + 1, batch.block, batch.blen, batch.target, batch.block,
+                            batch.blen)
+            B.ws_accept(dec.ctx, n, req.data_ptr(), a, stream.cuda_stream)
+        if e2e:
+            out = batch.transcript.to("cpu", non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            _ = out.numpy().sum()
+        return rnd
+
+    for _ in range(args.warmup):
+        step()
+    spec = batch.transcripts()
+    assert spec == ar, "speculative transcript differs from autoregressive"
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- device-resident timed region
+    barrier()
+    torch.cuda.synchronize()
+    l0 = B.ws_launch_count()
+    tstart, tend = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rounds = []
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        tstart.record(stream)
+        for _ in range(args.steps):
+            rounds.append(step(record=True))
+        tend.record(stream)
+        torch.cuda.synchronize()
+    launches = B.ws_launch_count() - l0
+    ms = tstart.elapsed_time(tend)
+    tokens = int(batch.out_len.sum().item()) * args.steps
+    # ---- end to end: host encoder states in, host transcript out
+    barrier()
+    torch.cuda.synchronize()
+    e2s, e2e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2s.record(stream)
+    for _ in range(args.steps):
+        step(e2e=True)
+    e2e_.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e2s.elapsed_time(e2e_)
+
+    vt = [a.elapsed_time(b) for a, b in ev_v]
+    n_ver = len(vt)
+    L_mean = len(s.prompt) + BUDGET / 2.0
+    vbytes = verify_bytes(s, n, s.K + 1, L_mean)
+    hbm, bf16_tf, src = peaks()
+    v_ms = float(np.mean(vt))
+    achieved = vbytes / (v_ms * 1e-3) / 1e9
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+        tt = torch.tensor([tokens], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt)
+        tokens_all = float(tt[0])
+    else:
+        tokens_all = float(tokens)
+    value = tokens_all / (ms * 1e-3)
+    e2e_val = tokens_all / (ms_e2e * 1e-3)
+    emitted_rounds = np.mean(rounds)
+    audio_s = n * 1500 * 0.02 * args.steps * world
+    ar_tps = n * BUDGET / ar_time
+    return {
+        "value": value, "ms_per_step": ms / args.steps, "e2e": e2e_val,
+        "h2d": int(host_enc.numel() * 2), "d2h": int(batch.transcript.numel() * 4),
+        "launches": int(launches),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "kernel": "ws_verify (one block verification, all its kernels)",
+                     "algorithmic_bytes_per_launch": vbytes, "avg_ms": v_ms, "launches_timed": n_ver,
+                     "peak_source": src},
+        "clocks": clk.summary(),
+        "extra": {"rounds_per_step": float(emitted_rounds), "tau": BUDGET / float(emitted_rounds),
+                  "audio_seconds_per_s": audio_s / (ms * 1e-3), "ar_tokens_per_s_untimed_host_loop": ar_tps,
+                  "gemm_engine": dec.engine, "verify_ms": v_ms},
+    }
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+def run_oracle_sample(budget_tokens: int = 12):
+    """The oracle, as it stands, on a bounded sample of the same workload: one
+    request, its own greedy trajectory (untimed, as on the GPU), then the
+    timed speculative decode — acoustic K/V of all 34 layers, prompt prefill,
+    rounds with proposals corrupted from that trajectory (p = 0.2) — until
+    `budget_tokens` are emitted."""
+    from oracle import model as M
+    s = synth.LARGE_V3
+    tw = synth.target_weights(s, SEED)
+    dw = synth.drafter_weights(s, SEED, tw)
+    orc = M.Oracle(s, tw, dw)
+    del tw, dw
+    A = synth.encoder_states(s, SEED, 0)
+    ar = M.greedy_cached(orc, orc.new_request(A), budget_tokens)
+    traj = list(s.prompt) + ar.tokens
+    plan = synth.corruption_plan(1, s.max_pos, s.K, synth.corruption_p_const(s.K, P_CORRUPT), s.vocab, SEED + 100)
+    t0 = time.perf_counter()
+    req = orc.new_request(A)
+    res = M.speculative_greedy(orc, req, budget_tokens, M.corrupted_proposer(traj, plan.mask[0], plan.tok[0]))
+    dt = time.perf_counter() - t0
+    assert res.tokens == ar.tokens
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1)))
+    return len(res.tokens), dt, cores
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals = []
+        run_oracle_sample(2)   # one short warm-up (imports, BLAS threads)
+        total_tok, total_t, cores = 0, 0.0, 1
+        for _ in range(args.steps):
+            tok, dt, cores = run_oracle_sample()
+            total_tok += tok
+            total_t += dt
+            vals.append(tok / dt)
+        v = total_tok / total_t
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload(1),
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": "1 request of the same workload: acoustic K/V of 34 layers + prefill + "
+                                           "speculative rounds until 12 tokens (numpy float64 oracle)"},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    r = run_gpu(args, rank, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok, dt, cores = run_oracle_sample()
+        cpu = {"value": tok / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"1 request of the same workload: acoustic K/V (34 layers) + prefill + speculative "
+                         f"rounds until {tok} tokens, numpy float64 oracle, {dt:.1f} s"}
+    if rank == 0:
+        line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": dict(workload(args.batch), parallelism=f"replicas x{world}"),
+                "e2e": {"value": r["e2e"], "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                        "d2h_bytes_per_step": r["d2h"]},
+                "gpu_launches": r["launches"], "roofline": r["roofline"], "cpu_baseline": cpu,
+                "clocks": r["clocks"], "extra": r["extra"]}
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

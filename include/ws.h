@@ -115,10 +115,12 @@ int ws_reset(ws_ctx* ctx, int n_req, const int32_t* req_ids, ws_stream stream);
  *   valid_frames [n_req] int32 frames that attention may see (<= F_i), or
  *                NULL (= F_i).  Frames at or beyond it are excluded from the
  *                softmax (padding), not zero-filled.
- *   max_frames_call  host int, max_i F_i (sizes the launch; <= max_frames) */
+ *   max_frames_call  host int, max_i F_i (sizes the launch; <= max_frames)
+ *   total_frames     host int, sum_i F_i = rows of `enc` (bounds every read
+ *                    of `enc`; must equal cu_frames[n_req]) */
 int ws_cross_kv(ws_ctx* ctx, int n_req, const int32_t* req_ids, const void* enc,
                 const int32_t* cu_frames, const int32_t* valid_frames,
-                int max_frames_call, ws_stream stream);
+                int max_frames_call, int total_frames, ws_stream stream);
 
 /* Block verification (Whisper-Flash §3.1): one causal target pass over
  * block[i, 0:block_len[i]] at positions L..L+block_len-1 of each request.
@@ -226,6 +228,10 @@ int ws_status(ws_ctx* ctx, ws_stream stream, int32_t* host_status);
 
 /* Name of the GEMM engine in use ("simt" or "tcgen05"). */
 const char* ws_gemm_engine(const ws_ctx* ctx);
+
+/* Number of CUDA kernels this library has launched in the process so far
+ * (all contexts; host-side counter, for instrumentation). */
+unsigned long long ws_launch_count(void);
 
 /* Last error message for ctx (or for the calling thread when ctx is NULL). */
 const char* ws_last_error(const ws_ctx* ctx);

@@ -21,7 +21,7 @@ WS_ACCEPT_GREEDY, WS_ACCEPT_SAMPLE, WS_ACCEPT_FORCED = 0, 1, 2
 
 EXPORTS = ("ws_query_workspace", "ws_load_weights", "ws_reset", "ws_cross_kv", "ws_verify", "ws_draft",
            "ws_accept", "ws_draft_synthetic", "ws_sample", "ws_set_suppress", "ws_get_lengths", "ws_status",
-           "ws_gemm_engine", "ws_last_error", "ws_free")
+           "ws_gemm_engine", "ws_launch_count", "ws_last_error", "ws_free")
 
 
 class WSError(RuntimeError):
@@ -57,7 +57,7 @@ def _load():
         "ws_query_workspace": (C.c_size_t, [C.POINTER(ModelDesc)]),
         "ws_load_weights": (I, [C.POINTER(P), C.POINTER(ModelDesc), P, C.c_size_t, P, P, S]),
         "ws_reset": (I, [P, I, P, S]),
-        "ws_cross_kv": (I, [P, I, P, P, P, P, I, S]),
+        "ws_cross_kv": (I, [P, I, P, P, P, P, I, I, S]),
         "ws_verify": (I, [P, I, P, I, P, P, P, P, S]),
         "ws_draft": (I, [P, I, P, P, F, U64, U64, P, S]),
         "ws_accept": (I, [P, I, P, C.POINTER(AcceptArgs), S]),
@@ -67,6 +67,7 @@ def _load():
         "ws_get_lengths": (I, [P, I, P, P, S]),
         "ws_status": (I, [P, S, C.POINTER(C.c_int32)]),
         "ws_gemm_engine": (C.c_char_p, [P]),
+        "ws_launch_count": (C.c_ulonglong, []),
         "ws_last_error": (C.c_char_p, [P]),
         "ws_free": (None, [P]),
     }
@@ -115,9 +116,9 @@ def ws_reset(ctx, n, req_ids, stream):
     return _check(ctx, lib.ws_reset(ctx, n, req_ids, stream))
 
 
-def ws_cross_kv(ctx, n, req_ids, enc, cu_frames, valid_frames, max_frames_call, stream):
+def ws_cross_kv(ctx, n, req_ids, enc, cu_frames, valid_frames, max_frames_call, total_frames, stream):
     return _check(ctx, lib.ws_cross_kv(ctx, n, req_ids, enc, cu_frames, valid_frames or None, max_frames_call,
-                                       stream))
+                                       total_frames, stream))
 
 
 def ws_verify(ctx, n, req_ids, H, block, block_len, target, logits, stream):
@@ -158,6 +159,10 @@ def ws_status(ctx, stream) -> int:
 
 def ws_gemm_engine(ctx) -> str:
     return lib.ws_gemm_engine(ctx).decode()
+
+
+def ws_launch_count() -> int:
+    return int(lib.ws_launch_count())
 
 
 def ws_last_error(ctx=None) -> str:

@@ -1,15 +1,26 @@
 // C ABI of libws: context, workspace layout and the host-side orchestration
 // of the decoding path (include/ws.h documents every entry point).
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <algorithm>
 #include <vector>
 
 #include "ws_internal.cuh"
 
+// A weight matrix [rows, cols] (row-major, model dtype) and, for the tcgen05
+// engine, its TMA tensor map (128-row boxes).
+struct Mat {
+  const void* p = nullptr;
+  int rows = 0, cols = 0;
+  TcMap map;
+};
+
 struct LayerW {
-  const void *w_qkv, *w_o, *w_qc, *w_kvc, *w_oc, *w_fc1, *w_fc2;
+  Mat w_qkv, w_o, w_qc, w_kvc, w_oc, w_fc1, w_fc2;
+  Mat w_kvrows;                 // rows k|v of w_qkv (drafter history projections)
   const void *b_q, *b_v, *b_o, *b_qc, *b_vc, *b_oc, *b_fc1, *b_fc2;
   const void *ln1_g, *ln1_b, *ln2_g, *ln2_b, *ln3_g, *ln3_b;
 };
@@ -21,7 +32,8 @@ struct ws_ctx {
   char* ws = nullptr;
   size_t ws_bytes = 0;
   const void *tok_emb = nullptr, *pos_emb = nullptr, *lnf_g = nullptr, *lnf_b = nullptr;
-  const void *fuse_w = nullptr, *lnh_g = nullptr, *lnh_b = nullptr, *mask_emb = nullptr;
+  Mat head, fuse_w;              // tied LM head (= tok_emb), fusion projection
+  const void *lnh_g = nullptr, *lnh_b = nullptr, *mask_emb = nullptr;
   const void *dlnf_g = nullptr, *dlnf_b = nullptr;
   std::vector<LayerW> tl, dl;
   char* kv = nullptr;  size_t kv_layer_bytes = 0;     // target self KV pool
@@ -40,10 +52,16 @@ struct ws_ctx {
   int max_fc = 0;
   const uint32_t* suppress = nullptr;
   int engine = WS_GEMM_SIMT;
+  bool split_ok = false;        // split-K allowed (small-batch contexts)
+  int mrows = 0;                // rows of the activation buffers
+  TcScratch tcs{};
   bool pdl = true;              // programmatic dependent launch allowed
   bool cur_pdl = false;         // PDL for the call in progress (never on the legacy stream)
   std::string err;
 };
+
+static std::atomic<unsigned long long> g_launches{0};
+void ws_count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 namespace {
 
@@ -89,6 +107,7 @@ struct Layout {
 
 struct Plan {
   size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
+  size_t tc_part, tc_cnt, tc_part_elems, tc_cnt_n;
   size_t kv_layer_bytes, total;
   int heads, ppr, n_pages, n_xl, max_split;
 };
@@ -151,6 +170,13 @@ Plan make_plan(const ws_model_desc& d) {
   p.feat = lay.take(M * nh * D * es);
   p.hpre = lay.take(M * D * 4);
   p.hh = lay.take(M * D * es);
+  // split-K partials of the tcgen05 engine (small-batch contexts only):
+  // tiles(<= ceil(max N / 128)) x splits(<= 16) x BN(<= 64) x 128 fp32
+  const size_t maxN = std::max<size_t>(std::max<size_t>(3 * D, d.d_ff), 2 * D);
+  p.tc_cnt_n = (maxN + 127) / 128 + 64;
+  p.tc_part_elems = (M <= 64) ? p.tc_cnt_n * 16 * 64 * 128 : 0;
+  p.tc_part = lay.take(p.tc_part_elems * 4);
+  p.tc_cnt = lay.take(p.tc_cnt_n * 4);
   p.total = lay.off;
   return p;
 }
@@ -158,8 +184,10 @@ Plan make_plan(const ws_model_desc& d) {
 void bind_layer(LayerW& w, const char*& p, const ws_model_desc& d, size_t es) {
   const size_t D = d.d_model, F = d.d_ff;
   auto take = [&](size_t n) { const void* r = p; p += n * es; return r; };
-  w.w_qkv = take(3 * D * D); w.w_o = take(D * D); w.w_qc = take(D * D); w.w_kvc = take(2 * D * D);
-  w.w_oc = take(D * D); w.w_fc1 = take(F * D); w.w_fc2 = take(D * F);
+  auto mat = [&](Mat& m, size_t rows, size_t cols) { m.p = take(rows * cols); m.rows = (int)rows; m.cols = (int)cols; };
+  mat(w.w_qkv, 3 * D, D); mat(w.w_o, D, D); mat(w.w_qc, D, D); mat(w.w_kvc, 2 * D, D);
+  mat(w.w_oc, D, D); mat(w.w_fc1, F, D); mat(w.w_fc2, D, F);
+  w.w_kvrows.p = (const char*)w.w_qkv.p + D * D * es; w.w_kvrows.rows = (int)(2 * D); w.w_kvrows.cols = (int)D;
   w.b_q = take(D); w.b_v = take(D); w.b_o = take(D); w.b_qc = take(D); w.b_vc = take(D); w.b_oc = take(D);
   w.b_fc1 = take(F); w.b_fc2 = take(D);
   w.ln1_g = take(D); w.ln1_b = take(D); w.ln2_g = take(D); w.ln2_b = take(D); w.ln3_g = take(D); w.ln3_b = take(D);
@@ -196,11 +224,25 @@ Epi epi0(ws_ctx* c, int kind) {
   return e;
 }
 
+// Split-K factor of a weight shape: a function of (N, K) and the context only,
+// never of the token count, so every row is reduced in the same order.
+int splits_for(const ws_ctx* c, int N, int K) {
+  if (!c->split_ok) return 1;
+  const int tiles = (N + 127) / 128, kb = K / 64;
+  if (tiles >= 100) return 1;
+  int s = (148 + tiles - 1) / tiles;
+  s = std::min(s, std::max(1, kb / 2));
+  return std::max(1, std::min(s, 16));
+}
+
+// Y = X W^T with a fused epilogue.  X has x_rows allocated rows.
 template <typename T>
-cudaError_t gemm(ws_ctx* c, const void* X, int ldx, const void* W, int M, int N, int K, const Epi& e,
-                 cudaStream_t s, int batch = 1) {
+cudaError_t gemm(ws_ctx* c, const void* X, uint64_t x_rows, const Mat& W, int M, const Epi& e, cudaStream_t s,
+                 int batch = 1, bool allow_split = true) {
   GemmShape g;
-  g.X = X; g.ldx = ldx; g.W = W; g.ldw = K; g.M = M; g.N = N; g.K = K; g.batch = batch;
+  g.X = X; g.ldx = W.cols; g.W = W.p; g.ldw = W.cols; g.M = M; g.N = W.rows; g.K = W.cols; g.batch = batch;
+  if (c->engine == WS_GEMM_TC && sizeof(T) == 2)
+    return launch_gemm_tc(g, e, W.map, X, x_rows, allow_split ? splits_for(c, g.N, g.K) : 1, c->tcs, s, c->cur_pdl);
   return launch_gemm_simt<T>(g, e, s, c->cur_pdl);
 }
 
@@ -236,37 +278,37 @@ int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* bloc
     CK(layernorm<T>(c, M, c->x, w.ln1_g, w.ln1_b, c->h, s));
     Epi e = epi0(c, EPI_QKV);
     e.bias = w.b_q; e.bias2 = w.b_v; e.out = c->q; e.rm = rm; e.kv = pool(c, c->kv, l);
-    CK(gemm<T>(c, c->h, D, w.w_qkv, M, 3 * D, D, e, s));
+    CK(gemm<T>(c, c->h, c->mrows, w.w_qkv, M, e, s));
     CK(launch_self_attn<T>(n, H, rm, (const T*)c->q, pool(c, c->kv, l), (T*)c->ao, c->heads, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_o; e.resid = c->x; e.ldr = D;
-    CK(gemm<T>(c, c->ao, D, w.w_o, M, D, D, e, s));
+    CK(gemm<T>(c, c->ao, c->mrows, w.w_o, M, e, s));
     CK(layernorm<T>(c, M, c->x, w.ln2_g, w.ln2_b, c->h, s));
     e = epi0(c, EPI_STORE);
     e.bias = w.b_qc; e.out = c->q; e.ldo = D;
-    CK(gemm<T>(c, c->h, D, w.w_qc, M, D, D, e, s));
+    CK(gemm<T>(c, c->h, c->mrows, w.w_qc, M, e, s));
     CK(launch_cross_attn<T>(n, H, req, c->Fv, (const T*)c->q, xkv_of(c), l, c->part, (T*)c->ao, c->heads, n_split,
                             s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_oc; e.resid = c->x; e.ldr = D;
-    CK(gemm<T>(c, c->ao, D, w.w_oc, M, D, D, e, s));
+    CK(gemm<T>(c, c->ao, c->mrows, w.w_oc, M, e, s));
     CK(layernorm<T>(c, M, c->x, w.ln3_g, w.ln3_b, c->h, s));
     e = epi0(c, EPI_GELU);
     e.bias = w.b_fc1; e.out = c->ffn; e.ldo = d.d_ff;
-    CK(gemm<T>(c, c->h, D, w.w_fc1, M, d.d_ff, D, e, s));
+    CK(gemm<T>(c, c->h, c->mrows, w.w_fc1, M, e, s));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_fc2; e.resid = c->x; e.ldr = D;
     int hidx;
     if (is_hist_layer(d, l, hidx)) {
       e.hist = c->hist; e.hist_idx = hidx; e.n_hist = d.n_hist; e.rm = rm;
     }
-    CK(gemm<T>(c, c->ffn, d.d_ff, w.w_fc2, M, D, d.d_ff, e, s));
+    CK(gemm<T>(c, c->ffn, c->mrows, w.w_fc2, M, e, s));
   }
   CK(layernorm<T>(c, M, c->x, c->lnf_g, c->lnf_b, c->h, s));
   CK(launch_argmax_init(M, c->amax, s, pdl));
   Epi e = epi0(c, EPI_LOGITS);
   e.logits = logits; e.ldl = d.vocab; e.amax = c->amax;
-  CK(gemm<T>(c, c->h, D, c->tok_emb, M, d.vocab, D, e, s));
+  CK(gemm<T>(c, c->h, c->mrows, c->head, M, e, s));
   CK(launch_argmax_finalize(n, H, blen, c->amax, target, H, 0, s, pdl));
   if (d.drafter_layers > 0) c->pending_H = H > c->pending_H ? H : c->pending_H;
   return WS_OK;
@@ -282,11 +324,11 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
   // 1) fold the rows of the last verify into the drafter history
   const int Hp = c->pending_H;
   if (Hp > 0) {
-    const int Mh = n * Hp, W = d.n_hist * D;
+    const int Mh = n * Hp;
     CK(launch_hist_gather<T>(n, Hp, req, c->pend_n, c->hist, d.max_block, d.n_hist, D, (T*)c->feat, s, pdl));
     Epi e = epi0(c, EPI_F32);
     e.out = c->hpre; e.ldo = D;
-    CK(gemm<T>(c, c->feat, W, c->fuse_w, Mh, D, W, e, s));
+    CK(gemm<T>(c, c->feat, c->mrows, c->fuse_w, Mh, e, s));
     CK(layernorm<T>(c, Mh, c->hpre, c->lnh_g, c->lnh_b, c->hh, s));
     RowMap rh;
     rh.mode = ROW_HIST; rh.H = Hp; rh.max_pos = d.max_pos; rh.req_ids = req; rh.L = c->L;
@@ -295,8 +337,7 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
       const LayerW& w = c->dl[l];
       Epi eh = epi0(c, EPI_HISTKV);
       eh.bias2 = w.b_v; eh.rm = rh; eh.kv = pool(c, c->hkv, l);
-      const char* wkv = (const char*)w.w_qkv + (size_t)D * D * c->es;   // rows k | v of w_qkv
-      CK(gemm<T>(c, c->hh, D, wkv, Mh, 2 * D, D, eh, s));
+      CK(gemm<T>(c, c->hh, c->mrows, w.w_kvrows, Mh, eh, s));
     }
   }
   // 2) the block X_t = [Emb(anchor), m, ..., m] through the drafter layers
@@ -312,28 +353,28 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
     CK(layernorm<T>(c, M, c->x, w.ln1_g, w.ln1_b, c->h, s));
     Epi e = epi0(c, EPI_QKV_DRAFT);
     e.bias = w.b_q; e.bias2 = w.b_v; e.out = c->q; e.kout = c->kb; e.vout = c->vb; e.rm = rd;
-    CK(gemm<T>(c, c->h, D, w.w_qkv, M, 3 * D, D, e, s));
+    CK(gemm<T>(c, c->h, c->mrows, w.w_qkv, M, e, s));
     CK(launch_draft_attn<T>(n, K1, req, c->L, (const T*)c->q, (const T*)c->kb, (const T*)c->vb,
                             pool(c, c->hkv, l), (T*)c->ao, c->heads, d.max_pos, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_o; e.resid = c->x; e.ldr = D;
-    CK(gemm<T>(c, c->ao, D, w.w_o, M, D, D, e, s));
+    CK(gemm<T>(c, c->ao, c->mrows, w.w_o, M, e, s));
     CK(layernorm<T>(c, M, c->x, w.ln2_g, w.ln2_b, c->h, s));
     e = epi0(c, EPI_STORE);
     e.bias = w.b_qc; e.out = c->q; e.ldo = D;
-    CK(gemm<T>(c, c->h, D, w.w_qc, M, D, D, e, s));
+    CK(gemm<T>(c, c->h, c->mrows, w.w_qc, M, e, s));
     CK(launch_cross_attn<T>(n, K1, req, c->Fv, (const T*)c->q, xkv_of(c), d.n_layers + l, c->part, (T*)c->ao,
                             c->heads, n_split, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_oc; e.resid = c->x; e.ldr = D;
-    CK(gemm<T>(c, c->ao, D, w.w_oc, M, D, D, e, s));
+    CK(gemm<T>(c, c->ao, c->mrows, w.w_oc, M, e, s));
     CK(layernorm<T>(c, M, c->x, w.ln3_g, w.ln3_b, c->h, s));
     e = epi0(c, EPI_GELU);
     e.bias = w.b_fc1; e.out = c->ffn; e.ldo = d.d_ff;
-    CK(gemm<T>(c, c->h, D, w.w_fc1, M, d.d_ff, D, e, s));
+    CK(gemm<T>(c, c->h, c->mrows, w.w_fc1, M, e, s));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_fc2; e.resid = c->x; e.ldr = D;
-    CK(gemm<T>(c, c->ffn, d.d_ff, w.w_fc2, M, D, d.d_ff, e, s));
+    CK(gemm<T>(c, c->ffn, c->mrows, w.w_fc2, M, e, s));
   }
   // 3) final LN on the K mask rows, shared LM head, argmax or sampling
   const int Mk = n * K;
@@ -343,10 +384,10 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
   if (temp <= 0.0f) {
     CK(launch_argmax_init(Mk, c->amax, s, pdl));
     e.amax = c->amax;
-    CK(gemm<T>(c, c->h, D, c->tok_emb, Mk, d.vocab, D, e, s));
+    CK(gemm<T>(c, c->h, c->mrows, c->head, Mk, e, s));
     CK(launch_argmax_finalize(n, K, nullptr, c->amax, block, K1, 1, s, pdl));
   } else {
-    CK(gemm<T>(c, c->h, D, c->tok_emb, Mk, d.vocab, D, e, s));
+    CK(gemm<T>(c, c->h, c->mrows, c->head, Mk, e, s));
     CK(launch_sample_rows(n, K, req, q_logits, d.vocab, d.vocab, temp, seed, rnd, c->suppress, block, K1, 1, s,
                           pdl));
   }
@@ -356,7 +397,7 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
 // --------------------------------------------------------------------------- cross K/V
 template <typename T>
 int cross_kv_impl(ws_ctx* c, int n, const int32_t* req, const void* enc, const int32_t* cu, const int32_t* valid,
-                  int maxF, cudaStream_t s) {
+                  int maxF, int total_frames, cudaStream_t s) {
   const ws_model_desc& d = c->d;
   const int D = d.d_model;
   CK(launch_set_frames(n, req, cu, valid, d.max_frames, c->Fc, c->Fv, c->status, s));
@@ -364,7 +405,7 @@ int cross_kv_impl(ws_ctx* c, int n, const int32_t* req, const void* enc, const i
     const LayerW& w = l < d.n_layers ? c->tl[l] : c->dl[l - d.n_layers];
     Epi e = epi0(c, EPI_CROSSKV);
     e.bias2 = w.b_vc; e.xkv = xkv_of(c); e.xlayer = l; e.cu_frames = cu; e.req_ids = req;
-    CK(gemm<T>(c, enc, D, w.w_kvc, maxF, 2 * D, D, e, s, n));
+    CK(gemm<T>(c, enc, (uint64_t)total_frames, w.w_kvc, maxF, e, s, n, false));
   }
   if (maxF > c->max_fc) c->max_fc = maxF;
   return WS_OK;
@@ -423,6 +464,7 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   const char* tp = b + p.tblob;
   const size_t D = desc->d_model;
   c->tok_emb = tp; tp += (size_t)desc->vocab * D * c->es;
+  c->head.p = c->tok_emb; c->head.rows = desc->vocab; c->head.cols = (int)D;
   c->pos_emb = tp; tp += (size_t)desc->max_pos * D * c->es;
   c->tl.resize(desc->n_layers);
   for (auto& w : c->tl) bind_layer(w, tp, *desc, c->es);
@@ -430,7 +472,8 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   c->lnf_b = tp;
   if (desc->drafter_layers > 0) {
     const char* dp = b + p.dblob;
-    c->fuse_w = dp; dp += D * desc->n_hist * D * c->es;
+    c->fuse_w.p = dp; c->fuse_w.rows = (int)D; c->fuse_w.cols = (int)(desc->n_hist * D);
+    dp += D * desc->n_hist * D * c->es;
     c->lnh_g = dp; dp += D * c->es;
     c->lnh_b = dp; dp += D * c->es;
     c->mask_emb = dp; dp += D * c->es;
@@ -454,6 +497,22 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   c->kb = b + p.kb; c->vb = b + p.vb; c->hist = (float*)(b + p.hist);
   c->amax = (unsigned long long*)(b + p.amax); c->part = (float*)(b + p.part);
   c->feat = b + p.feat; c->hpre = (float*)(b + p.hpre); c->hh = b + p.hh;
+  c->mrows = desc->max_batch * desc->max_block;
+  c->split_ok = c->mrows <= 64;
+  c->tcs.part = (float*)(b + p.tc_part); c->tcs.part_elems = p.tc_part_elems;
+  c->tcs.counters = (int*)(b + p.tc_cnt); c->tcs.counters_n = (int)p.tc_cnt_n;
+  if (c->engine == WS_GEMM_TC) {
+    bool ok = true;
+    auto enc = [&](Mat& m) { ok = ok && tc_encode_map(&m.map, m.p, (uint64_t)m.rows, (uint64_t)m.cols, 128); };
+    for (auto* L : {&c->tl, &c->dl})
+      for (auto& w : *L) {
+        enc(w.w_qkv); enc(w.w_o); enc(w.w_qc); enc(w.w_kvc); enc(w.w_oc); enc(w.w_fc1); enc(w.w_fc2);
+        enc(w.w_kvrows);
+      }
+    enc(c->head);
+    if (desc->drafter_layers > 0) enc(c->fuse_w);
+    if (!ok) { fail(nullptr, WS_ECUDA, "TMA descriptor encoding failed"); return cleanup(WS_ECUDA); }
+  }
 
   std::vector<int32_t> pt(p.n_pages);
   for (int i = 0; i < p.n_pages; ++i) pt[i] = i;   // each slot owns its own pages
@@ -461,6 +520,7 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   if (e == cudaSuccess) e = cudaMemsetAsync(st, 0, (size_t)desc->max_batch * 5 * 4 + 256, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->hist, 0, (size_t)desc->max_batch * desc->max_block *
                                                         (desc->drafter_layers ? desc->n_hist : 0) * D * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->tcs.counters, 0, (size_t)c->tcs.counters_n * 4, s);
   if (e == cudaSuccess) e = launch_rope_table(c->rope, desc->max_pos, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) { fail(nullptr, WS_ECUDA, "context init: %s", cudaGetErrorString(e)); return cleanup(WS_ECUDA); }
@@ -476,14 +536,16 @@ int ws_reset(ws_ctx* c, int n, const int32_t* req, ws_stream stream) {
 }
 
 int ws_cross_kv(ws_ctx* c, int n, const int32_t* req, const void* enc, const int32_t* cu, const int32_t* valid,
-                int maxF, ws_stream stream) {
+                int maxF, int total_frames, ws_stream stream) {
   if (int r = check_common(c, n, req, stream)) return r;
   if (n == 0) return WS_OK;
   if (!enc || !cu) return fail(c, WS_EINVAL, "null encoder states or cu_frames");
   if (maxF < 1 || maxF > c->d.max_frames) return fail(c, WS_EINVAL, "max_frames_call %d outside 1..%d", maxF, c->d.max_frames);
+  if (total_frames < maxF || (int64_t)total_frames > (int64_t)n * maxF)
+    return fail(c, WS_EINVAL, "total_frames %d inconsistent with n_req * max_frames_call", total_frames);
   cudaStream_t s = (cudaStream_t)stream;
-  return c->d.dtype == WS_BF16 ? cross_kv_impl<bf16>(c, n, req, enc, cu, valid, maxF, s)
-                               : cross_kv_impl<float>(c, n, req, enc, cu, valid, maxF, s);
+  return c->d.dtype == WS_BF16 ? cross_kv_impl<bf16>(c, n, req, enc, cu, valid, maxF, total_frames, s)
+                               : cross_kv_impl<float>(c, n, req, enc, cu, valid, maxF, total_frames, s);
 }
 
 int ws_verify(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* block, const int32_t* blen,
@@ -591,6 +653,8 @@ const char* ws_gemm_engine(const ws_ctx* c) {
   if (!c) return "none";
   return c->engine == WS_GEMM_TC ? "tcgen05" : "simt";
 }
+
+unsigned long long ws_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* ws_last_error(const ws_ctx* c) { return c ? c->err.c_str() : g_err.c_str(); }
 

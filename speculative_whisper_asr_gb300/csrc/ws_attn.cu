@@ -261,6 +261,7 @@ cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const K
   if (H > MAXR) return cudaErrorInvalidValue;
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n, n_heads), dim3(NW * 32), s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, self_attn_kernel<T>, rm, Q, kv, O, n_heads * WS_DH);
 }
 
@@ -270,11 +271,13 @@ cudaError_t launch_cross_attn(int n, int H, const int32_t* req_ids, const int32_
   if (H > MAXR) return cudaErrorInvalidValue;
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n, n_heads, n_split), dim3(NW * 32), s, pdl, at);
+  ws_count_launches(1);
   cudaError_t e = cudaLaunchKernelEx(&cfg, cross_attn_part_kernel<T>, H, req_ids, Fv, Q, x, layer, part,
                                      n_heads * WS_DH, n_split);
   if (e != cudaSuccess) return e;
   const int rows = n * H;
   cudaLaunchConfig_t cfg2 = make_cfg(dim3((rows * n_heads + 3) / 4), dim3(128), s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg2, cross_attn_combine_kernel<T>, rows, (const float*)part, O, n_heads * WS_DH,
                             n_split);
 }
@@ -286,6 +289,7 @@ cudaError_t launch_draft_attn(int n, int K1, const int32_t* req_ids, const int32
   if (K1 > MAXR) return cudaErrorInvalidValue;
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n, n_heads), dim3(NW * 32), s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, draft_attn_kernel<T>, K1, req_ids, L, Q, Kb, Vb, hkv, O, n_heads * WS_DH,
                             max_pos);
 }

@@ -116,6 +116,7 @@ cudaError_t launch_bt(const GemmShape& g, const Epi& e, cudaStream_t s, bool pdl
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, gemm_simt_kernel<T, BT>, g, e);
 }
 

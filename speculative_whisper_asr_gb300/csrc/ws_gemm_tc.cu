@@ -1,4 +1,420 @@
-// tcgen05 GEMM engine (Blackwell tensor cores, TMEM accumulators, TMA).
-#include "ws_internal.cuh"
+// tcgen05 GEMM engine for the bf16 model: Y[token, feature] = X[token, :] . W[feature, :]
+//
+// Blackwell datapath, written with inline PTX:
+//   * TMA (cp.async.bulk.tensor.2d, 128-byte swizzle) streams 128x64 weight
+//     tiles and BNx64 activation tiles into a shared-memory ring, completing
+//     on mbarriers;
+//   * one elected thread issues tcgen05.mma.cta_group::1.kind::f16 (M = 128
+//     weight rows, N = BN tokens, K = 16 per instruction) with fp32
+//     accumulators in tensor memory (TMEM), and releases each ring slot with
+//     tcgen05.commit;
+//   * four warps read the accumulator back with tcgen05.ld and run the shared
+//     epilogue (bias, GELU, residual, KV-cache scatter, RoPE, logits/argmax).
+// Weights are the 128-row A operand ("swap AB"), so a decode step with a
+// handful of tokens still fills the MMA M dimension and each token is one
+// column: every output element accumulates its k-blocks in the same order
+// whatever the number of tokens.  Split-K (fixed per weight shape, never per
+// token count) spreads small-M GEMMs over the SMs; the last CTA of a tile
+// adds the fp32 partials in split order.
+//
+// The weight TMA loads of the first ring slots are issued before
+// griddepcontrol.wait, so under programmatic dependent launch they overlap the
+// previous kernel's tail.  Every mbarrier wait is bounded (clock budget); a
+// timeout sets a device status bit instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
-bool tc_engine_available() { return false; }
+#include <mutex>
+
+#include "ws_epilogue.cuh"
+
+namespace {
+
+constexpr int BM = 128;                 // weight rows per tile (MMA M)
+constexpr int BK = 64;                  // k per ring slot (one 128-byte swizzle atom of bf16)
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr long long WAIT_BUDGET = 1ll << 32;   // clock cycles (~2 s) before a wait gives up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a phase parity; false when the budget ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > WAIT_BUDGET) return false;
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row core groups 1024 bytes apart (SBO), sm_100 descriptor version.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;                  // leading byte offset (unused with this swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset
+  d |= (uint64_t)1 << 46;                  // version
+  d |= (uint64_t)2 << 61;                  // SWIZZLE_128B
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+      ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns: thread = lane, v[i] = column i.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct TcParams {
+  int M, N, K;           // tokens, weight rows (features), reduction
+  int kb_total;          // K / BK
+  int splits;            // split-K factor (grid.x = tiles_f * splits)
+  int tiles_f, tiles_t;
+  float* part;           // [tile][split][BN][BM] partial sums (splits > 1)
+  int* counters;         // [tile] arrival counters, left at zero
+  int32_t* status;
+};
+
+// Epilogue for one column block of 16 tokens held as v[16] (feature = this thread's row).
+template <int BN>
+__device__ __forceinline__ void epilogue16(const Epi& e, const TcParams& p, int t0, int c0, int n, int M, int z,
+                                          const float* v) {
+  const int lane = threadIdx.x & 31;
+  if (e.kind == EPI_LOGITS) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int t = t0 + c0 + c;
+      unsigned long long key = 0ull;
+      if (t < M && n < p.N) {
+        const float y = epi_logit(e, n, v[c]);
+        if (e.logits) e.logits[(long long)t * e.ldl + n] = y;
+        key = argmax_key(y, n);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+        key = other > key ? other : key;
+      }
+      if (lane == 0 && key != 0ull && e.amax) atomicMax(e.amax + t, key);
+    }
+    return;
+  }
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    const float pc0 = __shfl_xor_sync(0xffffffffu, v[c], 1);
+    const float pc1 = __shfl_xor_sync(0xffffffffu, v[c + 1], 1);
+    if ((lane & 1) == 0) {
+      const int t = t0 + c0 + c;
+      if (t < M && n + 1 < p.N) epi_pair<bf16>(e, t, n, v[c], pc0, z);
+    } else {
+      const int t = t0 + c0 + c + 1;
+      if (t < M && n < p.N) epi_pair<bf16>(e, t, n - 1, pc1, v[c + 1], z);
+    }
+  }
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(128, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcParams p,
+                   Epi e) {
+  constexpr int B_BYTES = BN * BK * 2;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_abort, s_last;
+
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_f = blockIdx.x / p.splits, split = blockIdx.x - tile_f * p.splits;
+  const int f0 = tile_f * BM, t0 = blockIdx.y * BN, z = blockIdx.z;
+  const int kb0 = (int)((long long)split * p.kb_total / p.splits);
+  const int kb1 = (int)((long long)(split + 1) * p.kb_total / p.splits);
+  const int nkb = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    mbar_init(&done, 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc(&tmem_base, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  // Row count: a host value, except for the acoustic K/V GEMM whose per-request
+  // frame ranges live in device memory (read only after the dependency wait).
+  int M = p.M, row0 = 0;
+  const bool early = e.kind != EPI_CROSSKV;
+  if (!early) {
+    pdl_wait();
+    row0 = e.cu_frames[z];
+    M = min(e.cu_frames[z + 1] - row0, e.xkv.max_frames);
+  }
+  const bool active = t0 < M && nkb > 0;
+  // ---- weights of the first ring slots: independent of the previous kernel
+  const int npre = active ? (nkb < STAGES ? nkb : STAGES) : 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < npre; ++i) {
+      mbar_expect_tx(&full[i], STAGE_BYTES);
+      tma_load_2d(ring + i * STAGE_BYTES, &tmW, &full[i], (kb0 + i) * BK, f0);
+    }
+  }
+  if (early) pdl_wait();
+
+  if (threadIdx.x == 0 && active) {
+    // ---- producer
+    for (int i = 0; i < npre; ++i)
+      tma_load_2d(ring + i * STAGE_BYTES + A_BYTES, &tmX, &full[i], (kb0 + i) * BK, row0 + t0);
+    for (int i = npre; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (uint32_t)((i / STAGES) & 1);
+      if (!mbar_wait(&empty[s], ph ^ 1u)) { s_abort = 1; atomicOr(p.status, 8); break; }
+      mbar_expect_tx(&full[s], STAGE_BYTES);
+      uint8_t* st = ring + s * STAGE_BYTES;
+      tma_load_2d(st, &tmW, &full[s], (kb0 + i) * BK, f0);
+      tma_load_2d(st + A_BYTES, &tmX, &full[s], (kb0 + i) * BK, row0 + t0);
+    }
+  }
+  if (warp == 1 && lane == 0 && active) {
+    // ---- MMA issuer
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (uint32_t)((i / STAGES) & 1);
+      if (!mbar_wait(&full[s], ph)) { s_abort = 1; atomicOr(p.status, 8); break; }
+      tc_fence_after();
+      const uint32_t a = smem_u32(ring + s * STAGE_BYTES), b = a + A_BYTES;
+      const uint64_t ad = sdesc_sw128(a), bd = sdesc_sw128(b);
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        umma_bf16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), IDESC, (i | kk) != 0 ? 1u : 0u);
+      umma_commit(&empty[s]);
+    }
+    umma_commit(&done);
+  }
+  __syncwarp();
+
+  bool ok = true;
+  if (active) {
+    ok = mbar_wait(&done, 0);
+    if (!ok) atomicOr(p.status, 8);
+  }
+  ok = __syncthreads_and(ok) != 0;      // CTA-uniform before any further barrier
+  tc_fence_after();
+  pdl_trigger();
+
+  if (active && ok) {
+    const int row = warp * 32 + lane;          // TMEM lane == weight row of the tile
+    const int n = f0 + row;
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    if (p.splits == 1) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)c0, v);
+        epilogue16<BN>(e, p, t0, c0, n, M, z, v);
+      }
+    } else {
+      const int tile = (z * p.tiles_t + blockIdx.y) * p.tiles_f + tile_f;
+      float* mine = p.part + ((size_t)tile * p.splits + split) * BN * BM;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) mine[(size_t)(c0 + c) * BM + row] = v[c];
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const int old = atomicAdd(p.counters + tile, 1);
+        s_last = old == p.splits - 1;
+        if (s_last) p.counters[tile] = 0;
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        const float* base = p.part + (size_t)tile * p.splits * BN * BM;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            float acc = 0.0f;
+            for (int s = 0; s < p.splits; ++s) acc += __ldcg(base + ((size_t)s * BN + c0 + c) * BM + row);
+            v[c] = acc;
+          }
+          epilogue16<BN>(e, p, t0, c0, n, M, z, v);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+
+template <int BN, int STAGES>
+cudaError_t launch_bn(const GemmShape& g, const Epi& e, const CUtensorMap& mw, const CUtensorMap& mx,
+                      const TcParams& p, cudaStream_t s, bool pdl) {
+  constexpr int smem = STAGES * (A_BYTES + BN * BK * 2) + 1024;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t r = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem);
+    if (r != cudaSuccess) return r;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.tiles_f * p.splits, p.tiles_t, g.batch > 0 ? g.batch : 1);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES>, mw, mx, p, e);
+}
+
+}  // namespace
+
+bool tc_engine_available() {
+  std::call_once(g_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// Row-major bf16 matrix [rows, cols] as a TMA tensor map with 64-column x
+// box_rows boxes and 128-byte swizzle.  Returns false when the encoder
+// rejects it (alignment, sizes).
+bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  if (!tc_engine_available()) return false;
+  static_assert(sizeof(TcMap) >= sizeof(CUtensorMap), "TcMap too small");
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(reinterpret_cast<CUtensorMap*>(m), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int tc_pick_bn(int M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const void* x_base, uint64_t x_rows,
+                           int splits, const TcScratch& scr, cudaStream_t s, bool pdl) {
+  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  if (g.K % BK != 0 || g.ldx != g.K) return cudaErrorInvalidValue;
+  const int BN = tc_pick_bn(g.M);
+  TcMap mx;
+  if (!tc_encode_map(&mx, x_base, x_rows, (uint64_t)g.K, (uint32_t)BN)) return cudaErrorInvalidValue;
+  TcParams p;
+  p.M = g.M; p.N = g.N; p.K = g.K;
+  p.kb_total = g.K / BK;
+  p.splits = splits < 1 ? 1 : (splits > p.kb_total ? p.kb_total : splits);
+  p.tiles_f = (g.N + BM - 1) / BM;
+  p.tiles_t = (g.M + BN - 1) / BN;
+  p.part = scr.part;
+  p.counters = scr.counters;
+  p.status = e.status;
+  if (p.splits > 1) {
+    const size_t need = (size_t)p.tiles_f * p.tiles_t * (g.batch > 0 ? g.batch : 1) * p.splits * BN * BM;
+    const size_t tiles = (size_t)p.tiles_f * p.tiles_t * (g.batch > 0 ? g.batch : 1);
+    if (need > scr.part_elems || tiles > (size_t)scr.counters_n) return cudaErrorInvalidValue;
+  }
+  const CUtensorMap& W = *reinterpret_cast<const CUtensorMap*>(&mw);
+  const CUtensorMap& X = *reinterpret_cast<const CUtensorMap*>(&mx);
+  switch (BN) {
+    case 16: return launch_bn<16, 6>(g, e, W, X, p, s, pdl);
+    case 32: return launch_bn<32, 5>(g, e, W, X, p, s, pdl);
+    case 64: return launch_bn<64, 4>(g, e, W, X, p, s, pdl);
+    case 128: return launch_bn<128, 3>(g, e, W, X, p, s, pdl);
+    default: return launch_bn<256, 4>(g, e, W, X, p, s, pdl);
+  }
+}

@@ -186,6 +186,9 @@ struct Epi {
 };
 
 // ------------------------------------------------------------------ launchers
+// Every kernel launch made by the library is counted (ws_launch_count).
+void ws_count_launches(int n);
+
 // Implemented in ws_gemm_simt.cu / ws_gemm_tc.cu / ws_kernels.cu / ws_attn.cu.
 struct GemmShape {
   const void* X; int ldx;       // [M, K] activations, model dtype
@@ -196,8 +199,21 @@ struct GemmShape {
 
 template <typename T> cudaError_t launch_gemm_simt(const GemmShape& g, const Epi& e, cudaStream_t s, bool pdl);
 
-struct TcGemm;  // tcgen05 engine state (ws_gemm_tc.cu)
+// tcgen05 engine (ws_gemm_tc.cu).  TcMap holds an encoded TMA tensor map.
+struct alignas(64) TcMap { unsigned char bytes[128]; };
+struct TcScratch {
+  float* part;            // split-K partials
+  size_t part_elems;
+  int* counters;          // per-tile arrival counters (zero between launches)
+  int counters_n;
+};
 bool tc_engine_available();
+bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+int tc_pick_bn(int M);
+// X is the row-major activation buffer [x_rows, K] (bf16); W's map has 128-row boxes.
+cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const void* x_base, uint64_t x_rows,
+                           int splits, const TcScratch& scr, cudaStream_t s, bool pdl);
+#define WS_ST_TIMEOUT 8   // a bounded wait inside a kernel ran out
 
 template <typename T>
 cudaError_t launch_layernorm(int M, int d, const float* x, int ldx, const T* g, const T* b, T* y, int ldy,

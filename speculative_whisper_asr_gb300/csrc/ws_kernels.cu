@@ -453,6 +453,7 @@ cudaError_t launch_embed_target(int n, int H, const RowMap& rm, const int32_t* b
                                 cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n * H), dim3(128), 0, s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, embed_target_kernel<T>, rm, block, E, P, d, V, x, pend_start, pend_n, status);
 }
 template <typename T>
@@ -460,6 +461,7 @@ cudaError_t launch_embed_draft(int n, int K1, const int32_t* req_ids, const int3
                                int d, int V, float* x, int32_t* pend_n, int32_t* status, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n * K1), dim3(128), 0, s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, embed_draft_kernel<T>, K1, req_ids, block, E, m, d, V, x, pend_n, status);
 }
 template <typename T>
@@ -468,17 +470,20 @@ cudaError_t launch_layernorm(int M, int d, const float* x, int ldx, const T* g, 
   if (M <= 0) return cudaSuccess;
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(128), 0, s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, layernorm_kernel<T>, d, x, ldx, g, b, y, ldy, group_skip);
 }
 cudaError_t launch_argmax_init(int M, unsigned long long* keys, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3((M + 255) / 256), dim3(256), 0, s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, argmax_init_kernel, M, keys);
 }
 cudaError_t launch_argmax_finalize(int n, int H, const int32_t* block_len, const unsigned long long* keys,
                                    int32_t* out, int out_stride, int out_col0, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3((n * H + 255) / 256), dim3(256), 0, s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, argmax_finalize_kernel, n, H, block_len, keys, out, out_stride, out_col0);
 }
 template <typename T>
@@ -486,23 +491,28 @@ cudaError_t launch_hist_gather(int n, int Hp, const int32_t* req_ids, const int3
                                int max_block, int n_hist, int d, T* feat, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n * Hp), dim3(256), 0, s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, hist_gather_kernel<T>, Hp, req_ids, pend_n, hist, max_block, n_hist, d, feat);
 }
 cudaError_t launch_rope_table(float* tab, int max_pos, cudaStream_t s) {
   int n = max_pos * (WS_DH / 2);
+  ws_count_launches(1);
   rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(tab, max_pos);
   return cudaGetLastError();
 }
 cudaError_t launch_set_frames(int n, const int32_t* req_ids, const int32_t* cu, const int32_t* valid,
                               int max_frames, int32_t* Fc, int32_t* Fv, int32_t* status, cudaStream_t s) {
+  ws_count_launches(1);
   set_frames_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, cu, valid, max_frames, Fc, Fv, status);
   return cudaGetLastError();
 }
 cudaError_t launch_reset(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n, cudaStream_t s) {
+  ws_count_launches(1);
   reset_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, L, pend_n);
   return cudaGetLastError();
 }
 cudaError_t launch_get_lengths(int n, const int32_t* req_ids, const int32_t* L, int32_t* out, cudaStream_t s) {
+  ws_count_launches(1);
   get_lengths_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, L, out);
   return cudaGetLastError();
 }
@@ -511,12 +521,14 @@ cudaError_t launch_sample_rows(int n, int rows, const int32_t* req_ids, const fl
                                int out_stride, int out_col0, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n * rows), dim3(SNT), 0, s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, sample_rows_kernel, rows, req_ids, logits, row_stride, V, T, seed, rnd,
                             suppress, out, out_stride, out_col0);
 }
 cudaError_t launch_accept(int n, const AcceptParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n), dim3(SNT), 0, s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, accept_kernel, p);
 }
 cudaError_t launch_draft_synth(int n, int K, const int32_t* req_ids, const int32_t* L, int32_t* block,
@@ -524,6 +536,7 @@ cudaError_t launch_draft_synth(int n, int K, const int32_t* req_ids, const int32
                                cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n), dim3(32), 0, s, pdl, at);
+  ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, draft_synth_kernel, K, req_ids, L, block, traj, tlen, cmask, ctok, max_pos);
 }
 

@@ -75,8 +75,7 @@ class Decoder:
             self.ctx = None
 
     def _blob(self, tensors, order):
-        flat = synth.encode_blob(synth.pack_blob(tensors, order), self.s.dtype)
-        t = torch.from_numpy(flat)
+        t = torch.from_numpy(synth.blob_from(tensors, order, self.s.dtype))
         if self.s.dtype == "bf16":
             t = t.view(torch.int16)
         return t.to(self.dev)
@@ -99,7 +98,7 @@ class Decoder:
         cu = torch.as_tensor(np.concatenate([[0], np.cumsum(frames)]).astype(np.int32), device=self.dev)
         vt = None if valid is None else torch.as_tensor(np.asarray(valid, dtype=np.int32), device=self.dev)
         B.ws_cross_kv(self.ctx, req.numel(), req.data_ptr(), enc_packed.data_ptr(), cu.data_ptr(), _ptr(vt),
-                      int(frames.max()), _stream())
+                      int(frames.max()), int(frames.sum()), _stream())
         return cu, vt
 
     def verify(self, req, block, block_len, target, logits=None):

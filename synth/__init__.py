@@ -123,10 +123,14 @@ def drafter_tensor_shapes(s: ModelShape):
 # ---------------------------------------------------------------- rounding
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
-    """float32 -> nearest-even bf16 value, returned as float32 (input formatting)."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    r = ((u.astype(np.uint64) + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
-    return r.view(np.float32)
+    """float32 -> nearest-even bf16 value, returned as float32 (input formatting).
+    Finite inputs only (uint32 arithmetic cannot overflow below the NaN range)."""
+    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    r = (u >> 16) & 1
+    r += 0x7FFF
+    u += r
+    u &= np.uint32(0xFFFF0000)
+    return u.view(np.float32)
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -154,11 +158,6 @@ def _fmt(a: np.ndarray, dtype: str) -> np.ndarray:
     return round_to_bf16(a) if dtype == "bf16" else a.astype(np.float32, copy=False)
 
 
-def target_weights(s: ModelShape, seed: int) -> dict:
-    """All target tensors (float32 arrays, bf16-valued for bf16 shapes)."""
-    return {n: _fmt(_draw(n, sh, seed, 1), s.dtype) for n, sh in target_tensor_shapes(s)}
-
-
 def drafter_weights(s: ModelShape, seed: int, target: dict | None = None) -> dict:
     """Drafter tensors.  Its two layers are copies of target layers 0 and 1
     (Whisper-Flash §3.2: the drafter is initialised from Whisper's first two
@@ -181,6 +180,43 @@ def pack_blob(tensors: dict, order) -> np.ndarray:
     """Concatenate tensors in blob order into one flat array (f32 or bf16 bits)."""
     parts = [np.ascontiguousarray(tensors[n]).reshape(-1) for n, _ in order]
     return np.concatenate(parts)
+
+
+def _threads():
+    import os
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def target_weights(s: ModelShape, seed: int) -> dict:
+    """All target tensors (float32 arrays, bf16-valued for bf16 shapes)."""
+    from concurrent.futures import ThreadPoolExecutor
+    shapes = target_tensor_shapes(s)
+    with ThreadPoolExecutor(_threads()) as ex:
+        arrs = list(ex.map(lambda ns: _fmt(_draw(ns[0], ns[1], seed, 1), s.dtype), shapes))
+    return {n: a for (n, _), a in zip(shapes, arrs)}
+
+
+def blob_from(tensors: dict, order, dtype: str) -> np.ndarray:
+    """Serialise tensors in blob order: uint16 bf16 bits or float32, one flat array."""
+    total = sum(int(np.prod(sh)) for _, sh in order)
+    out = np.empty(total, dtype=np.uint16 if dtype == "bf16" else np.float32)
+    offs, off = [], 0
+    for n, sh in order:
+        offs.append(off)
+        off += int(np.prod(sh))
+    from concurrent.futures import ThreadPoolExecutor
+
+    def put(i):
+        n, sh = order[i]
+        a = np.ascontiguousarray(tensors[n], dtype=np.float32).reshape(-1)
+        dst = out[offs[i]:offs[i] + a.size]
+        if dtype == "bf16":
+            np.right_shift(a.view(np.uint32), 16, out=dst, casting="unsafe")
+        else:
+            dst[:] = a
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(put, range(len(order))))
+    return out
 
 
 def encode_blob(flat_f32: np.ndarray, dtype: str) -> np.ndarray:
