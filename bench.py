@@ -165,6 +165,16 @@ def run_gpu(args, rank: int, world: int):
     budgets = torch.full((n,), BUDGET, dtype=torch.int32, device=dev)
     ev_v = []
 
+    def draft_calls():
+        dec.draft(req, batch.block, 0.0, 0, 0, None)
+        B.ws_draft_synthetic(dec.ctx, n, req.data_ptr(), batch.block.data_ptr(), syn[0].data_ptr(),
+                             syn[0].shape[1], syn[1].data_ptr(), syn[2].data_ptr(), stream.cuda_stream)
+
+    def accept_calls():
+        a = batch._args(B.WS_ACCEPT_GREEDY, s.K + 1, batch.block, batch.blen, batch.target, batch.block,
+                        batch.blen)
+        B.ws_accept(dec.ctx, n, req.data_ptr(), a, stream.cuda_stream)
+
     def step(record=False, e2e=False):
         """One pass of the whole path; returns tokens emitted."""
         if e2e:
@@ -177,19 +187,17 @@ def run_gpu(args, rank: int, world: int):
         rnd = 0
         while batch.poll_done() < n:
             rnd += 1
-            dec.draft(req, batch.block, 0.0, 0, rnd, None)
-            B.ws_draft_synthetic(dec.ctx, n, req.data_ptr(), batch.block.data_ptr(), syn[0].data_ptr(),
-                                 syn[0].shape[1], syn[1].data_ptr(), syn[2].data_ptr(), stream.cuda_stream)
+            # each phase of the round replays its own captured graph (greedy
+            # rounds do not depend on the round number)
+            batch.replay("draft", draft_calls)
             if record:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-            dec.verify(req, batch.block, batch.blen, batch.target)
+            batch.replay("verify", lambda: dec.verify(req, batch.block, batch.blen, batch.target))
             if record:
                 e1.record(stream)
                 ev_v.append((e0, e1))
-            a = batch._args(B.WS_ACCEPT_GREEDY, s.K + 1, batch.block, batch.blen, batch.target, batch.block,
-                            batch.blen)
-            B.ws_accept(dec.ctx, n, req.data_ptr(), a, stream.cuda_stream)
+            batch.replay("accept", accept_calls)
         if e2e:
             out = batch.transcript.to("cpu", non_blocking=True)
             torch.cuda.current_stream().synchronize()
@@ -213,11 +221,13 @@ def run_gpu(args, rank: int, world: int):
     tstart, tend = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     rounds = []
     with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.nvtx.range_push("ws_timed")        # lets a profiler restrict itself to the timed steps
         tstart.record(stream)
         for _ in range(args.steps):
             rounds.append(step(record=True))
         tend.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     launches = B.ws_launch_count() - l0
     ms = tstart.elapsed_time(tend)
     tokens = int(batch.out_len.sum().item()) * args.steps
@@ -270,6 +280,43 @@ def run_gpu(args, rank: int, world: int):
     }
 
 
+# ---------------------------------------------------------------- profiling case
+def run_profile(args):
+    """Short case for kernel profilers: the same model and kernels as the
+    benchmark (acoustic K/V, prefill, then `--profile` speculative rounds
+    with uniformly random proposals), without the reference trajectory and
+    the CPU baseline.  The rounds run inside an NVTX range "ws_timed"."""
+    import torch
+    from speculative_whisper_asr_gb300 import binding as B
+    from speculative_whisper_asr_gb300 import runtime as R
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    s = synth.LARGE_V3
+    n = args.batch
+    tw = synth.target_weights(s, SEED)
+    dw = synth.drafter_weights(s, SEED, tw)
+    dec = R.Decoder(s, tw, dw, max_batch=n, max_frames=1500)
+    del tw, dw
+    req = dec.slots(list(range(n)))
+    enc = torch.cat([dec.enc_tensor(synth.encoder_states(s, SEED, i)) for i in range(n)])
+    dec.cross_kv(req, enc, [1500] * n)
+    plan = synth.corruption_plan(n, s.max_pos, s.K, synth.corruption_p_const(s.K, 1.0), s.vocab, SEED)
+    syn = (torch.zeros(n, s.max_pos, dtype=torch.int32, device="cuda"), torch.as_tensor(plan.mask, device="cuda"),
+           torch.as_tensor(plan.tok, device="cuda"))
+    b = dec.new_batch(req, [BUDGET] * n)
+    b.prefill()
+    for _ in range(2):                       # warm-up rounds (graph capture)
+        b.spec_step(0, syn)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("ws_timed")
+    for r in range(args.profile):
+        b.spec_step(0, syn)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    print(json.dumps({"profile_rounds": args.profile, "status": dec.status(), "engine": dec.engine}))
+
+
 # ---------------------------------------------------------------- oracle (CPU) arm
 def run_oracle_sample(budget_tokens: int = 12):
     """The oracle, as it stands, on a bounded sample of the same workload: one
@@ -304,9 +351,13 @@ def main():
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", type=int, default=0, help="run N rounds of the profiling case and exit")
     args = ap.parse_args()
     rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
+    if args.profile > 0:
+        run_profile(args)
+        return
     if args.impl == "reference":
         if rank != 0:
             return

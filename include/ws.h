@@ -229,6 +229,19 @@ int ws_status(ws_ctx* ctx, ws_stream stream, int32_t* host_status);
 /* Name of the GEMM engine in use ("simt" or "tcgen05"). */
 const char* ws_gemm_engine(const ws_ctx* ctx);
 
+/* CUDA-graph replay of a fixed call sequence (Whisper-Flash Appendix A.5
+ * replays prefill, drafting and each verification length from captured
+ * graphs).  Between ws_capture_begin and ws_capture_end every ws_* call on
+ * `stream` is recorded instead of executed (none of them synchronises);
+ * ws_capture_end instantiates the graph.  Pointers and host scalars are
+ * frozen at capture; device-resident state (cache lengths, blocks, budgets)
+ * is read at replay.  ws_graph_launch enqueues one replay on `stream`. */
+typedef struct ws_graph ws_graph;
+int ws_capture_begin(ws_ctx* ctx, ws_stream stream);
+int ws_capture_end(ws_ctx* ctx, ws_stream stream, ws_graph** out);
+int ws_graph_launch(ws_graph* graph, ws_stream stream);
+void ws_graph_free(ws_graph* graph);
+
 /* Number of CUDA kernels this library has launched in the process so far
  * (all contexts; host-side counter, for instrumentation). */
 unsigned long long ws_launch_count(void);

@@ -21,7 +21,8 @@ WS_ACCEPT_GREEDY, WS_ACCEPT_SAMPLE, WS_ACCEPT_FORCED = 0, 1, 2
 
 EXPORTS = ("ws_query_workspace", "ws_load_weights", "ws_reset", "ws_cross_kv", "ws_verify", "ws_draft",
            "ws_accept", "ws_draft_synthetic", "ws_sample", "ws_set_suppress", "ws_get_lengths", "ws_status",
-           "ws_gemm_engine", "ws_launch_count", "ws_last_error", "ws_free")
+           "ws_gemm_engine", "ws_launch_count", "ws_last_error", "ws_free", "ws_capture_begin",
+           "ws_capture_end", "ws_graph_launch", "ws_graph_free")
 
 
 class WSError(RuntimeError):
@@ -70,6 +71,10 @@ def _load():
         "ws_launch_count": (C.c_ulonglong, []),
         "ws_last_error": (C.c_char_p, [P]),
         "ws_free": (None, [P]),
+        "ws_capture_begin": (I, [P, S]),
+        "ws_capture_end": (I, [P, S, C.POINTER(P)]),
+        "ws_graph_launch": (I, [P, S]),
+        "ws_graph_free": (None, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -171,3 +176,21 @@ def ws_last_error(ctx=None) -> str:
 
 def ws_free(ctx):
     lib.ws_free(ctx)
+
+
+def ws_capture_begin(ctx, stream):
+    return _check(ctx, lib.ws_capture_begin(ctx, stream))
+
+
+def ws_capture_end(ctx, stream) -> int:
+    g = C.c_void_p()
+    _check(ctx, lib.ws_capture_end(ctx, stream, C.byref(g)))
+    return g.value
+
+
+def ws_graph_launch(graph, stream):
+    return _check(None, lib.ws_graph_launch(graph, stream))
+
+
+def ws_graph_free(graph):
+    lib.ws_graph_free(graph)

@@ -49,18 +49,26 @@ struct ws_ctx {
   float* part = nullptr;
   void* feat = nullptr; float* hpre = nullptr; void* hh = nullptr;
   int pending_H = 0;
+  unsigned long long cap_start = 0;   // launch counter when a capture began
   int max_fc = 0;
   const uint32_t* suppress = nullptr;
   int engine = WS_GEMM_SIMT;
   bool split_ok = false;        // split-K allowed (small-batch contexts)
   int mrows = 0;                // rows of the activation buffers
   TcScratch tcs{};
+  struct XMap { const void* base; TcMap bn[5]; };   // activation maps per token-tile width
+  std::vector<XMap> xmaps;
   bool pdl = true;              // programmatic dependent launch allowed
   bool cur_pdl = false;         // PDL for the call in progress (never on the legacy stream)
   std::string err;
 };
 
 static std::atomic<unsigned long long> g_launches{0};
+
+struct ws_graph {
+  cudaGraphExec_t exec;
+  unsigned long long kernels;   // kernel launches recorded in the graph
+};
 void ws_count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 namespace {
@@ -242,7 +250,13 @@ cudaError_t gemm(ws_ctx* c, const void* X, uint64_t x_rows, const Mat& W, int M,
   GemmShape g;
   g.X = X; g.ldx = W.cols; g.W = W.p; g.ldw = W.cols; g.M = M; g.N = W.rows; g.K = W.cols; g.batch = batch;
   if (c->engine == WS_GEMM_TC && sizeof(T) == 2)
-    return launch_gemm_tc(g, e, W.map, X, x_rows, allow_split ? splits_for(c, g.N, g.K) : 1, c->tcs, s, c->cur_pdl);
+  {
+    const TcMap* mx = nullptr;
+    for (const auto& xm : c->xmaps)
+      if (xm.base == X) { mx = &xm.bn[tc_bn_index(tc_pick_bn(M))]; break; }
+    return launch_gemm_tc(g, e, W.map, mx, X, x_rows, allow_split ? splits_for(c, g.N, g.K) : 1, c->tcs, s,
+                          c->cur_pdl);
+  }
   return launch_gemm_simt<T>(g, e, s, c->cur_pdl);
 }
 
@@ -511,6 +525,17 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
       }
     enc(c->head);
     if (desc->drafter_layers > 0) enc(c->fuse_w);
+    // activation buffers: one map per token-tile width
+    auto xm = [&](const void* base, int cols) {
+      ws_ctx::XMap m;
+      m.base = base;
+      const int bns[5] = {16, 32, 64, 128, 256};
+      for (int i = 0; i < 5; ++i) ok = ok && tc_encode_map(&m.bn[i], base, (uint64_t)c->mrows, (uint64_t)cols, bns[i]);
+      c->xmaps.push_back(m);
+    };
+    xm(c->h, (int)D); xm(c->ao, (int)D); xm(c->ffn, desc->d_ff); xm(c->hh, (int)D);
+    if (desc->drafter_layers > 0) xm(c->feat, (int)(desc->n_hist * D));
+    if (ok && tc_init_attributes() != cudaSuccess) ok = false;
     if (!ok) { fail(nullptr, WS_ECUDA, "TMA descriptor encoding failed"); return cleanup(WS_ECUDA); }
   }
 
@@ -655,6 +680,44 @@ const char* ws_gemm_engine(const ws_ctx* c) {
 }
 
 unsigned long long ws_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int ws_capture_begin(ws_ctx* c, ws_stream stream) {
+  if (!c) return fail(nullptr, WS_EINVAL, "null context");
+  if (!stream) return fail(c, WS_EINVAL, "capture needs a created stream");
+  CK(cudaStreamBeginCapture((cudaStream_t)stream, cudaStreamCaptureModeThreadLocal));
+  c->cap_start = g_launches.load();
+  return WS_OK;
+}
+
+int ws_capture_end(ws_ctx* c, ws_stream stream, ws_graph** out) {
+  if (!c || !out) return fail(c, WS_EINVAL, "null context or output");
+  *out = nullptr;
+  cudaGraph_t g = nullptr;
+  // kernels recorded while capturing did not run: move them to the graph
+  const unsigned long long recorded = g_launches.load() - c->cap_start;
+  g_launches.fetch_sub(recorded);
+  CK(cudaStreamEndCapture((cudaStream_t)stream, &g));
+  cudaGraphExec_t ex = nullptr;
+  cudaError_t e = cudaGraphInstantiate(&ex, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return fail(c, WS_ECUDA, "graph instantiate: %s", cudaGetErrorString(e));
+  *out = new ws_graph{ex, recorded};
+  return WS_OK;
+}
+
+int ws_graph_launch(ws_graph* graph, ws_stream stream) {
+  if (!graph) return fail(nullptr, WS_EINVAL, "null graph");
+  cudaError_t e = cudaGraphLaunch(graph->exec, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(nullptr, WS_ECUDA, "graph launch: %s", cudaGetErrorString(e));
+  g_launches.fetch_add(graph->kernels);
+  return WS_OK;
+}
+
+void ws_graph_free(ws_graph* graph) {
+  if (!graph) return;
+  cudaGraphExecDestroy(graph->exec);
+  delete graph;
+}
 
 const char* ws_last_error(const ws_ctx* c) { return c ? c->err.c_str() : g_err.c_str(); }
 

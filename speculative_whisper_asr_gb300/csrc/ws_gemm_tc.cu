@@ -303,12 +303,20 @@ __global__ void __launch_bounds__(128, 1)
         const float* base = p.part + (size_t)tile * p.splits * BN * BM;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
+          // splits outer, columns inner: the 16 loads of one split are
+          // independent and in flight together; the per-element order of
+          // the additions is still split 0, 1, 2, ...
           float v[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            float acc = 0.0f;
-            for (int s = 0; s < p.splits; ++s) acc += __ldcg(base + ((size_t)s * BN + c0 + c) * BM + row);
-            v[c] = acc;
+          for (int c = 0; c < 16; ++c) v[c] = 0.0f;
+#pragma unroll 1
+          for (int s = 0; s < p.splits; ++s) {
+            float w[16];
+            const float* src = base + ((size_t)s * BN + c0) * BM + row;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) w[c] = __ldcg(src + (size_t)c * BM);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] += w[c];
           }
           epilogue16<BN>(e, p, t0, c0, n, M, z, v);
         }
@@ -327,13 +335,6 @@ template <int BN, int STAGES>
 cudaError_t launch_bn(const GemmShape& g, const Epi& e, const CUtensorMap& mw, const CUtensorMap& mx,
                       const TcParams& p, cudaStream_t s, bool pdl) {
   constexpr int smem = STAGES * (A_BYTES + BN * BK * 2) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t r = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem);
-    if (r != cudaSuccess) return r;
-    attr = true;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.tiles_f * p.splits, p.tiles_t, g.batch > 0 ? g.batch : 1);
   cfg.blockDim = dim3(128);
@@ -379,6 +380,25 @@ bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uin
   return r == CUDA_SUCCESS;
 }
 
+// Raise the dynamic shared-memory limit of every kernel variant once, before
+// any launch (so no attribute call happens while a stream is being captured).
+cudaError_t tc_init_attributes() {
+  cudaError_t r = cudaSuccess;
+  auto set = [&](const void* fn, int bn, int stages) {
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               stages * (A_BYTES + bn * BK * 2) + 1024);
+  };
+  set((const void*)gemm_tc_kernel<16, 6>, 16, 6);
+  set((const void*)gemm_tc_kernel<32, 5>, 32, 5);
+  set((const void*)gemm_tc_kernel<64, 4>, 64, 4);
+  set((const void*)gemm_tc_kernel<128, 3>, 128, 3);
+  set((const void*)gemm_tc_kernel<256, 4>, 256, 4);
+  return r;
+}
+
+int tc_bn_index(int bn) { return bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <= 128 ? 3 : 4; }
+
 int tc_pick_bn(int M) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
@@ -387,13 +407,15 @@ int tc_pick_bn(int M) {
   return 256;
 }
 
-cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const void* x_base, uint64_t x_rows,
-                           int splits, const TcScratch& scr, cudaStream_t s, bool pdl) {
+cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const TcMap* mx_cached,
+                           const void* x_base, uint64_t x_rows, int splits, const TcScratch& scr, cudaStream_t s,
+                           bool pdl) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
   if (g.K % BK != 0 || g.ldx != g.K) return cudaErrorInvalidValue;
   const int BN = tc_pick_bn(g.M);
   TcMap mx;
-  if (!tc_encode_map(&mx, x_base, x_rows, (uint64_t)g.K, (uint32_t)BN)) return cudaErrorInvalidValue;
+  if (mx_cached) mx = *mx_cached;
+  else if (!tc_encode_map(&mx, x_base, x_rows, (uint64_t)g.K, (uint32_t)BN)) return cudaErrorInvalidValue;
   TcParams p;
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.kb_total = g.K / BK;

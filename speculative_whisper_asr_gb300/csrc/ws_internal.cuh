@@ -211,8 +211,13 @@ bool tc_engine_available();
 bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 int tc_pick_bn(int M);
 // X is the row-major activation buffer [x_rows, K] (bf16); W's map has 128-row boxes.
-cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const void* x_base, uint64_t x_rows,
-                           int splits, const TcScratch& scr, cudaStream_t s, bool pdl);
+// mx_cached: the activation map for this call's token tile (tc_pick_bn), or
+// NULL to encode one from x_base / x_rows.
+cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const TcMap* mx_cached,
+                           const void* x_base, uint64_t x_rows, int splits, const TcScratch& scr, cudaStream_t s,
+                           bool pdl);
+cudaError_t tc_init_attributes();
+int tc_bn_index(int bn);   // 16,32,64,128,256 -> 0..4
 #define WS_ST_TIMEOUT 8   // a bounded wait inside a kernel ran out
 
 template <typename T>

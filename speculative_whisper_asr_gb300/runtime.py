@@ -161,6 +161,25 @@ class Batch:
             self.p_logits = torch.empty(n, K + 1, dec.V, dtype=torch.float32, device=dev)
             self.q_logits = torch.empty(n, K, dec.V, dtype=torch.float32, device=dev)
         self.host_done = torch.zeros(1, dtype=torch.int32).pin_memory()
+        self.graphs = {}
+
+    def __del__(self):
+        for g in getattr(self, "graphs", {}).values():
+            B.ws_graph_free(g)
+
+    def replay(self, key, fn):
+        """Run `fn` (a fixed sequence of ws_* calls) through a CUDA graph
+        captured on first use; later calls replay it."""
+        g = self.graphs.get(key)
+        s = _stream()
+        if g is None:
+            B.ws_capture_begin(self.dec.ctx, s)
+            try:
+                fn()
+            finally:
+                g = B.ws_capture_end(self.dec.ctx, s)
+            self.graphs[key] = g
+        B.ws_graph_launch(g, s)
 
     def _args(self, mode, H, block, blen, target, next_block, next_len, p_logits=None, q_logits=None,
               temperature=0.0, seed=0, rnd=0) -> B.AcceptArgs:
@@ -186,14 +205,29 @@ class Batch:
                        self.blen)
         B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
 
-    def ar_step(self):
+    def ar_step(self, graph: bool = True):
         d = self.dec
-        d.verify(self.req, self.block1, self.blen, self.target1)
-        a = self._args(B.WS_ACCEPT_GREEDY, 1, self.block1, self.blen, self.target1, self.block1, self.blen)
-        B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
 
-    def spec_step(self, rnd: int, synthetic=None, temperature: float = 0.0, seed: int = 0, run_drafter=True):
-        """One propose / verify / accept round.  `synthetic` = (traj, tlen, cmask, ctok) device tensors."""
+        def calls():
+            d.verify(self.req, self.block1, self.blen, self.target1)
+            a = self._args(B.WS_ACCEPT_GREEDY, 1, self.block1, self.blen, self.target1, self.block1, self.blen)
+            B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
+        if graph:
+            self.replay(("ar",), calls)
+        else:
+            calls()
+
+    def spec_step(self, rnd: int, synthetic=None, temperature: float = 0.0, seed: int = 0, run_drafter=True,
+                  graph: bool = True):
+        """One propose / verify / accept round.  `synthetic` = (traj, cmask, ctok) device tensors.
+        Greedy rounds replay one captured graph (their calls do not depend on the round)."""
+        if graph and temperature <= 0.0:
+            self.replay(("spec", synthetic is not None, run_drafter),
+                        lambda: self._spec_calls(0, synthetic, 0.0, 0, run_drafter))
+        else:
+            self._spec_calls(rnd, synthetic, temperature, seed, run_drafter)
+
+    def _spec_calls(self, rnd, synthetic, temperature, seed, run_drafter):
         d = self.dec
         sampling = temperature > 0.0
         if run_drafter:
