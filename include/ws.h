@@ -242,6 +242,25 @@ int ws_capture_end(ws_ctx* ctx, ws_stream stream, ws_graph** out);
 int ws_graph_launch(ws_graph* graph, ws_stream stream);
 void ws_graph_free(ws_graph* graph);
 
+/* Greedy choice over given logits rows without allocating anything.
+ * The paper has no counterpart: this is an interface convenience.  Callers
+ * that cannot call cudaMalloc — code running during CUDA-graph capture
+ * (allocation is not capturable), code inside a host framework whose own
+ * pool owns all device memory, latency-critical threads that must not block
+ * on the driver — get argmax_v logits[r, v] (lowest id on ties, suppressed
+ * ids skipped) for each row, the same values ws_verify returns as `target`
+ * for the logits it writes.
+ *   logits  [rows, vocab] float (device); out [rows] int32 (device)
+ *   suppress  optional [ceil(vocab/32)] uint32 bitmask (device), or NULL
+ * Scratch is a fixed 256 KB array inside the library (held by every GPU
+ * that loads it until the process exits); rows > 1024 return WS_EINVAL.
+ * The first call on each device looks up that array's device address, so it
+ * should come before any stream capture.  Calls share the array: calls whose
+ * work overlaps on the GPU (other streams, other unordered threads) race.
+ * Errors: ws_last_error(NULL). */
+int ws_argmax_rows_noalloc(const float* logits, int rows, int vocab, const uint32_t* suppress,
+                           int32_t* out, ws_stream stream);
+
 /* Number of CUDA kernels this library has launched in the process so far
  * (all contexts; host-side counter, for instrumentation). */
 unsigned long long ws_launch_count(void);

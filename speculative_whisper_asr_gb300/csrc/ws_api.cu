@@ -75,6 +75,12 @@ namespace {
 
 thread_local std::string g_err;
 
+}  // namespace
+
+void ws_set_thread_error(const char* msg) { g_err = msg ? msg : ""; }
+
+namespace {
+
 int fail(ws_ctx* c, int code, const char* fmt, ...) {
   char buf[512];
   va_list ap;

@@ -188,6 +188,8 @@ struct Epi {
 // ------------------------------------------------------------------ launchers
 // Every kernel launch made by the library is counted (ws_launch_count).
 void ws_count_launches(int n);
+// Message returned by ws_last_error(NULL) on the calling thread.
+void ws_set_thread_error(const char* msg);
 
 // Implemented in ws_gemm_simt.cu / ws_gemm_tc.cu / ws_kernels.cu / ws_attn.cu.
 struct GemmShape {
