@@ -326,6 +326,7 @@ class Accepted:
     emitted: list       # tokens appended to the transcript this round
     next_anchor: int
     done: bool
+    margins: list = field(default_factory=list)   # sampling: decision margin per emitted token
 
 
 def accept_greedy(block, n_prop: int, g, budget: int, eos: int) -> Accepted:
@@ -375,8 +376,52 @@ def sample_inverse_cdf(w: np.ndarray, u: float) -> int:
     return v
 
 
+def cdf_margin(w: np.ndarray, u: float) -> float:
+    """How far u * sum(w) lies from the nearest boundary of the inverse-CDF
+    draw, as a fraction of sum(w): the size of a perturbation of the weights
+    that could change the drawn id."""
+    c = np.cumsum(np.asarray(w, dtype=np.float64))
+    t = float(u) * c[-1]
+    v = min(int(np.searchsorted(c, t, side="right")), len(c) - 1)
+    lo = c[v - 1] if v > 0 else 0.0
+    return float(min(t - lo, c[v] - t) / c[-1])
+
+
 def accept_sampling(block, n_prop: int, p_logits, q_logits, T: float, seed: int, slot: int,
-                    rnd: int, budget: int, eos: int, suppress=None, uniform=None):
+                    rnd: int, budget: int, eos: int, suppress=None, uniform=None, cand_margins=None):
+    """Rejection rule with per-token decision margins: `cand_margins[j-1]` is
+    the margin of the draw that produced candidate j (if known); the margin
+    of an emitted token is the smallest margin among the decisions that led
+    to it."""
+    acc, det = _accept_sampling(block, n_prop, p_logits, q_logits, T, seed, slot, rnd, budget, eos, suppress,
+                                uniform)
+    # (acceptance margin, inverse-CDF margin) of the decision chain so far
+    ca, cc = float("inf"), float("inf")
+    margins = []
+    for d in det:
+        if d[0] == "accept":
+            _, j, u, qv, pv, ok = d
+            ca = min(ca, abs(u * qv - pv) / max(pv, 1e-30))
+            if cand_margins is not None:
+                cc = min(cc, cand_margins[j - 1])
+            if ok:
+                margins.append((ca, cc))
+        else:
+            _, j, u2, tok = d
+            if d[0] == "residual":
+                p = probs_fp32(p_logits[j - 1], T, suppress)
+                q = probs_fp32(q_logits[j - 1], T, suppress)
+                w = np.maximum(p - q, np.float32(0))
+                w = w if np.any(w > 0) else p
+            else:
+                w = probs_fp32(p_logits[j - 1], T, suppress)
+            margins.append((ca, min(cc, cdf_margin(w, u2))))
+    acc.margins = margins
+    return acc, det
+
+
+def _accept_sampling(block, n_prop: int, p_logits, q_logits, T: float, seed: int, slot: int,
+                     rnd: int, budget: int, eos: int, suppress=None, uniform=None):
     """Speculative rejection rule (Whisper-Flash §3.1; Leviathan et al.,
     Chen et al.): candidate j is accepted iff u_j * q_j(y_j) < p_j(y_j)
     (probability min(1, p/q)); at the first rejection a token is drawn from
@@ -453,13 +498,22 @@ def greedy_plain(orc: Oracle, req: Request, budget: int) -> DecodeResult:
     return DecodeResult(out, rounds=len(out), margins=margins)
 
 
-def prefill(orc: Oracle, req: Request, budget: int):
+def prefill(orc: Oracle, req: Request, budget: int, T: float = 0.0, seed: int = 0, slot: int = 0):
     """Prompt pass: processes the prompt and emits the first transcript token,
-    which becomes the first anchor (Appendix A.1)."""
+    which becomes the first anchor (Appendix A.1).  With T > 0 that token is
+    drawn from softmax(z/T) of the last prompt row (counter (slot, 0, n, 2))."""
     prompt = list(orc.s.prompt)
     logits = orc.verify(req, prompt)
     g = [argmax_lowest(z) for z in logits]
-    acc = accept_forced(len(prompt) - 1, g, budget, orc.s.eos_id)
+    n_prop = len(prompt) - 1
+    margin = top2_margin(logits[n_prop])
+    if T > 0:
+        u = philox.uniform(seed, slot, 0, n_prop + 1, philox.PURPOSE_RESIDUAL)
+        p = probs_fp32(logits[n_prop], T)
+        g[n_prop] = sample_inverse_cdf(p, u)
+        margin = (float("inf"), cdf_margin(p, u))
+    acc = accept_forced(n_prop, g, budget, orc.s.eos_id)
+    acc.margins = [margin]
     req.L += 1 + acc.a
     return acc, logits
 
@@ -530,6 +584,60 @@ def corrupted_proposer(traj_with_prompt, mask, tok):
                 out.append(int(traj_with_prompt[p]) if p < len(traj_with_prompt) else int(tok[t, j - 1]))
         return out
     return propose
+
+
+def sampling_plain(orc: Oracle, req: Request, budget: int, T: float, seed: int, slot: int,
+                   suppress=None) -> DecodeResult:
+    """Autoregressive sampling from the target at temperature T: after the
+    prompt, every round verifies the anchor alone and draws the next token
+    from softmax(z/T) (the rejection rule with no candidates reduces to the
+    bonus draw; Philox counter (slot, round, 1, 2))."""
+    acc, logits = prefill(orc, req, budget, T, seed, slot)
+    out, done, anchor, rnd = list(acc.emitted), acc.done, acc.next_anchor, 0
+    res = DecodeResult(out, margins=list(acc.margins))
+    while not done:
+        rnd += 1
+        lg = orc.verify(req, [anchor])
+        acc, _ = accept_sampling([anchor], 0, lg, None, T, seed, slot, rnd, budget - len(out), orc.s.eos_id,
+                                 suppress)
+        req.L += 1 + acc.a
+        out += acc.emitted
+        res.margins += acc.margins
+        done, anchor = acc.done, acc.next_anchor
+        res.rounds += 1
+    return res
+
+
+def speculative_sampling(orc: Oracle, req: Request, budget: int, T: float, seed: int, slot: int,
+                         suppress=None) -> DecodeResult:
+    """Speculative sampling with the parallel drafter (Whisper-Flash §3.1,
+    Appendix A.4): each mask row is sampled independently from its draft
+    distribution (counter (slot, round, j, 0)), the target verifies the block,
+    the rejection rule accepts or resamples."""
+    K, eos = orc.s.K, orc.s.eos_id
+    acc, logits = prefill(orc, req, budget, T, seed, slot)
+    out, done, anchor, rnd = list(acc.emitted), acc.done, acc.next_anchor, 0
+    res = DecodeResult(out, margins=list(acc.margins))
+    while not done:
+        rnd += 1
+        R = budget - len(out)
+        n_prop = min(K, R - 1)
+        q = orc.draft_logits(req, anchor)
+        cand = [sample_draft(q[j], T, seed, slot, rnd, j + 1, suppress) for j in range(K)]
+        cmarg = [cdf_margin(probs_fp32(q[j], T, suppress),
+                            philox.uniform(seed, slot, rnd, j + 1, philox.PURPOSE_DRAFT)) for j in range(K)]
+        block = [anchor] + cand[:n_prop]
+        lg = orc.verify(req, block)
+        acc, _ = accept_sampling(block, n_prop, lg, q, T, seed, slot, rnd, R, eos, suppress, cand_margins=cmarg)
+        req.L += 1 + acc.a
+        out += acc.emitted
+        res.margins += acc.margins
+        res.rounds += 1
+        res.accepted.append(acc.a)
+        res.proposed.append(n_prop)
+        res.emitted.append(len(acc.emitted))
+        done, anchor = acc.done, acc.next_anchor
+    return res
 
 
 def acceptance_metrics(res: DecodeResult, K: int) -> dict:

@@ -240,33 +240,36 @@ __device__ RowStat row_stat(const float* z, int V, float T, const uint32_t* sup,
 // order: the smallest v whose running sum exceeds u * sum(w).  Each thread
 // owns a contiguous chunk; chunk sums are prefixed in thread order.
 template <class WF>
-__device__ int block_inverse_cdf(WF w, int V, float u, float* sh /* >= SNT + 8 floats */) {
+__device__ int block_inverse_cdf(WF w, int V, float u) {
+  // The weights are FP32 probabilities; their running sums are kept in FP64
+  // so that the drawn id depends on the weights, not on the summation order.
   __shared__ int found;
+  __shared__ double shd[SNT + 1];
   const int C = (V + SNT - 1) / SNT;
   const int lo = threadIdx.x * C, hi = min(V, lo + C);
-  float s = 0.0f;
-  for (int v = lo; v < hi; ++v) s += w(v);
+  double s = 0.0;
+  for (int v = lo; v < hi; ++v) s += (double)w(v);
   __syncthreads();
-  sh[threadIdx.x] = s;
+  shd[threadIdx.x] = s;
   if (threadIdx.x == 0) found = -1;
   __syncthreads();
   if (threadIdx.x == 0) {
-    float run = 0.0f;
-    for (int t = 0; t < SNT; ++t) { float c = sh[t]; sh[t] = run; run += c; }
-    sh[SNT] = run;
+    double run = 0.0;
+    for (int t = 0; t < SNT; ++t) { double c = shd[t]; shd[t] = run; run += c; }
+    shd[SNT] = run;
   }
   __syncthreads();
-  const float total = sh[SNT];
-  const float target = u * total;
-  const float pre = sh[threadIdx.x];
-  const float nxt = threadIdx.x + 1 < SNT ? sh[threadIdx.x + 1] : total;
-  if (s > 0.0f && pre <= target && target < nxt) {
-    float run = pre;
+  const double total = shd[SNT];
+  const double target = (double)u * total;
+  const double pre = shd[threadIdx.x];
+  const double nxt = threadIdx.x + 1 < SNT ? shd[threadIdx.x + 1] : total;
+  if (s > 0.0 && pre <= target && target < nxt) {
+    double run = pre;
     int tok = -1, last = -1;
     for (int v = lo; v < hi; ++v) {
-      float wv = w(v);
+      const float wv = w(v);
       if (wv > 0.0f) last = v;
-      run += wv;
+      run += (double)wv;
       if (run > target) { tok = v; break; }
     }
     atomicMax(&found, tok >= 0 ? tok : last);
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(SNT) sample_rows_kernel(int rows, const int32_
   const float* z = logits + ((long long)i * rows + r) * row_stride;
   RowStat st = row_stat(z, V, T, sup, sh);
   const float u = ws_uniform(seed, (uint32_t)slot, rnd, (uint32_t)(r + 1), 0u);
-  int tok = block_inverse_cdf([&](int v) { return expf(scaled(z, v, T, sup) - st.m); }, V, u, sh);
+  int tok = block_inverse_cdf([&](int v) { return expf(scaled(z, v, T, sup) - st.m) / st.S; }, V, u);
   pdl_trigger();
   if (threadIdx.x == 0) out[(size_t)i * out_stride + out_col0 + r] = tok;
 }
@@ -336,7 +339,10 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
   if (threadIdx.x == 0) { s_ne = 0; s_a = 0; s_stop = 0; }
   __syncthreads();
 
-  if (A.mode == WS_ACCEPT_GREEDY || A.mode == WS_ACCEPT_FORCED) {
+  // A forced block with a temperature and logits samples its emitted token
+  // (the first transcript token of a sampled decode) instead of taking the argmax.
+  const bool forced_sample = A.mode == WS_ACCEPT_FORCED && A.temperature > 0.0f && A.p_logits != nullptr;
+  if (A.mode == WS_ACCEPT_GREEDY || (A.mode == WS_ACCEPT_FORCED && !forced_sample)) {
     if (threadIdx.x == 0) {
       const int32_t* g = A.target + (size_t)i * A.H;
       int a = 0, ne = 0;
@@ -359,7 +365,8 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
   } else {
     // Rejection rule: accept y_j iff u_j * q_j(y_j) < p_j(y_j) (FP32).
     const float T = A.temperature;
-    for (int j = 1; j <= n_prop; ++j) {
+    if (forced_sample && threadIdx.x == 0) s_a = n_prop;
+    for (int j = 1; j <= (forced_sample ? 0 : n_prop); ++j) {
       const int y = blk[j];
       const float* zp = A.p_logits + ((long long)i * A.H + (j - 1)) * P.V;
       const float* zq = A.q_logits + ((long long)i * P.K + (j - 1)) * P.V;
@@ -386,8 +393,8 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
       rs = block_sum<SNT>(rs, sh);
       const float u2 = ws_uniform(A.seed, (uint32_t)slot, A.round, (uint32_t)j, 2u);
       int tok;
-      if (rs > 0.0f) tok = block_inverse_cdf(resid, P.V, u2, sh);
-      else tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m); }, P.V, u2, sh);
+      if (rs > 0.0f) tok = block_inverse_cdf(resid, P.V, u2);
+      else tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m) / sp.S; }, P.V, u2);
       if (threadIdx.x == 0) { s_emit[s_ne++] = tok; s_stop = 2; }
       __syncthreads();
       break;
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
       const float* zp = A.p_logits + ((long long)i * A.H + n_prop) * P.V;
       RowStat sp = row_stat(zp, P.V, T, P.suppress, sh);
       const float u2 = ws_uniform(A.seed, (uint32_t)slot, A.round, (uint32_t)(n_prop + 1), 2u);
-      int tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m); }, P.V, u2, sh);
+      int tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m) / sp.S; }, P.V, u2);
       if (threadIdx.x == 0) s_emit[s_ne++] = tok;
     }
     __syncthreads();

@@ -195,14 +195,16 @@ class Batch:
         a.n_done = self.n_done.data_ptr()
         return a
 
-    def prefill(self, ar: bool = False):
+    def prefill(self, ar: bool = False, temperature: float = 0.0, seed: int = 0):
         """Prompt pass: emits the first transcript token (the first anchor)."""
         d = self.dec
         d.reset(self.req)
-        d.verify(self.req, self.prompt, self.plen, self.ptarget)
+        sampled = temperature > 0.0 and self.p_logits is not None
+        d.verify(self.req, self.prompt, self.plen, self.ptarget, self.p_logits if sampled else None)
         nb = self.block1 if ar else self.block
         a = self._args(B.WS_ACCEPT_FORCED, self.prompt.shape[1], self.prompt, self.plen, self.ptarget, nb,
-                       self.blen)
+                       self.blen, self.p_logits if sampled else None, None, temperature if sampled else 0.0,
+                       seed, 0)
         B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
 
     def ar_step(self, graph: bool = True):
@@ -216,6 +218,14 @@ class Batch:
             self.replay(("ar",), calls)
         else:
             calls()
+
+    def ar_sample_step(self, rnd: int, temperature: float, seed: int):
+        """Autoregressive sampling round: verify the anchor, draw from softmax(z/T)."""
+        d = self.dec
+        d.verify(self.req, self.block1, self.blen, self.target1, self.p_logits)
+        a = self._args(B.WS_ACCEPT_SAMPLE, 1, self.block1, self.blen, self.target1, self.block1, self.blen,
+                       self.p_logits, self.q_logits, temperature, seed, rnd)
+        B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
 
     def spec_step(self, rnd: int, synthetic=None, temperature: float = 0.0, seed: int = 0, run_drafter=True,
                   graph: bool = True):
@@ -263,10 +273,56 @@ def run_ar(dec: Decoder, batch: Batch, max_rounds: int = 100000) -> int:
 
 
 def run_spec(dec: Decoder, batch: Batch, synthetic=None, temperature=0.0, seed=0, max_rounds=100000,
-             run_drafter=True) -> int:
-    batch.prefill()
+             run_drafter=True, graph=True) -> int:
+    batch.prefill(temperature=temperature, seed=seed)
     rounds = 0
     while batch.poll_done() < batch.n and rounds < max_rounds:
-        batch.spec_step(rounds + 1, synthetic, temperature, seed, run_drafter)
+        batch.spec_step(rounds + 1, synthetic, temperature, seed, run_drafter, graph=graph)
         rounds += 1
     return rounds
+
+
+def run_ar_sampling(dec: Decoder, batch: Batch, temperature: float, seed: int, max_rounds=100000) -> int:
+    batch.prefill(ar=True, temperature=temperature, seed=seed)
+    rounds = 0
+    while batch.poll_done() < batch.n and rounds < max_rounds:
+        rounds += 1
+        batch.ar_sample_step(rounds, temperature, seed)
+    return rounds
+
+
+def run_spec_packed(dec: Decoder, req_all: torch.Tensor, budgets, synthetic=None, max_rounds=100000):
+    """Varlen batch without padding rows: after every round the requests that
+    finished are dropped from the slot list, so later rounds only carry live
+    requests (their rows, attention and acceptance).  Returns (transcripts,
+    rounds, rows processed)."""
+    n_all = req_all.numel()
+    alive = list(range(n_all))
+    out = [None] * n_all
+    budgets = np.asarray(budgets, dtype=np.int32)
+    b = dec.new_batch(req_all, budgets)
+    b.prefill()
+    rounds, rows = 0, 0
+    syn_all = synthetic
+    while rounds < max_rounds:
+        done = b.done.cpu().numpy()
+        if done.any():
+            tr = b.transcripts()
+            keep = [k for k in range(len(alive)) if not done[k]]
+            for k in range(len(alive)):
+                if done[k]:
+                    out[alive[k]] = tr[k]
+            if not keep:
+                break
+            idx = torch.as_tensor(keep, device=dec.dev, dtype=torch.long)
+            nb = dec.new_batch(b.req[idx].contiguous(), b.budget[idx].cpu().numpy(), b.tcap)
+            for name in ("block", "blen", "budget", "done", "out_len", "transcript"):
+                getattr(nb, name).copy_(getattr(b, name)[idx])
+            if syn_all is not None:
+                syn_all = tuple(t[idx].contiguous() for t in syn_all)
+            alive = [alive[k] for k in keep]
+            b = nb
+        rounds += 1
+        rows += b.n * (dec.K + 1)
+        b.spec_step(rounds, syn_all, graph=False)
+    return out, rounds, rows
