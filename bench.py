@@ -120,6 +120,26 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- multi-rank
+def rank_requests(rank: int, n: int) -> list:
+    """Each rank decodes its own batch of n requests (weak scaling): request
+    ids rank*n .. rank*n+n-1 seed its encoder states."""
+    return [rank * n + i for i in range(n)]
+
+
+def reduce_over_ranks(ms: float, ms_e2e: float, tokens: int, world: int, device):
+    """Whole-job numbers: the slowest rank's times, the sum of tokens."""
+    if world <= 1:
+        return ms, ms_e2e, float(tokens)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    tt = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt)
+    return float(t[0]), float(t[1]), float(tt[0])
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_gpu(args, rank: int, world: int):
     import torch
@@ -137,7 +157,7 @@ def run_gpu(args, rank: int, world: int):
     dec = R.Decoder(s, tw, dw, max_batch=n, max_frames=1500)
     del tw, dw
     req = dec.slots(list(range(n)))
-    As = [synth.encoder_states(s, SEED, rank * n + i) for i in range(n)]
+    As = [synth.encoder_states(s, SEED, r) for r in rank_requests(rank, n)]
     host_enc = torch.from_numpy(np.concatenate([synth.bf16_bits(a) for a in As])).view(torch.int16)
     host_enc = host_enc.pin_memory()
     enc = host_enc.to(dev).view(torch.bfloat16)
@@ -250,16 +270,7 @@ def run_gpu(args, rank: int, world: int):
     v_ms = float(np.mean(vt))
     achieved = vbytes / (v_ms * 1e-3) / 1e9
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
-        tt = torch.tensor([tokens], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt)
-        tokens_all = float(tt[0])
-    else:
-        tokens_all = float(tokens)
+    ms, ms_e2e, tokens_all = reduce_over_ranks(ms, ms_e2e, tokens, world, dev)
     value = tokens_all / (ms * 1e-3)
     e2e_val = tokens_all / (ms_e2e * 1e-3)
     emitted_rounds = np.mean(rounds)
