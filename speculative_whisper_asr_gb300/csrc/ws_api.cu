@@ -56,6 +56,7 @@ struct ws_ctx {
   bool split_ok = false;        // split-K allowed (small-batch contexts)
   int mrows = 0;                // rows of the activation buffers
   TcScratch tcs{};
+  AttnScratch as{};
   struct XMap { const void* base; TcMap bn[5]; };   // activation maps per token-tile width
   std::vector<XMap> xmaps;
   bool pdl = true;              // programmatic dependent launch allowed
@@ -121,7 +122,7 @@ struct Layout {
 
 struct Plan {
   size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
-  size_t tc_part, tc_cnt, tc_part_elems, tc_cnt_n;
+  size_t tc_part, tc_cnt, tc_part_elems, tc_cnt_n, acnt;
   size_t kv_layer_bytes, total;
   int heads, ppr, n_pages, n_xl, max_split;
 };
@@ -159,7 +160,8 @@ Plan make_plan(const ws_model_desc& d) {
   p.ppr = (d.max_pos + WS_PAGE - 1) / WS_PAGE;
   p.n_pages = d.max_batch * p.ppr;
   p.n_xl = d.n_layers + d.drafter_layers;
-  p.max_split = (d.max_frames + WS_XCHUNK - 1) / WS_XCHUNK;
+  // attention splits: acoustic frames, cache positions, history positions + the drafter block
+  p.max_split = std::max((d.max_frames + WS_XCHUNK - 1) / WS_XCHUNK, (d.max_pos + WS_XCHUNK - 1) / WS_XCHUNK + 1);
   const size_t M = (size_t)d.max_batch * d.max_block;
   p.tblob = lay.take(target_elems(d) * es);
   p.dblob = lay.take(drafter_elems(d) * es);
@@ -181,6 +183,7 @@ Plan make_plan(const ws_model_desc& d) {
   p.hist = lay.take((size_t)d.max_batch * d.max_block * nh * D * 4);
   p.amax = lay.take(M * 8);
   p.part = lay.take(M * d.n_heads * p.max_split * (WS_DH + 2) * 4);
+  p.acnt = lay.take((size_t)d.max_batch * d.n_heads * 4);
   p.feat = lay.take(M * nh * D * es);
   p.hpre = lay.take(M * D * 4);
   p.hh = lay.take(M * D * es);
@@ -292,14 +295,13 @@ int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* bloc
   rm.block_len = blen; rm.pend_start = c->pend_start; rm.pend_n = c->pend_n;
   CK(launch_embed_target<T>(n, H, rm, block, (const T*)c->tok_emb, (const T*)c->pos_emb, D, d.vocab, c->x,
                             c->pend_start, c->pend_n, c->status, s, pdl));
-  const int n_split = c->max_fc > 0 ? (c->max_fc + WS_XCHUNK - 1) / WS_XCHUNK : 1;
   for (int l = 0; l < d.n_layers; ++l) {
     const LayerW& w = c->tl[l];
     CK(layernorm<T>(c, M, c->x, w.ln1_g, w.ln1_b, c->h, s));
     Epi e = epi0(c, EPI_QKV);
     e.bias = w.b_q; e.bias2 = w.b_v; e.out = c->q; e.rm = rm; e.kv = pool(c, c->kv, l);
     CK(gemm<T>(c, c->h, c->mrows, w.w_qkv, M, e, s));
-    CK(launch_self_attn<T>(n, H, rm, (const T*)c->q, pool(c, c->kv, l), (T*)c->ao, c->heads, s, pdl));
+    CK(launch_self_attn<T>(n, H, rm, (const T*)c->q, pool(c, c->kv, l), (T*)c->ao, c->heads, c->as, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_o; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ao, c->mrows, w.w_o, M, e, s));
@@ -307,7 +309,7 @@ int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* bloc
     e = epi0(c, EPI_STORE);
     e.bias = w.b_qc; e.out = c->q; e.ldo = D;
     CK(gemm<T>(c, c->h, c->mrows, w.w_qc, M, e, s));
-    CK(launch_cross_attn<T>(n, H, req, c->Fv, (const T*)c->q, xkv_of(c), l, c->part, (T*)c->ao, c->heads, n_split,
+    CK(launch_cross_attn<T>(n, H, req, c->Fv, (const T*)c->q, xkv_of(c), l, (T*)c->ao, c->heads, c->max_fc, c->as,
                             s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_oc; e.resid = c->x; e.ldr = D;
@@ -367,7 +369,6 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
   rd.block_len = nullptr; rd.pend_start = c->pend_start; rd.pend_n = c->pend_n;
   CK(launch_embed_draft<T>(n, K1, req, block, (const T*)c->tok_emb, (const T*)c->mask_emb, D, d.vocab, c->x,
                            c->pend_n, c->status, s, pdl));
-  const int n_split = c->max_fc > 0 ? (c->max_fc + WS_XCHUNK - 1) / WS_XCHUNK : 1;
   for (int l = 0; l < d.drafter_layers; ++l) {
     const LayerW& w = c->dl[l];
     CK(layernorm<T>(c, M, c->x, w.ln1_g, w.ln1_b, c->h, s));
@@ -375,7 +376,7 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
     e.bias = w.b_q; e.bias2 = w.b_v; e.out = c->q; e.kout = c->kb; e.vout = c->vb; e.rm = rd;
     CK(gemm<T>(c, c->h, c->mrows, w.w_qkv, M, e, s));
     CK(launch_draft_attn<T>(n, K1, req, c->L, (const T*)c->q, (const T*)c->kb, (const T*)c->vb,
-                            pool(c, c->hkv, l), (T*)c->ao, c->heads, d.max_pos, s, pdl));
+                            pool(c, c->hkv, l), (T*)c->ao, c->heads, d.max_pos, c->as, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_o; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ao, c->mrows, w.w_o, M, e, s));
@@ -383,8 +384,8 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
     e = epi0(c, EPI_STORE);
     e.bias = w.b_qc; e.out = c->q; e.ldo = D;
     CK(gemm<T>(c, c->h, c->mrows, w.w_qc, M, e, s));
-    CK(launch_cross_attn<T>(n, K1, req, c->Fv, (const T*)c->q, xkv_of(c), d.n_layers + l, c->part, (T*)c->ao,
-                            c->heads, n_split, s, pdl));
+    CK(launch_cross_attn<T>(n, K1, req, c->Fv, (const T*)c->q, xkv_of(c), d.n_layers + l, (T*)c->ao, c->heads,
+                            c->max_fc, c->as, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_oc; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ao, c->mrows, w.w_oc, M, e, s));
@@ -516,6 +517,7 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   c->x = (float*)(b + p.x); c->h = b + p.h; c->q = b + p.q; c->ao = b + p.ao; c->ffn = b + p.ffn;
   c->kb = b + p.kb; c->vb = b + p.vb; c->hist = (float*)(b + p.hist);
   c->amax = (unsigned long long*)(b + p.amax); c->part = (float*)(b + p.part);
+  c->as.part = c->part; c->as.counters = (int*)(b + p.acnt); c->as.status = st + 5 * desc->max_batch;
   c->feat = b + p.feat; c->hpre = (float*)(b + p.hpre); c->hh = b + p.hh;
   c->mrows = desc->max_batch * desc->max_block;
   c->split_ok = c->mrows <= 64;
@@ -552,6 +554,8 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   if (e == cudaSuccess) e = cudaMemsetAsync(c->hist, 0, (size_t)desc->max_batch * desc->max_block *
                                                         (desc->drafter_layers ? desc->n_hist : 0) * D * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->tcs.counters, 0, (size_t)c->tcs.counters_n * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->as.counters, 0, (size_t)desc->max_batch * desc->n_heads * 4, s);
+  if (e == cudaSuccess) e = desc->dtype == WS_BF16 ? attn_init_attributes<bf16>() : attn_init_attributes<float>();
   if (e == cudaSuccess) e = launch_rope_table(c->rope, desc->max_pos, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) { fail(nullptr, WS_ECUDA, "context init: %s", cudaGetErrorString(e)); return cleanup(WS_ECUDA); }

@@ -1,305 +1,340 @@
-// Block-verify attention kernels (decode-shaped: up to 16 query rows per
-// request and head, keys streamed through shared memory in tiles of 32).
+// Decode-shaped attention for block verification and drafting: up to 16
+// query rows per request and head against a key range split into 64-key
+// chunks.
 //
-// Every query row runs its own online softmax over key tiles that start at
-// absolute key 0, with fixed-order warp reductions, so a row's result does
-// not depend on how many other rows share the block (block verification and
-// one-token decoding give bit-identical rows).
+// One CTA owns (request, head, split).  Thread 0 stages the split's keys and
+// values with two bulk asynchronous copies (cp.async.bulk, completing on an
+// mbarrier), so all of the split's bytes are in flight at once; eight warps
+// then run one online softmax per query row over the split from shared
+// memory.  Each split writes a partial (max, sum, 64 weighted values); the
+// CTA that finishes last for a (request, head) folds the partials in split
+// order and writes the head's output.
+//
+// Splits start at absolute key multiples of 64 and every reduction has a
+// fixed order, so a row's result does not depend on how many other rows
+// share the block: verifying a block and decoding one token at a time give
+// bit-identical rows.
 #include "ws_internal.cuh"
 
 namespace {
 
-constexpr int KT = 32;        // keys per tile
-constexpr int MAXR = 16;      // rows per request per CTA
-constexpr int NW = 4;         // warps per CTA
-constexpr int RPW = MAXR / NW;
+constexpr int SPLIT = WS_XCHUNK;   // keys per split (64)
+constexpr int NW = 8;              // warps per CTA
+constexpr int MAXR = 16;           // query rows per request
+constexpr int PART = WS_DH + 2;    // floats per partial
+constexpr long long WAIT_BUDGET = 1ll << 32;
 
-cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, bool pdl, cudaLaunchAttribute* at) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.stream = s;
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cfg;
+enum { MODE_SELF = 0, MODE_CROSS = 1, MODE_DRAFT = 2 };
+
+struct AttnArgs {
+  int H;                     // query rows per request
+  int n_split;               // splits per (request, head); DRAFT: history splits + 1 block split
+  int d, max_pos;
+  const int32_t* req_ids;
+  const int32_t* L;          // cache lengths (SELF: block starts at L; DRAFT: history < L)
+  const int32_t* block_len;  // SELF: valid rows per request
+  const int32_t* Fv;         // CROSS: valid frames per slot
+  const void* Q;             // [n*H, d]
+  KVPool kv;                 // SELF / DRAFT history
+  XKV x; int xlayer;         // CROSS
+  const void* Kb; const void* Vb;   // DRAFT block keys/values [n*H, d]
+  float* part;               // [n*H][heads][n_split][PART]
+  int* counters;             // [n][heads], zero between launches
+  void* O;                   // [n*H, d]
+  int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > WAIT_BUDGET) return false;
+  }
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
 struct RowState { float m, l, a0, a1; };
 
-__device__ __forceinline__ void row_init(RowState& s) { s.m = -INFINITY; s.l = 0.0f; s.a0 = 0.0f; s.a1 = 0.0f; }
-
-// One tile of keys for one row held by a warp.  nvalid = keys of the tile
-// the row may see (prefix of the tile).  q in shared memory [64].
-__device__ __forceinline__ void row_tile(RowState& st, const float* q, const float (*Kt)[WS_DH + 1],
-                                         const float (*Vt)[WS_DH], int nvalid) {
+// One sub-tile of up to 32 keys for one row (warp-wide): scores by lane = key,
+// online-softmax update, then weighted values with lane = pair of dims.
+__device__ __forceinline__ void row_subtile(RowState& st, const float* q, const float (*Kt)[WS_DH + 1],
+                                            const float (*Vt)[WS_DH], int k0, int nvalid, float* pw) {
   const int lane = threadIdx.x & 31;
   float s = -INFINITY;
   if (lane < nvalid) {
-    float acc = 0.0f;
-#pragma unroll 16
-    for (int d = 0; d < WS_DH; ++d) acc = fmaf(q[d], Kt[lane][d], acc);
-    s = acc * 0.125f;                       // 1/sqrt(64)
+    const float* kr = Kt[k0 + lane];
+    float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll
+    for (int d = 0; d < WS_DH; d += 4) {
+      c0 = fmaf(q[d], kr[d], c0);
+      c1 = fmaf(q[d + 1], kr[d + 1], c1);
+      c2 = fmaf(q[d + 2], kr[d + 2], c2);
+      c3 = fmaf(q[d + 3], kr[d + 3], c3);
+    }
+    s = ((c0 + c1) + (c2 + c3)) * 0.125f;          // 1/sqrt(64)
   }
-  const float mt = warp_max(s);
-  const float mn = fmaxf(st.m, mt);
+  const float mn = fmaxf(st.m, warp_max(s));
   const float p = lane < nvalid ? expf(s - mn) : 0.0f;
   const float corr = expf(st.m - mn);
   st.l = st.l * corr + warp_sum(p);
-  float a0 = st.a0 * corr, a1 = st.a1 * corr;
-  for (int k = 0; k < nvalid; ++k) {
-    const float pk = __shfl_sync(0xffffffffu, p, k);
-    const float2 v = *reinterpret_cast<const float2*>(&Vt[k][2 * lane]);
-    a0 = fmaf(pk, v.x, a0);
-    a1 = fmaf(pk, v.y, a1);
+  pw[lane] = p;
+  __syncwarp();
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  int k = 0;
+  for (; k + 1 < nvalid; k += 2) {
+    const float2 v = *reinterpret_cast<const float2*>(&Vt[k0 + k][2 * lane]);
+    const float2 w = *reinterpret_cast<const float2*>(&Vt[k0 + k + 1][2 * lane]);
+    a0 = fmaf(pw[k], v.x, a0); a1 = fmaf(pw[k], v.y, a1);
+    b0 = fmaf(pw[k + 1], w.x, b0); b1 = fmaf(pw[k + 1], w.y, b1);
   }
-  st.a0 = a0; st.a1 = a1; st.m = mn;
+  if (k < nvalid) {
+    const float2 v = *reinterpret_cast<const float2*>(&Vt[k0 + k][2 * lane]);
+    a0 = fmaf(pw[k], v.x, a0); a1 = fmaf(pw[k], v.y, a1);
+  }
+  __syncwarp();
+  st.a0 = st.a0 * corr + (a0 + b0);
+  st.a1 = st.a1 * corr + (a1 + b1);
+  st.m = mn;
 }
 
-template <typename T>
-__device__ __forceinline__ void load_tile(float (*Kt)[WS_DH + 1], float (*Vt)[WS_DH], const T* kp, const T* vp,
-                                          int nkeys) {
-  // kp/vp point at key 0 of the tile, rows of 64 contiguous elements
-  for (int idx = threadIdx.x; idx < KT * WS_DH; idx += NW * 32) {
-    int k = idx / WS_DH, d = idx - k * WS_DH;
-    bool ok = k < nkeys;
-    Kt[k][d] = ok ? to_f<T>(kp[(size_t)k * WS_DH + d]) : 0.0f;
-    Vt[k][d] = ok ? to_f<T>(vp[(size_t)k * WS_DH + d]) : 0.0f;
-  }
-}
+template <typename T, int MODE>
+__global__ void __launch_bounds__(NW * 32) attn_split_kernel(AttnArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_last;
+  T* Kraw = reinterpret_cast<T*>(dsm);
+  T* Vraw = Kraw + SPLIT * WS_DH;
+  float (*Kt)[WS_DH + 1] = reinterpret_cast<float (*)[WS_DH + 1]>(Vraw + SPLIT * WS_DH);
+  float (*Vt)[WS_DH] = reinterpret_cast<float (*)[WS_DH]>(reinterpret_cast<float*>(Kt) + SPLIT * (WS_DH + 1));
+  float (*qs)[WS_DH] = reinterpret_cast<float (*)[WS_DH]>(reinterpret_cast<float*>(Vt) + SPLIT * WS_DH);
+  float* pws = reinterpret_cast<float*>(qs) + MAXR * WS_DH;
 
-// ------------------------------------------------------------------ target self-attention
-// Row j of request i sits at position L + j and sees cache keys 0..L+j
-// (causal; the block's own keys were written by the QKV epilogue).
-template <typename T>
-__global__ void __launch_bounds__(NW * 32) self_attn_kernel(RowMap rm, const T* Q, KVPool kv, T* O, int d) {
-  __shared__ float Kt[KT][WS_DH + 1];
-  __shared__ __align__(16) float Vt[KT][WS_DH];
-  __shared__ float qs[MAXR][WS_DH];
-  pdl_wait();
-  const int i = blockIdx.x, head = blockIdx.y, H = rm.H;
-  const int slot = rm.req_ids[i];
-  const int L = rm.L[slot];
-  const int nrow = min(rm.block_len[i], H);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int idx = threadIdx.x; idx < H * WS_DH; idx += NW * 32) {
-    int j = idx / WS_DH, dd = idx - j * WS_DH;
-    qs[j][dd] = to_f<T>(Q[((size_t)i * H + j) * d + head * WS_DH + dd]);
-  }
-  const int nkeys = min(L + nrow, rm.max_pos);
-  RowState st[RPW];
-#pragma unroll
-  for (int u = 0; u < RPW; ++u) row_init(st[u]);
-  for (int t0 = 0; t0 < nkeys; t0 += KT) {
-    __syncthreads();
-    const int pos0 = t0;   // tiles never straddle a page (WS_PAGE % KT == 0)
-    load_tile<T>(Kt, Vt, kv_ptr<T>(kv, slot, pos0, 0, head), kv_ptr<T>(kv, slot, pos0, 1, head),
-                 min(KT, nkeys - t0));
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < RPW; ++u) {
-      const int j = warp + u * NW;
-      if (j >= nrow) continue;
-      const int nk = min(L + j + 1, rm.max_pos);     // keys visible to this row
-      if (t0 >= nk) continue;
-      row_tile(st[u], qs[j], Kt, Vt, min(KT, nk - t0));
-    }
-  }
-  pdl_trigger();
-#pragma unroll
-  for (int u = 0; u < RPW; ++u) {
-    const int j = warp + u * NW;
-    if (j >= H) continue;
-    float o0 = 0.0f, o1 = 0.0f;
-    if (j < nrow && st[u].l > 0.0f) { o0 = st[u].a0 / st[u].l; o1 = st[u].a1 / st[u].l; }
-    T* o = O + ((size_t)i * H + j) * d + head * WS_DH + 2 * lane;
-    o[0] = from_f<T>(o0);
-    o[1] = from_f<T>(o1);
-  }
-}
-
-// ------------------------------------------------------------------ cross-attention
-// Split s covers frames [s*128, (s+1)*128) of the valid frames; partial
-// (m, l, acc[64]) per (row, head, split), folded in split order afterwards.
-template <typename T>
-__global__ void __launch_bounds__(NW * 32) cross_attn_part_kernel(int H, const int32_t* req_ids, const int32_t* Fv,
-                                                                  const T* Q, XKV x, int layer, float* part,
-                                                                  int d, int n_split) {
-  __shared__ float Kt[KT][WS_DH + 1];
-  __shared__ __align__(16) float Vt[KT][WS_DH];
-  __shared__ float qs[MAXR][WS_DH];
-  pdl_wait();
   const int i = blockIdx.x, head = blockIdx.y, sp = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slot = req_ids[i];
-  const int F = Fv[slot];
-  const int f0 = sp * WS_XCHUNK, f1 = min(F, f0 + WS_XCHUNK);
-  for (int idx = threadIdx.x; idx < H * WS_DH; idx += NW * 32) {
-    int j = idx / WS_DH, dd = idx - j * WS_DH;
-    qs[j][dd] = to_f<T>(Q[((size_t)i * H + j) * d + head * WS_DH + dd]);
+  const int heads = a.d / WS_DH, H = a.H;
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  RowState st[RPW];
-#pragma unroll
-  for (int u = 0; u < RPW; ++u) row_init(st[u]);
-  const T* kb = xkv_ptr<T>(x, slot, layer, 0, head, 0);
-  const T* vb = xkv_ptr<T>(x, slot, layer, 1, head, 0);
-  for (int t0 = f0; t0 < f1; t0 += KT) {
-    __syncthreads();
-    const int nk = min(KT, f1 - t0);
-    load_tile<T>(Kt, Vt, kb + (size_t)t0 * WS_DH, vb + (size_t)t0 * WS_DH, nk);
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < RPW; ++u) {
-      const int j = warp + u * NW;
-      if (j >= H) continue;
-      row_tile(st[u], qs[j], Kt, Vt, nk);
+  __syncthreads();
+  pdl_wait();
+
+  // ---- which keys this split covers, and how many rows may see them
+  const int slot = a.req_ids[i];
+  int k_lo = sp * SPLIT, k_hi = k_lo, nrow = H, Lr = 0;
+  bool block_split = false;
+  if (MODE == MODE_SELF) {
+    Lr = a.L[slot];
+    nrow = min(a.block_len[i], H);
+    k_hi = min(min(Lr + nrow, a.max_pos), k_lo + SPLIT);
+  } else if (MODE == MODE_CROSS) {
+    k_hi = min(a.Fv[slot], k_lo + SPLIT);
+  } else {
+    Lr = min(a.L[slot], a.max_pos);
+    block_split = sp == a.n_split - 1;
+    k_hi = block_split ? k_lo : min(Lr, k_lo + SPLIT);
+  }
+  const int nk = block_split ? H : max(0, k_hi - k_lo);
+
+  // ---- stage keys and values
+  if (nk > 0 && !block_split) {
+    if (threadIdx.x == 0) {
+      const T *ks, *vs;
+      if (MODE == MODE_CROSS) {
+        ks = xkv_ptr<T>(a.x, slot, a.xlayer, 0, head, k_lo);
+        vs = xkv_ptr<T>(a.x, slot, a.xlayer, 1, head, k_lo);
+      } else {
+        ks = kv_ptr<T>(a.kv, slot, k_lo, 0, head);
+        vs = kv_ptr<T>(a.kv, slot, k_lo, 1, head);
+      }
+      const uint32_t bytes = (uint32_t)(nk * WS_DH * sizeof(T));
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&bar)), "r"(2 * bytes)
+                   : "memory");
+      bulk_g2s(Kraw, ks, bytes, &bar);
+      bulk_g2s(Vraw, vs, bytes, &bar);
     }
   }
-  pdl_trigger();
+  const T* Q = reinterpret_cast<const T*>(a.Q);
+  for (int idx = threadIdx.x; idx < H * WS_DH; idx += NW * 32) {
+    const int j = idx / WS_DH, dd = idx - j * WS_DH;
+    qs[j][dd] = to_f<T>(Q[((size_t)i * H + j) * a.d + head * WS_DH + dd]);
+  }
+  bool ok = true;
+  if (nk > 0 && !block_split) ok = mbar_wait(&bar, 0);
+  if (!ok && threadIdx.x == 0) atomicOr(a.status, WS_ST_TIMEOUT);
+  if (nk > 0) {
+    for (int idx = threadIdx.x; idx < nk * WS_DH; idx += NW * 32) {
+      const int k = idx / WS_DH, dd = idx - k * WS_DH;
+      float kv, vv;
+      if (block_split) {
+        kv = to_f<T>(reinterpret_cast<const T*>(a.Kb)[((size_t)i * H + k) * a.d + head * WS_DH + dd]);
+        vv = to_f<T>(reinterpret_cast<const T*>(a.Vb)[((size_t)i * H + k) * a.d + head * WS_DH + dd]);
+      } else {
+        kv = to_f<T>(Kraw[idx]);
+        vv = to_f<T>(Vraw[idx]);
+      }
+      Kt[k][dd] = kv;
+      Vt[k][dd] = vv;
+    }
+  }
+  __syncthreads();
+
+  // ---- one online softmax per row over this split
 #pragma unroll
-  for (int u = 0; u < RPW; ++u) {
+  for (int u = 0; u < MAXR / NW; ++u) {
     const int j = warp + u * NW;
     if (j >= H) continue;
-    float* p = part + ((((size_t)i * H + j) * (d / WS_DH) + head) * n_split + sp) * (WS_DH + 2);
-    if (lane == 0) { p[0] = st[u].m; p[1] = st[u].l; }
-    p[2 + 2 * lane] = st[u].a0;
-    p[3 + 2 * lane] = st[u].a1;
+    RowState st;
+    st.m = -INFINITY; st.l = 0.f; st.a0 = 0.f; st.a1 = 0.f;
+    int visible = nk;                                   // keys of this split row j may see
+    if (MODE == MODE_SELF) visible = (j < nrow) ? max(0, min(k_hi, min(Lr + j + 1, a.max_pos)) - k_lo) : 0;
+    for (int k0 = 0; k0 < visible; k0 += 32)
+      row_subtile(st, qs[j], Kt, Vt, k0, min(32, visible - k0), pws + warp * 32);
+    float* p = a.part + ((((size_t)i * H + j) * heads + head) * a.n_split + sp) * PART;
+    if (lane == 0) { p[0] = st.m; p[1] = st.l; }
+    p[2 + 2 * lane] = st.a0;
+    p[3 + 2 * lane] = st.a1;
   }
-}
 
-template <typename T>
-__global__ void __launch_bounds__(128) cross_attn_combine_kernel(int rows, const float* part, T* O, int d,
-                                                                 int n_split) {
-  pdl_wait();
-  const int heads = d / WS_DH;
-  const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (w >= rows * heads) return;
-  const int r = w / heads, head = w - r * heads;
-  const float* p = part + ((size_t)r * heads + head) * n_split * (WS_DH + 2);
-  float M = -INFINITY;
-  for (int s = 0; s < n_split; ++s) M = fmaxf(M, p[s * (WS_DH + 2)]);
-  float den = 0.0f, n0 = 0.0f, n1 = 0.0f;
-  for (int s = 0; s < n_split; ++s) {
-    const float* q = p + s * (WS_DH + 2);
-    if (q[1] <= 0.0f) continue;
-    const float c = expf(q[0] - M);
-    den = fmaf(q[1], c, den);
-    n0 = fmaf(q[2 + 2 * lane], c, n0);
-    n1 = fmaf(q[3 + 2 * lane], c, n1);
+  // ---- the last split of (request, head) folds the partials in split order
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int* c = a.counters + (size_t)i * heads + head;
+    const int old = atomicAdd(c, 1);
+    s_last = old == a.n_split - 1;
+    if (s_last) *c = 0;
   }
+  __syncthreads();
   pdl_trigger();
-  T* o = O + (size_t)r * d + head * WS_DH + 2 * lane;
-  o[0] = from_f<T>(den > 0.0f ? n0 / den : 0.0f);
-  o[1] = from_f<T>(den > 0.0f ? n1 / den : 0.0f);
-}
-
-// ------------------------------------------------------------------ drafter attention
-// Block rows of request i attend, in one softmax, to the history keys at
-// positions 0..t-1 (t = L, the anchor position) and to all K+1 block keys:
-// bidirectional inside the block (Whisper-Flash §3.2, Appendix A.2).
-template <typename T>
-__global__ void __launch_bounds__(NW * 32) draft_attn_kernel(int K1, const int32_t* req_ids, const int32_t* Lp,
-                                                             const T* Q, const T* Kb, const T* Vb, KVPool hkv, T* O,
-                                                             int d, int max_pos) {
-  __shared__ float Kt[KT][WS_DH + 1];
-  __shared__ __align__(16) float Vt[KT][WS_DH];
-  __shared__ float qs[MAXR][WS_DH];
-  pdl_wait();
-  const int i = blockIdx.x, head = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slot = req_ids[i];
-  const int t = min(Lp[slot], max_pos);
-  for (int idx = threadIdx.x; idx < K1 * WS_DH; idx += NW * 32) {
-    int j = idx / WS_DH, dd = idx - j * WS_DH;
-    qs[j][dd] = to_f<T>(Q[((size_t)i * K1 + j) * d + head * WS_DH + dd]);
-  }
-  RowState st[RPW];
+  if (!s_last) return;
+  __threadfence();
+  T* O = reinterpret_cast<T*>(a.O);
 #pragma unroll
-  for (int u = 0; u < RPW; ++u) row_init(st[u]);
-  for (int t0 = 0; t0 < t; t0 += KT) {
-    __syncthreads();
-    const int nk = min(KT, t - t0);
-    load_tile<T>(Kt, Vt, kv_ptr<T>(hkv, slot, t0, 0, head), kv_ptr<T>(hkv, slot, t0, 1, head), nk);
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < RPW; ++u) {
-      const int j = warp + u * NW;
-      if (j < K1) row_tile(st[u], qs[j], Kt, Vt, nk);
+  for (int u = 0; u < MAXR / NW; ++u) {
+    const int j = warp + u * NW;
+    if (j >= H) continue;
+    const float* p = a.part + (((size_t)i * H + j) * heads + head) * a.n_split * PART;
+    float M = -INFINITY;
+    for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, __ldcg(p + s * PART));
+    float den = 0.f, n0 = 0.f, n1 = 0.f;
+    for (int s = 0; s < a.n_split; ++s) {
+      const float* q = p + s * PART;
+      const float l = __ldcg(q + 1);
+      if (l <= 0.f) continue;
+      const float c = expf(__ldcg(q) - M);
+      den = fmaf(l, c, den);
+      n0 = fmaf(__ldcg(q + 2 + 2 * lane), c, n0);
+      n1 = fmaf(__ldcg(q + 3 + 2 * lane), c, n1);
     }
+    T* o = O + ((size_t)i * H + j) * a.d + head * WS_DH + 2 * lane;
+    o[0] = from_f<T>(den > 0.f ? n0 / den : 0.f);
+    o[1] = from_f<T>(den > 0.f ? n1 / den : 0.f);
   }
-  // the block's own keys (rows of Kb / Vb, one row of d per block row)
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < KT * WS_DH; idx += NW * 32) {
-    int k = idx / WS_DH, dd = idx - k * WS_DH;
-    bool ok = k < K1;
-    Kt[k][dd] = ok ? to_f<T>(Kb[((size_t)i * K1 + k) * d + head * WS_DH + dd]) : 0.0f;
-    Vt[k][dd] = ok ? to_f<T>(Vb[((size_t)i * K1 + k) * d + head * WS_DH + dd]) : 0.0f;
+}
+
+template <typename T>
+constexpr size_t attn_smem() {
+  return 2 * SPLIT * WS_DH * sizeof(T) + SPLIT * (WS_DH + 1) * 4 + SPLIT * WS_DH * 4 + MAXR * WS_DH * 4 +
+         NW * 32 * 4;
+}
+
+template <typename T, int MODE>
+cudaError_t launch_mode(const AttnArgs& a, int n, int heads, cudaStream_t s, bool pdl) {
+  static bool attr = false;
+  constexpr size_t smem = attn_smem<T>();
+  if (!attr) {
+    cudaError_t r = cudaFuncSetAttribute(attn_split_kernel<T, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (r != cudaSuccess) return r;
+    attr = true;
   }
-  __syncthreads();
-#pragma unroll
-  for (int u = 0; u < RPW; ++u) {
-    const int j = warp + u * NW;
-    if (j < K1) row_tile(st[u], qs[j], Kt, Vt, K1);
-  }
-  pdl_trigger();
-#pragma unroll
-  for (int u = 0; u < RPW; ++u) {
-    const int j = warp + u * NW;
-    if (j >= K1) continue;
-    T* o = O + ((size_t)i * K1 + j) * d + head * WS_DH + 2 * lane;
-    o[0] = from_f<T>(st[u].a0 / st[u].l);
-    o[1] = from_f<T>(st[u].a1 / st[u].l);
-  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n, heads, a.n_split);
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&cfg, attn_split_kernel<T, MODE>, a);
 }
 
 }  // namespace
 
 template <typename T>
+cudaError_t attn_init_attributes() {
+  cudaError_t r = cudaSuccess;
+  constexpr int smem = (int)attn_smem<T>();
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_split_kernel<T, MODE_SELF>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_split_kernel<T, MODE_CROSS>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_split_kernel<T, MODE_DRAFT>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return r;
+}
+
+template <typename T>
 cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const KVPool& kv, T* O, int n_heads,
-                             cudaStream_t s, bool pdl) {
+                             const AttnScratch& sc, cudaStream_t s, bool pdl) {
   if (H > MAXR) return cudaErrorInvalidValue;
-  cudaLaunchAttribute at[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(n, n_heads), dim3(NW * 32), s, pdl, at);
-  ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg, self_attn_kernel<T>, rm, Q, kv, O, n_heads * WS_DH);
+  AttnArgs a = {};
+  a.H = H; a.d = n_heads * WS_DH; a.max_pos = rm.max_pos;
+  a.n_split = (rm.max_pos + SPLIT - 1) / SPLIT;
+  a.req_ids = rm.req_ids; a.L = rm.L; a.block_len = rm.block_len;
+  a.Q = Q; a.kv = kv; a.part = sc.part; a.counters = sc.counters; a.O = O; a.status = sc.status;
+  return launch_mode<T, MODE_SELF>(a, n, n_heads, s, pdl);
 }
 
 template <typename T>
 cudaError_t launch_cross_attn(int n, int H, const int32_t* req_ids, const int32_t* Fv, const T* Q, const XKV& x,
-                              int layer, float* part, T* O, int n_heads, int n_split, cudaStream_t s, bool pdl) {
+                              int layer, T* O, int n_heads, int max_frames_seen, const AttnScratch& sc,
+                              cudaStream_t s, bool pdl) {
   if (H > MAXR) return cudaErrorInvalidValue;
-  cudaLaunchAttribute at[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(n, n_heads, n_split), dim3(NW * 32), s, pdl, at);
-  ws_count_launches(1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, cross_attn_part_kernel<T>, H, req_ids, Fv, Q, x, layer, part,
-                                     n_heads * WS_DH, n_split);
-  if (e != cudaSuccess) return e;
-  const int rows = n * H;
-  cudaLaunchConfig_t cfg2 = make_cfg(dim3((rows * n_heads + 3) / 4), dim3(128), s, pdl, at);
-  ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg2, cross_attn_combine_kernel<T>, rows, (const float*)part, O, n_heads * WS_DH,
-                            n_split);
+  AttnArgs a = {};
+  a.H = H; a.d = n_heads * WS_DH;
+  a.n_split = max(1, (max_frames_seen + SPLIT - 1) / SPLIT);
+  a.req_ids = req_ids; a.Fv = Fv; a.Q = Q; a.x = x; a.xlayer = layer;
+  a.part = sc.part; a.counters = sc.counters; a.O = O; a.status = sc.status;
+  return launch_mode<T, MODE_CROSS>(a, n, n_heads, s, pdl);
 }
 
 template <typename T>
 cudaError_t launch_draft_attn(int n, int K1, const int32_t* req_ids, const int32_t* L, const T* Q, const T* Kb,
-                              const T* Vb, const KVPool& hkv, T* O, int n_heads, int max_pos, cudaStream_t s,
-                              bool pdl) {
+                              const T* Vb, const KVPool& hkv, T* O, int n_heads, int max_pos,
+                              const AttnScratch& sc, cudaStream_t s, bool pdl) {
   if (K1 > MAXR) return cudaErrorInvalidValue;
-  cudaLaunchAttribute at[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(n, n_heads), dim3(NW * 32), s, pdl, at);
-  ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg, draft_attn_kernel<T>, K1, req_ids, L, Q, Kb, Vb, hkv, O, n_heads * WS_DH,
-                            max_pos);
+  AttnArgs a = {};
+  a.H = K1; a.d = n_heads * WS_DH; a.max_pos = max_pos;
+  a.n_split = (max_pos + SPLIT - 1) / SPLIT + 1;
+  a.req_ids = req_ids; a.L = L; a.Q = Q; a.kv = hkv; a.Kb = Kb; a.Vb = Vb;
+  a.part = sc.part; a.counters = sc.counters; a.O = O; a.status = sc.status;
+  return launch_mode<T, MODE_DRAFT>(a, n, n_heads, s, pdl);
 }
 
 #define INST(T)                                                                                                  \
+  template cudaError_t attn_init_attributes<T>();                                                               \
   template cudaError_t launch_self_attn<T>(int, int, const RowMap&, const T*, const KVPool&, T*, int,            \
-                                           cudaStream_t, bool);                                                   \
+                                           const AttnScratch&, cudaStream_t, bool);                              \
   template cudaError_t launch_cross_attn<T>(int, int, const int32_t*, const int32_t*, const T*, const XKV&, int, \
-                                            float*, T*, int, int, cudaStream_t, bool);                            \
+                                            T*, int, int, const AttnScratch&, cudaStream_t, bool);               \
   template cudaError_t launch_draft_attn<T>(int, int, const int32_t*, const int32_t*, const T*, const T*,        \
-                                            const T*, const KVPool&, T*, int, int, cudaStream_t, bool);
+                                            const T*, const KVPool&, T*, int, int, const AttnScratch&,           \
+                                            cudaStream_t, bool);
 INST(float)
 INST(bf16)

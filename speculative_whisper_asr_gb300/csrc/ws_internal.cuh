@@ -12,8 +12,7 @@ typedef __nv_bfloat16 bf16;
 
 #define WS_DH 64          // head width (Whisper: d_model / n_heads = 64)
 #define WS_PAGE 64        // tokens per KV-cache page
-#define WS_XCHUNK 128     // encoder frames per cross-attention split
-#define WS_MAX_SPLIT 12   // ceil(1500 / WS_XCHUNK)
+#define WS_XCHUNK 64      // keys (frames, cache positions) per attention split
 
 // Device status bits (ws_status).
 #define WS_ST_POS 1       // a position at or beyond max_pos was requested
@@ -201,6 +200,13 @@ struct GemmShape {
 
 template <typename T> cudaError_t launch_gemm_simt(const GemmShape& g, const Epi& e, cudaStream_t s, bool pdl);
 
+// Attention partials and the per-(request, head) arrival counters.
+struct AttnScratch {
+  float* part;            // [rows][heads][splits][66]
+  int* counters;          // [max_batch][heads], zero between launches
+  int32_t* status;
+};
+
 // tcgen05 engine (ws_gemm_tc.cu).  TcMap holds an encoded TMA tensor map.
 struct alignas(64) TcMap { unsigned char bytes[128]; };
 struct TcScratch {
@@ -242,15 +248,17 @@ cudaError_t launch_hist_gather(int n, int Hp, const int32_t* req_ids, const int3
                                cudaStream_t s, bool pdl);
 template <typename T>
 cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const KVPool& kv, T* O,
-                             int n_heads, cudaStream_t s, bool pdl);
+                             int n_heads, const AttnScratch& sc, cudaStream_t s, bool pdl);
 template <typename T>
 cudaError_t launch_draft_attn(int n, int K1, const int32_t* req_ids, const int32_t* L, const T* Q,
                               const T* Kb, const T* Vb, const KVPool& hkv, T* O, int n_heads,
-                              int max_pos, cudaStream_t s, bool pdl);
+                              int max_pos, const AttnScratch& sc, cudaStream_t s, bool pdl);
 template <typename T>
 cudaError_t launch_cross_attn(int n, int H, const int32_t* req_ids, const int32_t* Fv, const T* Q,
-                              const XKV& x, int layer, float* part, T* O, int n_heads, int n_split,
-                              cudaStream_t s, bool pdl);
+                              const XKV& x, int layer, T* O, int n_heads, int max_frames_seen,
+                              const AttnScratch& sc, cudaStream_t s, bool pdl);
+template <typename T>
+cudaError_t attn_init_attributes();
 cudaError_t launch_rope_table(float* tab, int max_pos, cudaStream_t s);
 cudaError_t launch_set_frames(int n, const int32_t* req_ids, const int32_t* cu, const int32_t* valid,
                               int max_frames, int32_t* Fc, int32_t* Fv, int32_t* status, cudaStream_t s);
