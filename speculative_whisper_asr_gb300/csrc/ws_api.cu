@@ -55,7 +55,6 @@ struct ws_ctx {
   int engine = WS_GEMM_SIMT;
   bool split_ok = false;        // split-K allowed (small-batch contexts)
   int mrows = 0;                // rows of the activation buffers
-  TcScratch tcs{};
   AttnScratch as{};
   struct XMap { const void* base; TcMap bn[5]; };   // activation maps per token-tile width
   std::vector<XMap> xmaps;
@@ -122,7 +121,7 @@ struct Layout {
 
 struct Plan {
   size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
-  size_t tc_part, tc_cnt, tc_part_elems, tc_cnt_n, acnt;
+  size_t acnt;
   size_t kv_layer_bytes, total;
   int heads, ppr, n_pages, n_xl, max_split;
 };
@@ -187,13 +186,6 @@ Plan make_plan(const ws_model_desc& d) {
   p.feat = lay.take(M * nh * D * es);
   p.hpre = lay.take(M * D * 4);
   p.hh = lay.take(M * D * es);
-  // split-K partials of the tcgen05 engine (small-batch contexts only):
-  // tiles(<= ceil(max N / 128)) x splits(<= 16) x BN(<= 64) x 128 fp32
-  const size_t maxN = std::max<size_t>(std::max<size_t>(3 * D, d.d_ff), 2 * D);
-  p.tc_cnt_n = (maxN + 127) / 128 + 64;
-  p.tc_part_elems = (M <= 64) ? p.tc_cnt_n * 16 * 64 * 128 : 0;
-  p.tc_part = lay.take(p.tc_part_elems * 4);
-  p.tc_cnt = lay.take(p.tc_cnt_n * 4);
   p.total = lay.off;
   return p;
 }
@@ -249,7 +241,7 @@ int splits_for(const ws_ctx* c, int N, int K) {
   if (tiles >= 100) return 1;
   int s = (148 + tiles - 1) / tiles;
   s = std::min(s, std::max(1, kb / 2));
-  return std::max(1, std::min(s, 16));
+  return std::max(1, std::min(s, 8));       // one portable thread-block cluster per tile
 }
 
 // Y = X W^T with a fused epilogue.  X has x_rows allocated rows.
@@ -263,7 +255,7 @@ cudaError_t gemm(ws_ctx* c, const void* X, uint64_t x_rows, const Mat& W, int M,
     const TcMap* mx = nullptr;
     for (const auto& xm : c->xmaps)
       if (xm.base == X) { mx = &xm.bn[tc_bn_index(tc_pick_bn(M))]; break; }
-    return launch_gemm_tc(g, e, W.map, mx, X, x_rows, allow_split ? splits_for(c, g.N, g.K) : 1, c->tcs, s,
+    return launch_gemm_tc(g, e, W.map, mx, X, x_rows, allow_split ? splits_for(c, g.N, g.K) : 1, s,
                           c->cur_pdl);
   }
   return launch_gemm_simt<T>(g, e, s, c->cur_pdl);
@@ -271,7 +263,20 @@ cudaError_t gemm(ws_ctx* c, const void* X, uint64_t x_rows, const Mat& W, int M,
 
 template <typename T>
 cudaError_t layernorm(ws_ctx* c, int M, const float* x, const void* g, const void* b, void* y,
-                      cudaStream_t s, int group_skip = 0) {
+                      cudaStream_t s, int group_skip = 0);
+
+// Y = LayerNorm(x) W^T: a layer-norm kernel writes c->h, the GEMM reads it.
+template <typename T>
+cudaError_t ln_gemm(ws_ctx* c, int M, const float* x, const void* g, const void* b, const Mat& W, const Epi& e,
+                    cudaStream_t s, int group_skip = 0) {
+  cudaError_t r = layernorm<T>(c, M, x, g, b, c->h, s, group_skip);
+  if (r != cudaSuccess) return r;
+  return gemm<T>(c, c->h, c->mrows, W, M, e, s);
+}
+
+template <typename T>
+cudaError_t layernorm(ws_ctx* c, int M, const float* x, const void* g, const void* b, void* y,
+                      cudaStream_t s, int group_skip) {
   const int D = c->d.d_model;
   return launch_layernorm<T>(M, D, x, D, (const T*)g, (const T*)b, (T*)y, D, group_skip, s, c->cur_pdl);
 }
@@ -297,27 +302,24 @@ int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* bloc
                             c->pend_start, c->pend_n, c->status, s, pdl));
   for (int l = 0; l < d.n_layers; ++l) {
     const LayerW& w = c->tl[l];
-    CK(layernorm<T>(c, M, c->x, w.ln1_g, w.ln1_b, c->h, s));
     Epi e = epi0(c, EPI_QKV);
     e.bias = w.b_q; e.bias2 = w.b_v; e.out = c->q; e.rm = rm; e.kv = pool(c, c->kv, l);
-    CK(gemm<T>(c, c->h, c->mrows, w.w_qkv, M, e, s));
+    CK(ln_gemm<T>(c, M, c->x, w.ln1_g, w.ln1_b, w.w_qkv, e, s));
     CK(launch_self_attn<T>(n, H, rm, (const T*)c->q, pool(c, c->kv, l), (T*)c->ao, c->heads, c->as, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_o; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ao, c->mrows, w.w_o, M, e, s));
-    CK(layernorm<T>(c, M, c->x, w.ln2_g, w.ln2_b, c->h, s));
     e = epi0(c, EPI_STORE);
     e.bias = w.b_qc; e.out = c->q; e.ldo = D;
-    CK(gemm<T>(c, c->h, c->mrows, w.w_qc, M, e, s));
+    CK(ln_gemm<T>(c, M, c->x, w.ln2_g, w.ln2_b, w.w_qc, e, s));
     CK(launch_cross_attn<T>(n, H, req, c->Fv, (const T*)c->q, xkv_of(c), l, (T*)c->ao, c->heads, c->max_fc, c->as,
                             s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_oc; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ao, c->mrows, w.w_oc, M, e, s));
-    CK(layernorm<T>(c, M, c->x, w.ln3_g, w.ln3_b, c->h, s));
     e = epi0(c, EPI_GELU);
     e.bias = w.b_fc1; e.out = c->ffn; e.ldo = d.d_ff;
-    CK(gemm<T>(c, c->h, c->mrows, w.w_fc1, M, e, s));
+    CK(ln_gemm<T>(c, M, c->x, w.ln3_g, w.ln3_b, w.w_fc1, e, s));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_fc2; e.resid = c->x; e.ldr = D;
     int hidx;
@@ -326,11 +328,10 @@ int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* bloc
     }
     CK(gemm<T>(c, c->ffn, c->mrows, w.w_fc2, M, e, s));
   }
-  CK(layernorm<T>(c, M, c->x, c->lnf_g, c->lnf_b, c->h, s));
   CK(launch_argmax_init(M, c->amax, s, pdl));
   Epi e = epi0(c, EPI_LOGITS);
   e.logits = logits; e.ldl = d.vocab; e.amax = c->amax;
-  CK(gemm<T>(c, c->h, c->mrows, c->head, M, e, s));
+  CK(ln_gemm<T>(c, M, c->x, c->lnf_g, c->lnf_b, c->head, e, s));
   CK(launch_argmax_finalize(n, H, blen, c->amax, target, H, 0, s, pdl));
   if (d.drafter_layers > 0) c->pending_H = H > c->pending_H ? H : c->pending_H;
   return WS_OK;
@@ -371,44 +372,40 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
                            c->pend_n, c->status, s, pdl));
   for (int l = 0; l < d.drafter_layers; ++l) {
     const LayerW& w = c->dl[l];
-    CK(layernorm<T>(c, M, c->x, w.ln1_g, w.ln1_b, c->h, s));
     Epi e = epi0(c, EPI_QKV_DRAFT);
     e.bias = w.b_q; e.bias2 = w.b_v; e.out = c->q; e.kout = c->kb; e.vout = c->vb; e.rm = rd;
-    CK(gemm<T>(c, c->h, c->mrows, w.w_qkv, M, e, s));
+    CK(ln_gemm<T>(c, M, c->x, w.ln1_g, w.ln1_b, w.w_qkv, e, s));
     CK(launch_draft_attn<T>(n, K1, req, c->L, (const T*)c->q, (const T*)c->kb, (const T*)c->vb,
                             pool(c, c->hkv, l), (T*)c->ao, c->heads, d.max_pos, c->as, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_o; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ao, c->mrows, w.w_o, M, e, s));
-    CK(layernorm<T>(c, M, c->x, w.ln2_g, w.ln2_b, c->h, s));
     e = epi0(c, EPI_STORE);
     e.bias = w.b_qc; e.out = c->q; e.ldo = D;
-    CK(gemm<T>(c, c->h, c->mrows, w.w_qc, M, e, s));
+    CK(ln_gemm<T>(c, M, c->x, w.ln2_g, w.ln2_b, w.w_qc, e, s));
     CK(launch_cross_attn<T>(n, K1, req, c->Fv, (const T*)c->q, xkv_of(c), d.n_layers + l, (T*)c->ao, c->heads,
                             c->max_fc, c->as, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_oc; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ao, c->mrows, w.w_oc, M, e, s));
-    CK(layernorm<T>(c, M, c->x, w.ln3_g, w.ln3_b, c->h, s));
     e = epi0(c, EPI_GELU);
     e.bias = w.b_fc1; e.out = c->ffn; e.ldo = d.d_ff;
-    CK(gemm<T>(c, c->h, c->mrows, w.w_fc1, M, e, s));
+    CK(ln_gemm<T>(c, M, c->x, w.ln3_g, w.ln3_b, w.w_fc1, e, s));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_fc2; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ffn, c->mrows, w.w_fc2, M, e, s));
   }
   // 3) final LN on the K mask rows, shared LM head, argmax or sampling
   const int Mk = n * K;
-  CK(layernorm<T>(c, Mk, c->x, c->dlnf_g, c->dlnf_b, c->h, s, K1));
   Epi e = epi0(c, EPI_LOGITS);
   e.logits = q_logits; e.ldl = d.vocab;
   if (temp <= 0.0f) {
     CK(launch_argmax_init(Mk, c->amax, s, pdl));
     e.amax = c->amax;
-    CK(gemm<T>(c, c->h, c->mrows, c->head, Mk, e, s));
+    CK(ln_gemm<T>(c, Mk, c->x, c->dlnf_g, c->dlnf_b, c->head, e, s, K1));
     CK(launch_argmax_finalize(n, K, nullptr, c->amax, block, K1, 1, s, pdl));
   } else {
-    CK(gemm<T>(c, c->h, c->mrows, c->head, Mk, e, s));
+    CK(ln_gemm<T>(c, Mk, c->x, c->dlnf_g, c->dlnf_b, c->head, e, s, K1));
     CK(launch_sample_rows(n, K, req, q_logits, d.vocab, d.vocab, temp, seed, rnd, c->suppress, block, K1, 1, s,
                           pdl));
   }
@@ -521,8 +518,6 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   c->feat = b + p.feat; c->hpre = (float*)(b + p.hpre); c->hh = b + p.hh;
   c->mrows = desc->max_batch * desc->max_block;
   c->split_ok = c->mrows <= 64;
-  c->tcs.part = (float*)(b + p.tc_part); c->tcs.part_elems = p.tc_part_elems;
-  c->tcs.counters = (int*)(b + p.tc_cnt); c->tcs.counters_n = (int)p.tc_cnt_n;
   if (c->engine == WS_GEMM_TC) {
     bool ok = true;
     auto enc = [&](Mat& m) { ok = ok && tc_encode_map(&m.map, m.p, (uint64_t)m.rows, (uint64_t)m.cols, 128); };
@@ -553,7 +548,6 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   if (e == cudaSuccess) e = cudaMemsetAsync(st, 0, (size_t)desc->max_batch * 5 * 4 + 256, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->hist, 0, (size_t)desc->max_batch * desc->max_block *
                                                         (desc->drafter_layers ? desc->n_hist : 0) * D * 4, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(c->tcs.counters, 0, (size_t)c->tcs.counters_n * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->as.counters, 0, (size_t)desc->max_batch * desc->n_heads * 4, s);
   if (e == cudaSuccess) e = desc->dtype == WS_BF16 ? attn_init_attributes<bf16>() : attn_init_attributes<float>();
   if (e == cudaSuccess) e = launch_rope_table(c->rope, desc->max_pos, s);

@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AttnArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  pdl_trigger();        // the next kernel may launch and run its prologue now
   pdl_wait();
 
   // ---- which keys this split covers, and how many rows may see them
@@ -217,7 +218,6 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AttnArgs a) {
     if (s_last) *c = 0;
   }
   __syncthreads();
-  pdl_trigger();
   if (!s_last) return;
   __threadfence();
   T* O = reinterpret_cast<T*>(a.O);

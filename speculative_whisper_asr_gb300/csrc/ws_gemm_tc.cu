@@ -14,15 +14,19 @@
 // handful of tokens still fills the MMA M dimension and each token is one
 // column: every output element accumulates its k-blocks in the same order
 // whatever the number of tokens.  Split-K (fixed per weight shape, never per
-// token count) spreads small-M GEMMs over the SMs; the last CTA of a tile
-// adds the fp32 partials in split order.
+// token count) spreads small-M GEMMs over the SMs: the splits of a tile form
+// one thread-block cluster and rank 0 adds the fp32 partials in split order
+// through distributed shared memory.
 //
-// The weight TMA loads of the first ring slots are issued before
-// griddepcontrol.wait, so under programmatic dependent launch they overlap the
-// previous kernel's tail.  Every mbarrier wait is bounded (clock budget); a
-// timeout sets a device status bit instead of hanging.
+// Each kernel releases its dependents (programmatic dependent launch) right
+// after its prologue, and issues the weight TMA loads of the first ring slots
+// before griddepcontrol.wait, so the next GEMM's weight stream overlaps the
+// current kernel.  Every mbarrier wait is bounded (clock budget); a timeout
+// sets a device status bit instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <cooperative_groups.h>
 
 #include <mutex>
 
@@ -130,8 +134,6 @@ struct TcParams {
   int kb_total;          // K / BK
   int splits;            // split-K factor (grid.x = tiles_f * splits)
   int tiles_f, tiles_t;
-  float* part;           // [tile][split][BN][BM] partial sums (splits > 1)
-  int* counters;         // [tile] arrival counters, left at zero
   int32_t* status;
 };
 
@@ -184,7 +186,6 @@ __global__ void __launch_bounds__(128, 1)
   extern __shared__ __align__(1024) uint8_t dsm[];
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
   __shared__ uint32_t tmem_base;
-  __shared__ int s_abort, s_last;
 
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -197,7 +198,6 @@ __global__ void __launch_bounds__(128, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     mbar_init(&done, 1);
-    s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
@@ -207,6 +207,9 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  // Let the next kernel launch now: its prologue and weight prefetch overlap
+  // this kernel (it still waits for our completion before reading outputs).
+  pdl_trigger();
 
   // Row count: a host value, except for the acoustic K/V GEMM whose per-request
   // frame ranges live in device memory (read only after the dependency wait).
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(128, 1)
     for (int i = npre; i < nkb; ++i) {
       const int s = i % STAGES;
       const uint32_t ph = (uint32_t)((i / STAGES) & 1);
-      if (!mbar_wait(&empty[s], ph ^ 1u)) { s_abort = 1; atomicOr(p.status, 8); break; }
+      if (!mbar_wait(&empty[s], ph ^ 1u)) { atomicOr(p.status, WS_ST_TIMEOUT); break; }
       mbar_expect_tx(&full[s], STAGE_BYTES);
       uint8_t* st = ring + s * STAGE_BYTES;
       tma_load_2d(st, &tmW, &full[s], (kb0 + i) * BK, f0);
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(128, 1)
     for (int i = 0; i < nkb; ++i) {
       const int s = i % STAGES;
       const uint32_t ph = (uint32_t)((i / STAGES) & 1);
-      if (!mbar_wait(&full[s], ph)) { s_abort = 1; atomicOr(p.status, 8); break; }
+      if (!mbar_wait(&full[s], ph)) { atomicOr(p.status, WS_ST_TIMEOUT); break; }
       tc_fence_after();
       const uint32_t a = smem_u32(ring + s * STAGE_BYTES), b = a + A_BYTES;
       const uint64_t ad = sdesc_sw128(a), bd = sdesc_sw128(b);
@@ -267,61 +270,53 @@ __global__ void __launch_bounds__(128, 1)
   }
   ok = __syncthreads_and(ok) != 0;      // CTA-uniform before any further barrier
   tc_fence_after();
-  pdl_trigger();
 
-  if (active && ok) {
-    const int row = warp * 32 + lane;          // TMEM lane == weight row of the tile
-    const int n = f0 + row;
-    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-    if (p.splits == 1) {
+  const int row = warp * 32 + lane;            // TMEM lane == weight row of the tile
+  const int n = f0 + row;
+  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  if (active && p.splits == 1 && ok) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      float v[16];
+      tmem_ld16(taddr + (uint32_t)c0, v);
+      epilogue16<BN>(e, p, t0, c0, n, M, z, v);
+    }
+  } else if (active && p.splits > 1) {
+    // Split-K: the splits of one tile form a thread-block cluster.  Each CTA
+    // parks its fp32 partial in its own (now idle) ring memory; rank 0 reads
+    // the others through distributed shared memory and adds them in split
+    // order 0, 1, 2, ...  Every CTA of an active cluster reaches both cluster
+    // barriers, also after a timed-out wait.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    float* mine = reinterpret_cast<float*>(ring);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      float v[16];
+      if (ok) tmem_ld16(taddr + (uint32_t)c0, v);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) mine[(c0 + c) * BM + row] = ok ? v[c] : 0.0f;
+    }
+    cl.sync();
+    if (cl.block_rank() == 0) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
-        tmem_ld16(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] = mine[(c0 + c) * BM + row];
+#pragma unroll 1
+        for (int r = 1; r < p.splits; ++r) {
+          const float* rem = cl.map_shared_rank(mine, r);
+          float w[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) w[c] = rem[(c0 + c) * BM + row];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] += w[c];
+        }
         epilogue16<BN>(e, p, t0, c0, n, M, z, v);
       }
-    } else {
-      const int tile = (z * p.tiles_t + blockIdx.y) * p.tiles_f + tile_f;
-      float* mine = p.part + ((size_t)tile * p.splits + split) * BN * BM;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        tmem_ld16(taddr + (uint32_t)c0, v);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) mine[(size_t)(c0 + c) * BM + row] = v[c];
-      }
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const int old = atomicAdd(p.counters + tile, 1);
-        s_last = old == p.splits - 1;
-        if (s_last) p.counters[tile] = 0;
-      }
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        const float* base = p.part + (size_t)tile * p.splits * BN * BM;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          // splits outer, columns inner: the 16 loads of one split are
-          // independent and in flight together; the per-element order of
-          // the additions is still split 0, 1, 2, ...
-          float v[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] = 0.0f;
-#pragma unroll 1
-          for (int s = 0; s < p.splits; ++s) {
-            float w[16];
-            const float* src = base + ((size_t)s * BN + c0) * BM + row;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) w[c] = __ldcg(src + (size_t)c * BM);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] += w[c];
-          }
-          epilogue16<BN>(e, p, t0, c0, n, M, z, v);
-        }
-      }
     }
+    cl.sync();
   }
   tc_fence_before();
   __syncthreads();
@@ -332,19 +327,35 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 
 template <int BN, int STAGES>
+constexpr int tc_smem() {
+  return STAGES * (A_BYTES + BN * BK * 2) + 1024;
+}
+
+template <int BN, int STAGES>
 cudaError_t launch_bn(const GemmShape& g, const Epi& e, const CUtensorMap& mw, const CUtensorMap& mx,
                       const TcParams& p, cudaStream_t s, bool pdl) {
-  constexpr int smem = STAGES * (A_BYTES + BN * BK * 2) + 1024;
+  constexpr int smem = tc_smem<BN, STAGES>();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.tiles_f * p.splits, p.tiles_t, g.batch > 0 ? g.batch : 1);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (pdl) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (p.splits > 1) {      // the splits of a tile are one cluster
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = p.splits;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = at;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES>, mw, mx, p, e);
 }
@@ -384,16 +395,14 @@ bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uin
 // any launch (so no attribute call happens while a stream is being captured).
 cudaError_t tc_init_attributes() {
   cudaError_t r = cudaSuccess;
-  auto set = [&](const void* fn, int bn, int stages) {
-    if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               stages * (A_BYTES + bn * BK * 2) + 1024);
+  auto set = [&](const void* fn, int bytes) {
+    if (r == cudaSuccess) r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   };
-  set((const void*)gemm_tc_kernel<16, 6>, 16, 6);
-  set((const void*)gemm_tc_kernel<32, 5>, 32, 5);
-  set((const void*)gemm_tc_kernel<64, 4>, 64, 4);
-  set((const void*)gemm_tc_kernel<128, 3>, 128, 3);
-  set((const void*)gemm_tc_kernel<256, 4>, 256, 4);
+  set((const void*)gemm_tc_kernel<16, 6>, tc_smem<16, 6>());
+  set((const void*)gemm_tc_kernel<32, 5>, tc_smem<32, 5>());
+  set((const void*)gemm_tc_kernel<64, 4>, tc_smem<64, 4>());
+  set((const void*)gemm_tc_kernel<128, 3>, tc_smem<128, 3>());
+  set((const void*)gemm_tc_kernel<256, 4>, tc_smem<256, 4>());
   return r;
 }
 
@@ -408,7 +417,7 @@ int tc_pick_bn(int M) {
 }
 
 cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const TcMap* mx_cached,
-                           const void* x_base, uint64_t x_rows, int splits, const TcScratch& scr, cudaStream_t s,
+                           const void* x_base, uint64_t x_rows, int splits, cudaStream_t s,
                            bool pdl) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
   if (g.K % BK != 0 || g.ldx != g.K) return cudaErrorInvalidValue;
@@ -416,20 +425,15 @@ cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, co
   TcMap mx;
   if (mx_cached) mx = *mx_cached;
   else if (!tc_encode_map(&mx, x_base, x_rows, (uint64_t)g.K, (uint32_t)BN)) return cudaErrorInvalidValue;
-  TcParams p;
+  TcParams p = {};
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.kb_total = g.K / BK;
   p.splits = splits < 1 ? 1 : (splits > p.kb_total ? p.kb_total : splits);
   p.tiles_f = (g.N + BM - 1) / BM;
   p.tiles_t = (g.M + BN - 1) / BN;
-  p.part = scr.part;
-  p.counters = scr.counters;
   p.status = e.status;
-  if (p.splits > 1) {
-    const size_t need = (size_t)p.tiles_f * p.tiles_t * (g.batch > 0 ? g.batch : 1) * p.splits * BN * BM;
-    const size_t tiles = (size_t)p.tiles_f * p.tiles_t * (g.batch > 0 ? g.batch : 1);
-    if (need > scr.part_elems || tiles > (size_t)scr.counters_n) return cudaErrorInvalidValue;
-  }
+  // split-K partials live in the ring of each CTA of the cluster: BN <= 64 tokens
+  if (p.splits > 1 && BN > 64) p.splits = 1;
   const CUtensorMap& W = *reinterpret_cast<const CUtensorMap*>(&mw);
   const CUtensorMap& X = *reinterpret_cast<const CUtensorMap*>(&mx);
   switch (BN) {

@@ -82,6 +82,62 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// ------------------------------------------------------------------ layer norm of one row
+// One warp normalises one row of d fp32 values (d a multiple of 128, <= 2048):
+// lane l owns the float4 groups at 4*l + 128*i.  Mean and variance are
+// per-lane sequential sums followed by a fixed shuffle tree, so a row's
+// values never depend on which other rows share the launch.  out(k, ...)
+// receives the four normalised values of group k.
+template <class Out>
+__device__ __forceinline__ void ln_row_warp(const float* x, int d, const void* g, const void* b, bool g_bf16,
+                                            Out out) {
+  const int lane = threadIdx.x & 31;
+  const int nv = d >> 7;
+  float4 v[16];
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (i < nv) {
+      v[i] = *reinterpret_cast<const float4*>(x + 4 * lane + 128 * i);
+      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+  }
+  const float mean = warp_sum(s) / (float)d;
+  float q = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (i < nv) {
+      const float a = v[i].x - mean, bb = v[i].y - mean, c = v[i].z - mean, e = v[i].w - mean;
+      q += (a * a + bb * bb) + (c * c + e * e);
+    }
+  }
+  const float rstd = rsqrtf(warp_sum(q) / (float)d + 1e-5f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (i < nv) {
+      const int k = 4 * lane + 128 * i;
+      float gg[4], bv[4];
+      if (g_bf16) {
+        const uint2 gq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(g) + k);
+        const uint2 bq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(b) + k);
+        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.x));
+        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.y));
+        const float2 b01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.x));
+        const float2 b23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.y));
+        gg[0] = g01.x; gg[1] = g01.y; gg[2] = g23.x; gg[3] = g23.y;
+        bv[0] = b01.x; bv[1] = b01.y; bv[2] = b23.x; bv[3] = b23.y;
+      } else {
+        const float4 gq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + k);
+        const float4 bq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(b) + k);
+        gg[0] = gq.x; gg[1] = gq.y; gg[2] = gq.z; gg[3] = gq.w;
+        bv[0] = bq.x; bv[1] = bq.y; bv[2] = bq.z; bv[3] = bq.w;
+      }
+      out(k, (v[i].x - mean) * rstd * gg[0] + bv[0], (v[i].y - mean) * rstd * gg[1] + bv[1],
+          (v[i].z - mean) * rstd * gg[2] + bv[2], (v[i].w - mean) * rstd * gg[3] + bv[3]);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ PDL
 // Programmatic dependent launch: a kernel may start while its predecessor on
 // the stream drains; it must wait before touching the predecessor's outputs.
@@ -209,12 +265,6 @@ struct AttnScratch {
 
 // tcgen05 engine (ws_gemm_tc.cu).  TcMap holds an encoded TMA tensor map.
 struct alignas(64) TcMap { unsigned char bytes[128]; };
-struct TcScratch {
-  float* part;            // split-K partials
-  size_t part_elems;
-  int* counters;          // per-tile arrival counters (zero between launches)
-  int counters_n;
-};
 bool tc_engine_available();
 bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 int tc_pick_bn(int M);
@@ -222,7 +272,7 @@ int tc_pick_bn(int M);
 // mx_cached: the activation map for this call's token tile (tc_pick_bn), or
 // NULL to encode one from x_base / x_rows.
 cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const TcMap* mx_cached,
-                           const void* x_base, uint64_t x_rows, int splits, const TcScratch& scr, cudaStream_t s,
+                           const void* x_base, uint64_t x_rows, int splits, cudaStream_t s,
                            bool pdl);
 cudaError_t tc_init_attributes();
 int tc_bn_index(int bn);   // 16,32,64,128,256 -> 0..4

@@ -97,42 +97,23 @@ __global__ void embed_draft_kernel(int K1, const int32_t* req_ids, const int32_t
 // y = (x - mean) / sqrt(var + 1e-5) * g + b over each row, fp32 statistics.
 // group_skip > 0: output row o reads input row (o / (G-1)) * G + o % (G-1) + 1
 // (drops row 0 of every group of G rows: the drafter's anchor row).
+// One warp (one CTA) per row (ln_row_warp).
 template <typename T>
-__global__ void __launch_bounds__(128) layernorm_kernel(int d, const float* x, int ldx, const T* g, const T* b,
-                                                        T* y, int ldy, int group_skip) {
-  __shared__ float sh[4];
+__global__ void __launch_bounds__(32) layernorm_kernel(int M, int d, const float* x, int ldx, const T* g,
+                                                       const T* b, T* y, int ldy, int group_skip) {
+  pdl_trigger();
   pdl_wait();
   const int o = blockIdx.x;
+  if (o >= M) return;
   int src = o;
   if (group_skip > 0) {
     int G1 = group_skip - 1;
     src = (o / G1) * group_skip + (o % G1) + 1;
   }
-  const float* xr = x + (size_t)src * ldx;
-  float v[16];
-  float s = 0.0f;
-#pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    int n = threadIdx.x + u * 128;
-    v[u] = n < d ? xr[n] : 0.0f;
-    s += v[u];
-  }
-  const float mean = block_sum<128>(s, sh) / (float)d;
-  float q = 0.0f;
-#pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    int n = threadIdx.x + u * 128;
-    float c = n < d ? v[u] - mean : 0.0f;
-    q += c * c;
-  }
-  const float var = block_sum<128>(q, sh) / (float)d;
-  const float rstd = rsqrtf(var + 1e-5f);
-  pdl_trigger();
-#pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    int n = threadIdx.x + u * 128;
-    if (n < d) y[(size_t)o * ldy + n] = from_f<T>((v[u] - mean) * rstd * to_f<T>(g[n]) + to_f<T>(b[n]));
-  }
+  T* yr = y + (size_t)o * ldy;
+  ln_row_warp(x + (size_t)src * ldx, d, g, b, sizeof(T) == 2, [&](int k, float a0, float a1, float a2, float a3) {
+    yr[k] = from_f<T>(a0); yr[k + 1] = from_f<T>(a1); yr[k + 2] = from_f<T>(a2); yr[k + 3] = from_f<T>(a3);
+  });
 }
 
 // ------------------------------------------------------------------ argmax
@@ -476,9 +457,9 @@ cudaError_t launch_layernorm(int M, int d, const float* x, int ldx, const T* g, 
                              int group_skip, cudaStream_t s, bool pdl) {
   if (M <= 0) return cudaSuccess;
   cudaLaunchAttribute at[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(128), 0, s, pdl, at);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(32), 0, s, pdl, at);
   ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg, layernorm_kernel<T>, d, x, ldx, g, b, y, ldy, group_skip);
+  return cudaLaunchKernelEx(&cfg, layernorm_kernel<T>, M, d, x, ldx, g, b, y, ldy, group_skip);
 }
 cudaError_t launch_argmax_init(int M, unsigned long long* keys, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
