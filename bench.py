@@ -39,12 +39,58 @@ BUDGET = 224
 P_CORRUPT = 0.2
 
 
+class Workload:
+    """One measured configuration: model shape, batch, transcript lengths,
+    acoustic frames per request and how proposals are made."""
+
+    def __init__(self, name, shape, n, budgets, frames, pj=None, temperature=0.0, text=""):
+        self.name, self.shape, self.n = name, shape, n
+        self.budgets = np.asarray(budgets, dtype=np.int32)
+        self.frames = np.asarray(frames, dtype=np.int32)
+        self.pj = None if pj is None else np.asarray(pj, dtype=np.float64)
+        self.temperature = temperature
+        self.text = text
+
+    def config(self):
+        return {"workload": self.text, "global_batch": self.n, "seq_len": int(self.budgets.max()),
+                "K": self.shape.K, "frames": int(self.frames.max()),
+                "l2": "no flush: every step streams the decoder weights (>= 0.3 GB) and the acoustic K/V "
+                      "(>= 0.25 GB per large-v3 request), larger than the 129 MB L2"}
+
+
+def make_workload(name: str, batch: int = 1) -> Workload:
+    if name == "large-v3-b1":
+        return Workload(name, synth.LARGE_V3, batch, [BUDGET] * batch, [1500] * batch,
+                        synth.corruption_p_const(synth.LARGE_V3.K, P_CORRUPT),
+                        text=f"whisper-large-v3-shaped decoder, bf16, batch {batch}, {BUDGET}-token transcripts, "
+                             f"K=8, 2-layer parallel drafter run + synthetic proposals (p={P_CORRUPT}), "
+                             f"1500-frame encoder states")
+    if name == "turbo-b16":
+        s = synth.TURBO
+        return Workload(name, s, 16, synth.budgets_uniform(16, 40, 224, 3), [1500] * 16,
+                        synth.corruption_p_linear(s.K),
+                        text="whisper-large-v3-turbo-shaped decoder (4 layers), bf16, batch 16, transcripts "
+                             "U[40,224] tokens, K=8, 2-layer drafter run + continuation proposals "
+                             "(p_j 0.1..0.5), 1500-frame encoder states")
+    if name == "large-v3-b96-t0.7":
+        return Workload(name, synth.LARGE_V3, 96, [BUDGET] * 96, [1500] * 96, None, temperature=0.7,
+                        text="whisper-large-v3-shaped decoder, bf16, batch 96, 224-token transcripts, K=8, "
+                             "2-layer drafter sampling q at T=0.7, rejection-rule acceptance, 1500-frame "
+                             "encoder states")
+    if name == "turbo-b64-varlen":
+        F, bud = synth.varlen_frames_and_budgets(64, 5)
+        return Workload(name, synth.TURBO, 64, bud, F, synth.corruption_p_linear(synth.TURBO.K),
+                        text="whisper-large-v3-turbo-shaped decoder, bf16, batch 64 varlen: frames U{250..1500}, "
+                             "transcripts F/1500*200 +-20%, K=8, drafter run + continuation proposals, "
+                             "packed (frames and finished requests dropped)")
+    raise ValueError(name)
+
+
+WORKLOADS = ("large-v3-b1", "turbo-b16", "large-v3-b96-t0.7", "turbo-b64-varlen")
+
+
 def workload(batch: int):
-    return {"workload": f"whisper-large-v3-shaped decoder, bf16, batch {batch}, {BUDGET}-token transcripts, "
-                        f"K=8, 2-layer parallel drafter run + synthetic proposals (p={P_CORRUPT}), "
-                        f"1500-frame encoder states",
-            "global_batch": batch, "seq_len": BUDGET, "K": 8, "frames": 1500,
-            "l2": "no flush: every step streams 1.6 GB of weights + 0.25 GB/request of acoustic K/V (> 129 MB L2)"}
+    return make_workload("large-v3-b1", batch).config()
 
 
 def peaks():
@@ -141,49 +187,92 @@ def reduce_over_ranks(ms: float, ms_e2e: float, tokens: int, world: int, device)
 
 
 # ---------------------------------------------------------------- GPU arm
-def run_gpu(args, rank: int, world: int):
+def _setup(wl: Workload, rank: int, with_drafter: bool = True, max_frames: int | None = None):
+    """Context, request slots and pinned host encoder states of one workload."""
     import torch
-    from speculative_whisper_asr_gb300 import binding as B
     from speculative_whisper_asr_gb300 import runtime as R
-
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     dev = torch.device("cuda", torch.cuda.current_device())
-    s = synth.LARGE_V3
-    n = args.batch
+    s, n = wl.shape, wl.n
     tw = synth.target_weights(s, SEED)
-    dw = synth.drafter_weights(s, SEED, tw)
-    dec = R.Decoder(s, tw, dw, max_batch=n, max_frames=1500)
+    dw = synth.drafter_weights(s, SEED, tw) if with_drafter else None
+    dec = R.Decoder(s, tw, dw, max_batch=n, max_frames=max_frames or int(wl.frames.max()))
     del tw, dw
     req = dec.slots(list(range(n)))
-    As = [synth.encoder_states(s, SEED, r) for r in rank_requests(rank, n)]
-    host_enc = torch.from_numpy(np.concatenate([synth.bf16_bits(a) for a in As])).view(torch.int16)
-    host_enc = host_enc.pin_memory()
-    enc = host_enc.to(dev).view(torch.bfloat16)
-    frames = [1500] * n
-    cu, _ = dec.cross_kv(req, enc, frames)
+    ids = rank_requests(rank, n)
+    As = [synth.encoder_states(s, SEED, ids[i], frames=int(wl.frames[i])) for i in range(n)]
+    host_enc = torch.from_numpy(np.concatenate([synth.bf16_bits(a) for a in As])).view(torch.int16).pin_memory()
+    return dec, req, host_enc, stream, dev
 
-    # reference trajectory (target's own greedy output), then the corruption plan
-    b_ar = dec.new_batch(req, [BUDGET] * n)
+
+def _trajectory_plan(dec, req, wl: Workload, rank: int, dev):
+    """The target's own greedy transcripts (untimed) and, from them, the
+    corrupted-proposal tensors (reference trajectory, mask, random tokens)."""
+    import torch
+    from speculative_whisper_asr_gb300 import runtime as R
+    s, n = wl.shape, wl.n
+    b_ar = dec.new_batch(req, wl.budgets)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     R.run_ar(dec, b_ar)
     torch.cuda.synchronize()
     ar_time = time.perf_counter() - t0
     ar = b_ar.transcripts()
-    traj = np.full((n, s.max_pos), 0, dtype=np.int32)
+    traj = np.zeros((n, s.max_pos), dtype=np.int32)
     for i in range(n):
         t = list(s.prompt) + ar[i]
         traj[i, :len(t)] = t
-    plan = synth.corruption_plan(n, s.max_pos, s.K, synth.corruption_p_const(s.K, P_CORRUPT), s.vocab,
-                                 SEED + 100 + rank)
+    plan = synth.corruption_plan(n, s.max_pos, s.K, wl.pj, s.vocab, SEED + 100 + rank)
     syn = (torch.as_tensor(traj, device=dev), torch.as_tensor(plan.mask, device=dev),
            torch.as_tensor(plan.tok, device=dev))
+    return ar, syn, ar_time
 
-    batch = dec.new_batch(req, [BUDGET] * n)
-    budgets = torch.full((n,), BUDGET, dtype=torch.int32, device=dev)
+
+def _timed(step, steps, world, stream):
+    """Barrier, then `steps` calls of step() between CUDA events on the
+    launching stream, with the clocks sampled meanwhile."""
+    import torch
+    from speculative_whisper_asr_gb300 import binding as B
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    l0 = B.ws_launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = []
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.nvtx.range_push("ws_timed")        # lets a profiler restrict itself to the timed steps
+        t0.record(stream)
+        for _ in range(steps):
+            out.append(step())
+        t1.record(stream)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+    return t0.elapsed_time(t1), B.ws_launch_count() - l0, clk.summary(), out
+
+
+def run_gpu(args, rank: int, world: int, wl: Workload):
+    """Greedy decoding with synthetic proposals (the headline workload and
+    turbo batch 16): every timed step repeats the whole path and its
+    transcripts equal the autoregressive ones."""
+    import torch
+    from speculative_whisper_asr_gb300 import binding as B
+
+    dec, req, host_enc, stream, dev = _setup(wl, rank)
+    s, n = wl.shape, wl.n
+    enc = host_enc.to(dev).view(torch.bfloat16)
+    maxF, totF = int(wl.frames.max()), int(wl.frames.sum())
+    cu, _ = dec.cross_kv(req, enc, wl.frames)
+    ar, syn, ar_time = _trajectory_plan(dec, req, wl, rank, dev)
+
+    batch = dec.new_batch(req, wl.budgets)
+    budgets = torch.as_tensor(wl.budgets, device=dev)
     ev_v = []
+    live = torch.zeros(n, dtype=torch.int64, device=dev)
+    acc = torch.zeros(n, dtype=torch.int64, device=dev)
+    prop = torch.zeros(n, dtype=torch.int64, device=dev)
 
     def draft_calls():
         dec.draft(req, batch.block, 0.0, 0, 0, None)
@@ -195,11 +284,11 @@ def run_gpu(args, rank: int, world: int):
                         batch.blen)
         B.ws_accept(dec.ctx, n, req.data_ptr(), a, stream.cuda_stream)
 
-    def step(record=False, e2e=False):
-        """One pass of the whole path; returns tokens emitted."""
+    def step(record=False, e2e=False, stats=False):
+        """One pass of the whole path; returns the number of rounds."""
         if e2e:
             enc.view(torch.int16).copy_(host_enc, non_blocking=True)
-        B.ws_cross_kv(dec.ctx, n, req.data_ptr(), enc.data_ptr(), cu.data_ptr(), None, 1500, 1500 * n,
+        B.ws_cross_kv(dec.ctx, n, req.data_ptr(), enc.data_ptr(), cu.data_ptr(), None, maxF, totF,
                       stream.cuda_stream)
         batch.budget.copy_(budgets)
         batch.done.zero_(); batch.out_len.zero_(); batch.n_done.zero_()
@@ -207,6 +296,9 @@ def run_gpu(args, rank: int, world: int):
         rnd = 0
         while batch.poll_done() < n:
             rnd += 1
+            if stats:                       # untimed bookkeeping for tau and alpha
+                live.add_((batch.done == 0).long())
+                prop.add_((batch.blen - 1).clamp(min=0))
             # each phase of the round replays its own captured graph (greedy
             # rounds do not depend on the round number)
             batch.replay("draft", draft_calls)
@@ -218,54 +310,28 @@ def run_gpu(args, rank: int, world: int):
                 e1.record(stream)
                 ev_v.append((e0, e1))
             batch.replay("accept", accept_calls)
+            if stats:
+                acc.add_(batch.n_acc)
         if e2e:
             out = batch.transcript.to("cpu", non_blocking=True)
             torch.cuda.current_stream().synchronize()
             _ = out.numpy().sum()
         return rnd
 
-    for _ in range(args.warmup):
-        step()
+    for w in range(args.warmup):
+        step(stats=(w == 0))
     spec = batch.transcripts()
     assert spec == ar, "speculative transcript differs from autoregressive"
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     # ---- device-resident timed region
-    barrier()
-    torch.cuda.synchronize()
-    l0 = B.ws_launch_count()
-    tstart, tend = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    rounds = []
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        torch.cuda.nvtx.range_push("ws_timed")        # lets a profiler restrict itself to the timed steps
-        tstart.record(stream)
-        for _ in range(args.steps):
-            rounds.append(step(record=True))
-        tend.record(stream)
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
-    launches = B.ws_launch_count() - l0
-    ms = tstart.elapsed_time(tend)
+    ms, launches, clocks, rounds = _timed(lambda: step(record=True), args.steps, world, stream)
     tokens = int(batch.out_len.sum().item()) * args.steps
     # ---- end to end: host encoder states in, host transcript out
-    barrier()
-    torch.cuda.synchronize()
-    e2s, e2e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2s.record(stream)
-    for _ in range(args.steps):
-        step(e2e=True)
-    e2e_.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = e2s.elapsed_time(e2e_)
+    ms_e2e, _, _, _ = _timed(lambda: step(e2e=True), args.steps, world, stream)
 
     vt = [a.elapsed_time(b) for a, b in ev_v]
-    n_ver = len(vt)
-    L_mean = len(s.prompt) + BUDGET / 2.0
-    vbytes = verify_bytes(s, n, s.K + 1, L_mean)
+    L_mean = len(s.prompt) + float(wl.budgets.mean()) / 2.0
+    vbytes = verify_bytes(s, n, s.K + 1, L_mean, float(wl.frames.mean()))
     hbm, bf16_tf, src = peaks()
     v_ms = float(np.mean(vt))
     achieved = vbytes / (v_ms * 1e-3) / 1e9
@@ -273,21 +339,171 @@ def run_gpu(args, rank: int, world: int):
     ms, ms_e2e, tokens_all = reduce_over_ranks(ms, ms_e2e, tokens, world, dev)
     value = tokens_all / (ms * 1e-3)
     e2e_val = tokens_all / (ms_e2e * 1e-3)
-    emitted_rounds = np.mean(rounds)
-    audio_s = n * 1500 * 0.02 * args.steps * world
-    ar_tps = n * BUDGET / ar_time
+    audio_s = float(wl.frames.sum()) * 0.02 * args.steps * world
+    n_live = float(live.sum().item())
     return {
         "value": value, "ms_per_step": ms / args.steps, "e2e": e2e_val,
         "h2d": int(host_enc.numel() * 2), "d2h": int(batch.transcript.numel() * 4),
         "launches": int(launches),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": None, "kernel": "ws_verify (one block verification, all its kernels)",
-                     "algorithmic_bytes_per_launch": vbytes, "avg_ms": v_ms, "launches_timed": n_ver,
+                     "algorithmic_bytes_per_launch": vbytes, "avg_ms": v_ms, "launches_timed": len(vt),
                      "peak_source": src},
-        "clocks": clk.summary(),
-        "extra": {"rounds_per_step": float(emitted_rounds), "tau": BUDGET / float(emitted_rounds),
-                  "audio_seconds_per_s": audio_s / (ms * 1e-3), "ar_tokens_per_s_untimed_host_loop": ar_tps,
+        "clocks": clocks,
+        "extra": {"rounds_per_step": float(np.mean(rounds)),
+                  "tau": float(wl.budgets.sum()) / n_live,
+                  "alpha": float(acc.sum().item()) / max(1.0, float(prop.sum().item())),
+                  "audio_seconds_per_s": audio_s / (ms * 1e-3),
+                  "ar_tokens_per_s_untimed_host_loop": float(wl.budgets.sum()) / ar_time,
                   "gemm_engine": dec.engine, "verify_ms": v_ms},
+    }
+
+
+def run_sampling(args, rank: int, world: int, wl: Workload):
+    """Sampling at temperature T with the rejection rule: the drafter samples
+    its proposals from q = softmax(z_q / T) and ws_accept accepts or
+    resamples against p = softmax(z_p / T); both logits tensors are fp32."""
+    import torch
+    from speculative_whisper_asr_gb300 import binding as B
+
+    dec, req, host_enc, stream, dev = _setup(wl, rank)
+    s, n, T, seed = wl.shape, wl.n, wl.temperature, 7
+    enc = host_enc.to(dev).view(torch.bfloat16)
+    maxF, totF = int(wl.frames.max()), int(wl.frames.sum())
+    cu, _ = dec.cross_kv(req, enc, wl.frames)
+    batch = dec.new_batch(req, wl.budgets, sampling=True)
+    budgets = torch.as_tensor(wl.budgets, device=dev)
+    ev_v = []
+    live = torch.zeros(n, dtype=torch.int64, device=dev)
+    acc = torch.zeros(n, dtype=torch.int64, device=dev)
+    prop = torch.zeros(n, dtype=torch.int64, device=dev)
+
+    def step(record=False, stats=False):
+        B.ws_cross_kv(dec.ctx, n, req.data_ptr(), enc.data_ptr(), cu.data_ptr(), None, maxF, totF,
+                      stream.cuda_stream)
+        batch.budget.copy_(budgets)
+        batch.done.zero_(); batch.out_len.zero_(); batch.n_done.zero_()
+        batch.prefill(temperature=T, seed=seed)
+        rnd = 0
+        while batch.poll_done() < n:
+            rnd += 1
+            if stats:
+                live.add_((batch.done == 0).long())
+                prop.add_((batch.blen - 1).clamp(min=0))
+            dec.draft(req, batch.block, T, seed, rnd, batch.q_logits)
+            if record:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            dec.verify(req, batch.block, batch.blen, batch.target, batch.p_logits)
+            if record:
+                e1.record(stream)
+                ev_v.append((e0, e1))
+            a = batch._args(B.WS_ACCEPT_SAMPLE, s.K + 1, batch.block, batch.blen, batch.target, batch.block,
+                            batch.blen, batch.p_logits, batch.q_logits, T, seed, rnd)
+            B.ws_accept(dec.ctx, n, req.data_ptr(), a, stream.cuda_stream)
+            if stats:
+                acc.add_(batch.n_acc)
+        return rnd
+
+    for w in range(args.warmup):
+        step(stats=(w == 0))
+    ms, launches, clocks, rounds = _timed(lambda: step(record=True), args.steps, world, stream)
+    tokens = int(batch.out_len.sum().item()) * args.steps
+    vt = [a.elapsed_time(b) for a, b in ev_v]
+    v_ms = float(np.mean(vt))
+    L_mean = len(s.prompt) + float(wl.budgets.mean()) / 2.0
+    vbytes = verify_bytes(s, n, s.K + 1, L_mean, float(wl.frames.mean()))
+    hbm, bf16_tf, src = peaks()
+    d, f, nl = s.d_model, s.d_ff, s.n_layers
+    rows = n * (s.K + 1)
+    vflops = 2.0 * rows * (nl * (6 * d * d + 2 * d * f) + s.vocab * d)
+    ms, _, tokens_all = reduce_over_ranks(ms, ms, tokens, world, dev)
+    return {
+        "value": tokens_all / (ms * 1e-3), "ms_per_step": ms / args.steps, "launches": int(launches),
+        "roofline": {"bound": "hbm", "achieved": vbytes / (v_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": vbytes / (v_ms * 1e-3) / 1e9 / hbm, "traffic": None,
+                     "kernel": "ws_verify (one block verification, all its kernels, fp32 logits written)",
+                     "algorithmic_bytes_per_launch": vbytes, "avg_ms": v_ms, "launches_timed": len(vt),
+                     "peak_source": src,
+                     "tensor": {"flops_per_launch": vflops, "achieved_tflops": vflops / (v_ms * 1e-3) / 1e12,
+                                "peak_tflops": bf16_tf,
+                                "frac": vflops / (v_ms * 1e-3) / 1e12 / bf16_tf}},
+        "clocks": clocks,
+        "extra": {"rounds_per_step": float(np.mean(rounds)),
+                  "tau": float(wl.budgets.sum()) / float(live.sum().item()),
+                  "alpha": float(acc.sum().item()) / max(1.0, float(prop.sum().item())),
+                  "temperature": T, "gemm_engine": dec.engine, "verify_ms": v_ms},
+    }
+
+
+def varlen_flops(s: synth.ModelShape, frames, live_rounds, H: int):
+    """FLOPs of a varlen run, counted per decoder row (projections and LM head)
+    and per (row, acoustic key) (cross-attention scores and mixing), plus the
+    acoustic K/V projection per frame."""
+    d, f, nl = s.d_model, s.d_ff, s.n_layers
+    per_row = 2.0 * (nl * (6 * d * d + 2 * d * f) + s.vocab * d)
+    per_row_key = 4.0 * d * nl
+    per_frame = 2.0 * nl * 2 * d * d
+    rows = sum(r * H for r in live_rounds)
+    rowkeys = sum(r * H * F for r, F in zip(live_rounds, frames))
+    return {"rows": rows * per_row, "cross_attention": rowkeys * per_row_key,
+            "acoustic_kv": float(sum(frames)) * per_frame}
+
+
+def run_varlen(args, rank: int, world: int, wl: Workload):
+    """Varlen batch: packed (frames of each request only, finished requests
+    dropped between rounds) against padded (every request carries the
+    longest input, 1500 frames masked beyond its own, and stays in the batch
+    until the last one ends).  Both decode the same transcripts."""
+    import torch
+    from speculative_whisper_asr_gb300 import runtime as R
+
+    Fpad = 1500
+    dec, req, host_enc, stream, dev = _setup(wl, rank, max_frames=Fpad)
+    s, n = wl.shape, wl.n
+    enc = host_enc.to(dev).view(torch.bfloat16)
+    F = [int(x) for x in wl.frames]
+    dec.cross_kv(req, enc, F)
+    ar, syn, _ = _trajectory_plan(dec, req, wl, rank, dev)
+    # padded encoder states: zeros beyond each request's frames
+    pad = torch.zeros(n * Fpad, s.d_model, dtype=torch.bfloat16, device=dev)
+    off = 0
+    for i in range(n):
+        pad[i * Fpad:i * Fpad + F[i]].copy_(enc[off:off + F[i]])
+        off += F[i]
+    live_p = []
+
+    def packed_step():
+        dec.cross_kv(req, enc, F)
+        out, rounds, rows = R.run_spec_packed(dec, req, wl.budgets, synthetic=syn, live_rounds=live_p)
+        return out, rounds
+
+    def padded_step():
+        dec.cross_kv(req, pad, [Fpad] * n, valid=F)
+        b = dec.new_batch(req, wl.budgets)
+        rounds = R.run_spec(dec, b, synthetic=syn)
+        return b, rounds
+
+    for _ in range(args.warmup):
+        out_p, rounds_p = packed_step()
+        b_pad, rounds_pad = padded_step()
+    assert out_p == ar and b_pad.transcripts() == ar, "varlen transcripts differ from autoregressive"
+    ms_p, l_p, clocks, _ = _timed(packed_step, args.steps, world, stream)
+    ms_pad, l_pad, clocks_pad, _ = _timed(padded_step, args.steps, world, stream)
+    tokens = int(wl.budgets.sum()) * args.steps
+    H = s.K + 1
+    fp = varlen_flops(s, F, live_p, H)
+    fd = varlen_flops(s, [Fpad] * n, [rounds_pad] * n, H)
+    frac = {k: (fd[k] - fp[k]) / fd[k] for k in fp}
+    frac["total"] = (sum(fd.values()) - sum(fp.values())) / sum(fd.values())
+    ms_p, ms_pad, tokens_all = reduce_over_ranks(ms_p, ms_pad, tokens, world, dev)
+    return {
+        "value": tokens_all / (ms_p * 1e-3), "ms_per_step": ms_p / args.steps, "launches": int(l_p),
+        "roofline": None, "clocks": clocks,
+        "extra": {"padded_tokens_per_s": tokens_all / (ms_pad * 1e-3), "padded_ms_per_step": ms_pad / args.steps,
+                  "padded_launches": int(l_pad), "padded_clocks": clocks_pad,
+                  "padded_flop_fraction": frac, "rounds_packed": rounds_p, "rounds_padded": rounds_pad,
+                  "tau": float(wl.budgets.sum()) / float(sum(live_p)), "gemm_engine": dec.engine},
     }
 
 
@@ -329,7 +545,7 @@ def run_profile(args):
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
-def run_oracle_sample(budget_tokens: int = 12):
+def run_oracle_sample(budget_tokens: int = 48):
     """The oracle, as it stands, on a bounded sample of the same workload: one
     request, its own greedy trajectory (untimed, as on the GPU), then the
     timed speculative decode — acoustic K/V of all 34 layers, prompt prefill,
@@ -363,6 +579,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", type=int, default=0, help="run N rounds of the profiling case and exit")
+    ap.add_argument("--workload", default="large-v3-b1", choices=WORKLOADS,
+                    help="large-v3-b1 is the headline; the others measure the batch 16 / 96 and varlen cases")
     args = ap.parse_args()
     rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
@@ -387,7 +605,8 @@ def main():
                 "data": "synthetic", "config": workload(1),
                 "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                  "sample": "1 request of the same workload: acoustic K/V of 34 layers + prefill + "
-                                           "speculative rounds until 12 tokens (numpy float64 oracle)"},
+                                           f"speculative rounds until {total_tok // max(1, args.steps)} tokens "
+                                           "(numpy float64 oracle)"},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -397,21 +616,29 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    r = run_gpu(args, rank, world)
+    wl = make_workload(args.workload, args.batch)
+    if wl.temperature > 0.0:
+        r = run_sampling(args, rank, world, wl)
+    elif args.workload == "turbo-b64-varlen":
+        r = run_varlen(args, rank, world, wl)
+    else:
+        r = run_gpu(args, rank, world, wl)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "large-v3-b1":
         tok, dt, cores = run_oracle_sample()
         cpu = {"value": tok / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"1 request of the same workload: acoustic K/V (34 layers) + prefill + speculative "
                          f"rounds until {tok} tokens, numpy float64 oracle, {dt:.1f} s"}
     if rank == 0:
+        e2e = None
+        if "e2e" in r:
+            e2e = {"value": r["e2e"], "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                   "d2h_bytes_per_step": r["d2h"]}
         line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": dict(workload(args.batch), parallelism=f"replicas x{world}"),
-                "e2e": {"value": r["e2e"], "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
-                        "d2h_bytes_per_step": r["d2h"]},
-                "gpu_launches": r["launches"], "roofline": r["roofline"], "cpu_baseline": cpu,
+                "config": dict(wl.config(), parallelism=f"replicas x{world}"),
+                "e2e": e2e, "gpu_launches": r["launches"], "roofline": r["roofline"], "cpu_baseline": cpu,
                 "clocks": r["clocks"], "extra": r["extra"]}
         print(json.dumps(line))
     if world > 1:

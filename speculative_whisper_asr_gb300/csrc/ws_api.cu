@@ -235,6 +235,8 @@ Epi epi0(ws_ctx* c, int kind) {
 
 // Split-K factor of a weight shape: a function of (N, K) and the context only,
 // never of the token count, so every row is reduced in the same order.
+// Only small-batch contexts split: their tiles are at most 64 tokens wide, so
+// the fp32 partials folded through distributed shared memory stay small.
 int splits_for(const ws_ctx* c, int N, int K) {
   if (!c->split_ok) return 1;
   const int tiles = (N + 127) / 128, kb = K / 64;

@@ -14,14 +14,14 @@
 // fixed order, so a row's result does not depend on how many other rows
 // share the block: verifying a block and decoding one token at a time give
 // bit-identical rows.
-#include "ws_internal.cuh"
+#include "ws_attn_common.cuh"
 
 namespace {
 
 constexpr int SPLIT = WS_XCHUNK;   // keys per split (64)
 constexpr int NW = 8;              // warps per CTA
 constexpr int MAXR = 16;           // query rows per request
-constexpr int PART = WS_DH + 2;    // floats per partial
+constexpr int PART = WS_ATTN_PART;
 constexpr long long WAIT_BUDGET = 1ll << 32;
 
 enum { MODE_SELF = 0, MODE_CROSS = 1, MODE_DRAFT = 2 };
@@ -62,50 +62,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(smem_u32(dst)), "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
-
-struct RowState { float m, l, a0, a1; };
-
-// One sub-tile of up to 32 keys for one row (warp-wide): scores by lane = key,
-// online-softmax update, then weighted values with lane = pair of dims.
-__device__ __forceinline__ void row_subtile(RowState& st, const float* q, const float (*Kt)[WS_DH + 1],
-                                            const float (*Vt)[WS_DH], int k0, int nvalid, float* pw) {
-  const int lane = threadIdx.x & 31;
-  float s = -INFINITY;
-  if (lane < nvalid) {
-    const float* kr = Kt[k0 + lane];
-    float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-#pragma unroll
-    for (int d = 0; d < WS_DH; d += 4) {
-      c0 = fmaf(q[d], kr[d], c0);
-      c1 = fmaf(q[d + 1], kr[d + 1], c1);
-      c2 = fmaf(q[d + 2], kr[d + 2], c2);
-      c3 = fmaf(q[d + 3], kr[d + 3], c3);
-    }
-    s = ((c0 + c1) + (c2 + c3)) * 0.125f;          // 1/sqrt(64)
-  }
-  const float mn = fmaxf(st.m, warp_max(s));
-  const float p = lane < nvalid ? expf(s - mn) : 0.0f;
-  const float corr = expf(st.m - mn);
-  st.l = st.l * corr + warp_sum(p);
-  pw[lane] = p;
-  __syncwarp();
-  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-  int k = 0;
-  for (; k + 1 < nvalid; k += 2) {
-    const float2 v = *reinterpret_cast<const float2*>(&Vt[k0 + k][2 * lane]);
-    const float2 w = *reinterpret_cast<const float2*>(&Vt[k0 + k + 1][2 * lane]);
-    a0 = fmaf(pw[k], v.x, a0); a1 = fmaf(pw[k], v.y, a1);
-    b0 = fmaf(pw[k + 1], w.x, b0); b1 = fmaf(pw[k + 1], w.y, b1);
-  }
-  if (k < nvalid) {
-    const float2 v = *reinterpret_cast<const float2*>(&Vt[k0 + k][2 * lane]);
-    a0 = fmaf(pw[k], v.x, a0); a1 = fmaf(pw[k], v.y, a1);
-  }
-  __syncwarp();
-  st.a0 = st.a0 * corr + (a0 + b0);
-  st.a1 = st.a1 * corr + (a1 + b1);
-  st.m = mn;
 }
 
 template <typename T, int MODE>
@@ -226,21 +182,11 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AttnArgs a) {
     const int j = warp + u * NW;
     if (j >= H) continue;
     const float* p = a.part + (((size_t)i * H + j) * heads + head) * a.n_split * PART;
-    float M = -INFINITY;
-    for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, __ldcg(p + s * PART));
-    float den = 0.f, n0 = 0.f, n1 = 0.f;
-    for (int s = 0; s < a.n_split; ++s) {
-      const float* q = p + s * PART;
-      const float l = __ldcg(q + 1);
-      if (l <= 0.f) continue;
-      const float c = expf(__ldcg(q) - M);
-      den = fmaf(l, c, den);
-      n0 = fmaf(__ldcg(q + 2 + 2 * lane), c, n0);
-      n1 = fmaf(__ldcg(q + 3 + 2 * lane), c, n1);
-    }
+    float o0, o1;
+    attn_fold_row(p, a.n_split, o0, o1);
     T* o = O + ((size_t)i * H + j) * a.d + head * WS_DH + 2 * lane;
-    o[0] = from_f<T>(den > 0.f ? n0 / den : 0.f);
-    o[1] = from_f<T>(den > 0.f ? n1 / den : 0.f);
+    o[0] = from_f<T>(o0);
+    o[1] = from_f<T>(o1);
   }
 }
 

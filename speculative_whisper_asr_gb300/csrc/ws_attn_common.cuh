@@ -1,0 +1,73 @@
+// Attention arithmetic shared by the per-op attention kernel and the
+// persistent block-verification kernel, so both produce bit-identical rows:
+// the online-softmax update of one query row over up to 32 keys, and the
+// fold of per-split partials (max, sum, 64 weighted values) in split order.
+#pragma once
+#include "ws_internal.cuh"
+
+constexpr int WS_ATTN_PART = WS_DH + 2;    // floats per split partial
+
+struct RowState { float m, l, a0, a1; };
+
+// One sub-tile of up to 32 keys for one row (warp-wide): scores by lane = key,
+// online-softmax update, then weighted values with lane = pair of dims.
+__device__ __forceinline__ void row_subtile(RowState& st, const float* q, const float (*Kt)[WS_DH + 1],
+                                            const float (*Vt)[WS_DH], int k0, int nvalid, float* pw) {
+  const int lane = threadIdx.x & 31;
+  float s = -INFINITY;
+  if (lane < nvalid) {
+    const float* kr = Kt[k0 + lane];
+    float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll
+    for (int d = 0; d < WS_DH; d += 4) {
+      c0 = fmaf(q[d], kr[d], c0);
+      c1 = fmaf(q[d + 1], kr[d + 1], c1);
+      c2 = fmaf(q[d + 2], kr[d + 2], c2);
+      c3 = fmaf(q[d + 3], kr[d + 3], c3);
+    }
+    s = ((c0 + c1) + (c2 + c3)) * 0.125f;          // 1/sqrt(64)
+  }
+  const float mn = fmaxf(st.m, warp_max(s));
+  const float p = lane < nvalid ? expf(s - mn) : 0.0f;
+  const float corr = expf(st.m - mn);
+  st.l = st.l * corr + warp_sum(p);
+  pw[lane] = p;
+  __syncwarp();
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  int k = 0;
+  for (; k + 1 < nvalid; k += 2) {
+    const float2 v = *reinterpret_cast<const float2*>(&Vt[k0 + k][2 * lane]);
+    const float2 w = *reinterpret_cast<const float2*>(&Vt[k0 + k + 1][2 * lane]);
+    a0 = fmaf(pw[k], v.x, a0); a1 = fmaf(pw[k], v.y, a1);
+    b0 = fmaf(pw[k + 1], w.x, b0); b1 = fmaf(pw[k + 1], w.y, b1);
+  }
+  if (k < nvalid) {
+    const float2 v = *reinterpret_cast<const float2*>(&Vt[k0 + k][2 * lane]);
+    a0 = fmaf(pw[k], v.x, a0); a1 = fmaf(pw[k], v.y, a1);
+  }
+  __syncwarp();
+  st.a0 = st.a0 * corr + (a0 + b0);
+  st.a1 = st.a1 * corr + (a1 + b1);
+  st.m = mn;
+}
+
+// Fold the partials p[s * WS_ATTN_PART] of one row, s = 0 .. n_split-1 in
+// order; lane l returns output dims (2l, 2l+1).  Partials are read from L2
+// (they were written by other CTAs).
+__device__ __forceinline__ void attn_fold_row(const float* p, int n_split, float& o0, float& o1) {
+  const int lane = threadIdx.x & 31;
+  float M = -INFINITY;
+  for (int s = 0; s < n_split; ++s) M = fmaxf(M, __ldcg(p + s * WS_ATTN_PART));
+  float den = 0.f, n0 = 0.f, n1 = 0.f;
+  for (int s = 0; s < n_split; ++s) {
+    const float* q = p + s * WS_ATTN_PART;
+    const float l = __ldcg(q + 1);
+    if (l <= 0.f) continue;
+    const float c = expf(__ldcg(q) - M);
+    den = fmaf(l, c, den);
+    n0 = fmaf(__ldcg(q + 2 + 2 * lane), c, n0);
+    n1 = fmaf(__ldcg(q + 3 + 2 * lane), c, n1);
+  }
+  o0 = den > 0.f ? n0 / den : 0.f;
+  o1 = den > 0.f ? n1 / den : 0.f;
+}

@@ -39,8 +39,9 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int r, int n, float y0, f
     }
     case EPI_RESID: {
       float* x = e.resid + (size_t)r * e.ldr + n;
-      float v0 = x[0] + (y0 + bias_at<T>(e.bias, n));
-      float v1 = x[1] + (y1 + bias_at<T>(e.bias, n + 1));
+      // L2 loads: in the persistent kernel the residual was last written by another SM
+      float v0 = __ldcg(x) + (y0 + bias_at<T>(e.bias, n));
+      float v1 = __ldcg(x + 1) + (y1 + bias_at<T>(e.bias, n + 1));
       x[0] = v0; x[1] = v1;
       if (e.hist) {
         int slot, j, pos;
@@ -101,4 +102,43 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int r, int n, float y0, f
 __device__ __forceinline__ float epi_logit(const Epi& e, int n, float y) {
   if (e.suppress && ((e.suppress[n >> 5] >> (n & 31)) & 1u)) return -INFINITY;
   return y;
+}
+
+// Epilogue of 16 accumulator columns held by one warp: lane l holds feature
+// n (consecutive across the warp) and v[c] is its value for row t + c.
+// LOGITS reduces each row's (value, id) key over the warp before one
+// atomicMax; the other kinds pair features (n, n + 1) through a shuffle.
+__device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n, int M, int z, const float* v) {
+  const int lane = threadIdx.x & 31;
+  if (e.kind == EPI_LOGITS) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int r = t + c;
+      unsigned long long key = 0ull;
+      if (r < M && n < N) {
+        const float y = epi_logit(e, n, v[c]);
+        if (e.logits) e.logits[(long long)r * e.ldl + n] = y;
+        key = argmax_key(y, n);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+        key = other > key ? other : key;
+      }
+      if (lane == 0 && key != 0ull && e.amax) atomicMax(e.amax + r, key);
+    }
+    return;
+  }
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    const float pc0 = __shfl_xor_sync(0xffffffffu, v[c], 1);
+    const float pc1 = __shfl_xor_sync(0xffffffffu, v[c + 1], 1);
+    if ((lane & 1) == 0) {
+      const int r = t + c;
+      if (r < M && n + 1 < N) epi_pair<bf16>(e, r, n, v[c], pc0, z);
+    } else {
+      const int r = t + c + 1;
+      if (r < M && n < N) epi_pair<bf16>(e, r, n - 1, pc1, v[c + 1], z);
+    }
+  }
 }

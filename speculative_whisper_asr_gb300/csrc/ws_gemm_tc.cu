@@ -31,103 +31,11 @@
 #include <mutex>
 
 #include "ws_epilogue.cuh"
+#include "ws_tc.cuh"
 
 namespace {
 
-constexpr int BM = 128;                 // weight rows per tile (MMA M)
-constexpr int BK = 64;                  // k per ring slot (one 128-byte swizzle atom of bf16)
-constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-constexpr long long WAIT_BUDGET = 1ll << 32;   // clock cycles (~2 s) before a wait gives up
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait on a phase parity; false when the budget ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > WAIT_BUDGET) return false;
-  return true;
-}
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_u32(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row core groups 1024 bytes apart (SBO), sm_100 descriptor version.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)1 << 16;                  // leading byte offset (unused with this swizzle)
-  d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset
-  d |= (uint64_t)1 << 46;                  // version
-  d |= (uint64_t)2 << 61;                  // SWIZZLE_128B
-  return d;
-}
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
-      ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// 32 lanes x 16 consecutive 32-bit columns: thread = lane, v[i] = column i.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
+using namespace tc;
 
 struct TcParams {
   int M, N, K;           // tokens, weight rows (features), reduction
@@ -137,44 +45,6 @@ struct TcParams {
   int32_t* status;
 };
 
-// Epilogue for one column block of 16 tokens held as v[16] (feature = this thread's row).
-template <int BN>
-__device__ __forceinline__ void epilogue16(const Epi& e, const TcParams& p, int t0, int c0, int n, int M, int z,
-                                          const float* v) {
-  const int lane = threadIdx.x & 31;
-  if (e.kind == EPI_LOGITS) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int t = t0 + c0 + c;
-      unsigned long long key = 0ull;
-      if (t < M && n < p.N) {
-        const float y = epi_logit(e, n, v[c]);
-        if (e.logits) e.logits[(long long)t * e.ldl + n] = y;
-        key = argmax_key(y, n);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-        key = other > key ? other : key;
-      }
-      if (lane == 0 && key != 0ull && e.amax) atomicMax(e.amax + t, key);
-    }
-    return;
-  }
-#pragma unroll
-  for (int c = 0; c < 16; c += 2) {
-    const float pc0 = __shfl_xor_sync(0xffffffffu, v[c], 1);
-    const float pc1 = __shfl_xor_sync(0xffffffffu, v[c + 1], 1);
-    if ((lane & 1) == 0) {
-      const int t = t0 + c0 + c;
-      if (t < M && n + 1 < p.N) epi_pair<bf16>(e, t, n, v[c], pc0, z);
-    } else {
-      const int t = t0 + c0 + c + 1;
-      if (t < M && n < p.N) epi_pair<bf16>(e, t, n - 1, pc1, v[c + 1], z);
-    }
-  }
-}
-
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(128, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcParams p,
@@ -183,6 +53,7 @@ __global__ void __launch_bounds__(128, 1)
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+  static_assert(BN * BM * 4 <= STAGES * STAGE_BYTES, "a split-K partial must fit in the ring");
   extern __shared__ __align__(1024) uint8_t dsm[];
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
   __shared__ uint32_t tmem_base;
@@ -279,7 +150,7 @@ __global__ void __launch_bounds__(128, 1)
     for (int c0 = 0; c0 < BN; c0 += 16) {
       float v[16];
       tmem_ld16(taddr + (uint32_t)c0, v);
-      epilogue16<BN>(e, p, t0, c0, n, M, z, v);
+      epi_columns16(e, p.N, t0 + c0, n, M, z, v);
     }
   } else if (active && p.splits > 1) {
     // Split-K: the splits of one tile form a thread-block cluster.  Each CTA
@@ -313,7 +184,7 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] += w[c];
         }
-        epilogue16<BN>(e, p, t0, c0, n, M, z, v);
+        epi_columns16(e, p.N, t0 + c0, n, M, z, v);
       }
     }
     cl.sync();

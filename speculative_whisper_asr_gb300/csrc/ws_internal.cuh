@@ -88,7 +88,8 @@ __device__ __forceinline__ float warp_max(float v) {
 // per-lane sequential sums followed by a fixed shuffle tree, so a row's
 // values never depend on which other rows share the launch.  out(k, ...)
 // receives the four normalised values of group k.
-template <class Out>
+// CG: read x from L2 (rows written by other SMs in the same kernel).
+template <bool CG = false, class Out>
 __device__ __forceinline__ void ln_row_warp(const float* x, int d, const void* g, const void* b, bool g_bf16,
                                             Out out) {
   const int lane = threadIdx.x & 31;
@@ -98,7 +99,8 @@ __device__ __forceinline__ void ln_row_warp(const float* x, int d, const void* g
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     if (i < nv) {
-      v[i] = *reinterpret_cast<const float4*>(x + 4 * lane + 128 * i);
+      const float4* src = reinterpret_cast<const float4*>(x + 4 * lane + 128 * i);
+      v[i] = CG ? __ldcg(src) : *src;
       s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
     }
   }

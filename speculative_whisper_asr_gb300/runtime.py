@@ -291,14 +291,17 @@ def run_ar_sampling(dec: Decoder, batch: Batch, temperature: float, seed: int, m
     return rounds
 
 
-def run_spec_packed(dec: Decoder, req_all: torch.Tensor, budgets, synthetic=None, max_rounds=100000):
+def run_spec_packed(dec: Decoder, req_all: torch.Tensor, budgets, synthetic=None, max_rounds=100000,
+                    live_rounds: list | None = None):
     """Varlen batch without padding rows: after every round the requests that
     finished are dropped from the slot list, so later rounds only carry live
     requests (their rows, attention and acceptance).  Returns (transcripts,
-    rounds, rows processed)."""
+    rounds, rows processed); `live_rounds`, when given, receives the number
+    of rounds each request took part in."""
     n_all = req_all.numel()
     alive = list(range(n_all))
     out = [None] * n_all
+    live = [0] * n_all
     budgets = np.asarray(budgets, dtype=np.int32)
     b = dec.new_batch(req_all, budgets)
     b.prefill()
@@ -324,5 +327,9 @@ def run_spec_packed(dec: Decoder, req_all: torch.Tensor, budgets, synthetic=None
             b = nb
         rounds += 1
         rows += b.n * (dec.K + 1)
+        for k in alive:
+            live[k] += 1
         b.spec_step(rounds, syn_all, graph=False)
+    if live_rounds is not None:
+        live_rounds[:] = live
     return out, rounds, rows
