@@ -229,6 +229,19 @@ int ws_status(ws_ctx* ctx, ws_stream stream, int32_t* host_status);
 /* Name of the GEMM engine in use ("simt" or "tcgen05"). */
 const char* ws_gemm_engine(const ws_ctx* ctx);
 
+/* Persistent block verification (Whisper-Flash §3.1 block verification; the
+ * same target pass as ws_verify's kernel-per-operation path, with the same
+ * arithmetic, so rows are bit-identical).  A bf16 context on the tcgen05
+ * engine runs every ws_verify call with n_req * H <= 16 rows as one
+ * cooperative kernel (one CTA per SM, grid-wide barriers between stages,
+ * weights streamed ahead through shared memory) when the device supports
+ * cooperative launch.  Off by default: on GB300 the per-operation path is
+ * faster at batch 1 (3.75 vs 5.67 ms per large-v3 verify).
+ *   enable  1: use it when eligible; 0: never (the default); -1: query only.
+ * Returns 1 when eligible calls take the persistent path, 0 when not, or
+ * WS_EINVAL for a null context.  Host-only; no device work. */
+int ws_fused_verify(ws_ctx* ctx, int enable);
+
 /* CUDA-graph replay of a fixed call sequence (Whisper-Flash Appendix A.5
  * replays prefill, drafting and each verification length from captured
  * graphs).  Between ws_capture_begin and ws_capture_end every ws_* call on

@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <vector>
 
+#include "ws_fused.cuh"
 #include "ws_internal.cuh"
 
 // A weight matrix [rows, cols] (row-major, model dtype) and, for the tcgen05
@@ -60,6 +61,15 @@ struct ws_ctx {
   std::vector<XMap> xmaps;
   bool pdl = true;              // programmatic dependent launch allowed
   bool cur_pdl = false;         // PDL for the call in progress (never on the legacy stream)
+  // persistent block verification (bf16, tcgen05, at most 16 rows per call)
+  bool fused_ok = false;        // built and runnable on this device
+  bool fused_on = false;        // caller's switch (ws_fused_verify); off: the per-op path is faster here
+  int fused_grid = 0, fused_ring = 0, n_fstages = 0;
+  size_t fused_work = 0;
+  FusedStage* fstages = nullptr;     // device copy of the stage table
+  float* fpart = nullptr;
+  int* fctr = nullptr;
+  unsigned* gbar = nullptr;
   std::string err;
 };
 
@@ -122,6 +132,7 @@ struct Layout {
 struct Plan {
   size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
   size_t acnt;
+  size_t fmaps, fstages, fpart, fctr, gbar;
   size_t kv_layer_bytes, total;
   int heads, ppr, n_pages, n_xl, max_split;
 };
@@ -186,6 +197,13 @@ Plan make_plan(const ws_model_desc& d) {
   p.feat = lay.take(M * nh * D * es);
   p.hpre = lay.take(M * D * 4);
   p.hh = lay.take(M * D * es);
+  // persistent verify: weight TMA maps, stage table, split-K partials, tile counters, grid barrier
+  const size_t widest = std::max({(size_t)3 * D, (size_t)d.d_ff, (size_t)d.vocab});
+  p.fmaps = lay.take((6 * (size_t)d.n_layers + 1) * sizeof(TcMap));
+  p.fstages = lay.take((8 * (size_t)d.n_layers + 3) * sizeof(FusedStage));
+  p.fpart = lay.take((widest + 127) / 128 * 8 * FUSED_MAX_ROWS * 128 * 4);
+  p.fctr = lay.take(((widest + 127) / 128 + 1) * 4);
+  p.gbar = lay.take(64);
   p.total = lay.off;
   return p;
 }
@@ -290,12 +308,110 @@ bool is_hist_layer(const ws_model_desc& d, int l, int& idx) {
   return false;
 }
 
+// --------------------------------------------------------------------------- persistent verify
+// Stage table of the target pass (embedding, 8 stages per layer, LM head,
+// argmax) with the per-op path's split-K factors, copied to the device with
+// the weight TMA maps it points to.  Leaves fused_ok false when the device
+// cannot run the kernel.
+cudaError_t setup_fused(ws_ctx* c, const Plan& p, cudaStream_t s) {
+  const ws_model_desc& d = c->d;
+  if (c->engine != WS_GEMM_TC || d.dtype != WS_BF16) return cudaSuccess;
+  const int D = d.d_model;
+  std::vector<TcMap> maps;
+  std::vector<FusedStage> st;
+  TcMap* dmaps = (TcMap*)(c->ws + p.fmaps);
+  int max_unit_kb = 1;
+  auto gemm_stage = [&](int layer, const Mat& W, int in_kind, const void* g, const void* b, const void* act,
+                        int ld_act, int epi, const void* bias, const void* bias2, void* out, int ldo, int hist) {
+    FusedStage f;
+    memset(&f, 0, sizeof f);
+    f.kind = FS_GEMM; f.layer = layer;
+    f.map = dmaps + maps.size();
+    maps.push_back(W.map);
+    f.N = W.rows; f.kb_total = W.cols / 64; f.splits = splits_for(c, W.rows, W.cols);
+    f.in_kind = in_kind; f.ln_g = g; f.ln_b = b; f.act = (const bf16*)act; f.ld_act = ld_act;
+    f.epi = epi; f.bias = bias; f.bias2 = bias2; f.out = out; f.ldo = ldo; f.hist_idx = hist;
+    max_unit_kb = std::max(max_unit_kb, (f.kb_total + f.splits - 1) / f.splits);
+    st.push_back(f);
+  };
+  auto plain = [&](int kind, int layer) {
+    FusedStage f;
+    memset(&f, 0, sizeof f);
+    f.kind = kind; f.layer = layer; f.hist_idx = -1;
+    st.push_back(f);
+  };
+  plain(FS_EMBED, 0);
+  for (int l = 0; l < d.n_layers; ++l) {
+    const LayerW& w = c->tl[l];
+    int hidx = -1;
+    if (!is_hist_layer(d, l, hidx)) hidx = -1;
+    gemm_stage(l, w.w_qkv, FIN_LN, w.ln1_g, w.ln1_b, nullptr, 0, EPI_QKV, w.b_q, w.b_v, c->q, D, -1);
+    plain(FS_SELF, l);
+    gemm_stage(l, w.w_o, FIN_ACT, nullptr, nullptr, c->ao, D, EPI_RESID, w.b_o, nullptr, nullptr, 0, -1);
+    gemm_stage(l, w.w_qc, FIN_LN, w.ln2_g, w.ln2_b, nullptr, 0, EPI_STORE, w.b_qc, nullptr, c->q, D, -1);
+    plain(FS_CROSS, l);
+    gemm_stage(l, w.w_oc, FIN_ACT, nullptr, nullptr, c->ao, D, EPI_RESID, w.b_oc, nullptr, nullptr, 0, -1);
+    gemm_stage(l, w.w_fc1, FIN_LN, w.ln3_g, w.ln3_b, nullptr, 0, EPI_GELU, w.b_fc1, nullptr, c->ffn, d.d_ff, -1);
+    gemm_stage(l, w.w_fc2, FIN_ACT, nullptr, nullptr, c->ffn, d.d_ff, EPI_RESID, w.b_fc2, nullptr, nullptr, 0, hidx);
+  }
+  gemm_stage(d.n_layers, c->head, FIN_LN, c->lnf_g, c->lnf_b, nullptr, 0, EPI_LOGITS, nullptr, nullptr, nullptr, 0,
+             -1);
+  plain(FS_ARGMAX, 0);
+  for (const FusedStage& f : st)    // every store target the kernel will use exists
+    if (f.kind == FS_GEMM && ((f.epi == EPI_STORE || f.epi == EPI_GELU) ? f.out == nullptr : false)) return cudaSuccess;
+  c->fstages = (FusedStage*)(c->ws + p.fstages);
+  c->fpart = (float*)(c->ws + p.fpart);
+  c->fctr = (int*)(c->ws + p.fctr);
+  c->gbar = (unsigned*)(c->ws + p.gbar);
+  c->n_fstages = (int)st.size();
+  cudaError_t e = cudaMemcpyAsync(dmaps, maps.data(), maps.size() * sizeof(TcMap), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(c->fstages, st.data(), st.size() * sizeof(FusedStage), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->fctr, 0, p.gbar - p.fctr, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->gbar, 0, 64, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);    // host vectors go out of scope
+  if (e != cudaSuccess) return e;
+  c->fused_work = fused_work_bytes(max_unit_kb);
+  c->fused_ring = fused_prepare(c->fused_work, &c->fused_grid);
+  c->fused_ok = c->fused_ring > 0;
+  cudaGetLastError();      // a device without cooperative launch is not an error
+  return cudaSuccess;
+}
+
+int fused_verify(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* block, const int32_t* blen,
+                 int32_t* target, float* logits, cudaStream_t s) {
+  const ws_model_desc& d = c->d;
+  FusedArgs a;
+  memset(&a, 0, sizeof a);
+  a.stages = c->fstages; a.n_stages = c->n_fstages; a.ring_slots = c->fused_ring; a.work_bytes = c->fused_work;
+  a.n = n; a.H = H; a.M = n * H;
+  a.d = d.d_model; a.V = d.vocab; a.heads = c->heads; a.max_pos = d.max_pos; a.max_block = d.max_block;
+  a.n_hist = d.n_hist;
+  a.nsplit_self = (d.max_pos + WS_XCHUNK - 1) / WS_XCHUNK;
+  a.nsplit_cross = std::max(1, (c->max_fc + WS_XCHUNK - 1) / WS_XCHUNK);
+  a.rm.mode = ROW_VERIFY; a.rm.H = H; a.rm.max_pos = d.max_pos; a.rm.req_ids = req; a.rm.L = c->L;
+  a.rm.block_len = blen; a.rm.pend_start = c->pend_start; a.rm.pend_n = c->pend_n;
+  a.req_ids = req; a.block = block; a.block_len = blen;
+  a.tok_emb = (const bf16*)c->tok_emb; a.pos_emb = (const bf16*)c->pos_emb;
+  a.x = c->x; a.ao = (bf16*)c->ao; a.q = (bf16*)c->q;
+  a.kv = c->kv; a.kv_layer_bytes = c->kv_layer_bytes; a.ptab = c->ptab; a.ppr = c->ppr;
+  a.xkv = xkv_of(c); a.Fv = c->Fv; a.hist = c->hist;
+  a.part = c->fpart; a.tile_ctr = c->fctr; a.apart = c->as.part; a.actr = c->as.counters;
+  a.amax = c->amax; a.logits = logits; a.suppress = c->suppress; a.target = target;
+  a.pend_start = c->pend_start; a.pend_n = c->pend_n; a.gbar = c->gbar; a.status = c->status;
+  CK(launch_fused_verify(a, c->fused_grid, c->fused_work, s));
+  if (d.drafter_layers > 0) c->pending_H = H > c->pending_H ? H : c->pending_H;
+  return WS_OK;
+}
+
 // --------------------------------------------------------------------------- verify
 template <typename T>
 int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* block, const int32_t* blen,
                 int32_t* target, float* logits, cudaStream_t s) {
   const ws_model_desc& d = c->d;
   const int D = d.d_model, M = n * H;
+  if (sizeof(T) == 2 && c->fused_ok && c->fused_on && M <= FUSED_MAX_ROWS)
+    return fused_verify(c, n, req, H, block, blen, target, logits, s);
   const bool pdl = c->cur_pdl;
   RowMap rm;
   rm.mode = ROW_VERIFY; rm.H = H; rm.max_pos = d.max_pos; rm.req_ids = req; rm.L = c->L;
@@ -553,6 +669,7 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   if (e == cudaSuccess) e = cudaMemsetAsync(c->as.counters, 0, (size_t)desc->max_batch * desc->n_heads * 4, s);
   if (e == cudaSuccess) e = desc->dtype == WS_BF16 ? attn_init_attributes<bf16>() : attn_init_attributes<float>();
   if (e == cudaSuccess) e = launch_rope_table(c->rope, desc->max_pos, s);
+  if (e == cudaSuccess) e = setup_fused(c, p, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) { fail(nullptr, WS_ECUDA, "context init: %s", cudaGetErrorString(e)); return cleanup(WS_ECUDA); }
   *out = c;
@@ -683,6 +800,12 @@ int ws_status(ws_ctx* c, ws_stream stream, int32_t* host_status) {
 const char* ws_gemm_engine(const ws_ctx* c) {
   if (!c) return "none";
   return c->engine == WS_GEMM_TC ? "tcgen05" : "simt";
+}
+
+int ws_fused_verify(ws_ctx* c, int enable) {
+  if (!c) return fail(nullptr, WS_EINVAL, "null context");
+  if (enable >= 0) c->fused_on = enable != 0;
+  return (c->fused_ok && c->fused_on) ? 1 : 0;
 }
 
 unsigned long long ws_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -53,20 +53,43 @@ __device__ __forceinline__ void row_subtile(RowState& st, const float* q, const 
 
 // Fold the partials p[s * WS_ATTN_PART] of one row, s = 0 .. n_split-1 in
 // order; lane l returns output dims (2l, 2l+1).  Partials are read from L2
-// (they were written by other CTAs).
+// (they were written by other CTAs).  All loads of a group of splits are
+// issued before their values are used (one L2 round trip per group instead
+// of one per split); the arithmetic and its order are those of the
+// sequential fold: M = max_s m_s, then den, n0, n1 accumulate over s = 0, 1,
+// ... with weights exp(m_s - M), skipping empty splits.
 __device__ __forceinline__ void attn_fold_row(const float* p, int n_split, float& o0, float& o1) {
   const int lane = threadIdx.x & 31;
   float M = -INFINITY;
-  for (int s = 0; s < n_split; ++s) M = fmaxf(M, __ldcg(p + s * WS_ATTN_PART));
+  for (int s0 = 0; s0 < n_split; s0 += 32) {
+    const int s = s0 + lane;
+    const float m = s < n_split ? __ldcg(p + (size_t)s * WS_ATTN_PART) : -INFINITY;
+    M = fmaxf(M, warp_max(m));
+  }
   float den = 0.f, n0 = 0.f, n1 = 0.f;
-  for (int s = 0; s < n_split; ++s) {
-    const float* q = p + s * WS_ATTN_PART;
-    const float l = __ldcg(q + 1);
-    if (l <= 0.f) continue;
-    const float c = expf(__ldcg(q) - M);
-    den = fmaf(l, c, den);
-    n0 = fmaf(__ldcg(q + 2 + 2 * lane), c, n0);
-    n1 = fmaf(__ldcg(q + 3 + 2 * lane), c, n1);
+  for (int s0 = 0; s0 < n_split; s0 += 32) {
+    const int sl = s0 + lane;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (sl < n_split) ml = __ldcg(reinterpret_cast<const float2*>(p + (size_t)sl * WS_ATTN_PART));
+    const int nin = min(32, n_split - s0);
+    for (int t = 0; t < nin; t += 8) {
+      float2 av[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (t + u < nin)
+          av[u] = __ldcg(reinterpret_cast<const float2*>(p + (size_t)(s0 + t + u) * WS_ATTN_PART + 2 + 2 * lane));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (t + u >= nin) break;
+        const float l = __shfl_sync(0xffffffffu, ml.y, t + u);
+        const float m = __shfl_sync(0xffffffffu, ml.x, t + u);
+        if (l <= 0.f) continue;
+        const float c = expf(m - M);
+        den = fmaf(l, c, den);
+        n0 = fmaf(av[u].x, c, n0);
+        n1 = fmaf(av[u].y, c, n1);
+      }
+    }
   }
   o0 = den > 0.f ? n0 / den : 0.f;
   o1 = den > 0.f ? n1 / den : 0.f;

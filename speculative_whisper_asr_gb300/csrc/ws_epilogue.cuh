@@ -129,6 +129,36 @@ __device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n,
     }
     return;
   }
+  if (e.kind == EPI_RESID) {
+    // residual update: the 8 (row, feature pair) residual values of this lane
+    // are loaded together (one L2 round trip), then x += y + b as in epi_pair
+    const int odd = lane & 1, nn = n - odd;
+    const float b0 = bias_at<bf16>(e.bias, nn), b1 = bias_at<bf16>(e.bias, nn + 1);
+    float2 xr[8];
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const int r = t + c + odd;
+      if (r < M && nn + 1 < N) xr[c / 2] = __ldcg(reinterpret_cast<const float2*>(e.resid + (size_t)r * e.ldr + nn));
+    }
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const float pc0 = __shfl_xor_sync(0xffffffffu, v[c], 1);
+      const float pc1 = __shfl_xor_sync(0xffffffffu, v[c + 1], 1);
+      const int r = t + c + odd;
+      const float y0 = odd ? pc1 : v[c], y1 = odd ? v[c + 1] : pc0;
+      if (r < M && nn + 1 < N) {
+        const float v0 = xr[c / 2].x + (y0 + b0), v1 = xr[c / 2].y + (y1 + b1);
+        *reinterpret_cast<float2*>(e.resid + (size_t)r * e.ldr + nn) = make_float2(v0, v1);
+        if (e.hist) {
+          int slot, j, pos;
+          row_info(e.rm, r, slot, j, pos);
+          float* h = e.hist + (((size_t)slot * e.max_block + j) * e.n_hist + e.hist_idx) * e.d + nn;
+          h[0] = v0; h[1] = v1;
+        }
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int c = 0; c < 16; c += 2) {
     const float pc0 = __shfl_xor_sync(0xffffffffu, v[c], 1);

@@ -83,61 +83,83 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // ------------------------------------------------------------------ layer norm of one row
-// One warp normalises one row of d fp32 values (d a multiple of 128, <= 2048):
-// lane l owns the float4 groups at 4*l + 128*i.  Mean and variance are
-// per-lane sequential sums followed by a fixed shuffle tree, so a row's
-// values never depend on which other rows share the launch.  out(k, ...)
-// receives the four normalised values of group k.
-// CG: read x from L2 (rows written by other SMs in the same kernel).
+// One warp normalises one row of d fp32 values (d a multiple of 128, at most
+// 128 * MAXV): lane l owns the float4 groups at 4*l + 128*i.  Mean and
+// variance are per-lane sequential sums followed by a fixed shuffle tree, so
+// a row's values never depend on which other rows share the launch.
+// ln_rows_warp takes NR rows at once: the loads of all of them are issued
+// before any is reduced (one memory round trip for NR rows); each row's
+// arithmetic is the same.  out(r, k, ...) receives the four normalised
+// values of group k of row r.  CG: read x from L2 (rows written by other SMs
+// in the same kernel).
+template <bool CG, int NR, int MAXV, class Out>
+__device__ __forceinline__ void ln_rows_warp(const float* const* xs, int nr, int d, const void* g, const void* b,
+                                             bool g_bf16, Out out) {
+  const int lane = threadIdx.x & 31;
+  const int nv = d >> 7;
+  float4 v[NR][MAXV];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    if (r < nr) {
+#pragma unroll
+      for (int i = 0; i < MAXV; ++i) {
+        if (i < nv) {
+          const float4* src = reinterpret_cast<const float4*>(xs[r] + 4 * lane + 128 * i);
+          v[r][i] = CG ? __ldcg(src) : *src;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    if (r >= nr) break;
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i)
+      if (i < nv) s += (v[r][i].x + v[r][i].y) + (v[r][i].z + v[r][i].w);
+    const float mean = warp_sum(s) / (float)d;
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      if (i < nv) {
+        const float a = v[r][i].x - mean, bb = v[r][i].y - mean, c = v[r][i].z - mean, e = v[r][i].w - mean;
+        q += (a * a + bb * bb) + (c * c + e * e);
+      }
+    }
+    const float rstd = rsqrtf(warp_sum(q) / (float)d + 1e-5f);
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      if (i < nv) {
+        const int k = 4 * lane + 128 * i;
+        float gg[4], bv[4];
+        if (g_bf16) {
+          const uint2 gq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(g) + k);
+          const uint2 bq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(b) + k);
+          const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.x));
+          const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.y));
+          const float2 b01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.x));
+          const float2 b23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.y));
+          gg[0] = g01.x; gg[1] = g01.y; gg[2] = g23.x; gg[3] = g23.y;
+          bv[0] = b01.x; bv[1] = b01.y; bv[2] = b23.x; bv[3] = b23.y;
+        } else {
+          const float4 gq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + k);
+          const float4 bq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(b) + k);
+          gg[0] = gq.x; gg[1] = gq.y; gg[2] = gq.z; gg[3] = gq.w;
+          bv[0] = bq.x; bv[1] = bq.y; bv[2] = bq.z; bv[3] = bq.w;
+        }
+        out(r, k, (v[r][i].x - mean) * rstd * gg[0] + bv[0], (v[r][i].y - mean) * rstd * gg[1] + bv[1],
+            (v[r][i].z - mean) * rstd * gg[2] + bv[2], (v[r][i].w - mean) * rstd * gg[3] + bv[3]);
+      }
+    }
+  }
+}
+
 template <bool CG = false, class Out>
 __device__ __forceinline__ void ln_row_warp(const float* x, int d, const void* g, const void* b, bool g_bf16,
                                             Out out) {
-  const int lane = threadIdx.x & 31;
-  const int nv = d >> 7;
-  float4 v[16];
-  float s = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    if (i < nv) {
-      const float4* src = reinterpret_cast<const float4*>(x + 4 * lane + 128 * i);
-      v[i] = CG ? __ldcg(src) : *src;
-      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
-    }
-  }
-  const float mean = warp_sum(s) / (float)d;
-  float q = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    if (i < nv) {
-      const float a = v[i].x - mean, bb = v[i].y - mean, c = v[i].z - mean, e = v[i].w - mean;
-      q += (a * a + bb * bb) + (c * c + e * e);
-    }
-  }
-  const float rstd = rsqrtf(warp_sum(q) / (float)d + 1e-5f);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    if (i < nv) {
-      const int k = 4 * lane + 128 * i;
-      float gg[4], bv[4];
-      if (g_bf16) {
-        const uint2 gq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(g) + k);
-        const uint2 bq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(b) + k);
-        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.x));
-        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.y));
-        const float2 b01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.x));
-        const float2 b23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.y));
-        gg[0] = g01.x; gg[1] = g01.y; gg[2] = g23.x; gg[3] = g23.y;
-        bv[0] = b01.x; bv[1] = b01.y; bv[2] = b23.x; bv[3] = b23.y;
-      } else {
-        const float4 gq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + k);
-        const float4 bq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(b) + k);
-        gg[0] = gq.x; gg[1] = gq.y; gg[2] = gq.z; gg[3] = gq.w;
-        bv[0] = bq.x; bv[1] = bq.y; bv[2] = bq.z; bv[3] = bq.w;
-      }
-      out(k, (v[i].x - mean) * rstd * gg[0] + bv[0], (v[i].y - mean) * rstd * gg[1] + bv[1],
-          (v[i].z - mean) * rstd * gg[2] + bv[2], (v[i].w - mean) * rstd * gg[3] + bv[3]);
-    }
-  }
+  const float* xs[1] = {x};
+  ln_rows_warp<CG, 1, 16>(xs, 1, d, g, b, g_bf16,
+                          [&](int, int k, float v0, float v1, float v2, float v3) { out(k, v0, v1, v2, v3); });
 }
 
 // ------------------------------------------------------------------ PDL
