@@ -274,7 +274,7 @@ cudaError_t gemm(ws_ctx* c, const void* X, uint64_t x_rows, const Mat& W, int M,
   {
     const TcMap* mx = nullptr;
     for (const auto& xm : c->xmaps)
-      if (xm.base == X) { mx = &xm.bn[tc_bn_index(tc_pick_bn(M))]; break; }
+      if (xm.base == X) { mx = &xm.bn[tc_bn_index(tc_pick_bn(M, g.N, batch))]; break; }
     return launch_gemm_tc(g, e, W.map, mx, X, x_rows, allow_split ? splits_for(c, g.N, g.K) : 1, s,
                           c->cur_pdl);
   }

@@ -42,6 +42,7 @@ struct TcParams {
   int kb_total;          // K / BK
   int splits;            // split-K factor (grid.x = tiles_f * splits)
   int tiles_f, tiles_t;
+  int nz;                // batch entries (CROSSKV: requests)
   int32_t* status;
 };
 
@@ -194,6 +195,196 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ------------------------------------------------------------------ persistent variant
+// Calls without split-K (all large-token GEMMs, the acoustic K/V projection,
+// the LM head) run as a persistent, warp-specialised kernel: one CTA per SM
+// walks tiles t = blockIdx.x, + gridDim.x, ... (feature tile fastest, so
+// the CTAs of a wave share the activation tile in L2).  Warp 0 streams
+// weight and activation tiles through the ring, warp 1 issues the MMAs into
+// one of two TMEM accumulators, warps 2..5 (TMEM lane quarters 2,3,0,1) run
+// the epilogue of tile i while the MMAs of tile i+1 proceed.  A tile's k
+// order is that of gemm_tc_kernel, so both give bit-identical outputs.
+template <int BN>
+constexpr int persistent_stages() { return (200 * 1024) / (A_BYTES + BN * BK * 2); }
+
+template <int BN>
+constexpr int persistent_smem() { return persistent_stages<BN>() * (A_BYTES + BN * BK * 2) + 1024; }
+
+struct TileInfo { int tile_f, t0, z, row0, M; bool active; };
+
+__device__ __forceinline__ TileInfo tile_of(const TcParams& p, const Epi& e, int t, int BN) {
+  TileInfo ti;
+  ti.tile_f = t % p.tiles_f;
+  const int rest = t / p.tiles_f;
+  const int tt = rest % p.tiles_t;
+  ti.z = rest / p.tiles_t;
+  ti.t0 = tt * BN;
+  ti.row0 = 0;
+  ti.M = p.M;
+  if (e.kind == EPI_CROSSKV) {        // per-request frame ranges (device memory, read after the dependency wait)
+    ti.row0 = e.cu_frames[ti.z];
+    ti.M = min(e.cu_frames[ti.z + 1] - ti.row0, e.xkv.max_frames);
+  }
+  ti.active = ti.t0 < ti.M;
+  return ti;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_persistent(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcParams p,
+                       Epi e) {
+  constexpr int STAGES = persistent_stages<BN>();
+  constexpr int B_BYTES = BN * BK * 2;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t ACC_COLS = BN < 32 ? 32 : BN;
+  constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2];
+  __shared__ uint32_t tmem_base, issued;
+
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = p.tiles_f * p.tiles_t * p.nz;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 4); }
+    issued = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc(&tmem_base, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer.  Weights of the first tile's first slots go out before
+      // the dependency wait (they do not depend on the previous kernel).
+      int npre = 0;
+      if (e.kind != EPI_CROSSKV && blockIdx.x < T) {
+        const TileInfo ti = tile_of(p, e, blockIdx.x, BN);
+        if (ti.active) {
+          npre = p.kb_total < STAGES ? p.kb_total : STAGES;
+          for (int i = 0; i < npre; ++i) {
+            mbar_expect_tx(&full[i], STAGE_BYTES);
+            tma_load_2d(ring + i * STAGE_BYTES, &tmW, &full[i], i * BK, ti.tile_f * BM);
+          }
+        }
+      }
+      pdl_wait();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        const TileInfo ti = tile_of(p, e, t, BN);
+        if (!ti.active) continue;
+        for (int kb = 0; kb < p.kb_total; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          uint8_t* st = ring + s * STAGE_BYTES;
+          if ((int)it >= npre) {
+            if (!mbar_wait(&empty[s], ((it / STAGES) & 1u) ^ 1u)) { atomicOr(p.status, WS_ST_TIMEOUT); ok = false; break; }
+            mbar_expect_tx(&full[s], STAGE_BYTES);
+            tma_load_2d(st, &tmW, &full[s], kb * BK, ti.tile_f * BM);
+          }
+          tma_load_2d(st + A_BYTES, &tmX, &full[s], kb * BK, ti.row0 + ti.t0);
+        }
+      }
+      issued = it > (uint32_t)npre ? it : (uint32_t)npre;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      uint32_t it = 0, local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        if (e.kind == EPI_CROSSKV && t == (int)blockIdx.x) pdl_wait();
+        const TileInfo ti = tile_of(p, e, t, BN);
+        if (!ti.active) continue;
+        const uint32_t acc = local & 1u;
+        if (!mbar_wait(&acc_empty[acc], ((local >> 1) & 1u) ^ 1u)) { atomicOr(p.status, WS_ST_TIMEOUT); break; }
+        tc_fence_after();
+        const uint32_t d = tmem + acc * ACC_COLS;
+        for (int kb = 0; kb < p.kb_total; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          if (!mbar_wait(&full[s], (it / STAGES) & 1u)) { atomicOr(p.status, WS_ST_TIMEOUT); ok = false; break; }
+          tc_fence_after();
+          const uint32_t a = smem_u32(ring + s * STAGE_BYTES), b = a + A_BYTES;
+          const uint64_t ad = sdesc_sw128(a), bd = sdesc_sw128(b);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), IDESC, (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&acc_full[acc]);
+        ++local;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: warps 2..5 hold TMEM lane quarters 2, 3, 0, 1
+    pdl_wait();
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    uint32_t local = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+      const TileInfo ti = tile_of(p, e, t, BN);
+      if (!ti.active) continue;
+      const uint32_t acc = local & 1u;
+      const bool ok = mbar_wait(&acc_full[acc], (local >> 1) & 1u);
+      if (!ok) { if (lane == 0) atomicOr(p.status, WS_ST_TIMEOUT); break; }
+      tc_fence_after();
+      const uint32_t taddr = tmem + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+      const int n = ti.tile_f * BM + row;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        if (ti.t0 + c0 >= ti.M) break;
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)c0, v);
+        epi_columns16(e, p.N, ti.t0 + c0, n, ti.M, ti.z, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&acc_empty[acc])) : "memory");
+      ++local;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // every copy issued has landed (bounded), also after an early stop
+    const uint32_t n = issued, first = n > (uint32_t)STAGES ? n - STAGES : 0u;
+    for (uint32_t it = first; it < n; ++it)
+      if (!mbar_wait(&full[it % STAGES], (it / STAGES) & 1u)) { atomicOr(p.status, WS_ST_TIMEOUT); break; }
+  }
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+int g_sm_count = 0;
+
+template <int BN>
+cudaError_t launch_persistent(const GemmShape& g, const Epi& e, const CUtensorMap& mw, const CUtensorMap& mx,
+                              const TcParams& p, cudaStream_t s, bool pdl) {
+  const int T = p.tiles_f * p.tiles_t * p.nz;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T < g_sm_count ? T : g_sm_count);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = persistent_smem<BN>();
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_persistent<BN>, mw, mx, p, e);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 
@@ -274,17 +465,34 @@ cudaError_t tc_init_attributes() {
   set((const void*)gemm_tc_kernel<64, 4>, tc_smem<64, 4>());
   set((const void*)gemm_tc_kernel<128, 3>, tc_smem<128, 3>());
   set((const void*)gemm_tc_kernel<256, 4>, tc_smem<256, 4>());
+  set((const void*)gemm_tc_persistent<16>, persistent_smem<16>());
+  set((const void*)gemm_tc_persistent<32>, persistent_smem<32>());
+  set((const void*)gemm_tc_persistent<64>, persistent_smem<64>());
+  set((const void*)gemm_tc_persistent<128>, persistent_smem<128>());
+  set((const void*)gemm_tc_persistent<256>, persistent_smem<256>());
+  if (r == cudaSuccess) {
+    int dev = 0;
+    r = cudaGetDevice(&dev);
+    if (r == cudaSuccess) r = cudaDeviceGetAttribute(&g_sm_count, cudaDevAttrMultiProcessorCount, dev);
+  }
   return r;
 }
 
 int tc_bn_index(int bn) { return bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <= 128 ? 3 : 4; }
 
-int tc_pick_bn(int M) {
+// Token-tile width.  Up to 64 tokens: the smallest tile that holds them.
+// Beyond: the widest of 256 / 128 / 64 whose tile count (feature tiles x
+// token tiles x batch) still fills about the SMs.  A row's k order does not
+// depend on the width, so the choice never changes a result.
+int tc_pick_bn(int M, int N, int batch) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
-  if (M <= 128) return 128;
-  return 256;
+  const int tf = (N + BM - 1) / BM, b = batch > 0 ? batch : 1;
+  const int want = g_sm_count > 0 ? g_sm_count * 9 / 10 : 133;
+  for (int bn = 256; bn >= 128; bn /= 2)
+    if (tf * ((M + bn - 1) / bn) * b >= want) return bn;
+  return M <= 128 ? 128 : 64;
 }
 
 cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const TcMap* mx_cached,
@@ -292,7 +500,7 @@ cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, co
                            bool pdl) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
   if (g.K % BK != 0 || g.ldx != g.K) return cudaErrorInvalidValue;
-  const int BN = tc_pick_bn(g.M);
+  const int BN = tc_pick_bn(g.M, g.N, g.batch);
   TcMap mx;
   if (mx_cached) mx = *mx_cached;
   else if (!tc_encode_map(&mx, x_base, x_rows, (uint64_t)g.K, (uint32_t)BN)) return cudaErrorInvalidValue;
@@ -302,11 +510,21 @@ cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, co
   p.splits = splits < 1 ? 1 : (splits > p.kb_total ? p.kb_total : splits);
   p.tiles_f = (g.N + BM - 1) / BM;
   p.tiles_t = (g.M + BN - 1) / BN;
+  p.nz = g.batch > 0 ? g.batch : 1;
   p.status = e.status;
   // split-K partials live in the ring of each CTA of the cluster: BN <= 64 tokens
   if (p.splits > 1 && BN > 64) p.splits = 1;
   const CUtensorMap& W = *reinterpret_cast<const CUtensorMap*>(&mw);
   const CUtensorMap& X = *reinterpret_cast<const CUtensorMap*>(&mx);
+  if (p.splits == 1 && g_sm_count > 0) {
+    switch (BN) {
+      case 16: return launch_persistent<16>(g, e, W, X, p, s, pdl);
+      case 32: return launch_persistent<32>(g, e, W, X, p, s, pdl);
+      case 64: return launch_persistent<64>(g, e, W, X, p, s, pdl);
+      case 128: return launch_persistent<128>(g, e, W, X, p, s, pdl);
+      default: return launch_persistent<256>(g, e, W, X, p, s, pdl);
+    }
+  }
   switch (BN) {
     case 16: return launch_bn<16, 6>(g, e, W, X, p, s, pdl);
     case 32: return launch_bn<32, 5>(g, e, W, X, p, s, pdl);

@@ -291,7 +291,7 @@ struct AttnScratch {
 struct alignas(64) TcMap { unsigned char bytes[128]; };
 bool tc_engine_available();
 bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
-int tc_pick_bn(int M);
+int tc_pick_bn(int M, int N, int batch);
 // X is the row-major activation buffer [x_rows, K] (bf16); W's map has 128-row boxes.
 // mx_cached: the activation map for this call's token tile (tc_pick_bn), or
 // NULL to encode one from x_base / x_rows.
