@@ -58,6 +58,7 @@ struct ws_ctx {
   int mrows = 0;                // rows of the activation buffers
   AttnScratch as{};
   struct XMap { const void* base; TcMap bn[5]; };   // activation maps per token-tile width
+  TcMap xkv_map, kv_map;        // acoustic K/V and target self K/V as [rows, 64] (tensor-core attention)
   std::vector<XMap> xmaps;
   bool pdl = true;              // programmatic dependent launch allowed
   bool cur_pdl = false;         // PDL for the call in progress (never on the legacy stream)
@@ -655,6 +656,10 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
       c->xmaps.push_back(m);
     };
     xm(c->h, (int)D); xm(c->ao, (int)D); xm(c->ffn, desc->d_ff); xm(c->hh, (int)D);
+    // tensor-core attention: K/V chunks as 64 x 64 boxes of [rows, 64] matrices
+    ok = ok && tc_encode_map(&c->xkv_map, c->xkv, (uint64_t)desc->max_batch * c->x_slot_elems / WS_DH, WS_DH, 64);
+    ok = ok && tc_encode_map(&c->kv_map, c->kv, (uint64_t)desc->n_layers * p.kv_layer_bytes / (WS_DH * 2), WS_DH, 64);
+    if (ok) { c->as.xkv_map = &c->xkv_map; c->as.kv_map = &c->kv_map; c->as.kv_base = c->kv; }
     if (desc->drafter_layers > 0) xm(c->feat, (int)(desc->n_hist * D));
     if (ok && tc_init_attributes() != cudaSuccess) ok = false;
     if (!ok) { fail(nullptr, WS_ECUDA, "TMA descriptor encoding failed"); return cleanup(WS_ECUDA); }

@@ -14,7 +14,10 @@
 // fixed order, so a row's result does not depend on how many other rows
 // share the block: verifying a block and decoding one token at a time give
 // bit-identical rows.
+#include <cuda.h>
+
 #include "ws_attn_common.cuh"
+#include "ws_attn_mma.cuh"
 
 namespace {
 
@@ -190,6 +193,145 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AttnArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ tensor-core variant (bf16)
+// One CTA per (request, head, group of MG chunks of 64 keys); warp w handles
+// chunk group * MG + w.  Thread 0 stages each chunk's keys and values with
+// 2-D TMA loads (64 x 64 bf16 boxes, 128-byte swizzle) into shared memory;
+// the warp computes the chunk's partial with attn_chunk_partial and the last
+// CTA of (request, head) folds all partials in chunk order.
+constexpr int MG = 4;
+constexpr int CHUNK_BYTES = 2 * WS_XCHUNK * WS_DH * 2;   // K + V, 16 KB
+
+__device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(MG * 32) attn_mma_kernel(const __grid_constant__ CUtensorMap tmKV, AttnArgs a,
+                                                           const bf16* kv_base) {
+  extern __shared__ uint8_t dsm_m[];
+  __shared__ __align__(8) uint64_t bar[MG];
+  __shared__ int s_last;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_m) + 1023) & ~uintptr_t(1023));
+  const int i = blockIdx.x, head = blockIdx.y, grp = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads = a.d / WS_DH, H = a.H;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < MG; ++w)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[w])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  const int slot = a.req_ids[i];
+  int Lr = 0, nrow = H, kend;
+  if (MODE == MODE_SELF) {
+    Lr = a.L[slot];
+    nrow = min(a.block_len[i], H);
+    kend = min(Lr + nrow, a.max_pos);
+  } else {
+    kend = a.Fv[slot];
+  }
+  const int nch = min(MG, a.n_split - grp * MG);
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < nch; ++w) {
+      const int k_lo = (grp * MG + w) * WS_XCHUNK;
+      if (kend - k_lo <= 0) continue;
+      const bf16 *ks, *vs;
+      if (MODE == MODE_CROSS) {
+        ks = xkv_ptr<bf16>(a.x, slot, a.xlayer, 0, head, k_lo);
+        vs = xkv_ptr<bf16>(a.x, slot, a.xlayer, 1, head, k_lo);
+      } else {
+        ks = kv_ptr<bf16>(a.kv, slot, k_lo, 0, head);
+        vs = kv_ptr<bf16>(a.kv, slot, k_lo, 1, head);
+      }
+      uint8_t* dst = base + w * CHUNK_BYTES;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&bar[w])),
+                   "r"(CHUNK_BYTES) : "memory");
+      tma2d(dst, &tmKV, &bar[w], 0, (int)((ks - kv_base) / WS_DH));
+      tma2d(dst + CHUNK_BYTES / 2, &tmKV, &bar[w], 0, (int)((vs - kv_base) / WS_DH));
+    }
+  }
+  if (warp < nch) {
+    const int sp = grp * MG + warp, k_lo = sp * WS_XCHUNK;
+    const int nk = max(0, min(kend - k_lo, WS_XCHUNK));
+    auto part = [&](int j) {
+      return a.part + ((((size_t)i * H + j) * heads + head) * a.n_split + sp) * PART;
+    };
+    if (nk > 0) {
+      uint32_t qf[4][4];
+      attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
+      bool ok = mbar_wait(&bar[warp], 0);
+      if (!ok && lane == 0) atomicOr(a.status, WS_ST_TIMEOUT);
+      uint8_t* Ks = base + warp * CHUNK_BYTES;
+      uint8_t* Vs = Ks + CHUNK_BYTES / 2;
+      // keys nk..63 of the box are other rows: values there must be finite
+      // (they meet a zero weight in P V)
+      for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)
+        *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+      const int g = lane >> 2;
+      auto vis = [&](int j) {
+        if (j >= H) return 0;
+        if (MODE == MODE_CROSS) return nk;
+        if (j >= nrow) return 0;
+        return max(0, min(k_lo + nk, min(Lr + j + 1, a.max_pos)) - k_lo);
+      };
+      attn_chunk_partial<true>(Ks, Vs, qf, vis(g), vis(g + 8), H, part);
+    } else {
+      for (int j = 0; j < H; ++j) {
+        float* p = part(j);
+        if (lane == 0) { p[0] = -INFINITY; p[1] = 0.f; }
+        p[2 + 2 * lane] = 0.f;
+        p[3 + 2 * lane] = 0.f;
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int* c = a.counters + (size_t)i * heads + head;
+    const int old = atomicAdd(c, nch);
+    s_last = old + nch == a.n_split;
+    if (s_last) *c = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  bf16* O = reinterpret_cast<bf16*>(a.O);
+  for (int j = warp; j < H; j += MG) {
+    const float* p = a.part + (((size_t)i * H + j) * heads + head) * a.n_split * PART;
+    float o0, o1;
+    attn_fold_row(p, a.n_split, o0, o1);
+    bf16* o = O + ((size_t)i * H + j) * a.d + head * WS_DH + 2 * lane;
+    o[0] = __float2bfloat16_rn(o0);
+    o[1] = __float2bfloat16_rn(o1);
+  }
+}
+
+constexpr int MMA_SMEM = MG * CHUNK_BYTES + 1024;
+
+template <int MODE>
+cudaError_t launch_mma(const AttnArgs& a, int n, int heads, const CUtensorMap& map, const void* kv_base,
+                       cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n, heads, (a.n_split + MG - 1) / MG);
+  cfg.blockDim = dim3(MG * 32);
+  cfg.dynamicSmemBytes = MMA_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&cfg, attn_mma_kernel<MODE>, map, a, reinterpret_cast<const bf16*>(kv_base));
+}
+
 template <typename T>
 constexpr size_t attn_smem() {
   return 2 * SPLIT * WS_DH * sizeof(T) + SPLIT * (WS_DH + 1) * 4 + SPLIT * WS_DH * 4 + MAXR * WS_DH * 4 +
@@ -232,6 +374,10 @@ cudaError_t attn_init_attributes() {
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_split_kernel<T, MODE_DRAFT>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_mma_kernel<MODE_SELF>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_mma_kernel<MODE_CROSS>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM);
   return r;
 }
 
@@ -244,6 +390,9 @@ cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const K
   a.n_split = (rm.max_pos + SPLIT - 1) / SPLIT;
   a.req_ids = rm.req_ids; a.L = rm.L; a.block_len = rm.block_len;
   a.Q = Q; a.kv = kv; a.part = sc.part; a.counters = sc.counters; a.O = O; a.status = sc.status;
+  if (sizeof(T) == 2 && sc.kv_map)
+    return launch_mma<MODE_SELF>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.kv_map), sc.kv_base, s,
+                                 pdl);
   return launch_mode<T, MODE_SELF>(a, n, n_heads, s, pdl);
 }
 
@@ -257,6 +406,8 @@ cudaError_t launch_cross_attn(int n, int H, const int32_t* req_ids, const int32_
   a.n_split = max(1, (max_frames_seen + SPLIT - 1) / SPLIT);
   a.req_ids = req_ids; a.Fv = Fv; a.Q = Q; a.x = x; a.xlayer = layer;
   a.part = sc.part; a.counters = sc.counters; a.O = O; a.status = sc.status;
+  if (sizeof(T) == 2 && sc.xkv_map)
+    return launch_mma<MODE_CROSS>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.xkv_map), x.base, s, pdl);
   return launch_mode<T, MODE_CROSS>(a, n, n_heads, s, pdl);
 }
 

@@ -30,6 +30,7 @@
 #include <cudaTypedefs.h>
 
 #include "ws_attn_common.cuh"
+#include "ws_attn_mma.cuh"
 #include "ws_epilogue.cuh"
 #include "ws_fused.cuh"
 #include "ws_tc.cuh"
@@ -51,13 +52,10 @@ constexpr uint32_t TMEM_COLS = 32;
 constexpr long long SPIN_BUDGET = 1ll << 31;   // clock cycles (~1 s) before a grid barrier gives up
 constexpr int LN_MAXV = 10;          // layer-norm rows up to d = 1280 in 10 float4 per lane
 
-// attention scratch inside the work region
-constexpr int ATT_KT = 0;                                      // float Kt[64][65]
-constexpr int ATT_VT = ATT_KT + WS_XCHUNK * (WS_DH + 1) * 4;   // float Vt[64][64]
-constexpr int ATT_Q = ATT_VT + WS_XCHUNK * WS_DH * 4;          // float q[16][64]
-constexpr int ATT_PW = ATT_Q + MAXR * WS_DH * 4;               // float pw[7][32]
-constexpr int ATT_BYTES = ATT_PW + NCW * 32 * 4;
-static_assert(ATT_VT % 16 == 0 && ATT_Q % 16 == 0 && ATT_PW % 16 == 0, "aligned scratch");
+// attention scratch inside the work region: one chunk of keys and values (bf16)
+constexpr int ATT_K = 0;
+constexpr int ATT_V = ATT_K + WS_XCHUNK * WS_DH * 2;
+constexpr int ATT_BYTES = ATT_V + WS_XCHUNK * WS_DH * 2;
 
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -78,7 +76,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ float bf_bits(unsigned short u) { return __bfloat162float(__ushort_as_bfloat16(u)); }
 
 struct Shared {
   uint64_t full[FUSED_MAX_RING], empty[FUSED_MAX_RING], mma_done, la_bar;
@@ -486,10 +483,6 @@ __device__ void attn_stage(const FusedArgs& a, const FusedStage& st, int u0, uin
   const bool cross = st.kind == FS_CROSS;
   const int G = gridDim.x, R = a.ring_slots;
   const int tid = threadIdx.x - 32, warp = tid >> 5, lane = threadIdx.x & 31;
-  float (*Kt)[WS_DH + 1] = reinterpret_cast<float (*)[WS_DH + 1]>(work + ATT_KT);
-  float (*Vt)[WS_DH] = reinterpret_cast<float (*)[WS_DH]>(work + ATT_VT);
-  float (*qs)[WS_DH] = reinterpret_cast<float (*)[WS_DH]>(work + ATT_Q);
-  float* pw = reinterpret_cast<float*>(work + ATT_PW);
   const int nsplit = cross ? a.nsplit_cross : a.nsplit_self;
   const int per_req = a.heads * nsplit;
   const int units = a.n * per_req;
@@ -507,64 +500,64 @@ __device__ void attn_stage(const FusedArgs& a, const FusedStage& st, int u0, uin
       k_hi = min(a.Fv[slot], k_lo + WS_XCHUNK);
     }
     const int nk = max(0, k_hi - k_lo);
-    // query rows of this head (written by the previous stage on other SMs)
-    for (int idx = tid; idx < H * (WS_DH / 8); idx += NCT) {
-      const int j = idx / (WS_DH / 8), c = idx - j * (WS_DH / 8);
-      const uint4 q8 = __ldcg(reinterpret_cast<const uint4*>(a.q + ((size_t)i * H + j) * a.d + head * WS_DH + c * 8));
-      const unsigned short* h = reinterpret_cast<const unsigned short*>(&q8);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qs[j][c * 8 + e] = bf_bits(h[e]);
-    }
+    // keys / values of the chunk as linear [key][64] bf16 rows: the producer's
+    // ring slot (acoustic) or copied from the paged cache (self)
+    uint8_t* Ks = work + ATT_K;
+    uint8_t* Vs = work + ATT_V;
+    int s = -1;
     if (cross) {
-      const int s = (int)(it % (uint32_t)R);
+      s = (int)(it % (uint32_t)R);
       if (!mbar_wait(&sh.full[s], (it / (uint32_t)R) & 1u)) { atomicOr(a.status, WS_ST_TIMEOUT); sh.abort = 1; }
-      const unsigned short* kr = reinterpret_cast<const unsigned short*>(ring + (size_t)s * SLOT);
-      const unsigned short* vr = reinterpret_cast<const unsigned short*>(ring + (size_t)s * SLOT + KV_HALF);
-      for (int idx = tid; idx < nk * WS_DH; idx += NCT) {
-        const int k = idx / WS_DH, dd = idx - k * WS_DH;
-        Kt[k][dd] = bf_bits(kr[idx]);
-        Vt[k][dd] = bf_bits(vr[idx]);
-      }
-      compute_sync();
-      if (tid == 0) mbar_arrive(&sh.empty[s]);
+      Ks = ring + (size_t)s * SLOT;
+      Vs = Ks + KV_HALF;
       ++it;
-    } else {
+    } else if (nk > 0) {
+      KVPool pool;
+      pool.base = a.kv + (size_t)st.layer * a.kv_layer_bytes;
+      pool.ptab = a.ptab;
+      pool.ppr = a.ppr;
+      pool.n_heads = a.heads;
+      const bf16* ks = kv_ptr<bf16>(pool, slot, k_lo, 0, head);
+      const bf16* vs = kv_ptr<bf16>(pool, slot, k_lo, 1, head);
+      for (int idx = tid; idx < nk * (WS_DH / 8); idx += NCT) {
+        reinterpret_cast<uint4*>(Ks)[idx] = __ldcg(reinterpret_cast<const uint4*>(ks) + idx);
+        reinterpret_cast<uint4*>(Vs)[idx] = __ldcg(reinterpret_cast<const uint4*>(vs) + idx);
+      }
+    }
+    // values of keys nk..63 meet a zero weight in P V: make them finite
+    for (int idx = nk * (WS_DH / 8) + tid; idx < WS_XCHUNK * (WS_DH / 8); idx += NCT)
+      reinterpret_cast<uint4*>(Vs)[idx] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();      // the slot is refilled by TMA after it is released
+    compute_sync();
+    if (sh.abort) return;
+    // ---- the chunk's partial for all rows (one warp, tensor cores)
+    if (warp == 0) {
+      auto part = [&](int j) {
+        return a.apart + ((((size_t)i * H + j) * a.heads + head) * nsplit + sp) * WS_ATTN_PART;
+      };
       if (nk > 0) {
-        KVPool pool;
-        pool.base = a.kv + (size_t)st.layer * a.kv_layer_bytes;
-        pool.ptab = a.ptab;
-        pool.ppr = a.ppr;
-        pool.n_heads = a.heads;
-        const bf16* ks = kv_ptr<bf16>(pool, slot, k_lo, 0, head);
-        const bf16* vs = kv_ptr<bf16>(pool, slot, k_lo, 1, head);
-        for (int idx = tid; idx < nk * (WS_DH / 8); idx += NCT) {
-          const int k = idx / (WS_DH / 8), c = idx - k * (WS_DH / 8);
-          const uint4 k8 = __ldcg(reinterpret_cast<const uint4*>(ks + (size_t)k * WS_DH + c * 8));
-          const uint4 v8 = __ldcg(reinterpret_cast<const uint4*>(vs + (size_t)k * WS_DH + c * 8));
-          const unsigned short* hk = reinterpret_cast<const unsigned short*>(&k8);
-          const unsigned short* hv = reinterpret_cast<const unsigned short*>(&v8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            Kt[k][c * 8 + e] = bf_bits(hk[e]);
-            Vt[k][c * 8 + e] = bf_bits(hv[e]);
-          }
+        uint32_t qf[4][4];
+        attn_q_frags(a.q, a.d, i * H, H, head * WS_DH, qf);
+        auto vis = [&](int j) {
+          if (j >= H) return 0;
+          if (cross) return nk;
+          if (j >= nrow) return 0;
+          return max(0, min(k_hi, min(Lr + j + 1, a.max_pos)) - k_lo);
+        };
+        const int g = lane >> 2;
+        attn_chunk_partial<false>(Ks, Vs, qf, vis(g), vis(g + 8), H, part);
+      } else {
+        for (int j = 0; j < H; ++j) {
+          float* p = part(j);
+          if (lane == 0) { p[0] = -INFINITY; p[1] = 0.f; }
+          p[2 + 2 * lane] = 0.f;
+          p[3 + 2 * lane] = 0.f;
         }
       }
-      compute_sync();
     }
-    if (sh.abort) return;
-    // ---- one online softmax per row over this split
-    for (int j = warp; j < H; j += NCW) {
-      RowState rs;
-      rs.m = -INFINITY; rs.l = 0.f; rs.a0 = 0.f; rs.a1 = 0.f;
-      int visible = nk;
-      if (!cross) visible = (j < nrow) ? max(0, min(k_hi, min(Lr + j + 1, a.max_pos)) - k_lo) : 0;
-      for (int k0 = 0; k0 < visible; k0 += 32)
-        row_subtile(rs, qs[j], Kt, Vt, k0, min(32, visible - k0), pw + warp * 32);
-      float* p = a.apart + ((((size_t)i * H + j) * a.heads + head) * nsplit + sp) * WS_ATTN_PART;
-      if (lane == 0) { p[0] = rs.m; p[1] = rs.l; }
-      p[2 + 2 * lane] = rs.a0;
-      p[3 + 2 * lane] = rs.a1;
+    if (cross) {
+      compute_sync();
+      if (tid == 0) mbar_arrive(&sh.empty[s]);
     }
     // ---- the last split of (request, head) folds the partials in split order
     __threadfence();

@@ -280,11 +280,18 @@ struct GemmShape {
 
 template <typename T> cudaError_t launch_gemm_simt(const GemmShape& g, const Epi& e, cudaStream_t s, bool pdl);
 
-// Attention partials and the per-(request, head) arrival counters.
+struct TcMap;
+// Attention partials and the per-(request, head) arrival counters.  For the
+// tensor-core attention (bf16): TMA maps of the acoustic K/V slabs and of
+// the target self K/V pool as [rows, 64] bf16 matrices (64 x 64 boxes,
+// 128-byte swizzle); kv_base is the pool's row 0.
 struct AttnScratch {
   float* part;            // [rows][heads][splits][66]
   int* counters;          // [max_batch][heads], zero between launches
   int32_t* status;
+  const TcMap* xkv_map = nullptr;
+  const TcMap* kv_map = nullptr;
+  const void* kv_base = nullptr;
 };
 
 // tcgen05 engine (ws_gemm_tc.cu).  TcMap holds an encoded TMA tensor map.

@@ -6,6 +6,11 @@ import synth
 from oracle import model as M
 
 MARGIN = 1e-3     # near-tie rule: a token may differ where the oracle's top-2 margin is below this
+# bf16 configs: logits may differ from the oracle by up to 2e-2 relative, and
+# the measured top-2 margin differences at large-v3 (32 layers, |logits| < 3.4)
+# reach 9e-3 whatever the fp32 summation order, so there a near tie is a
+# margin below 1e-2 (test_large_v3_teacher_forced_margin_error pins the bound).
+MARGIN_BF16 = 1e-2
 
 
 def logits_close(gpu: np.ndarray, ora: np.ndarray, tol: float):
@@ -23,6 +28,14 @@ def logits_close(gpu: np.ndarray, ora: np.ndarray, tol: float):
 
 def greedy_near_tie(m) -> bool:
     return m < MARGIN
+
+
+def greedy_near_tie_bf16(m) -> bool:
+    return m < MARGIN_BF16
+
+
+def near_tie_for(dtype: str):
+    return greedy_near_tie_bf16 if dtype == "bf16" else greedy_near_tie
 
 
 def sampled_near_boundary(m) -> bool:
@@ -57,3 +70,31 @@ def small_shape(dtype="f32", **kw):
 
 def dev_i32(a, dev="cuda"):
     return torch.as_tensor(np.asarray(a, dtype=np.int32), device=dev)
+
+
+def teacher_forced_logits(dec, req, s, tokens):
+    """Logits of the one-request AR path fed the given tokens: the prompt
+    block, then one verify per token, each followed by a forced accept (the
+    cache advances exactly as in greedy decoding).  Returns [4 + len(tokens), V]
+    rows aligned with the oracle's forward_full over prompt + tokens."""
+    import speculative_whisper_asr_gb300.binding as B
+    stream = torch.cuda.current_stream().cuda_stream
+    dec.reset(req)
+    b = dec.new_batch(req, [10 ** 6])
+    out = []
+
+    def step(block):
+        H = len(block)
+        blk = dev_i32([block])
+        bl = dev_i32([H])
+        t = torch.zeros(1, H, dtype=torch.int32, device="cuda")
+        lg = torch.empty(1, H, s.vocab, device="cuda")
+        dec.verify(req, blk, bl, t, lg)
+        a = b._args(B.WS_ACCEPT_FORCED, H, blk, bl, t, b.block1, b.blen)
+        B.ws_accept(dec.ctx, 1, req.data_ptr(), a, stream)
+        out.append(lg[0].cpu().numpy())
+
+    step(list(s.prompt))
+    for tok in tokens:
+        step([tok])
+    return np.concatenate(out)

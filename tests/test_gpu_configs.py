@@ -24,7 +24,8 @@ import torch
 import synth
 from oracle import model as M
 from oracle import philox
-from gpu_common import dev_i32, logits_close, sampled_near_boundary, small_shape, tokens_match
+from gpu_common import (dev_i32, greedy_near_tie_bf16, logits_close, sampled_near_boundary, small_shape,
+                        tokens_match)
 
 pytestmark = pytest.mark.gpu
 
@@ -233,7 +234,7 @@ def test_turbo_batch16_continuation_drafts(RB):
     orc = M.Oracle(s, tw, None)
     for i in (0, n - 1):
         ref = M.greedy_cached(orc, orc.new_request(As[i]), 12)
-        tokens_match(ar[i][:12], ref.tokens, ref.margins)
+        tokens_match(ar[i][:12], ref.tokens, ref.margins, greedy_near_tie_bf16)
     assert dec.status() == 0
 
 
@@ -272,5 +273,5 @@ def test_varlen_batch64_packed_and_padded(RB):
     orc = M.Oracle(s, tw, None)
     i = int(np.argmin(F))
     ref = M.greedy_cached(orc, orc.new_request(As[i]), min(10, int(budgets[i])))
-    tokens_match(ar[i][:len(ref.tokens)], ref.tokens, ref.margins)
+    tokens_match(ar[i][:len(ref.tokens)], ref.tokens, ref.margins, greedy_near_tie_bf16)
     assert dec.status() == 0

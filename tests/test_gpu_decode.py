@@ -9,7 +9,7 @@ import torch
 
 import synth
 from oracle import model as M
-from gpu_common import MARGIN, dev_i32, logits_close, small_shape, tokens_match
+from gpu_common import MARGIN, dev_i32, logits_close, near_tie_for, small_shape, tokens_match
 
 pytestmark = pytest.mark.gpu
 
@@ -154,7 +154,7 @@ def test_small_batch_varlen(R, dtype):
     assert b2.transcripts() == ar
     for i in range(3):
         ref = M.greedy_cached(orc, orc.new_request(As[i]), budgets[i])
-        tokens_match(ar[i], ref.tokens, ref.margins)
+        tokens_match(ar[i], ref.tokens, ref.margins, near_tie_for(dtype))
     # prefill logits of every request
     dec.reset(req)
     blk = dev_i32([s.prompt] * 3)
