@@ -150,6 +150,8 @@ const char* check_desc(const ws_model_desc* d) {
   if (d->drafter_layers < 0 || d->drafter_layers > 8) return "drafter_layers out of range";
   if (d->K < 1 || d->K > 15) return "K must be 1..15";
   if (d->max_block < d->K + 1 || d->max_block > 16) return "max_block must be in K+1..16";
+  if ((double)d->max_batch * ((d->max_pos + WS_PAGE - 1) / WS_PAGE) * 2 * d->n_heads * WS_PAGE * WS_DH >= 2147483648.0)
+    return "self K/V pool of one layer must hold fewer than 2^31 elements";
   if (d->max_batch < 1 || d->max_batch > 4096) return "max_batch out of range";
   if (d->max_frames < 1 || d->max_frames > 4096) return "max_frames out of range";
   if (d->eos_id < 0 || d->eos_id >= d->vocab) return "eos_id outside the vocabulary";

@@ -229,6 +229,84 @@ __device__ __forceinline__ TileInfo tile_of(const TcParams& p, const Epi& e, int
   return ti;
 }
 
+// Fast epilogues of the persistent kernel for the kinds of large-token
+// calls: per tile, each thread's feature constants (bias, q/k/v part, head,
+// output column) are taken once, then every column is one add (and GELU) and
+// one store.  Per element the arithmetic is epi_pair's, so results match the
+// generic path bit for bit.  tok[c] (QKV only): element offset of token
+// t0 + c's cache row in a K/V page, or -1 where the token is not written.
+__device__ __forceinline__ bool fast_epilogue_kind(const Epi& e) {
+  return e.kind == EPI_STORE || e.kind == EPI_GELU || e.kind == EPI_CROSSKV || e.kind == EPI_QKV ||
+         (e.kind == EPI_RESID && e.hist == nullptr);
+}
+
+__device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int M, int n, int z, const float* v,
+                                                const int* tok, int c0) {
+  if (n >= N) return;
+  const int cmax = min(16, M - t);
+  switch (e.kind) {
+    case EPI_STORE:
+    case EPI_GELU: {
+      const float b = bias_at<bf16>(e.bias, n);
+      bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.ldo + n;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        if (c < cmax) {
+          float y = v[c] + b;
+          if (e.kind == EPI_GELU) y = gelu_erf(y);
+          o[(size_t)c * e.ldo] = __float2bfloat16_rn(y);
+        }
+      }
+      break;
+    }
+    case EPI_RESID: {
+      const float b = bias_at<bf16>(e.bias, n);
+      float* x = e.resid + (size_t)t * e.ldr + n;
+      float xr[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < cmax) xr[c] = __ldcg(x + (size_t)c * e.ldr);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < cmax) x[(size_t)c * e.ldr] = xr[c] + (v[c] + b);
+      break;
+    }
+    case EPI_CROSSKV: {
+      const int part = n / e.d, nn = n - part * e.d;
+      const float b = part == 1 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
+      bf16* o = xkv_ptr<bf16>(e.xkv, e.req_ids[z], e.xlayer, part, nn / WS_DH, t) + (nn % WS_DH);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < cmax) o[(size_t)c * WS_DH] = __float2bfloat16_rn(part == 1 ? v[c] + b : v[c]);
+      break;
+    }
+    case EPI_QKV: {
+      const int part = n / e.d, nn = n - part * e.d;
+      if (part == 0) {
+        const float b = bias_at<bf16>(e.bias, nn);
+        bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.d + nn;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (c < cmax) o[(size_t)c * e.d] = __float2bfloat16_rn(v[c] + b);
+      } else {
+        const float b = part == 2 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
+        bf16* base = reinterpret_cast<bf16*>(e.kv.base) +
+                     ((size_t)(part - 1) * e.kv.n_heads + nn / WS_DH) * (WS_PAGE * WS_DH) + (nn % WS_DH);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c < cmax) {
+            const int off = tok[c0 + c];
+            if (off >= 0) base[off] = __float2bfloat16_rn(part == 2 ? v[c] + b : v[c]);
+          }
+        }
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_persistent(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcParams p,
@@ -242,6 +320,7 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ __align__(1024) uint8_t dsm[];
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base, issued;
+  __shared__ int tok_tab[BN];
 
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -330,10 +409,25 @@ __global__ void __launch_bounds__(192, 1)
     pdl_wait();
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    const bool fast = fast_epilogue_kind(e);
     uint32_t local = 0;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
       const TileInfo ti = tile_of(p, e, t, BN);
       if (!ti.active) continue;
+      if (e.kind == EPI_QKV) {
+        // cache rows of this tile's tokens (one entry per column)
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        for (int c = row; c < BN; c += 128) {
+          int slot, j, pos, off = -1;
+          const int r = ti.t0 + c;
+          if (r < ti.M && row_info(e.rm, r, slot, j, pos)) {
+            const int page = e.kv.ptab[slot * e.kv.ppr + pos / WS_PAGE];
+            off = (int)((size_t)page * 2 * e.kv.n_heads * (WS_PAGE * WS_DH) + (size_t)(pos % WS_PAGE) * WS_DH);
+          }
+          tok_tab[c] = off;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+      }
       const uint32_t acc = local & 1u;
       const bool ok = mbar_wait(&acc_full[acc], (local >> 1) & 1u);
       if (!ok) { if (lane == 0) atomicOr(p.status, WS_ST_TIMEOUT); break; }
@@ -345,7 +439,8 @@ __global__ void __launch_bounds__(192, 1)
         if (ti.t0 + c0 >= ti.M) break;
         float v[16];
         tmem_ld16(taddr + (uint32_t)c0, v);
-        epi_columns16(e, p.N, ti.t0 + c0, n, ti.M, ti.z, v);
+        if (fast) fast_epilogue16(e, p.N, ti.t0 + c0, ti.M, n, ti.z, v, tok_tab, c0);
+        else epi_columns16(e, p.N, ti.t0 + c0, n, ti.M, ti.z, v);
       }
       tc_fence_before();
       __syncwarp();
