@@ -509,39 +509,53 @@ def run_varlen(args, rank: int, world: int, wl: Workload):
 
 # ---------------------------------------------------------------- profiling case
 def run_profile(args):
-    """Short case for kernel profilers: the same model and kernels as the
-    benchmark (acoustic K/V, prefill, then `--profile` speculative rounds
-    with uniformly random proposals), without the reference trajectory and
-    the CPU baseline.  The rounds run inside an NVTX range "ws_timed"."""
+    """Short case for kernel profilers: the workload's model and batch, its
+    acoustic K/V, prefill and two warm-up rounds, then `--profile` rounds
+    (or, with --profile-part cross_kv, that many acoustic K/V projections)
+    inside the NVTX range "ws_timed".  Rounds use random proposals (greedy
+    workloads) or the drafter's samples (sampling workloads).
+    --profile-layers L keeps the widths but builds L decoder layers, so a
+    full-metric capture holds a few GB."""
+    import dataclasses
     import torch
-    from speculative_whisper_asr_gb300 import binding as B
     from speculative_whisper_asr_gb300 import runtime as R
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
-    s = synth.LARGE_V3
-    n = args.batch
+    wl = make_workload(args.workload, args.batch)
+    s, n = wl.shape, wl.n
+    if args.profile_layers:
+        L = args.profile_layers
+        s = dataclasses.replace(s, n_layers=L, hist_layers=tuple(h for h in s.hist_layers if h < L) or (0,))
     tw = synth.target_weights(s, SEED)
     dw = synth.drafter_weights(s, SEED, tw)
-    dec = R.Decoder(s, tw, dw, max_batch=n, max_frames=1500)
+    F = [int(f) for f in wl.frames]
+    dec = R.Decoder(s, tw, dw, max_batch=n, max_frames=max(F))
     del tw, dw
     req = dec.slots(list(range(n)))
-    enc = torch.cat([dec.enc_tensor(synth.encoder_states(s, SEED, i)) for i in range(n)])
-    dec.cross_kv(req, enc, [1500] * n)
-    plan = synth.corruption_plan(n, s.max_pos, s.K, synth.corruption_p_const(s.K, 1.0), s.vocab, SEED)
-    syn = (torch.zeros(n, s.max_pos, dtype=torch.int32, device="cuda"), torch.as_tensor(plan.mask, device="cuda"),
-           torch.as_tensor(plan.tok, device="cuda"))
-    b = dec.new_batch(req, [BUDGET] * n)
-    b.prefill()
-    for _ in range(2):                       # warm-up rounds (graph capture)
-        b.spec_step(0, syn)
+    enc = torch.cat([dec.enc_tensor(synth.encoder_states(s, SEED, i, frames=F[i])) for i in range(n)])
+    dec.cross_kv(req, enc, F)
+    T, seed = wl.temperature, 7
+    b = dec.new_batch(req, [BUDGET] * n, sampling=T > 0)
+    syn = None
+    if T <= 0:
+        plan = synth.corruption_plan(n, s.max_pos, s.K, synth.corruption_p_const(s.K, 1.0), s.vocab, SEED)
+        syn = (torch.zeros(n, s.max_pos, dtype=torch.int32, device="cuda"), torch.as_tensor(plan.mask, device="cuda"),
+               torch.as_tensor(plan.tok, device="cuda"))
+    b.prefill(temperature=T, seed=seed)
+    for r in range(2):                       # warm-up rounds (graph capture)
+        b.spec_step(r + 1, syn, T, seed)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("ws_timed")
     for r in range(args.profile):
-        b.spec_step(0, syn)
+        if args.profile_part == "cross_kv":
+            dec.cross_kv(req, enc, F)
+        else:
+            b.spec_step(r + 3, syn, T, seed)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
-    print(json.dumps({"profile_rounds": args.profile, "status": dec.status(), "engine": dec.engine}))
+    print(json.dumps({"profile_rounds": args.profile, "part": args.profile_part, "workload": args.workload,
+                      "layers": s.n_layers, "status": dec.status(), "engine": dec.engine}))
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
@@ -579,6 +593,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", type=int, default=0, help="run N rounds of the profiling case and exit")
+    ap.add_argument("--profile-part", default="round", choices=["round", "cross_kv"])
+    ap.add_argument("--profile-layers", type=int, default=0, help="profiling case with fewer decoder layers")
     ap.add_argument("--workload", default="large-v3-b1", choices=WORKLOADS,
                     help="large-v3-b1 is the headline; the others measure the batch 16 / 96 and varlen cases")
     args = ap.parse_args()
