@@ -71,6 +71,8 @@ struct ws_ctx {
   float* fpart = nullptr;
   int* fctr = nullptr;
   unsigned* gbar = nullptr;
+  float2* pstat = nullptr;      // acceptance scratch: (max, sum exp) per p / q logits row
+  float2* qstat = nullptr;
   std::string err;
 };
 
@@ -133,7 +135,7 @@ struct Layout {
 struct Plan {
   size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
   size_t acnt;
-  size_t fmaps, fstages, fpart, fctr, gbar;
+  size_t fmaps, fstages, fpart, fctr, gbar, pstat, qstat;
   size_t kv_layer_bytes, total;
   int heads, ppr, n_pages, n_xl, max_split;
 };
@@ -207,6 +209,8 @@ Plan make_plan(const ws_model_desc& d) {
   p.fpart = lay.take((widest + 127) / 128 * 8 * FUSED_MAX_ROWS * 128 * 4);
   p.fctr = lay.take(((widest + 127) / 128 + 1) * 4);
   p.gbar = lay.take(64);
+  p.pstat = lay.take(M * 8);        // sampling acceptance: softmax statistics per logits row
+  p.qstat = lay.take(M * 8);
   p.total = lay.off;
   return p;
 }
@@ -637,6 +641,7 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   c->amax = (unsigned long long*)(b + p.amax); c->part = (float*)(b + p.part);
   c->as.part = c->part; c->as.counters = (int*)(b + p.acnt); c->as.status = st + 5 * desc->max_batch;
   c->feat = b + p.feat; c->hpre = (float*)(b + p.hpre); c->hh = b + p.hh;
+  c->pstat = (float2*)(b + p.pstat); c->qstat = (float2*)(b + p.qstat);
   c->mrows = desc->max_batch * desc->max_block;
   c->split_ok = c->mrows <= 64;
   if (c->engine == WS_GEMM_TC) {
@@ -752,6 +757,8 @@ int ws_accept(ws_ctx* c, int n, const int32_t* req, const ws_accept_args* a, ws_
   p.eos = c->d.eos_id;
   p.suppress = c->suppress;
   p.status = c->status;
+  p.pstat = c->pstat;
+  p.qstat = c->qstat;
   CK(launch_accept(n, p, (cudaStream_t)stream, c->cur_pdl));
   return WS_OK;
 }

@@ -354,7 +354,11 @@ struct AcceptParams {
   int K, V, eos;
   const uint32_t* suppress;
   int32_t* status;
+  float2* pstat;     // sampling: (max, sum exp) of each target row [n][H] at T ...
+  float2* qstat;     // ... and of each drafter row [n][K] (filled by launch_accept)
 };
+// Sampling acceptance first fills pstat / qstat with one CTA per logits row,
+// then runs one CTA per request.
 cudaError_t launch_accept(int n, const AcceptParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_draft_synth(int n, int K, const int32_t* req_ids, const int32_t* L, int32_t* block,
                                const int32_t* traj, int tlen, const uint8_t* cmask, const int32_t* ctok,

@@ -286,6 +286,18 @@ __global__ void __launch_bounds__(SNT) sample_rows_kernel(int rows, const int32_
   if (threadIdx.x == 0) out[(size_t)i * out_stride + out_col0 + r] = tok;
 }
 
+// (max, sum exp) of softmax(z / T) for every row of a [n][rows] block of
+// logits rows (row_stat, one CTA per row): the statistics the acceptance
+// kernel needs for p and q, computed in parallel instead of per request.
+__global__ void __launch_bounds__(SNT) row_stats_kernel(const float* logits, int rows, int V, float T,
+                                                        const uint32_t* sup, float2* out) {
+  __shared__ float sh[SNT + 8];
+  pdl_wait();
+  const RowStat st = row_stat(logits + (long long)blockIdx.x * V, V, T, sup, sh);
+  pdl_trigger();
+  if (threadIdx.x == 0) out[blockIdx.x] = make_float2(st.m, st.S);
+}
+
 // ------------------------------------------------------------------ acceptance
 // One CTA per request.  Whisper-Flash §3.1 / Appendix A.1 / A.4.
 __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
@@ -351,8 +363,10 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
       const int y = blk[j];
       const float* zp = A.p_logits + ((long long)i * A.H + (j - 1)) * P.V;
       const float* zq = A.q_logits + ((long long)i * P.K + (j - 1)) * P.V;
-      RowStat sp = row_stat(zp, P.V, T, P.suppress, sh);
-      RowStat sq = row_stat(zq, P.V, T, P.suppress, sh);
+      const float2 ps = P.pstat[(size_t)i * A.H + (j - 1)], qs = P.qstat[(size_t)i * P.K + (j - 1)];
+      RowStat sp, sq;
+      sp.m = ps.x; sp.S = ps.y;
+      sq.m = qs.x; sq.S = qs.y;
       const bool yok = y >= 0 && y < P.V;
       const float py = yok ? expf(scaled(zp, y, T, P.suppress) - sp.m) / sp.S : 0.0f;
       const float qy = yok ? expf(scaled(zq, y, T, P.suppress) - sq.m) / sq.S : 0.0f;
@@ -383,7 +397,9 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
     __syncthreads();
     if (s_stop == 0) {   // every candidate accepted: bonus from the target row n_prop
       const float* zp = A.p_logits + ((long long)i * A.H + n_prop) * P.V;
-      RowStat sp = row_stat(zp, P.V, T, P.suppress, sh);
+      const float2 ps = P.pstat[(size_t)i * A.H + n_prop];
+      RowStat sp;
+      sp.m = ps.x; sp.S = ps.y;
       const float u2 = ws_uniform(A.seed, (uint32_t)slot, A.round, (uint32_t)(n_prop + 1), 2u);
       int tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m) / sp.S; }, P.V, u2);
       if (threadIdx.x == 0) s_emit[s_ne++] = tok;
@@ -515,6 +531,23 @@ cudaError_t launch_sample_rows(int n, int rows, const int32_t* req_ids, const fl
 }
 cudaError_t launch_accept(int n, const AcceptParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
+  const ws_accept_args& a = p.a;
+  const bool sampling = a.p_logits && a.temperature > 0.0f &&
+                        (a.mode == WS_ACCEPT_SAMPLE || a.mode == WS_ACCEPT_FORCED);
+  if (sampling) {
+    cudaLaunchConfig_t c1 = make_cfg(dim3(n * a.H), dim3(SNT), 0, s, pdl, at);
+    ws_count_launches(1);
+    cudaError_t e = cudaLaunchKernelEx(&c1, row_stats_kernel, (const float*)a.p_logits, a.H, p.V, a.temperature,
+                                       p.suppress, p.pstat);
+    if (e != cudaSuccess) return e;
+    if (a.mode == WS_ACCEPT_SAMPLE) {
+      cudaLaunchConfig_t c2 = make_cfg(dim3(n * p.K), dim3(SNT), 0, s, pdl, at);
+      ws_count_launches(1);
+      e = cudaLaunchKernelEx(&c2, row_stats_kernel, (const float*)a.q_logits, p.K, p.V, a.temperature, p.suppress,
+                             p.qstat);
+      if (e != cudaSuccess) return e;
+    }
+  }
   cudaLaunchConfig_t cfg = make_cfg(dim3(n), dim3(SNT), 0, s, pdl, at);
   ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, accept_kernel, p);
