@@ -30,6 +30,7 @@ constexpr long long WAIT_BUDGET = 1ll << 32;
 enum { MODE_SELF = 0, MODE_CROSS = 1, MODE_DRAFT = 2 };
 
 struct AttnArgs {
+  int n_req;                 // requests in the call
   int H;                     // query rows per request
   int n_split;               // splits per (request, head); DRAFT: history splits + 1 block split
   int d, max_pos;
@@ -194,12 +195,8 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AttnArgs a) {
 }
 
 // ------------------------------------------------------------------ tensor-core variant (bf16)
-// One CTA per (request, head, group of MG chunks of 64 keys); warp w handles
-// chunk group * MG + w.  Thread 0 stages each chunk's keys and values with
-// 2-D TMA loads (64 x 64 bf16 boxes, 128-byte swizzle) into shared memory;
-// the warp computes the chunk's partial with attn_chunk_partial and the last
-// CTA of (request, head) folds all partials in chunk order.
-constexpr int MG = 4;
+// K/V chunks of 64 keys arrive by 2-D TMA (64 x 64 bf16 boxes, 128-byte
+// swizzle); attn_chunk_partial computes a chunk's partial on tensor cores.
 constexpr int CHUNK_BYTES = 2 * WS_XCHUNK * WS_DH * 2;   // K + V, 16 KB
 
 __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
@@ -209,71 +206,107 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_
       : "memory");
 }
 
+// ------------------------------------------------------------------ streaming variant
+// Persistent warps walk the (request, head, chunk) units: global warp gw =
+// blockIdx.x * SW + w takes units gw, gw + GW, gw + 2 GW, ... (GW = all
+// warps).  Each warp owns two 16 KB slots and stages its next unit's K and
+// V boxes by TMA while it computes the current one, so every SM keeps
+// several chunks in flight; a slot's mbarrier has one consumer, which
+// takes its phases in order.  A second kernel (attn_fold_kernel) folds each
+// row's chunk partials in chunk order.
+constexpr int SW = 2;                        // warps per CTA
+constexpr int STREAM_SMEM = SW * 2 * CHUNK_BYTES + 1024;
+
 template <int MODE>
-__global__ void __launch_bounds__(MG * 32) attn_mma_kernel(const __grid_constant__ CUtensorMap tmKV, AttnArgs a,
-                                                           const bf16* kv_base) {
-  extern __shared__ uint8_t dsm_m[];
-  __shared__ __align__(8) uint64_t bar[MG];
-  __shared__ int s_last;
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_m) + 1023) & ~uintptr_t(1023));
-  const int i = blockIdx.x, head = blockIdx.y, grp = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int heads = a.d / WS_DH, H = a.H;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < MG; ++w)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[w])) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  pdl_trigger();
-  pdl_wait();
+__device__ __forceinline__ void unit_range(const AttnArgs& a, int i, int sp, int& k_lo, int& nk, int& Lr, int& nrow) {
   const int slot = a.req_ids[i];
-  int Lr = 0, nrow = H, kend;
+  k_lo = sp * WS_XCHUNK;
+  Lr = 0;
+  nrow = a.H;
+  int kend;
   if (MODE == MODE_SELF) {
     Lr = a.L[slot];
-    nrow = min(a.block_len[i], H);
+    nrow = min(a.block_len[i], a.H);
     kend = min(Lr + nrow, a.max_pos);
   } else {
     kend = a.Fv[slot];
   }
-  const int nch = min(MG, a.n_split - grp * MG);
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < nch; ++w) {
-      const int k_lo = (grp * MG + w) * WS_XCHUNK;
-      if (kend - k_lo <= 0) continue;
-      const bf16 *ks, *vs;
-      if (MODE == MODE_CROSS) {
-        ks = xkv_ptr<bf16>(a.x, slot, a.xlayer, 0, head, k_lo);
-        vs = xkv_ptr<bf16>(a.x, slot, a.xlayer, 1, head, k_lo);
-      } else {
-        ks = kv_ptr<bf16>(a.kv, slot, k_lo, 0, head);
-        vs = kv_ptr<bf16>(a.kv, slot, k_lo, 1, head);
-      }
-      uint8_t* dst = base + w * CHUNK_BYTES;
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&bar[w])),
-                   "r"(CHUNK_BYTES) : "memory");
-      tma2d(dst, &tmKV, &bar[w], 0, (int)((ks - kv_base) / WS_DH));
-      tma2d(dst + CHUNK_BYTES / 2, &tmKV, &bar[w], 0, (int)((vs - kv_base) / WS_DH));
-    }
+  nk = max(0, min(kend - k_lo, WS_XCHUNK));
+}
+
+// Issue unit u's K and V boxes into dst (lane 0); returns whether bytes were requested.
+template <int MODE>
+__device__ __forceinline__ bool stage_unit(const AttnArgs& a, const CUtensorMap* map, const bf16* kv_base, int u,
+                                           uint8_t* dst, uint64_t* bar) {
+  const int heads = a.d / WS_DH, ns = a.n_split;
+  const int i = u / (heads * ns), head = (u / ns) % heads, sp = u % ns;
+  int k_lo, nk, Lr, nrow;
+  unit_range<MODE>(a, i, sp, k_lo, nk, Lr, nrow);
+  if (nk <= 0) return false;
+  const int slot = a.req_ids[i];
+  const bf16 *ks, *vs;
+  if (MODE == MODE_CROSS) {
+    ks = xkv_ptr<bf16>(a.x, slot, a.xlayer, 0, head, k_lo);
+    vs = xkv_ptr<bf16>(a.x, slot, a.xlayer, 1, head, k_lo);
+  } else {
+    ks = kv_ptr<bf16>(a.kv, slot, k_lo, 0, head);
+    vs = kv_ptr<bf16>(a.kv, slot, k_lo, 1, head);
   }
-  if (warp < nch) {
-    const int sp = grp * MG + warp, k_lo = sp * WS_XCHUNK;
-    const int nk = max(0, min(kend - k_lo, WS_XCHUNK));
-    auto part = [&](int j) {
-      return a.part + ((((size_t)i * H + j) * heads + head) * a.n_split + sp) * PART;
-    };
-    if (nk > 0) {
-      uint32_t qf[4][4];
-      attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
-      bool ok = mbar_wait(&bar[warp], 0);
-      if (!ok && lane == 0) atomicOr(a.status, WS_ST_TIMEOUT);
-      uint8_t* Ks = base + warp * CHUNK_BYTES;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier reads / writes of the slot first
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(CHUNK_BYTES)
+               : "memory");
+  tma2d(dst, map, bar, 0, (int)((ks - kv_base) / WS_DH));
+  tma2d(dst + CHUNK_BYTES / 2, map, bar, 0, (int)((vs - kv_base) / WS_DH));
+  return true;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_constant__ CUtensorMap tmKV, AttnArgs a,
+                                                               const bf16* kv_base) {
+  extern __shared__ uint8_t dsm_s[];
+  __shared__ __align__(8) uint64_t bar[SW][2];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_s) + 1023) & ~uintptr_t(1023));
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads = a.d / WS_DH, H = a.H, ns = a.n_split;
+  const int total = a.n_req * heads * ns;
+  const int gw = blockIdx.x * SW + w, GW = gridDim.x * SW;
+  uint8_t* slot_mem[2] = {base + (2 * w) * CHUNK_BYTES, base + (2 * w + 1) * CHUNK_BYTES};
+  if (lane == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[w][0])) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[w][1])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  pdl_trigger();
+  pdl_wait();
+  // loaded[b]: slot b holds a requested (not yet consumed) copy; uses[b]: phases issued on bar[w][b]
+  bool loaded[2] = {false, false};
+  uint32_t uses[2] = {0u, 0u};
+  if (lane == 0 && gw < total) loaded[0] = stage_unit<MODE>(a, &tmKV, kv_base, gw, slot_mem[0], &bar[w][0]);
+  loaded[0] = __shfl_sync(0xffffffffu, loaded[0], 0);
+  int m = 0;
+  for (int u = gw; u < total; u += GW, ++m) {
+    const int cur = m & 1, nxt = cur ^ 1;
+    // prefetch the next unit into the other slot (consumed in the previous iteration)
+    const int un = u + GW;
+    bool ln = false;
+    if (lane == 0 && un < total) ln = stage_unit<MODE>(a, &tmKV, kv_base, un, slot_mem[nxt], &bar[w][nxt]);
+    ln = __shfl_sync(0xffffffffu, ln, 0);
+    const int i = u / (heads * ns), head = (u / ns) % heads, sp = u % ns;
+    int k_lo, nk, Lr, nrow;
+    unit_range<MODE>(a, i, sp, k_lo, nk, Lr, nrow);
+    auto part = [&](int j) { return a.part + ((((size_t)i * H + j) * heads + head) * ns + sp) * PART; };
+    if (loaded[cur]) {
+      const bool ok = mbar_wait(&bar[w][cur], uses[cur] & 1u);
+      ++uses[cur];
+      if (!ok) { if (lane == 0) atomicOr(a.status, WS_ST_TIMEOUT); break; }
+      uint8_t* Ks = slot_mem[cur];
       uint8_t* Vs = Ks + CHUNK_BYTES / 2;
-      // keys nk..63 of the box are other rows: values there must be finite
-      // (they meet a zero weight in P V)
-      for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)
+      for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)   // finite values beyond the keys
         *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
       __syncwarp();
+      uint32_t qf[4][4];
+      attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
       const int g = lane >> 2;
       auto vis = [&](int j) {
         if (j >= H) return 0;
@@ -290,38 +323,43 @@ __global__ void __launch_bounds__(MG * 32) attn_mma_kernel(const __grid_constant
         p[3 + 2 * lane] = 0.f;
       }
     }
+    __syncwarp();                 // the slot is free for the unit after next
+    loaded[cur] = false;
+    loaded[nxt] = ln;
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int* c = a.counters + (size_t)i * heads + head;
-    const int old = atomicAdd(c, nch);
-    s_last = old + nch == a.n_split;
-    if (s_last) *c = 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  bf16* O = reinterpret_cast<bf16*>(a.O);
-  for (int j = warp; j < H; j += MG) {
-    const float* p = a.part + (((size_t)i * H + j) * heads + head) * a.n_split * PART;
-    float o0, o1;
-    attn_fold_row(p, a.n_split, o0, o1);
-    bf16* o = O + ((size_t)i * H + j) * a.d + head * WS_DH + 2 * lane;
-    o[0] = __float2bfloat16_rn(o0);
-    o[1] = __float2bfloat16_rn(o1);
-  }
+  // copies still requested (an early stop) land before exit (bounded)
+  for (int b = 0; b < 2; ++b)
+    if (loaded[b] && lane == 0 && !mbar_wait(&bar[w][b], uses[b] & 1u)) atomicOr(a.status, WS_ST_TIMEOUT);
+  __syncwarp();
 }
 
-constexpr int MMA_SMEM = MG * CHUNK_BYTES + 1024;
+// One warp per (request, row, head): fold the row's chunk partials in order.
+__global__ void __launch_bounds__(512) attn_fold_kernel(AttnArgs a) {
+  pdl_wait();
+  const int i = blockIdx.x, head = blockIdx.y, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads = a.d / WS_DH;
+  pdl_trigger();
+  if (j >= a.H) return;
+  const float* p = a.part + (((size_t)i * a.H + j) * heads + head) * a.n_split * PART;
+  float o0, o1;
+  attn_fold_row(p, a.n_split, o0, o1);
+  bf16* o = reinterpret_cast<bf16*>(a.O) + ((size_t)i * a.H + j) * a.d + head * WS_DH + 2 * lane;
+  o[0] = __float2bfloat16_rn(o0);
+  o[1] = __float2bfloat16_rn(o1);
+}
+
+int g_attn_sms = 0;
 
 template <int MODE>
-cudaError_t launch_mma(const AttnArgs& a, int n, int heads, const CUtensorMap& map, const void* kv_base,
-                       cudaStream_t s, bool pdl) {
+cudaError_t launch_stream(const AttnArgs& a, int n, int heads, const CUtensorMap& map, const void* kv_base,
+                          cudaStream_t s, bool pdl) {
+  const int total = n * heads * a.n_split;
+  const int cap = 3 * (g_attn_sms > 0 ? g_attn_sms : 148);       // three CTAs (six warps) per SM
+  const int ctas = (total + SW - 1) / SW;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n, heads, (a.n_split + MG - 1) / MG);
-  cfg.blockDim = dim3(MG * 32);
-  cfg.dynamicSmemBytes = MMA_SMEM;
+  cfg.gridDim = dim3(ctas < cap ? ctas : cap);
+  cfg.blockDim = dim3(SW * 32);
+  cfg.dynamicSmemBytes = STREAM_SMEM;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -329,7 +367,16 @@ cudaError_t launch_mma(const AttnArgs& a, int n, int heads, const CUtensorMap& m
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
   ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg, attn_mma_kernel<MODE>, map, a, reinterpret_cast<const bf16*>(kv_base));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_stream_kernel<MODE>, map, a, reinterpret_cast<const bf16*>(kv_base));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t f = {};
+  f.gridDim = dim3(n, heads);
+  f.blockDim = dim3(32 * a.H);
+  f.stream = s;
+  f.attrs = at;
+  f.numAttrs = pdl ? 1 : 0;
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&f, attn_fold_kernel, a);
 }
 
 template <typename T>
@@ -374,10 +421,15 @@ cudaError_t attn_init_attributes() {
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_split_kernel<T, MODE_DRAFT>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_mma_kernel<MODE_SELF>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM);
-  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_mma_kernel<MODE_CROSS>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_stream_kernel<MODE_SELF>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_stream_kernel<MODE_CROSS>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
+  if (r == cudaSuccess) {
+    int dev = 0;
+    r = cudaGetDevice(&dev);
+    if (r == cudaSuccess) r = cudaDeviceGetAttribute(&g_attn_sms, cudaDevAttrMultiProcessorCount, dev);
+  }
   return r;
 }
 
@@ -390,9 +442,10 @@ cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const K
   a.n_split = (rm.max_pos + SPLIT - 1) / SPLIT;
   a.req_ids = rm.req_ids; a.L = rm.L; a.block_len = rm.block_len;
   a.Q = Q; a.kv = kv; a.part = sc.part; a.counters = sc.counters; a.O = O; a.status = sc.status;
+  a.n_req = n;
   if (sizeof(T) == 2 && sc.kv_map)
-    return launch_mma<MODE_SELF>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.kv_map), sc.kv_base, s,
-                                 pdl);
+    return launch_stream<MODE_SELF>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.kv_map), sc.kv_base, s,
+                                    pdl);
   return launch_mode<T, MODE_SELF>(a, n, n_heads, s, pdl);
 }
 
@@ -406,8 +459,10 @@ cudaError_t launch_cross_attn(int n, int H, const int32_t* req_ids, const int32_
   a.n_split = max(1, (max_frames_seen + SPLIT - 1) / SPLIT);
   a.req_ids = req_ids; a.Fv = Fv; a.Q = Q; a.x = x; a.xlayer = layer;
   a.part = sc.part; a.counters = sc.counters; a.O = O; a.status = sc.status;
+  a.n_req = n;
   if (sizeof(T) == 2 && sc.xkv_map)
-    return launch_mma<MODE_CROSS>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.xkv_map), x.base, s, pdl);
+    return launch_stream<MODE_CROSS>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.xkv_map), x.base, s,
+                                     pdl);
   return launch_mode<T, MODE_CROSS>(a, n, n_heads, s, pdl);
 }
 
