@@ -208,8 +208,10 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_
 
 // ------------------------------------------------------------------ streaming variant
 // Persistent warps walk the (request, head, chunk) units: global warp gw =
-// blockIdx.x * SW + w takes units gw, gw + GW, gw + 2 GW, ... (GW = all
-// warps).  Each warp owns two 16 KB slots and stages its next unit's K and
+// blockIdx.x * SW + w takes the contiguous range [gw * U / GW, (gw + 1) * U
+// / GW) of the U units (GW = all warps), so it streams one (request, head)'s
+// chunks in key order and reloads its query fragments only when the head
+// changes.  Each warp owns two 16 KB slots and stages its next unit's K and
 // V boxes by TMA while it computes the current one, so every SM keeps
 // several chunks in flight; a slot's mbarrier has one consumer, which
 // takes its phases in order.  A second kernel (attn_fold_kernel) folds each
@@ -282,15 +284,17 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
   // loaded[b]: slot b holds a requested (not yet consumed) copy; uses[b]: phases issued on bar[w][b]
   bool loaded[2] = {false, false};
   uint32_t uses[2] = {0u, 0u};
-  if (lane == 0 && gw < total) loaded[0] = stage_unit<MODE>(a, &tmKV, kv_base, gw, slot_mem[0], &bar[w][0]);
+  const int u_beg = (int)((long long)gw * total / GW), u_end = (int)((long long)(gw + 1) * total / GW);
+  if (lane == 0 && u_beg < u_end) loaded[0] = stage_unit<MODE>(a, &tmKV, kv_base, u_beg, slot_mem[0], &bar[w][0]);
   loaded[0] = __shfl_sync(0xffffffffu, loaded[0], 0);
-  int m = 0;
-  for (int u = gw; u < total; u += GW, ++m) {
+  int m = 0, qi = -1, qh = -1;
+  uint32_t qf[4][4];
+  for (int u = u_beg; u < u_end; ++u, ++m) {
     const int cur = m & 1, nxt = cur ^ 1;
     // prefetch the next unit into the other slot (consumed in the previous iteration)
-    const int un = u + GW;
+    const int un = u + 1;
     bool ln = false;
-    if (lane == 0 && un < total) ln = stage_unit<MODE>(a, &tmKV, kv_base, un, slot_mem[nxt], &bar[w][nxt]);
+    if (lane == 0 && un < u_end) ln = stage_unit<MODE>(a, &tmKV, kv_base, un, slot_mem[nxt], &bar[w][nxt]);
     ln = __shfl_sync(0xffffffffu, ln, 0);
     const int i = u / (heads * ns), head = (u / ns) % heads, sp = u % ns;
     int k_lo, nk, Lr, nrow;
@@ -305,8 +309,11 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
       for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)   // finite values beyond the keys
         *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
       __syncwarp();
-      uint32_t qf[4][4];
-      attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
+      if (i != qi || head != qh) {
+        attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
+        qi = i;
+        qh = head;
+      }
       const int g = lane >> 2;
       auto vis = [&](int j) {
         if (j >= H) return 0;
