@@ -46,6 +46,85 @@ struct TcParams {
   int32_t* status;
 };
 
+// Fast epilogues: per tile, each thread's feature constants (bias, q/k/v
+// part, head, output column) are taken once, then every column is one add
+// (and GELU) and one store.  Per element the arithmetic is epi_pair's, so
+// results match the generic path bit for bit.  tok[c] (QKV only): element
+// offset of token t0 + c's cache row in a K/V page, or -1 where the token is
+// not written.  xpre (RESID, optional): the 16 residual values of this
+// thread's feature, already loaded.
+__device__ __forceinline__ bool fast_epilogue_kind(const Epi& e) {
+  return e.kind == EPI_STORE || e.kind == EPI_GELU || e.kind == EPI_CROSSKV || e.kind == EPI_QKV ||
+         (e.kind == EPI_RESID && e.hist == nullptr);
+}
+
+__device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int M, int n, int z, const float* v,
+                                                const int* tok, int c0, const float* xpre = nullptr) {
+  if (n >= N) return;
+  const int cmax = min(16, M - t);
+  switch (e.kind) {
+    case EPI_STORE:
+    case EPI_GELU: {
+      const float b = bias_at<bf16>(e.bias, n);
+      bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.ldo + n;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        if (c < cmax) {
+          float y = v[c] + b;
+          if (e.kind == EPI_GELU) y = gelu_erf(y);
+          o[(size_t)c * e.ldo] = __float2bfloat16_rn(y);
+        }
+      }
+      break;
+    }
+    case EPI_RESID: {
+      const float b = bias_at<bf16>(e.bias, n);
+      float* x = e.resid + (size_t)t * e.ldr + n;
+      float xr[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < cmax) xr[c] = xpre ? xpre[c] : __ldcg(x + (size_t)c * e.ldr);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < cmax) x[(size_t)c * e.ldr] = xr[c] + (v[c] + b);
+      break;
+    }
+    case EPI_CROSSKV: {
+      const int part = n / e.d, nn = n - part * e.d;
+      const float b = part == 1 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
+      bf16* o = xkv_ptr<bf16>(e.xkv, e.req_ids[z], e.xlayer, part, nn / WS_DH, t) + (nn % WS_DH);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < cmax) o[(size_t)c * WS_DH] = __float2bfloat16_rn(part == 1 ? v[c] + b : v[c]);
+      break;
+    }
+    case EPI_QKV: {
+      const int part = n / e.d, nn = n - part * e.d;
+      if (part == 0) {
+        const float b = bias_at<bf16>(e.bias, nn);
+        bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.d + nn;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (c < cmax) o[(size_t)c * e.d] = __float2bfloat16_rn(v[c] + b);
+      } else {
+        const float b = part == 2 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
+        bf16* base = reinterpret_cast<bf16*>(e.kv.base) +
+                     ((size_t)(part - 1) * e.kv.n_heads + nn / WS_DH) * (WS_PAGE * WS_DH) + (nn % WS_DH);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c < cmax) {
+            const int off = tok[c0 + c];
+            if (off >= 0) base[off] = __float2bfloat16_rn(part == 2 ? v[c] + b : v[c]);
+          }
+        }
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(128, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcParams p,
@@ -103,6 +182,29 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (early) pdl_wait();
 
+  // Epilogue inputs that do not depend on the MMAs are loaded now, while the
+  // weights stream (one-token-tile calls): this thread's residual values and
+  // the cache rows of the tile's tokens.
+  __shared__ int tok_tab[16];
+  float xpre[16];
+  const bool pre_resid = BN == 16 && active && e.kind == EPI_RESID && e.hist == nullptr;
+  if (pre_resid) {
+    const int pn = f0 + warp * 32 + lane;
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      xpre[c] = (t0 + c < M && pn < p.N) ? __ldcg(e.resid + (size_t)(t0 + c) * e.ldr + pn) : 0.0f;
+  }
+  if (BN == 16 && active && e.kind == EPI_QKV && threadIdx.x < 16) {
+    int slot, j, pos, off = -1;
+    const int r = t0 + (int)threadIdx.x;
+    if (r < M && row_info(e.rm, r, slot, j, pos)) {
+      const int page = e.kv.ptab[slot * e.kv.ppr + pos / WS_PAGE];
+      off = (int)((size_t)page * 2 * e.kv.n_heads * (WS_PAGE * WS_DH) + (size_t)(pos % WS_PAGE) * WS_DH);
+    }
+    tok_tab[threadIdx.x] = off;
+  }
+  const bool fast16 = BN == 16 && (pre_resid || e.kind == EPI_QKV || e.kind == EPI_STORE || e.kind == EPI_GELU);
+
   if (threadIdx.x == 0 && active) {
     // ---- producer
     for (int i = 0; i < npre; ++i)
@@ -151,7 +253,8 @@ __global__ void __launch_bounds__(128, 1)
     for (int c0 = 0; c0 < BN; c0 += 16) {
       float v[16];
       tmem_ld16(taddr + (uint32_t)c0, v);
-      epi_columns16(e, p.N, t0 + c0, n, M, z, v);
+      if (fast16) fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr);
+      else epi_columns16(e, p.N, t0 + c0, n, M, z, v);
     }
   } else if (active && p.splits > 1) {
     // Split-K: the splits of one tile form a thread-block cluster.  Each CTA
@@ -185,7 +288,8 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] += w[c];
         }
-        epi_columns16(e, p.N, t0 + c0, n, M, z, v);
+        if (fast16) fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr);
+        else epi_columns16(e, p.N, t0 + c0, n, M, z, v);
       }
     }
     cl.sync();
@@ -227,84 +331,6 @@ __device__ __forceinline__ TileInfo tile_of(const TcParams& p, const Epi& e, int
   }
   ti.active = ti.t0 < ti.M;
   return ti;
-}
-
-// Fast epilogues of the persistent kernel for the kinds of large-token
-// calls: per tile, each thread's feature constants (bias, q/k/v part, head,
-// output column) are taken once, then every column is one add (and GELU) and
-// one store.  Per element the arithmetic is epi_pair's, so results match the
-// generic path bit for bit.  tok[c] (QKV only): element offset of token
-// t0 + c's cache row in a K/V page, or -1 where the token is not written.
-__device__ __forceinline__ bool fast_epilogue_kind(const Epi& e) {
-  return e.kind == EPI_STORE || e.kind == EPI_GELU || e.kind == EPI_CROSSKV || e.kind == EPI_QKV ||
-         (e.kind == EPI_RESID && e.hist == nullptr);
-}
-
-__device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int M, int n, int z, const float* v,
-                                                const int* tok, int c0) {
-  if (n >= N) return;
-  const int cmax = min(16, M - t);
-  switch (e.kind) {
-    case EPI_STORE:
-    case EPI_GELU: {
-      const float b = bias_at<bf16>(e.bias, n);
-      bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.ldo + n;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        if (c < cmax) {
-          float y = v[c] + b;
-          if (e.kind == EPI_GELU) y = gelu_erf(y);
-          o[(size_t)c * e.ldo] = __float2bfloat16_rn(y);
-        }
-      }
-      break;
-    }
-    case EPI_RESID: {
-      const float b = bias_at<bf16>(e.bias, n);
-      float* x = e.resid + (size_t)t * e.ldr + n;
-      float xr[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        if (c < cmax) xr[c] = __ldcg(x + (size_t)c * e.ldr);
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        if (c < cmax) x[(size_t)c * e.ldr] = xr[c] + (v[c] + b);
-      break;
-    }
-    case EPI_CROSSKV: {
-      const int part = n / e.d, nn = n - part * e.d;
-      const float b = part == 1 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
-      bf16* o = xkv_ptr<bf16>(e.xkv, e.req_ids[z], e.xlayer, part, nn / WS_DH, t) + (nn % WS_DH);
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        if (c < cmax) o[(size_t)c * WS_DH] = __float2bfloat16_rn(part == 1 ? v[c] + b : v[c]);
-      break;
-    }
-    case EPI_QKV: {
-      const int part = n / e.d, nn = n - part * e.d;
-      if (part == 0) {
-        const float b = bias_at<bf16>(e.bias, nn);
-        bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.d + nn;
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          if (c < cmax) o[(size_t)c * e.d] = __float2bfloat16_rn(v[c] + b);
-      } else {
-        const float b = part == 2 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
-        bf16* base = reinterpret_cast<bf16*>(e.kv.base) +
-                     ((size_t)(part - 1) * e.kv.n_heads + nn / WS_DH) * (WS_PAGE * WS_DH) + (nn % WS_DH);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          if (c < cmax) {
-            const int off = tok[c0 + c];
-            if (off >= 0) base[off] = __float2bfloat16_rn(part == 2 ? v[c] + b : v[c]);
-          }
-        }
-      }
-      break;
-    }
-    default:
-      break;
-  }
 }
 
 template <int BN>
