@@ -300,6 +300,11 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
     int k_lo, nk, Lr, nrow;
     unit_range<MODE>(a, i, sp, k_lo, nk, Lr, nrow);
     auto part = [&](int j) { return a.part + ((((size_t)i * H + j) * heads + head) * ns + sp) * PART; };
+    if (loaded[cur] && (i != qi || head != qh)) {      // query fragments while the chunk lands
+      attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
+      qi = i;
+      qh = head;
+    }
     if (loaded[cur]) {
       const bool ok = mbar_wait(&bar[w][cur], uses[cur] & 1u);
       ++uses[cur];
@@ -309,11 +314,6 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
       for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)   // finite values beyond the keys
         *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
       __syncwarp();
-      if (i != qi || head != qh) {
-        attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
-        qi = i;
-        qh = head;
-      }
       const int g = lane >> 2;
       auto vis = [&](int j) {
         if (j >= H) return 0;

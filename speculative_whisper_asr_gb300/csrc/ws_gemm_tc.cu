@@ -58,14 +58,25 @@ __device__ __forceinline__ bool fast_epilogue_kind(const Epi& e) {
          (e.kind == EPI_RESID && e.hist == nullptr);
 }
 
+// Bias of feature n as the fast epilogue adds it (q / v bias for QKV, none for k).
+__device__ __forceinline__ float fast_bias(const Epi& e, int n) {
+  if (e.kind == EPI_QKV || e.kind == EPI_CROSSKV) {
+    const int part = n / e.d, nn = n - part * e.d;
+    if (e.kind == EPI_QKV) return part == 0 ? bias_at<bf16>(e.bias, nn) : part == 2 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
+    return part == 1 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
+  }
+  return bias_at<bf16>(e.bias, n);
+}
+
 __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int M, int n, int z, const float* v,
-                                                const int* tok, int c0, const float* xpre = nullptr) {
+                                                const int* tok, int c0, const float* xpre = nullptr,
+                                                const float* bpre = nullptr) {
   if (n >= N) return;
   const int cmax = min(16, M - t);
   switch (e.kind) {
     case EPI_STORE:
     case EPI_GELU: {
-      const float b = bias_at<bf16>(e.bias, n);
+      const float b = bpre ? *bpre : bias_at<bf16>(e.bias, n);
       bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.ldo + n;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
@@ -78,7 +89,7 @@ __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int 
       break;
     }
     case EPI_RESID: {
-      const float b = bias_at<bf16>(e.bias, n);
+      const float b = bpre ? *bpre : bias_at<bf16>(e.bias, n);
       float* x = e.resid + (size_t)t * e.ldr + n;
       float xr[16];
 #pragma unroll
@@ -101,13 +112,13 @@ __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int 
     case EPI_QKV: {
       const int part = n / e.d, nn = n - part * e.d;
       if (part == 0) {
-        const float b = bias_at<bf16>(e.bias, nn);
+        const float b = bpre ? *bpre : bias_at<bf16>(e.bias, nn);
         bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.d + nn;
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           if (c < cmax) o[(size_t)c * e.d] = __float2bfloat16_rn(v[c] + b);
       } else {
-        const float b = part == 2 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
+        const float b = bpre ? *bpre : (part == 2 ? bias_at<bf16>(e.bias2, nn) : 0.0f);
         bf16* base = reinterpret_cast<bf16*>(e.kv.base) +
                      ((size_t)(part - 1) * e.kv.n_heads + nn / WS_DH) * (WS_PAGE * WS_DH) + (nn % WS_DH);
 #pragma unroll
@@ -180,6 +191,11 @@ __global__ void __launch_bounds__(128, 1)
       tma_load_2d(ring + i * STAGE_BYTES, &tmW, &full[i], (kb0 + i) * BK, f0);
     }
   }
+  // the bias of this thread's feature is a weight: load it before the wait
+  float bpre = 0.0f;
+  if (BN == 16 && active && (e.kind == EPI_RESID || e.kind == EPI_QKV || e.kind == EPI_STORE || e.kind == EPI_GELU) &&
+      f0 + warp * 32 + lane < p.N)
+    bpre = fast_bias(e, f0 + warp * 32 + lane);
   if (early) pdl_wait();
 
   // Epilogue inputs that do not depend on the MMAs are loaded now, while the
@@ -253,7 +269,7 @@ __global__ void __launch_bounds__(128, 1)
     for (int c0 = 0; c0 < BN; c0 += 16) {
       float v[16];
       tmem_ld16(taddr + (uint32_t)c0, v);
-      if (fast16) fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr);
+      if (fast16) fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr, &bpre);
       else epi_columns16(e, p.N, t0 + c0, n, M, z, v);
     }
   } else if (active && p.splits > 1) {
@@ -288,7 +304,7 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] += w[c];
         }
-        if (fast16) fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr);
+        if (fast16) fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr, &bpre);
         else epi_columns16(e, p.N, t0 + c0, n, M, z, v);
       }
     }
