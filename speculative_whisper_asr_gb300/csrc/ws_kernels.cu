@@ -102,6 +102,13 @@ template <typename T>
 __global__ void __launch_bounds__(32) layernorm_kernel(int M, int d, const float* x, int ldx, const T* g,
                                                        const T* b, T* y, int ldy, int group_skip) {
   pdl_trigger();
+  // gain and bias are weights: bring this lane's groups into L1 before the
+  // dependency wait, so the normalisation does not wait on L2 after the
+  // reductions
+  for (int k = 4 * (int)threadIdx.x; k < d; k += 128) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(g + k));
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(b + k));
+  }
   pdl_wait();
   const int o = blockIdx.x;
   if (o >= M) return;
