@@ -280,13 +280,19 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
   }
   __syncwarp();
   pdl_trigger();
-  pdl_wait();
+  // Acoustic K/V, frame counts and request ids were all written before this
+  // library call began (the first kernel of every call releases its
+  // dependents only after its own dependency wait), so cross-attention
+  // stages its first chunk before waiting on the previous kernel; only the
+  // queries depend on it.  Self-attention reads cache rows this call wrote.
+  if (MODE == MODE_SELF) pdl_wait();
   // loaded[b]: slot b holds a requested (not yet consumed) copy; uses[b]: phases issued on bar[w][b]
   bool loaded[2] = {false, false};
   uint32_t uses[2] = {0u, 0u};
   const int u_beg = (int)((long long)gw * total / GW), u_end = (int)((long long)(gw + 1) * total / GW);
   if (lane == 0 && u_beg < u_end) loaded[0] = stage_unit<MODE>(a, &tmKV, kv_base, u_beg, slot_mem[0], &bar[w][0]);
   loaded[0] = __shfl_sync(0xffffffffu, loaded[0], 0);
+  if (MODE == MODE_CROSS) pdl_wait();
   int m = 0, qi = -1, qh = -1;
   uint32_t qf[4][4];
   for (int u = u_beg; u < u_end; ++u, ++m) {
