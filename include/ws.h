@@ -242,6 +242,17 @@ const char* ws_gemm_engine(const ws_ctx* ctx);
  * WS_EINVAL for a null context.  Host-only; no device work. */
 int ws_fused_verify(ws_ctx* ctx, int enable);
 
+/* Layer norm inside the projection GEMMs (Whisper-Flash §3.1 block
+ * verification runs the target's pre-LN decoder layers: a LayerNorm before
+ * self-attention, cross-attention and the MLP).  A bf16 context on the tcgen05 engine normalises the
+ * residual rows inside the split-K GEMM that consumes them when a call has
+ * at most 16 rows, instead of running a separate layer-norm kernel; the
+ * normalised operand is bit-identical either way.  On by default.
+ *   enable  1: use it when eligible (the default); 0: never; -1: query only.
+ * Returns 1 when on, 0 when off, or WS_EINVAL for a null context.
+ * Host-only; no device work. */
+int ws_fused_layernorm(ws_ctx* ctx, int enable);
+
 /* CUDA-graph replay of a fixed call sequence (Whisper-Flash Appendix A.5
  * replays prefill, drafting and each verification length from captured
  * graphs).  Between ws_capture_begin and ws_capture_end every ws_* call on

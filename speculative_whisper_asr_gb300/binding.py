@@ -22,7 +22,8 @@ WS_ACCEPT_GREEDY, WS_ACCEPT_SAMPLE, WS_ACCEPT_FORCED = 0, 1, 2
 EXPORTS = ("ws_query_workspace", "ws_load_weights", "ws_reset", "ws_cross_kv", "ws_verify", "ws_draft",
            "ws_accept", "ws_draft_synthetic", "ws_sample", "ws_set_suppress", "ws_get_lengths", "ws_status",
            "ws_gemm_engine", "ws_launch_count", "ws_last_error", "ws_free", "ws_capture_begin",
-           "ws_capture_end", "ws_graph_launch", "ws_graph_free", "ws_argmax_rows_noalloc", "ws_fused_verify")
+           "ws_capture_end", "ws_graph_launch", "ws_graph_free", "ws_argmax_rows_noalloc", "ws_fused_verify",
+           "ws_fused_layernorm")
 
 
 class WSError(RuntimeError):
@@ -69,6 +70,7 @@ def _load():
         "ws_status": (I, [P, S, C.POINTER(C.c_int32)]),
         "ws_gemm_engine": (C.c_char_p, [P]),
         "ws_fused_verify": (C.c_int, [P, C.c_int]),
+        "ws_fused_layernorm": (C.c_int, [P, C.c_int]),
         "ws_launch_count": (C.c_ulonglong, []),
         "ws_last_error": (C.c_char_p, [P]),
         "ws_free": (None, [P]),
@@ -171,6 +173,14 @@ def ws_gemm_engine(ctx) -> str:
 def ws_fused_verify(ctx, enable: int = -1) -> int:
     """Switch the persistent verify path (1 on, 0 off, -1 query); returns 1 when in use."""
     r = lib.ws_fused_verify(ctx, enable)
+    if r < 0:
+        raise WSError(r, lib.ws_last_error(ctx).decode())
+    return r
+
+
+def ws_fused_layernorm(ctx, enable: int = -1) -> int:
+    """Switch layer norm inside eligible GEMMs (1 on, 0 off, -1 query); returns 1 when on."""
+    r = lib.ws_fused_layernorm(ctx, enable)
     if r < 0:
         raise WSError(r, lib.ws_last_error(ctx).decode())
     return r

@@ -64,6 +64,7 @@ struct ws_ctx {
   bool cur_pdl = false;         // PDL for the call in progress (never on the legacy stream)
   // persistent block verification (bf16, tcgen05, at most 16 rows per call)
   bool fused_ok = false;        // built and runnable on this device
+  bool ln_in_gemm = true;       // layer norm inside eligible GEMMs (ws_fused_layernorm)
   bool fused_on = false;        // caller's switch (ws_fused_verify); off: the per-op path is faster here
   int fused_grid = 0, fused_ring = 0, n_fstages = 0;
   size_t fused_work = 0;
@@ -272,11 +273,18 @@ int splits_for(const ws_ctx* c, int N, int K) {
 }
 
 // Y = X W^T with a fused epilogue.  X has x_rows allocated rows.
+struct LnIn {
+  const float* x;
+  const void* g;
+  const void* b;
+};
+
 template <typename T>
 cudaError_t gemm(ws_ctx* c, const void* X, uint64_t x_rows, const Mat& W, int M, const Epi& e, cudaStream_t s,
-                 int batch = 1, bool allow_split = true) {
+                 int batch = 1, bool allow_split = true, const LnIn* ln = nullptr) {
   GemmShape g;
   g.X = X; g.ldx = W.cols; g.W = W.p; g.ldw = W.cols; g.M = M; g.N = W.rows; g.K = W.cols; g.batch = batch;
+  if (ln) { g.ln_x = ln->x; g.ln_g = ln->g; g.ln_b = ln->b; }
   if (c->engine == WS_GEMM_TC && sizeof(T) == 2)
   {
     const TcMap* mx = nullptr;
@@ -292,10 +300,17 @@ template <typename T>
 cudaError_t layernorm(ws_ctx* c, int M, const float* x, const void* g, const void* b, void* y,
                       cudaStream_t s, int group_skip = 0);
 
-// Y = LayerNorm(x) W^T: a layer-norm kernel writes c->h, the GEMM reads it.
+// Y = LayerNorm(x) W^T.  Small split-K calls on the tcgen05 engine normalise
+// inside the GEMM (bit-identical operand); otherwise a layer-norm kernel
+// writes c->h and the GEMM reads it.
 template <typename T>
 cudaError_t ln_gemm(ws_ctx* c, int M, const float* x, const void* g, const void* b, const Mat& W, const Epi& e,
                     cudaStream_t s, int group_skip = 0) {
+  if (sizeof(T) == 2 && group_skip == 0 && c->ln_in_gemm && c->engine == WS_GEMM_TC &&
+      tc_ln_input_ok(M, W.rows, W.cols, splits_for(c, W.rows, W.cols))) {
+    const LnIn ln = {x, g, b};
+    return gemm<T>(c, c->h, c->mrows, W, M, e, s, 1, true, &ln);
+  }
   cudaError_t r = layernorm<T>(c, M, x, g, b, c->h, s, group_skip);
   if (r != cudaSuccess) return r;
   return gemm<T>(c, c->h, c->mrows, W, M, e, s);
@@ -820,6 +835,12 @@ int ws_fused_verify(ws_ctx* c, int enable) {
   if (!c) return fail(nullptr, WS_EINVAL, "null context");
   if (enable >= 0) c->fused_on = enable != 0;
   return (c->fused_ok && c->fused_on) ? 1 : 0;
+}
+
+int ws_fused_layernorm(ws_ctx* c, int enable) {
+  if (!c) return fail(nullptr, WS_EINVAL, "null context");
+  if (enable >= 0) c->ln_in_gemm = enable != 0;
+  return c->ln_in_gemm ? 1 : 0;
 }
 
 unsigned long long ws_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -108,14 +108,17 @@ __device__ __forceinline__ float epi_logit(const Epi& e, int n, float y) {
 // n (consecutive across the warp) and v[c] is its value for row t + c.
 // LOGITS reduces each row's (value, id) key over the warp before one
 // atomicMax; the other kinds pair features (n, n + 1) through a shuffle.
-__device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n, int M, int z, const float* v) {
+// Only columns c_lo <= c < c_hi are stored.
+__device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n, int M, int z, const float* v,
+                                              int c_lo = 0, int c_hi = 16) {
   const int lane = threadIdx.x & 31;
+  const int mc = min(M, t + c_hi), m0 = t + c_lo;     // rows m0 <= r < mc
   if (e.kind == EPI_LOGITS) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int r = t + c;
       unsigned long long key = 0ull;
-      if (r < M && n < N) {
+      if (r >= m0 && r < mc && n < N) {
         const float y = epi_logit(e, n, v[c]);
         if (e.logits) e.logits[(long long)r * e.ldl + n] = y;
         key = argmax_key(y, n);
@@ -138,7 +141,7 @@ __device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n,
 #pragma unroll
     for (int c = 0; c < 16; c += 2) {
       const int r = t + c + odd;
-      if (r < M && nn + 1 < N) xr[c / 2] = __ldcg(reinterpret_cast<const float2*>(e.resid + (size_t)r * e.ldr + nn));
+      if (r >= m0 && r < mc && nn + 1 < N) xr[c / 2] = __ldcg(reinterpret_cast<const float2*>(e.resid + (size_t)r * e.ldr + nn));
     }
 #pragma unroll
     for (int c = 0; c < 16; c += 2) {
@@ -146,7 +149,7 @@ __device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n,
       const float pc1 = __shfl_xor_sync(0xffffffffu, v[c + 1], 1);
       const int r = t + c + odd;
       const float y0 = odd ? pc1 : v[c], y1 = odd ? v[c + 1] : pc0;
-      if (r < M && nn + 1 < N) {
+      if (r >= m0 && r < mc && nn + 1 < N) {
         const float v0 = xr[c / 2].x + (y0 + b0), v1 = xr[c / 2].y + (y1 + b1);
         *reinterpret_cast<float2*>(e.resid + (size_t)r * e.ldr + nn) = make_float2(v0, v1);
         if (e.hist) {
@@ -165,10 +168,10 @@ __device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n,
     const float pc1 = __shfl_xor_sync(0xffffffffu, v[c + 1], 1);
     if ((lane & 1) == 0) {
       const int r = t + c;
-      if (r < M && n + 1 < N) epi_pair<bf16>(e, r, n, v[c], pc0, z);
+      if (r >= m0 && r < mc && n + 1 < N) epi_pair<bf16>(e, r, n, v[c], pc0, z);
     } else {
       const int r = t + c + 1;
-      if (r < M && n < N) epi_pair<bf16>(e, r, n - 1, pc1, v[c + 1], z);
+      if (r >= m0 && r < mc && n < N) epi_pair<bf16>(e, r, n - 1, pc1, v[c + 1], z);
     }
   }
 }

@@ -44,6 +44,12 @@ struct TcParams {
   int tiles_f, tiles_t;
   int nz;                // batch entries (CROSSKV: requests)
   int32_t* status;
+  // Layer-norm input (split-K, one token tile, all k-blocks of a CTA in the
+  // ring at once): B = LayerNorm(ln_x; ln_g, ln_b) built in the kernel, rows
+  // of ln_x K floats apart; ln_x == nullptr: B is loaded through tmX.
+  const float* ln_x;
+  const void* ln_g;
+  const void* ln_b;
 };
 
 // Fast epilogues: per tile, each thread's feature constants (bias, q/k/v
@@ -68,11 +74,13 @@ __device__ __forceinline__ float fast_bias(const Epi& e, int n) {
   return bias_at<bf16>(e.bias, n);
 }
 
+// Columns c_lo <= c < c_hi of the 16 are stored (the others are another
+// CTA's share of a split-K tile).
 __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int M, int n, int z, const float* v,
                                                 const int* tok, int c0, const float* xpre = nullptr,
-                                                const float* bpre = nullptr) {
+                                                const float* bpre = nullptr, int c_lo = 0, int c_hi = 16) {
   if (n >= N) return;
-  const int cmax = min(16, M - t);
+  const int cmax = min(c_hi, M - t);
   switch (e.kind) {
     case EPI_STORE:
     case EPI_GELU: {
@@ -80,7 +88,7 @@ __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int 
       bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.ldo + n;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        if (c < cmax) {
+        if (c >= c_lo && c < cmax) {
           float y = v[c] + b;
           if (e.kind == EPI_GELU) y = gelu_erf(y);
           o[(size_t)c * e.ldo] = __float2bfloat16_rn(y);
@@ -94,10 +102,10 @@ __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int 
       float xr[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        if (c < cmax) xr[c] = xpre ? xpre[c] : __ldcg(x + (size_t)c * e.ldr);
+        if (c >= c_lo && c < cmax) xr[c] = xpre ? xpre[c] : __ldcg(x + (size_t)c * e.ldr);
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        if (c < cmax) x[(size_t)c * e.ldr] = xr[c] + (v[c] + b);
+        if (c >= c_lo && c < cmax) x[(size_t)c * e.ldr] = xr[c] + (v[c] + b);
       break;
     }
     case EPI_CROSSKV: {
@@ -106,7 +114,7 @@ __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int 
       bf16* o = xkv_ptr<bf16>(e.xkv, e.req_ids[z], e.xlayer, part, nn / WS_DH, t) + (nn % WS_DH);
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        if (c < cmax) o[(size_t)c * WS_DH] = __float2bfloat16_rn(part == 1 ? v[c] + b : v[c]);
+        if (c >= c_lo && c < cmax) o[(size_t)c * WS_DH] = __float2bfloat16_rn(part == 1 ? v[c] + b : v[c]);
       break;
     }
     case EPI_QKV: {
@@ -116,14 +124,14 @@ __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int 
         bf16* o = reinterpret_cast<bf16*>(e.out) + (size_t)t * e.d + nn;
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          if (c < cmax) o[(size_t)c * e.d] = __float2bfloat16_rn(v[c] + b);
+          if (c >= c_lo && c < cmax) o[(size_t)c * e.d] = __float2bfloat16_rn(v[c] + b);
       } else {
         const float b = bpre ? *bpre : (part == 2 ? bias_at<bf16>(e.bias2, nn) : 0.0f);
         bf16* base = reinterpret_cast<bf16*>(e.kv.base) +
                      ((size_t)(part - 1) * e.kv.n_heads + nn / WS_DH) * (WS_PAGE * WS_DH) + (nn % WS_DH);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          if (c < cmax) {
+          if (c >= c_lo && c < cmax) {
             const int off = tok[c0 + c];
             if (off >= 0) base[off] = __float2bfloat16_rn(part == 2 ? v[c] + b : v[c]);
           }
@@ -156,6 +164,12 @@ __global__ void __launch_bounds__(128, 1)
   const int kb0 = (int)((long long)split * p.kb_total / p.splits);
   const int kb1 = (int)((long long)(split + 1) * p.kb_total / p.splits);
   const int nkb = kb1 - kb0;
+  // columns of each 16-column group this CTA stores: all, or with split K its
+  // share (the cluster rank of a split is its index)
+  const int c_lo = p.splits > 1 ? split * 16 / p.splits : 0;
+  const int c_hi = p.splits > 1 ? (split + 1) * 16 / p.splits : 16;
+  const bool lnin = BN == 16 && p.ln_x != nullptr;
+  const uint32_t stage_tx = lnin ? (uint32_t)A_BYTES : (uint32_t)STAGE_BYTES;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -187,9 +201,14 @@ __global__ void __launch_bounds__(128, 1)
   const int npre = active ? (nkb < STAGES ? nkb : STAGES) : 0;
   if (threadIdx.x == 0) {
     for (int i = 0; i < npre; ++i) {
-      mbar_expect_tx(&full[i], STAGE_BYTES);
+      mbar_expect_tx(&full[i], stage_tx);
       tma_load_2d(ring + i * STAGE_BYTES, &tmW, &full[i], (kb0 + i) * BK, f0);
     }
+  }
+  // layer-norm gain and bias of this CTA's k-range are weights: into L1 now
+  if (lnin && active && (int)threadIdx.x < 2 * nkb) {
+    const bf16* src = reinterpret_cast<const bf16*>((threadIdx.x & 1) ? p.ln_b : p.ln_g);
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(src + (kb0 + (int)(threadIdx.x >> 1)) * BK));
   }
   // the bias of this thread's feature is a weight: load it before the wait
   float bpre = 0.0f;
@@ -208,7 +227,8 @@ __global__ void __launch_bounds__(128, 1)
     const int pn = f0 + warp * 32 + lane;
 #pragma unroll
     for (int c = 0; c < 16; ++c)
-      xpre[c] = (t0 + c < M && pn < p.N) ? __ldcg(e.resid + (size_t)(t0 + c) * e.ldr + pn) : 0.0f;
+      xpre[c] = (c >= c_lo && c < c_hi && t0 + c < M && pn < p.N) ? __ldcg(e.resid + (size_t)(t0 + c) * e.ldr + pn)
+                                                                  : 0.0f;
   }
   if (BN == 16 && active && e.kind == EPI_QKV && threadIdx.x < 16) {
     int slot, j, pos, off = -1;
@@ -221,11 +241,46 @@ __global__ void __launch_bounds__(128, 1)
   }
   const bool fast16 = BN == 16 && (pre_resid || e.kind == EPI_QKV || e.kind == EPI_STORE || e.kind == EPI_GELU);
 
+  if (lnin && active) {
+    // B = LayerNorm(x) for token rows t0 .. t0 + 15 and this CTA's k-blocks,
+    // written into the B half of ring slot i (k-block kb0 + i) in the layout a
+    // 16-row x 64-column TMA box with 128-byte swizzle has: row r at byte
+    // r * 128, 16-byte chunk c at chunk c ^ (r & 7).  Warp w normalises rows
+    // w, w + 4, w + 8, w + 12 (all loads of a warp in one memory round trip)
+    // with the layer-norm kernel's per-row warp arithmetic, so the operand is
+    // bit-identical to the normalised copy that kernel would write.
+    const int nr = min(BN, M - t0), k_lo = kb0 * BK;
+    const int nrw = nr > warp ? (nr - warp + 3) >> 2 : 0;     // rows warp + 4j < nr
+    const float* xs[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) xs[j] = p.ln_x + (size_t)(t0 + warp + 4 * j) * p.K;   // read for j < nrw only
+    ln_rows_warp<true, 4, 10>(
+        xs, nrw, p.K, p.ln_g, p.ln_b, true,
+        [&](int j, int k, float v0, float v1, float v2, float v3) {
+          const int r = warp + 4 * j, kl = k - k_lo, col = kl & 63;
+          __nv_bfloat162 h0 = __floats2bfloat162_rn(v0, v1), h1 = __floats2bfloat162_rn(v2, v3);
+          uint2 w;
+          w.x = *reinterpret_cast<uint32_t*>(&h0);
+          w.y = *reinterpret_cast<uint32_t*>(&h1);
+          *reinterpret_cast<uint2*>(ring + (kl >> 6) * STAGE_BYTES + A_BYTES + r * 128 +
+                                    ((((col >> 3) ^ (r & 7)) << 4) | ((col & 7) * 2))) = w;
+        },
+        k_lo, kb1 * BK);
+    for (int idx = threadIdx.x; idx < (BN - nr) * nkb * 8; idx += 128) {   // rows nr .. 15 are zero
+      const int r = nr + idx / (nkb * 8), rem = idx % (nkb * 8);
+      *reinterpret_cast<uint4*>(ring + (rem >> 3) * STAGE_BYTES + A_BYTES + r * 128 + ((rem & 7) << 4)) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core
+    __syncthreads();
+  }
+
   if (threadIdx.x == 0 && active) {
     // ---- producer
-    for (int i = 0; i < npre; ++i)
-      tma_load_2d(ring + i * STAGE_BYTES + A_BYTES, &tmX, &full[i], (kb0 + i) * BK, row0 + t0);
-    for (int i = npre; i < nkb; ++i) {
+    if (!lnin)
+      for (int i = 0; i < npre; ++i)
+        tma_load_2d(ring + i * STAGE_BYTES + A_BYTES, &tmX, &full[i], (kb0 + i) * BK, row0 + t0);
+    for (int i = npre; i < nkb; ++i) {     // (none with a layer-norm input: nkb <= STAGES)
       const int s = i % STAGES;
       const uint32_t ph = (uint32_t)((i / STAGES) & 1);
       if (!mbar_wait(&empty[s], ph ^ 1u)) { atomicOr(p.status, WS_ST_TIMEOUT); break; }
@@ -278,6 +333,10 @@ __global__ void __launch_bounds__(128, 1)
     // the others through distributed shared memory and adds them in split
     // order 0, 1, 2, ...  Every CTA of an active cluster reaches both cluster
     // barriers, also after a timed-out wait.
+    // Every rank then folds its own share of each 16-column group (columns
+    // [c_lo, c_hi)), reading the partials of ranks 0, 1, 2, ... through
+    // distributed shared memory and adding them in that order, and stores
+    // those columns; the ranks' shares are disjoint and cover the group.
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
     float* mine = reinterpret_cast<float*>(ring);
@@ -289,24 +348,26 @@ __global__ void __launch_bounds__(128, 1)
       for (int c = 0; c < 16; ++c) mine[(c0 + c) * BM + row] = ok ? v[c] : 0.0f;
     }
     cl.sync();
-    if (cl.block_rank() == 0) {
+    const float* part[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) part[r] = cl.map_shared_rank(mine, r < p.splits ? r : 0);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      float v[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) v[c] = mine[(c0 + c) * BM + row];
-#pragma unroll 1
-        for (int r = 1; r < p.splits; ++r) {
-          const float* rem = cl.map_shared_rank(mine, r);
-          float w[16];
+      for (int c = 0; c < 16; ++c) {
+        float a = 0.0f;
+        if (c >= c_lo && c < c_hi) {
+          a = part[0][(c0 + c) * BM + row];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) w[c] = rem[(c0 + c) * BM + row];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] += w[c];
+          for (int r = 1; r < 8; ++r)
+            if (r < p.splits) a += part[r][(c0 + c) * BM + row];
         }
-        if (fast16) fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr, &bpre);
-        else epi_columns16(e, p.N, t0 + c0, n, M, z, v);
+        v[c] = a;
       }
+      if (fast16)
+        fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr, &bpre, c_lo, c_hi);
+      else epi_columns16(e, p.N, t0 + c0, n, M, z, v, c_lo, c_hi);
     }
     cl.sync();
   }
@@ -632,6 +693,12 @@ int tc_pick_bn(int M, int N, int batch) {
   return M <= 128 ? 128 : 64;
 }
 
+bool tc_ln_input_ok(int M, int N, int K, int splits) {
+  if (M <= 0 || K % 128 != 0 || K > 1280 || tc_pick_bn(M, N, 1) != 16) return false;
+  const int kb = K / BK, s = splits < 1 ? 1 : (splits > kb ? kb : splits);
+  return s > 1 && (kb + s - 1) / s <= 6;     // 6: ring slots of gemm_tc_kernel<16, 6>
+}
+
 cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const TcMap* mx_cached,
                            const void* x_base, uint64_t x_rows, int splits, cudaStream_t s,
                            bool pdl) {
@@ -651,6 +718,10 @@ cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, co
   p.status = e.status;
   // split-K partials live in the ring of each CTA of the cluster: BN <= 64 tokens
   if (p.splits > 1 && BN > 64) p.splits = 1;
+  if (g.ln_x) {
+    if (g.batch > 1 || !tc_ln_input_ok(g.M, g.N, g.K, p.splits) || !g.ln_g || !g.ln_b) return cudaErrorInvalidValue;
+    p.ln_x = g.ln_x; p.ln_g = g.ln_g; p.ln_b = g.ln_b;
+  }
   const CUtensorMap& W = *reinterpret_cast<const CUtensorMap*>(&mw);
   const CUtensorMap& X = *reinterpret_cast<const CUtensorMap*>(&mx);
   if (p.splits == 1 && g_sm_count > 0) {

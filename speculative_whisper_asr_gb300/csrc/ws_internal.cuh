@@ -91,10 +91,11 @@ __device__ __forceinline__ float warp_max(float v) {
 // before any is reduced (one memory round trip for NR rows); each row's
 // arithmetic is the same.  out(r, k, ...) receives the four normalised
 // values of group k of row r.  CG: read x from L2 (rows written by other SMs
-// in the same kernel).
+// in the same kernel).  Only features k_lo <= k < k_hi are normalised and
+// passed to out (the statistics always cover the whole row).
 template <bool CG, int NR, int MAXV, class Out>
 __device__ __forceinline__ void ln_rows_warp(const float* const* xs, int nr, int d, const void* g, const void* b,
-                                             bool g_bf16, Out out) {
+                                             bool g_bf16, Out out, int k_lo = 0, int k_hi = 1 << 30) {
   const int lane = threadIdx.x & 31;
   const int nv = d >> 7;
   float4 v[NR][MAXV];
@@ -129,8 +130,8 @@ __device__ __forceinline__ void ln_rows_warp(const float* const* xs, int nr, int
     const float rstd = rsqrtf(warp_sum(q) / (float)d + 1e-5f);
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
-      if (i < nv) {
-        const int k = 4 * lane + 128 * i;
+      const int k = 4 * lane + 128 * i;
+      if (i < nv && k >= k_lo && k < k_hi) {
         float gg[4], bv[4];
         if (g_bf16) {
           const uint2 gq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(g) + k);
@@ -276,6 +277,11 @@ struct GemmShape {
   const void* W; int ldw;       // [N, K] weights, model dtype
   int M, N, K;
   int batch;                    // grid.z repeats (CROSSKV: n_req), row offset by cu_frames
+  // tcgen05 engine only: X = LayerNorm(ln_x; ln_g, ln_b) computed inside the
+  // GEMM (rows of ln_x K floats apart) when tc_ln_input_ok; X is then unused
+  const float* ln_x = nullptr;
+  const void* ln_g = nullptr;
+  const void* ln_b = nullptr;
 };
 
 template <typename T> cudaError_t launch_gemm_simt(const GemmShape& g, const Epi& e, cudaStream_t s, bool pdl);
@@ -299,6 +305,10 @@ struct alignas(64) TcMap { unsigned char bytes[128]; };
 bool tc_engine_available();
 bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 int tc_pick_bn(int M, int N, int batch);
+// Whether a GEMM of this shape and split-K factor can take its layer-norm
+// input in-kernel (GemmShape::ln_x): one 16-token tile, split K, every CTA's
+// k-blocks in its ring at once, K a multiple of 128 up to 1280.
+bool tc_ln_input_ok(int M, int N, int K, int splits);
 // X is the row-major activation buffer [x_rows, K] (bf16); W's map has 128-row boxes.
 // mx_cached: the activation map for this call's token tile (tc_pick_bn), or
 // NULL to encode one from x_base / x_rows.

@@ -104,3 +104,34 @@ def test_fused_graph_capture_replays_identically(RB):
     assert torch.equal(l1, l2)
     assert torch.equal(t1, t2)
     assert dec.status() == 0
+
+
+@pytest.mark.parametrize("wide", [False, True])
+def test_layernorm_in_gemm_bit_identical(RB, wide):
+    """Layer norm computed inside the projection GEMMs gives the same logits,
+    bit for bit, as the layer-norm kernel path: d 256 (two 128-feature groups
+    per lane row) and d 1280 (ten, the widest Whisper decoder), with 16 rows
+    (four rows per warp) and with 5 rows (ragged: warps with one and two rows)."""
+    R, B = RB
+    kw = dict(n_layers=2, d_model=1280, n_heads=20, d_ff=5120) if wide else {}
+    s = small_shape("bf16", **kw)
+    tw = synth.target_weights(s, 47)
+    A = synth.encoder_states(s, 47, 0, frames=200)
+    dec = R.Decoder(s, tw, None, max_batch=1, max_frames=200, max_block=16)
+    req = dec.slots([0])
+    dec.cross_kv(req, dec.enc_tensor(A), [200])
+    dec.reset(req)
+    assert B.ws_fused_layernorm(dec.ctx, -1) == 1
+    rng = np.random.default_rng(11)
+    for H in (16, 5):
+        block = [list(s.prompt) + rng.integers(0, s.vocab, size=H - len(s.prompt)).tolist()]
+        lf, tf = _verify(dec, req, block, H)
+        assert B.ws_fused_layernorm(dec.ctx, 0) == 0
+        lp, tp = _verify(dec, req, block, H)
+        assert B.ws_fused_layernorm(dec.ctx, 1) == 1
+        assert torch.equal(lf, lp)
+        assert torch.equal(tf, tp)
+        orc = M.Oracle(s, tw, None)
+        ora, _ = orc.forward_full(orc.new_request(A), block[0])
+        logits_close(lf[0].cpu().numpy(), ora, 2e-2)
+    assert dec.status() == 0
