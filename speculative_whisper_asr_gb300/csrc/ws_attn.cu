@@ -15,6 +15,7 @@
 // share the block: verifying a block and decoding one token at a time give
 // bit-identical rows.
 #include <cuda.h>
+#include <cooperative_groups.h>
 
 #include "ws_attn_common.cuh"
 #include "ws_attn_mma.cuh"
@@ -361,7 +362,130 @@ __global__ void __launch_bounds__(512) attn_fold_kernel(AttnArgs a) {
   o[1] = __float2bfloat16_rn(o1);
 }
 
+// ------------------------------------------------------------------ cluster variant
+// One thread-block cluster per (request, head) and one warp per chunk: CTA c
+// of a cluster of ceil(n_split / CW) CTAs holds chunks CW * c .. CW * c +
+// CW - 1.  Each warp stages its chunk's K and V boxes by TMA (cross-attention
+// before the dependency wait, as in the streaming variant) and writes the
+// chunk partial (attn_chunk_partial) into its CTA's shared memory.  After a
+// cluster barrier the cluster's warps fold the rows (cluster warp g takes
+// rows g, g + CW * C, ...) from the partials of every CTA through
+// distributed shared memory, in chunk order with the fold kernel's
+// arithmetic, and store the attention output: one kernel, no partials in
+// global memory, and rows bit-identical to the streaming variant's.
+constexpr int CW = 4;                                     // warps (chunks) per CTA
+constexpr int CL_MAX = 8;                                 // CTAs per cluster (portable size)
+constexpr int CLUSTER_SMEM = CW * CHUNK_BYTES + CW * MAXR * PART * 4 + 1024;
+
+template <int MODE>
+__global__ void __launch_bounds__(CW * 32) attn_cluster_kernel(const __grid_constant__ CUtensorMap tmKV, AttnArgs a,
+                                                                const bf16* kv_base) {
+  namespace cg = cooperative_groups;
+  extern __shared__ uint8_t dsm_c[];
+  __shared__ __align__(8) uint64_t bar[CW];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_c) + 1023) & ~uintptr_t(1023));
+  float* parts = reinterpret_cast<float*>(base + CW * CHUNK_BYTES);     // [CW][MAXR][PART]
+  cg::cluster_group cl = cg::this_cluster();
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = (int)gridDim.x, rank = (int)blockIdx.x;                 // the cluster spans grid.x
+  const int head = blockIdx.y, i = blockIdx.z;
+  const int heads = a.d / WS_DH, H = a.H, ns = a.n_split;
+  const int sp = rank * CW + w;                                        // this warp's chunk
+  uint8_t* Ks = base + w * CHUNK_BYTES;
+  uint8_t* Vs = Ks + CHUNK_BYTES / 2;
+  if (lane == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[w])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  pdl_trigger();
+  // cross-attention K/V were written before this library call began (see
+  // the streaming variant); self-attention reads rows this call wrote
+  if (MODE == MODE_SELF) pdl_wait();
+  bool loaded = false;
+  if (lane == 0 && sp < ns) loaded = stage_unit<MODE>(a, &tmKV, kv_base, (i * heads + head) * ns + sp, Ks, &bar[w]);
+  loaded = __shfl_sync(0xffffffffu, loaded, 0);
+  if (MODE == MODE_CROSS) pdl_wait();
+  auto part = [&](int j) { return parts + (w * MAXR + j) * PART; };
+  bool landed = !loaded;
+  if (sp < ns) {
+    if (loaded) {
+      uint32_t qf[4][4];
+      attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);   // while the chunk lands
+      landed = mbar_wait(&bar[w], 0);
+      if (!landed && lane == 0) atomicOr(a.status, WS_ST_TIMEOUT);
+      if (landed) {
+        int k_lo, nk, Lr, nrow;
+        unit_range<MODE>(a, i, sp, k_lo, nk, Lr, nrow);
+        for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)   // finite values beyond the keys
+          *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+        auto vis = [&](int j) {
+          if (j >= H) return 0;
+          if (MODE == MODE_CROSS) return nk;
+          if (j >= nrow) return 0;
+          return max(0, min(k_lo + nk, min(Lr + j + 1, a.max_pos)) - k_lo);
+        };
+        attn_chunk_partial<true>(Ks, Vs, qf, vis(lane >> 2), vis((lane >> 2) + 8), H, part);
+      }
+    }
+    if (!loaded || !landed) {       // no keys here (or the copy timed out): an empty partial
+      for (int j = 0; j < H; ++j) {
+        float* p = part(j);
+        if (lane == 0) { p[0] = -INFINITY; p[1] = 0.f; }
+        p[2 + 2 * lane] = 0.f;
+        p[3 + 2 * lane] = 0.f;
+      }
+    }
+  }
+  cl.sync();                        // every chunk partial of the cluster is written
+  for (int j = rank * CW + w; j < H; j += C * CW) {
+    float o0, o1;
+    attn_fold_row_of<false>(
+        [&](int s) { return cl.map_shared_rank(parts, s / CW) + ((s % CW) * MAXR + j) * PART; }, ns, o0, o1);
+    bf16* o = reinterpret_cast<bf16*>(a.O) + ((size_t)i * H + j) * a.d + head * WS_DH + 2 * lane;
+    o[0] = __float2bfloat16_rn(o0);
+    o[1] = __float2bfloat16_rn(o1);
+  }
+  cl.sync();                        // peers have read this CTA's partials
+  // a copy whose wait timed out lands before exit (bounded)
+  if (loaded && !landed && lane == 0 && !mbar_wait(&bar[w], 0)) atomicOr(a.status, WS_ST_TIMEOUT);
+  __syncwarp();
+}
+
 int g_attn_sms = 0;
+
+// Requests per call up to which the cluster variant runs (one cluster per
+// (request, head)); larger calls stream.
+constexpr int CLUSTER_MAX_REQ = 4;
+
+template <int MODE>
+cudaError_t launch_cluster(const AttnArgs& a, int n, int heads, const CUtensorMap& map, const void* kv_base,
+                           cudaStream_t s, bool pdl) {
+  const int C = (a.n_split + CW - 1) / CW;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, heads, n);
+  cfg.blockDim = dim3(CW * 32);
+  cfg.dynamicSmemBytes = CLUSTER_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (pdl) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  at[na].id = cudaLaunchAttributeClusterDimension;
+  at[na].val.clusterDim.x = C;
+  at[na].val.clusterDim.y = 1;
+  at[na].val.clusterDim.z = 1;
+  ++na;
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<MODE>, map, a, reinterpret_cast<const bf16*>(kv_base));
+}
+
 
 template <int MODE>
 cudaError_t launch_stream(const AttnArgs& a, int n, int heads, const CUtensorMap& map, const void* kv_base,
@@ -390,6 +514,14 @@ cudaError_t launch_stream(const AttnArgs& a, int n, int heads, const CUtensorMap
   f.numAttrs = pdl ? 1 : 0;
   ws_count_launches(1);
   return cudaLaunchKernelEx(&f, attn_fold_kernel, a);
+}
+
+template <int MODE>
+cudaError_t launch_chunks(const AttnArgs& a, int n, int heads, const CUtensorMap& map, const void* kv_base,
+                          cudaStream_t s, bool pdl) {
+  if (n <= CLUSTER_MAX_REQ && a.n_split <= CW * CL_MAX && a.H <= MAXR)
+    return launch_cluster<MODE>(a, n, heads, map, kv_base, s, pdl);
+  return launch_stream<MODE>(a, n, heads, map, kv_base, s, pdl);
 }
 
 template <typename T>
@@ -438,6 +570,10 @@ cudaError_t attn_init_attributes() {
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
   if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_stream_kernel<MODE_CROSS>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_cluster_kernel<MODE_SELF>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, CLUSTER_SMEM);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_cluster_kernel<MODE_CROSS>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, CLUSTER_SMEM);
   if (r == cudaSuccess) {
     int dev = 0;
     r = cudaGetDevice(&dev);
@@ -457,7 +593,7 @@ cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const K
   a.Q = Q; a.kv = kv; a.part = sc.part; a.counters = sc.counters; a.O = O; a.status = sc.status;
   a.n_req = n;
   if (sizeof(T) == 2 && sc.kv_map)
-    return launch_stream<MODE_SELF>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.kv_map), sc.kv_base, s,
+    return launch_chunks<MODE_SELF>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.kv_map), sc.kv_base, s,
                                     pdl);
   return launch_mode<T, MODE_SELF>(a, n, n_heads, s, pdl);
 }
@@ -474,7 +610,7 @@ cudaError_t launch_cross_attn(int n, int H, const int32_t* req_ids, const int32_
   a.part = sc.part; a.counters = sc.counters; a.O = O; a.status = sc.status;
   a.n_req = n;
   if (sizeof(T) == 2 && sc.xkv_map)
-    return launch_stream<MODE_CROSS>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.xkv_map), x.base, s,
+    return launch_chunks<MODE_CROSS>(a, n, n_heads, *reinterpret_cast<const CUtensorMap*>(sc.xkv_map), x.base, s,
                                      pdl);
   return launch_mode<T, MODE_CROSS>(a, n, n_heads, s, pdl);
 }

@@ -51,33 +51,42 @@ __device__ __forceinline__ void row_subtile(RowState& st, const float* q, const 
   st.m = mn;
 }
 
-// Fold the partials p[s * WS_ATTN_PART] of one row, s = 0 .. n_split-1 in
-// order; lane l returns output dims (2l, 2l+1).  Partials are read from L2
-// (they were written by other CTAs).  All loads of a group of splits are
-// issued before their values are used (one L2 round trip per group instead
-// of one per split); the arithmetic and its order are those of the
-// sequential fold: M = max_s m_s, then den, n0, n1 accumulate over s = 0, 1,
-// ... with weights exp(m_s - M), skipping empty splits.
-__device__ __forceinline__ void attn_fold_row(const float* p, int n_split, float& o0, float& o1) {
+// Fold the partials of one row, splits s = 0 .. n_split-1 in order, split s
+// at part_of(s) (m, l, 64 weighted values); lane l returns output dims (2l,
+// 2l+1).  GLOBAL: the partials are in global memory, written by other CTAs
+// (read from L2); else in this cluster's shared memory (generic loads).  All
+// loads of a group of splits are issued before their values are used (one
+// round trip per group instead of one per split); the arithmetic and its
+// order are those of the sequential fold: M = max_s m_s, then den, n0, n1
+// accumulate over s = 0, 1, ... with weights exp(m_s - M), skipping empty
+// splits.
+template <bool GLOBAL>
+__device__ __forceinline__ float fold_ld(const float* p) { return GLOBAL ? __ldcg(p) : *p; }
+template <bool GLOBAL>
+__device__ __forceinline__ float2 fold_ld2(const float* p) {
+  return GLOBAL ? __ldcg(reinterpret_cast<const float2*>(p)) : *reinterpret_cast<const float2*>(p);
+}
+
+template <bool GLOBAL, class PartOf>
+__device__ __forceinline__ void attn_fold_row_of(PartOf part_of, int n_split, float& o0, float& o1) {
   const int lane = threadIdx.x & 31;
   float M = -INFINITY;
   for (int s0 = 0; s0 < n_split; s0 += 32) {
     const int s = s0 + lane;
-    const float m = s < n_split ? __ldcg(p + (size_t)s * WS_ATTN_PART) : -INFINITY;
+    const float m = s < n_split ? fold_ld<GLOBAL>(part_of(s)) : -INFINITY;
     M = fmaxf(M, warp_max(m));
   }
   float den = 0.f, n0 = 0.f, n1 = 0.f;
   for (int s0 = 0; s0 < n_split; s0 += 32) {
     const int sl = s0 + lane;
     float2 ml = make_float2(-INFINITY, 0.f);
-    if (sl < n_split) ml = __ldcg(reinterpret_cast<const float2*>(p + (size_t)sl * WS_ATTN_PART));
+    if (sl < n_split) ml = fold_ld2<GLOBAL>(part_of(sl));
     const int nin = min(32, n_split - s0);
     for (int t = 0; t < nin; t += 8) {
       float2 av[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        if (t + u < nin)
-          av[u] = __ldcg(reinterpret_cast<const float2*>(p + (size_t)(s0 + t + u) * WS_ATTN_PART + 2 + 2 * lane));
+        if (t + u < nin) av[u] = fold_ld2<GLOBAL>(part_of(s0 + t + u) + 2 + 2 * lane);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         if (t + u >= nin) break;
@@ -93,4 +102,9 @@ __device__ __forceinline__ void attn_fold_row(const float* p, int n_split, float
   }
   o0 = den > 0.f ? n0 / den : 0.f;
   o1 = den > 0.f ? n1 / den : 0.f;
+}
+
+// Partials p[s * WS_ATTN_PART] in global memory.
+__device__ __forceinline__ void attn_fold_row(const float* p, int n_split, float& o0, float& o1) {
+  attn_fold_row_of<true>([p](int s) { return p + (size_t)s * WS_ATTN_PART; }, n_split, o0, o1);
 }
