@@ -67,9 +67,34 @@ __device__ __forceinline__ float2 fold_ld2(const float* p) {
   return GLOBAL ? __ldcg(reinterpret_cast<const float2*>(p)) : *reinterpret_cast<const float2*>(p);
 }
 
-template <bool GLOBAL, class PartOf>
+template <bool GLOBAL, bool ONE_TRIP = true, class PartOf>
 __device__ __forceinline__ void attn_fold_row_of(PartOf part_of, int n_split, float& o0, float& o1) {
   const int lane = threadIdx.x & 31;
+  if (ONE_TRIP && n_split <= 32) {
+    // every load at once (one round trip): split `lane`'s (m, l) and each
+    // split's two output dims of this lane; same arithmetic as below
+    const float2 ml = lane < n_split ? fold_ld2<GLOBAL>(part_of(lane)) : make_float2(-INFINITY, 0.f);
+    float2 av[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u)
+      if (u < n_split) av[u] = fold_ld2<GLOBAL>(part_of(u) + 2 + 2 * lane);
+    const float M = fmaxf(-INFINITY, warp_max(ml.x));
+    float den = 0.f, n0 = 0.f, n1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      if (u >= n_split) break;
+      const float l = __shfl_sync(0xffffffffu, ml.y, u);
+      const float m = __shfl_sync(0xffffffffu, ml.x, u);
+      if (l <= 0.f) continue;
+      const float c = expf(m - M);
+      den = fmaf(l, c, den);
+      n0 = fmaf(av[u].x, c, n0);
+      n1 = fmaf(av[u].y, c, n1);
+    }
+    o0 = den > 0.f ? n0 / den : 0.f;
+    o1 = den > 0.f ? n1 / den : 0.f;
+    return;
+  }
   float M = -INFINITY;
   for (int s0 = 0; s0 < n_split; s0 += 32) {
     const int s = s0 + lane;
@@ -104,7 +129,9 @@ __device__ __forceinline__ void attn_fold_row_of(PartOf part_of, int n_split, fl
   o1 = den > 0.f ? n1 / den : 0.f;
 }
 
-// Partials p[s * WS_ATTN_PART] in global memory.
+// Partials p[s * WS_ATTN_PART] in global memory.  ONE_TRIP = false keeps
+// the register footprint small (grouped loads); the result is the same.
+template <bool ONE_TRIP = true>
 __device__ __forceinline__ void attn_fold_row(const float* p, int n_split, float& o0, float& o1) {
-  attn_fold_row_of<true>([p](int s) { return p + (size_t)s * WS_ATTN_PART; }, n_split, o0, o1);
+  attn_fold_row_of<true, ONE_TRIP>([p](int s) { return p + (size_t)s * WS_ATTN_PART; }, n_split, o0, o1);
 }

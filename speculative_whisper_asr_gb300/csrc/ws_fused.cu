@@ -575,7 +575,7 @@ __device__ void attn_stage(const FusedArgs& a, const FusedStage& st, int u0, uin
       for (int j = warp; j < H; j += NCW) {
         const float* p = a.apart + (((size_t)i * H + j) * a.heads + head) * nsplit * WS_ATTN_PART;
         float o0, o1;
-        attn_fold_row(p, nsplit, o0, o1);
+        attn_fold_row<false>(p, nsplit, o0, o1);
         bf16* o = a.ao + ((size_t)i * H + j) * a.d + head * WS_DH + 2 * lane;
         o[0] = __float2bfloat16_rn(o0);
         o[1] = __float2bfloat16_rn(o1);

@@ -205,10 +205,13 @@ __global__ void __launch_bounds__(128, 1)
       tma_load_2d(ring + i * STAGE_BYTES, &tmW, &full[i], (kb0 + i) * BK, f0);
     }
   }
-  // layer-norm gain and bias of this CTA's k-range are weights: into L1 now
-  if (lnin && active && (int)threadIdx.x < 2 * nkb) {
-    const bf16* src = reinterpret_cast<const bf16*>((threadIdx.x & 1) ? p.ln_b : p.ln_g);
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(src + (kb0 + (int)(threadIdx.x >> 1)) * BK));
+  // layer-norm gain and bias of this CTA's k-range are weights: into shared
+  // memory now (16 bytes a thread), read after the dependency wait
+  __shared__ __align__(16) bf16 ln_gb[2][6 * BK];
+  if (lnin && active && (int)threadIdx.x < nkb * 16) {
+    const int h = threadIdx.x >> 3 & 1, off = (threadIdx.x >> 4) * BK + (threadIdx.x & 7) * 8;
+    const bf16* src = reinterpret_cast<const bf16*>(h ? p.ln_b : p.ln_g) + kb0 * BK + off;
+    *reinterpret_cast<uint4*>(&ln_gb[h][off]) = *reinterpret_cast<const uint4*>(src);
   }
   // the bias of this thread's feature is a weight: load it before the wait
   float bpre = 0.0f;
@@ -254,8 +257,9 @@ __global__ void __launch_bounds__(128, 1)
     const float* xs[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) xs[j] = p.ln_x + (size_t)(t0 + warp + 4 * j) * p.K;   // read for j < nrw only
+    __syncthreads();                   // gain and bias staged
     ln_rows_warp<true, 4, 10>(
-        xs, nrw, p.K, p.ln_g, p.ln_b, true,
+        xs, nrw, p.K, ln_gb[0], ln_gb[1], true,
         [&](int j, int k, float v0, float v1, float v2, float v3) {
           const int r = warp + 4 * j, kl = k - k_lo, col = kl & 63;
           __nv_bfloat162 h0 = __floats2bfloat162_rn(v0, v1), h1 = __floats2bfloat162_rn(v2, v3);
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(128, 1)
           *reinterpret_cast<uint2*>(ring + (kl >> 6) * STAGE_BYTES + A_BYTES + r * 128 +
                                     ((((col >> 3) ^ (r & 7)) << 4) | ((col & 7) * 2))) = w;
         },
-        k_lo, kb1 * BK);
+        k_lo, kb1 * BK, k_lo);
     for (int idx = threadIdx.x; idx < (BN - nr) * nkb * 8; idx += 128) {   // rows nr .. 15 are zero
       const int r = nr + idx / (nkb * 8), rem = idx % (nkb * 8);
       *reinterpret_cast<uint4*>(ring + (rem >> 3) * STAGE_BYTES + A_BYTES + r * 128 + ((rem & 7) << 4)) =
@@ -351,25 +355,33 @@ __global__ void __launch_bounds__(128, 1)
     const float* part[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) part[r] = cl.map_shared_rank(mine, r < p.splits ? r : 0);
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      float v[16];
+    float v[BN / 16][16];
+#pragma unroll
+    for (int g = 0; g < BN / 16; ++g) {
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         float a = 0.0f;
         if (c >= c_lo && c < c_hi) {
-          a = part[0][(c0 + c) * BM + row];
+          a = part[0][(16 * g + c) * BM + row];
 #pragma unroll
           for (int r = 1; r < 8; ++r)
-            if (r < p.splits) a += part[r][(c0 + c) * BM + row];
+            if (r < p.splits) a += part[r][(16 * g + c) * BM + row];
         }
-        v[c] = a;
+        v[g][c] = a;
       }
-      if (fast16)
-        fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr, &bpre, c_lo, c_hi);
-      else epi_columns16(e, p.N, t0 + c0, n, M, z, v, c_lo, c_hi);
     }
-    cl.sync();
+    // this CTA's reads of the others' partials are done: arrive now, and
+    // wait (for the others' reads of this CTA's partial) only before exit,
+    // so the barrier's latency overlaps the stores below
+    auto reads_done = cl.barrier_arrive();
+#pragma unroll
+    for (int g = 0; g < BN / 16; ++g) {
+      if (fast16)
+        fast_epilogue16(e, p.N, t0 + 16 * g, M, n, z, v[g], tok_tab, 16 * g, pre_resid ? xpre : nullptr, &bpre, c_lo,
+                        c_hi);
+      else epi_columns16(e, p.N, t0 + 16 * g, n, M, z, v[g], c_lo, c_hi);
+    }
+    cl.barrier_wait(std::move(reads_done));
   }
   tc_fence_before();
   __syncthreads();

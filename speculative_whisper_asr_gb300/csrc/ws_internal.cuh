@@ -88,14 +88,17 @@ __device__ __forceinline__ float warp_max(float v) {
 // variance are per-lane sequential sums followed by a fixed shuffle tree, so
 // a row's values never depend on which other rows share the launch.
 // ln_rows_warp takes NR rows at once: the loads of all of them are issued
-// before any is reduced (one memory round trip for NR rows); each row's
-// arithmetic is the same.  out(r, k, ...) receives the four normalised
-// values of group k of row r.  CG: read x from L2 (rows written by other SMs
-// in the same kernel).  Only features k_lo <= k < k_hi are normalised and
-// passed to out (the statistics always cover the whole row).
+// before any is reduced (one memory round trip for NR rows), and the rows'
+// reductions are interleaved phase by phase (their shuffle chains overlap);
+// each row's arithmetic is the same as alone.  out(r, k, ...) receives the
+// four normalised values of group k of row r.  CG: read x from L2 (rows
+// written by other SMs in the same kernel).  Only features k_lo <= k < k_hi
+// are normalised and passed to out (the statistics always cover the whole
+// row); gain and bias of feature k are read at g[k - g_off], b[k - g_off].
 template <bool CG, int NR, int MAXV, class Out>
 __device__ __forceinline__ void ln_rows_warp(const float* const* xs, int nr, int d, const void* g, const void* b,
-                                             bool g_bf16, Out out, int k_lo = 0, int k_hi = 1 << 30) {
+                                             bool g_bf16, Out out, int k_lo = 0, int k_hi = 1 << 30,
+                                             int g_off = 0) {
   const int lane = threadIdx.x & 31;
   const int nv = d >> 7;
   float4 v[NR][MAXV];
@@ -111,45 +114,63 @@ __device__ __forceinline__ void ln_rows_warp(const float* const* xs, int nr, int
       }
     }
   }
+  float mean[NR], rstd[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
-    if (r >= nr) break;
     float s = 0.0f;
+    if (r < nr) {
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i)
-      if (i < nv) s += (v[r][i].x + v[r][i].y) + (v[r][i].z + v[r][i].w);
-    const float mean = warp_sum(s) / (float)d;
+      for (int i = 0; i < MAXV; ++i)
+        if (i < nv) s += (v[r][i].x + v[r][i].y) + (v[r][i].z + v[r][i].w);
+    }
+    mean[r] = s;
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+    if (r < nr) mean[r] = warp_sum(mean[r]) / (float)d;
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
     float q = 0.0f;
+    if (r < nr) {
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      if (i < nv) {
-        const float a = v[r][i].x - mean, bb = v[r][i].y - mean, c = v[r][i].z - mean, e = v[r][i].w - mean;
-        q += (a * a + bb * bb) + (c * c + e * e);
+      for (int i = 0; i < MAXV; ++i) {
+        if (i < nv) {
+          const float a = v[r][i].x - mean[r], bb = v[r][i].y - mean[r], c = v[r][i].z - mean[r],
+                      e = v[r][i].w - mean[r];
+          q += (a * a + bb * bb) + (c * c + e * e);
+        }
       }
     }
-    const float rstd = rsqrtf(warp_sum(q) / (float)d + 1e-5f);
+    rstd[r] = q;
+  }
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int k = 4 * lane + 128 * i;
-      if (i < nv && k >= k_lo && k < k_hi) {
-        float gg[4], bv[4];
-        if (g_bf16) {
-          const uint2 gq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(g) + k);
-          const uint2 bq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(b) + k);
-          const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.x));
-          const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.y));
-          const float2 b01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.x));
-          const float2 b23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.y));
-          gg[0] = g01.x; gg[1] = g01.y; gg[2] = g23.x; gg[3] = g23.y;
-          bv[0] = b01.x; bv[1] = b01.y; bv[2] = b23.x; bv[3] = b23.y;
-        } else {
-          const float4 gq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + k);
-          const float4 bq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(b) + k);
-          gg[0] = gq.x; gg[1] = gq.y; gg[2] = gq.z; gg[3] = gq.w;
-          bv[0] = bq.x; bv[1] = bq.y; bv[2] = bq.z; bv[3] = bq.w;
-        }
-        out(r, k, (v[r][i].x - mean) * rstd * gg[0] + bv[0], (v[r][i].y - mean) * rstd * gg[1] + bv[1],
-            (v[r][i].z - mean) * rstd * gg[2] + bv[2], (v[r][i].w - mean) * rstd * gg[3] + bv[3]);
+  for (int r = 0; r < NR; ++r)
+    if (r < nr) rstd[r] = rsqrtf(warp_sum(rstd[r]) / (float)d + 1e-5f);
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int k = 4 * lane + 128 * i;
+    if (i < nv && k >= k_lo && k < k_hi) {
+      float gg[4], bv[4];
+      if (g_bf16) {
+        const uint2 gq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(g) + (k - g_off));
+        const uint2 bq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(b) + (k - g_off));
+        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.x));
+        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.y));
+        const float2 b01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.x));
+        const float2 b23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.y));
+        gg[0] = g01.x; gg[1] = g01.y; gg[2] = g23.x; gg[3] = g23.y;
+        bv[0] = b01.x; bv[1] = b01.y; bv[2] = b23.x; bv[3] = b23.y;
+      } else {
+        const float4 gq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + (k - g_off));
+        const float4 bq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(b) + (k - g_off));
+        gg[0] = gq.x; gg[1] = gq.y; gg[2] = gq.z; gg[3] = gq.w;
+        bv[0] = bq.x; bv[1] = bq.y; bv[2] = bq.z; bv[3] = bq.w;
+      }
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        if (r < nr)
+          out(r, k, (v[r][i].x - mean[r]) * rstd[r] * gg[0] + bv[0], (v[r][i].y - mean[r]) * rstd[r] * gg[1] + bv[1],
+              (v[r][i].z - mean[r]) * rstd[r] * gg[2] + bv[2], (v[r][i].w - mean[r]) * rstd[r] * gg[3] + bv[3]);
       }
     }
   }
