@@ -31,6 +31,7 @@ constexpr long long WAIT_BUDGET = 1ll << 32;
 enum { MODE_SELF = 0, MODE_CROSS = 1, MODE_DRAFT = 2 };
 
 struct AttnArgs {
+  int mode;                  // MODE_SELF / MODE_CROSS / MODE_DRAFT (kernels compiled for any mode)
   int n_req;                 // requests in the call
   int H;                     // query rows per request
   int n_split;               // splits per (request, head); DRAFT: history splits + 1 block split
@@ -220,14 +221,16 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_
 constexpr int SW = 2;                        // warps per CTA
 constexpr int STREAM_SMEM = SW * 2 * CHUNK_BYTES + 1024;
 
+// MODE < 0: the mode is a.mode (one compiled copy serves self- and cross-attention)
 template <int MODE>
 __device__ __forceinline__ void unit_range(const AttnArgs& a, int i, int sp, int& k_lo, int& nk, int& Lr, int& nrow) {
+  const int mode = MODE >= 0 ? MODE : a.mode;
   const int slot = a.req_ids[i];
   k_lo = sp * WS_XCHUNK;
   Lr = 0;
   nrow = a.H;
   int kend;
-  if (MODE == MODE_SELF) {
+  if (mode == MODE_SELF) {
     Lr = a.L[slot];
     nrow = min(a.block_len[i], a.H);
     kend = min(Lr + nrow, a.max_pos);
@@ -241,6 +244,7 @@ __device__ __forceinline__ void unit_range(const AttnArgs& a, int i, int sp, int
 template <int MODE>
 __device__ __forceinline__ bool stage_unit(const AttnArgs& a, const CUtensorMap* map, const bf16* kv_base, int u,
                                            uint8_t* dst, uint64_t* bar) {
+  const int mode = MODE >= 0 ? MODE : a.mode;
   const int heads = a.d / WS_DH, ns = a.n_split;
   const int i = u / (heads * ns), head = (u / ns) % heads, sp = u % ns;
   int k_lo, nk, Lr, nrow;
@@ -248,7 +252,7 @@ __device__ __forceinline__ bool stage_unit(const AttnArgs& a, const CUtensorMap*
   if (nk <= 0) return false;
   const int slot = a.req_ids[i];
   const bf16 *ks, *vs;
-  if (MODE == MODE_CROSS) {
+  if (mode == MODE_CROSS) {
     ks = xkv_ptr<bf16>(a.x, slot, a.xlayer, 0, head, k_lo);
     vs = xkv_ptr<bf16>(a.x, slot, a.xlayer, 1, head, k_lo);
   } else {
@@ -271,6 +275,7 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_s) + 1023) & ~uintptr_t(1023));
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int heads = a.d / WS_DH, H = a.H, ns = a.n_split;
+  const int mode = MODE >= 0 ? MODE : a.mode;
   const int total = a.n_req * heads * ns;
   const int gw = blockIdx.x * SW + w, GW = gridDim.x * SW;
   uint8_t* slot_mem[2] = {base + (2 * w) * CHUNK_BYTES, base + (2 * w + 1) * CHUNK_BYTES};
@@ -286,14 +291,14 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
   // dependents only after its own dependency wait), so cross-attention
   // stages its first chunk before waiting on the previous kernel; only the
   // queries depend on it.  Self-attention reads cache rows this call wrote.
-  if (MODE == MODE_SELF) pdl_wait();
+  if (mode == MODE_SELF) pdl_wait();
   // loaded[b]: slot b holds a requested (not yet consumed) copy; uses[b]: phases issued on bar[w][b]
   bool loaded[2] = {false, false};
   uint32_t uses[2] = {0u, 0u};
   const int u_beg = (int)((long long)gw * total / GW), u_end = (int)((long long)(gw + 1) * total / GW);
   if (lane == 0 && u_beg < u_end) loaded[0] = stage_unit<MODE>(a, &tmKV, kv_base, u_beg, slot_mem[0], &bar[w][0]);
   loaded[0] = __shfl_sync(0xffffffffu, loaded[0], 0);
-  if (MODE == MODE_CROSS) pdl_wait();
+  if (mode == MODE_CROSS) pdl_wait();
   int m = 0, qi = -1, qh = -1;
   uint32_t qf[4][4];
   for (int u = u_beg; u < u_end; ++u, ++m) {
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
       const int g = lane >> 2;
       auto vis = [&](int j) {
         if (j >= H) return 0;
-        if (MODE == MODE_CROSS) return nk;
+        if (mode == MODE_CROSS) return nk;
         if (j >= nrow) return 0;
         return max(0, min(k_lo + nk, min(Lr + j + 1, a.max_pos)) - k_lo);
       };
@@ -391,6 +396,7 @@ __global__ void __launch_bounds__(CW * 32) attn_cluster_kernel(const __grid_cons
   const int head = blockIdx.y, i = blockIdx.z;
   const int heads = a.d / WS_DH, H = a.H, ns = a.n_split;
   const int sp = rank * CW + w;                                        // this warp's chunk
+  const int mode = MODE >= 0 ? MODE : a.mode;
   uint8_t* Ks = base + w * CHUNK_BYTES;
   uint8_t* Vs = Ks + CHUNK_BYTES / 2;
   if (lane == 0) {
@@ -401,11 +407,11 @@ __global__ void __launch_bounds__(CW * 32) attn_cluster_kernel(const __grid_cons
   pdl_trigger();
   // cross-attention K/V were written before this library call began (see
   // the streaming variant); self-attention reads rows this call wrote
-  if (MODE == MODE_SELF) pdl_wait();
+  if (mode == MODE_SELF) pdl_wait();
   bool loaded = false;
   if (lane == 0 && sp < ns) loaded = stage_unit<MODE>(a, &tmKV, kv_base, (i * heads + head) * ns + sp, Ks, &bar[w]);
   loaded = __shfl_sync(0xffffffffu, loaded, 0);
-  if (MODE == MODE_CROSS) pdl_wait();
+  if (mode == MODE_CROSS) pdl_wait();
   auto part = [&](int j) { return parts + (w * MAXR + j) * PART; };
   bool landed = !loaded;
   if (sp < ns) {
@@ -422,7 +428,7 @@ __global__ void __launch_bounds__(CW * 32) attn_cluster_kernel(const __grid_cons
         __syncwarp();
         auto vis = [&](int j) {
           if (j >= H) return 0;
-          if (MODE == MODE_CROSS) return nk;
+          if (mode == MODE_CROSS) return nk;
           if (j >= nrow) return 0;
           return max(0, min(k_lo + nk, min(Lr + j + 1, a.max_pos)) - k_lo);
         };
@@ -483,7 +489,7 @@ cudaError_t launch_cluster(const AttnArgs& a, int n, int heads, const CUtensorMa
   cfg.attrs = at;
   cfg.numAttrs = na;
   ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<MODE>, map, a, reinterpret_cast<const bf16*>(kv_base));
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<-1>, map, a, reinterpret_cast<const bf16*>(kv_base));
 }
 
 
@@ -504,7 +510,7 @@ cudaError_t launch_stream(const AttnArgs& a, int n, int heads, const CUtensorMap
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
   ws_count_launches(1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_stream_kernel<MODE>, map, a, reinterpret_cast<const bf16*>(kv_base));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_stream_kernel<-1>, map, a, reinterpret_cast<const bf16*>(kv_base));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t f = {};
   f.gridDim = dim3(n, heads);
@@ -566,13 +572,9 @@ cudaError_t attn_init_attributes() {
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_split_kernel<T, MODE_DRAFT>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_stream_kernel<MODE_SELF>,
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_stream_kernel<-1>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
-  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_stream_kernel<MODE_CROSS>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
-  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_cluster_kernel<MODE_SELF>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, CLUSTER_SMEM);
-  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_cluster_kernel<MODE_CROSS>,
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_cluster_kernel<-1>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, CLUSTER_SMEM);
   if (r == cudaSuccess) {
     int dev = 0;
@@ -587,6 +589,7 @@ cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const K
                              const AttnScratch& sc, cudaStream_t s, bool pdl) {
   if (H > MAXR) return cudaErrorInvalidValue;
   AttnArgs a = {};
+  a.mode = MODE_SELF;
   a.H = H; a.d = n_heads * WS_DH; a.max_pos = rm.max_pos;
   a.n_split = (rm.max_pos + SPLIT - 1) / SPLIT;
   a.req_ids = rm.req_ids; a.L = rm.L; a.block_len = rm.block_len;
@@ -604,6 +607,7 @@ cudaError_t launch_cross_attn(int n, int H, const int32_t* req_ids, const int32_
                               cudaStream_t s, bool pdl) {
   if (H > MAXR) return cudaErrorInvalidValue;
   AttnArgs a = {};
+  a.mode = MODE_CROSS;
   a.H = H; a.d = n_heads * WS_DH;
   a.n_split = max(1, (max_frames_seen + SPLIT - 1) / SPLIT);
   a.req_ids = req_ids; a.Fv = Fv; a.Q = Q; a.x = x; a.xlayer = layer;
@@ -621,6 +625,7 @@ cudaError_t launch_draft_attn(int n, int K1, const int32_t* req_ids, const int32
                               const AttnScratch& sc, cudaStream_t s, bool pdl) {
   if (K1 > MAXR) return cudaErrorInvalidValue;
   AttnArgs a = {};
+  a.mode = MODE_DRAFT;
   a.H = K1; a.d = n_heads * WS_DH; a.max_pos = max_pos;
   a.n_split = (max_pos + SPLIT - 1) / SPLIT + 1;
   a.req_ids = req_ids; a.L = L; a.Q = Q; a.kv = hkv; a.Kb = Kb; a.Vb = Vb;
