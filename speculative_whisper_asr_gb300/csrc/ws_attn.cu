@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AttnArgs a) {
     if (j >= H) continue;
     const float* p = a.part + (((size_t)i * H + j) * heads + head) * a.n_split * PART;
     float o0, o1;
-    attn_fold_row(p, a.n_split, o0, o1);
+    attn_fold_row<false>(p, a.n_split, o0, o1);
     T* o = O + ((size_t)i * H + j) * a.d + head * WS_DH + 2 * lane;
     o[0] = from_f<T>(o0);
     o[1] = from_f<T>(o1);
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(512) attn_fold_kernel(AttnArgs a) {
   if (j >= a.H) return;
   const float* p = a.part + (((size_t)i * a.H + j) * heads + head) * a.n_split * PART;
   float o0, o1;
-  attn_fold_row(p, a.n_split, o0, o1);
+  attn_fold_row<false>(p, a.n_split, o0, o1);
   bf16* o = reinterpret_cast<bf16*>(a.O) + ((size_t)i * a.H + j) * a.d + head * WS_DH + 2 * lane;
   o[0] = __float2bfloat16_rn(o0);
   o[1] = __float2bfloat16_rn(o1);
@@ -510,7 +510,7 @@ cudaError_t launch_stream(const AttnArgs& a, int n, int heads, const CUtensorMap
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
   ws_count_launches(1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_stream_kernel<-1>, map, a, reinterpret_cast<const bf16*>(kv_base));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_stream_kernel<MODE>, map, a, reinterpret_cast<const bf16*>(kv_base));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t f = {};
   f.gridDim = dim3(n, heads);
@@ -572,7 +572,9 @@ cudaError_t attn_init_attributes() {
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_split_kernel<T, MODE_DRAFT>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_stream_kernel<-1>,
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_stream_kernel<MODE_SELF>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_stream_kernel<MODE_CROSS>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
   if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_cluster_kernel<-1>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, CLUSTER_SMEM);
