@@ -236,7 +236,8 @@ const char* ws_gemm_engine(const ws_ctx* ctx);
  * cooperative kernel (one CTA per SM, grid-wide barriers between stages,
  * weights streamed ahead through shared memory) when the device supports
  * cooperative launch.  Off by default: on GB300 the per-operation path is
- * faster at batch 1 (3.75 vs 5.67 ms per large-v3 verify).
+ * faster at batch 1 (its kernel boundaries cost less than the persistent
+ * kernel's software grid barriers).
  *   enable  1: use it when eligible; 0: never (the default); -1: query only.
  * Returns 1 when eligible calls take the persistent path, 0 when not, or
  * WS_EINVAL for a null context.  Host-only; no device work. */

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   // layer-norm gain and bias of this CTA's k-range are weights: into shared
   // memory now (16 bytes a thread), read after the dependency wait
-  __shared__ __align__(16) bf16 ln_gb[2][6 * BK];
+  __shared__ __align__(16) bf16 ln_gb[2][STAGES * BK];
   if (lnin && active && (int)threadIdx.x < nkb * 16) {
     const int h = threadIdx.x >> 3 & 1, off = (threadIdx.x >> 4) * BK + (threadIdx.x & 7) * 8;
     const bf16* src = reinterpret_cast<const bf16*>(h ? p.ln_b : p.ln_g) + kb0 * BK + off;
@@ -670,7 +670,7 @@ cudaError_t tc_init_attributes() {
   auto set = [&](const void* fn, int bytes) {
     if (r == cudaSuccess) r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   };
-  set((const void*)gemm_tc_kernel<16, 6>, tc_smem<16, 6>());
+  set((const void*)gemm_tc_kernel<16, 5>, tc_smem<16, 5>());
   set((const void*)gemm_tc_kernel<32, 5>, tc_smem<32, 5>());
   set((const void*)gemm_tc_kernel<64, 4>, tc_smem<64, 4>());
   set((const void*)gemm_tc_kernel<128, 3>, tc_smem<128, 3>());
@@ -708,7 +708,7 @@ int tc_pick_bn(int M, int N, int batch) {
 bool tc_ln_input_ok(int M, int N, int K, int splits) {
   if (M <= 0 || K % 128 != 0 || K > 1280 || tc_pick_bn(M, N, 1) != 16) return false;
   const int kb = K / BK, s = splits < 1 ? 1 : (splits > kb ? kb : splits);
-  return s > 1 && (kb + s - 1) / s <= 6;     // 6: ring slots of gemm_tc_kernel<16, 6>
+  return s > 1 && (kb + s - 1) / s <= 5;     // 5: ring slots of gemm_tc_kernel<16, 5>
 }
 
 cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, const TcMap* mx_cached,
@@ -746,7 +746,7 @@ cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, co
     }
   }
   switch (BN) {
-    case 16: return launch_bn<16, 6>(g, e, W, X, p, s, pdl);
+    case 16: return launch_bn<16, 5>(g, e, W, X, p, s, pdl);
     case 32: return launch_bn<32, 5>(g, e, W, X, p, s, pdl);
     case 64: return launch_bn<64, 4>(g, e, W, X, p, s, pdl);
     case 128: return launch_bn<128, 3>(g, e, W, X, p, s, pdl);
