@@ -218,21 +218,10 @@ __global__ void __launch_bounds__(128, 1)
   if (BN == 16 && active && (e.kind == EPI_RESID || e.kind == EPI_QKV || e.kind == EPI_STORE || e.kind == EPI_GELU) &&
       f0 + warp * 32 + lane < p.N)
     bpre = fast_bias(e, f0 + warp * 32 + lane);
-  if (early) pdl_wait();
-
-  // Epilogue inputs that do not depend on the MMAs are loaded now, while the
-  // weights stream (one-token-tile calls): this thread's residual values and
-  // the cache rows of the tile's tokens.
+  // Cache rows of the tile's tokens (QKV): positions, request slots and the
+  // page table were all written before this library call began, so the
+  // table is built before the dependency wait.
   __shared__ int tok_tab[16];
-  float xpre[16];
-  const bool pre_resid = BN == 16 && active && e.kind == EPI_RESID && e.hist == nullptr;
-  if (pre_resid) {
-    const int pn = f0 + warp * 32 + lane;
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-      xpre[c] = (c >= c_lo && c < c_hi && t0 + c < M && pn < p.N) ? __ldcg(e.resid + (size_t)(t0 + c) * e.ldr + pn)
-                                                                  : 0.0f;
-  }
   if (BN == 16 && active && e.kind == EPI_QKV && threadIdx.x < 16) {
     int slot, j, pos, off = -1;
     const int r = t0 + (int)threadIdx.x;
@@ -241,6 +230,19 @@ __global__ void __launch_bounds__(128, 1)
       off = (int)((size_t)page * 2 * e.kv.n_heads * (WS_PAGE * WS_DH) + (size_t)(pos % WS_PAGE) * WS_DH);
     }
     tok_tab[threadIdx.x] = off;
+  }
+  if (early) pdl_wait();
+
+  // Epilogue inputs that do not depend on the MMAs are loaded now, while the
+  // weights stream (one-token-tile calls): this thread's residual values.
+  float xpre[16];
+  const bool pre_resid = BN == 16 && active && e.kind == EPI_RESID && e.hist == nullptr;
+  if (pre_resid) {
+    const int pn = f0 + warp * 32 + lane;
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      xpre[c] = (c >= c_lo && c < c_hi && t0 + c < M && pn < p.N) ? __ldcg(e.resid + (size_t)(t0 + c) * e.ldr + pn)
+                                                                  : 0.0f;
   }
   const bool fast16 = BN == 16 && (pre_resid || e.kind == EPI_QKV || e.kind == EPI_STORE || e.kind == EPI_GELU);
 
