@@ -52,7 +52,7 @@ enum {
   WS_EPOS = -3,          /* a block would pass the decoder context max_pos */
   WS_ECUDA = -4,         /* a CUDA runtime / driver call failed */
   WS_EDEVICE = -5,       /* device status word was set (see ws_status) */
-  WS_EUNSUPPORTED = -6   /* shape or option this build does not implement */
+  WS_EUNSUPPORTED = -6   /* shape or option the library does not implement */
 };
 
 enum { WS_F32 = 0, WS_BF16 = 1 };
