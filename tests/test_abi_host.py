@@ -82,7 +82,9 @@ def test_null_context_calls_fail_cleanly(B):
     for rc in (B.lib.ws_verify(None, 1, 1, 1, 1, 1, 1, None, None),
                B.lib.ws_draft(None, 1, 1, 1, 0.0, 0, 0, None, None),
                B.lib.ws_reset(None, 1, 1, None),
-               B.lib.ws_cross_kv(None, 1, 1, 1, 1, None, 10, 10, None)):
+               B.lib.ws_cross_kv(None, 1, 1, 1, 1, None, 10, 10, None),
+               B.lib.ws_fused_verify(None, 1),
+               B.lib.ws_fused_layernorm(None, -1)):
         assert rc == B.WS_EINVAL
     assert "context" in B.ws_last_error()
     assert B.ws_gemm_engine(None) == "none"
