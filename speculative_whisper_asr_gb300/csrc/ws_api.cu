@@ -557,7 +557,6 @@ template <typename T>
 int cross_kv_impl(ws_ctx* c, int n, const int32_t* req, const void* enc, const int32_t* cu, const int32_t* valid,
                   int maxF, int total_frames, cudaStream_t s) {
   const ws_model_desc& d = c->d;
-  const int D = d.d_model;
   CK(launch_set_frames(n, req, cu, valid, d.max_frames, c->Fc, c->Fv, c->status, s));
   for (int l = 0; l < c->n_xl; ++l) {
     const LayerW& w = l < d.n_layers ? c->tl[l] : c->dl[l - d.n_layers];
