@@ -15,8 +15,10 @@
 // column: every output element accumulates its k-blocks in the same order
 // whatever the number of tokens.  Split-K (fixed per weight shape, never per
 // token count) spreads small-M GEMMs over the SMs: the splits of a tile form
-// one thread-block cluster and rank 0 adds the fp32 partials in split order
-// through distributed shared memory.
+// one thread-block cluster whose ranks each add the fp32 partials of their
+// share of the token columns in split order through distributed shared
+// memory.  A one-token-tile GEMM whose input is the layer norm of the
+// residual builds that operand itself.
 //
 // Each kernel releases its dependents (programmatic dependent launch) right
 // after its prologue, and issues the weight TMA loads of the first ring slots
@@ -335,14 +337,13 @@ __global__ void __launch_bounds__(128, 1)
     }
   } else if (active && p.splits > 1) {
     // Split-K: the splits of one tile form a thread-block cluster.  Each CTA
-    // parks its fp32 partial in its own (now idle) ring memory; rank 0 reads
-    // the others through distributed shared memory and adds them in split
-    // order 0, 1, 2, ...  Every CTA of an active cluster reaches both cluster
-    // barriers, also after a timed-out wait.
-    // Every rank then folds its own share of each 16-column group (columns
-    // [c_lo, c_hi)), reading the partials of ranks 0, 1, 2, ... through
-    // distributed shared memory and adding them in that order, and stores
-    // those columns; the ranks' shares are disjoint and cover the group.
+    // parks its fp32 partial in its own (now idle) ring memory; after a
+    // cluster barrier every rank folds its own share of each 16-column group
+    // (columns [c_lo, c_hi)), reading the partials of ranks 0, 1, 2, ...
+    // through distributed shared memory and adding them in that order, and
+    // stores those columns; the ranks' shares are disjoint and cover the
+    // group.  Every CTA of an active cluster reaches both cluster barriers,
+    // also after a timed-out wait.
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
     float* mine = reinterpret_cast<float*>(ring);
