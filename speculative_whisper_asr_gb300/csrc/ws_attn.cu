@@ -1,14 +1,19 @@
 // Decode-shaped attention for block verification and drafting: up to 16
 // query rows per request and head against a key range split into 64-key
-// chunks.
+// chunks.  Each chunk gives a partial (max, sum, 64 weighted values) and
+// the partials of a row are folded in chunk order.  Three variants:
 //
-// One CTA owns (request, head, split).  Thread 0 stages the split's keys and
-// values with two bulk asynchronous copies (cp.async.bulk, completing on an
-// mbarrier), so all of the split's bytes are in flight at once; eight warps
-// then run one online softmax per query row over the split from shared
-// memory.  Each split writes a partial (max, sum, 64 weighted values); the
-// CTA that finishes last for a (request, head) folds the partials in split
-// order and writes the head's output.
+//   * attn_cluster_kernel (bf16, calls of up to 4 requests): one
+//     thread-block cluster per (request, head), one warp per chunk computing
+//     its partial with mma.sync; the cluster folds the rows through
+//     distributed shared memory.
+//   * attn_stream_kernel + attn_fold_kernel (bf16, larger calls): persistent
+//     warps stream (request, head, chunk) units through double-buffered TMA
+//     slots; a second kernel folds the partials.
+//   * attn_split_kernel (fp32 contexts, the drafter's block attention): one
+//     CTA per (request, head, split) stages the split with bulk copies and
+//     runs a scalar online softmax per row; the CTA that finishes last for a
+//     (request, head) folds the partials.
 //
 // Splits start at absolute key multiples of 64 and every reduction has a
 // fixed order, so a row's result does not depend on how many other rows
