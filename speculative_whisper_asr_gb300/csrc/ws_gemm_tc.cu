@@ -585,7 +585,7 @@ cudaError_t launch_persistent(const GemmShape& g, const Epi& e, const CUtensorMa
                               const TcParams& p, cudaStream_t s, bool pdl) {
   const int T = p.tiles_f * p.tiles_t * p.nz;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(T < g_sm_count ? T : g_sm_count);
+  cfg.gridDim = dim3(g_sm_count > 0 && T > g_sm_count ? g_sm_count : T);
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = persistent_smem<BN>();
   cfg.stream = s;
@@ -676,8 +676,6 @@ cudaError_t tc_init_attributes() {
   set((const void*)gemm_tc_kernel<16, 5>, tc_smem<16, 5>());
   set((const void*)gemm_tc_kernel<32, 5>, tc_smem<32, 5>());
   set((const void*)gemm_tc_kernel<64, 4>, tc_smem<64, 4>());
-  set((const void*)gemm_tc_kernel<128, 3>, tc_smem<128, 3>());
-  set((const void*)gemm_tc_kernel<256, 4>, tc_smem<256, 4>());
   set((const void*)gemm_tc_persistent<16>, persistent_smem<16>());
   set((const void*)gemm_tc_persistent<32>, persistent_smem<32>());
   set((const void*)gemm_tc_persistent<64>, persistent_smem<64>());
@@ -739,7 +737,9 @@ cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, co
   }
   const CUtensorMap& W = *reinterpret_cast<const CUtensorMap*>(&mw);
   const CUtensorMap& X = *reinterpret_cast<const CUtensorMap*>(&mx);
-  if (p.splits == 1 && g_sm_count > 0) {
+  // Token tiles wider than 64 never split K: they always run persistent, so
+  // the split-K kernel is compiled for 16 / 32 / 64 tokens only.
+  if (BN > 64 || (p.splits == 1 && g_sm_count > 0)) {
     switch (BN) {
       case 16: return launch_persistent<16>(g, e, W, X, p, s, pdl);
       case 32: return launch_persistent<32>(g, e, W, X, p, s, pdl);
@@ -751,8 +751,6 @@ cudaError_t launch_gemm_tc(const GemmShape& g, const Epi& e, const TcMap& mw, co
   switch (BN) {
     case 16: return launch_bn<16, 5>(g, e, W, X, p, s, pdl);
     case 32: return launch_bn<32, 5>(g, e, W, X, p, s, pdl);
-    case 64: return launch_bn<64, 4>(g, e, W, X, p, s, pdl);
-    case 128: return launch_bn<128, 3>(g, e, W, X, p, s, pdl);
-    default: return launch_bn<256, 4>(g, e, W, X, p, s, pdl);
+    default: return launch_bn<64, 4>(g, e, W, X, p, s, pdl);
   }
 }
