@@ -13,6 +13,10 @@ Weights are random N(0, 0.02), encoder states N(0, 1) (seeded).
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
   --impl reference  times the CPU oracle (the reference arm) on a bounded
                     sample of the same workload.
+The default line also carries, under "workloads", the batch-96 sampling
+workload (large-v3, T = 0.7, rejection rule) and the batch-16 turbo workload
+of the same metric (--no-sub leaves them out).  Timed steps of the headline
+cycle through four corruption plans, so tau is an average over plans.
 Under torchrun (N > 1) every rank decodes its own batch (weak scaling); the
 time is the max over ranks.
 """
@@ -37,6 +41,7 @@ METRIC = "accepted decoder tokens/s at batch 1/16/96; verify-step HBM GB/s vs pe
 SEED = 1
 BUDGET = 224
 P_CORRUPT = 0.2
+N_PLANS = 4          # corruption plans; step k uses plan k mod 4, so tau averages over plans
 
 
 class Workload:
@@ -116,6 +121,15 @@ def verify_bytes(s: synth.ModelShape, n_req: int, H: int, L_mean: float, frames:
     return float(weights + xkv + skv)
 
 
+def tau_closed_form(pj) -> float | None:
+    """Expected tokens per verify of a full round with independent
+    corruption probabilities p_j: 1 + sum_k prod_{j<=k} (1 - p_j) (chance
+    matches of a random token, ~1/V, ignored)."""
+    if pj is None:
+        return None
+    return float(1.0 + sum(np.prod(1.0 - np.asarray(pj)[:k]) for k in range(1, len(pj) + 1)))
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -187,6 +201,19 @@ def reduce_over_ranks(ms: float, ms_e2e: float, tokens: int, world: int, device)
 
 
 # ---------------------------------------------------------------- GPU arm
+_WEIGHTS: dict = {}
+
+
+def _weights(s: synth.ModelShape, with_drafter: bool):
+    """Seeded target (and drafter) weights of a shape, drawn once per process."""
+    if s.name not in _WEIGHTS:
+        _WEIGHTS.clear()
+        tw = synth.target_weights(s, SEED)
+        _WEIGHTS[s.name] = (tw, synth.drafter_weights(s, SEED, tw))
+    tw, dw = _WEIGHTS[s.name]
+    return tw, (dw if with_drafter else None)
+
+
 def _setup(wl: Workload, rank: int, with_drafter: bool = True, max_frames: int | None = None):
     """Context, request slots and pinned host encoder states of one workload."""
     import torch
@@ -196,10 +223,8 @@ def _setup(wl: Workload, rank: int, with_drafter: bool = True, max_frames: int |
     torch.cuda.set_stream(stream)
     dev = torch.device("cuda", torch.cuda.current_device())
     s, n = wl.shape, wl.n
-    tw = synth.target_weights(s, SEED)
-    dw = synth.drafter_weights(s, SEED, tw) if with_drafter else None
+    tw, dw = _weights(s, with_drafter)
     dec = R.Decoder(s, tw, dw, max_batch=n, max_frames=max_frames or int(wl.frames.max()))
-    del tw, dw
     req = dec.slots(list(range(n)))
     ids = rank_requests(rank, n)
     As = [synth.encoder_states(s, SEED, ids[i], frames=int(wl.frames[i])) for i in range(n)]
@@ -224,10 +249,13 @@ def _trajectory_plan(dec, req, wl: Workload, rank: int, dev):
     for i in range(n):
         t = list(s.prompt) + ar[i]
         traj[i, :len(t)] = t
-    plan = synth.corruption_plan(n, s.max_pos, s.K, wl.pj, s.vocab, SEED + 100 + rank)
-    syn = (torch.as_tensor(traj, device=dev), torch.as_tensor(plan.mask, device=dev),
-           torch.as_tensor(plan.tok, device=dev))
-    return ar, syn, ar_time
+    plans = [synth.corruption_plan(n, s.max_pos, s.K, wl.pj, s.vocab, SEED + 100 + 10 * rank + k)
+             for k in range(N_PLANS)]
+    syn = (torch.as_tensor(traj, device=dev), torch.as_tensor(plans[0].mask, device=dev),
+           torch.as_tensor(plans[0].tok, device=dev))
+    stacked = (torch.as_tensor(np.stack([p.mask for p in plans]), device=dev),
+               torch.as_tensor(np.stack([p.tok for p in plans]), device=dev))
+    return ar, syn, ar_time, stacked
 
 
 def _timed(step, steps, world, stream):
@@ -265,7 +293,8 @@ def run_gpu(args, rank: int, world: int, wl: Workload):
     enc = host_enc.to(dev).view(torch.bfloat16)
     maxF, totF = int(wl.frames.max()), int(wl.frames.sum())
     cu, _ = dec.cross_kv(req, enc, wl.frames)
-    ar, syn, ar_time = _trajectory_plan(dec, req, wl, rank, dev)
+    ar, syn, ar_time, plans = _trajectory_plan(dec, req, wl, rank, dev)
+    n_step = [0]
 
     batch = dec.new_batch(req, wl.budgets)
     budgets = torch.as_tensor(wl.budgets, device=dev)
@@ -288,6 +317,10 @@ def run_gpu(args, rank: int, world: int, wl: Workload):
         """One pass of the whole path; returns the number of rounds."""
         if e2e:
             enc.view(torch.int16).copy_(host_enc, non_blocking=True)
+        k = n_step[0] % N_PLANS            # this step's corruption plan (device-to-device, ~0.2 MB)
+        n_step[0] += 1
+        syn[1].copy_(plans[0][k], non_blocking=True)
+        syn[2].copy_(plans[1][k], non_blocking=True)
         B.ws_cross_kv(dec.ctx, n, req.data_ptr(), enc.data_ptr(), cu.data_ptr(), None, maxF, totF,
                       stream.cuda_stream)
         batch.budget.copy_(budgets)
@@ -319,9 +352,10 @@ def run_gpu(args, rank: int, world: int, wl: Workload):
         return rnd
 
     for w in range(args.warmup):
-        step(stats=(w == 0))
+        step(stats=True)
     spec = batch.transcripts()
     assert spec == ar, "speculative transcript differs from autoregressive"
+    n_step[0] = 0
 
     # ---- device-resident timed region
     ms, launches, clocks, rounds = _timed(lambda: step(record=True), args.steps, world, stream)
@@ -351,7 +385,10 @@ def run_gpu(args, rank: int, world: int, wl: Workload):
                      "peak_source": src},
         "clocks": clocks,
         "extra": {"rounds_per_step": float(np.mean(rounds)),
-                  "tau": float(wl.budgets.sum()) / n_live,
+                  "tau": float(wl.budgets.sum()) * args.warmup / n_live,
+                  "tau_closed_form": tau_closed_form(wl.pj),
+                  "tau_note": f"measured over the warm-up steps, corruption plans 0..{min(args.warmup, N_PLANS) - 1}; "
+                              f"closed form 1 + sum_k prod_(j<=k) (1 - p_j) for rounds not cut by the budget",
                   "alpha": float(acc.sum().item()) / max(1.0, float(prop.sum().item())),
                   "audio_seconds_per_s": audio_s / (ms * 1e-3),
                   "ar_tokens_per_s_untimed_host_loop": float(wl.budgets.sum()) / ar_time,
@@ -464,7 +501,7 @@ def run_varlen(args, rank: int, world: int, wl: Workload):
     enc = host_enc.to(dev).view(torch.bfloat16)
     F = [int(x) for x in wl.frames]
     dec.cross_kv(req, enc, F)
-    ar, syn, _ = _trajectory_plan(dec, req, wl, rank, dev)
+    ar, syn, _, _ = _trajectory_plan(dec, req, wl, rank, dev)
     # padded encoder states: zeros beyond each request's frames
     pad = torch.zeros(n * Fpad, s.d_model, dtype=torch.bfloat16, device=dev)
     off = 0
@@ -584,14 +621,39 @@ def run_oracle_sample(budget_tokens: int = 48):
     return len(res.tokens), dt, cores
 
 
+def run_workload(args, rank: int, world: int, wl: Workload):
+    import torch
+    if wl.temperature > 0.0:
+        r = run_sampling(args, rank, world, wl)
+    elif wl.name == "turbo-b64-varlen":
+        r = run_varlen(args, rank, world, wl)
+    else:
+        r = run_gpu(args, rank, world, wl)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()            # the next workload's context gets the memory back
+    return r
+
+
+def sub_summary(wl: Workload, args, r: dict) -> dict:
+    """One workload of the metric, as a sub-object of the headline line."""
+    out = {"config": wl.config(), "value": r["value"], "unit": "tokens/s", "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "gpu_launches": r["launches"],
+           "roofline": r["roofline"], "clocks": r["clocks"], "extra": r["extra"]}
+    if "e2e" in r:
+        out["e2e"] = {"value": r["e2e"], "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                      "d2h_bytes_per_step": r["d2h"]}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=8)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="headline workload only (no batch 16 / 96 sub-objects)")
     ap.add_argument("--profile", type=int, default=0, help="run N rounds of the profiling case and exit")
     ap.add_argument("--profile-part", default="round", choices=["round", "cross_kv"])
     ap.add_argument("--profile-layers", type=int, default=0, help="profiling case with fewer decoder layers")
@@ -633,12 +695,16 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
     wl = make_workload(args.workload, args.batch)
-    if wl.temperature > 0.0:
-        r = run_sampling(args, rank, world, wl)
-    elif args.workload == "turbo-b64-varlen":
-        r = run_varlen(args, rank, world, wl)
-    else:
-        r = run_gpu(args, rank, world, wl)
+    r = run_workload(args, rank, world, wl)
+    subs = {}
+    if args.workload == "large-v3-b1" and args.batch == 1 and not args.no_sub:
+        # the batch-96 and batch-16 workloads of the same metric, fewer timed steps
+        sub = argparse.Namespace(**vars(args))
+        sub.steps, sub.warmup = min(args.steps, 4), 3
+        for name in ("large-v3-b96-t0.7", "turbo-b16"):
+            w2 = make_workload(name)
+            r2 = run_workload(sub, rank, world, w2)
+            subs[name] = sub_summary(w2, sub, r2)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "large-v3-b1":
         tok, dt, cores = run_oracle_sample()
@@ -656,6 +722,8 @@ def main():
                 "config": dict(wl.config(), parallelism=f"replicas x{world}"),
                 "e2e": e2e, "gpu_launches": r["launches"], "roofline": r["roofline"], "cpu_baseline": cpu,
                 "clocks": r["clocks"], "extra": r["extra"]}
+        if subs:
+            line["workloads"] = subs
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

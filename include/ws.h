@@ -279,9 +279,14 @@ void ws_graph_free(ws_graph* graph);
  *   suppress  optional [ceil(vocab/32)] uint32 bitmask (device), or NULL
  * Scratch is a fixed 256 KB array inside the library (held by every GPU
  * that loads it until the process exits); rows > 1024 return WS_EINVAL.
- * The first call on each device looks up that array's device address, so it
- * should come before any stream capture.  Calls share the array: calls whose
- * work overlaps on the GPU (other streams, other unordered threads) race.
+ * The array's device address belongs to one CUDA context: the first call in
+ * each context (the primary context of a device, a context the caller
+ * created and made current, a new primary context after cudaDeviceReset)
+ * looks it up with that context current and caches it for that context
+ * only, so that first call should come before any stream capture.  Calls
+ * share the array: calls whose work overlaps on the GPU (other streams,
+ * other unordered threads) race.  A CUDA error already pending on the
+ * calling thread is returned as WS_ECUDA without launching anything.
  * Errors: ws_last_error(NULL). */
 int ws_argmax_rows_noalloc(const float* logits, int rows, int vocab, const uint32_t* suppress,
                            int32_t* out, ws_stream stream);

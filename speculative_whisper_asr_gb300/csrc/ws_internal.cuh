@@ -37,8 +37,10 @@ __device__ __forceinline__ uint32_t f32_order(float f) {
   uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-// Argmax key: value first, then the LOWEST id wins ties.
+// Argmax key: value first, then the LOWEST id wins ties.  -0 and +0 are
+// equal values, so -0 is keyed as +0 and the tie goes to the lower id.
 __device__ __forceinline__ unsigned long long argmax_key(float v, int id) {
+  if (v == 0.0f) v = 0.0f;
   return ((unsigned long long)f32_order(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
 }
 __device__ __forceinline__ int argmax_key_id(unsigned long long k) {

@@ -71,12 +71,44 @@ __global__ void noalloc_argmax_final(int rows, const unsigned long long* part, i
   out[row] = argmax_key_id(best);
 }
 
+// Device address of g_argmax_part per CUDA context: a __device__ array has
+// its own copy, at its own address, in every context that loads the module
+// (the primary context of each device, any context a host framework creates
+// itself, a fresh primary context after cudaDeviceReset).  Entries are
+// looked up with the context current and never cross contexts.
+struct PartAddr {
+  void* ctx;
+  unsigned long long* ptr;
+};
 std::mutex g_mu;
-unsigned long long* g_part_ptr[64] = {};   // device address of g_argmax_part, per device
+PartAddr g_part[64] = {};
+int g_n_part = 0;
+using CtxGetCurrent = int (*)(void**);     // CUresult cuCtxGetCurrent(CUcontext*)
+CtxGetCurrent g_ctx_get = nullptr;
 
 int fail(int code, const char* msg) {
   ws_set_thread_error(msg);   // readable through ws_last_error(NULL)
   return code;
+}
+
+// The calling thread's current context (after making sure the runtime has
+// one), or nullptr.  Called with g_mu held.
+void* current_context() {
+  if (!g_ctx_get) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return nullptr;
+    g_ctx_get = reinterpret_cast<CtxGetCurrent>(fn);
+  }
+  void* ctx = nullptr;
+  if (g_ctx_get(&ctx) != 0) return nullptr;
+  if (!ctx) {
+    // no context on this thread yet: the runtime binds the device's primary one
+    if (cudaFree(nullptr) != cudaSuccess || g_ctx_get(&ctx) != 0) return nullptr;
+  }
+  return ctx;
 }
 
 }  // namespace
@@ -87,25 +119,37 @@ extern "C" int ws_argmax_rows_noalloc(const float* logits, int rows, int vocab, 
   if (rows < 0 || vocab < 1) return fail(WS_EINVAL, "rows must be >= 0 and vocab >= 1");
   if (rows > WS_NOALLOC_MAX_ROWS) return fail(WS_EINVAL, "rows exceed the no-allocation scratch capacity (1024)");
   if (rows == 0) return WS_OK;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(WS_ECUDA, "no current CUDA device");
+  // an error left by the caller's earlier work is reported as such, not as ours
+  if (cudaError_t prior = cudaPeekAtLastError(); prior != cudaSuccess)
+    return fail(WS_ECUDA, (std::string("a CUDA error was pending before this call: ") +
+                           cudaGetErrorString(prior)).c_str());
   unsigned long long* part = nullptr;
   {
-    // once per device, with that device current: host code needs the
+    // once per context, with that context current: host code needs the
     // array's device address (its name on the host is only a stand-in)
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_part_ptr[dev]) {
+    void* ctx = current_context();
+    if (!ctx) return fail(WS_ECUDA, "no current CUDA context");
+    for (int i = 0; i < g_n_part; ++i)
+      if (g_part[i].ctx == ctx) part = g_part[i].ptr;
+    if (!part) {
+      if (g_n_part == 64) return fail(WS_ECUDA, "more than 64 CUDA contexts used this entry point");
       void* p = nullptr;
       cudaError_t e = cudaGetSymbolAddress(&p, g_argmax_part);
       if (e != cudaSuccess || !p) return fail(WS_ECUDA, "cudaGetSymbolAddress of the scratch array failed");
-      g_part_ptr[dev] = static_cast<unsigned long long*>(p);
+      part = static_cast<unsigned long long*>(p);
+      g_part[g_n_part++] = {ctx, part};
     }
-    part = g_part_ptr[dev];
   }
   cudaStream_t s = (cudaStream_t)stream;
-  noalloc_argmax_part<<<dim3(rows, WS_NOALLOC_CHUNKS), NT, 0, s>>>(logits, vocab, suppress, part);
-  noalloc_argmax_final<<<(rows + 127) / 128, 128, 0, s>>>(rows, part, out);
-  ws_count_launches(2);
-  if (cudaGetLastError() != cudaSuccess) return fail(WS_ECUDA, "kernel launch failed");
+  void* a1[] = {(void*)&logits, (void*)&vocab, (void*)&suppress, (void*)&part};
+  cudaError_t e = cudaLaunchKernel((const void*)noalloc_argmax_part, dim3(rows, WS_NOALLOC_CHUNKS), dim3(NT), a1,
+                                   0, s);
+  if (e != cudaSuccess) return fail(WS_ECUDA, (std::string("pass 1 launch: ") + cudaGetErrorString(e)).c_str());
+  const unsigned long long* cpart = part;
+  void* a2[] = {(void*)&rows, (void*)&cpart, (void*)&out};
+  e = cudaLaunchKernel((const void*)noalloc_argmax_final, dim3((rows + 127) / 128), dim3(128), a2, 0, s);
+  ws_count_launches(e == cudaSuccess ? 2 : 1);
+  if (e != cudaSuccess) return fail(WS_ECUDA, (std::string("pass 2 launch: ") + cudaGetErrorString(e)).c_str());
   return WS_OK;
 }

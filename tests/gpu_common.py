@@ -49,14 +49,107 @@ def sampled_near_boundary(m) -> bool:
 
 
 def tokens_match(gpu: list, ora: list, margins: list, near=greedy_near_tie):
-    """Exact token equality, except at a first difference where the oracle's
-    decision was a near tie (`near(margin)`); there the comparison stops."""
+    """Exact token equality up to the first difference, which must sit where
+    the oracle's decision was a near tie (`near(margin)`).  Returns the number
+    of positions compared.  Used where the decoding cannot be restarted from
+    the oracle's token with the same random stream (speculative sampling,
+    whose Philox counters follow the round boundaries)."""
     for i, (g, o) in enumerate(zip(gpu, ora)):
         if g != o:
             assert near(margins[i]), f"token {i}: gpu {g} != oracle {o} with margin {margins[i]}"
             return i
     assert len(gpu) == len(ora), (len(gpu), len(ora))
     return len(gpu)
+
+
+def tokens_match_resuming(run_from, ora: list, margins: list, near=greedy_near_tie, max_resumes: int = 12,
+                          first=None):
+    """Emitted tokens compared exactly over the whole transcript; at a
+    difference where the oracle's decision was a near tie the GPU decode is
+    restarted from the oracle's tokens up to and including that position and
+    the comparison goes on from there.  `run_from(prefix)` returns the GPU
+    transcript of a decode that starts from `prefix` (prefix included);
+    `first`, when given, is the GPU transcript of the unrestarted decode
+    (e.g. one request of a batched run), compared over len(ora) tokens.
+    Returns (positions compared, restarts)."""
+    prefix: list = []
+    gpu = list(first[:len(ora)]) if first is not None else run_from(prefix)
+    resumes = 0
+    while True:
+        n = min(len(gpu), len(ora))
+        diff = next((k for k in range(len(prefix), n) if gpu[k] != ora[k]), None)
+        if diff is None:
+            assert len(gpu) == len(ora), (len(gpu), len(ora))
+            return len(ora), resumes
+        assert near(margins[diff]), f"token {diff}: gpu {gpu[diff]} != oracle {ora[diff]} with margin {margins[diff]}"
+        resumes += 1
+        assert resumes <= max_resumes, f"more than {max_resumes} near ties"
+        prefix = list(ora[:diff + 1])
+        gpu = run_from(prefix)
+        assert gpu[:len(prefix)] == prefix
+
+
+def force_prefix(dec, req, s, prefix: list):
+    """Enter the prompt and prefix[:-1] into request `req`'s cache by forced
+    verification (one block for the prompt, then one row per token): the
+    cache state greedy decoding leaves after emitting those tokens.  The
+    caller makes prefix[-1] the next anchor."""
+    import speculative_whisper_asr_gb300.binding as B
+    stream = torch.cuda.current_stream().cuda_stream
+    dec.reset(req)
+    scratch = dec.new_batch(req, [10 ** 6])
+    for block in [list(s.prompt)] + [[t] for t in prefix[:-1]]:
+        H = len(block)
+        blk, bl = dev_i32([block]), dev_i32([H])
+        t = torch.zeros(1, H, dtype=torch.int32, device="cuda")
+        dec.verify(req, blk, bl, t)
+        a = scratch._args(B.WS_ACCEPT_FORCED, H, blk, bl, t, scratch.block1, scratch.blen)
+        B.ws_accept(dec.ctx, 1, req.data_ptr(), a, stream)
+
+
+def ar_from(R, dec, req, s, budget: int):
+    """`run_from` for tokens_match_resuming: one request's autoregressive
+    greedy decode of `budget` tokens on the GPU, restartable from a prefix."""
+    def run(prefix):
+        if not prefix:
+            b = dec.new_batch(req, [budget])
+            R.run_ar(dec, b)
+            return b.transcripts()[0]
+        left = budget - len(prefix)
+        if left <= 0 or prefix[-1] == s.eos_id:
+            return list(prefix)
+        force_prefix(dec, req, s, prefix)
+        b = dec.new_batch(req, [left])
+        b.block1[0, 0] = int(prefix[-1])
+        b.blen[0] = 1
+        while b.poll_done() < 1:
+            b.ar_step(graph=False)
+        return list(prefix) + b.transcripts()[0]
+    return run
+
+
+def ar_sampling_from(R, dec, req, s, budget: int, T: float, seed: int):
+    """`run_from` for autoregressive sampling: token r of the transcript is
+    drawn in round r (Philox counter (slot, r, 1, 2)), so a restart from the
+    oracle's first r tokens continues with round r on both sides."""
+    def run(prefix):
+        if not prefix:
+            b = dec.new_batch(req, [budget], sampling=True)
+            R.run_ar_sampling(dec, b, T, seed)
+            return b.transcripts()[0]
+        left = budget - len(prefix)
+        if left <= 0 or prefix[-1] == s.eos_id:
+            return list(prefix)
+        force_prefix(dec, req, s, prefix)
+        b = dec.new_batch(req, [left], sampling=True)
+        b.block1[0, 0] = int(prefix[-1])
+        b.blen[0] = 1
+        rnd = len(prefix)
+        while b.poll_done() < 1:
+            b.ar_sample_step(rnd, T, seed)
+            rnd += 1
+        return list(prefix) + b.transcripts()[0]
+    return run
 
 
 def small_shape(dtype="f32", **kw):

@@ -24,8 +24,8 @@ import torch
 import synth
 from oracle import model as M
 from oracle import philox
-from gpu_common import (dev_i32, greedy_near_tie_bf16, logits_close, sampled_near_boundary, small_shape,
-                        tokens_match)
+from gpu_common import (ar_from, ar_sampling_from, dev_i32, greedy_near_tie_bf16, logits_close,
+                        sampled_near_boundary, small_shape, tokens_match, tokens_match_resuming)
 
 pytestmark = pytest.mark.gpu
 
@@ -133,14 +133,16 @@ def test_tiny_sampling_transcripts_match_oracle(RB):
     R.run_ar_sampling(dec, b, T, seed)
     ref = M.sampling_plain(orc, orc.new_request(A), budget, T, seed, 1)
     assert len(ref.margins) == len(ref.tokens)
-    n1 = tokens_match(b.transcripts()[0], ref.tokens, ref.margins, sampled_near_boundary)
+    n1, _ = tokens_match_resuming(ar_sampling_from(R, dec, req, s, budget, T, seed), ref.tokens, ref.margins,
+                                  sampled_near_boundary, first=b.transcripts()[0])
+    assert n1 == budget
     b2 = dec.new_batch(req, [budget], sampling=True)
     rounds = R.run_spec(dec, b2, temperature=T, seed=seed)
     ref2 = M.speculative_sampling(orc, orc.new_request(A), budget, T, seed, 1)
     n2 = tokens_match(b2.transcripts()[0], ref2.tokens, ref2.margins, sampled_near_boundary)
     if n2 == len(ref2.tokens):
         assert rounds == ref2.rounds
-    assert n1 >= 10 and n2 >= 10        # a boundary case this early would be suspicious
+    assert n2 >= 10        # a boundary case this early would be suspicious
     assert dec.status() == 0
 
 
@@ -233,8 +235,10 @@ def test_turbo_batch16_continuation_drafts(RB):
     assert rounds < max(budgets) / 2.5
     orc = M.Oracle(s, tw, None)
     for i in (0, n - 1):
-        ref = M.greedy_cached(orc, orc.new_request(As[i]), 12)
-        tokens_match(ar[i][:12], ref.tokens, ref.margins, greedy_near_tie_bf16)
+        ref = M.greedy_cached(orc, orc.new_request(As[i]), 32)
+        cnt, _ = tokens_match_resuming(ar_from(R, dec, dec.slots([i]), s, 32), ref.tokens, ref.margins,
+                                       greedy_near_tie_bf16, first=ar[i])
+        assert cnt == 32
     assert dec.status() == 0
 
 
@@ -272,6 +276,10 @@ def test_varlen_batch64_packed_and_padded(RB):
     assert rows_p < rounds_pad * n * (s.K + 1)
     orc = M.Oracle(s, tw, None)
     i = int(np.argmin(F))
-    ref = M.greedy_cached(orc, orc.new_request(As[i]), min(10, int(budgets[i])))
-    tokens_match(ar[i][:len(ref.tokens)], ref.tokens, ref.margins, greedy_near_tie_bf16)
+    nb = min(32, int(budgets[i]))
+    ref = M.greedy_cached(orc, orc.new_request(As[i]), nb)
+    dec.cross_kv(dec.slots([i]), dec.enc_tensor(As[i]), [int(F[i])])     # packed again for the restarts
+    cnt, _ = tokens_match_resuming(ar_from(R, dec, dec.slots([i]), s, nb), ref.tokens, ref.margins,
+                                   greedy_near_tie_bf16, first=ar[i])
+    assert cnt == nb
     assert dec.status() == 0

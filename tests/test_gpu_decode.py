@@ -9,7 +9,8 @@ import torch
 
 import synth
 from oracle import model as M
-from gpu_common import MARGIN, dev_i32, logits_close, near_tie_for, small_shape, tokens_match
+from gpu_common import (MARGIN, ar_from, dev_i32, logits_close, near_tie_for, small_shape,
+                        tokens_match_resuming)
 
 pytestmark = pytest.mark.gpu
 
@@ -57,7 +58,8 @@ def test_tiny_autoregressive_matches_oracle(R, tiny):
     R.run_ar(dec, b)
     got = b.transcripts()[0]
     assert len(got) == 64
-    tokens_match(got, ref.tokens, ref.margins)
+    n, _ = tokens_match_resuming(ar_from(R, dec, req, s, 64), ref.tokens, ref.margins, first=got)
+    assert n == 64
 
 
 def test_tiny_speculative_equals_autoregressive(R, tiny):
@@ -154,7 +156,10 @@ def test_small_batch_varlen(R, dtype):
     assert b2.transcripts() == ar
     for i in range(3):
         ref = M.greedy_cached(orc, orc.new_request(As[i]), budgets[i])
-        tokens_match(ar[i], ref.tokens, ref.margins, near_tie_for(dtype))
+        one = dec.slots([[3, 0, 4][i]])
+        n, _ = tokens_match_resuming(ar_from(R, dec, one, s, budgets[i]), ref.tokens, ref.margins,
+                                     near_tie_for(dtype), first=ar[i])
+        assert n == budgets[i]
     # prefill logits of every request
     dec.reset(req)
     blk = dev_i32([s.prompt] * 3)

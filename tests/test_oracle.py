@@ -245,6 +245,86 @@ def test_drafter_history_mask_and_block_symmetry(small):
     assert np.abs(z1[0] - z1[-1]).max() > 1e-6
 
 
+def _torch_rope(x, pos, n_heads):
+    """RoPE written as complex multiplication: each pair (2i, 2i+1) of a head
+    is the complex number x_2i + j x_2i+1, turned by e^{j phi}, phi the fp32
+    product of the position and theta_i = 10000^(-2i/d_head) (RoFormer;
+    Whisper-Flash App. A.2: base 10,000, FP32 phases)."""
+    R, d = x.shape
+    dh = d // n_heads
+    theta = torch.pow(torch.tensor(10000.0, dtype=torch.float64),
+                      -torch.arange(0, dh, 2, dtype=torch.float64) / dh).float()
+    phi = (torch.as_tensor(pos, dtype=torch.float32)[:, None] * theta[None, :]).double()
+    rot = torch.polar(torch.ones_like(phi), phi)[:, None, :]
+    xc = torch.view_as_complex(x.reshape(R, n_heads, dh // 2, 2).contiguous())
+    return torch.view_as_real(xc * rot).reshape(R, d)
+
+
+def _torch_heads_attend(q, k, v, n_heads):
+    R, d = q.shape
+    sp = lambda t: t.reshape(t.shape[0], n_heads, d // n_heads).transpose(0, 1)
+    return F.scaled_dot_product_attention(sp(q), sp(k), sp(v)).transpose(0, 1).reshape(R, d)
+
+
+def _torch_drafter_logits(shape, tw, dw, resid, A, anchor, t, shift=0):
+    """The drafter of Whisper-Flash §3.2 (Eq. 2) / App. A.2 assembled from
+    torch primitives in float64: input rows [Emb(anchor), m, ..., m] with no
+    absolute position; history memory = LN_h(W_f concat(residual streams))
+    of the accepted positions 0..t-1; per layer one unmasked softmax of the
+    block queries over [history ; block] keys (RoPE at the text positions,
+    history at 0..t-1, block at t..t+K, all moved by `shift`), cross-attention
+    to the drafter's own acoustic K/V, GELU FFN; then the drafter's final LN
+    and the tied head on the K mask rows."""
+    d, nh, K = shape.d_model, shape.n_heads, shape.K
+    T = lambda src, n: torch.from_numpy(np.asarray(src[n], dtype=np.float64))
+    E = T(tw, "tok_emb")
+    hh = F.layer_norm(torch.from_numpy(resid.reshape(t, -1)) @ T(dw, "fuse_w").T, (d,),
+                      T(dw, "lnh_g"), T(dw, "lnh_b"))
+    x = torch.cat([E[anchor][None], T(dw, "mask_emb")[None].repeat(K, 1)])
+    pb = [shift + t + j for j in range(K + 1)]
+    ph = [shift + j for j in range(t)]
+    mem = torch.from_numpy(np.asarray(A, dtype=np.float64))
+    for l in range(shape.drafter_layers):
+        W = lambda n: T(dw, f"layers.{l}.{n}")
+        wq, wk, wv = W("w_qkv")[:d], W("w_qkv")[d:2 * d], W("w_qkv")[2 * d:]
+        h = F.layer_norm(x, (d,), W("ln1_g"), W("ln1_b"))
+        q = _torch_rope(h @ wq.T + W("b_q"), pb, nh)
+        k = torch.cat([_torch_rope(hh @ wk.T, ph, nh), _torch_rope(h @ wk.T, pb, nh)])
+        v = torch.cat([hh @ wv.T + W("b_v"), h @ wv.T + W("b_v")])
+        x = x + F.linear(_torch_heads_attend(q, k, v, nh), W("w_o"), W("b_o"))
+        qc = F.linear(F.layer_norm(x, (d,), W("ln2_g"), W("ln2_b")), W("w_qc"), W("b_qc"))
+        kc, vc = mem @ W("w_kvc")[:d].T, mem @ W("w_kvc")[d:].T + W("b_vc")
+        x = x + F.linear(_torch_heads_attend(qc, kc, vc, nh), W("w_oc"), W("b_oc"))
+        f = F.gelu(F.linear(F.layer_norm(x, (d,), W("ln3_g"), W("ln3_b")), W("w_fc1"), W("b_fc1")))
+        x = x + F.linear(f, W("w_fc2"), W("b_fc2"))
+    hf = F.layer_norm(x[1:], (d,), T(dw, "lnf_g"), T(dw, "lnf_b"))
+    return (hf @ E.T).numpy()
+
+
+def test_draft_logits_match_torch_drafter_block(small):
+    """Pins the drafter's block assembly end to end (anchor row first, K mask
+    rows after it, RoPE at t..t+K against history at 0..t-1, proposals from
+    rows 1..K): the oracle equals the torch drafter above, and moving every
+    position by the same amount leaves the logits unchanged (RoPE only sees
+    relative positions), so no absolute offset hides in either."""
+    orc, tw, dw, A = small
+    req = orc.new_request(A)
+    t = 6
+    rng = np.random.default_rng(12)
+    req.hist[:t] = rng.standard_normal((t, SMALL.n_hist, SMALL.d_model))
+    req.L = t
+    got = orc.draft_logits(req, 321)
+    ref = _torch_drafter_logits(SMALL, tw, dw, req.hist[:t], A, 321, t)
+    assert got.shape == (SMALL.K, SMALL.vocab)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-9)
+    moved = _torch_drafter_logits(SMALL, tw, dw, req.hist[:t], A, 321, t, shift=37)
+    np.testing.assert_allclose(got, moved, rtol=0, atol=1e-4 * np.abs(ref).max())
+    # the anchor token and the history both reach every proposal row
+    assert (np.abs(orc.draft_logits(req, 322) - got).max(axis=1) > 1e-8).all()
+    req.hist[0] += 1.0
+    assert (np.abs(orc.draft_logits(req, 321) - got).max(axis=1) > 1e-8).all()
+
+
 def test_drafter_parameter_counts_match_paper():
     """Whisper-Flash §3.2 / Table 3: 60.7M trainable parameters with audio and
     history, 47.5M without direct audio, 52.5M without the target history."""
