@@ -6,11 +6,11 @@ import synth
 from oracle import model as M
 
 MARGIN = 1e-3     # near-tie rule: a token may differ where the oracle's top-2 margin is below this
-# bf16 configs: logits may differ from the oracle by up to 2e-2 relative, and
-# the measured top-2 margin differences at large-v3 (32 layers, |logits| < 3.4)
-# reach 9e-3 whatever the fp32 summation order, so there a near tie is a
-# margin below 1e-2 (test_large_v3_teacher_forced_margin_error pins the bound).
-MARGIN_BF16 = 1e-2
+# bf16 configs: logits are only fixed to within 2e-2 of the oracle's, so two
+# logits closer than 2e-2 are not resolved by the stated precision: there a
+# near tie is a top-2 margin below 2e-2 (the teacher-forced large-v3 test
+# asserts that the margin itself moves by less than that at every position).
+MARGIN_BF16 = 2e-2
 
 
 def logits_close(gpu: np.ndarray, ora: np.ndarray, tol: float):
