@@ -229,17 +229,20 @@ int ws_status(ws_ctx* ctx, ws_stream stream, int32_t* host_status);
 /* Name of the GEMM engine in use ("simt" or "tcgen05"). */
 const char* ws_gemm_engine(const ws_ctx* ctx);
 
-/* Persistent block verification (Whisper-Flash §3.1 block verification; the
- * same target pass as ws_verify's kernel-per-operation path, with the same
- * arithmetic, so rows are bit-identical).  A bf16 context on the tcgen05
- * engine runs every ws_verify call with n_req * H <= 16 rows as one
- * cooperative kernel (one CTA per SM, grid-wide barriers between stages,
- * weights streamed ahead through shared memory) when the device supports
- * cooperative launch.  Off by default: on GB300 the per-operation path is
- * faster at batch 1 (its kernel boundaries cost less than the persistent
- * kernel's software grid barriers).
+/* Dataflow block verification (Whisper-Flash §3.1: the target scores the
+ * anchor and the proposals in one decoder pass).  A context with one request
+ * slot (max_batch 1), bf16, the tcgen05 engine, d_model a multiple of 256 up
+ * to 1280, d_ff a multiple of d_model and max_pos <= 576 runs every
+ * ws_verify call as one cooperative kernel (one CTA per SM): the work of
+ * each step is cut into tasks that wait only on counters of the tasks whose
+ * outputs they read, and each SM streams its weight tiles ahead through
+ * shared memory independently of those waits.  Its rows agree with the
+ * kernel-per-operation path within the bf16 tolerance, not bit for bit, and
+ * a context should keep one setting for a whole decode (both settings give
+ * speculative output bit-identical to autoregressive output).  Off by
+ * default.
  *   enable  1: use it when eligible; 0: never (the default); -1: query only.
- * Returns 1 when eligible calls take the persistent path, 0 when not, or
+ * Returns 1 when eligible calls take the dataflow path, 0 when not, or
  * WS_EINVAL for a null context.  Host-only; no device work. */
 int ws_fused_verify(ws_ctx* ctx, int enable);
 

@@ -8,7 +8,7 @@
 #include <algorithm>
 #include <vector>
 
-#include "ws_fused.cuh"
+#include "ws_flow.cuh"
 #include "ws_internal.cuh"
 
 // A weight matrix [rows, cols] (row-major, model dtype) and, for the tcgen05
@@ -62,16 +62,17 @@ struct ws_ctx {
   std::vector<XMap> xmaps;
   bool pdl = true;              // programmatic dependent launch allowed
   bool cur_pdl = false;         // PDL for the call in progress (never on the legacy stream)
-  // persistent block verification (bf16, tcgen05, at most 16 rows per call)
-  bool fused_ok = false;        // built and runnable on this device
+  // dataflow block verification (one-request bf16 contexts on the tcgen05 engine)
+  bool flow_ok = false;         // eligible shape, set up and runnable on this device
   bool ln_in_gemm = true;       // layer norm inside eligible GEMMs (ws_fused_layernorm)
-  bool fused_on = false;        // caller's switch (ws_fused_verify); off: the per-op path is faster here
-  int fused_grid = 0, fused_ring = 0, n_fstages = 0;
-  size_t fused_work = 0;
-  FusedStage* fstages = nullptr;     // device copy of the stage table
-  float* fpart = nullptr;
+  bool flow_on = false;         // caller's switch (ws_fused_verify)
+  int flow_grid = 0;
+  const TcMap* fmaps = nullptr; // device: weight maps (16-row boxes), then head, ao, ffn, kv, xkv
+  const FlowLayer* flayers = nullptr;
   int* fctr = nullptr;
-  unsigned* gbar = nullptr;
+  float* xpart = nullptr;
+  float* f2part = nullptr;
+  int max_xchunks = 0;
   float2* pstat = nullptr;      // acceptance scratch: (max, sum exp) per p / q logits row
   float2* qstat = nullptr;
   std::string err;
@@ -136,7 +137,8 @@ struct Layout {
 struct Plan {
   size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
   size_t acnt;
-  size_t fmaps, fstages, fpart, fctr, gbar, pstat, qstat;
+  size_t fmaps, flayers, fctr, xpart, f2part, pstat, qstat;
+  bool flow_shape;
   size_t kv_layer_bytes, total;
   int heads, ppr, n_pages, n_xl, max_split;
 };
@@ -165,6 +167,16 @@ const char* check_desc(const ws_model_desc* d) {
       if (d->hist_layers[i] < 0 || d->hist_layers[i] >= d->n_layers) return "history layer out of range";
   }
   return nullptr;
+}
+
+// Shapes the dataflow verify kernel handles: one request of <= 16 block rows,
+// bf16, d a multiple of 256 up to 1280 (a compute warp's weight quarter of a
+// 16-row task fits one 10 KB ring slot), the FFN a multiple of d, a decoder
+// context of <= 576 positions (self-attention partials of <= 9 chunks).
+bool flow_shape_ok(const ws_model_desc& d) {
+  return d.dtype == WS_BF16 && d.max_batch == 1 && d.max_block <= FLOW_MAX_ROWS && d.d_model % 256 == 0 &&
+         d.d_model <= 1280 && d.d_ff % d.d_model == 0 && d.d_ff / d.d_model <= 8 && d.n_heads <= 64 &&
+         d.max_pos <= 576;
 }
 
 Plan make_plan(const ws_model_desc& d) {
@@ -203,13 +215,15 @@ Plan make_plan(const ws_model_desc& d) {
   p.feat = lay.take(M * nh * D * es);
   p.hpre = lay.take(M * D * 4);
   p.hh = lay.take(M * D * es);
-  // persistent verify: weight TMA maps, stage table, split-K partials, tile counters, grid barrier
-  const size_t widest = std::max({(size_t)3 * D, (size_t)d.d_ff, (size_t)d.vocab});
-  p.fmaps = lay.take((6 * (size_t)d.n_layers + 1) * sizeof(TcMap));
-  p.fstages = lay.take((8 * (size_t)d.n_layers + 3) * sizeof(FusedStage));
-  p.fpart = lay.take((widest + 127) / 128 * 8 * FUSED_MAX_ROWS * 128 * 4);
-  p.fctr = lay.take(((widest + 127) / 128 + 1) * 4);
-  p.gbar = lay.take(64);
+  // dataflow verify (one-request contexts): weight maps, layer table, counters, partials
+  p.flow_shape = flow_shape_ok(d);
+  const size_t fl = p.flow_shape ? 1 : 0;
+  const size_t xch = (d.max_frames + WS_XCHUNK - 1) / WS_XCHUNK;
+  p.fmaps = lay.take(fl * (6 * (size_t)d.n_layers + 5) * sizeof(TcMap));
+  p.flayers = lay.take(fl * d.n_layers * sizeof(FlowLayer));
+  p.fctr = lay.take(fl * ((size_t)d.n_layers * FLOW_CTR_LAYER + FLOW_CTR_GLOBAL) * 4);
+  p.xpart = lay.take(fl * FLOW_MAX_ROWS * d.n_heads * xch * (WS_DH + 2) * 4);
+  p.f2part = lay.take(fl * (D / 16) * (d.d_ff / std::max(1, d.d_model)) * 256 * 4);
   p.pstat = lay.take(M * 8);        // sampling acceptance: softmax statistics per logits row
   p.qstat = lay.take(M * 8);
   p.total = lay.off;
@@ -330,98 +344,92 @@ bool is_hist_layer(const ws_model_desc& d, int l, int& idx) {
   return false;
 }
 
-// --------------------------------------------------------------------------- persistent verify
-// Stage table of the target pass (embedding, 8 stages per layer, LM head,
-// argmax) with the per-op path's split-K factors, copied to the device with
-// the weight TMA maps it points to.  Leaves fused_ok false when the device
-// cannot run the kernel.
-cudaError_t setup_fused(ws_ctx* c, const Plan& p, cudaStream_t s) {
+// --------------------------------------------------------------------------- dataflow verify
+// Weight maps with 16-row boxes for every projection and the LM head, the
+// activation / K/V maps the kernel loads with, and the per-layer table, all
+// copied to the device once.  Leaves flow_ok false when the shape or the
+// device does not allow the kernel.
+cudaError_t setup_flow(ws_ctx* c, const Plan& p, cudaStream_t s) {
   const ws_model_desc& d = c->d;
-  if (c->engine != WS_GEMM_TC || d.dtype != WS_BF16) return cudaSuccess;
-  const int D = d.d_model;
+  if (!p.flow_shape || c->engine != WS_GEMM_TC || !c->as.kv_map || !c->as.xkv_map) return cudaSuccess;
+  const int grid = flow_prepare();
+  cudaGetLastError();                 // a device that cannot run it is not an error
+  if (grid <= 0) return cudaSuccess;
   std::vector<TcMap> maps;
-  std::vector<FusedStage> st;
-  TcMap* dmaps = (TcMap*)(c->ws + p.fmaps);
-  int max_unit_kb = 1;
-  auto gemm_stage = [&](int layer, const Mat& W, int in_kind, const void* g, const void* b, const void* act,
-                        int ld_act, int epi, const void* bias, const void* bias2, void* out, int ldo, int hist) {
-    FusedStage f;
-    memset(&f, 0, sizeof f);
-    f.kind = FS_GEMM; f.layer = layer;
-    f.map = dmaps + maps.size();
-    maps.push_back(W.map);
-    f.N = W.rows; f.kb_total = W.cols / 64; f.splits = splits_for(c, W.rows, W.cols);
-    f.in_kind = in_kind; f.ln_g = g; f.ln_b = b; f.act = (const bf16*)act; f.ld_act = ld_act;
-    f.epi = epi; f.bias = bias; f.bias2 = bias2; f.out = out; f.ldo = ldo; f.hist_idx = hist;
-    max_unit_kb = std::max(max_unit_kb, (f.kb_total + f.splits - 1) / f.splits);
-    st.push_back(f);
+  bool ok = true;
+  auto map16 = [&](const Mat& m) {
+    TcMap t;
+    ok = ok && tc_encode_map(&t, m.p, (uint64_t)m.rows, (uint64_t)m.cols, 16);
+    maps.push_back(t);
   };
-  auto plain = [&](int kind, int layer) {
-    FusedStage f;
-    memset(&f, 0, sizeof f);
-    f.kind = kind; f.layer = layer; f.hist_idx = -1;
-    st.push_back(f);
-  };
-  plain(FS_EMBED, 0);
+  for (const LayerW& w : c->tl) {
+    map16(w.w_qkv); map16(w.w_o); map16(w.w_qc); map16(w.w_oc); map16(w.w_fc1); map16(w.w_fc2);
+  }
+  map16(c->head);
+  const TcMap* ao = nullptr;
+  const TcMap* ffn = nullptr;
+  for (const auto& xm : c->xmaps) {
+    if (xm.base == c->ao) ao = &xm.bn[0];
+    if (xm.base == c->ffn) ffn = &xm.bn[0];
+  }
+  if (!ok || !ao || !ffn) return cudaSuccess;
+  maps.push_back(*ao); maps.push_back(*ffn); maps.push_back(c->kv_map); maps.push_back(c->xkv_map);
+  TcMap* dm = (TcMap*)(c->ws + p.fmaps);
+  std::vector<FlowLayer> fl(d.n_layers);
   for (int l = 0; l < d.n_layers; ++l) {
     const LayerW& w = c->tl[l];
+    FlowLayer& f = fl[l];
+    f.map_qkv = dm + 6 * l; f.map_o = dm + 6 * l + 1; f.map_qc = dm + 6 * l + 2;
+    f.map_oc = dm + 6 * l + 3; f.map_fc1 = dm + 6 * l + 4; f.map_fc2 = dm + 6 * l + 5;
+    f.b_q = (const bf16*)w.b_q; f.b_v = (const bf16*)w.b_v; f.b_o = (const bf16*)w.b_o;
+    f.b_qc = (const bf16*)w.b_qc; f.b_oc = (const bf16*)w.b_oc; f.b_fc1 = (const bf16*)w.b_fc1;
+    f.b_fc2 = (const bf16*)w.b_fc2;
+    f.ln1_g = (const bf16*)w.ln1_g; f.ln1_b = (const bf16*)w.ln1_b; f.ln2_g = (const bf16*)w.ln2_g;
+    f.ln2_b = (const bf16*)w.ln2_b; f.ln3_g = (const bf16*)w.ln3_g; f.ln3_b = (const bf16*)w.ln3_b;
     int hidx = -1;
-    if (!is_hist_layer(d, l, hidx)) hidx = -1;
-    gemm_stage(l, w.w_qkv, FIN_LN, w.ln1_g, w.ln1_b, nullptr, 0, EPI_QKV, w.b_q, w.b_v, c->q, D, -1);
-    plain(FS_SELF, l);
-    gemm_stage(l, w.w_o, FIN_ACT, nullptr, nullptr, c->ao, D, EPI_RESID, w.b_o, nullptr, nullptr, 0, -1);
-    gemm_stage(l, w.w_qc, FIN_LN, w.ln2_g, w.ln2_b, nullptr, 0, EPI_STORE, w.b_qc, nullptr, c->q, D, -1);
-    plain(FS_CROSS, l);
-    gemm_stage(l, w.w_oc, FIN_ACT, nullptr, nullptr, c->ao, D, EPI_RESID, w.b_oc, nullptr, nullptr, 0, -1);
-    gemm_stage(l, w.w_fc1, FIN_LN, w.ln3_g, w.ln3_b, nullptr, 0, EPI_GELU, w.b_fc1, nullptr, c->ffn, d.d_ff, -1);
-    gemm_stage(l, w.w_fc2, FIN_ACT, nullptr, nullptr, c->ffn, d.d_ff, EPI_RESID, w.b_fc2, nullptr, nullptr, 0, hidx);
+    f.hist_idx = is_hist_layer(d, l, hidx) ? hidx : -1;
   }
-  gemm_stage(d.n_layers, c->head, FIN_LN, c->lnf_g, c->lnf_b, nullptr, 0, EPI_LOGITS, nullptr, nullptr, nullptr, 0,
-             -1);
-  plain(FS_ARGMAX, 0);
-  for (const FusedStage& f : st)    // every store target the kernel will use exists
-    if (f.kind == FS_GEMM && ((f.epi == EPI_STORE || f.epi == EPI_GELU) ? f.out == nullptr : false)) return cudaSuccess;
-  c->fstages = (FusedStage*)(c->ws + p.fstages);
-  c->fpart = (float*)(c->ws + p.fpart);
-  c->fctr = (int*)(c->ws + p.fctr);
-  c->gbar = (unsigned*)(c->ws + p.gbar);
-  c->n_fstages = (int)st.size();
-  cudaError_t e = cudaMemcpyAsync(dmaps, maps.data(), maps.size() * sizeof(TcMap), cudaMemcpyHostToDevice, s);
+  cudaError_t e = cudaMemcpyAsync(dm, maps.data(), maps.size() * sizeof(TcMap), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
-    e = cudaMemcpyAsync(c->fstages, st.data(), st.size() * sizeof(FusedStage), cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(c->fctr, 0, p.gbar - p.fctr, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(c->gbar, 0, 64, s);
+    e = cudaMemcpyAsync(c->ws + p.flayers, fl.data(), fl.size() * sizeof(FlowLayer), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(c->ws + p.fctr, 0, ((size_t)d.n_layers * FLOW_CTR_LAYER + FLOW_CTR_GLOBAL) * 4, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);    // host vectors go out of scope
   if (e != cudaSuccess) return e;
-  c->fused_work = fused_work_bytes(max_unit_kb);
-  c->fused_ring = fused_prepare(c->fused_work, &c->fused_grid);
-  c->fused_ok = c->fused_ring > 0;
-  cudaGetLastError();      // a device without cooperative launch is not an error
+  c->fmaps = dm;
+  c->flayers = (const FlowLayer*)(c->ws + p.flayers);
+  c->fctr = (int*)(c->ws + p.fctr);
+  c->xpart = (float*)(c->ws + p.xpart);
+  c->f2part = (float*)(c->ws + p.f2part);
+  c->max_xchunks = (d.max_frames + WS_XCHUNK - 1) / WS_XCHUNK;
+  c->flow_grid = grid;
+  c->flow_ok = true;
   return cudaSuccess;
 }
 
-int fused_verify(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* block, const int32_t* blen,
-                 int32_t* target, float* logits, cudaStream_t s) {
+int flow_verify(ws_ctx* c, const int32_t* req, int H, const int32_t* block, const int32_t* blen, int32_t* target,
+                float* logits, cudaStream_t s) {
   const ws_model_desc& d = c->d;
-  FusedArgs a;
+  const int nL = d.n_layers;
+  FlowArgs a;
   memset(&a, 0, sizeof a);
-  a.stages = c->fstages; a.n_stages = c->n_fstages; a.ring_slots = c->fused_ring; a.work_bytes = c->fused_work;
-  a.n = n; a.H = H; a.M = n * H;
-  a.d = d.d_model; a.V = d.vocab; a.heads = c->heads; a.max_pos = d.max_pos; a.max_block = d.max_block;
-  a.n_hist = d.n_hist;
-  a.nsplit_self = (d.max_pos + WS_XCHUNK - 1) / WS_XCHUNK;
-  a.nsplit_cross = std::max(1, (c->max_fc + WS_XCHUNK - 1) / WS_XCHUNK);
-  a.rm.mode = ROW_VERIFY; a.rm.H = H; a.rm.max_pos = d.max_pos; a.rm.req_ids = req; a.rm.L = c->L;
-  a.rm.block_len = blen; a.rm.pend_start = c->pend_start; a.rm.pend_n = c->pend_n;
-  a.req_ids = req; a.block = block; a.block_len = blen;
+  a.layers = c->flayers;
+  a.map_head = c->fmaps + 6 * nL; a.map_ao = c->fmaps + 6 * nL + 1; a.map_ffn = c->fmaps + 6 * nL + 2;
+  a.map_kv = c->fmaps + 6 * nL + 3; a.map_xkv = c->fmaps + 6 * nL + 4;
+  a.n_layers = nL; a.d = d.d_model; a.f = d.d_ff; a.heads = c->heads; a.V = d.vocab; a.max_pos = d.max_pos;
+  a.max_block = d.max_block; a.n_hist = d.drafter_layers > 0 ? d.n_hist : 0;
+  a.H = H; a.req_ids = req; a.block = block; a.block_len = blen;
   a.tok_emb = (const bf16*)c->tok_emb; a.pos_emb = (const bf16*)c->pos_emb;
-  a.x = c->x; a.ao = (bf16*)c->ao; a.q = (bf16*)c->q;
+  a.lnf_g = (const bf16*)c->lnf_g; a.lnf_b = (const bf16*)c->lnf_b;
+  a.x = c->x; a.q = (bf16*)c->q; a.ao = (bf16*)c->ao; a.ffn = (bf16*)c->ffn;
+  a.L = c->L; a.Fv = c->Fv; a.pend_start = c->pend_start; a.pend_n = c->pend_n;
   a.kv = c->kv; a.kv_layer_bytes = c->kv_layer_bytes; a.ptab = c->ptab; a.ppr = c->ppr;
-  a.xkv = xkv_of(c); a.Fv = c->Fv; a.hist = c->hist;
-  a.part = c->fpart; a.tile_ctr = c->fctr; a.apart = c->as.part; a.actr = c->as.counters;
+  a.xkv_slot_rows = c->x_slot_elems / WS_DH; a.xkv_layer_rows = c->x_layer_elems / WS_DH;
+  a.max_frames = d.max_frames;
+  a.hist = c->hist; a.xpart = c->xpart; a.max_xchunks = c->max_xchunks; a.fpart = c->f2part;
   a.amax = c->amax; a.logits = logits; a.suppress = c->suppress; a.target = target;
-  a.pend_start = c->pend_start; a.pend_n = c->pend_n; a.gbar = c->gbar; a.status = c->status;
-  CK(launch_fused_verify(a, c->fused_grid, c->fused_work, s));
+  a.ctr = c->fctr; a.status = c->status;
+  CK(launch_flow_verify(a, c->flow_grid, s));
   if (d.drafter_layers > 0) c->pending_H = H > c->pending_H ? H : c->pending_H;
   return WS_OK;
 }
@@ -432,8 +440,8 @@ int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* bloc
                 int32_t* target, float* logits, cudaStream_t s) {
   const ws_model_desc& d = c->d;
   const int D = d.d_model, M = n * H;
-  if (sizeof(T) == 2 && c->fused_ok && c->fused_on && M <= FUSED_MAX_ROWS)
-    return fused_verify(c, n, req, H, block, blen, target, logits, s);
+  if (sizeof(T) == 2 && c->flow_ok && c->flow_on && n == 1 && H <= FLOW_MAX_ROWS)
+    return flow_verify(c, req, H, block, blen, target, logits, s);
   const bool pdl = c->cur_pdl;
   RowMap rm;
   rm.mode = ROW_VERIFY; rm.H = H; rm.max_pos = d.max_pos; rm.req_ids = req; rm.L = c->L;
@@ -695,7 +703,13 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   if (e == cudaSuccess) e = cudaMemsetAsync(c->as.counters, 0, (size_t)desc->max_batch * desc->n_heads * 4, s);
   if (e == cudaSuccess) e = desc->dtype == WS_BF16 ? attn_init_attributes<bf16>() : attn_init_attributes<float>();
   if (e == cudaSuccess) e = launch_rope_table(c->rope, desc->max_pos, s);
-  if (e == cudaSuccess) e = setup_fused(c, p, s);
+  // caches start at zero: masked keys beyond a request's length or frames
+  // then hold finite values (the probabilities of masked keys are exact zeros)
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->kv, 0, p.kv_layer_bytes * desc->n_layers, s);
+  if (e == cudaSuccess && desc->drafter_layers > 0)
+    e = cudaMemsetAsync(c->hkv, 0, p.kv_layer_bytes * desc->drafter_layers, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->xkv, 0, (size_t)desc->max_batch * c->x_slot_elems * c->es, s);
+  if (e == cudaSuccess) e = setup_flow(c, p, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) { fail(nullptr, WS_ECUDA, "context init: %s", cudaGetErrorString(e)); return cleanup(WS_ECUDA); }
   *out = c;
@@ -832,8 +846,8 @@ const char* ws_gemm_engine(const ws_ctx* c) {
 
 int ws_fused_verify(ws_ctx* c, int enable) {
   if (!c) return fail(nullptr, WS_EINVAL, "null context");
-  if (enable >= 0) c->fused_on = enable != 0;
-  return (c->fused_ok && c->fused_on) ? 1 : 0;
+  if (enable >= 0) c->flow_on = enable != 0;
+  return (c->flow_ok && c->flow_on) ? 1 : 0;
 }
 
 int ws_fused_layernorm(ws_ctx* c, int enable) {
