@@ -72,7 +72,8 @@ struct ws_ctx {
   int* fctr = nullptr;
   float* xpart = nullptr;
   float* f2part = nullptr;
-  int max_xchunks = 0;
+  int max_groups = 0;           // cross-attention chunk groups per head
+  int xs_rows = 0;              // residual rows per layer-norm staging pass
   float2* pstat = nullptr;      // acceptance scratch: (max, sum exp) per p / q logits row
   float2* qstat = nullptr;
   std::string err;
@@ -218,11 +219,11 @@ Plan make_plan(const ws_model_desc& d) {
   // dataflow verify (one-request contexts): weight maps, layer table, counters, partials
   p.flow_shape = flow_shape_ok(d);
   const size_t fl = p.flow_shape ? 1 : 0;
-  const size_t xch = (d.max_frames + WS_XCHUNK - 1) / WS_XCHUNK;
-  p.fmaps = lay.take(fl * (6 * (size_t)d.n_layers + 5) * sizeof(TcMap));
+  const size_t xgroups = ((d.max_frames + WS_XCHUNK - 1) / WS_XCHUNK + 3) / 4;
+  p.fmaps = lay.take(fl * (6 * (size_t)d.n_layers + 6) * sizeof(TcMap));
   p.flayers = lay.take(fl * d.n_layers * sizeof(FlowLayer));
   p.fctr = lay.take(fl * ((size_t)d.n_layers * FLOW_CTR_LAYER + FLOW_CTR_GLOBAL) * 4);
-  p.xpart = lay.take(fl * FLOW_MAX_ROWS * d.n_heads * xch * (WS_DH + 2) * 4);
+  p.xpart = lay.take(fl * d.n_heads * xgroups * FLOW_MAX_ROWS * FLOW_GP * 4);
   p.f2part = lay.take(fl * (D / 16) * (d.d_ff / std::max(1, d.d_model)) * 256 * 4);
   p.pstat = lay.take(M * 8);        // sampling acceptance: softmax statistics per logits row
   p.qstat = lay.take(M * 8);
@@ -374,6 +375,12 @@ cudaError_t setup_flow(ws_ctx* c, const Plan& p, cudaStream_t s) {
   }
   if (!ok || !ao || !ffn) return cudaSuccess;
   maps.push_back(*ao); maps.push_back(*ffn); maps.push_back(c->kv_map); maps.push_back(c->xkv_map);
+  // residual rows for the layer norms: whole fp32 rows, as many as the staging buffer holds
+  const int xs_rows = std::min(FLOW_MAX_ROWS, FLOW_XS_BYTES / (4 * d.d_model));
+  TcMap xm;
+  if (!tc_encode_rows_f32(&xm, c->x, (uint64_t)c->mrows, (uint64_t)d.d_model, (uint32_t)xs_rows))
+    return cudaSuccess;
+  maps.push_back(xm);
   TcMap* dm = (TcMap*)(c->ws + p.fmaps);
   std::vector<FlowLayer> fl(d.n_layers);
   for (int l = 0; l < d.n_layers; ++l) {
@@ -401,7 +408,8 @@ cudaError_t setup_flow(ws_ctx* c, const Plan& p, cudaStream_t s) {
   c->fctr = (int*)(c->ws + p.fctr);
   c->xpart = (float*)(c->ws + p.xpart);
   c->f2part = (float*)(c->ws + p.f2part);
-  c->max_xchunks = (d.max_frames + WS_XCHUNK - 1) / WS_XCHUNK;
+  c->max_groups = ((d.max_frames + WS_XCHUNK - 1) / WS_XCHUNK + 3) / 4;
+  c->xs_rows = xs_rows;
   c->flow_grid = grid;
   c->flow_ok = true;
   return cudaSuccess;
@@ -415,7 +423,8 @@ int flow_verify(ws_ctx* c, const int32_t* req, int H, const int32_t* block, cons
   memset(&a, 0, sizeof a);
   a.layers = c->flayers;
   a.map_head = c->fmaps + 6 * nL; a.map_ao = c->fmaps + 6 * nL + 1; a.map_ffn = c->fmaps + 6 * nL + 2;
-  a.map_kv = c->fmaps + 6 * nL + 3; a.map_xkv = c->fmaps + 6 * nL + 4;
+  a.map_kv = c->fmaps + 6 * nL + 3; a.map_xkv = c->fmaps + 6 * nL + 4; a.map_x = c->fmaps + 6 * nL + 5;
+  a.xs_rows = c->xs_rows;
   a.n_layers = nL; a.d = d.d_model; a.f = d.d_ff; a.heads = c->heads; a.V = d.vocab; a.max_pos = d.max_pos;
   a.max_block = d.max_block; a.n_hist = d.drafter_layers > 0 ? d.n_hist : 0;
   a.H = H; a.req_ids = req; a.block = block; a.block_len = blen;
@@ -426,7 +435,7 @@ int flow_verify(ws_ctx* c, const int32_t* req, int H, const int32_t* block, cons
   a.kv = c->kv; a.kv_layer_bytes = c->kv_layer_bytes; a.ptab = c->ptab; a.ppr = c->ppr;
   a.xkv_slot_rows = c->x_slot_elems / WS_DH; a.xkv_layer_rows = c->x_layer_elems / WS_DH;
   a.max_frames = d.max_frames;
-  a.hist = c->hist; a.xpart = c->xpart; a.max_xchunks = c->max_xchunks; a.fpart = c->f2part;
+  a.hist = c->hist; a.xpart = c->xpart; a.max_groups = c->max_groups; a.fpart = c->f2part;
   a.amax = c->amax; a.logits = logits; a.suppress = c->suppress; a.target = target;
   a.ctr = c->fctr; a.status = c->status;
   CK(launch_flow_verify(a, c->flow_grid, s));

@@ -6,6 +6,8 @@
 #define FLOW_MAX_ROWS 16       // block rows one call may carry (a 16-token MMA tile)
 #define FLOW_CTR_LAYER 512     // dependency counters per decoder layer (ints)
 #define FLOW_CTR_GLOBAL 16     // counters after the per-layer blocks
+#define FLOW_XS_BYTES 46080    // shared-memory staging of residual rows for a layer norm
+#define FLOW_GP 68             // floats per cross-attention group partial (m, l, 64 values, pad)
 
 // Counter offsets inside one layer's block.
 enum FlowCtr {
@@ -43,6 +45,8 @@ struct FlowArgs {
   const void* map_ffn;         // FFN activation [rows, f], 16-row boxes
   const void* map_kv;          // self K/V pool as [rows, 64], 64 x 64 boxes
   const void* map_xkv;         // acoustic K/V slabs as [rows, 64], 64 x 64 boxes
+  const void* map_x;           // fp32 residual [rows, d], boxes of xs_rows whole rows
+  int xs_rows;                 // residual rows one layer-norm staging pass holds
   int n_layers, d, f, heads, V, max_pos, max_block, n_hist;
   int H;                       // block rows of this call (one request)
   const int32_t* req_ids;      // [1]
@@ -67,8 +71,8 @@ struct FlowArgs {
   size_t xkv_slot_rows, xkv_layer_rows;   // rows of map_xkv per request slot / per layer
   int max_frames;
   float* hist;                 // history residuals [slot][max_block][n_hist][d]
-  float* xpart;                // cross-attention partials [16][heads][max_xchunks][66]
-  int max_xchunks;
+  float* xpart;                // cross-attention group partials [heads][max_groups][16][FLOW_GP]
+  int max_groups;              // groups of four 64-frame chunks per head
   float* fpart;                // FC2 partials [d / 16][f / d][16][16]
   unsigned long long* amax;    // [16] argmax keys
   float* logits;               // [H, V] or NULL

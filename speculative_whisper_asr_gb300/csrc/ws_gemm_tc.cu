@@ -666,6 +666,22 @@ bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uin
   return r == CUDA_SUCCESS;
 }
 
+// Row-major fp32 matrix [rows, cols] (cols a multiple of 256) as a 3-D TMA
+// map {256, cols / 256, rows} whose box holds box_rows whole rows, stored
+// row after row in shared memory (no swizzle).  Rows beyond `rows` read as 0.
+bool tc_encode_rows_f32(TcMap* m, const float* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  if (!tc_engine_available() || cols % 256 != 0) return false;
+  cuuint64_t dims[3] = {256, (cuuint64_t)cols / 256, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {256 * 4, (cuuint64_t)cols * 4};
+  cuuint32_t box[3] = {256, (cuuint32_t)(cols / 256), box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(reinterpret_cast<CUtensorMap*>(m), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                        const_cast<float*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Raise the dynamic shared-memory limit of every kernel variant once, before
 // any launch (so no attribute call happens while a stream is being captured).
 cudaError_t tc_init_attributes() {

@@ -327,6 +327,7 @@ struct AttnScratch {
 struct alignas(64) TcMap { unsigned char bytes[128]; };
 bool tc_engine_available();
 bool tc_encode_map(TcMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+bool tc_encode_rows_f32(TcMap* m, const float* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 int tc_pick_bn(int M, int N, int batch);
 // Whether a GEMM of this shape and split-K factor can take its layer-norm
 // input in-kernel (GemmShape::ln_x): one 16-token tile, split K, every CTA's
