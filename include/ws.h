@@ -207,6 +207,31 @@ int ws_draft_synthetic(ws_ctx* ctx, int n_req, const int32_t* req_ids, int32_t* 
                        const int32_t* traj, int tlen, const uint8_t* cmask,
                        const int32_t* ctok, ws_stream stream);
 
+/* Truncated verification and confidence-threshold stopping (Whisper-Flash
+ * Table A5 verifies only the first K' of the K proposals; Alignment Drift
+ * Table 21 stops drafting when confidence falls below a threshold).  Between
+ * ws_draft and ws_verify: decides how many drafted proposals each request
+ * sends to verification and copies the block into the verify layout.
+ *   block      [n, stride_in] int32, the drafted block (column 0 anchor,
+ *              columns 1..K proposals); stride_in >= K + 1
+ *   q_logits   [n, K, V] float draft logits written by ws_draft, or NULL
+ *              when threshold <= 0
+ *   k_verify   0..K proposals at most (K' of Table A5)
+ *   threshold  proposals stop before the first position j whose confidence
+ *              q_j(y_j) -- the drafter's FP32 softmax probability of its
+ *              own token at `temperature` (1 when temperature is 0) -- is
+ *              below it; <= 0: no threshold
+ *   block_out  [n, stride_out] int32 out: columns 0..k_verify of block
+ *              (stride_out >= k_verify + 1: pass stride_out as ws_verify's H)
+ *   block_len  [n] int32 in/out: in, 1 + the proposals the budget allows
+ *              (ws_accept's next_len; 0 = request finished); out,
+ *              1 + the proposals kept (0 stays 0)
+ * The output equals autoregressive greedy output for every k_verify and
+ * threshold (only fewer candidates are checked). */
+int ws_draft_limit(ws_ctx* ctx, int n_req, const int32_t* req_ids, const int32_t* block, int stride_in,
+                   const float* q_logits, int k_verify, float threshold, float temperature,
+                   int32_t* block_out, int stride_out, int32_t* block_len, ws_stream stream);
+
 /* Sample rows of given logits with the drafter's sampler: out[i, r] ~
  * softmax(logits[i, r, :] / T) using Philox counter (slot, round, r+1, 0).
  *   logits [n, rows, V] float; out [n, rows] int32 (row stride `rows`). */

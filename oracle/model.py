@@ -563,6 +563,60 @@ def speculative_greedy(orc: Oracle, req: Request, budget: int, propose) -> Decod
     return res
 
 
+def proposal_confidence(q_logits_row, tok: int, T: float, suppress=None) -> float:
+    """Confidence of a drafted token: its probability under the drafter's own
+    softmax (FP32, Appendix A.4), at temperature T when sampling, T = 1 for
+    greedy proposals."""
+    return float(probs_fp32(q_logits_row, T if T > 0 else 1.0, suppress)[int(tok)])
+
+
+def limit_proposals(cand, q_logits, k_verify: int, threshold: float, T: float, R: int, suppress=None) -> int:
+    """How many of the drafted candidates go to verification: truncated
+    verification keeps only the first k_verify (Whisper-Flash Table A5), a
+    confidence threshold stops drafting before the first position whose
+    confidence is below it (Alignment Drift Table 21), and at most R - 1 are
+    proposed when R output tokens remain (Appendix A.1)."""
+    n = max(0, min(k_verify, len(cand), R - 1))
+    if threshold > 0:
+        for j in range(n):
+            if proposal_confidence(q_logits[j], cand[j], T, suppress) < threshold:
+                return j
+    return n
+
+
+def speculative_greedy_limited(orc: Oracle, req: Request, budget: int, k_verify: int, threshold: float,
+                               conf_log: list | None = None) -> DecodeResult:
+    """Propose / verify / advance with the parallel drafter's greedy proposals,
+    verifying only the first k_verify of them and stopping at the first one
+    below the confidence threshold.  conf_log, when given, receives each
+    round's confidences of the K drafted tokens."""
+    eos = orc.s.eos_id
+    acc, logits = prefill(orc, req, budget)
+    out = list(acc.emitted)
+    res = DecodeResult(out, margins=[top2_margin(logits[-1])])
+    done, anchor = acc.done, acc.next_anchor
+    while not done:
+        R = budget - len(out)
+        q = orc.draft_logits(req, anchor)
+        cand = [argmax_lowest(q[j]) for j in range(orc.s.K)]
+        if conf_log is not None:
+            conf_log.append([proposal_confidence(q[j], cand[j], 0.0) for j in range(orc.s.K)])
+        n_prop = limit_proposals(cand, q, k_verify, threshold, 0.0, R)
+        block = [anchor] + cand[:n_prop]
+        lg = orc.verify(req, block)
+        g = [argmax_lowest(z) for z in lg]
+        acc = accept_greedy(block, n_prop, g, R, eos)
+        res.margins += [top2_margin(lg[i]) for i in range(len(acc.emitted))]
+        req.L += 1 + acc.a
+        out += acc.emitted
+        res.rounds += 1
+        res.accepted.append(acc.a)
+        res.proposed.append(n_prop)
+        res.emitted.append(len(acc.emitted))
+        done, anchor = acc.done, acc.next_anchor
+    return res
+
+
 def drafter_proposer(orc: Oracle):
     """Greedy proposals from the parallel drafter (argmax of each mask row)."""
     def propose(req, anchor, t, n_prop):

@@ -74,6 +74,7 @@ struct ws_ctx {
   float* f2part = nullptr;
   int max_groups = 0;           // cross-attention chunk groups per head
   int xs_rows = 0;              // residual rows per layer-norm staging pass
+  float* conf = nullptr;        // drafted-token confidences [max_batch][K]
   float2* pstat = nullptr;      // acceptance scratch: (max, sum exp) per p / q logits row
   float2* qstat = nullptr;
   std::string err;
@@ -138,7 +139,7 @@ struct Layout {
 struct Plan {
   size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
   size_t acnt;
-  size_t fmaps, flayers, fctr, xpart, f2part, pstat, qstat;
+  size_t fmaps, flayers, fctr, xpart, f2part, pstat, qstat, conf;
   bool flow_shape;
   size_t kv_layer_bytes, total;
   int heads, ppr, n_pages, n_xl, max_split;
@@ -225,6 +226,7 @@ Plan make_plan(const ws_model_desc& d) {
   p.fctr = lay.take(fl * ((size_t)d.n_layers * FLOW_CTR_LAYER + FLOW_CTR_GLOBAL) * 4);
   p.xpart = lay.take(fl * d.n_heads * xgroups * FLOW_MAX_ROWS * FLOW_GP * 4);
   p.f2part = lay.take(fl * (D / 16) * (d.d_ff / std::max(1, d.d_model)) * 256 * 4);
+  p.conf = lay.take((size_t)d.max_batch * d.K * 4);   // drafted-token confidences
   p.pstat = lay.take(M * 8);        // sampling acceptance: softmax statistics per logits row
   p.qstat = lay.take(M * 8);
   p.total = lay.off;
@@ -672,7 +674,7 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   c->amax = (unsigned long long*)(b + p.amax); c->part = (float*)(b + p.part);
   c->as.part = c->part; c->as.counters = (int*)(b + p.acnt); c->as.status = st + 5 * desc->max_batch;
   c->feat = b + p.feat; c->hpre = (float*)(b + p.hpre); c->hh = b + p.hh;
-  c->pstat = (float2*)(b + p.pstat); c->qstat = (float2*)(b + p.qstat);
+  c->pstat = (float2*)(b + p.pstat); c->qstat = (float2*)(b + p.qstat); c->conf = (float*)(b + p.conf);
   c->mrows = desc->max_batch * desc->max_block;
   c->split_ok = c->mrows <= 64;
   if (c->engine == WS_GEMM_TC) {
@@ -807,6 +809,23 @@ int ws_draft_synthetic(ws_ctx* c, int n, const int32_t* req, int32_t* block, con
   if (!block || !traj || !cmask || !ctok || tlen < 1) return fail(c, WS_EINVAL, "null synthetic-draft input");
   CK(launch_draft_synth(n, c->d.K, req, c->L, block, traj, tlen, cmask, ctok, c->d.max_pos, (cudaStream_t)stream,
                         c->cur_pdl));
+  return WS_OK;
+}
+
+int ws_draft_limit(ws_ctx* c, int n, const int32_t* req, const int32_t* block, int stride_in, const float* q_logits,
+                   int k_verify, float threshold, float temperature, int32_t* block_out, int stride_out,
+                   int32_t* block_len, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (!block || !block_out || !block_len) return fail(c, WS_EINVAL, "null block, block_out or block_len");
+  if (k_verify < 0 || k_verify > c->d.K) return fail(c, WS_EINVAL, "k_verify %d outside 0..K (%d)", k_verify, c->d.K);
+  if (stride_in < c->d.K + 1 || stride_out < k_verify + 1)
+    return fail(c, WS_EINVAL, "block strides must hold K+1 (in) and k_verify+1 (out) tokens");
+  if (!(threshold == threshold) || !(temperature >= 0.0f)) return fail(c, WS_EINVAL, "bad threshold or temperature");
+  if (threshold > 0.0f && !q_logits) return fail(c, WS_EINVAL, "a confidence threshold needs q_logits");
+  CK(launch_draft_limit(n, c->d.K, block, stride_in, q_logits, c->d.vocab, temperature > 0.0f ? temperature : 1.0f,
+                        c->suppress, c->conf, k_verify, threshold, block_out, stride_out, block_len,
+                        (cudaStream_t)stream, c->cur_pdl));
   return WS_OK;
 }
 

@@ -398,3 +398,6 @@ cudaError_t launch_draft_synth(int n, int K, const int32_t* req_ids, const int32
                                const int32_t* traj, int tlen, const uint8_t* cmask, const int32_t* ctok,
                                int max_pos, cudaStream_t s, bool pdl);
 cudaError_t launch_get_lengths(int n, const int32_t* req_ids, const int32_t* L, int32_t* out, cudaStream_t s);
+cudaError_t launch_draft_limit(int n, int K, const int32_t* block, int stride_in, const float* q, int V, float T,
+                               const uint32_t* sup, float* conf, int k_verify, float thr, int32_t* out,
+                               int stride_out, int32_t* blen, cudaStream_t s, bool pdl);

@@ -305,6 +305,44 @@ __global__ void __launch_bounds__(SNT) row_stats_kernel(const float* logits, int
   if (threadIdx.x == 0) out[blockIdx.x] = make_float2(st.m, st.S);
 }
 
+// ------------------------------------------------------------------ limited proposals
+// Confidence of drafted token j of request i: its probability under the
+// drafter's softmax at temperature T (1 for greedy proposals), FP32, with the
+// shared token suppression.  One CTA per (j, i).
+__global__ void __launch_bounds__(SNT) draft_conf_kernel(const int32_t* block, int stride, const float* q, int K,
+                                                         int V, float T, const uint32_t* sup, float* conf) {
+  __shared__ float sh[SNT + 8];
+  pdl_wait();
+  const int j = blockIdx.x, i = blockIdx.y;
+  const float* z = q + ((long long)i * K + j) * V;
+  const RowStat st = row_stat(z, V, T, sup, sh);
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    const int y = block[(size_t)i * stride + 1 + j];
+    conf[(size_t)i * K + j] = (y >= 0 && y < V) ? expf(scaled(z, y, T, sup) - st.m) / st.S : 0.0f;
+  }
+}
+
+// Proposals that go to verification: the first min(k_verify, block_len - 1)
+// (truncated verification; block_len - 1 already holds the R - 1 budget
+// cap), cut before the first one whose confidence is below the threshold
+// (conf == NULL: no threshold).  Copies the block to the verify layout.
+__global__ void draft_limit_kernel(int n, const int32_t* block, int stride_in, const float* conf, int K,
+                                   int k_verify, float thr, int32_t* out, int stride_out, int32_t* blen) {
+  pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    const int b_in = blen[i];
+    int np = min(k_verify, max(b_in - 1, 0));
+    if (conf)
+      for (int j = 0; j < np; ++j)
+        if (conf[(size_t)i * K + j] < thr) { np = j; break; }
+    for (int j = 0; j <= k_verify; ++j) out[(size_t)i * stride_out + j] = block[(size_t)i * stride_in + j];
+    blen[i] = b_in > 0 ? 1 + np : 0;
+  }
+  pdl_trigger();
+}
+
 // ------------------------------------------------------------------ acceptance
 // One CTA per request.  Whisper-Flash §3.1 / Appendix A.1 / A.4.
 __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
@@ -522,6 +560,23 @@ cudaError_t launch_reset(int n, const int32_t* req_ids, int32_t* L, int32_t* pen
   reset_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, L, pend_n);
   return cudaGetLastError();
 }
+cudaError_t launch_draft_limit(int n, int K, const int32_t* block, int stride_in, const float* q, int V, float T,
+                               const uint32_t* sup, float* conf, int k_verify, float thr, int32_t* out,
+                               int stride_out, int32_t* blen, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaError_t e = cudaSuccess;
+  if (thr > 0.0f && min(K, k_verify) > 0) {
+    cudaLaunchConfig_t cfg = make_cfg(dim3(min(K, k_verify), n), dim3(SNT), 0, s, pdl, at);
+    ws_count_launches(1);
+    e = cudaLaunchKernelEx(&cfg, draft_conf_kernel, block, stride_in, q, K, V, T, sup, conf);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = make_cfg(dim3((n + 127) / 128), dim3(128), 0, s, pdl, at);
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&cfg, draft_limit_kernel, n, block, stride_in, thr > 0.0f ? (const float*)conf : nullptr,
+                            K, k_verify, thr, out, stride_out, blen);
+}
+
 cudaError_t launch_get_lengths(int n, const int32_t* req_ids, const int32_t* L, int32_t* out, cudaStream_t s) {
   ws_count_launches(1);
   get_lengths_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, L, out);

@@ -124,14 +124,18 @@ class Decoder:
         return B.ws_status(self.ctx, _stream())
 
     # ------------------------------------------------------------------ batch state
-    def new_batch(self, req, budgets, tcap: int | None = None, sampling: bool = False) -> "Batch":
-        return Batch(self, req, budgets, tcap or self.s.max_pos, sampling)
+    def new_batch(self, req, budgets, tcap: int | None = None, sampling: bool = False,
+                  draft_logits: bool = False) -> "Batch":
+        """draft_logits: keep the drafter's logits also for greedy decoding
+        (needed by a confidence threshold)."""
+        return Batch(self, req, budgets, tcap or self.s.max_pos, sampling, draft_logits)
 
 
 class Batch:
     """Device arrays of one decoding batch (request slots `req`)."""
 
-    def __init__(self, dec: Decoder, req: torch.Tensor, budgets, tcap: int, sampling: bool):
+    def __init__(self, dec: Decoder, req: torch.Tensor, budgets, tcap: int, sampling: bool,
+                 draft_logits: bool = False):
         self.dec = dec
         self.req = req
         n = req.numel()
@@ -159,7 +163,9 @@ class Batch:
         self.p_logits = self.q_logits = self.p_logits1 = None
         if sampling:
             self.p_logits = torch.empty(n, K + 1, dec.V, dtype=torch.float32, device=dev)
+        if sampling or draft_logits:
             self.q_logits = torch.empty(n, K, dec.V, dtype=torch.float32, device=dev)
+        self.vblock = torch.zeros(n, K + 1, **i32)      # the block as verified (truncated proposals)
         self.host_done = torch.zeros(1, dtype=torch.int32).pin_memory()
         self.graphs = {}
 
@@ -228,27 +234,41 @@ class Batch:
         B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
 
     def spec_step(self, rnd: int, synthetic=None, temperature: float = 0.0, seed: int = 0, run_drafter=True,
-                  graph: bool = True):
+                  graph: bool = True, k_verify: int | None = None, threshold: float = 0.0):
         """One propose / verify / accept round.  `synthetic` = (traj, cmask, ctok) device tensors.
-        Greedy rounds replay one captured graph (their calls do not depend on the round)."""
+        k_verify / threshold: verify only the first k_verify proposals, stopping
+        before the first one whose drafter confidence is below threshold
+        (ws_draft_limit).  Greedy rounds replay one captured graph per
+        (proposal source, verify length, threshold): their calls do not depend
+        on the round."""
         if graph and temperature <= 0.0:
-            self.replay(("spec", synthetic is not None, run_drafter),
-                        lambda: self._spec_calls(0, synthetic, 0.0, 0, run_drafter))
+            self.replay(("spec", synthetic is not None, run_drafter, k_verify, threshold),
+                        lambda: self._spec_calls(0, synthetic, 0.0, 0, run_drafter, k_verify, threshold))
         else:
-            self._spec_calls(rnd, synthetic, temperature, seed, run_drafter)
+            self._spec_calls(rnd, synthetic, temperature, seed, run_drafter, k_verify, threshold)
 
-    def _spec_calls(self, rnd, synthetic, temperature, seed, run_drafter):
+    def _spec_calls(self, rnd, synthetic, temperature, seed, run_drafter, k_verify=None, threshold=0.0):
         d = self.dec
         sampling = temperature > 0.0
+        K = d.K
+        limited = k_verify is not None and (k_verify < K or threshold > 0.0)
         if run_drafter:
-            d.draft(self.req, self.block, temperature, seed, rnd, self.q_logits if sampling else None)
+            d.draft(self.req, self.block, temperature, seed, rnd,
+                    self.q_logits if (sampling or threshold > 0.0) else None)
         if synthetic is not None:
             traj, cmask, ctok = synthetic
             B.ws_draft_synthetic(d.ctx, self.n, self.req.data_ptr(), self.block.data_ptr(), traj.data_ptr(),
                                  traj.shape[1], cmask.data_ptr(), ctok.data_ptr(), _stream())
-        d.verify(self.req, self.block, self.blen, self.target, self.p_logits if sampling else None)
+        H, vb = K + 1, self.block
+        if limited:
+            H, vb = k_verify + 1, self.vblock
+            B.ws_draft_limit(d.ctx, self.n, self.req.data_ptr(), self.block.data_ptr(), K + 1,
+                             _ptr(self.q_logits) if threshold > 0.0 else 0, k_verify, threshold, temperature,
+                             vb.data_ptr(), H, self.blen.data_ptr(), _stream())
+        B.ws_verify(d.ctx, self.n, self.req.data_ptr(), H, vb.data_ptr(), self.blen.data_ptr(),
+                    self.target.data_ptr(), _ptr(self.p_logits) if sampling else 0, _stream())
         mode = B.WS_ACCEPT_SAMPLE if sampling else B.WS_ACCEPT_GREEDY
-        a = self._args(mode, d.K + 1, self.block, self.blen, self.target, self.block, self.blen,
+        a = self._args(mode, H, vb, self.blen, self.target, self.block, self.blen,
                        self.p_logits, self.q_logits, temperature, seed, rnd)
         B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
 
@@ -273,11 +293,12 @@ def run_ar(dec: Decoder, batch: Batch, max_rounds: int = 100000) -> int:
 
 
 def run_spec(dec: Decoder, batch: Batch, synthetic=None, temperature=0.0, seed=0, max_rounds=100000,
-             run_drafter=True, graph=True) -> int:
+             run_drafter=True, graph=True, k_verify=None, threshold=0.0) -> int:
     batch.prefill(temperature=temperature, seed=seed)
     rounds = 0
     while batch.poll_done() < batch.n and rounds < max_rounds:
-        batch.spec_step(rounds + 1, synthetic, temperature, seed, run_drafter, graph=graph)
+        batch.spec_step(rounds + 1, synthetic, temperature, seed, run_drafter, graph=graph, k_verify=k_verify,
+                        threshold=threshold)
         rounds += 1
     return rounds
 

@@ -542,3 +542,70 @@ def test_first_token_chi_square_montecarlo():
         counts[acc.emitted[0]] += 1
     chi2 = ((counts - n * p) ** 2 / (n * p)).sum()
     assert chi2 < 43.8   # chi-square 99.9% quantile, 19 dof
+
+
+# ---------------------------------------------------------------- truncated verification, confidence stopping
+
+@pytest.fixture(scope="module")
+def small_drafter():
+    s = synth.ModelShape("small-d", 2, 128, 2, 256, vocab=300, max_pos=64, hist_layers=(0, 1), dtype="f32",
+                         eos_id=299, prompt=(290, 291, 292, 293))
+    tw = synth.target_weights(s, 71)
+    dw = synth.drafter_weights(s, 71, tw)
+    orc = M.Oracle(s, tw, dw)
+    A = synth.encoder_states(s, 71, 0, frames=50)
+    return s, orc, A
+
+
+@pytest.mark.parametrize("k_verify,threshold", [(1, 0.0), (2, 0.0), (4, 0.3), (8, 0.0), (8, 0.3), (8, 0.05)])
+def test_limited_speculation_is_exact_and_accounts_tau(small_drafter, k_verify, threshold):
+    """Truncating the verified block (Whisper-Flash Table A5) and stopping at
+    low confidence (Alignment Drift Table 21) keep the output equal to
+    autoregressive greedy decoding; tokens per target call follow
+    tau = 1 + (accepted per round), <= 1 + alpha K' (Table A5's identity)."""
+    s, orc, A = small_drafter
+    budget = 30
+    ar = M.greedy_cached(orc, orc.new_request(A), budget).tokens
+    res = M.speculative_greedy_limited(orc, orc.new_request(A), budget, k_verify, threshold)
+    assert res.tokens == ar
+    assert max(res.proposed) <= k_verify
+    a, prop = sum(res.accepted), sum(res.proposed)
+    emitted_rounds = sum(res.emitted)
+    assert emitted_rounds == res.rounds + a                 # no EOS: each round = accepted + 1
+    tau = emitted_rounds / res.rounds
+    alpha = a / max(prop, 1)
+    assert tau <= 1 + alpha * k_verify + 1e-12
+    if threshold == 0.0 and k_verify == s.K:
+        base = M.speculative_greedy(orc, orc.new_request(A), budget, M.drafter_proposer(orc))
+        assert base.proposed == res.proposed and base.accepted == res.accepted
+
+
+def test_confidence_threshold_one_means_no_proposals(small_drafter):
+    """No probability reaches a threshold above 1: every round verifies the
+    anchor alone, so the loop is autoregressive (one token per target call)."""
+    s, orc, A = small_drafter
+    res = M.speculative_greedy_limited(orc, orc.new_request(A), 12, s.K, 1.01)
+    assert set(res.proposed) == {0}
+    assert res.rounds == 11                                 # the prefill emits the first token
+
+
+def test_proposal_confidence_and_stop_rule_brute_force():
+    """The confidence is the drafter's softmax probability of its token
+    (torch softmax in float64 agrees to fp32 precision); the limit is the
+    first position below the threshold, capped by K' and R - 1."""
+    g = np.random.default_rng(14)
+    q = g.standard_normal((8, 50)) * 3
+    cand = [int(np.argmax(r)) for r in q]
+    conf = [M.proposal_confidence(q[j], cand[j], 0.0) for j in range(8)]
+    ref = torch.softmax(torch.from_numpy(q), dim=-1).numpy()
+    np.testing.assert_allclose(conf, [ref[j, cand[j]] for j in range(8)], rtol=1e-5)
+    for thr in (0.0, 0.2, 0.5, 0.9):
+        for kv in (1, 3, 8):
+            for R in (1, 2, 5, 100):
+                n = 0
+                while n < min(kv, R - 1) and (thr <= 0 or conf[n] >= thr):
+                    n += 1
+                assert M.limit_proposals(cand, q, kv, thr, 0.0, R) == n
+    # sampling: confidence at the drafter's temperature
+    assert abs(M.proposal_confidence(q[0], 3, 0.7) -
+               torch.softmax(torch.from_numpy(q[0] / 0.7), -1)[3].item()) < 1e-6
