@@ -232,6 +232,35 @@ int ws_draft_limit(ws_ctx* ctx, int n_req, const int32_t* req_ids, const int32_t
                    const float* q_logits, int k_verify, float threshold, float temperature,
                    int32_t* block_out, int stride_out, int32_t* block_len, ws_stream stream);
 
+/* Verification-attention readout and windowed drafter cross-attention
+ * (Alignment Drift §5 and App. D.2: the target's audio attention at one
+ * decoder layer, averaged over heads, is read from the existing acoustic
+ * keys after each verify; its peak frame centres a fixed-width window on
+ * the drafter's cross-attention, App. A.2, +-400 ms = +-20 frames).
+ *   layer       target layer whose cross-attention is read (0..n_layers-1),
+ *               or -1 to switch the readout off
+ *   half_width  > 0: every ws_draft restricts the drafter's cross-attention
+ *               of each request to frames max(0, c - half_width) <= f <
+ *               min(F, c + half_width + 1), c the request's current centre
+ *               (every frame until its first readout); 0: unrestricted
+ * With a readout layer set, ws_verify keeps that layer's cross-attention
+ * queries of its block rows (the kernel-per-operation path is used).
+ * Host-only; no device work.  Acceptance is unchanged, so greedy output
+ * stays equal to autoregressive greedy output. */
+int ws_set_readout(ws_ctx* ctx, int layer, int half_width);
+
+/* The readout after ws_accept: for each request, softmax over its valid
+ * frames of q k_f / sqrt(64) per head at the readout layer, averaged over
+ * heads (in head order, fp32), for block row row[i] of the last ws_verify
+ * (the row whose output became the next anchor: ws_accept's n_acc); its
+ * peak frame (lowest on ties) becomes the request's window centre.
+ *   row  [n] int32 (device) */
+int ws_readout(ws_ctx* ctx, int n_req, const int32_t* req_ids, const int32_t* row, ws_stream stream);
+
+/* Copy the current window centres of the listed slots into out [n] int32
+ * (-1: none yet). */
+int ws_get_centers(ws_ctx* ctx, int n_req, const int32_t* req_ids, int32_t* out, ws_stream stream);
+
 /* Sample rows of given logits with the drafter's sampler: out[i, r] ~
  * softmax(logits[i, r, :] / T) using Philox counter (slot, round, r+1, 0).
  *   logits [n, rows, V] float; out [n, rows] int32 (row stride `rows`). */

@@ -145,6 +145,8 @@ class Request:
     sv: list
     hist: np.ndarray    # residual streams at the history layers [max_pos, n_hist, d]
     L: int = 0          # target cache length
+    peaks: list = field(default_factory=list)   # readout: per block row, the head-averaged attention peak frame
+    center: int = -1    # centre of the drafter's cross-attention window (-1: no window yet)
 
 
 class Oracle:
@@ -190,8 +192,21 @@ class Oracle:
                        [np.zeros((P, d)) for _ in range(self.s.n_layers)],
                        np.zeros((P, self.s.n_hist, d)))
 
+    # ---------------------------------------------------- verification-attention readout
+    def attention_peaks(self, qc: np.ndarray, ck: np.ndarray) -> list:
+        """Alignment Drift §5 / App. D.2: the target's audio attention of each
+        query row at one layer, averaged over heads (softmax per head of
+        q k^T / sqrt(d_head) over the valid frames), and its peak frame
+        (lowest frame on ties)."""
+        R, d = qc.shape
+        dh = d // self.H
+        qh = qc.reshape(R, self.H, dh).transpose(1, 0, 2)
+        kh = ck.reshape(ck.shape[0], self.H, dh).transpose(1, 0, 2)
+        p = softmax(np.einsum("hrd,hsd->hrs", qh, kh) / math.sqrt(dh), axis=-1)
+        return [int(np.argmax(row)) for row in p.mean(axis=0)]
+
     # ---------------------------------------------------- target decoder
-    def _layer(self, x, l, q_rows_attend, ck, cv):
+    def _layer(self, x, l, q_rows_attend, ck, cv, readout=None):
         """One pre-LN decoder layer.  `q_rows_attend(q, k, v)` does the
         self-attention (cached or full)."""
         w, p, d = self.t, f"layers.{l}.", self.d
@@ -204,6 +219,8 @@ class Oracle:
         x = x + (o @ w[p + "w_o"].T + w[p + "b_o"])
         h2 = self.rb(layer_norm(x, w[p + "ln2_g"], w[p + "ln2_b"]))
         qc = self.rb(h2 @ w[p + "w_qc"].T + w[p + "b_qc"])
+        if readout is not None:
+            readout.extend(self.attention_peaks(qc, ck))
         oc = self.rb(mha(qc, ck, cv, self.H))
         x = x + (oc @ w[p + "w_oc"].T + w[p + "b_oc"])
         h3 = self.rb(layer_norm(x, w[p + "ln3_g"], w[p + "ln3_b"]))
@@ -237,7 +254,7 @@ class Oracle:
                 hist.append(x.copy())
         return self._head(x), np.stack(hist, axis=1)
 
-    def verify(self, req: Request, block) -> np.ndarray:
+    def verify(self, req: Request, block, readout_layer: int | None = None) -> np.ndarray:
         """One causal target pass over the block [anchor, candidates...] at
         positions L..L+H-1 (Whisper-Flash §3.1).  Writes the block's K/V into
         the cache and its history-layer residuals into req.hist; does not
@@ -255,11 +272,14 @@ class Oracle:
             vis = np.arange(last)[None, :] <= pos[:, None]
             return mha(q, req.sk[l][:last], req.sv[l][:last], self.H, vis)
 
+        peaks = []
         for l in range(self.s.n_layers):
-            x = self._layer(x, l, attend, req.ck[l][:req.frames], req.cv[l][:req.frames])
+            x = self._layer(x, l, attend, req.ck[l][:req.frames], req.cv[l][:req.frames],
+                            peaks if l == readout_layer else None)
             if l in self.s.hist_layers:
                 hist.append(x.copy())
         req.hist[pos] = np.stack(hist, axis=1)
+        req.peaks = peaks
         return self._head(x)
 
     # ---------------------------------------------------- drafter (§3.2, A.2)
@@ -274,7 +294,7 @@ class Oracle:
         feat = self.rb(resid.reshape(n, -1))
         return self.rb(layer_norm(feat @ dr["fuse_w"].T, dr["lnh_g"], dr["lnh_b"]))
 
-    def drafter_layer(self, x, l: int, pos, h_hist, pos_hist, dck, dcv):
+    def drafter_layer(self, x, l: int, pos, h_hist, pos_hist, dck, dcv, window=None):
         """One drafter layer.  Block rows x [R, d] at RoPE positions `pos`;
         history features h_hist [S, d] at positions `pos_hist`.  The block's
         queries attend to [history ; block] in one softmax with no mask
@@ -294,26 +314,36 @@ class Oracle:
         x = x + (o @ dr[p + "w_o"].T + dr[p + "b_o"])
         h2 = self.rb(layer_norm(x, dr[p + "ln2_g"], dr[p + "ln2_b"]))
         qc = self.rb(h2 @ dr[p + "w_qc"].T + dr[p + "b_qc"])
-        oc = self.rb(mha(qc, dck, dcv, self.H))
+        vis = None
+        if window is not None:            # windowed cross-attention: frames lo <= f < hi only
+            f = np.arange(dck.shape[0])
+            vis = np.broadcast_to(((f >= window[0]) & (f < window[1]))[None, :], (qc.shape[0], dck.shape[0]))
+        oc = self.rb(mha(qc, dck, dcv, self.H, vis))
         x = x + (oc @ dr[p + "w_oc"].T + dr[p + "b_oc"])
         h3 = self.rb(layer_norm(x, dr[p + "ln3_g"], dr[p + "ln3_b"]))
         f = self.rb(gelu(h3 @ dr[p + "w_fc1"].T + dr[p + "b_fc1"]))
         return x + (f @ dr[p + "w_fc2"].T + dr[p + "b_fc2"])
 
-    def draft_logits(self, req: Request, anchor: int) -> np.ndarray:
+    def draft_logits(self, req: Request, anchor: int, half_width: int = 0) -> np.ndarray:
         """Drafter forward for the anchor at position t = L: input
         X_t = [Emb(y_t), m, ..., m] (Eq. 2) at RoPE positions t..t+K, history =
         accepted positions < t (never at or beyond the anchor, Appendix A.2).
         Returns the logits of the K mask rows [K, V] (the anchor row's output
-        is not a proposal)."""
+        is not a proposal).  half_width > 0: the drafter's cross-attention sees
+        only the frames within half_width of req.center (Alignment Drift App.
+        A.2, a fixed-width window; ±400 ms is ±20 Whisper frames), clipped to
+        the valid frames."""
         dr, K = self.dr, self.s.K
         t = req.L
         pos = t + np.arange(K + 1)
         x = np.concatenate([self.t["tok_emb"][[anchor]], np.repeat(dr["mask_emb"][None, :], K, 0)])
         h_hist = self.history_features(req.hist[:t])
+        window = None
+        if half_width > 0 and req.center >= 0:
+            window = (max(0, req.center - half_width), min(req.frames, req.center + half_width + 1))
         for l in range(self.s.drafter_layers):
             x = self.drafter_layer(x, l, pos, h_hist, np.arange(t),
-                                   req.dck[l][:req.frames], req.dcv[l][:req.frames])
+                                   req.dck[l][:req.frames], req.dcv[l][:req.frames], window)
         hf = self.rb(layer_norm(x[1:], dr["lnf_g"], dr["lnf_b"]))
         return hf @ self.t["tok_emb"].T
 
@@ -614,6 +644,47 @@ def speculative_greedy_limited(orc: Oracle, req: Request, budget: int, k_verify:
         res.proposed.append(n_prop)
         res.emitted.append(len(acc.emitted))
         done, anchor = acc.done, acc.next_anchor
+    return res
+
+
+def speculative_greedy_windowed(orc: Oracle, req: Request, budget: int, readout_layer: int,
+                                half_width: int) -> DecodeResult:
+    """Verification-attention correction (Alignment Drift §5, App. D.2):
+    every target pass also reads its head-averaged audio attention at
+    `readout_layer`; the peak frame of the row that produced the next anchor
+    centres the drafter's cross-attention window for the next round (the
+    prompt pass sets the first centre).  Proposals are the drafter's greedy
+    tokens; acceptance is unchanged, so the output is greedy decoding's."""
+    K, eos = orc.s.K, orc.s.eos_id
+    prompt = list(orc.s.prompt)
+    logits = orc.verify(req, prompt, readout_layer)
+    g = [argmax_lowest(z) for z in logits]
+    acc = accept_forced(len(prompt) - 1, g, budget, eos)
+    req.center = req.peaks[acc.a]
+    req.L += 1 + acc.a
+    out = list(acc.emitted)
+    res = DecodeResult(out)
+    done, anchor = acc.done, acc.next_anchor
+    centers = [req.center]
+    while not done:
+        R = budget - len(out)
+        n_prop = min(K, R - 1)
+        q = orc.draft_logits(req, anchor, half_width)
+        cand = [argmax_lowest(q[j]) for j in range(n_prop)]
+        block = [anchor] + cand
+        lg = orc.verify(req, block, readout_layer)
+        g = [argmax_lowest(z) for z in lg]
+        acc = accept_greedy(block, n_prop, g, R, eos)
+        req.center = req.peaks[acc.a]
+        centers.append(req.center)
+        req.L += 1 + acc.a
+        out += acc.emitted
+        res.rounds += 1
+        res.accepted.append(acc.a)
+        res.proposed.append(n_prop)
+        res.emitted.append(len(acc.emitted))
+        done, anchor = acc.done, acc.next_anchor
+    res.margins = centers            # the window centre used by each round (prompt's first)
     return res
 
 

@@ -22,7 +22,8 @@ WS_ACCEPT_GREEDY, WS_ACCEPT_SAMPLE, WS_ACCEPT_FORCED = 0, 1, 2
 EXPORTS = ("ws_query_workspace", "ws_load_weights", "ws_reset", "ws_cross_kv", "ws_verify", "ws_draft",
            "ws_accept", "ws_draft_synthetic", "ws_sample", "ws_set_suppress", "ws_get_lengths", "ws_status",
            "ws_gemm_engine", "ws_launch_count", "ws_last_error", "ws_free", "ws_capture_begin",
-           "ws_capture_end", "ws_graph_launch", "ws_graph_free", "ws_argmax_rows_noalloc", "ws_fused_verify", "ws_draft_limit",
+           "ws_capture_end", "ws_graph_launch", "ws_graph_free", "ws_argmax_rows_noalloc", "ws_fused_verify", "ws_draft_limit", "ws_set_readout", "ws_readout",
+           "ws_get_centers",
            "ws_fused_layernorm")
 
 
@@ -80,6 +81,9 @@ def _load():
         "ws_graph_free": (None, [P]),
         "ws_argmax_rows_noalloc": (I, [P, I, I, P, P, S]),
         "ws_draft_limit": (I, [P, I, P, P, I, P, I, C.c_float, C.c_float, P, I, P, S]),
+        "ws_set_readout": (I, [P, I, I]),
+        "ws_readout": (I, [P, I, P, P, S]),
+        "ws_get_centers": (I, [P, I, P, P, S]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -222,6 +226,18 @@ def ws_draft_limit(ctx, n, req, block, stride_in, q_logits, k_verify, threshold,
     return _check(ctx, lib.ws_draft_limit(ctx, n, req, block, stride_in, q_logits or None, k_verify,
                                           float(threshold), float(temperature), block_out, stride_out, block_len,
                                           stream))
+
+
+def ws_set_readout(ctx, layer, half_width):
+    return _check(ctx, lib.ws_set_readout(ctx, layer, half_width))
+
+
+def ws_readout(ctx, n, req, row, stream):
+    return _check(ctx, lib.ws_readout(ctx, n, req, row, stream))
+
+
+def ws_get_centers(ctx, n, req, out, stream):
+    return _check(ctx, lib.ws_get_centers(ctx, n, req, out, stream))
 
 
 def ws_argmax_rows_noalloc(logits, rows, vocab, suppress, out, stream):

@@ -43,6 +43,12 @@ struct ws_ctx {
   int32_t* ptab = nullptr;
   float* rope = nullptr;
   int32_t *L = nullptr, *Fc = nullptr, *Fv = nullptr, *pend_start = nullptr, *pend_n = nullptr, *status = nullptr;
+  int32_t* xcenter = nullptr;   // per slot: centre frame of the drafter's cross-attention window (-1: none)
+  // verification-attention readout (ws_set_readout)
+  int readout_layer = -1, half_width = 0, read_H = 0;
+  void* qread = nullptr;        // the readout layer's cross-attention queries of the last verify [rows, d]
+  float* rsc = nullptr;         // readout scores [max_batch][heads][max_frames]
+  float2* rst = nullptr;        // readout softmax statistics [max_batch][heads]
   float* x = nullptr;
   void *h = nullptr, *q = nullptr, *ao = nullptr, *ffn = nullptr, *kb = nullptr, *vb = nullptr;
   float* hist = nullptr;
@@ -139,7 +145,7 @@ struct Layout {
 struct Plan {
   size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
   size_t acnt;
-  size_t fmaps, flayers, fctr, xpart, f2part, pstat, qstat, conf;
+  size_t fmaps, flayers, fctr, xpart, f2part, pstat, qstat, conf, qread, rsc, rst;
   bool flow_shape;
   size_t kv_layer_bytes, total;
   int heads, ppr, n_pages, n_xl, max_split;
@@ -201,7 +207,7 @@ Plan make_plan(const ws_model_desc& d) {
   p.xkv = lay.take((size_t)d.max_batch * p.n_xl * 2 * D * d.max_frames * es);
   p.ptab = lay.take((size_t)p.n_pages * 4);
   p.rope = lay.take((size_t)d.max_pos * WS_DH * 4);
-  p.state = lay.take((size_t)d.max_batch * 5 * 4 + 256);
+  p.state = lay.take((size_t)d.max_batch * 6 * 4 + 256);
   p.x = lay.take(M * D * 4);
   p.h = lay.take(M * D * es);
   p.q = lay.take(M * D * es);
@@ -227,6 +233,9 @@ Plan make_plan(const ws_model_desc& d) {
   p.xpart = lay.take(fl * d.n_heads * xgroups * FLOW_MAX_ROWS * FLOW_GP * 4);
   p.f2part = lay.take(fl * (D / 16) * (d.d_ff / std::max(1, d.d_model)) * 256 * 4);
   p.conf = lay.take((size_t)d.max_batch * d.K * 4);   // drafted-token confidences
+  p.qread = lay.take(M * D * es);                      // readout: queries of the readout layer
+  p.rsc = lay.take((size_t)d.max_batch * d.n_heads * d.max_frames * 4);
+  p.rst = lay.take((size_t)d.max_batch * d.n_heads * 8);
   p.pstat = lay.take(M * 8);        // sampling acceptance: softmax statistics per logits row
   p.qstat = lay.take(M * 8);
   p.total = lay.off;
@@ -451,8 +460,9 @@ int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* bloc
                 int32_t* target, float* logits, cudaStream_t s) {
   const ws_model_desc& d = c->d;
   const int D = d.d_model, M = n * H;
-  if (sizeof(T) == 2 && c->flow_ok && c->flow_on && n == 1 && H <= FLOW_MAX_ROWS)
+  if (sizeof(T) == 2 && c->flow_ok && c->flow_on && c->readout_layer < 0 && n == 1 && H <= FLOW_MAX_ROWS)
     return flow_verify(c, req, H, block, blen, target, logits, s);
+  c->read_H = H;
   const bool pdl = c->cur_pdl;
   RowMap rm;
   rm.mode = ROW_VERIFY; rm.H = H; rm.max_pos = d.max_pos; rm.req_ids = req; rm.L = c->L;
@@ -471,6 +481,7 @@ int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* bloc
     e = epi0(c, EPI_STORE);
     e.bias = w.b_qc; e.out = c->q; e.ldo = D;
     CK(ln_gemm<T>(c, M, c->x, w.ln2_g, w.ln2_b, w.w_qc, e, s));
+    if (l == c->readout_layer) CK(cudaMemcpyAsync(c->qread, c->q, (size_t)M * D * c->es, cudaMemcpyDeviceToDevice, s));
     CK(launch_cross_attn<T>(n, H, req, c->Fv, (const T*)c->q, xkv_of(c), l, (T*)c->ao, c->heads, c->max_fc, c->as,
                             s, pdl));
     e = epi0(c, EPI_RESID);
@@ -542,8 +553,12 @@ int draft_impl(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temp,
     e = epi0(c, EPI_STORE);
     e.bias = w.b_qc; e.out = c->q; e.ldo = D;
     CK(ln_gemm<T>(c, M, c->x, w.ln2_g, w.ln2_b, w.w_qc, e, s));
-    CK(launch_cross_attn<T>(n, K1, req, c->Fv, (const T*)c->q, xkv_of(c), d.n_layers + l, (T*)c->ao, c->heads,
-                            c->max_fc, c->as, s, pdl));
+    if (c->half_width > 0)
+      CK(launch_window_attn<T>(n, K1, req, c->Fv, c->xcenter, c->half_width, (const T*)c->q, D, xkv_of(c),
+                               d.n_layers + l, (T*)c->ao, s, pdl));
+    else
+      CK(launch_cross_attn<T>(n, K1, req, c->Fv, (const T*)c->q, xkv_of(c), d.n_layers + l, (T*)c->ao, c->heads,
+                              c->max_fc, c->as, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_oc; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ao, c->mrows, w.w_oc, M, e, s));
@@ -669,12 +684,14 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   c->L = st; c->Fc = st + desc->max_batch; c->Fv = st + 2 * desc->max_batch;
   c->pend_start = st + 3 * desc->max_batch; c->pend_n = st + 4 * desc->max_batch;
   c->status = st + 5 * desc->max_batch;
+  c->xcenter = st + 5 * desc->max_batch + 64;     // after the status word (its 256-byte pad)
   c->x = (float*)(b + p.x); c->h = b + p.h; c->q = b + p.q; c->ao = b + p.ao; c->ffn = b + p.ffn;
   c->kb = b + p.kb; c->vb = b + p.vb; c->hist = (float*)(b + p.hist);
   c->amax = (unsigned long long*)(b + p.amax); c->part = (float*)(b + p.part);
   c->as.part = c->part; c->as.counters = (int*)(b + p.acnt); c->as.status = st + 5 * desc->max_batch;
   c->feat = b + p.feat; c->hpre = (float*)(b + p.hpre); c->hh = b + p.hh;
   c->pstat = (float2*)(b + p.pstat); c->qstat = (float2*)(b + p.qstat); c->conf = (float*)(b + p.conf);
+  c->qread = b + p.qread; c->rsc = (float*)(b + p.rsc); c->rst = (float2*)(b + p.rst);
   c->mrows = desc->max_batch * desc->max_block;
   c->split_ok = c->mrows <= 64;
   if (c->engine == WS_GEMM_TC) {
@@ -709,6 +726,7 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   for (int i = 0; i < p.n_pages; ++i) pt[i] = i;   // each slot owns its own pages
   e = cudaMemcpyAsync(c->ptab, pt.data(), pt.size() * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(st, 0, (size_t)desc->max_batch * 5 * 4 + 256, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->xcenter, 0xFF, (size_t)desc->max_batch * 4, s);   // -1: no centre
   if (e == cudaSuccess) e = cudaMemsetAsync(c->hist, 0, (size_t)desc->max_batch * desc->max_block *
                                                         (desc->drafter_layers ? desc->n_hist : 0) * D * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->as.counters, 0, (size_t)desc->max_batch * desc->n_heads * 4, s);
@@ -730,7 +748,7 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
 int ws_reset(ws_ctx* c, int n, const int32_t* req, ws_stream stream) {
   if (int r = check_common(c, n, req, stream)) return r;
   if (n == 0) return WS_OK;
-  CK(launch_reset(n, req, c->L, c->pend_n, (cudaStream_t)stream));
+  CK(launch_reset(n, req, c->L, c->pend_n, c->xcenter, (cudaStream_t)stream));
   return WS_OK;
 }
 
@@ -826,6 +844,39 @@ int ws_draft_limit(ws_ctx* c, int n, const int32_t* req, const int32_t* block, i
   CK(launch_draft_limit(n, c->d.K, block, stride_in, q_logits, c->d.vocab, temperature > 0.0f ? temperature : 1.0f,
                         c->suppress, c->conf, k_verify, threshold, block_out, stride_out, block_len,
                         (cudaStream_t)stream, c->cur_pdl));
+  return WS_OK;
+}
+
+int ws_set_readout(ws_ctx* c, int layer, int half_width) {
+  if (!c) return fail(nullptr, WS_EINVAL, "null context");
+  if (layer < -1 || layer >= c->d.n_layers) return fail(c, WS_EINVAL, "readout layer %d outside -1..n_layers-1", layer);
+  if (half_width < 0) return fail(c, WS_EINVAL, "half_width must be >= 0");
+  if (half_width > 0 && c->d.drafter_layers == 0) return fail(c, WS_EUNSUPPORTED, "context has no drafter");
+  c->readout_layer = layer;
+  c->half_width = half_width;
+  return WS_OK;
+}
+
+int ws_readout(ws_ctx* c, int n, const int32_t* req, const int32_t* row, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (!row) return fail(c, WS_EINVAL, "null row");
+  if (c->readout_layer < 0 || c->read_H < 1) return fail(c, WS_EINVAL, "no readout layer set, or no verify since");
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (c->d.dtype == WS_BF16)
+    CK(launch_readout<bf16>(n, c->read_H, req, row, (const bf16*)c->qread, c->d.d_model, xkv_of(c), c->readout_layer,
+                            c->Fv, c->d.max_frames, c->rsc, c->rst, c->xcenter, s, c->cur_pdl));
+  else
+    CK(launch_readout<float>(n, c->read_H, req, row, (const float*)c->qread, c->d.d_model, xkv_of(c),
+                             c->readout_layer, c->Fv, c->d.max_frames, c->rsc, c->rst, c->xcenter, s, c->cur_pdl));
+  return WS_OK;
+}
+
+int ws_get_centers(ws_ctx* c, int n, const int32_t* req, int32_t* out, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (!out) return fail(c, WS_EINVAL, "null output");
+  CK(launch_get_lengths(n, req, c->xcenter, out, (cudaStream_t)stream));
   return WS_OK;
 }
 

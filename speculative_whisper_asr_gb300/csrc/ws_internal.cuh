@@ -377,7 +377,15 @@ cudaError_t attn_init_attributes();
 cudaError_t launch_rope_table(float* tab, int max_pos, cudaStream_t s);
 cudaError_t launch_set_frames(int n, const int32_t* req_ids, const int32_t* cu, const int32_t* valid,
                               int max_frames, int32_t* Fc, int32_t* Fv, int32_t* status, cudaStream_t s);
-cudaError_t launch_reset(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n, cudaStream_t s);
+cudaError_t launch_reset(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n, int32_t* xcenter,
+                         cudaStream_t s);
+template <typename T>
+cudaError_t launch_readout(int n, int H, const int32_t* req_ids, const int32_t* row, const T* q, int d, const XKV& x,
+                           int layer, const int32_t* Fv, int max_frames, float* sc, float2* st, int32_t* xcenter,
+                           cudaStream_t s, bool pdl);
+template <typename T>
+cudaError_t launch_window_attn(int n, int H, const int32_t* req_ids, const int32_t* Fv, const int32_t* xcenter, int w,
+                               const T* Q, int d, const XKV& x, int layer, T* O, cudaStream_t s, bool pdl);
 cudaError_t launch_sample_rows(int n, int rows, const int32_t* req_ids, const float* logits, long long row_stride,
                                int V, float T, uint64_t seed, uint64_t rnd, const uint32_t* suppress,
                                int32_t* out, int out_stride, int out_col0, cudaStream_t s, bool pdl);

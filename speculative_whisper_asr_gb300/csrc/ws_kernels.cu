@@ -190,9 +190,9 @@ __global__ void set_frames_kernel(int n, const int32_t* req_ids, const int32_t* 
   Fv[req_ids[i]] = v;
 }
 
-__global__ void reset_kernel(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n) {
+__global__ void reset_kernel(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n, int32_t* xcenter) {
   int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) { L[req_ids[i]] = 0; pend_n[req_ids[i]] = 0; }
+  if (i < n) { L[req_ids[i]] = 0; pend_n[req_ids[i]] = 0; xcenter[req_ids[i]] = -1; }
 }
 
 __global__ void get_lengths_kernel(int n, const int32_t* req_ids, const int32_t* L, int32_t* out) {
@@ -341,6 +341,169 @@ __global__ void draft_limit_kernel(int n, const int32_t* block, int stride_in, c
     blen[i] = b_in > 0 ? 1 + np : 0;
   }
   pdl_trigger();
+}
+
+// ------------------------------------------------------------------ verification-attention readout
+// Alignment Drift §5 / App. D.2: the target's audio attention at one layer,
+// averaged over heads, of the block row that produced the next anchor; its
+// peak frame centres the drafter's cross-attention window.
+// Pass 1, one CTA per (head, request): scores s(f) = q . k_f / sqrt(64) over
+// the valid frames (fp32), their max and sum of exp(s - max).
+template <typename T>
+__global__ void __launch_bounds__(SNT) readout_scores_kernel(int H, const int32_t* req_ids, const int32_t* row,
+                                                             const T* q, int d, XKV x, int layer, const int32_t* Fv,
+                                                             int max_frames, float* sc, float2* st) {
+  __shared__ float sh[SNT + 8];
+  __shared__ float qs[WS_DH];
+  pdl_wait();
+  const int h = blockIdx.x, i = blockIdx.y, heads = gridDim.x;
+  const int slot = req_ids[i], F = Fv[slot];
+  const int r = min(max(row[i], 0), H - 1);
+  if (threadIdx.x < WS_DH) qs[threadIdx.x] = to_f<T>(q[((size_t)i * H + r) * d + h * WS_DH + threadIdx.x]);
+  __syncthreads();
+  const T* kb = xkv_ptr<T>(x, slot, layer, 0, h, 0);
+  float* out = sc + ((size_t)i * heads + h) * max_frames;
+  float m = -INFINITY;
+  for (int f = threadIdx.x; f < F; f += SNT) {
+    const T* kr = kb + (size_t)f * WS_DH;
+    float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll 4
+    for (int e = 0; e < WS_DH; e += 4) {
+      c0 = fmaf(qs[e], to_f<T>(kr[e]), c0);
+      c1 = fmaf(qs[e + 1], to_f<T>(kr[e + 1]), c1);
+      c2 = fmaf(qs[e + 2], to_f<T>(kr[e + 2]), c2);
+      c3 = fmaf(qs[e + 3], to_f<T>(kr[e + 3]), c3);
+    }
+    const float v = ((c0 + c1) + (c2 + c3)) * 0.125f;
+    out[f] = v;
+    m = fmaxf(m, v);
+  }
+  m = block_max<SNT>(m, sh);
+  float S = 0.f;
+  for (int f = threadIdx.x; f < F; f += SNT) S += expf(out[f] - m);
+  S = block_sum<SNT>(S, sh);
+  pdl_trigger();
+  if (threadIdx.x == 0) st[(size_t)i * heads + h] = make_float2(m, S);
+}
+
+// Pass 2, one CTA per request: mean over heads (in head order) of the
+// softmax probabilities, argmax over frames (lowest frame on ties).
+__global__ void __launch_bounds__(SNT) readout_peak_kernel(int heads, const int32_t* req_ids, const int32_t* Fv,
+                                                           int max_frames, const float* sc, const float2* st,
+                                                           int32_t* xcenter) {
+  __shared__ unsigned long long best[SNT / 32];
+  pdl_wait();
+  const int i = blockIdx.x, slot = req_ids[i], F = Fv[slot];
+  unsigned long long key = 0ull;
+  for (int f = threadIdx.x; f < F; f += SNT) {
+    float a = 0.f;
+    for (int h = 0; h < heads; ++h) {
+      const float2 ms = st[(size_t)i * heads + h];
+      a += expf(sc[((size_t)i * heads + h) * max_frames + f] - ms.x) / ms.y;
+    }
+    const unsigned long long k = argmax_key(a / (float)heads, f);
+    key = k > key ? k : key;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+    key = other > key ? other : key;
+  }
+  if ((threadIdx.x & 31) == 0) best[threadIdx.x >> 5] = key;
+  __syncthreads();
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < SNT / 32; ++w) key = best[w] > key ? best[w] : key;
+    xcenter[slot] = F > 0 ? argmax_key_id(key) : -1;
+  }
+}
+
+// Windowed cross-attention of the drafter (Alignment Drift App. A.2: a
+// fixed-width mask around a centre frame): rows of request i attend to
+// frames max(0, c - w) <= f < min(F, c + w + 1), c = xcenter[slot] (no
+// centre yet: every valid frame).  One CTA per (request, head), one warp
+// per row; keys in chunks of 64 staged as fp32 in shared memory, online
+// softmax in fp32.
+template <typename T>
+__global__ void __launch_bounds__(128) window_attn_kernel(int H, const int32_t* req_ids, const int32_t* Fv,
+                                                          const int32_t* xcenter, int w, const T* Q, int d, XKV x,
+                                                          int layer, T* O) {
+  __shared__ float Ks[WS_XCHUNK][WS_DH + 1];
+  __shared__ float Vs[WS_XCHUNK][WS_DH];
+  __shared__ float pw[4][WS_XCHUNK];
+  __shared__ float qsh[4][WS_DH];
+  pdl_wait();
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = req_ids[i], F = Fv[slot], c = xcenter[slot];
+  const int lo = c >= 0 ? max(0, c - w) : 0, hi = c >= 0 ? min(F, c + w + 1) : F;
+  const T* kb = xkv_ptr<T>(x, slot, layer, 0, h, 0);
+  const T* vb = xkv_ptr<T>(x, slot, layer, 1, h, 0);
+  // per row: q (2 dims per lane), running max, sum and weighted values
+  float qv[4][2], m[4], l[4], a0[4], a1[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = warp + 4 * j;
+    m[j] = -INFINITY; l[j] = 0.f; a0[j] = 0.f; a1[j] = 0.f;
+    qv[j][0] = qv[j][1] = 0.f;
+    if (r < H) {
+      qv[j][0] = to_f<T>(Q[((size_t)i * H + r) * d + h * WS_DH + 2 * lane]);
+      qv[j][1] = to_f<T>(Q[((size_t)i * H + r) * d + h * WS_DH + 2 * lane + 1]);
+    }
+  }
+  for (int k0 = lo; k0 < hi; k0 += WS_XCHUNK) {
+    const int nk = min(WS_XCHUNK, hi - k0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < nk * WS_DH; e += 128) {
+      const int kk = e / WS_DH, dd = e - kk * WS_DH;
+      Ks[kk][dd] = to_f<T>(kb[(size_t)(k0 + kk) * WS_DH + dd]);
+      Vs[kk][dd] = to_f<T>(vb[(size_t)(k0 + kk) * WS_DH + dd]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = warp + 4 * j;
+      if (r >= H) continue;
+      // scores: lane handles keys lane and lane + 32 (the row's query in shared memory)
+      qsh[warp][2 * lane] = qv[j][0];
+      qsh[warp][2 * lane + 1] = qv[j][1];
+      __syncwarp();
+      float s[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int kk = lane + 32 * t;
+        float acc = 0.f;
+        if (kk < nk)
+          for (int dd = 0; dd < WS_DH; ++dd) acc = fmaf(qsh[warp][dd], Ks[kk][dd], acc);
+        s[t] = kk < nk ? acc * 0.125f : -INFINITY;
+      }
+      const float mn = fmaxf(m[j], warp_max(fmaxf(s[0], s[1])));
+      const float p0 = s[0] > -INFINITY ? expf(s[0] - mn) : 0.f, p1 = s[1] > -INFINITY ? expf(s[1] - mn) : 0.f;
+      const float corr = m[j] > -INFINITY ? expf(m[j] - mn) : 0.f;
+      l[j] = l[j] * corr + warp_sum(p0 + p1);
+      pw[warp][lane] = p0;
+      pw[warp][lane + 32] = p1;
+      __syncwarp();
+      float b0 = 0.f, b1 = 0.f;
+      for (int kk = 0; kk < nk; ++kk) {
+        b0 = fmaf(pw[warp][kk], Vs[kk][2 * lane], b0);
+        b1 = fmaf(pw[warp][kk], Vs[kk][2 * lane + 1], b1);
+      }
+      __syncwarp();
+      a0[j] = a0[j] * corr + b0;
+      a1[j] = a1[j] * corr + b1;
+      m[j] = mn;
+    }
+  }
+  pdl_trigger();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = warp + 4 * j;
+    if (r >= H) continue;
+    const float inv = l[j] > 0.f ? 1.f / l[j] : 0.f;
+    O[((size_t)i * H + r) * d + h * WS_DH + 2 * lane] = from_f<T>(a0[j] * inv);
+    O[((size_t)i * H + r) * d + h * WS_DH + 2 * lane + 1] = from_f<T>(a1[j] * inv);
+  }
 }
 
 // ------------------------------------------------------------------ acceptance
@@ -555,11 +718,45 @@ cudaError_t launch_set_frames(int n, const int32_t* req_ids, const int32_t* cu, 
   set_frames_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, cu, valid, max_frames, Fc, Fv, status);
   return cudaGetLastError();
 }
-cudaError_t launch_reset(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n, cudaStream_t s) {
+cudaError_t launch_reset(int n, const int32_t* req_ids, int32_t* L, int32_t* pend_n, int32_t* xcenter,
+                         cudaStream_t s) {
   ws_count_launches(1);
-  reset_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, L, pend_n);
+  reset_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, req_ids, L, pend_n, xcenter);
   return cudaGetLastError();
 }
+template <typename T>
+cudaError_t launch_readout(int n, int H, const int32_t* req_ids, const int32_t* row, const T* q, int d, const XKV& x,
+                           int layer, const int32_t* Fv, int max_frames, float* sc, float2* st, int32_t* xcenter,
+                           cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  const int heads = d / WS_DH;
+  cudaLaunchConfig_t cfg = make_cfg(dim3(heads, n), dim3(SNT), 0, s, pdl, at);
+  ws_count_launches(2);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, readout_scores_kernel<T>, H, req_ids, row, q, d, x, layer, Fv, max_frames,
+                                     sc, st);
+  if (e != cudaSuccess) return e;
+  cfg = make_cfg(dim3(n), dim3(SNT), 0, s, pdl, at);
+  return cudaLaunchKernelEx(&cfg, readout_peak_kernel, heads, req_ids, Fv, max_frames, (const float*)sc,
+                            (const float2*)st, xcenter);
+}
+template cudaError_t launch_readout<float>(int, int, const int32_t*, const int32_t*, const float*, int, const XKV&,
+                                           int, const int32_t*, int, float*, float2*, int32_t*, cudaStream_t, bool);
+template cudaError_t launch_readout<bf16>(int, int, const int32_t*, const int32_t*, const bf16*, int, const XKV&, int,
+                                          const int32_t*, int, float*, float2*, int32_t*, cudaStream_t, bool);
+
+template <typename T>
+cudaError_t launch_window_attn(int n, int H, const int32_t* req_ids, const int32_t* Fv, const int32_t* xcenter, int w,
+                               const T* Q, int d, const XKV& x, int layer, T* O, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(n, d / WS_DH), dim3(128), 0, s, pdl, at);
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&cfg, window_attn_kernel<T>, H, req_ids, Fv, xcenter, w, Q, d, x, layer, O);
+}
+template cudaError_t launch_window_attn<float>(int, int, const int32_t*, const int32_t*, const int32_t*, int,
+                                               const float*, int, const XKV&, int, float*, cudaStream_t, bool);
+template cudaError_t launch_window_attn<bf16>(int, int, const int32_t*, const int32_t*, const int32_t*, int,
+                                              const bf16*, int, const XKV&, int, bf16*, cudaStream_t, bool);
+
 cudaError_t launch_draft_limit(int n, int K, const int32_t* block, int stride_in, const float* q, int V, float T,
                                const uint32_t* sup, float* conf, int k_verify, float thr, int32_t* out,
                                int stride_out, int32_t* blen, cudaStream_t s, bool pdl) {

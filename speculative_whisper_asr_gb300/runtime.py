@@ -52,6 +52,7 @@ class Decoder:
         self.V = shape.vocab
         self.dtype = B.WS_BF16 if shape.dtype == "bf16" else B.WS_F32
         self.tdtype = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+        self.readout = False
         dl = shape.drafter_layers if drafter is not None else 0
         self.max_block = max_block or max(shape.K + 1, len(shape.prompt))
         self.desc = B.make_desc(shape.n_layers, shape.d_model, shape.n_heads, shape.d_ff, shape.vocab,
@@ -122,6 +123,17 @@ class Decoder:
 
     def status(self) -> int:
         return B.ws_status(self.ctx, _stream())
+
+    def set_readout(self, layer: int, half_width: int):
+        """Verification-attention readout at `layer` centring a +-half_width
+        frame window on the drafter's cross-attention (layer -1: off)."""
+        B.ws_set_readout(self.ctx, layer, half_width)
+        self.readout = layer >= 0
+
+    def centers(self, req) -> np.ndarray:
+        out = torch.empty(req.numel(), dtype=torch.int32, device=self.dev)
+        B.ws_get_centers(self.ctx, req.numel(), req.data_ptr(), out.data_ptr(), _stream())
+        return out.cpu().numpy()
 
     # ------------------------------------------------------------------ batch state
     def new_batch(self, req, budgets, tcap: int | None = None, sampling: bool = False,
@@ -212,6 +224,8 @@ class Batch:
                        self.blen, self.p_logits if sampled else None, None, temperature if sampled else 0.0,
                        seed, 0)
         B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
+        if d.readout and not ar:
+            B.ws_readout(d.ctx, self.n, self.req.data_ptr(), self.n_acc.data_ptr(), _stream())
 
     def ar_step(self, graph: bool = True):
         d = self.dec
@@ -271,6 +285,8 @@ class Batch:
         a = self._args(mode, H, vb, self.blen, self.target, self.block, self.blen,
                        self.p_logits, self.q_logits, temperature, seed, rnd)
         B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
+        if d.readout:              # the row that produced the next anchor centres the next draft window
+            B.ws_readout(d.ctx, self.n, self.req.data_ptr(), self.n_acc.data_ptr(), _stream())
 
     def poll_done(self) -> int:
         self.host_done.copy_(self.n_done, non_blocking=True)

@@ -609,3 +609,50 @@ def test_proposal_confidence_and_stop_rule_brute_force():
     # sampling: confidence at the drafter's temperature
     assert abs(M.proposal_confidence(q[0], 3, 0.7) -
                torch.softmax(torch.from_numpy(q[0] / 0.7), -1)[3].item()) < 1e-6
+
+
+# ---------------------------------------------------------------- verification-attention readout, windowed drafter
+
+def test_attention_peaks_match_torch_head_averaged_weights():
+    """The readout is the argmax over frames of torch's head-averaged
+    multi-head attention weights (identity projections)."""
+    g = np.random.default_rng(21)
+    d, heads, R, F_ = 128, 2, 5, 37
+    q, k = g.standard_normal((R, d)), g.standard_normal((F_, d))
+    orc = M.Oracle(SMALL, synth.target_weights(SMALL, 11), None)
+    got = orc.attention_peaks(q, k)
+    eye = torch.eye(d, dtype=torch.float64)
+    _, w = F.multi_head_attention_forward(
+        torch.from_numpy(q)[:, None], torch.from_numpy(k)[:, None], torch.from_numpy(k)[:, None], d, heads,
+        in_proj_weight=torch.cat([eye, eye, eye]), in_proj_bias=None, bias_k=None, bias_v=None,
+        add_zero_attn=False, dropout_p=0.0, out_proj_weight=eye, out_proj_bias=None, need_weights=True,
+        average_attn_weights=True)
+    assert got == [int(i) for i in w[0].argmax(dim=-1)]
+
+
+def test_windowed_drafter_equals_drafter_on_window_frames(small):
+    """The windowed drafter cross-attention equals the torch drafter given only
+    the window's encoder frames; a window covering every frame is the
+    unrestricted drafter."""
+    orc, tw, dw, A = small
+    req = orc.new_request(A)
+    t = 5
+    req.hist[:t] = np.random.default_rng(22).standard_normal((t, SMALL.n_hist, SMALL.d_model))
+    req.L = t
+    req.center = 31
+    got = orc.draft_logits(req, 77, half_width=6)
+    ref = _torch_drafter_logits(SMALL, tw, dw, req.hist[:t], A[25:38], 77, t)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-9)
+    req.center = 2                                       # clipped at frame 0
+    np.testing.assert_allclose(orc.draft_logits(req, 77, half_width=6),
+                               _torch_drafter_logits(SMALL, tw, dw, req.hist[:t], A[0:9], 77, t), atol=1e-9)
+    req.center = 30
+    np.testing.assert_array_equal(orc.draft_logits(req, 77, half_width=1000), orc.draft_logits(req, 77))
+
+
+def test_windowed_speculation_is_exact(small_drafter):
+    s, orc, A = small_drafter
+    ar = M.greedy_cached(orc, orc.new_request(A), 20).tokens
+    res = M.speculative_greedy_windowed(orc, orc.new_request(A), 20, 1, 5)
+    assert res.tokens == ar
+    assert all(0 <= c < 50 for c in res.margins)
