@@ -153,15 +153,15 @@ int ws_draft(ws_ctx* ctx, int n_req, const int32_t* req_ids, int32_t* block,
              float temperature, uint64_t seed, uint64_t round, float* q_logits,
              ws_stream stream);
 
-enum { WS_ACCEPT_GREEDY = 0, WS_ACCEPT_SAMPLE = 1, WS_ACCEPT_FORCED = 2 };
+enum { WS_ACCEPT_GREEDY = 0, WS_ACCEPT_SAMPLE = 1, WS_ACCEPT_FORCED = 2, WS_ACCEPT_TREE = 3 };
 
 /* Inputs and outputs of ws_accept (all device int32 unless noted). */
 typedef struct {
   int32_t mode;              /* WS_ACCEPT_* */
-  int32_t H;                 /* row stride of block / target / p_logits */
+  int32_t H;                 /* row stride of block / target / p_logits (TREE: the tree's rows) */
   const int32_t* block;      /* [n, H] the verified block */
   const int32_t* block_len;  /* [n] 1 + proposals; 0 = idle */
-  const int32_t* target;     /* [n, H] target argmax per row (GREEDY, FORCED) */
+  const int32_t* target;     /* [n, H] target argmax per row (GREEDY, FORCED, TREE) */
   const float* p_logits;     /* [n, H, V] target logits (SAMPLE) */
   const float* q_logits;     /* [n, K, V] draft logits (SAMPLE) */
   float temperature;         /* SAMPLE */
@@ -192,6 +192,15 @@ typedef struct {
  *   suppression as the drafter.
  * FORCED: all block tokens are given (prompt prefill); emits the argmax of
  *   the last row.
+ * TREE: the block is the candidate tree of ws_set_tree, verified by
+ *   ws_verify_tree (Alignment Drift App. E.3).  From the root, step to the
+ *   lowest-numbered child row whose token equals the target's argmax at the
+ *   current row, at most R - 1 times; emit the path's tokens plus the
+ *   target's token at its last row (none after an accepted EOS).  The
+ *   path's self keys/values (every target layer), history rows and readout
+ *   queries then move from their tree rows to block rows 1..a, so the cache
+ *   holds the accepted tokens at positions L+1..L+a as after a linear
+ *   acceptance.
  * Then L <- L + 1 + a (the old anchor plus the accepted candidates), R -= n_emit,
  * done when EOS was emitted or R == 0. */
 int ws_accept(ws_ctx* ctx, int n_req, const int32_t* req_ids,
@@ -231,6 +240,43 @@ int ws_draft_synthetic(ws_ctx* ctx, int n_req, const int32_t* req_ids, int32_t* 
 int ws_draft_limit(ws_ctx* ctx, int n_req, const int32_t* req_ids, const int32_t* block, int stride_in,
                    const float* q_logits, int k_verify, float threshold, float temperature,
                    int32_t* block_out, int stride_out, int32_t* block_len, ws_stream stream);
+
+/* Candidate trees (Alignment Drift App. E.3: the drafter's ranked tokens
+ * fill a fixed tree, the target verifies every node in one pass under a
+ * tree attention mask, and the longest root path that matches the
+ * target's argmax is accepted; a one-branch tree is the linear block).
+ *   n_nodes  rows of the tree, the root (the anchor) included, 1..max_block
+ *            (at most 16); 0 removes the tree
+ *   parent   [n_nodes] host int32: parent[0] = -1, 0 <= parent[j] < j
+ *   rank     [n_nodes] host int32: row j at depth k takes the rank[j]-th most
+ *            likely token of the drafter's mask row k (0 = its argmax;
+ *            equal logits rank the lower id first), 0..15; rank[0] = 0
+ * Depths must not exceed K when the context has a drafter.  Host-only; the
+ * tree is read when ws_tree_tokens / ws_verify_tree / ws_accept(TREE) are
+ * called (a captured graph keeps the tree it was captured with). */
+int ws_set_tree(ws_ctx* ctx, int n_nodes, const int32_t* parent, const int32_t* rank);
+
+/* Fill the tree's tokens from the drafter's logits.
+ *   block      [n, stride_in] int32 (device): column 0 = the anchor
+ *   q_logits   [n, K, V] float (device): ws_draft's logits (suppressed ids
+ *              are already -inf there)
+ *   block_out  [n, stride_out] int32 out, stride_out >= n_nodes: column 0
+ *              the anchor, column j the token of tree row j
+ *   block_len  [n] int32 in/out: in 0 = request finished (stays 0); out
+ *              min(n_nodes, max_pos - L), the tree's first rows that fit
+ *              the cache (a prefix of rows is a tree) */
+int ws_tree_tokens(ws_ctx* ctx, int n_req, const int32_t* req_ids, const int32_t* block, int stride_in,
+                   const float* q_logits, int32_t* block_out, int stride_out, int32_t* block_len,
+                   ws_stream stream);
+
+/* Tree verification: ws_verify with H = n_nodes of the tree, where row j is
+ * embedded at position L + depth(j) and attends to the cache positions
+ * before L and to its ancestors' rows (itself included); row j's keys and
+ * values go to cache slot L + j until ws_accept(TREE) commits the path.
+ * Arguments as for ws_verify. */
+int ws_verify_tree(ws_ctx* ctx, int n_req, const int32_t* req_ids, int H,
+                   const int32_t* block, const int32_t* block_len, int32_t* target,
+                   float* logits, ws_stream stream);
 
 /* Verification-attention readout and windowed drafter cross-attention
  * (Alignment Drift §5 and App. D.2: the target's audio attention at one

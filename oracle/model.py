@@ -282,6 +282,51 @@ class Oracle:
         req.peaks = peaks
         return self._head(x)
 
+    # ---------------------------------------------------- tree verification (Alignment Drift App. E.3)
+    def verify_tree(self, req: Request, tokens, parent) -> np.ndarray:
+        """One target pass over a candidate tree: node j (0 = the anchor, the
+        root; parent[j] < j) sits at position L + depth(j) and attends to the
+        cache positions before L and to its own ancestors (itself included) --
+        a tree attention mask.  Node j's keys and values are stored at cache
+        slot L + j until acceptance commits a path.  Returns logits [N, V]."""
+        N = len(tokens)
+        depth = [0] * N
+        anc = [[j] for j in range(N)]
+        for j in range(1, N):
+            depth[j] = depth[parent[j]] + 1
+            anc[j] = anc[parent[j]] + [j]
+        L = req.L
+        assert L + N <= self.s.max_pos, "tree beyond the decoder context"
+        x = self._embed(tokens, L + np.asarray(depth))
+        vis = np.zeros((N, L + N), dtype=bool)
+        vis[:, :L] = True
+        for j in range(N):
+            vis[j, [L + m for m in anc[j]]] = True
+        slots = L + np.arange(N)
+
+        def attend(l, q, k, v):
+            req.sk[l][slots] = k
+            req.sv[l][slots] = v
+            return mha(q, req.sk[l][:L + N], req.sv[l][:L + N], self.H, vis)
+
+        hist = []
+        for l in range(self.s.n_layers):
+            x = self._layer(x, l, attend, req.ck[l][:req.frames], req.cv[l][:req.frames])
+            if l in self.s.hist_layers:
+                hist.append(x.copy())
+        req.hist[slots] = np.stack(hist, axis=1)
+        return self._head(x)
+
+    def commit_path(self, req: Request, path) -> None:
+        """Move the accepted path's keys, values and history rows from their
+        node slots L + path[j] to positions L + j."""
+        L = req.L
+        for j, node in enumerate(path):
+            for l in range(self.s.n_layers):
+                req.sk[l][L + j] = req.sk[l][L + node]
+                req.sv[l][L + j] = req.sv[l][L + node]
+            req.hist[L + j] = req.hist[L + node]
+
     # ---------------------------------------------------- drafter (§3.2, A.2)
     def history_features(self, resid: np.ndarray) -> np.ndarray:
         """History memory H_<t: the residual streams of the history layers,
@@ -375,6 +420,78 @@ def accept_greedy(block, n_prop: int, g, budget: int, eos: int) -> Accepted:
             return Accepted(a, out, int(block[j]), True)
     out.append(int(g[a]))
     return Accepted(a, out, int(g[a]), out[-1] == eos or len(out) >= budget)
+
+
+def accept_tree(tokens, parent, g, budget: int, eos: int):
+    """Greedy acceptance on a candidate tree: from the root, move to the
+    child whose token equals the target's argmax at the current node, while
+    one exists (at most budget - 1 candidates); emit the accepted tokens and
+    the target's token at the last accepted node (none after an accepted
+    EOS).  Returns (Accepted, path of node indices from the root)."""
+    children = {}
+    for j in range(1, len(tokens)):
+        children.setdefault(parent[j], []).append(j)
+    cur, path, out = 0, [0], []
+    while len(out) < budget - 1:
+        nxt = [c for c in children.get(cur, []) if int(tokens[c]) == int(g[cur])]
+        if not nxt:
+            break
+        cur = nxt[0]
+        path.append(cur)
+        out.append(int(tokens[cur]))
+        if int(tokens[cur]) == eos:
+            return Accepted(len(out), out, int(tokens[cur]), True), path
+    out.append(int(g[cur]))
+    a = len(path) - 1
+    return Accepted(a, out, int(g[cur]), out[-1] == eos or len(out) >= budget), path
+
+
+def tree_tokens(q_logits, parent, rank, anchor: int) -> list:
+    """Candidate tokens of a fixed tree from the parallel drafter: node j at
+    depth k takes the rank[j]-th most likely token of mask row k (rank 0 =
+    argmax; equal logits rank the lower id first); node 0 is the anchor."""
+    out = [int(anchor)]
+    depth = [0] * len(parent)
+    for j in range(1, len(parent)):
+        depth[j] = depth[parent[j]] + 1
+        row = np.asarray(q_logits[depth[j] - 1])
+        order = np.lexsort((np.arange(len(row)), -row))
+        out.append(int(order[rank[j]]))
+    return out
+
+
+def speculative_greedy_tree(orc: Oracle, req: Request, budget: int, parent, rank, log=None) -> DecodeResult:
+    """Propose / verify / advance with a candidate tree (Alignment Drift
+    App. E.3): the drafter's ranked tokens fill a fixed tree, the target
+    verifies every node in one pass under the tree mask, the longest
+    matching root path is accepted and committed to the cache.  Rows that
+    would pass the decoder's last position are left out (the tree's first
+    rows form a tree).  log: per round (drafter logits, tokens, target
+    logits, path) appended when given."""
+    eos = orc.s.eos_id
+    acc, logits = prefill(orc, req, budget)
+    out = list(acc.emitted)
+    res = DecodeResult(out, margins=[top2_margin(logits[-1])])
+    done, anchor = acc.done, acc.next_anchor
+    while not done:
+        R = budget - len(out)
+        n = min(len(parent), orc.s.max_pos - req.L)
+        q = orc.draft_logits(req, anchor)
+        toks = tree_tokens(q, parent[:n], rank[:n], anchor)
+        lg = orc.verify_tree(req, toks, parent[:n])
+        g = [argmax_lowest(z) for z in lg]
+        acc, path = accept_tree(toks, parent[:n], g, R, eos)
+        if log is not None:
+            log.append((q, toks, lg, path))
+        orc.commit_path(req, path)
+        req.L += 1 + acc.a
+        out += acc.emitted
+        res.rounds += 1
+        res.accepted.append(acc.a)
+        res.proposed.append(len(toks) - 1)
+        res.emitted.append(len(acc.emitted))
+        done, anchor = acc.done, acc.next_anchor
+    return res
 
 
 def accept_forced(n_prop: int, g, budget: int, eos: int) -> Accepted:

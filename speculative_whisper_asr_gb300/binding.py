@@ -17,13 +17,13 @@ LIB_PATH = os.path.join(_HERE, "libws.so")
 WS_OK, WS_EINVAL, WS_ENOSPACE, WS_EPOS, WS_ECUDA, WS_EDEVICE, WS_EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 WS_F32, WS_BF16 = 0, 1
 WS_GEMM_AUTO, WS_GEMM_SIMT, WS_GEMM_TC = 0, 1, 2
-WS_ACCEPT_GREEDY, WS_ACCEPT_SAMPLE, WS_ACCEPT_FORCED = 0, 1, 2
+WS_ACCEPT_GREEDY, WS_ACCEPT_SAMPLE, WS_ACCEPT_FORCED, WS_ACCEPT_TREE = 0, 1, 2, 3
 
 EXPORTS = ("ws_query_workspace", "ws_load_weights", "ws_reset", "ws_cross_kv", "ws_verify", "ws_draft",
            "ws_accept", "ws_draft_synthetic", "ws_sample", "ws_set_suppress", "ws_get_lengths", "ws_status",
            "ws_gemm_engine", "ws_launch_count", "ws_last_error", "ws_free", "ws_capture_begin",
            "ws_capture_end", "ws_graph_launch", "ws_graph_free", "ws_argmax_rows_noalloc", "ws_fused_verify", "ws_draft_limit", "ws_set_readout", "ws_readout",
-           "ws_get_centers",
+           "ws_get_centers", "ws_set_tree", "ws_tree_tokens", "ws_verify_tree",
            "ws_fused_layernorm")
 
 
@@ -84,6 +84,9 @@ def _load():
         "ws_set_readout": (I, [P, I, I]),
         "ws_readout": (I, [P, I, P, P, S]),
         "ws_get_centers": (I, [P, I, P, P, S]),
+        "ws_set_tree": (I, [P, I, P, P]),
+        "ws_tree_tokens": (I, [P, I, P, P, I, P, P, I, P, S]),
+        "ws_verify_tree": (I, [P, I, P, I, P, P, P, P, S]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -238,6 +241,23 @@ def ws_readout(ctx, n, req, row, stream):
 
 def ws_get_centers(ctx, n, req, out, stream):
     return _check(ctx, lib.ws_get_centers(ctx, n, req, out, stream))
+
+
+def ws_set_tree(ctx, parent, rank):
+    """parent, rank: host sequences of the tree's rows (empty = no tree)."""
+    n = len(parent)
+    pa = (C.c_int32 * max(n, 1))(*parent)
+    ra = (C.c_int32 * max(n, 1))(*rank)
+    return _check(ctx, lib.ws_set_tree(ctx, n, pa if n else None, ra if n else None))
+
+
+def ws_tree_tokens(ctx, n, req, block, stride_in, q_logits, block_out, stride_out, block_len, stream):
+    return _check(ctx, lib.ws_tree_tokens(ctx, n, req, block, stride_in, q_logits, block_out, stride_out, block_len,
+                                          stream))
+
+
+def ws_verify_tree(ctx, n, req_ids, H, block, block_len, target, logits, stream):
+    return _check(ctx, lib.ws_verify_tree(ctx, n, req_ids, H, block, block_len, target, logits or None, stream))
 
 
 def ws_argmax_rows_noalloc(logits, rows, vocab, suppress, out, stream):

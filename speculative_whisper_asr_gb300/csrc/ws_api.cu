@@ -49,6 +49,11 @@ struct ws_ctx {
   void* qread = nullptr;        // the readout layer's cross-attention queries of the last verify [rows, d]
   float* rsc = nullptr;         // readout scores [max_batch][heads][max_frames]
   float2* rst = nullptr;        // readout softmax statistics [max_batch][heads]
+  // candidate tree (ws_set_tree): row topology, drafter ranks, acceptance records
+  int tree_n = 0;
+  TreeMask tree = linear_tree();
+  unsigned long long tree_parent4 = 0, tree_rank4 = 0;
+  int32_t* tpath = nullptr;     // [max_batch][WS_TREE_REC]
   float* x = nullptr;
   void *h = nullptr, *q = nullptr, *ao = nullptr, *ffn = nullptr, *kb = nullptr, *vb = nullptr;
   float* hist = nullptr;
@@ -145,7 +150,7 @@ struct Layout {
 struct Plan {
   size_t tblob, dblob, kv, hkv, xkv, ptab, rope, state, x, h, q, ao, ffn, kb, vb, hist, amax, part, feat, hpre, hh;
   size_t acnt;
-  size_t fmaps, flayers, fctr, xpart, f2part, pstat, qstat, conf, qread, rsc, rst;
+  size_t fmaps, flayers, fctr, xpart, f2part, pstat, qstat, conf, qread, rsc, rst, tpath;
   bool flow_shape;
   size_t kv_layer_bytes, total;
   int heads, ppr, n_pages, n_xl, max_split;
@@ -236,6 +241,7 @@ Plan make_plan(const ws_model_desc& d) {
   p.qread = lay.take(M * D * es);                      // readout: queries of the readout layer
   p.rsc = lay.take((size_t)d.max_batch * d.n_heads * d.max_frames * 4);
   p.rst = lay.take((size_t)d.max_batch * d.n_heads * 8);
+  p.tpath = lay.take((size_t)d.max_batch * WS_TREE_REC * 4);   // tree acceptance records
   p.pstat = lay.take(M * 8);        // sampling acceptance: softmax statistics per logits row
   p.qstat = lay.take(M * 8);
   p.total = lay.off;
@@ -457,24 +463,25 @@ int flow_verify(ws_ctx* c, const int32_t* req, int H, const int32_t* block, cons
 // --------------------------------------------------------------------------- verify
 template <typename T>
 int verify_impl(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* block, const int32_t* blen,
-                int32_t* target, float* logits, cudaStream_t s) {
+                int32_t* target, float* logits, cudaStream_t s, const TreeMask* tree = nullptr) {
   const ws_model_desc& d = c->d;
   const int D = d.d_model, M = n * H;
-  if (sizeof(T) == 2 && c->flow_ok && c->flow_on && c->readout_layer < 0 && n == 1 && H <= FLOW_MAX_ROWS)
+  if (sizeof(T) == 2 && c->flow_ok && c->flow_on && c->readout_layer < 0 && !tree && n == 1 && H <= FLOW_MAX_ROWS)
     return flow_verify(c, req, H, block, blen, target, logits, s);
+  const TreeMask tm = tree ? *tree : linear_tree();
   c->read_H = H;
   const bool pdl = c->cur_pdl;
   RowMap rm;
   rm.mode = ROW_VERIFY; rm.H = H; rm.max_pos = d.max_pos; rm.req_ids = req; rm.L = c->L;
   rm.block_len = blen; rm.pend_start = c->pend_start; rm.pend_n = c->pend_n;
-  CK(launch_embed_target<T>(n, H, rm, block, (const T*)c->tok_emb, (const T*)c->pos_emb, D, d.vocab, c->x,
-                            c->pend_start, c->pend_n, c->status, s, pdl));
+  CK(launch_embed_target<T>(n, H, rm, tm.depth4, block, (const T*)c->tok_emb, (const T*)c->pos_emb, D, d.vocab,
+                            c->x, c->pend_start, c->pend_n, c->status, s, pdl));
   for (int l = 0; l < d.n_layers; ++l) {
     const LayerW& w = c->tl[l];
     Epi e = epi0(c, EPI_QKV);
     e.bias = w.b_q; e.bias2 = w.b_v; e.out = c->q; e.rm = rm; e.kv = pool(c, c->kv, l);
     CK(ln_gemm<T>(c, M, c->x, w.ln1_g, w.ln1_b, w.w_qkv, e, s));
-    CK(launch_self_attn<T>(n, H, rm, (const T*)c->q, pool(c, c->kv, l), (T*)c->ao, c->heads, c->as, s, pdl));
+    CK(launch_self_attn<T>(n, H, rm, tm, (const T*)c->q, pool(c, c->kv, l), (T*)c->ao, c->heads, c->as, s, pdl));
     e = epi0(c, EPI_RESID);
     e.bias = w.b_o; e.resid = c->x; e.ldr = D;
     CK(gemm<T>(c, c->ao, c->mrows, w.w_o, M, e, s));
@@ -692,6 +699,7 @@ int ws_load_weights(ws_ctx** out, const ws_model_desc* desc, void* workspace, si
   c->feat = b + p.feat; c->hpre = (float*)(b + p.hpre); c->hh = b + p.hh;
   c->pstat = (float2*)(b + p.pstat); c->qstat = (float2*)(b + p.qstat); c->conf = (float*)(b + p.conf);
   c->qread = b + p.qread; c->rsc = (float*)(b + p.rsc); c->rst = (float2*)(b + p.rst);
+  c->tpath = (int32_t*)(b + p.tpath);
   c->mrows = desc->max_batch * desc->max_block;
   c->split_ok = c->mrows <= 64;
   if (c->engine == WS_GEMM_TC) {
@@ -776,6 +784,19 @@ int ws_verify(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* block,
                                : verify_impl<float>(c, n, req, H, block, blen, target, logits, s);
 }
 
+int ws_verify_tree(ws_ctx* c, int n, const int32_t* req, int H, const int32_t* block, const int32_t* blen,
+                   int32_t* target, float* logits, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (c->tree_n < 1) return fail(c, WS_EINVAL, "no candidate tree set (ws_set_tree)");
+  if (H != c->tree_n) return fail(c, WS_EINVAL, "H %d must equal the tree's row count %d", H, c->tree_n);
+  if (!block || !blen || !target) return fail(c, WS_EINVAL, "null block, block_len or target");
+  cudaStream_t s = (cudaStream_t)stream;
+  const TreeMask tm = c->tree;
+  return c->d.dtype == WS_BF16 ? verify_impl<bf16>(c, n, req, H, block, blen, target, logits, s, &tm)
+                               : verify_impl<float>(c, n, req, H, block, blen, target, logits, s, &tm);
+}
+
 int ws_draft(ws_ctx* c, int n, const int32_t* req, int32_t* block, float temperature, uint64_t seed, uint64_t round,
              float* q_logits, ws_stream stream) {
   if (int r = check_common(c, n, req, stream)) return r;
@@ -793,7 +814,9 @@ int ws_accept(ws_ctx* c, int n, const int32_t* req, const ws_accept_args* a, ws_
   if (int r = check_common(c, n, req, stream)) return r;
   if (!a) return fail(c, WS_EINVAL, "null accept args");
   if (n == 0) return WS_OK;
-  if (a->mode < WS_ACCEPT_GREEDY || a->mode > WS_ACCEPT_FORCED) return fail(c, WS_EINVAL, "unknown accept mode");
+  if (a->mode < WS_ACCEPT_GREEDY || a->mode > WS_ACCEPT_TREE) return fail(c, WS_EINVAL, "unknown accept mode");
+  if (a->mode == WS_ACCEPT_TREE && (c->tree_n < 1 || a->H != c->tree_n))
+    return fail(c, WS_EINVAL, "tree acceptance needs a tree (ws_set_tree) and H equal to its row count");
   if (a->H < 1 || a->H > c->d.max_block) return fail(c, WS_EINVAL, "H outside 1..max_block");
   if (!a->block || !a->block_len || !a->budget || !a->done || !a->n_acc || !a->n_emit || !a->next_block ||
       !a->next_len)
@@ -812,11 +835,26 @@ int ws_accept(ws_ctx* c, int n, const int32_t* req, const ws_accept_args* a, ws_
   p.K = c->d.K;
   p.V = c->d.vocab;
   p.eos = c->d.eos_id;
+  p.max_pos = c->d.max_pos;
   p.suppress = c->suppress;
   p.status = c->status;
   p.pstat = c->pstat;
   p.qstat = c->qstat;
+  const bool tree = a->mode == WS_ACCEPT_TREE;
+  p.tree_n = tree ? c->tree_n : 0;
+  p.parent4 = c->tree_parent4;
+  p.tpath = c->tpath;
+  if (tree) p.a.mode = WS_ACCEPT_GREEDY;            // the greedy rule, walked over the tree
   CK(launch_accept(n, p, (cudaStream_t)stream, c->cur_pdl));
+  if (tree) {
+    TreeCommit t;
+    t.req_ids = req; t.tpath = c->tpath; t.kv = c->kv; t.kv_layer_bytes = c->kv_layer_bytes;
+    t.ptab = c->ptab; t.ppr = c->ppr; t.heads = c->heads; t.es = c->es; t.n_layers = c->d.n_layers;
+    const bool hist = c->d.drafter_layers > 0 && c->d.n_hist > 0;
+    t.hist = hist ? c->hist : nullptr; t.max_block = c->d.max_block; t.hist_w = hist ? c->d.n_hist * c->d.d_model : 0;
+    t.qread = c->readout_layer >= 0 ? (char*)c->qread : nullptr; t.H = a->H; t.d = c->d.d_model;
+    CK(launch_tree_commit(n, t, (cudaStream_t)stream, c->cur_pdl));
+  }
   return WS_OK;
 }
 
@@ -844,6 +882,57 @@ int ws_draft_limit(ws_ctx* c, int n, const int32_t* req, const int32_t* block, i
   CK(launch_draft_limit(n, c->d.K, block, stride_in, q_logits, c->d.vocab, temperature > 0.0f ? temperature : 1.0f,
                         c->suppress, c->conf, k_verify, threshold, block_out, stride_out, block_len,
                         (cudaStream_t)stream, c->cur_pdl));
+  return WS_OK;
+}
+
+int ws_set_tree(ws_ctx* c, int n_nodes, const int32_t* parent, const int32_t* rank) {
+  if (!c) return fail(nullptr, WS_EINVAL, "null context");
+  if (n_nodes == 0) {
+    c->tree_n = 0;
+    c->tree = linear_tree();
+    c->tree_parent4 = c->tree_rank4 = 0;
+    return WS_OK;
+  }
+  if (n_nodes < 1 || n_nodes > c->d.max_block || n_nodes > 16)
+    return fail(c, WS_EINVAL, "n_nodes %d outside 0..max_block (%d)", n_nodes, c->d.max_block);
+  if (!parent || !rank) return fail(c, WS_EINVAL, "null parent or rank");
+  if (parent[0] != -1 || rank[0] != 0) return fail(c, WS_EINVAL, "row 0 is the root: parent -1, rank 0");
+  TreeMask t;
+  t.depth4 = 0;
+  unsigned long long p4 = 0, r4 = 0;
+  int depth[16] = {0};
+  t.anc[0] = 1u;
+  for (int j = 1; j < n_nodes; ++j) {
+    if (parent[j] < 0 || parent[j] >= j) return fail(c, WS_EINVAL, "parent[%d] = %d not in 0..%d", j, parent[j], j - 1);
+    if (rank[j] < 0 || rank[j] > 15) return fail(c, WS_EINVAL, "rank[%d] = %d outside 0..15", j, rank[j]);
+    depth[j] = depth[parent[j]] + 1;
+    if (c->d.drafter_layers > 0 && depth[j] > c->d.K)
+      return fail(c, WS_EINVAL, "row %d at depth %d beyond the drafter's K = %d rows", j, depth[j], c->d.K);
+    t.anc[j] = t.anc[parent[j]] | (1u << j);
+    t.depth4 |= (unsigned long long)depth[j] << (4 * j);
+    p4 |= (unsigned long long)parent[j] << (4 * j);
+    r4 |= (unsigned long long)rank[j] << (4 * j);
+  }
+  for (int j = n_nodes; j < 16; ++j) t.anc[j] = 0u;
+  c->tree_n = n_nodes;
+  c->tree = t;
+  c->tree_parent4 = p4;
+  c->tree_rank4 = r4;
+  return WS_OK;
+}
+
+int ws_tree_tokens(ws_ctx* c, int n, const int32_t* req, const int32_t* block, int stride_in, const float* q_logits,
+                   int32_t* block_out, int stride_out, int32_t* block_len, ws_stream stream) {
+  if (int r = check_common(c, n, req, stream)) return r;
+  if (n == 0) return WS_OK;
+  if (c->tree_n < 1) return fail(c, WS_EINVAL, "no candidate tree set (ws_set_tree)");
+  if (!block || !q_logits || !block_out || !block_len) return fail(c, WS_EINVAL, "null block, q_logits, block_out or block_len");
+  if (stride_in < 1 || stride_out < c->tree_n) return fail(c, WS_EINVAL, "stride_out must hold the tree's rows");
+  for (int j = 1; j < c->tree_n; ++j)
+    if (tree_depth(c->tree.depth4, j) > c->d.K) return fail(c, WS_EINVAL, "tree deeper than the K draft rows");
+  CK(launch_tree_tokens(n, c->tree_n, c->tree.depth4, c->tree_rank4, req, c->L, c->d.max_pos, block, stride_in,
+                        q_logits, c->d.K, c->d.vocab, block_out, stride_out, block_len, (cudaStream_t)stream,
+                        c->cur_pdl));
   return WS_OK;
 }
 

@@ -53,6 +53,7 @@ struct AttnArgs {
   int* counters;             // [n][heads], zero between launches
   void* O;                   // [n*H, d]
   int32_t* status;
+  TreeMask tree;             // SELF: which block rows each row sees
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -165,10 +166,11 @@ __global__ void __launch_bounds__(NW * 32) attn_split_kernel(AttnArgs a) {
     if (j >= H) continue;
     RowState st;
     st.m = -INFINITY; st.l = 0.f; st.a0 = 0.f; st.a1 = 0.f;
-    int visible = nk;                                   // keys of this split row j may see
-    if (MODE == MODE_SELF) visible = (j < nrow) ? max(0, min(k_hi, min(Lr + j + 1, a.max_pos)) - k_lo) : 0;
+    uint64_t vm = prefix_mask(nk);                      // keys of this split row j may see
+    if (MODE == MODE_SELF) vm = (j < nrow) ? self_key_mask(k_lo, k_hi - k_lo, Lr, tree_anc(a.tree, j)) : 0ull;
+    const int visible = vm ? 64 - __clzll((long long)vm) : 0;
     for (int k0 = 0; k0 < visible; k0 += 32)
-      row_subtile(st, qs[j], Kt, Vt, k0, min(32, visible - k0), pws + warp * 32);
+      row_subtile(st, qs[j], Kt, Vt, k0, min(32, visible - k0), pws + warp * 32, (uint32_t)(vm >> k0));
     float* p = a.part + ((((size_t)i * H + j) * heads + head) * a.n_split + sp) * PART;
     if (lane == 0) { p[0] = st.m; p[1] = st.l; }
     p[2 + 2 * lane] = st.a0;
@@ -332,11 +334,11 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
         *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
       __syncwarp();
       const int g = lane >> 2;
-      auto vis = [&](int j) {
-        if (j >= H) return 0;
-        if (mode == MODE_CROSS) return nk;
-        if (j >= nrow) return 0;
-        return max(0, min(k_lo + nk, min(Lr + j + 1, a.max_pos)) - k_lo);
+      auto vis = [&](int j) -> uint64_t {
+        if (j >= H) return 0ull;
+        if (mode == MODE_CROSS) return prefix_mask(nk);
+        if (j >= nrow) return 0ull;
+        return self_key_mask(k_lo, nk, Lr, tree_anc(a.tree, j));
       };
       attn_chunk_partial<true>(Ks, Vs, qf, vis(g), vis(g + 8), H, part);
     } else {
@@ -431,11 +433,11 @@ __global__ void __launch_bounds__(CW * 32) attn_cluster_kernel(const __grid_cons
         for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)   // finite values beyond the keys
           *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
-        auto vis = [&](int j) {
-          if (j >= H) return 0;
-          if (mode == MODE_CROSS) return nk;
-          if (j >= nrow) return 0;
-          return max(0, min(k_lo + nk, min(Lr + j + 1, a.max_pos)) - k_lo);
+        auto vis = [&](int j) -> uint64_t {
+          if (j >= H) return 0ull;
+          if (mode == MODE_CROSS) return prefix_mask(nk);
+          if (j >= nrow) return 0ull;
+          return self_key_mask(k_lo, nk, Lr, tree_anc(a.tree, j));
         };
         attn_chunk_partial<true>(Ks, Vs, qf, vis(lane >> 2), vis((lane >> 2) + 8), H, part);
       }
@@ -592,10 +594,11 @@ cudaError_t attn_init_attributes() {
 }
 
 template <typename T>
-cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const KVPool& kv, T* O, int n_heads,
-                             const AttnScratch& sc, cudaStream_t s, bool pdl) {
+cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const TreeMask& tree, const T* Q, const KVPool& kv, T* O,
+                             int n_heads, const AttnScratch& sc, cudaStream_t s, bool pdl) {
   if (H > MAXR) return cudaErrorInvalidValue;
   AttnArgs a = {};
+  a.tree = tree;
   a.mode = MODE_SELF;
   a.H = H; a.d = n_heads * WS_DH; a.max_pos = rm.max_pos;
   a.n_split = (rm.max_pos + SPLIT - 1) / SPLIT;
@@ -642,7 +645,7 @@ cudaError_t launch_draft_attn(int n, int K1, const int32_t* req_ids, const int32
 
 #define INST(T)                                                                                                  \
   template cudaError_t attn_init_attributes<T>();                                                               \
-  template cudaError_t launch_self_attn<T>(int, int, const RowMap&, const T*, const KVPool&, T*, int,            \
+  template cudaError_t launch_self_attn<T>(int, int, const RowMap&, const TreeMask&, const T*, const KVPool&, T*, int,            \
                                            const AttnScratch&, cudaStream_t, bool);                              \
   template cudaError_t launch_cross_attn<T>(int, int, const int32_t*, const int32_t*, const T*, const XKV&, int, \
                                             T*, int, int, const AttnScratch&, cudaStream_t, bool);               \

@@ -9,13 +9,32 @@ constexpr int WS_ATTN_PART = WS_DH + 2;    // floats per split partial
 
 struct RowState { float m, l, a0, a1; };
 
+// Keys 0 .. n-1 of a chunk of 64.
+__device__ __forceinline__ uint64_t prefix_mask(int n) {
+  return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1ull));
+}
+// Self-attention keys of the chunk [k_lo, k_lo + nk) that a block row sees:
+// every cache key before the block start L, and of the block's own slots L,
+// L + 1, ... those whose bit is set in anc (the row's ancestors in the
+// candidate tree; rows 0..j for a linear block).
+__device__ __forceinline__ uint64_t self_key_mask(int k_lo, int nk, int L, uint32_t anc) {
+  const int sh = L - k_lo;
+  uint64_t m = prefix_mask(sh);
+  if (sh >= 0 && sh < 64) m |= (uint64_t)anc << sh;
+  else if (sh < 0 && sh > -32) m |= (uint64_t)(anc >> (-sh));
+  return m & prefix_mask(nk);
+}
+
 // One sub-tile of up to 32 keys for one row (warp-wide): scores by lane = key,
 // online-softmax update, then weighted values with lane = pair of dims.
+// Keys whose bit in vmask is clear get no weight; the first key of every
+// sub-tile a row visits is visible (the keys before the block start are).
 __device__ __forceinline__ void row_subtile(RowState& st, const float* q, const float (*Kt)[WS_DH + 1],
-                                            const float (*Vt)[WS_DH], int k0, int nvalid, float* pw) {
+                                            const float (*Vt)[WS_DH], int k0, int nvalid, float* pw,
+                                            uint32_t vmask = 0xFFFFFFFFu) {
   const int lane = threadIdx.x & 31;
   float s = -INFINITY;
-  if (lane < nvalid) {
+  if (lane < nvalid && ((vmask >> lane) & 1u)) {
     const float* kr = Kt[k0 + lane];
     float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
 #pragma unroll

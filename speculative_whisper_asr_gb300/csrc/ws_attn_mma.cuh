@@ -62,12 +62,13 @@ __device__ __forceinline__ void attn_q_frags(const bf16* q, int ldq, int q_row0,
   }
 }
 
-// One chunk: keys 0 .. 63 of Ks / Vs, row r (0..15) sees keys [0, vis[r]).
-// Writes the partial of row r to part(r) (m, l, a[64]) for rows r < nrows.
-// Rows with no visible key get m = -inf, l = 0, a = 0.
+// One chunk: keys 0 .. 63 of Ks / Vs; the lanes' rows g and g + 8 see the
+// keys whose bits are set in vis_lo / vis_hi.  Writes the partial of row r to
+// part(r) (m, l, a[64]) for rows r < nrows.  Rows with no visible key get
+// m = -inf, l = 0, a = 0.
 template <bool SWZ, class PartPtr>
 __device__ __forceinline__ void attn_chunk_partial(const uint8_t* Ks, const uint8_t* Vs, const uint32_t qf[4][4],
-                                                   int vis_lo, int vis_hi, int nrows, PartPtr part) {
+                                                   uint64_t vis_lo, uint64_t vis_hi, int nrows, PartPtr part) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const uint32_t kb = smem_addr_u32(Ks), vb = smem_addr_u32(Vs);
   // ---- S = Q K^T: key tile j (keys 8j..8j+7), two dim steps per ldmatrix.x4
@@ -94,8 +95,8 @@ __device__ __forceinline__ void attn_chunk_partial(const uint8_t* Ks, const uint
       const int key = 8 * j + 2 * c + e;
       sc[j][e] *= 0.125f;                      // 1/sqrt(64)
       sc[j][2 + e] *= 0.125f;
-      if (key < vis_lo) m0 = fmaxf(m0, sc[j][e]);
-      if (key < vis_hi) m1 = fmaxf(m1, sc[j][2 + e]);
+      if ((vis_lo >> key) & 1ull) m0 = fmaxf(m0, sc[j][e]);
+      if ((vis_hi >> key) & 1ull) m1 = fmaxf(m1, sc[j][2 + e]);
     }
   }
   m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
@@ -108,8 +109,8 @@ __device__ __forceinline__ void attn_chunk_partial(const uint8_t* Ks, const uint
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int key = 8 * j + 2 * c + e;
-      const float p0 = key < vis_lo ? expf(sc[j][e] - m0) : 0.f;
-      const float p1 = key < vis_hi ? expf(sc[j][2 + e] - m1) : 0.f;
+      const float p0 = ((vis_lo >> key) & 1ull) ? expf(sc[j][e] - m0) : 0.f;
+      const float p1 = ((vis_hi >> key) & 1ull) ? expf(sc[j][2 + e] - m1) : 0.f;
       sc[j][e] = p0;
       sc[j][2 + e] = p1;
       l0 += p0;
@@ -150,7 +151,7 @@ __device__ __forceinline__ void attn_chunk_partial(const uint8_t* Ks, const uint
     }
   }
   // ---- partials of rows g and g + 8
-  const bool has0 = vis_lo > 0, has1 = vis_hi > 0;
+  const bool has0 = vis_lo != 0ull, has1 = vis_hi != 0ull;
   if (g < nrows) {
     float* p = part(g);
     if (c == 0) { p[0] = has0 ? m0 : -INFINITY; p[1] = has0 ? l0 : 0.f; }

@@ -686,7 +686,7 @@ __device__ __noinline__ void weight_bundle(const FlowArgs& a, const Plan& P, uin
 // attention kinds.
 __device__ __noinline__ void chunk_partial(const uint8_t* Ks, const uint8_t* Vs, const uint32_t (*qf)[4], int vis_lo,
                                            int vis_hi, int nrows, float* out) {
-  attn_chunk_partial<true>(Ks, Vs, qf, vis_lo, vis_hi, nrows,
+  attn_chunk_partial<true>(Ks, Vs, qf, prefix_mask(vis_lo), prefix_mask(vis_hi), nrows,
                            [&](int r) { return out + (size_t)r * WS_ATTN_PART; });
 }
 

@@ -206,6 +206,32 @@ struct RowMap {
   const int32_t* pend_start;   // [max_batch] (ROW_HIST)
   const int32_t* pend_n;       // [max_batch] (ROW_HIST)
 };
+// A block of verification rows as a candidate tree (Alignment Drift App. E.3):
+// row j is embedded at position L + depth(j) and its self-attention sees the
+// cache before L and the block rows in anc[j] (bit m = row m, row j itself
+// included); its keys and values are stored at cache slot L + j.  The
+// linear block is the chain depth(j) = j, anc[j] = rows 0..j.
+struct TreeMask {
+  unsigned long long depth4;   // depth of row j in bits 4j .. 4j + 3
+  uint32_t anc[16];
+};
+inline TreeMask linear_tree() {
+  TreeMask t;
+  t.depth4 = 0xFEDCBA9876543210ull;
+  for (int j = 0; j < 16; ++j) t.anc[j] = (2u << j) - 1u;
+  return t;
+}
+__host__ __device__ __forceinline__ int tree_depth(unsigned long long depth4, int j) {
+  return (int)((depth4 >> (4 * j)) & 15ull);
+}
+// anc[j] without a dynamic index into the (parameter-space) array
+__device__ __forceinline__ uint32_t tree_anc(const TreeMask& t, int j) {
+  uint32_t r = 0u;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) r = (m == j) ? t.anc[m] : r;
+  return r;
+}
+
 // Returns true when the row holds a real token whose K/V may be written.
 __device__ __forceinline__ bool row_info(const RowMap& m, int r, int& slot, int& j, int& pos) {
   int i = r / m.H;
@@ -347,9 +373,9 @@ template <typename T>
 cudaError_t launch_layernorm(int M, int d, const float* x, int ldx, const T* g, const T* b, T* y, int ldy,
                              int group_skip, cudaStream_t s, bool pdl);
 template <typename T>
-cudaError_t launch_embed_target(int n, int H, const RowMap& rm, const int32_t* block, const T* E,
-                                const T* P, int d, int V, float* x, int32_t* pend_start, int32_t* pend_n,
-                                int32_t* status, cudaStream_t s, bool pdl);
+cudaError_t launch_embed_target(int n, int H, const RowMap& rm, unsigned long long depth4, const int32_t* block,
+                                const T* E, const T* P, int d, int V, float* x, int32_t* pend_start,
+                                int32_t* pend_n, int32_t* status, cudaStream_t s, bool pdl);
 template <typename T>
 cudaError_t launch_embed_draft(int n, int K1, const int32_t* req_ids, const int32_t* block, const T* E,
                                const T* m, int d, int V, float* x, int32_t* pend_n, int32_t* status,
@@ -362,8 +388,8 @@ cudaError_t launch_hist_gather(int n, int Hp, const int32_t* req_ids, const int3
                                const float* hist, int max_block, int n_hist, int d, T* feat,
                                cudaStream_t s, bool pdl);
 template <typename T>
-cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const T* Q, const KVPool& kv, T* O,
-                             int n_heads, const AttnScratch& sc, cudaStream_t s, bool pdl);
+cudaError_t launch_self_attn(int n, int H, const RowMap& rm, const TreeMask& tree, const T* Q, const KVPool& kv,
+                             T* O, int n_heads, const AttnScratch& sc, cudaStream_t s, bool pdl);
 template <typename T>
 cudaError_t launch_draft_attn(int n, int K1, const int32_t* req_ids, const int32_t* L, const T* Q,
                               const T* Kb, const T* Vb, const KVPool& hkv, T* O, int n_heads,
@@ -398,7 +424,34 @@ struct AcceptParams {
   int32_t* status;
   float2* pstat;     // sampling: (max, sum exp) of each target row [n][H] at T ...
   float2* qstat;     // ... and of each drafter row [n][K] (filled by launch_accept)
+  int max_pos;
+  int tree_n;                  // > 0: greedy acceptance walks a candidate tree of this many rows
+  unsigned long long parent4;  // tree: parent row of row j in bits 4j .. 4j + 3
+  int32_t* tpath;              // tree: per request [L before, a, path rows 0..a] (WS_TREE_REC ints)
 };
+#define WS_TREE_REC 18
+// Move the accepted root path's self keys / values (every target layer),
+// history rows and readout queries from their tree rows to block rows 0..a.
+struct TreeCommit {
+  const int32_t* req_ids;
+  const int32_t* tpath;        // written by the acceptance kernel
+  char* kv;                    // self K/V pool of layer 0
+  size_t kv_layer_bytes;
+  const int32_t* ptab;
+  int ppr, heads, es, n_layers;
+  float* hist;                 // [slot][max_block][hist_w] fp32, or NULL
+  int max_block, hist_w;
+  char* qread;                 // [n * H][d] model dtype, or NULL
+  int H, d;
+};
+cudaError_t launch_tree_commit(int n, const TreeCommit& t, cudaStream_t s, bool pdl);
+// Tokens of a fixed candidate tree from the drafter's logits: row j at
+// depth k >= 1 takes the rank(j)-th largest logit of mask row k - 1 (ties
+// to the lower id); row 0 keeps the anchor.
+cudaError_t launch_tree_tokens(int n, int n_nodes, unsigned long long depth4, unsigned long long rank4,
+                               const int32_t* req_ids, const int32_t* L, int max_pos, const int32_t* block,
+                               int stride_in, const float* q, int K, int V, int32_t* out, int stride_out,
+                               int32_t* blen, cudaStream_t s, bool pdl);
 // Sampling acceptance first fills pstat / qstat with one CTA per logits row,
 // then runs one CTA per request.
 cudaError_t launch_accept(int n, const AcceptParams& p, cudaStream_t s, bool pdl);

@@ -46,17 +46,21 @@ __device__ float block_max(float v, float* sh) {
 
 // ------------------------------------------------------------------ embeddings
 // Target rows: x = E[token] + P[position] (token + learned position embedding).
+// Block row j sits at position L + depth(j) (depth(j) = j for a linear block,
+// the tree depth for a candidate tree); its cache slot L + j is checked.
 template <typename T>
-__global__ void embed_target_kernel(RowMap rm, const int32_t* block, const T* E, const T* P, int d, int V,
-                                    float* x, int32_t* pend_start, int32_t* pend_n, int32_t* status) {
+__global__ void embed_target_kernel(RowMap rm, unsigned long long depth4, const int32_t* block, const T* E,
+                                    const T* P, int d, int V, float* x, int32_t* pend_start, int32_t* pend_n,
+                                    int32_t* status) {
   pdl_wait();
   const int r = blockIdx.x;
   int slot, j, pos;
-  bool valid = row_info(rm, r, slot, j, pos);
+  bool valid = row_info(rm, r, slot, j, pos);         // pos: the row's cache slot L + j
   const int i = r / rm.H;
   int tok = block[r];
   bool in_block = j < rm.block_len[i];
   if (in_block && pos >= rm.max_pos && threadIdx.x == 0) atomicOr(status, WS_ST_POS);
+  pos -= j - tree_depth(depth4, j);                   // the embedded position L + depth(j) <= L + j
   if (!valid) { tok = 0; pos = min(pos, rm.max_pos - 1); }
   if (tok < 0 || tok >= V) {
     if (threadIdx.x == 0) atomicOr(status, WS_ST_TOKEN);
@@ -519,6 +523,10 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
   const int blen = A.block_len[i];
   const bool was_done = A.done[i] != 0;
   int R = A.budget[i];
+  if (P.tree_n > 0 && threadIdx.x == 0) {       // nothing to commit unless the walk below says so
+    P.tpath[(size_t)i * WS_TREE_REC] = P.L[slot];
+    P.tpath[(size_t)i * WS_TREE_REC + 1] = 0;
+  }
   if (was_done || blen <= 0 || R <= 0) {
     if (threadIdx.x == 0) {
       A.n_acc[i] = 0;
@@ -546,10 +554,32 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
   if (A.mode == WS_ACCEPT_GREEDY || (A.mode == WS_ACCEPT_FORCED && !forced_sample)) {
     if (threadIdx.x == 0) {
       const int32_t* g = A.target + (size_t)i * A.H;
-      int a = 0, ne = 0;
+      int a = 0, ne = 0, last_row = -1;   // last_row: the row whose argmax follows the accepted tokens
       bool eos_hit = false;
       if (A.mode == WS_ACCEPT_FORCED) {
         a = n_prop;
+      } else if (P.tree_n > 0) {
+        // candidate tree (Alignment Drift App. E.3): from the root, step to the
+        // lowest-numbered child whose token is the target's argmax at the
+        // current row, at most R - 1 times
+        int* rec = P.tpath + (size_t)i * WS_TREE_REC;
+        const int rows = min(min(blen, A.H), P.max_pos - P.L[slot]);   // rows whose cache slots exist
+        int cur = 0;
+        rec[2] = 0;
+        while (a < R - 1) {
+          int nxt = -1;
+          for (int c = cur + 1; c < rows; ++c)
+            if ((int)((P.parent4 >> (4 * c)) & 15ull) == cur && blk[c] == g[cur]) { nxt = c; break; }
+          if (nxt < 0) break;
+          cur = nxt;
+          ++a;
+          rec[2 + a] = cur;
+          s_emit[ne++] = blk[cur];
+          if (blk[cur] == P.eos) { eos_hit = true; break; }
+        }
+        rec[0] = P.L[slot];
+        rec[1] = a;
+        last_row = cur;
       } else {
         for (int j = 1; j <= n_prop; ++j) {
           if (blk[j] != g[j - 1]) break;
@@ -558,7 +588,7 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
           if (blk[j] == P.eos) { eos_hit = true; break; }
         }
       }
-      if (!eos_hit) s_emit[ne++] = g[a];
+      if (!eos_hit) s_emit[ne++] = g[last_row < 0 ? a : last_row];
       s_a = a;
       s_ne = ne;
     }
@@ -640,6 +670,98 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
   pdl_trigger();
 }
 
+// ------------------------------------------------------------------ candidate trees
+// After a tree acceptance, block row j (1 <= j <= a) takes the contents of
+// tree row path[j] >= j.  grid (2 * n_layers + 2, n): job x < 2 * n_layers
+// moves layer x / 2's keys (x even) or values of cache slots L + path[j] to
+// L + j; job 2 * n_layers the history rows; the last job the readout
+// queries.  Each thread owns a set of 4-byte words and walks j upwards, so
+// a row is read before a later j overwrites it (path[j] >= j).
+__global__ void __launch_bounds__(256) tree_commit_kernel(TreeCommit t) {
+  pdl_wait();
+  const int job = blockIdx.x, i = blockIdx.y;
+  const int* rec = t.tpath + (size_t)i * WS_TREE_REC;
+  const int slot = t.req_ids[i], L0 = rec[0], a = rec[1];
+  const int* path = rec + 2;
+  pdl_trigger();
+  if (a <= 0) return;
+  if (job < 2 * t.n_layers) {
+    const int l = job >> 1, kv = job & 1;
+    const int nw = WS_DH * t.es / 4;                       // words per head row
+    const char* base = t.kv + (size_t)l * t.kv_layer_bytes;
+    auto row = [&](int pos, int head) {
+      const int page = t.ptab[slot * t.ppr + pos / WS_PAGE];
+      const size_t off = (((size_t)page * 2 + kv) * t.heads + head) * (WS_PAGE * WS_DH) + (size_t)(pos % WS_PAGE) * WS_DH;
+      return reinterpret_cast<uint32_t*>(const_cast<char*>(base) + off * t.es);
+    };
+    for (int w = threadIdx.x; w < t.heads * nw; w += blockDim.x) {
+      const int head = w / nw, o = w - head * nw;
+      for (int j = 1; j <= a; ++j)
+        if (path[j] != j) row(L0 + j, head)[o] = row(L0 + path[j], head)[o];
+    }
+  } else if (job == 2 * t.n_layers) {
+    if (!t.hist) return;
+    float* h = t.hist + (size_t)slot * t.max_block * t.hist_w;
+    for (int w = threadIdx.x; w < t.hist_w; w += blockDim.x)
+      for (int j = 1; j <= a; ++j)
+        if (path[j] != j) h[(size_t)j * t.hist_w + w] = h[(size_t)path[j] * t.hist_w + w];
+  } else {
+    if (!t.qread) return;
+    const int nw = t.d * t.es / 4;
+    uint32_t* q = reinterpret_cast<uint32_t*>(t.qread) + (size_t)i * t.H * nw;
+    for (int w = threadIdx.x; w < nw; w += blockDim.x)
+      for (int j = 1; j <= a; ++j)
+        if (path[j] != j) q[(size_t)j * nw + w] = q[(size_t)path[j] * nw + w];
+  }
+}
+
+// One CTA per (tree row j, request): row 0 copies the anchor and sets the
+// block length (every row of the tree that fits before max_pos; 0 for an
+// idle request); row j >= 1 ranks the logits of mask row depth(j) - 1 by
+// (value, lower id first) and takes the one of rank rank(j).
+__global__ void __launch_bounds__(SNT) tree_tokens_kernel(int n_nodes, unsigned long long depth4,
+                                                          unsigned long long rank4, const int32_t* req_ids,
+                                                          const int32_t* L, int max_pos, const int32_t* block,
+                                                          int stride_in, const float* q, int K, int V, int32_t* out,
+                                                          int stride_out, int32_t* blen) {
+  __shared__ unsigned long long sk[SNT / 32];
+  pdl_wait();
+  const int j = blockIdx.x, i = blockIdx.y;
+  if (j == 0) {
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+      out[(size_t)i * stride_out] = block[(size_t)i * stride_in];
+      const int b_in = blen[i];
+      blen[i] = b_in > 0 ? max(1, min(n_nodes, max_pos - L[req_ids[i]])) : 0;
+    }
+    return;
+  }
+  const int depth = tree_depth(depth4, j), rank = (int)((rank4 >> (4 * j)) & 15ull);
+  const float* z = q + ((long long)i * K + (depth - 1)) * V;
+  unsigned long long prev = ~0ull;
+  for (int r = 0; r <= rank; ++r) {
+    unsigned long long best = 0ull;
+    for (int v = threadIdx.x; v < V; v += SNT) {
+      const unsigned long long k = argmax_key(z[v], v);
+      if (k < prev && k > best) best = k;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sk[threadIdx.x >> 5] = best;
+    __syncthreads();
+    best = 0ull;
+#pragma unroll
+    for (int w = 0; w < SNT / 32; ++w) best = sk[w] > best ? sk[w] : best;
+    prev = best;
+  }
+  pdl_trigger();
+  if (threadIdx.x == 0) out[(size_t)i * stride_out + j] = argmax_key_id(prev);
+}
+
 // ------------------------------------------------------------------ synthetic drafts
 __global__ void draft_synth_kernel(int K, const int32_t* req_ids, const int32_t* L, int32_t* block,
                                    const int32_t* traj, int tlen, const uint8_t* cmask, const int32_t* ctok,
@@ -660,13 +782,14 @@ __global__ void draft_synth_kernel(int K, const int32_t* req_ids, const int32_t*
 
 // ------------------------------------------------------------------ launchers
 template <typename T>
-cudaError_t launch_embed_target(int n, int H, const RowMap& rm, const int32_t* block, const T* E, const T* P,
-                                int d, int V, float* x, int32_t* pend_start, int32_t* pend_n, int32_t* status,
-                                cudaStream_t s, bool pdl) {
+cudaError_t launch_embed_target(int n, int H, const RowMap& rm, unsigned long long depth4, const int32_t* block,
+                                const T* E, const T* P, int d, int V, float* x, int32_t* pend_start, int32_t* pend_n,
+                                int32_t* status, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n * H), dim3(128), 0, s, pdl, at);
   ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg, embed_target_kernel<T>, rm, block, E, P, d, V, x, pend_start, pend_n, status);
+  return cudaLaunchKernelEx(&cfg, embed_target_kernel<T>, rm, depth4, block, E, P, d, V, x, pend_start, pend_n,
+                            status);
 }
 template <typename T>
 cudaError_t launch_embed_draft(int n, int K1, const int32_t* req_ids, const int32_t* block, const T* E, const T* m,
@@ -811,6 +934,22 @@ cudaError_t launch_accept(int n, const AcceptParams& p, cudaStream_t s, bool pdl
   ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, accept_kernel, p);
 }
+cudaError_t launch_tree_commit(int n, const TreeCommit& t, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(2 * t.n_layers + 2, n), dim3(256), 0, s, pdl, at);
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&cfg, tree_commit_kernel, t);
+}
+cudaError_t launch_tree_tokens(int n, int n_nodes, unsigned long long depth4, unsigned long long rank4,
+                               const int32_t* req_ids, const int32_t* L, int max_pos, const int32_t* block,
+                               int stride_in, const float* q, int K, int V, int32_t* out, int stride_out,
+                               int32_t* blen, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(n_nodes, n), dim3(SNT), 0, s, pdl, at);
+  ws_count_launches(1);
+  return cudaLaunchKernelEx(&cfg, tree_tokens_kernel, n_nodes, depth4, rank4, req_ids, L, max_pos, block, stride_in,
+                            q, K, V, out, stride_out, blen);
+}
 cudaError_t launch_draft_synth(int n, int K, const int32_t* req_ids, const int32_t* L, int32_t* block,
                                const int32_t* traj, int tlen, const uint8_t* cmask, const int32_t* ctok, int max_pos,
                                cudaStream_t s, bool pdl) {
@@ -821,7 +960,8 @@ cudaError_t launch_draft_synth(int n, int K, const int32_t* req_ids, const int32
 }
 
 #define INST(T)                                                                                                     \
-  template cudaError_t launch_embed_target<T>(int, int, const RowMap&, const int32_t*, const T*, const T*, int, int, \
+  template cudaError_t launch_embed_target<T>(int, int, const RowMap&, unsigned long long, const int32_t*, const T*,  \
+                                              const T*, int, int,                                                    \
                                               float*, int32_t*, int32_t*, int32_t*, cudaStream_t, bool);             \
   template cudaError_t launch_embed_draft<T>(int, int, const int32_t*, const int32_t*, const T*, const T*, int, int, \
                                              float*, int32_t*, int32_t*, cudaStream_t, bool);                        \

@@ -53,6 +53,7 @@ class Decoder:
         self.dtype = B.WS_BF16 if shape.dtype == "bf16" else B.WS_F32
         self.tdtype = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
         self.readout = False
+        self.tree = None
         dl = shape.drafter_layers if drafter is not None else 0
         self.max_block = max_block or max(shape.K + 1, len(shape.prompt))
         self.desc = B.make_desc(shape.n_layers, shape.d_model, shape.n_heads, shape.d_ff, shape.vocab,
@@ -130,6 +131,13 @@ class Decoder:
         B.ws_set_readout(self.ctx, layer, half_width)
         self.readout = layer >= 0
 
+    def set_tree(self, parent=(), rank=()):
+        """Candidate tree of block rows for tree verification (Alignment Drift
+        App. E.3): parent[j] < j (parent[0] = -1), rank[j] = which of the
+        drafter's ranked tokens row j takes at its depth; empty: no tree."""
+        B.ws_set_tree(self.ctx, list(parent), list(rank))
+        self.tree = (tuple(parent), tuple(rank)) if len(parent) else None
+
     def centers(self, req) -> np.ndarray:
         out = torch.empty(req.numel(), dtype=torch.int32, device=self.dev)
         B.ws_get_centers(self.ctx, req.numel(), req.data_ptr(), out.data_ptr(), _stream())
@@ -175,9 +183,11 @@ class Batch:
         self.p_logits = self.q_logits = self.p_logits1 = None
         if sampling:
             self.p_logits = torch.empty(n, K + 1, dec.V, dtype=torch.float32, device=dev)
-        if sampling or draft_logits:
+        if sampling or draft_logits or dec.tree is not None:
             self.q_logits = torch.empty(n, K, dec.V, dtype=torch.float32, device=dev)
         self.vblock = torch.zeros(n, K + 1, **i32)      # the block as verified (truncated proposals)
+        self.tblock = torch.zeros(n, dec.max_block, **i32)    # a candidate tree's tokens
+        self.ttarget = torch.zeros(n, dec.max_block, **i32)
         self.host_done = torch.zeros(1, dtype=torch.int32).pin_memory()
         self.graphs = {}
 
@@ -248,18 +258,41 @@ class Batch:
         B.ws_accept(d.ctx, self.n, self.req.data_ptr(), a, _stream())
 
     def spec_step(self, rnd: int, synthetic=None, temperature: float = 0.0, seed: int = 0, run_drafter=True,
-                  graph: bool = True, k_verify: int | None = None, threshold: float = 0.0):
+                  graph: bool = True, k_verify: int | None = None, threshold: float = 0.0, tree: bool = False):
         """One propose / verify / accept round.  `synthetic` = (traj, cmask, ctok) device tensors.
         k_verify / threshold: verify only the first k_verify proposals, stopping
         before the first one whose drafter confidence is below threshold
         (ws_draft_limit).  Greedy rounds replay one captured graph per
         (proposal source, verify length, threshold): their calls do not depend
-        on the round."""
-        if graph and temperature <= 0.0:
+        on the round.  tree: the drafter's ranked tokens fill the decoder's
+        candidate tree (set_tree), verified in one pass and accepted along
+        the longest matching root path (greedy only)."""
+        if tree:
+            if temperature > 0.0 or synthetic is not None or not run_drafter or self.dec.tree is None:
+                raise ValueError("tree rounds need set_tree, the drafter and greedy decoding")
+            if graph:
+                self.replay(("tree", self.dec.tree), self._tree_calls)
+            else:
+                self._tree_calls()
+        elif graph and temperature <= 0.0:
             self.replay(("spec", synthetic is not None, run_drafter, k_verify, threshold),
                         lambda: self._spec_calls(0, synthetic, 0.0, 0, run_drafter, k_verify, threshold))
         else:
             self._spec_calls(rnd, synthetic, temperature, seed, run_drafter, k_verify, threshold)
+
+    def _tree_calls(self):
+        d = self.dec
+        N = len(d.tree[0])
+        req = self.req.data_ptr()
+        d.draft(self.req, self.block, 0.0, 0, 0, self.q_logits)
+        B.ws_tree_tokens(d.ctx, self.n, req, self.block.data_ptr(), d.K + 1, self.q_logits.data_ptr(),
+                         self.tblock.data_ptr(), N, self.blen.data_ptr(), _stream())
+        B.ws_verify_tree(d.ctx, self.n, req, N, self.tblock.data_ptr(), self.blen.data_ptr(),
+                         self.ttarget.data_ptr(), 0, _stream())
+        a = self._args(B.WS_ACCEPT_TREE, N, self.tblock, self.blen, self.ttarget, self.block, self.blen)
+        B.ws_accept(d.ctx, self.n, req, a, _stream())
+        if d.readout:              # the path's rows are in block order after acceptance
+            B.ws_readout(d.ctx, self.n, req, self.n_acc.data_ptr(), _stream())
 
     def _spec_calls(self, rnd, synthetic, temperature, seed, run_drafter, k_verify=None, threshold=0.0):
         d = self.dec
@@ -309,12 +342,12 @@ def run_ar(dec: Decoder, batch: Batch, max_rounds: int = 100000) -> int:
 
 
 def run_spec(dec: Decoder, batch: Batch, synthetic=None, temperature=0.0, seed=0, max_rounds=100000,
-             run_drafter=True, graph=True, k_verify=None, threshold=0.0) -> int:
+             run_drafter=True, graph=True, k_verify=None, threshold=0.0, tree=False) -> int:
     batch.prefill(temperature=temperature, seed=seed)
     rounds = 0
     while batch.poll_done() < batch.n and rounds < max_rounds:
         batch.spec_step(rounds + 1, synthetic, temperature, seed, run_drafter, graph=graph, k_verify=k_verify,
-                        threshold=threshold)
+                        threshold=threshold, tree=tree)
         rounds += 1
     return rounds
 

@@ -656,3 +656,60 @@ def test_windowed_speculation_is_exact(small_drafter):
     res = M.speculative_greedy_windowed(orc, orc.new_request(A), 20, 1, 5)
     assert res.tokens == ar
     assert all(0 <= c < 50 for c in res.margins)
+
+
+# ---------------------------------------------------------------- tree drafts (Alignment Drift App. E.3)
+
+TREE_PARENT = [-1, 0, 0, 0, 1, 2, 4, 6, 7, 8, 9, 10]      # 11 candidate nodes under the anchor
+TREE_RANK = [0, 0, 1, 2, 0, 0, 0, 0, 0, 0, 0, 0]
+
+
+def test_tree_verify_node_logits_equal_plain_forward_over_root_path(small):
+    """Every node's logits equal the plain uncached forward over prompt +
+    cache + the tokens on the node's root path (the tree mask is exactly
+    'see your ancestors')."""
+    orc, _, _, A = small
+    req = orc.new_request(A)
+    prefix = [5, 6, 7, 8, 9]
+    orc.verify(req, prefix)
+    req.L = len(prefix)
+    toks = [11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22]
+    lg = orc.verify_tree(req, toks, TREE_PARENT)
+    for j in range(len(toks)):
+        path, c = [], j
+        while c >= 0:
+            path.append(toks[c])
+            c = TREE_PARENT[c]
+        full, _ = orc.forward_full(orc.new_request(A), prefix + path[::-1])
+        np.testing.assert_allclose(lg[j], full[-1], atol=1e-9)
+
+
+def test_tree_speculation_exact_and_one_branch_is_linear(small_drafter):
+    """A candidate tree keeps the output equal to autoregressive greedy
+    decoding, and a one-branch tree (a chain of K nodes taking the argmax of
+    each mask row) reproduces the linear drafter decode round for round."""
+    s, orc, A = small_drafter
+    budget = 24
+    ar = M.greedy_cached(orc, orc.new_request(A), budget).tokens
+    res = M.speculative_greedy_tree(orc, orc.new_request(A), budget, TREE_PARENT, TREE_RANK)
+    assert res.tokens == ar
+    chain = [-1] + list(range(s.K))
+    lin_t = M.speculative_greedy_tree(orc, orc.new_request(A), budget, chain, [0] * (s.K + 1))
+    lin = M.speculative_greedy(orc, orc.new_request(A), budget, M.drafter_proposer(orc))
+    assert lin_t.tokens == lin.tokens == ar
+    # a linear round proposes min(K, R-1); the tree proposes its nodes but accepts at most R-1
+    assert lin_t.accepted == lin.accepted and lin_t.rounds == lin.rounds
+
+
+def test_accept_tree_walk_and_tokens_by_rank():
+    g = [50, 60, 0, 0, 70, 0, 55, 0, 0, 0, 0, 0]        # argmax at node j
+    toks = [1, 50, 51, 52, 60, 53, 70, 71, 72, 73, 74, 75]
+    acc, path = M.accept_tree(toks, TREE_PARENT, g, 100, 999)
+    assert path == [0, 1, 4, 6] and acc.emitted == [50, 60, 70, 55] and acc.a == 3
+    acc, path = M.accept_tree(toks, TREE_PARENT, g, 3, 999)       # at most R - 1 = 2 candidates
+    assert path == [0, 1, 4] and acc.emitted == [50, 60, 70]
+    acc, path = M.accept_tree(toks, TREE_PARENT, [51] + g[1:], 100, 999)   # second branch at depth 1
+    assert path[:2] == [0, 2]
+    q = np.zeros((8, 10)); q[0, [4, 7, 2]] = [3.0, 2.0, 2.0]
+    t = M.tree_tokens(q, TREE_PARENT, TREE_RANK, 9)
+    assert t[:4] == [9, 4, 2, 7]                                  # ties rank the lower id first
