@@ -8,8 +8,9 @@ What it produces
   * model shapes (Whisper large-v3, large-v3-turbo and a tiny 4-layer shape);
   * decoder / drafter weights, N(0, 0.02) random init, one independent PCG64
     stream per tensor so that any tensor can be regenerated on its own;
-  * encoder states A = E(x) ~ N(0, 1) (the encoder itself is not built:
-    Whisper-Flash, arXiv 2609.32869, §3.2 names A as the acoustic memory);
+  * encoder states A = E(x) ~ N(0, 1) for the decoding path (Whisper-Flash
+    §3.2 names A as the acoustic memory), and for the audio encoder its
+    weights and log-mel stand-ins;
   * workload plans: synthetic draft corruption, transcript budgets, varlen
     frame counts.
 
@@ -230,6 +231,61 @@ def encoder_states(s: ModelShape, seed: int, request: int, frames: int = 1500) -
     g = _rng(seed + 1000 + request, 3)
     a = g.standard_normal(size=(frames, s.d_model), dtype=np.float32)
     return _fmt(a, s.dtype)
+
+
+# ---------------------------------------------------------------- audio encoder
+
+@dataclass(frozen=True)
+class EncoderShape:
+    """Whisper audio encoder: a two-convolution stem over 2 * n_frames mel
+    frames, n_layers pre-LN transformer blocks over n_frames positions."""
+    name: str
+    n_layers: int
+    d_model: int
+    n_heads: int
+    d_ff: int
+    n_mels: int
+    n_frames: int = 1500
+    dtype: str = "bf16"
+
+
+ENC_LARGE_V3 = EncoderShape("large-v3-encoder", 32, 1280, 20, 5120, 128)
+ENC_TINY = EncoderShape("tiny-encoder", 4, 384, 6, 1536, 80)
+
+ENC_LAYER = ("ln1_g", "ln1_b", "w_qkv", "b_q", "b_v", "w_o", "b_o", "ln2_g", "ln2_b",
+             "w_fc1", "b_fc1", "w_fc2", "b_fc2")
+
+
+def encoder_tensor_shapes(e: EncoderShape):
+    """(name, shape) in blob order for the audio encoder:
+    conv1_w[d, n_mels, 3], conv1_b[d], conv2_w[d, d, 3], conv2_b[d],
+    layer 0..n-1 (ENC_LAYER order; w_qkv rows q|k|v, no key bias),
+    lnp_g[d], lnp_b[d] (the final layer norm)."""
+    d, f = e.d_model, e.d_ff
+    shp = {"w_qkv": (3 * d, d), "w_o": (d, d), "w_fc1": (f, d), "w_fc2": (d, f), "b_fc1": (f,)}
+    out = [("conv1_w", (d, e.n_mels, 3)), ("conv1_b", (d,)), ("conv2_w", (d, d, 3)), ("conv2_b", (d,))]
+    for l in range(e.n_layers):
+        out += [(f"layers.{l}.{n}", shp.get(n, (d,))) for n in ENC_LAYER]
+    out += [("lnp_g", (d,)), ("lnp_b", (d,))]
+    return out
+
+
+def encoder_weights(e: EncoderShape, seed: int) -> dict:
+    """All encoder tensors, N(0, 0.02) (LN gains 1 + N(0, 0.02)), bf16-valued
+    for bf16 shapes."""
+    from concurrent.futures import ThreadPoolExecutor
+    shapes = encoder_tensor_shapes(e)
+    with ThreadPoolExecutor(_threads()) as ex:
+        arrs = list(ex.map(lambda ns: _fmt(_draw(ns[0], ns[1], seed, 4), e.dtype), shapes))
+    return {n: a for (n, _), a in zip(shapes, arrs)}
+
+
+def mel_input(e: EncoderShape, seed: int, request: int) -> np.ndarray:
+    """Log-mel stand-in [n_mels, 2 * n_frames] ~ 0.5 N(0, 1) (normalised
+    Whisper features lie within about +-1.5), seeded per request."""
+    g = _rng(seed + 2000 + request, 5)
+    a = g.standard_normal(size=(e.n_mels, 2 * e.n_frames), dtype=np.float32) * np.float32(0.5)
+    return _fmt(a, e.dtype)
 
 
 # ---------------------------------------------------------------- workloads

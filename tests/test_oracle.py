@@ -713,3 +713,89 @@ def test_accept_tree_walk_and_tokens_by_rank():
     q = np.zeros((8, 10)); q[0, [4, 7, 2]] = [3.0, 2.0, 2.0]
     t = M.tree_tokens(q, TREE_PARENT, TREE_RANK, 9)
     assert t[:4] == [9, 4, 2, 7]                                  # ties rank the lower id first
+
+
+# ---------------------------------------------------------------- audio encoder
+
+from oracle import encoder as ENC
+
+ENC_SMALL = synth.EncoderShape("enc-small", 2, 128, 2, 512, 16, n_frames=48, dtype="f32")
+
+
+def test_encoder_positions_closed_forms():
+    """Sine half and cosine half of one frequency: sin^2 + cos^2 = 1; row 0 is
+    (0, ..., 0, 1, ..., 1); the first frequency is 1 rad per position and the
+    last 1/10000."""
+    P = ENC.sinusoids(1500, 384)
+    np.testing.assert_allclose(P[:, :192] ** 2 + P[:, 192:] ** 2, 1.0, atol=1e-12)
+    np.testing.assert_array_equal(P[0], np.r_[np.zeros(192), np.ones(192)])
+    t = np.arange(1500)
+    np.testing.assert_allclose(P[:, 0], np.sin(t), atol=1e-12)
+    np.testing.assert_allclose(P[:, 191], np.sin(t / 10000.0), atol=1e-12)
+    np.testing.assert_allclose(P[:, 383], np.cos(t / 10000.0), atol=1e-12)
+
+
+def test_encoder_fp64_equals_torch_modules():
+    """The whole fp64 encoder against torch: F.conv1d (padding 1, strides 1
+    and 2) with exact GELU, an independently built position table,
+    nn.TransformerEncoderLayer(norm_first=True, activation='gelu') holding
+    the same weights (key bias zero), and F.layer_norm."""
+    e = ENC_SMALL
+    w = synth.encoder_weights(e, 3)
+    mel = synth.mel_input(e, 3, 0)
+    ora = ENC.Encoder(e, w).encode(mel)
+    t = {k: torch.tensor(np.asarray(v, dtype=np.float64)) for k, v in w.items()}
+    x = torch.tensor(np.asarray(mel, dtype=np.float64))[None]
+    x = F.gelu(F.conv1d(x, t["conv1_w"], t["conv1_b"], stride=1, padding=1))
+    x = F.gelu(F.conv1d(x, t["conv2_w"], t["conv2_b"], stride=2, padding=1))[0].T
+    d, F_ = e.d_model, e.n_frames
+    pos = torch.arange(F_, dtype=torch.float64)[:, None]
+    inv = 10000.0 ** (-torch.arange(d // 2, dtype=torch.float64) / (d // 2 - 1))
+    x = (x + torch.cat([torch.sin(pos * inv), torch.cos(pos * inv)], dim=1))[None]
+    for l in range(e.n_layers):
+        p = f"layers.{l}."
+        layer = torch.nn.TransformerEncoderLayer(d, e.n_heads, e.d_ff, dropout=0.0, activation="gelu",
+                                                 norm_first=True, batch_first=True, dtype=torch.float64)
+        with torch.no_grad():
+            layer.self_attn.in_proj_weight.copy_(t[p + "w_qkv"])
+            layer.self_attn.in_proj_bias.copy_(torch.cat([t[p + "b_q"], torch.zeros(d, dtype=torch.float64),
+                                                          t[p + "b_v"]]))
+            layer.self_attn.out_proj.weight.copy_(t[p + "w_o"])
+            layer.self_attn.out_proj.bias.copy_(t[p + "b_o"])
+            layer.linear1.weight.copy_(t[p + "w_fc1"]); layer.linear1.bias.copy_(t[p + "b_fc1"])
+            layer.linear2.weight.copy_(t[p + "w_fc2"]); layer.linear2.bias.copy_(t[p + "b_fc2"])
+            layer.norm1.weight.copy_(t[p + "ln1_g"]); layer.norm1.bias.copy_(t[p + "ln1_b"])
+            layer.norm2.weight.copy_(t[p + "ln2_g"]); layer.norm2.bias.copy_(t[p + "ln2_b"])
+        layer.eval()
+        with torch.no_grad():
+            x = layer(x)
+    ref = F.layer_norm(x[0], (d,), t["lnp_g"], t["lnp_b"], eps=1e-5).numpy()
+    np.testing.assert_allclose(ora, ref, atol=1e-9, rtol=1e-9)
+
+
+def test_encoder_conv_stem_by_brute_force():
+    """Output position t of the stride-2 convolution reads mel frames 2t-1 ..
+    2t+1 of the first convolution's output (zero outside): one output value
+    summed term by term."""
+    e = ENC_SMALL
+    w = synth.encoder_weights(e, 4)
+    mel = np.asarray(synth.mel_input(e, 4, 1), dtype=np.float64)
+    h1 = ENC.conv1d(mel, w["conv1_w"], w["conv1_b"], 1)
+    for t, o in ((0, 5), (17, 0), (e.n_frames - 1, 127)):
+        s = float(w["conv2_b"][o])
+        for k in range(3):
+            src = 2 * t + k - 1
+            if 0 <= src < 2 * e.n_frames:
+                s += sum(float(w["conv2_w"][o, c, k]) * h1[c, src] for c in range(e.d_model))
+        assert abs(ENC.conv1d(h1, w["conv2_w"], w["conv2_b"], 2)[o, t] - s) < 1e-12
+
+
+def test_encoder_bf16_mode_stays_near_fp64():
+    """bf16 storage rounding moves the encoder output by far less than the
+    2e-2 parity tolerance (relative to the largest output)."""
+    e = synth.EncoderShape("enc-small-bf16", 2, 128, 2, 512, 16, n_frames=48, dtype="bf16")
+    w = synth.encoder_weights(e, 5)
+    mel = synth.mel_input(e, 5, 0)
+    a = ENC.Encoder(e, w, bf16=True).encode(mel)
+    b = ENC.Encoder(e, w, bf16=False).encode(mel)
+    assert np.abs(a - b).max() < 2e-2 * np.abs(b).max()
