@@ -404,6 +404,60 @@ const char* ws_last_error(const ws_ctx* ctx);
 /* Destroy the host handle (the workspace stays owned by the caller). */
 void ws_free(ws_ctx* ctx);
 
+/* ------------------------------------------------------------------------
+ * Audio encoder (the step before the decoding path: Whisper-Flash App. B.2,
+ * Table A2, once speculation removes most decoder calls the encoder takes
+ * 15-34% of request time at batch one and about half at batch 32-96).  The
+ * pages do not print its layers; this is the published Whisper audio
+ * encoder: conv1 (n_mels -> d, kernel 3, padding 1) + GELU, conv2 (d -> d,
+ * kernel 3, stride 2, padding 1) + GELU, + sinusoidal positions
+ * P[t, i] = sin(t w_i), P[t, d/2 + i] = cos(t w_i), w_i = 10000^(-i/(d/2-1)),
+ * n_layers pre-LN blocks (non-causal attention over the window's frames,
+ * GELU MLP), and a final layer norm.  bf16 weights and activations, fp32
+ * accumulation and residual stream; needs the tcgen05 engine.  Same
+ * conventions as the decoder context (caller-owned workspace, asynchronous
+ * calls, negative WS_E* codes, no aborts).
+ * ------------------------------------------------------------------------ */
+typedef struct ws_enc ws_enc;
+
+typedef struct {
+  int32_t n_layers, d_model, n_heads, d_ff;   /* large-v3: 32, 1280, 20, 5120 */
+  int32_t n_mels;                             /* 128 (large-v3), 80 (tiny) */
+  int32_t n_frames;                           /* output positions F (1500 for 30 s); input 2F mel frames */
+  int32_t max_batch;                          /* windows per ws_encode call */
+} ws_encoder_desc;
+
+/* Workspace bytes for the encoder (weights, repacked convolutions, position
+ * table, activations for max_batch windows); 0 if the description is invalid. */
+size_t ws_encoder_workspace(const ws_encoder_desc* desc);
+
+/* Create an encoder inside `workspace` (device, 256-byte aligned) and copy
+ * the bf16 weight blob (host or device) into it:
+ *   conv1_w[d, n_mels, 3] conv1_b[d] conv2_w[d, d, 3] conv2_b[d]
+ *   layer * n_layers: ln1_g[d] ln1_b[d] w_qkv[3d, d] b_q[d] b_v[d] w_o[d, d]
+ *                     b_o[d] ln2_g[d] ln2_b[d] w_fc1[f, d] b_fc1[f] w_fc2[d, f] b_fc2[d]
+ *   lnp_g[d] lnp_b[d]
+ * Convolution weights are [out, in, tap]; matrices [out, in]; no key bias.
+ * Synchronises `stream` before returning. */
+int ws_encoder_load(ws_enc** out, const ws_encoder_desc* desc, void* workspace, size_t workspace_bytes,
+                    const void* blob, ws_stream stream);
+
+/* Encode n windows (0 <= n <= max_batch).
+ *   mel  [n, n_mels, 2F] bf16 (device): log-mel features, time innermost
+ *   out  [n, F, d] bf16 (device): the encoder states A, ready for
+ *        ws_cross_kv as n packed requests of F frames each
+ * Device-side timeouts of bounded waits set the status word (ws_encoder_status). */
+int ws_encode(ws_enc* enc, int n, const void* mel, void* out, ws_stream stream);
+
+/* Synchronise `stream`, return and clear the encoder's device status word. */
+int ws_encoder_status(ws_enc* enc, ws_stream stream, int32_t* host_status);
+
+/* Last error message of enc (or of the calling thread when enc is NULL). */
+const char* ws_encoder_error(const ws_enc* enc);
+
+/* Destroy the encoder's host handle (the workspace stays owned by the caller). */
+void ws_encoder_free(ws_enc* enc);
+
 #ifdef __cplusplus
 }
 #endif

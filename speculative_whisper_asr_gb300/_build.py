@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libws.so")
 SOURCES = ["ws_api.cu", "ws_kernels.cu", "ws_attn.cu", "ws_gemm_simt.cu", "ws_gemm_tc.cu", "ws_noalloc.cu",
-           "ws_flow.cu"]
+           "ws_flow.cu", "ws_encoder.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v", "-I", os.path.join(ROOT, "include")]

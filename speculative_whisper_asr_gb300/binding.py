@@ -24,6 +24,8 @@ EXPORTS = ("ws_query_workspace", "ws_load_weights", "ws_reset", "ws_cross_kv", "
            "ws_gemm_engine", "ws_launch_count", "ws_last_error", "ws_free", "ws_capture_begin",
            "ws_capture_end", "ws_graph_launch", "ws_graph_free", "ws_argmax_rows_noalloc", "ws_fused_verify", "ws_draft_limit", "ws_set_readout", "ws_readout",
            "ws_get_centers", "ws_set_tree", "ws_tree_tokens", "ws_verify_tree",
+           "ws_encoder_workspace", "ws_encoder_load", "ws_encode", "ws_encoder_status", "ws_encoder_error",
+           "ws_encoder_free",
            "ws_fused_layernorm")
 
 
@@ -49,6 +51,11 @@ class AcceptArgs(C.Structure):
                 ("next_block", C.c_void_p), ("next_stride", C.c_int32), ("next_len", C.c_void_p),
                 ("transcript", C.c_void_p), ("out_len", C.c_void_p), ("tcap", C.c_int32),
                 ("n_done", C.c_void_p)]
+
+
+class EncoderDesc(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32), ("n_heads", C.c_int32), ("d_ff", C.c_int32),
+                ("n_mels", C.c_int32), ("n_frames", C.c_int32), ("max_batch", C.c_int32)]
 
 
 def _load():
@@ -87,6 +94,12 @@ def _load():
         "ws_set_tree": (I, [P, I, P, P]),
         "ws_tree_tokens": (I, [P, I, P, P, I, P, P, I, P, S]),
         "ws_verify_tree": (I, [P, I, P, I, P, P, P, P, S]),
+        "ws_encoder_workspace": (C.c_size_t, [C.POINTER(EncoderDesc)]),
+        "ws_encoder_load": (I, [C.POINTER(P), C.POINTER(EncoderDesc), P, C.c_size_t, P, S]),
+        "ws_encode": (I, [P, I, P, P, S]),
+        "ws_encoder_status": (I, [P, S, C.POINTER(C.c_int32)]),
+        "ws_encoder_error": (C.c_char_p, [P]),
+        "ws_encoder_free": (None, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -258,6 +271,43 @@ def ws_tree_tokens(ctx, n, req, block, stride_in, q_logits, block_out, stride_ou
 
 def ws_verify_tree(ctx, n, req_ids, H, block, block_len, target, logits, stream):
     return _check(ctx, lib.ws_verify_tree(ctx, n, req_ids, H, block, block_len, target, logits or None, stream))
+
+
+def _echeck(enc, rc: int) -> int:
+    if rc < 0:
+        raise WSError(rc, lib.ws_encoder_error(enc).decode())
+    return rc
+
+
+def make_encoder_desc(n_layers, d_model, n_heads, d_ff, n_mels, n_frames, max_batch) -> EncoderDesc:
+    d = EncoderDesc()
+    d.n_layers, d.d_model, d.n_heads, d.d_ff, d.n_mels, d.n_frames, d.max_batch = (
+        n_layers, d_model, n_heads, d_ff, n_mels, n_frames, max_batch)
+    return d
+
+
+def ws_encoder_workspace(desc: EncoderDesc) -> int:
+    return int(lib.ws_encoder_workspace(C.byref(desc)))
+
+
+def ws_encoder_load(desc: EncoderDesc, workspace: int, nbytes: int, blob: int, stream: int) -> int:
+    h = C.c_void_p()
+    _echeck(None, lib.ws_encoder_load(C.byref(h), C.byref(desc), workspace, nbytes, blob, stream))
+    return h.value
+
+
+def ws_encode(enc, n, mel, out, stream):
+    return _echeck(enc, lib.ws_encode(enc, n, mel, out, stream))
+
+
+def ws_encoder_status(enc, stream) -> int:
+    v = C.c_int32(0)
+    _echeck(enc, lib.ws_encoder_status(enc, stream, C.byref(v)))
+    return v.value
+
+
+def ws_encoder_free(enc):
+    lib.ws_encoder_free(enc)
 
 
 def ws_argmax_rows_noalloc(logits, rows, vocab, suppress, out, stream):

@@ -403,3 +403,48 @@ def run_spec_packed(dec: Decoder, req_all: torch.Tensor, budgets, synthetic=None
     if live_rounds is not None:
         live_rounds[:] = live
     return out, rounds, rows
+
+
+class Encoder:
+    """libws audio encoder on the current CUDA device (bf16): log-mel windows
+    [n, n_mels, 2F] -> encoder states [n, F, d], the input of Decoder.cross_kv."""
+
+    def __init__(self, shape: synth.EncoderShape, weights: dict, max_batch: int):
+        if not torch.cuda.is_available():
+            raise RuntimeError("libws needs a CUDA device")
+        if shape.dtype != "bf16":
+            raise ValueError("the encoder runs in bf16")
+        self.s = shape
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        self.max_batch = max_batch
+        self.desc = B.make_encoder_desc(shape.n_layers, shape.d_model, shape.n_heads, shape.d_ff, shape.n_mels,
+                                        shape.n_frames, max_batch)
+        nbytes = B.ws_encoder_workspace(self.desc)
+        if nbytes == 0:
+            raise ValueError("invalid encoder description")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+        blob = torch.from_numpy(synth.blob_from(weights, synth.encoder_tensor_shapes(shape), "bf16"))
+        blob = blob.view(torch.int16).to(self.dev)
+        self.enc = B.ws_encoder_load(self.desc, self.workspace.data_ptr(), nbytes, blob.data_ptr(), _stream())
+        del blob
+
+    def __del__(self):
+        enc = getattr(self, "enc", None)
+        if enc:
+            B.ws_encoder_free(enc)
+            self.enc = None
+
+    def mel_tensor(self, mels) -> torch.Tensor:
+        """Stack bf16-valued log-mel arrays [n_mels, 2F] into one device tensor."""
+        a = np.stack([np.asarray(m, dtype=np.float32) for m in mels])
+        return torch.from_numpy(synth.bf16_bits(a)).view(torch.int16).to(self.dev).view(torch.bfloat16)
+
+    def encode(self, mel: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+        n = mel.shape[0]
+        if out is None:
+            out = torch.empty(n, self.s.n_frames, self.s.d_model, dtype=torch.bfloat16, device=self.dev)
+        B.ws_encode(self.enc, n, mel.data_ptr(), out.data_ptr(), _stream())
+        return out
+
+    def status(self) -> int:
+        return B.ws_encoder_status(self.enc, _stream())
