@@ -15,7 +15,9 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     sample of the same workload.
 The default line also carries, under "workloads", the batch-96 sampling
 workload (large-v3, T = 0.7, rejection rule) and the batch-16 turbo workload
-of the same metric (--no-sub leaves them out).  Timed steps of the headline
+of the same metric, and the large-v3 audio encoder (the step before the
+path) at 1 and 16 windows with its share of request time (--no-sub leaves
+them out).  Timed steps of the headline
 cycle through four corruption plans, so tau is an average over plans.
 Under torchrun (N > 1) every rank decodes its own batch (weak scaling); the
 time is the max over ranks.
@@ -621,6 +623,49 @@ def run_oracle_sample(budget_tokens: int = 48):
     return len(res.tokens), dt, cores
 
 
+def encoder_flops(e: synth.EncoderShape) -> float:
+    """Algorithmic FLOPs of one window: both convolutions (3 taps), and per
+    block the q/k/v, output and FFN projections plus S = QK^T and PV."""
+    F, d, f = e.n_frames, e.d_model, e.d_ff
+    stem = 2.0 * (2 * F) * (3 * e.n_mels) * d + 2.0 * F * (3 * d) * d
+    block = 2.0 * F * (3 * d * d + d * d + 2 * d * f) + 4.0 * F * F * d
+    return stem + e.n_layers * block
+
+
+def run_encoder(args, n: int) -> dict:
+    """The large-v3 audio encoder over n 30 s windows (the step before the
+    decoding path): windows/s, and the whole encoder's tensor throughput
+    against the sustained bf16 peak."""
+    import torch
+    from speculative_whisper_asr_gb300 import runtime as R
+    e = synth.ENC_LARGE_V3
+    enc = R.Encoder(e, synth.encoder_weights(e, SEED), max_batch=n)
+    mel = enc.mel_tensor([synth.mel_input(e, SEED, i) for i in range(n)])
+    out = torch.empty(n, e.n_frames, e.d_model, dtype=torch.bfloat16, device=enc.dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        enc.encode(mel, out)
+    steps = max(1, args.steps)
+    ms, launches, clocks, _ = _timed(lambda: enc.encode(mel, out), steps, 1, stream)
+    assert enc.status() == 0
+    ms_step = ms / steps
+    _, _, src = peaks()
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+        sus = float(json.load(fh).get("bf16_tflops_sustained", 1700.0)) if src == "measured" else 1700.0
+    tf = encoder_flops(e) * n / (ms_step * 1e-3) / 1e12
+    del enc
+    torch.cuda.empty_cache()
+    return {"config": {"workload": f"large-v3-encoder-b{n}", "windows": n, "frames": e.n_frames,
+                       "mel_frames": 2 * e.n_frames, "layers": e.n_layers, "d_model": e.d_model,
+                       "weights_larger_than_l2": True},
+            "value": n * steps / (ms * 1e-3), "unit": "windows/s", "audio_s_per_s": 30.0 * n * steps / (ms * 1e-3),
+            "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_window": ms_step / n,
+            "gpu_launches": launches // steps,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": sus, "unit": "TFLOP/s", "frac": tf / sus,
+                         "peak_kind": f"{src} sustained bf16 (whole encoder, all kernels)", "traffic": None},
+            "clocks": clocks}
+
+
 def run_workload(args, rank: int, world: int, wl: Workload):
     import torch
     if wl.temperature > 0.0:
@@ -705,6 +750,16 @@ def main():
             w2 = make_workload(name)
             r2 = run_workload(sub, rank, world, w2)
             subs[name] = sub_summary(w2, sub, r2)
+        if rank == 0:
+            # the audio encoder before the path, at batch 1 and 16, and its share of request time
+            e1 = run_encoder(sub, 1)
+            e16 = run_encoder(sub, 16)
+            e1["encoder_share_b1"] = e1["ms_per_window"] / (e1["ms_per_window"] + r["ms_per_step"] / wl.n)
+            if "turbo-b16" in subs:
+                e16["encoder_share_turbo_b16"] = e16["ms_per_step"] / (e16["ms_per_step"] +
+                                                                       subs["turbo-b16"]["ms_per_step"])
+            subs["large-v3-encoder-b1"] = e1
+            subs["large-v3-encoder-b16"] = e16
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "large-v3-b1":
         tok, dt, cores = run_oracle_sample()
