@@ -21,13 +21,15 @@ __device__ __forceinline__ void rope_pair(const float* tab, int pos, int n, floa
 
 // n is even; features n and n+1 are both < N.  `z` is the batch index
 // (request) for CROSSKV, whose rows are frame indices of that request.
+// `kind` is e.kind, or the same value as a compile-time constant in a kernel
+// compiled for one epilogue kind (the other cases then drop out).
 template <typename T>
-__device__ __forceinline__ void epi_pair(const Epi& e, int r, int n, float y0, float y1, int z) {
-  switch (e.kind) {
+__device__ __forceinline__ void epi_pair(int kind, const Epi& e, int r, int n, float y0, float y1, int z) {
+  switch (kind) {
     case EPI_STORE:
     case EPI_GELU: {
       float v0 = y0 + bias_at<T>(e.bias, n), v1 = y1 + bias_at<T>(e.bias, n + 1);
-      if (e.kind == EPI_GELU) { v0 = gelu_erf(v0); v1 = gelu_erf(v1); }
+      if (kind == EPI_GELU) { v0 = gelu_erf(v0); v1 = gelu_erf(v1); }
       T* o = reinterpret_cast<T*>(e.out) + (size_t)r * e.ldo + n;
       o[0] = from_f<T>(v0); o[1] = from_f<T>(v1);
       break;
@@ -58,12 +60,12 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int r, int n, float y0, f
       bool valid = row_info(e.rm, r, slot, j, pos);
       if (part == 0) {
         y0 += bias_at<T>(e.bias, nn); y1 += bias_at<T>(e.bias, nn + 1);
-        if (e.kind == EPI_QKV_DRAFT) rope_pair(e.rope, min(pos, e.rm.max_pos - 1), nn, y0, y1);
+        if (kind == EPI_QKV_DRAFT) rope_pair(e.rope, min(pos, e.rm.max_pos - 1), nn, y0, y1);
         T* o = reinterpret_cast<T*>(e.out) + (size_t)r * e.d + nn;
         o[0] = from_f<T>(y0); o[1] = from_f<T>(y1);
       } else {
         if (part == 2) { y0 += bias_at<T>(e.bias2, nn); y1 += bias_at<T>(e.bias2, nn + 1); }
-        if (e.kind == EPI_QKV_DRAFT) {
+        if (kind == EPI_QKV_DRAFT) {
           if (part == 1) rope_pair(e.rope, min(pos, e.rm.max_pos - 1), nn, y0, y1);
           T* o = reinterpret_cast<T*>(part == 1 ? e.kout : e.vout) + (size_t)r * e.d + nn;
           o[0] = from_f<T>(y0); o[1] = from_f<T>(y1);
@@ -97,6 +99,11 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int r, int n, float y0, f
   }
 }
 
+template <typename T>
+__device__ __forceinline__ void epi_pair(const Epi& e, int r, int n, float y0, float y1, int z) {
+  epi_pair<T>(e.kind, e, r, n, y0, y1, z);
+}
+
 // LM head value of one logit: suppressed ids become -inf (Whisper-Flash
 // Appendix A.4: draft and target logits get the same token suppression).
 __device__ __forceinline__ float epi_logit(const Epi& e, int n, float y) {
@@ -109,11 +116,11 @@ __device__ __forceinline__ float epi_logit(const Epi& e, int n, float y) {
 // LOGITS reduces each row's (value, id) key over the warp before one
 // atomicMax; the other kinds pair features (n, n + 1) through a shuffle.
 // Only columns c_lo <= c < c_hi are stored.
-__device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n, int M, int z, const float* v,
+__device__ __forceinline__ void epi_columns16(int kind, const Epi& e, int N, int t, int n, int M, int z, const float* v,
                                               int c_lo = 0, int c_hi = 16) {
   const int lane = threadIdx.x & 31;
   const int mc = min(M, t + c_hi), m0 = t + c_lo;     // rows m0 <= r < mc
-  if (e.kind == EPI_LOGITS) {
+  if (kind == EPI_LOGITS) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int r = t + c;
@@ -132,7 +139,7 @@ __device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n,
     }
     return;
   }
-  if (e.kind == EPI_RESID) {
+  if (kind == EPI_RESID) {
     // residual update: the 8 (row, feature pair) residual values of this lane
     // are loaded together (one L2 round trip), then x += y + b as in epi_pair
     const int odd = lane & 1, nn = n - odd;
@@ -168,10 +175,10 @@ __device__ __forceinline__ void epi_columns16(const Epi& e, int N, int t, int n,
     const float pc1 = __shfl_xor_sync(0xffffffffu, v[c + 1], 1);
     if ((lane & 1) == 0) {
       const int r = t + c;
-      if (r >= m0 && r < mc && n + 1 < N) epi_pair<bf16>(e, r, n, v[c], pc0, z);
+      if (r >= m0 && r < mc && n + 1 < N) epi_pair<bf16>(kind, e, r, n, v[c], pc0, z);
     } else {
       const int r = t + c + 1;
-      if (r >= m0 && r < mc && n < N) epi_pair<bf16>(e, r, n - 1, pc1, v[c + 1], z);
+      if (r >= m0 && r < mc && n < N) epi_pair<bf16>(kind, e, r, n - 1, pc1, v[c + 1], z);
     }
   }
 }

@@ -61,16 +61,16 @@ struct TcParams {
 // offset of token t0 + c's cache row in a K/V page, or -1 where the token is
 // not written.  xpre (RESID, optional): the 16 residual values of this
 // thread's feature, already loaded.
-__device__ __forceinline__ bool fast_epilogue_kind(const Epi& e) {
-  return e.kind == EPI_STORE || e.kind == EPI_GELU || e.kind == EPI_CROSSKV || e.kind == EPI_QKV ||
-         (e.kind == EPI_RESID && e.hist == nullptr);
+__device__ __forceinline__ bool fast_epilogue_kind(int kind, const Epi& e) {
+  return kind == EPI_STORE || kind == EPI_GELU || kind == EPI_CROSSKV || kind == EPI_QKV ||
+         (kind == EPI_RESID && e.hist == nullptr);
 }
 
 // Bias of feature n as the fast epilogue adds it (q / v bias for QKV, none for k).
-__device__ __forceinline__ float fast_bias(const Epi& e, int n) {
-  if (e.kind == EPI_QKV || e.kind == EPI_CROSSKV) {
+__device__ __forceinline__ float fast_bias(int kind, const Epi& e, int n) {
+  if (kind == EPI_QKV || kind == EPI_CROSSKV) {
     const int part = n / e.d, nn = n - part * e.d;
-    if (e.kind == EPI_QKV) return part == 0 ? bias_at<bf16>(e.bias, nn) : part == 2 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
+    if (kind == EPI_QKV) return part == 0 ? bias_at<bf16>(e.bias, nn) : part == 2 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
     return part == 1 ? bias_at<bf16>(e.bias2, nn) : 0.0f;
   }
   return bias_at<bf16>(e.bias, n);
@@ -78,12 +78,12 @@ __device__ __forceinline__ float fast_bias(const Epi& e, int n) {
 
 // Columns c_lo <= c < c_hi of the 16 are stored (the others are another
 // CTA's share of a split-K tile).
-__device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int M, int n, int z, const float* v,
+__device__ __forceinline__ void fast_epilogue16(int kind, const Epi& e, int N, int t, int M, int n, int z, const float* v,
                                                 const int* tok, int c0, const float* xpre = nullptr,
                                                 const float* bpre = nullptr, int c_lo = 0, int c_hi = 16) {
   if (n >= N) return;
   const int cmax = min(c_hi, M - t);
-  switch (e.kind) {
+  switch (kind) {
     case EPI_STORE:
     case EPI_GELU: {
       const float b = bpre ? *bpre : bias_at<bf16>(e.bias, n);
@@ -92,7 +92,7 @@ __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int 
       for (int c = 0; c < 16; ++c) {
         if (c >= c_lo && c < cmax) {
           float y = v[c] + b;
-          if (e.kind == EPI_GELU) y = gelu_erf(y);
+          if (kind == EPI_GELU) y = gelu_erf(y);
           o[(size_t)c * e.ldo] = __float2bfloat16_rn(y);
         }
       }
@@ -146,10 +146,13 @@ __device__ __forceinline__ void fast_epilogue16(const Epi& e, int N, int t, int 
   }
 }
 
-template <int BN, int STAGES>
+// KIND >= 0: compiled for that epilogue kind only (the host picks it from
+// e.kind); -1: any kind, read from e.kind.
+template <int BN, int STAGES, int KIND>
 __global__ void __launch_bounds__(128, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcParams p,
                    Epi e) {
+  const int kind = KIND >= 0 ? KIND : e.kind;
   constexpr int B_BYTES = BN * BK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(128, 1)
   // Row count: a host value, except for the acoustic K/V GEMM whose per-request
   // frame ranges live in device memory (read only after the dependency wait).
   int M = p.M, row0 = 0;
-  const bool early = e.kind != EPI_CROSSKV;
+  const bool early = kind != EPI_CROSSKV;
   if (!early) {
     pdl_wait();
     row0 = e.cu_frames[z];
@@ -217,14 +220,14 @@ __global__ void __launch_bounds__(128, 1)
   }
   // the bias of this thread's feature is a weight: load it before the wait
   float bpre = 0.0f;
-  if (BN == 16 && active && (e.kind == EPI_RESID || e.kind == EPI_QKV || e.kind == EPI_STORE || e.kind == EPI_GELU) &&
+  if (BN == 16 && active && (kind == EPI_RESID || kind == EPI_QKV || kind == EPI_STORE || kind == EPI_GELU) &&
       f0 + warp * 32 + lane < p.N)
-    bpre = fast_bias(e, f0 + warp * 32 + lane);
+    bpre = fast_bias(kind, e, f0 + warp * 32 + lane);
   // Cache rows of the tile's tokens (QKV): positions, request slots and the
   // page table were all written before this library call began, so the
   // table is built before the dependency wait.
   __shared__ int tok_tab[16];
-  if (BN == 16 && active && e.kind == EPI_QKV && threadIdx.x < 16) {
+  if (BN == 16 && active && kind == EPI_QKV && threadIdx.x < 16) {
     int slot, j, pos, off = -1;
     const int r = t0 + (int)threadIdx.x;
     if (r < M && row_info(e.rm, r, slot, j, pos)) {
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(128, 1)
   // Epilogue inputs that do not depend on the MMAs are loaded now, while the
   // weights stream (one-token-tile calls): this thread's residual values.
   float xpre[16];
-  const bool pre_resid = BN == 16 && active && e.kind == EPI_RESID && e.hist == nullptr;
+  const bool pre_resid = BN == 16 && active && kind == EPI_RESID && e.hist == nullptr;
   if (pre_resid) {
     const int pn = f0 + warp * 32 + lane;
 #pragma unroll
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(128, 1)
       xpre[c] = (c >= c_lo && c < c_hi && t0 + c < M && pn < p.N) ? __ldcg(e.resid + (size_t)(t0 + c) * e.ldr + pn)
                                                                   : 0.0f;
   }
-  const bool fast16 = BN == 16 && (pre_resid || e.kind == EPI_QKV || e.kind == EPI_STORE || e.kind == EPI_GELU);
+  const bool fast16 = BN == 16 && (pre_resid || kind == EPI_QKV || kind == EPI_STORE || kind == EPI_GELU);
 
   if (lnin && active) {
     // B = LayerNorm(x) for token rows t0 .. t0 + 15 and this CTA's k-blocks,
@@ -327,26 +330,19 @@ __global__ void __launch_bounds__(128, 1)
   const int row = warp * 32 + lane;            // TMEM lane == weight row of the tile
   const int n = f0 + row;
   const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-  if (active && p.splits == 1 && ok) {
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      float v[16];
-      tmem_ld16(taddr + (uint32_t)c0, v);
-      if (fast16) fast_epilogue16(e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr, &bpre);
-      else epi_columns16(e, p.N, t0 + c0, n, M, z, v);
-    }
-  } else if (active && p.splits > 1) {
-    // Split-K: the splits of one tile form a thread-block cluster.  Each CTA
-    // parks its fp32 partial in its own (now idle) ring memory; after a
-    // cluster barrier every rank folds its own share of each 16-column group
-    // (columns [c_lo, c_hi)), reading the partials of ranks 0, 1, 2, ...
-    // through distributed shared memory and adding them in that order, and
-    // stores those columns; the ranks' shares are disjoint and cover the
-    // group.  Every CTA of an active cluster reaches both cluster barriers,
-    // also after a timed-out wait.
-    namespace cg = cooperative_groups;
-    cg::cluster_group cl = cg::this_cluster();
-    float* mine = reinterpret_cast<float*>(ring);
+  // Split-K: the splits of one tile form a thread-block cluster.  Each CTA
+  // parks its fp32 partial in its own (now idle) ring memory; after a
+  // cluster barrier every rank folds its own share of each 16-column group
+  // (columns [c_lo, c_hi)), reading the partials of ranks 0, 1, 2, ...
+  // through distributed shared memory and adding them in that order, and
+  // stores those columns; the ranks' shares are disjoint and cover the
+  // group.  Every CTA of an active cluster reaches both cluster barriers,
+  // also after a timed-out wait.  One epilogue call site serves both paths
+  // (the code stays small: a layer's projections all run this kernel).
+  namespace cg = cooperative_groups;
+  const bool splitk = p.splits > 1;
+  float* mine = reinterpret_cast<float*>(ring);
+  if (active && splitk) {
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
       float v[16];
@@ -354,37 +350,42 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
       for (int c = 0; c < 16; ++c) mine[(c0 + c) * BM + row] = ok ? v[c] : 0.0f;
     }
-    cl.sync();
+    cg::this_cluster().sync();
+  }
+  if (active && (splitk || ok)) {
     const float* part[8];
+    if (splitk) {
+      cg::cluster_group cl = cg::this_cluster();
 #pragma unroll
-    for (int r = 0; r < 8; ++r) part[r] = cl.map_shared_rank(mine, r < p.splits ? r : 0);
-    float v[BN / 16][16];
+      for (int r = 0; r < 8; ++r) part[r] = cl.map_shared_rank(mine, r < p.splits ? r : 0);
+    }
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      float v[16];
+      if (splitk) {
 #pragma unroll
-    for (int g = 0; g < BN / 16; ++g) {
+        for (int c = 0; c < 16; ++c) {
+          float a = 0.0f;
+          if (c >= c_lo && c < c_hi) {
+            a = part[0][(c0 + c) * BM + row];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float a = 0.0f;
-        if (c >= c_lo && c < c_hi) {
-          a = part[0][(16 * g + c) * BM + row];
-#pragma unroll
-          for (int r = 1; r < 8; ++r)
-            if (r < p.splits) a += part[r][(16 * g + c) * BM + row];
+            for (int r = 1; r < 8; ++r)
+              if (r < p.splits) a += part[r][(c0 + c) * BM + row];
+          }
+          v[c] = a;
         }
-        v[g][c] = a;
+        // the last group's reads of the others' partials are done: arrive
+        // now, and wait (for the others' reads of this CTA's partial) only
+        // before exit, so the barrier's latency overlaps the stores
+        if (c0 + 16 >= BN) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+      } else {
+        tmem_ld16(taddr + (uint32_t)c0, v);
       }
+      if (fast16) fast_epilogue16(kind, e, p.N, t0 + c0, M, n, z, v, tok_tab, c0, pre_resid ? xpre : nullptr, &bpre,
+                                  splitk ? c_lo : 0, splitk ? c_hi : 16);
+      else epi_columns16(kind, e, p.N, t0 + c0, n, M, z, v, splitk ? c_lo : 0, splitk ? c_hi : 16);
     }
-    // this CTA's reads of the others' partials are done: arrive now, and
-    // wait (for the others' reads of this CTA's partial) only before exit,
-    // so the barrier's latency overlaps the stores below
-    auto reads_done = cl.barrier_arrive();
-#pragma unroll
-    for (int g = 0; g < BN / 16; ++g) {
-      if (fast16)
-        fast_epilogue16(e, p.N, t0 + 16 * g, M, n, z, v[g], tok_tab, 16 * g, pre_resid ? xpre : nullptr, &bpre, c_lo,
-                        c_hi);
-      else epi_columns16(e, p.N, t0 + 16 * g, n, M, z, v[g], c_lo, c_hi);
-    }
-    cl.barrier_wait(std::move(reads_done));
+    if (splitk) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
@@ -397,8 +398,10 @@ __global__ void __launch_bounds__(128, 1)
 // walks tiles t = blockIdx.x, + gridDim.x, ... (feature tile fastest, so
 // the CTAs of a wave share the activation tile in L2).  Warp 0 streams
 // weight and activation tiles through the ring, warp 1 issues the MMAs into
-// one of two TMEM accumulators, warps 2..5 (TMEM lane quarters 2,3,0,1) run
-// the epilogue of tile i while the MMAs of tile i+1 proceed.  A tile's k
+// one of two TMEM accumulators, warps 2..9 run the epilogue of tile i while
+// the MMAs of tile i+1 proceed: two warps per TMEM lane quarter (a warp may
+// only read its own quarter), each taking alternate 16-column groups, so the
+// bias / GELU / residual arithmetic of a wide tile keeps pace with its MMAs.  A tile's k
 // order is that of gemm_tc_kernel, so both give bit-identical outputs.
 template <int BN>
 constexpr int persistent_stages() { return (200 * 1024) / (A_BYTES + BN * BK * 2); }
@@ -408,7 +411,7 @@ constexpr int persistent_smem() { return persistent_stages<BN>() * (A_BYTES + BN
 
 struct TileInfo { int tile_f, t0, z, row0, M; bool active; };
 
-__device__ __forceinline__ TileInfo tile_of(const TcParams& p, const Epi& e, int t, int BN) {
+__device__ __forceinline__ TileInfo tile_of(const TcParams& p, const Epi& e, int kind, int t, int BN) {
   TileInfo ti;
   ti.tile_f = t % p.tiles_f;
   const int rest = t / p.tiles_f;
@@ -417,7 +420,7 @@ __device__ __forceinline__ TileInfo tile_of(const TcParams& p, const Epi& e, int
   ti.t0 = tt * BN;
   ti.row0 = 0;
   ti.M = p.M;
-  if (e.kind == EPI_CROSSKV) {        // per-request frame ranges (device memory, read after the dependency wait)
+  if (kind == EPI_CROSSKV) {        // per-request frame ranges (device memory, read after the dependency wait)
     ti.row0 = e.cu_frames[ti.z];
     ti.M = min(e.cu_frames[ti.z + 1] - ti.row0, e.xkv.max_frames);
   }
@@ -425,10 +428,13 @@ __device__ __forceinline__ TileInfo tile_of(const TcParams& p, const Epi& e, int
   return ti;
 }
 
-template <int BN>
-__global__ void __launch_bounds__(192, 1)
+constexpr int PERSIST_THREADS = 320;        // producer, MMA issuer, 8 epilogue warps
+
+template <int BN, int KIND>
+__global__ void __launch_bounds__(PERSIST_THREADS, 1)
     gemm_tc_persistent(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcParams p,
                        Epi e) {
+  const int kind = KIND >= 0 ? KIND : e.kind;
   constexpr int STAGES = persistent_stages<BN>();
   constexpr int B_BYTES = BN * BK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(192, 1)
   const int T = p.tiles_f * p.tiles_t * p.nz;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 4); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 8); }
     issued = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tmW);
@@ -463,8 +469,8 @@ __global__ void __launch_bounds__(192, 1)
       // ---- producer.  Weights of the first tile's first slots go out before
       // the dependency wait (they do not depend on the previous kernel).
       int npre = 0;
-      if (e.kind != EPI_CROSSKV && blockIdx.x < T) {
-        const TileInfo ti = tile_of(p, e, blockIdx.x, BN);
+      if (kind != EPI_CROSSKV && blockIdx.x < T) {
+        const TileInfo ti = tile_of(p, e, kind, blockIdx.x, BN);
         if (ti.active) {
           npre = p.kb_total < STAGES ? p.kb_total : STAGES;
           for (int i = 0; i < npre; ++i) {
@@ -477,7 +483,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-        const TileInfo ti = tile_of(p, e, t, BN);
+        const TileInfo ti = tile_of(p, e, kind, t, BN);
         if (!ti.active) continue;
         for (int kb = 0; kb < p.kb_total; ++kb, ++it) {
           const int s = (int)(it % STAGES);
@@ -499,8 +505,8 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t it = 0, local = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-        if (e.kind == EPI_CROSSKV && t == (int)blockIdx.x) pdl_wait();
-        const TileInfo ti = tile_of(p, e, t, BN);
+        if (kind == EPI_CROSSKV && t == (int)blockIdx.x) pdl_wait();
+        const TileInfo ti = tile_of(p, e, kind, t, BN);
         if (!ti.active) continue;
         const uint32_t acc = local & 1u;
         if (!mbar_wait(&acc_empty[acc], ((local >> 1) & 1u) ^ 1u)) { atomicOr(p.status, WS_ST_TIMEOUT); break; }
@@ -523,19 +529,20 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ---- epilogue: warps 2..5 hold TMEM lane quarters 2, 3, 0, 1
+    // ---- epilogue: warps 2..9; warp w reads TMEM lane quarter w % 4 and
+    // the column groups 16 h, 16 h + 32, ... with h = (w - 2) / 4
     pdl_wait();
-    const int quarter = warp & 3;
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
-    const bool fast = fast_epilogue_kind(e);
+    const bool fast = fast_epilogue_kind(kind, e);
     uint32_t local = 0;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
-      const TileInfo ti = tile_of(p, e, t, BN);
+      const TileInfo ti = tile_of(p, e, kind, t, BN);
       if (!ti.active) continue;
-      if (e.kind == EPI_QKV) {
+      if (kind == EPI_QKV) {
         // cache rows of this tile's tokens (one entry per column)
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        for (int c = row; c < BN; c += 128) {
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        for (int c = row + half * 128; c < BN; c += 256) {
           int slot, j, pos, off = -1;
           const int r = ti.t0 + c;
           if (r < ti.M && row_info(e.rm, r, slot, j, pos)) {
@@ -544,7 +551,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           tok_tab[c] = off;
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, 256;" ::: "memory");
       }
       const uint32_t acc = local & 1u;
       const bool ok = mbar_wait(&acc_full[acc], (local >> 1) & 1u);
@@ -553,12 +560,12 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t taddr = tmem + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
       const int n = ti.tile_f * BM + row;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
+      for (int c0 = half * 16; c0 < BN; c0 += 32) {
         if (ti.t0 + c0 >= ti.M) break;
         float v[16];
         tmem_ld16(taddr + (uint32_t)c0, v);
-        if (fast) fast_epilogue16(e, p.N, ti.t0 + c0, ti.M, n, ti.z, v, tok_tab, c0);
-        else epi_columns16(e, p.N, ti.t0 + c0, n, ti.M, ti.z, v);
+        if (fast) fast_epilogue16(kind, e, p.N, ti.t0 + c0, ti.M, n, ti.z, v, tok_tab, c0);
+        else epi_columns16(kind, e, p.N, ti.t0 + c0, n, ti.M, ti.z, v);
       }
       tc_fence_before();
       __syncwarp();
@@ -580,13 +587,28 @@ __global__ void __launch_bounds__(192, 1)
 
 int g_sm_count = 0;
 
+// The instance for e's epilogue kind: specialised for the kinds of the
+// decoder's batch-1 LM head and the encoder's projections, else generic.
+template <int BN>
+auto persistent_for(const Epi& e) -> decltype(&gemm_tc_persistent<BN, -1>) {
+  if constexpr (BN == 16) {
+    if (e.kind == EPI_LOGITS) return gemm_tc_persistent<BN, EPI_LOGITS>;
+  }
+  if constexpr (BN >= 64) {
+    if (e.kind == EPI_STORE) return gemm_tc_persistent<BN, EPI_STORE>;
+    if (e.kind == EPI_GELU) return gemm_tc_persistent<BN, EPI_GELU>;
+    if (e.kind == EPI_RESID && e.hist == nullptr) return gemm_tc_persistent<BN, EPI_RESID>;
+  }
+  return gemm_tc_persistent<BN, -1>;
+}
+
 template <int BN>
 cudaError_t launch_persistent(const GemmShape& g, const Epi& e, const CUtensorMap& mw, const CUtensorMap& mx,
                               const TcParams& p, cudaStream_t s, bool pdl) {
   const int T = p.tiles_f * p.tiles_t * p.nz;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g_sm_count > 0 && T > g_sm_count ? g_sm_count : T);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(PERSIST_THREADS);
   cfg.dynamicSmemBytes = persistent_smem<BN>();
   cfg.stream = s;
   cudaLaunchAttribute at[1];
@@ -595,7 +617,7 @@ cudaError_t launch_persistent(const GemmShape& g, const Epi& e, const CUtensorMa
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
   ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg, gemm_tc_persistent<BN>, mw, mx, p, e);
+  return cudaLaunchKernelEx(&cfg, persistent_for<BN>(e), mw, mx, p, e);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -632,7 +654,10 @@ cudaError_t launch_bn(const GemmShape& g, const Epi& e, const CUtensorMap& mw, c
   cfg.attrs = at;
   cfg.numAttrs = na;
   ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES>, mw, mx, p, e);
+  // One instance serves every epilogue kind: the decoder's projections of a
+  // layer alternate kinds, and a single code body they share stays in the
+  // instruction caches (one instance per kind measured slower at batch 1).
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES, -1>, mw, mx, p, e);
 }
 
 }  // namespace
@@ -682,6 +707,18 @@ bool tc_encode_rows_f32(TcMap* m, const float* base, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+template <int BN>
+const void* persistent_instance(int k) {
+  switch (k) {
+    case EPI_STORE: return (const void*)gemm_tc_persistent<BN, EPI_STORE>;
+    case EPI_GELU: return (const void*)gemm_tc_persistent<BN, EPI_GELU>;
+    case EPI_RESID: return (const void*)gemm_tc_persistent<BN, EPI_RESID>;
+    default: return (const void*)gemm_tc_persistent<BN, -1>;
+  }
+}
+}  // namespace
+
 // Raise the dynamic shared-memory limit of every kernel variant once, before
 // any launch (so no attribute call happens while a stream is being captured).
 cudaError_t tc_init_attributes() {
@@ -689,14 +726,17 @@ cudaError_t tc_init_attributes() {
   auto set = [&](const void* fn, int bytes) {
     if (r == cudaSuccess) r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   };
-  set((const void*)gemm_tc_kernel<16, 5>, tc_smem<16, 5>());
-  set((const void*)gemm_tc_kernel<32, 5>, tc_smem<32, 5>());
-  set((const void*)gemm_tc_kernel<64, 4>, tc_smem<64, 4>());
-  set((const void*)gemm_tc_persistent<16>, persistent_smem<16>());
-  set((const void*)gemm_tc_persistent<32>, persistent_smem<32>());
-  set((const void*)gemm_tc_persistent<64>, persistent_smem<64>());
-  set((const void*)gemm_tc_persistent<128>, persistent_smem<128>());
-  set((const void*)gemm_tc_persistent<256>, persistent_smem<256>());
+  set((const void*)gemm_tc_kernel<16, 5, -1>, tc_smem<16, 5>());
+  set((const void*)gemm_tc_kernel<32, 5, -1>, tc_smem<32, 5>());
+  set((const void*)gemm_tc_kernel<64, 4, -1>, tc_smem<64, 4>());
+  set((const void*)gemm_tc_persistent<16, -1>, persistent_smem<16>());
+  set((const void*)gemm_tc_persistent<16, EPI_LOGITS>, persistent_smem<16>());
+  set((const void*)gemm_tc_persistent<32, -1>, persistent_smem<32>());
+  for (int k : {-1, (int)EPI_STORE, (int)EPI_GELU, (int)EPI_RESID}) {
+    set(persistent_instance<64>(k), persistent_smem<64>());
+    set(persistent_instance<128>(k), persistent_smem<128>());
+    set(persistent_instance<256>(k), persistent_smem<256>());
+  }
   if (r == cudaSuccess) {
     int dev = 0;
     r = cudaGetDevice(&dev);
