@@ -551,7 +551,8 @@ def run_profile(args):
     """Short case for kernel profilers: the workload's model and batch, its
     acoustic K/V, prefill and two warm-up rounds, then `--profile` rounds
     (or, with --profile-part cross_kv, that many acoustic K/V projections)
-    inside the NVTX range "ws_timed".  Rounds use random proposals (greedy
+    inside the NVTX range "ws_timed"; --profile-part encoder runs that many
+    encodes of --batch windows instead.  Rounds use random proposals (greedy
     workloads) or the drafter's samples (sampling workloads).
     --profile-layers L keeps the widths but builds L decoder layers, so a
     full-metric capture holds a few GB."""
@@ -561,6 +562,24 @@ def run_profile(args):
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
+    if args.profile_part == "encoder":
+        # the large-v3 audio encoder over --batch windows (--profile-layers L: its first L blocks)
+        e = synth.ENC_LARGE_V3
+        if args.profile_layers:
+            e = dataclasses.replace(e, n_layers=args.profile_layers)
+        enc = R.Encoder(e, synth.encoder_weights(e, SEED), max_batch=args.batch)
+        mel = enc.mel_tensor([synth.mel_input(e, SEED, i) for i in range(args.batch)])
+        out = enc.encode(mel)
+        enc.encode(mel, out)                  # warm-up
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("ws_timed")
+        for _ in range(args.profile):
+            enc.encode(mel, out)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        print(json.dumps({"profile_rounds": args.profile, "part": "encoder", "windows": args.batch,
+                          "layers": e.n_layers, "status": enc.status()}))
+        return
     wl = make_workload(args.workload, args.batch)
     s, n = wl.shape, wl.n
     if args.profile_layers:
@@ -700,7 +719,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub", action="store_true", help="headline workload only (no batch 16 / 96 sub-objects)")
     ap.add_argument("--profile", type=int, default=0, help="run N rounds of the profiling case and exit")
-    ap.add_argument("--profile-part", default="round", choices=["round", "cross_kv"])
+    ap.add_argument("--profile-part", default="round", choices=["round", "cross_kv", "encoder"])
     ap.add_argument("--profile-layers", type=int, default=0, help="profiling case with fewer decoder layers")
     ap.add_argument("--workload", default="large-v3-b1", choices=WORKLOADS,
                     help="large-v3-b1 is the headline; the others measure the batch 16 / 96 and varlen cases")

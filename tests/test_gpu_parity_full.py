@@ -10,7 +10,10 @@
   * speculative sampling through the bf16 drafter: the first token of a
     round follows the target's distribution (Whisper-Flash §3.1, the
     rejection rule preserves p; App. A.4), checked by chi-square against the
-    oracle's p at the same prefix.
+    oracle's p at the same prefix;
+  * bf16 sampled transcripts, autoregressive and speculative, token by token
+    against the oracle's, with the near-boundary rule widened to the
+    precision the bf16 logits measurably have.
 """
 import math
 
@@ -20,7 +23,8 @@ import torch
 
 import synth
 from oracle import model as M
-from gpu_common import dev_i32, logits_close, small_shape
+from gpu_common import (ar_sampling_from, dev_i32, logits_close, small_shape, teacher_forced_logits, tokens_match,
+                        tokens_match_resuming)
 
 pytestmark = pytest.mark.gpu
 
@@ -169,4 +173,66 @@ def test_bf16_speculative_sampling_first_token_distribution(RB):
     keep = exp > 0
     stat = float(((obs[keep] - exp[keep]) ** 2 / exp[keep]).sum())
     assert stat < chi2.ppf(1 - 1e-3, int(keep.sum()) - 1), stat
+    assert dec.status() == 0
+
+
+def test_bf16_sampling_transcripts_vs_oracle(RB):
+    """Small bf16 shape, T = 0.7, 40 tokens.  First the bf16 logit precision
+    of this model is measured: the largest |GPU - oracle| logit difference,
+    target over the oracle's own sampled transcript (teacher forced) and
+    drafter after the prompt, delta.  A logit error of delta moves a
+    probability of softmax(z / T) by a factor within exp(+-2 delta / T), so
+    a sampled decision counts as a near boundary where the oracle's
+    acceptance test u q < p sat within exp(4 delta / T) - 1 of equality (p
+    and q both move) or its inverse-CDF draw within exp(2 delta / T) - 1 of a
+    boundary (delta doubled for margin).  The autoregressive transcript is
+    compared over all 40 tokens, restarting from the oracle's token at a near
+    boundary; speculative ones (four seeds) up to their first difference,
+    which must be a near boundary, at least 40 tokens in all."""
+    R, B = RB
+    s = small_shape("bf16", vocab=500, eos_id=499, prompt=(490, 491, 492, 493))
+    tw = synth.target_weights(s, 63)
+    dw = synth.drafter_weights(s, 63, tw)
+    A = synth.encoder_states(s, 63, 0, frames=160)
+    orc = M.Oracle(s, tw, dw)
+    dec = R.Decoder(s, tw, dw, max_batch=1, max_frames=160)
+    req = dec.slots([0])
+    dec.cross_kv(req, dec.enc_tensor(A), [160])
+    T, seed, budget = 0.7, 4242, 40
+    ref = M.sampling_plain(orc, orc.new_request(A), budget, T, seed, 0)
+    toks = ref.tokens[:-1]
+    gpu = teacher_forced_logits(dec, req, s, toks)
+    ora, _ = orc.forward_full(orc.new_request(A), list(s.prompt) + toks)
+    delta = float(np.abs(gpu - ora).max())
+    b = dec.new_batch(req, [64], sampling=True)
+    b.prefill()
+    r = orc.new_request(A)
+    acc, _ = M.prefill(orc, r, 64)
+    b.block[0, 0] = acc.next_anchor
+    dec.draft(req, b.block, 1.0, 3, 1, b.q_logits)
+    delta = max(delta, float(np.abs(b.q_logits[0].cpu().numpy() - orc.draft_logits(r, acc.next_anchor)).max()))
+    assert delta < 2e-2 * 4                                # the stated bf16 tolerance, |logits| < 4 here
+    d2 = 2.0 * delta
+    ca_thr, cc_thr = math.exp(4 * d2 / T) - 1.0, math.exp(2 * d2 / T) - 1.0
+
+    def near(m):
+        ca, cc = m
+        return ca < ca_thr or cc < cc_thr
+
+    b = dec.new_batch(req, [budget], sampling=True)
+    R.run_ar_sampling(dec, b, T, seed)
+    n1, _ = tokens_match_resuming(ar_sampling_from(R, dec, req, s, budget, T, seed), ref.tokens, ref.margins, near,
+                                  first=b.transcripts()[0])
+    assert n1 == budget
+    compared = []
+    for sd in (seed, seed + 1, seed + 2, seed + 3):        # speculative: four seeds, each up to its first difference
+        b2 = dec.new_batch(req, [budget], sampling=True)
+        rounds = R.run_spec(dec, b2, temperature=T, seed=sd)
+        ref2 = M.speculative_sampling(orc, orc.new_request(A), budget, T, sd, 0)
+        n2 = tokens_match(b2.transcripts()[0], ref2.tokens, ref2.margins, near)
+        if n2 == len(ref2.tokens):
+            assert rounds == ref2.rounds
+        compared.append(n2)
+    assert sum(compared) >= budget, compared
+    print(f"bf16 sampling: delta {delta:.4f}, thresholds {ca_thr:.4f} / {cc_thr:.4f}, spec compared {compared}")
     assert dec.status() == 0
