@@ -449,6 +449,12 @@ int ws_encoder_load(ws_enc** out, const ws_encoder_desc* desc, void* workspace, 
  * Device-side timeouts of bounded waits set the status word (ws_encoder_status). */
 int ws_encode(ws_enc* enc, int n, const void* mel, void* out, ws_stream stream);
 
+/* Attention kernel of the encoder: 1 = tcgen05 flash attention (S and O in
+ * tensor memory, the default), 0 = the legacy mma.sync kernel (kept for
+ * comparison), -1 = query only.  Returns the mode in use, or WS_EINVAL for a
+ * null encoder.  Host-only. */
+int ws_encoder_attention(ws_enc* enc, int mode);
+
 /* Synchronise `stream`, return and clear the encoder's device status word. */
 int ws_encoder_status(ws_enc* enc, ws_stream stream, int32_t* host_status);
 

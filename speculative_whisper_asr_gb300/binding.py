@@ -25,7 +25,7 @@ EXPORTS = ("ws_query_workspace", "ws_load_weights", "ws_reset", "ws_cross_kv", "
            "ws_capture_end", "ws_graph_launch", "ws_graph_free", "ws_argmax_rows_noalloc", "ws_fused_verify", "ws_draft_limit", "ws_set_readout", "ws_readout",
            "ws_get_centers", "ws_set_tree", "ws_tree_tokens", "ws_verify_tree",
            "ws_encoder_workspace", "ws_encoder_load", "ws_encode", "ws_encoder_status", "ws_encoder_error",
-           "ws_encoder_free",
+           "ws_encoder_free", "ws_encoder_attention",
            "ws_fused_layernorm")
 
 
@@ -100,6 +100,7 @@ def _load():
         "ws_encoder_status": (I, [P, S, C.POINTER(C.c_int32)]),
         "ws_encoder_error": (C.c_char_p, [P]),
         "ws_encoder_free": (None, [P]),
+        "ws_encoder_attention": (I, [P, I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -304,6 +305,10 @@ def ws_encoder_status(enc, stream) -> int:
     v = C.c_int32(0)
     _echeck(enc, lib.ws_encoder_status(enc, stream, C.byref(v)))
     return v.value
+
+
+def ws_encoder_attention(enc, mode: int) -> int:
+    return _echeck(enc, lib.ws_encoder_attention(enc, mode))
 
 
 def ws_encoder_free(enc):

@@ -30,6 +30,7 @@
 
 #include "ws_attn_mma.cuh"
 #include "ws_internal.cuh"
+#include "ws_tc.cuh"
 
 struct EncLayer {
   const bf16 *w_qkv, *w_o, *w_fc1, *w_fc2;
@@ -51,6 +52,7 @@ struct ws_enc {
   float* x = nullptr;           // residual stream [B F, d]
   int32_t* status = nullptr;
   std::map<std::tuple<const void*, int, int>, TcMap> maps;   // activation maps by (base, rows, token tile)
+  int attn_tc = 1;              // attention on tcgen05 (1) or on mma.sync (0)
   std::string err;
 };
 
@@ -378,6 +380,331 @@ __global__ void __launch_bounds__(128) enc_attn_kernel(const __grid_constant__ C
   }
 }
 
+// ------------------------------------------------------------------ attention on tcgen05
+// The same attention with both products on the 5th-generation tensor cores:
+// one CTA per (128 query rows, head, window), key tiles of 64.
+//   warp 0      TMA producer (Q once; K and V tiles through two stages) and
+//               V transposer: V[key][dim] -> Vt[dim][key] in shared memory,
+//               so both products take K-major operands;
+//   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers,
+//               then O += P_{j-1} V_{j-1} (O stays in TMEM);
+//   warps 2..5  softmax, one thread per query row (TMEM lane): S_j by
+//               tcgen05.ld, scores in log2 units (x log2(e) / 8), running
+//               max m, p = 2^(s - m) written as bf16 to P_j (shared memory,
+//               the 128-byte-swizzled K-major layout), running sum l.  The
+//               max m moves only when a row's max grows by more than 8
+//               (p stays <= 256); then O is rescaled in TMEM (tcgen05.ld /
+//               st) after the previous P V has finished.  At the end
+//               O / l is stored as bf16.
+// Keys past the window are masked (p = 0).  Every wait is bounded and an
+// abort flag in shared memory ends every role's loop after a timeout.
+constexpr int FA_Q = 128, FA_K = 64;
+constexpr int FA_TILE = FA_K * WS_DH * 2;                 // one 64 x 64 bf16 tile, 8 KB
+// shared memory: Q 16 KB | K x2 | V x2 | Vt x2 | P x2 (16 KB each)
+constexpr int FA_OFF_K = 2 * FA_TILE, FA_OFF_V = FA_OFF_K + 2 * FA_TILE, FA_OFF_VT = FA_OFF_V + 2 * FA_TILE;
+constexpr int FA_OFF_P = FA_OFF_VT + 2 * FA_TILE;
+constexpr int FA_SMEM = FA_OFF_P + 2 * FA_Q * FA_K * 2 + 1024;
+constexpr uint32_t FA_TMEM_COLS = 256;                    // S0 | S1 | O
+constexpr uint32_t FA_IDESC = tc::idesc_bf16(FA_Q, FA_K);  // M 128, N 64 (both products)
+constexpr float FA_SCALE = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) in log2 units
+constexpr float FA_HOLD = 8.0f;                           // max growth (log2) before O is rescaled
+
+struct FaBars {
+  uint64_t q_full, kv_full[2], k_empty[2], v_empty[2], vt_full[2], vt_empty[2], s_full[2], s_empty[2], p_full[2],
+      pv_done[2];
+};
+
+__device__ __forceinline__ float fa_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool fa_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > tc::WAIT_BUDGET) {
+      *abort = 1;
+      atomicOr(status, WS_ST_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Warp-uniform form: lane 0 waits, the warp takes its answer.
+__device__ __forceinline__ bool fa_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = fa_wait(bar, parity, abort, status);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+__device__ __forceinline__ void fa_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+// 64 consecutive TMEM columns of this warp's 32 lanes (one wait).
+__device__ __forceinline__ void fa_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[16 * q + 0]), "=r"(r[16 * q + 1]), "=r"(r[16 * q + 2]), "=r"(r[16 * q + 3]), "=r"(r[16 * q + 4]),
+          "=r"(r[16 * q + 5]), "=r"(r[16 * q + 6]), "=r"(r[16 * q + 7]), "=r"(r[16 * q + 8]), "=r"(r[16 * q + 9]),
+          "=r"(r[16 * q + 10]), "=r"(r[16 * q + 11]), "=r"(r[16 * q + 12]), "=r"(r[16 * q + 13]),
+          "=r"(r[16 * q + 14]), "=r"(r[16 * q + 15])
+        : "r"(taddr + 16u * q));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void fa_st64(uint32_t taddr, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr + 16u * q), "r"(__float_as_uint(v[16 * q + 0])), "r"(__float_as_uint(v[16 * q + 1])),
+          "r"(__float_as_uint(v[16 * q + 2])), "r"(__float_as_uint(v[16 * q + 3])),
+          "r"(__float_as_uint(v[16 * q + 4])), "r"(__float_as_uint(v[16 * q + 5])),
+          "r"(__float_as_uint(v[16 * q + 6])), "r"(__float_as_uint(v[16 * q + 7])),
+          "r"(__float_as_uint(v[16 * q + 8])), "r"(__float_as_uint(v[16 * q + 9])),
+          "r"(__float_as_uint(v[16 * q + 10])), "r"(__float_as_uint(v[16 * q + 11])),
+          "r"(__float_as_uint(v[16 * q + 12])), "r"(__float_as_uint(v[16 * q + 13])),
+          "r"(__float_as_uint(v[16 * q + 14])), "r"(__float_as_uint(v[16 * q + 15]))
+        : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(192, 2) enc_fa_kernel(const __grid_constant__ CUtensorMap tmQKV, bf16* out, int F,
+                                                        int d, int32_t* status) {
+  extern __shared__ uint8_t fa_dsm[];
+  __shared__ __align__(8) FaBars B;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_abort;
+  __shared__ int s_issued[2];           // TMA tile copies requested per stage (producer)
+  __shared__ int s_commits[2], pv_commits[2];   // S and P V products issued per TMEM / P buffer
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fa_dsm) + 1023) & ~uintptr_t(1023));
+  const int qt = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = i * F, q0 = qt * FA_Q;
+  const int nt = (F + FA_K - 1) / FA_K;
+  const int xq = h * WS_DH, xk = d + h * WS_DH, xv = 2 * d + h * WS_DH;
+  volatile int* abort = &s_abort;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&B.q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&B.kv_full[b], 1); tc::mbar_init(&B.k_empty[b], 1); tc::mbar_init(&B.v_empty[b], 1);
+      tc::mbar_init(&B.vt_full[b], 1); tc::mbar_init(&B.vt_empty[b], 1); tc::mbar_init(&B.s_full[b], 1);
+      tc::mbar_init(&B.s_empty[b], 4); tc::mbar_init(&B.p_full[b], 4); tc::mbar_init(&B.pv_done[b], 1);
+    }
+    s_abort = 0;
+    s_issued[0] = s_issued[1] = 0;
+    s_commits[0] = s_commits[1] = pv_commits[0] = pv_commits[1] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::tma_prefetch_desc(&tmQKV);
+  }
+  if (warp == 1) tc::tmem_alloc(&tmem_base, FA_TMEM_COLS);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  uint8_t* sQ = sm;
+  auto sK = [&](int b) { return sm + FA_OFF_K + b * FA_TILE; };
+  auto sV = [&](int b) { return sm + FA_OFF_V + b * FA_TILE; };
+  auto sVt = [&](int b) { return sm + FA_OFF_VT + b * FA_TILE; };
+  auto sP = [&](int b) { return sm + FA_OFF_P + b * (FA_Q * FA_K * 2); };
+
+  if (warp == 0) {
+    // ---- producer and V transposer
+    auto load_kv = [&](int j) {
+      const int b = j & 1;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic reads of the stage first
+      tc::mbar_expect_tx(&B.kv_full[b], 2 * FA_TILE);
+      tc::tma_load_2d(sK(b), &tmQKV, &B.kv_full[b], xk, row0 + j * FA_K);
+      tc::tma_load_2d(sV(b), &tmQKV, &B.kv_full[b], xv, row0 + j * FA_K);
+      ++s_issued[b];
+    };
+    if (lane == 0) {
+      tc::mbar_expect_tx(&B.q_full, 2 * FA_TILE);
+      tc::tma_load_2d(sQ, &tmQKV, &B.q_full, xq, row0 + q0);
+      tc::tma_load_2d(sQ + FA_TILE, &tmQKV, &B.q_full, xq, row0 + q0 + 64);
+      load_kv(0);
+      if (nt > 1) load_kv(1);
+    }
+    __syncwarp();
+    for (int j = 0; j < nt; ++j) {
+      const int b = j & 1;
+      const uint32_t ph = (uint32_t)((j >> 1) & 1);
+      if (!fa_wait_warp(&B.kv_full[b], ph, abort, status)) break;
+      if (j >= 2 && !fa_wait_warp(&B.vt_empty[b], ph ^ 1u, abort, status)) break;    // P V of tile j - 2 done
+      // transpose: 16 ldmatrix.x4.trans of 8 x 8 blocks (key block kb, dim chunk c)
+      const uint32_t vsrc = tc::smem_u32(sV(b));
+      uint8_t* vt = sVt(b);
+      const int qm = lane >> 3, r = lane & 7;
+#pragma unroll 4
+      for (int it = 0; it < 16; ++it) {
+        const int blk = it * 4 + qm, kb = blk >> 3, cc = blk & 7;
+        uint32_t t0, t1, t2, t3;
+        ldsm_x4_t(vsrc + (uint32_t)((kb * 8 + r) * 128 + ((cc ^ r) << 4)), t0, t1, t2, t3);
+        const uint32_t tv[4] = {t0, t1, t2, t3};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int bq = it * 4 + q, kbq = bq >> 3, cq = bq & 7;
+          const int n = cq * 8 + (lane >> 2);                          // Vt row = head dim
+          *reinterpret_cast<uint32_t*>(vt + n * 128 + ((kbq ^ (n & 7)) << 4) + 4 * (lane & 3)) = tv[q];
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");      // Vt visible to the tensor core
+      __syncwarp();
+      if (lane == 0) { fa_arrive(&B.vt_full[b]); fa_arrive(&B.v_empty[b]); }
+      // refill this stage with tile j + 2 once S_j has read K_j
+      if (j + 2 < nt) {
+        bool ok = true;
+        if (lane == 0) ok = fa_wait(&B.k_empty[b], ph, abort, status) && fa_wait(&B.v_empty[b], ph, abort, status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) load_kv(j + 2);
+        __syncwarp();
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      const uint64_t qd = tc::sdesc_sw128(tc::smem_u32(sQ));
+      bool ok = fa_wait(&B.q_full, 0, abort, status);
+      auto issue_s = [&](int j) -> bool {
+        const int b = j & 1;
+        const uint32_t ph = (uint32_t)((j >> 1) & 1);
+        if (!fa_wait(&B.kv_full[b], ph, abort, status)) return false;
+        if (j >= 2 && !fa_wait(&B.s_empty[b], ph ^ 1u, abort, status)) return false;   // S_{j-2} read
+        tc::tc_fence_after();
+        const uint64_t kd = tc::sdesc_sw128(tc::smem_u32(sK(b)));
+#pragma unroll
+        for (int kk = 0; kk < WS_DH / 16; ++kk)
+          tc::umma_bf16(tmem + (uint32_t)(b * FA_K), qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), FA_IDESC,
+                        kk ? 1u : 0u);
+        tc::umma_commit(&B.s_full[b]);
+        tc::umma_commit(&B.k_empty[b]);
+        ++s_commits[b];
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < nt && ok; ++j) {
+        if (j + 1 < nt && !issue_s(j + 1)) break;
+        const int b = j & 1;
+        const uint32_t ph = (uint32_t)((j >> 1) & 1);
+        if (!fa_wait(&B.p_full[b], ph, abort, status) || !fa_wait(&B.vt_full[b], ph, abort, status)) break;
+        tc::tc_fence_after();
+        const uint64_t pd = tc::sdesc_sw128(tc::smem_u32(sP(b))), vd = tc::sdesc_sw128(tc::smem_u32(sVt(b)));
+#pragma unroll
+        for (int kk = 0; kk < FA_K / 16; ++kk)
+          tc::umma_bf16(tmem + 128u, pd + (uint64_t)(kk * 2), vd + (uint64_t)(kk * 2), FA_IDESC, (j | kk) ? 1u : 0u);
+        tc::umma_commit(&B.pv_done[b]);
+        tc::umma_commit(&B.vt_empty[b]);
+        ++pv_commits[b];
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31
+    const int quarter = warp & 3, row = quarter * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int b = j & 1;
+      const uint32_t ph = (uint32_t)((j >> 1) & 1);
+      if (!fa_wait_warp(&B.s_full[b], ph, abort, status)) { ok = false; break; }
+      tc::tc_fence_after();
+      float sv[64];
+      fa_ld64(tl + (uint32_t)(b * FA_K), sv);
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) fa_arrive(&B.s_empty[b]);
+      const int nvis = min(FA_K, F - j * FA_K);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        sv[k] = k < nvis ? sv[k] * FA_SCALE : -INFINITY;
+        mx = fmaxf(mx, sv[k]);
+      }
+      // the running max moves on the first tile, or when it grew by more than FA_HOLD
+      const bool move = j == 0 || mx > m + FA_HOLD;
+      const float mnew = move ? fmaxf(m, mx) : m;
+      const float alpha = (j == 0) ? 0.0f : fa_ex2(m - mnew);    // 1 when the max stays
+      m = mnew;
+      float sum = 0.0f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int k = 0; k < 64; k += 2) {
+        const float p0 = fa_ex2(sv[k] - m), p1 = fa_ex2(sv[k + 1] - m);
+        const __nv_bfloat162 hp = __floats2bfloat162_rn(p0, p1);
+        const float2 hf = __bfloat1622float2(hp);
+        sum += hf.x + hf.y;                                      // the weights P V uses
+        pk[k / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+      }
+      l = l * alpha + sum;
+      // P_j's buffer was last read by P V of tile j - 2
+      if (j >= 2 && !fa_wait_warp(&B.pv_done[b], ph ^ 1u, abort, status)) { ok = false; break; }
+      if (j >= 1 && __any_sync(0xffffffffu, move)) {
+        // rescale O: its last update (P V of tile j - 1) must be complete
+        if (!fa_wait_warp(&B.pv_done[b ^ 1], (uint32_t)(((j - 1) >> 1) & 1), abort, status)) { ok = false; break; }
+        tc::tc_fence_after();
+        float ov[64];
+        fa_ld64(tl + 128u, ov);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) ov[c] *= alpha;
+        fa_st64(tl + 128u, ov);
+      }
+      uint8_t* prow = sP(b) + row * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) fa_arrive(&B.p_full[b]);
+    }
+    if (ok) {
+      const int jl = nt - 1;
+      ok = fa_wait_warp(&B.pv_done[jl & 1], (uint32_t)((jl >> 1) & 1), abort, status);
+    }
+    if (ok) {
+      tc::tc_fence_after();
+      float ov[64];
+      fa_ld64(tl + 128u, ov);
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      if (q0 + row < F) {
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)(row0 + q0 + row) * d + h * WS_DH);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float* o8 = ov + 8 * c;
+          dst[c] = make_uint4(pack_bf16(o8[0] * inv, o8[1] * inv), pack_bf16(o8[2] * inv, o8[3] * inv),
+                              pack_bf16(o8[4] * inv, o8[5] * inv), pack_bf16(o8[6] * inv, o8[7] * inv));
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort) {
+    // after a timeout: copies requested and products issued complete (bounded) before the CTA exits
+    for (int b = 0; b < 2; ++b) {
+      if (s_issued[b] > 0) tc::mbar_wait(&B.kv_full[b], (uint32_t)((s_issued[b] - 1) & 1));
+      if (s_commits[b] > 0) tc::mbar_wait(&B.s_full[b], (uint32_t)((s_commits[b] - 1) & 1));
+      if (pv_commits[b] > 0) tc::mbar_wait(&B.pv_done[b], (uint32_t)((pv_commits[b] - 1) & 1));
+    }
+    tc::mbar_wait(&B.q_full, 0);
+  }
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, FA_TMEM_COLS);
+}
+
 // ------------------------------------------------------------------ host helpers
 const TcMap* act_map(ws_enc* e, const void* base, int rows, int cols, int bn) {
   auto key = std::make_tuple(base, rows, bn);
@@ -499,6 +826,7 @@ int ws_encoder_load(ws_enc** out, const ws_encoder_desc* desc, void* workspace, 
   if (!ok) { efail(e, WS_ECUDA, "tensor map encoding failed"); return bail(WS_ECUDA); }
   r = tc_init_attributes();
   if (r == cudaSuccess) r = cudaFuncSetAttribute(enc_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, EA_SMEM);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(enc_fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FA_SMEM);
   if (r != cudaSuccess) { efail(e, WS_ECUDA, "kernel attributes: %s", cudaGetErrorString(r)); return bail(WS_ECUDA); }
   *out = e;
   return WS_OK;
@@ -538,9 +866,14 @@ int ws_encode(ws_enc* e, int n, const void* mel, void* out, ws_stream stream) {
     ep = epi_of(e, EPI_STORE);
     ep.bias = L.b_qkv; ep.out = e->qkv; ep.ldo = 3 * D;
     ECK(enc_gemm(e, e->h, M, L.w_qkv, L.m_qkv, 3 * D, D, ep, s));
-    c = cfg_of(dim3(qtiles, D / WS_DH, n), dim3(128), EA_SMEM, s);
-    ECK(cudaLaunchKernelEx(&c, enc_attn_kernel, *reinterpret_cast<const CUtensorMap*>(mq), (const bf16*)e->qkv,
-                           e->ao, F, D, e->status));
+    if (e->attn_tc) {
+      c = cfg_of(dim3((F + FA_Q - 1) / FA_Q, D / WS_DH, n), dim3(192), FA_SMEM, s);
+      ECK(cudaLaunchKernelEx(&c, enc_fa_kernel, *reinterpret_cast<const CUtensorMap*>(mq), e->ao, F, D, e->status));
+    } else {
+      c = cfg_of(dim3(qtiles, D / WS_DH, n), dim3(128), EA_SMEM, s);
+      ECK(cudaLaunchKernelEx(&c, enc_attn_kernel, *reinterpret_cast<const CUtensorMap*>(mq), (const bf16*)e->qkv,
+                             e->ao, F, D, e->status));
+    }
     ws_count_launches(1);
     ep = epi_of(e, EPI_RESID);
     ep.bias = L.b_o; ep.resid = e->x; ep.ldr = D;
@@ -568,6 +901,12 @@ int ws_encoder_status(ws_enc* e, ws_stream stream, int32_t* host_status) {
   if (host_status) *host_status = v;
   if (v) return efail(e, WS_EDEVICE, "device status 0x%x (8 = a bounded wait ran out)", v);
   return WS_OK;
+}
+
+int ws_encoder_attention(ws_enc* e, int mode) {
+  if (!e) return efail(nullptr, WS_EINVAL, "null encoder");
+  if (mode == 0 || mode == 1) e->attn_tc = mode;
+  return e->attn_tc;
 }
 
 const char* ws_encoder_error(const ws_enc* e) { return e ? e->err.c_str() : g_enc_err.c_str(); }

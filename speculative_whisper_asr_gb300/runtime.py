@@ -448,3 +448,7 @@ class Encoder:
 
     def status(self) -> int:
         return B.ws_encoder_status(self.enc, _stream())
+
+    def set_attention(self, tcgen05: bool):
+        """Attention kernel: tcgen05 flash attention (default) or the legacy mma.sync one."""
+        B.ws_encoder_attention(self.enc, 1 if tcgen05 else 0)

@@ -61,3 +61,24 @@ def test_large_v3_width_two_layers_vs_oracle(R):
     s = synth.EncoderShape("large-v3-encoder-2l", 2, 1280, 20, 5120, 128)
     w, mels, got = _run(R, s, 9, 1)
     logits_close(got[0], ENC.Encoder(s, w).encode(mels[0]), 2e-2)
+
+
+def test_tcgen05_and_legacy_attention_agree_with_oracle(R):
+    """The tcgen05 flash attention (default) and the legacy mma.sync kernel
+    both match the oracle on two 100-frame windows (key tiles of 64 and 128
+    query rows cross the windows' ends)."""
+    s = synth.EncoderShape("tiny-encoder-100", 2, 384, 6, 1536, 80, n_frames=100)
+    w = synth.encoder_weights(s, 12)
+    mels = [synth.mel_input(s, 12, i) for i in range(2)]
+    enc = R.Encoder(s, w, max_batch=2)
+    mel = enc.mel_tensor(mels)
+    outs = []
+    for tc in (True, False):
+        enc.set_attention(tc)
+        outs.append(enc.encode(mel).float().cpu().numpy())
+    assert enc.status() == 0
+    orc = ENC.Encoder(s, w)
+    for i in range(2):
+        ref = orc.encode(mels[i])
+        logits_close(outs[0][i], ref, 2e-2)
+        logits_close(outs[1][i], ref, 2e-2)
