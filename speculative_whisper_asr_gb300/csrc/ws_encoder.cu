@@ -382,16 +382,20 @@ __global__ void __launch_bounds__(128) enc_attn_kernel(const __grid_constant__ C
 
 // ------------------------------------------------------------------ attention on tcgen05
 // The same attention with both products on the 5th-generation tensor cores:
-// one CTA per (128 query rows, head, window), key tiles of 64.
-//   warp 0      TMA producer (Q once; K and V tiles through two stages) and
-//               V transposer: V[key][dim] -> Vt[dim][key] in shared memory,
-//               so both products take K-major operands;
+// one CTA per (128 query rows, head, window), key tiles of 64; two CTAs
+// share an SM.
+//   warp 0      TMA producer of Q (once) and the K tiles (three stages);
+//   warp 6      TMA producer of the V tiles (two stages) and V transposer:
+//               V[key][dim] -> Vt[dim][key] in shared memory (ldmatrix /
+//               stmatrix.trans), so both products take K-major operands;
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers,
 //               then O += P_{j-1} V_{j-1} (O stays in TMEM);
 //   warps 2..5  softmax, one thread per query row (TMEM lane): S_j by
 //               tcgen05.ld, scores in log2 units (x log2(e) / 8), running
 //               max m, p = 2^(s - m) written as bf16 to P_j (shared memory,
-//               the 128-byte-swizzled K-major layout), running sum l.  The
+//               the 128-byte-swizzled K-major layout), running sum l of the
+//               fp32 weights (their bf16 rounding moves a row's output by
+//               ~2^-9 relative at most).  The
 //               max m moves only when a row's max grows by more than 8
 //               (p stays <= 256); then O is rescaled in TMEM (tcgen05.ld /
 //               st) after the previous P V has finished.  At the end
@@ -400,9 +404,13 @@ __global__ void __launch_bounds__(128) enc_attn_kernel(const __grid_constant__ C
 // abort flag in shared memory ends every role's loop after a timeout.
 constexpr int FA_Q = 128, FA_K = 64;
 constexpr int FA_TILE = FA_K * WS_DH * 2;                 // one 64 x 64 bf16 tile, 8 KB
-// shared memory: Q 16 KB | K x2 | V x2 | Vt x2 | P x2 (16 KB each)
-constexpr int FA_OFF_K = 2 * FA_TILE, FA_OFF_V = FA_OFF_K + 2 * FA_TILE, FA_OFF_VT = FA_OFF_V + 2 * FA_TILE;
-constexpr int FA_OFF_P = FA_OFF_VT + 2 * FA_TILE;
+// shared memory: Q 16 KB | K x3 | V x2 | Vt x2 (8 KB each) | P x2 (16 KB each).
+// K tiles are the critical operand (S waits for them), so they get three
+// stages and a producer of their own.
+constexpr int FA_NK = 3, FA_NV = 2, FA_NVT = 2;
+constexpr int FA_THREADS = 224;                           // K producer, MMA, 4 softmax, V producer + transposer
+constexpr int FA_OFF_K = 2 * FA_TILE, FA_OFF_V = FA_OFF_K + FA_NK * FA_TILE, FA_OFF_VT = FA_OFF_V + FA_NV * FA_TILE;
+constexpr int FA_OFF_P = FA_OFF_VT + FA_NVT * FA_TILE;
 constexpr int FA_SMEM = FA_OFF_P + 2 * FA_Q * FA_K * 2 + 1024;
 constexpr uint32_t FA_TMEM_COLS = 256;                    // S0 | S1 | O
 constexpr uint32_t FA_IDESC = tc::idesc_bf16(FA_Q, FA_K);  // M 128, N 64 (both products)
@@ -410,8 +418,8 @@ constexpr float FA_SCALE = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) in log2 
 constexpr float FA_HOLD = 8.0f;                           // max growth (log2) before O is rescaled
 
 struct FaBars {
-  uint64_t q_full, kv_full[2], k_empty[2], v_empty[2], vt_full[2], vt_empty[2], s_full[2], s_empty[2], p_full[2],
-      pv_done[2];
+  uint64_t q_full, k_full[FA_NK], k_empty[FA_NK], v_full[FA_NV], vt_full[FA_NVT], vt_empty[FA_NVT], s_full[2],
+      s_empty[2], p_full[2], pv_done[2];
 };
 
 __device__ __forceinline__ float fa_ex2(float x) {
@@ -479,13 +487,13 @@ __device__ __forceinline__ void fa_st64(uint32_t taddr, const float* v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(192, 2) enc_fa_kernel(const __grid_constant__ CUtensorMap tmQKV, bf16* out, int F,
+__global__ void __launch_bounds__(FA_THREADS, 2) enc_fa_kernel(const __grid_constant__ CUtensorMap tmQKV, bf16* out, int F,
                                                         int d, int32_t* status) {
   extern __shared__ uint8_t fa_dsm[];
   __shared__ __align__(8) FaBars B;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
-  __shared__ int s_issued[2];           // TMA tile copies requested per stage (producer)
+  __shared__ int k_issued[FA_NK], v_issued[FA_NV];   // K / V tile copies requested per stage
   __shared__ int s_commits[2], pv_commits[2];   // S and P V products issued per TMEM / P buffer
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fa_dsm) + 1023) & ~uintptr_t(1023));
   const int qt = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
@@ -496,13 +504,14 @@ __global__ void __launch_bounds__(192, 2) enc_fa_kernel(const __grid_constant__ 
   volatile int* abort = &s_abort;
   if (threadIdx.x == 0) {
     tc::mbar_init(&B.q_full, 1);
+    for (int b = 0; b < FA_NK; ++b) { tc::mbar_init(&B.k_full[b], 1); tc::mbar_init(&B.k_empty[b], 1); k_issued[b] = 0; }
+    for (int b = 0; b < FA_NV; ++b) { tc::mbar_init(&B.v_full[b], 1); v_issued[b] = 0; }
     for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(&B.kv_full[b], 1); tc::mbar_init(&B.k_empty[b], 1); tc::mbar_init(&B.v_empty[b], 1);
-      tc::mbar_init(&B.vt_full[b], 1); tc::mbar_init(&B.vt_empty[b], 1); tc::mbar_init(&B.s_full[b], 1);
+      tc::mbar_init(&B.s_full[b], 1);
       tc::mbar_init(&B.s_empty[b], 4); tc::mbar_init(&B.p_full[b], 4); tc::mbar_init(&B.pv_done[b], 1);
     }
+    for (int b = 0; b < FA_NVT; ++b) { tc::mbar_init(&B.vt_full[b], 1); tc::mbar_init(&B.vt_empty[b], 1); }
     s_abort = 0;
-    s_issued[0] = s_issued[1] = 0;
     s_commits[0] = s_commits[1] = pv_commits[0] = pv_commits[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tc::tma_prefetch_desc(&tmQKV);
@@ -519,57 +528,59 @@ __global__ void __launch_bounds__(192, 2) enc_fa_kernel(const __grid_constant__ 
   auto sP = [&](int b) { return sm + FA_OFF_P + b * (FA_Q * FA_K * 2); };
 
   if (warp == 0) {
-    // ---- producer and V transposer
-    auto load_kv = [&](int j) {
-      const int b = j & 1;
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic reads of the stage first
-      tc::mbar_expect_tx(&B.kv_full[b], 2 * FA_TILE);
-      tc::tma_load_2d(sK(b), &tmQKV, &B.kv_full[b], xk, row0 + j * FA_K);
-      tc::tma_load_2d(sV(b), &tmQKV, &B.kv_full[b], xv, row0 + j * FA_K);
-      ++s_issued[b];
-    };
+    // ---- Q and K producer (one lane): K tile j waits only for S_{j-3}
     if (lane == 0) {
       tc::mbar_expect_tx(&B.q_full, 2 * FA_TILE);
       tc::tma_load_2d(sQ, &tmQKV, &B.q_full, xq, row0 + q0);
       tc::tma_load_2d(sQ + FA_TILE, &tmQKV, &B.q_full, xq, row0 + q0 + 64);
-      load_kv(0);
-      if (nt > 1) load_kv(1);
+      for (int j = 0; j < nt; ++j) {
+        const int kb = j % FA_NK;
+        if (j >= FA_NK && !fa_wait(&B.k_empty[kb], (uint32_t)(((j / FA_NK) & 1) ^ 1), abort, status)) break;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc::mbar_expect_tx(&B.k_full[kb], FA_TILE);
+        tc::tma_load_2d(sK(kb), &tmQKV, &B.k_full[kb], xk, row0 + j * FA_K);
+        ++k_issued[kb];
+      }
     }
     __syncwarp();
+  } else if (warp == 6) {
+    // ---- V producer and transposer: V tile j + 2 refills the stage of V_j
+    // once V_j is transposed; V_j waits for the Vt buffer of P V_{j-2}
+    auto load_v = [&](int j) {
+      const int b = j % FA_NV;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the transposer's reads of the stage first
+      tc::mbar_expect_tx(&B.v_full[b], FA_TILE);
+      tc::tma_load_2d(sV(b), &tmQKV, &B.v_full[b], xv, row0 + j * FA_K);
+      ++v_issued[b];
+    };
+    if (lane == 0)
+      for (int j = 0; j < FA_NV && j < nt; ++j) load_v(j);
+    __syncwarp();
     for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      const uint32_t ph = (uint32_t)((j >> 1) & 1);
-      if (!fa_wait_warp(&B.kv_full[b], ph, abort, status)) break;
-      if (j >= 2 && !fa_wait_warp(&B.vt_empty[b], ph ^ 1u, abort, status)) break;    // P V of tile j - 2 done
-      // transpose: 16 ldmatrix.x4.trans of 8 x 8 blocks (key block kb, dim chunk c)
-      const uint32_t vsrc = tc::smem_u32(sV(b));
-      uint8_t* vt = sVt(b);
+      const int b = j % FA_NV, bt = j % FA_NVT;
+      if (!fa_wait_warp(&B.v_full[b], (uint32_t)((j / FA_NV) & 1), abort, status)) break;
+      if (j >= FA_NVT && !fa_wait_warp(&B.vt_empty[bt], (uint32_t)(((j / FA_NVT) & 1) ^ 1), abort, status)) break;
+      // transpose by 8 x 8 blocks: ldmatrix.x4 reads four blocks of V (rows =
+      // keys), stmatrix.x4.trans writes them as rows of Vt (rows = head dims)
+      const uint32_t vsrc = tc::smem_u32(sV(b)), vdst = tc::smem_u32(sVt(bt));
       const int qm = lane >> 3, r = lane & 7;
 #pragma unroll 4
       for (int it = 0; it < 16; ++it) {
-        const int blk = it * 4 + qm, kb = blk >> 3, cc = blk & 7;
+        const int blk = it * 4 + qm, kb = blk >> 3, cc = blk & 7;    // key block kb, dim chunk cc
         uint32_t t0, t1, t2, t3;
-        ldsm_x4_t(vsrc + (uint32_t)((kb * 8 + r) * 128 + ((cc ^ r) << 4)), t0, t1, t2, t3);
-        const uint32_t tv[4] = {t0, t1, t2, t3};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int bq = it * 4 + q, kbq = bq >> 3, cq = bq & 7;
-          const int n = cq * 8 + (lane >> 2);                          // Vt row = head dim
-          *reinterpret_cast<uint32_t*>(vt + n * 128 + ((kbq ^ (n & 7)) << 4) + 4 * (lane & 3)) = tv[q];
-        }
+        ldsm_x4(vsrc + (uint32_t)((kb * 8 + r) * 128 + ((cc ^ r) << 4)), t0, t1, t2, t3);
+        const int n = cc * 8 + r;                                    // Vt row (head dim) this lane addresses
+        const uint32_t dst = vdst + (uint32_t)(n * 128 + ((kb ^ (n & 7)) << 4));
+        asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};"
+                     ::"r"(dst), "r"(t0), "r"(t1), "r"(t2), "r"(t3) : "memory");
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");      // Vt visible to the tensor core
       __syncwarp();
-      if (lane == 0) { fa_arrive(&B.vt_full[b]); fa_arrive(&B.v_empty[b]); }
-      // refill this stage with tile j + 2 once S_j has read K_j
-      if (j + 2 < nt) {
-        bool ok = true;
-        if (lane == 0) ok = fa_wait(&B.k_empty[b], ph, abort, status) && fa_wait(&B.v_empty[b], ph, abort, status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (lane == 0) load_kv(j + 2);
-        __syncwarp();
+      if (lane == 0) {
+        fa_arrive(&B.vt_full[bt]);
+        if (j + FA_NV < nt) load_v(j + FA_NV);
       }
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ---- MMA issuer
@@ -577,18 +588,18 @@ __global__ void __launch_bounds__(192, 2) enc_fa_kernel(const __grid_constant__ 
       const uint64_t qd = tc::sdesc_sw128(tc::smem_u32(sQ));
       bool ok = fa_wait(&B.q_full, 0, abort, status);
       auto issue_s = [&](int j) -> bool {
-        const int b = j & 1;
+        const int b = j & 1, kb = j % FA_NK;
         const uint32_t ph = (uint32_t)((j >> 1) & 1);
-        if (!fa_wait(&B.kv_full[b], ph, abort, status)) return false;
+        if (!fa_wait(&B.k_full[kb], (uint32_t)((j / FA_NK) & 1), abort, status)) return false;
         if (j >= 2 && !fa_wait(&B.s_empty[b], ph ^ 1u, abort, status)) return false;   // S_{j-2} read
         tc::tc_fence_after();
-        const uint64_t kd = tc::sdesc_sw128(tc::smem_u32(sK(b)));
+        const uint64_t kd = tc::sdesc_sw128(tc::smem_u32(sK(kb)));
 #pragma unroll
         for (int kk = 0; kk < WS_DH / 16; ++kk)
           tc::umma_bf16(tmem + (uint32_t)(b * FA_K), qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), FA_IDESC,
                         kk ? 1u : 0u);
         tc::umma_commit(&B.s_full[b]);
-        tc::umma_commit(&B.k_empty[b]);
+        tc::umma_commit(&B.k_empty[kb]);
         ++s_commits[b];
         return true;
       };
@@ -597,14 +608,17 @@ __global__ void __launch_bounds__(192, 2) enc_fa_kernel(const __grid_constant__ 
         if (j + 1 < nt && !issue_s(j + 1)) break;
         const int b = j & 1;
         const uint32_t ph = (uint32_t)((j >> 1) & 1);
-        if (!fa_wait(&B.p_full[b], ph, abort, status) || !fa_wait(&B.vt_full[b], ph, abort, status)) break;
+        const int bt = j % FA_NVT;
+        if (!fa_wait(&B.p_full[b], ph, abort, status) ||
+            !fa_wait(&B.vt_full[bt], (uint32_t)((j / FA_NVT) & 1), abort, status))
+          break;
         tc::tc_fence_after();
-        const uint64_t pd = tc::sdesc_sw128(tc::smem_u32(sP(b))), vd = tc::sdesc_sw128(tc::smem_u32(sVt(b)));
+        const uint64_t pd = tc::sdesc_sw128(tc::smem_u32(sP(b))), vd = tc::sdesc_sw128(tc::smem_u32(sVt(bt)));
 #pragma unroll
         for (int kk = 0; kk < FA_K / 16; ++kk)
           tc::umma_bf16(tmem + 128u, pd + (uint64_t)(kk * 2), vd + (uint64_t)(kk * 2), FA_IDESC, (j | kk) ? 1u : 0u);
         tc::umma_commit(&B.pv_done[b]);
-        tc::umma_commit(&B.vt_empty[b]);
+        tc::umma_commit(&B.vt_empty[bt]);
         ++pv_commits[b];
       }
     }
@@ -626,27 +640,35 @@ __global__ void __launch_bounds__(192, 2) enc_fa_kernel(const __grid_constant__ 
       __syncwarp();
       if (lane == 0) fa_arrive(&B.s_empty[b]);
       const int nvis = min(FA_K, F - j * FA_K);
-      float mx = -INFINITY;
+      if (nvis < FA_K) {                                         // the window's last tile
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        sv[k] = k < nvis ? sv[k] * FA_SCALE : -INFINITY;
-        mx = fmaxf(mx, sv[k]);
+        for (int k = 0; k < 64; ++k) sv[k] = k < nvis ? sv[k] : -INFINITY;
       }
+      // row max of the raw scores: eight independent chains
+      float mx8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx8[q] = sv[q];
+#pragma unroll
+      for (int k = 8; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * FA_SCALE;
       // the running max moves on the first tile, or when it grew by more than FA_HOLD
       const bool move = j == 0 || mx > m + FA_HOLD;
       const float mnew = move ? fmaxf(m, mx) : m;
       const float alpha = (j == 0) ? 0.0f : fa_ex2(m - mnew);    // 1 when the max stays
       m = mnew;
-      float sum = 0.0f;
+      // p = 2^(s * scale - m): one FFMA and one EX2 per score; eight partial sums
+      float sum8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sum8[q] = 0.0f;
       uint32_t pk[32];
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
-        const float p0 = fa_ex2(sv[k] - m), p1 = fa_ex2(sv[k + 1] - m);
-        const __nv_bfloat162 hp = __floats2bfloat162_rn(p0, p1);
-        const float2 hf = __bfloat1622float2(hp);
-        sum += hf.x + hf.y;                                      // the weights P V uses
-        pk[k / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+        const float p0 = fa_ex2(fmaf(sv[k], FA_SCALE, -m)), p1 = fa_ex2(fmaf(sv[k + 1], FA_SCALE, -m));
+        sum8[(k >> 1) & 7] += p0 + p1;
+        pk[k / 2] = pack_bf16(p0, p1);
       }
+      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l = l * alpha + sum;
       // P_j's buffer was last read by P V of tile j - 2
       if (j >= 2 && !fa_wait_warp(&B.pv_done[b], ph ^ 1u, abort, status)) { ok = false; break; }
@@ -694,8 +716,11 @@ __global__ void __launch_bounds__(192, 2) enc_fa_kernel(const __grid_constant__ 
   __syncthreads();
   if (threadIdx.x == 0 && s_abort) {
     // after a timeout: copies requested and products issued complete (bounded) before the CTA exits
+    for (int b = 0; b < FA_NK; ++b)
+      if (k_issued[b] > 0) tc::mbar_wait(&B.k_full[b], (uint32_t)((k_issued[b] - 1) & 1));
+    for (int b = 0; b < FA_NV; ++b)
+      if (v_issued[b] > 0) tc::mbar_wait(&B.v_full[b], (uint32_t)((v_issued[b] - 1) & 1));
     for (int b = 0; b < 2; ++b) {
-      if (s_issued[b] > 0) tc::mbar_wait(&B.kv_full[b], (uint32_t)((s_issued[b] - 1) & 1));
       if (s_commits[b] > 0) tc::mbar_wait(&B.s_full[b], (uint32_t)((s_commits[b] - 1) & 1));
       if (pv_commits[b] > 0) tc::mbar_wait(&B.pv_done[b], (uint32_t)((pv_commits[b] - 1) & 1));
     }
@@ -867,7 +892,7 @@ int ws_encode(ws_enc* e, int n, const void* mel, void* out, ws_stream stream) {
     ep.bias = L.b_qkv; ep.out = e->qkv; ep.ldo = 3 * D;
     ECK(enc_gemm(e, e->h, M, L.w_qkv, L.m_qkv, 3 * D, D, ep, s));
     if (e->attn_tc) {
-      c = cfg_of(dim3((F + FA_Q - 1) / FA_Q, D / WS_DH, n), dim3(192), FA_SMEM, s);
+      c = cfg_of(dim3((F + FA_Q - 1) / FA_Q, D / WS_DH, n), dim3(FA_THREADS), FA_SMEM, s);
       ECK(cudaLaunchKernelEx(&c, enc_fa_kernel, *reinterpret_cast<const CUtensorMap*>(mq), e->ao, F, D, e->status));
     } else {
       c = cfg_of(dim3(qtiles, D / WS_DH, n), dim3(128), EA_SMEM, s);
