@@ -216,15 +216,16 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_
 }
 
 // ------------------------------------------------------------------ streaming variant
-// Persistent warps walk the (request, head, chunk) units: global warp gw =
-// blockIdx.x * SW + w takes the contiguous range [gw * U / GW, (gw + 1) * U
-// / GW) of the U units (GW = all warps), so it streams one (request, head)'s
-// chunks in key order and reloads its query fragments only when the head
-// changes.  Each warp owns two 16 KB slots and stages its next unit's K and
-// V boxes by TMA while it computes the current one, so every SM keeps
-// several chunks in flight; a slot's mbarrier has one consumer, which
-// takes its phases in order.  A second kernel (attn_fold_kernel) folds each
-// row's chunk partials in chunk order.
+// Persistent warps walk the (request, head, group of 4 chunks) units: global
+// warp gw = blockIdx.x * SW + w takes the contiguous range [gw * U / GW,
+// (gw + 1) * U / GW) of the U units (GW = all warps), so it streams one
+// (request, head)'s chunks in key order and reloads its query fragments only
+// when the head changes.  Each warp owns two 16 KB slots and stages its next
+// chunk's K and V boxes by TMA while it computes the current one, so every
+// SM keeps several chunks in flight; a slot's mbarrier has one consumer,
+// which takes its phases in order.  A unit's chunk partials are merged in
+// registers and stored once; a second kernel (attn_fold_kernel) folds each
+// row's group partials in group order.
 constexpr int SW = 2;                        // warps per CTA
 constexpr int STREAM_SMEM = SW * 2 * CHUNK_BYTES + 1024;
 
@@ -274,16 +275,40 @@ __device__ __forceinline__ bool stage_unit(const AttnArgs& a, const CUtensorMap*
   return true;
 }
 
+// Chunks per partial of the streaming variant: a warp merges the partials of
+// STREAM_GROUP consecutive 64-key chunks of one (request, head) in registers
+// (in chunk order) and writes one partial per group, which the fold kernel
+// folds in group order.  The grouping depends only on the chunk index, so a
+// row's result does not depend on the batch or the grid.
+constexpr int STREAM_GROUP = 4;
+
+__device__ __forceinline__ void merge_partial(float& M, float& L, float* A, float m, float l, const float* a) {
+  if (!(l > 0.f)) return;
+  if (!(L > 0.f)) {
+    M = m;
+    L = l;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) A[k] = a[k];
+    return;
+  }
+  const float Mn = fmaxf(M, m), cr = expf(M - Mn), cn = expf(m - Mn);
+  L = L * cr + l * cn;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) A[k] = A[k] * cr + a[k] * cn;
+  M = Mn;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_constant__ CUtensorMap tmKV, AttnArgs a,
                                                                const bf16* kv_base) {
   extern __shared__ uint8_t dsm_s[];
   __shared__ __align__(8) uint64_t bar[SW][2];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_s) + 1023) & ~uintptr_t(1023));
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int heads = a.d / WS_DH, H = a.H, ns = a.n_split;
+  const int ng = (ns + STREAM_GROUP - 1) / STREAM_GROUP;      // partials per (request, head)
   const int mode = MODE >= 0 ? MODE : a.mode;
-  const int total = a.n_req * heads * ns;
+  const int total = a.n_req * heads * ng;                     // units: (request, head, group)
   const int gw = blockIdx.x * SW + w, GW = gridDim.x * SW;
   uint8_t* slot_mem[2] = {base + (2 * w) * CHUNK_BYTES, base + (2 * w + 1) * CHUNK_BYTES};
   if (lane == 0) {
@@ -299,59 +324,92 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
   // stages its first chunk before waiting on the previous kernel; only the
   // queries depend on it.  Self-attention reads cache rows this call wrote.
   if (mode == MODE_SELF) pdl_wait();
+  // The warp walks the chunks of its units [u_beg, u_end) in order; chunk
+  // (u, sp) is staged into slot `cur` while the previous one is computed.
+  const int u_beg = (int)((long long)gw * total / GW), u_end = (int)((long long)(gw + 1) * total / GW);
+  auto sp_first = [&](int u) { return (u % ng) * STREAM_GROUP; };
+  auto sp_end = [&](int u) { return min(ns, sp_first(u) + STREAM_GROUP); };
+  auto flat = [&](int u, int sp) { return (u / ng) * ns + sp; };     // (request, head) * ns + chunk
   // loaded[b]: slot b holds a requested (not yet consumed) copy; uses[b]: phases issued on bar[w][b]
   bool loaded[2] = {false, false};
   uint32_t uses[2] = {0u, 0u};
-  const int u_beg = (int)((long long)gw * total / GW), u_end = (int)((long long)(gw + 1) * total / GW);
-  if (lane == 0 && u_beg < u_end) loaded[0] = stage_unit<MODE>(a, &tmKV, kv_base, u_beg, slot_mem[0], &bar[w][0]);
+  if (lane == 0 && u_beg < u_end)
+    loaded[0] = stage_unit<MODE>(a, &tmKV, kv_base, flat(u_beg, sp_first(u_beg)), slot_mem[0], &bar[w][0]);
   loaded[0] = __shfl_sync(0xffffffffu, loaded[0], 0);
   if (mode == MODE_CROSS) pdl_wait();
-  int m = 0, qi = -1, qh = -1;
+  int qi = -1, qh = -1, m = 0;
   uint32_t qf[4][4];
-  for (int u = u_beg; u < u_end; ++u, ++m) {
-    const int cur = m & 1, nxt = cur ^ 1;
-    // prefetch the next unit into the other slot (consumed in the previous iteration)
-    const int un = u + 1;
-    bool ln = false;
-    if (lane == 0 && un < u_end) ln = stage_unit<MODE>(a, &tmKV, kv_base, un, slot_mem[nxt], &bar[w][nxt]);
-    ln = __shfl_sync(0xffffffffu, ln, 0);
-    const int i = u / (heads * ns), head = (u / ns) % heads, sp = u % ns;
-    int k_lo, nk, Lr, nrow;
-    unit_range<MODE>(a, i, sp, k_lo, nk, Lr, nrow);
-    auto part = [&](int j) { return a.part + ((((size_t)i * H + j) * heads + head) * ns + sp) * PART; };
-    if (loaded[cur] && (i != qi || head != qh)) {      // query fragments while the chunk lands
-      attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
-      qi = i;
-      qh = head;
-    }
-    if (loaded[cur]) {
-      const bool ok = mbar_wait(&bar[w][cur], uses[cur] & 1u);
-      ++uses[cur];
-      if (!ok) { if (lane == 0) atomicOr(a.status, WS_ST_TIMEOUT); break; }
-      uint8_t* Ks = slot_mem[cur];
-      uint8_t* Vs = Ks + CHUNK_BYTES / 2;
-      for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)   // finite values beyond the keys
-        *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
-      __syncwarp();
-      const int g = lane >> 2;
-      auto vis = [&](int j) -> uint64_t {
-        if (j >= H) return 0ull;
-        if (mode == MODE_CROSS) return prefix_mask(nk);
-        if (j >= nrow) return 0ull;
-        return self_key_mask(k_lo, nk, Lr, tree_anc(a.tree, j));
-      };
-      attn_chunk_partial<true>(Ks, Vs, qf, vis(g), vis(g + 8), H, part);
-    } else {
-      for (int j = 0; j < H; ++j) {
-        float* p = part(j);
-        if (lane == 0) { p[0] = -INFINITY; p[1] = 0.f; }
-        p[2 + 2 * lane] = 0.f;
-        p[3 + 2 * lane] = 0.f;
+  bool stop = false;
+  for (int u = u_beg; u < u_end && !stop; ++u) {
+    const int i = u / (heads * ng), head = (u / ng) % heads, grp = u % ng;
+    float RM0 = -INFINITY, RL0 = 0.f, RM1 = -INFINITY, RL1 = 0.f, RA0[16], RA1[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) RA0[k] = RA1[k] = 0.f;
+    for (int sp = sp_first(u); sp < sp_end(u); ++sp, ++m) {
+      const int cur = m & 1, nxt = cur ^ 1;
+      // prefetch the next chunk of the walk into the other slot
+      int un = u, spn = sp + 1;
+      if (spn >= sp_end(u)) { un = u + 1; spn = un < u_end ? sp_first(un) : 0; }
+      bool ln = false;
+      if (lane == 0 && un < u_end) ln = stage_unit<MODE>(a, &tmKV, kv_base, flat(un, spn), slot_mem[nxt], &bar[w][nxt]);
+      ln = __shfl_sync(0xffffffffu, ln, 0);
+      int k_lo, nk, Lr, nrow;
+      unit_range<MODE>(a, i, sp, k_lo, nk, Lr, nrow);
+      if (loaded[cur] && (i != qi || head != qh)) {      // query fragments while the chunk lands
+        attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
+        qi = i;
+        qh = head;
       }
+      if (loaded[cur]) {
+        const bool ok = mbar_wait(&bar[w][cur], uses[cur] & 1u);
+        if (!ok) {               // both slots' copies are waited for (bounded) below
+          if (lane == 0) atomicOr(a.status, WS_ST_TIMEOUT);
+          stop = true;
+          loaded[nxt] = ln;
+          break;
+        }
+        ++uses[cur];
+        uint8_t* Ks = slot_mem[cur];
+        uint8_t* Vs = Ks + CHUNK_BYTES / 2;
+        for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)   // finite values beyond the keys
+          *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+        auto vis = [&](int j) -> uint64_t {
+          if (j >= H) return 0ull;
+          if (mode == MODE_CROSS) return prefix_mask(nk);
+          if (j >= nrow) return 0ull;
+          return self_key_mask(k_lo, nk, Lr, tree_anc(a.tree, j));
+        };
+        float m0, l0, m1, l1, acc[8][4];
+        attn_chunk_regs<true>(Ks, Vs, qf, vis(g), vis(g + 8), m0, l0, m1, l1, acc);
+        float a0[16], a1[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          a0[2 * j] = acc[j][0]; a0[2 * j + 1] = acc[j][1];
+          a1[2 * j] = acc[j][2]; a1[2 * j + 1] = acc[j][3];
+        }
+        merge_partial(RM0, RL0, RA0, m0, l0, a0);
+        merge_partial(RM1, RL1, RA1, m1, l1, a1);
+      }
+      __syncwarp();                 // the slot is free for the chunk after next
+      loaded[cur] = false;
+      loaded[nxt] = ln;
     }
-    __syncwarp();                 // the slot is free for the unit after next
-    loaded[cur] = false;
-    loaded[nxt] = ln;
+    if (stop) break;
+    // the group's partial of rows g and g + 8
+    auto part = [&](int j) { return a.part + ((((size_t)i * H + j) * heads + head) * ng + grp) * PART; };
+    if (g < H) {
+      float* p = part(g);
+      if (c == 0) { p[0] = RM0; p[1] = RL0; }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) *reinterpret_cast<float2*>(p + 2 + 8 * j + 2 * c) = make_float2(RA0[2 * j], RA0[2 * j + 1]);
+    }
+    if (g + 8 < H) {
+      float* p = part(g + 8);
+      if (c == 0) { p[0] = RM1; p[1] = RL1; }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) *reinterpret_cast<float2*>(p + 2 + 8 * j + 2 * c) = make_float2(RA1[2 * j], RA1[2 * j + 1]);
+    }
   }
   // copies still requested (an early stop) land before exit (bounded)
   for (int b = 0; b < 2; ++b)
@@ -359,16 +417,16 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
   __syncwarp();
 }
 
-// One warp per (request, row, head): fold the row's chunk partials in order.
+// One warp per (request, row, head): fold the row's group partials in order.
 __global__ void __launch_bounds__(512) attn_fold_kernel(AttnArgs a) {
   pdl_wait();
   const int i = blockIdx.x, head = blockIdx.y, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int heads = a.d / WS_DH;
+  const int heads = a.d / WS_DH, ng = (a.n_split + STREAM_GROUP - 1) / STREAM_GROUP;
   pdl_trigger();
   if (j >= a.H) return;
-  const float* p = a.part + (((size_t)i * a.H + j) * heads + head) * a.n_split * PART;
+  const float* p = a.part + (((size_t)i * a.H + j) * heads + head) * ng * PART;
   float o0, o1;
-  attn_fold_row<false>(p, a.n_split, o0, o1);
+  attn_fold_row<false>(p, ng, o0, o1);
   bf16* o = reinterpret_cast<bf16*>(a.O) + ((size_t)i * a.H + j) * a.d + head * WS_DH + 2 * lane;
   o[0] = __float2bfloat16_rn(o0);
   o[1] = __float2bfloat16_rn(o1);
@@ -503,7 +561,7 @@ cudaError_t launch_cluster(const AttnArgs& a, int n, int heads, const CUtensorMa
 template <int MODE>
 cudaError_t launch_stream(const AttnArgs& a, int n, int heads, const CUtensorMap& map, const void* kv_base,
                           cudaStream_t s, bool pdl) {
-  const int total = n * heads * a.n_split;
+  const int total = n * heads * ((a.n_split + STREAM_GROUP - 1) / STREAM_GROUP);
   const int cap = 3 * (g_attn_sms > 0 ? g_attn_sms : 148);       // three CTAs (six warps) per SM
   const int ctas = (total + SW - 1) / SW;
   cudaLaunchConfig_t cfg = {};

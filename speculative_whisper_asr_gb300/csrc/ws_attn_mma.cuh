@@ -62,13 +62,14 @@ __device__ __forceinline__ void attn_q_frags(const bf16* q, int ldq, int q_row0,
   }
 }
 
-// One chunk: keys 0 .. 63 of Ks / Vs; the lanes' rows g and g + 8 see the
-// keys whose bits are set in vis_lo / vis_hi.  Writes the partial of row r to
-// part(r) (m, l, a[64]) for rows r < nrows.  Rows with no visible key get
-// m = -inf, l = 0, a = 0.
-template <bool SWZ, class PartPtr>
-__device__ __forceinline__ void attn_chunk_partial(const uint8_t* Ks, const uint8_t* Vs, const uint32_t qf[4][4],
-                                                   uint64_t vis_lo, uint64_t vis_hi, int nrows, PartPtr part) {
+// The chunk's partial in registers: lane (g = lane / 4, c = lane % 4) holds
+// rows g and g + 8: (m0, l0) and acc[j][0..1] (dims 8j + 2c, + 1) for row g,
+// (m1, l1) and acc[j][2..3] for row g + 8.  A row with no visible key has
+// m = -inf, l = 0 and zero values.
+template <bool SWZ>
+__device__ __forceinline__ void attn_chunk_regs(const uint8_t* Ks, const uint8_t* Vs, const uint32_t qf[4][4],
+                                                uint64_t vis_lo, uint64_t vis_hi, float& om0, float& ol0, float& om1,
+                                                float& ol1, float acc[8][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const uint32_t kb = smem_addr_u32(Ks), vb = smem_addr_u32(Vs);
   // ---- S = Q K^T: key tile j (keys 8j..8j+7), two dim steps per ldmatrix.x4
@@ -122,7 +123,6 @@ __device__ __forceinline__ void attn_chunk_partial(const uint8_t* Ks, const uint
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   // ---- a = P V with P = hi + lo (bf16 each); key step s uses key tiles 2s, 2s+1
-  float acc[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll
@@ -150,22 +150,38 @@ __device__ __forceinline__ void attn_chunk_partial(const uint8_t* Ks, const uint
       mma_bf16_16816(acc[j2 + 1], pl, b2, b3);
     }
   }
-  // ---- partials of rows g and g + 8
   const bool has0 = vis_lo != 0ull, has1 = vis_hi != 0ull;
+  om0 = has0 ? m0 : -INFINITY;
+  ol0 = has0 ? l0 : 0.f;
+  om1 = has1 ? m1 : -INFINITY;
+  ol1 = has1 ? l1 : 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (!has0) acc[j][0] = acc[j][1] = 0.f;
+    if (!has1) acc[j][2] = acc[j][3] = 0.f;
+  }
+}
+
+// One chunk: keys 0 .. 63 of Ks / Vs; the lanes' rows g and g + 8 see the
+// keys whose bits are set in vis_lo / vis_hi.  Writes the partial of row r to
+// part(r) (m, l, a[64]) for rows r < nrows.  Rows with no visible key get
+// m = -inf, l = 0, a = 0.
+template <bool SWZ, class PartPtr>
+__device__ __forceinline__ void attn_chunk_partial(const uint8_t* Ks, const uint8_t* Vs, const uint32_t qf[4][4],
+                                                   uint64_t vis_lo, uint64_t vis_hi, int nrows, PartPtr part) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  float m0, l0, m1, l1, acc[8][4];
+  attn_chunk_regs<SWZ>(Ks, Vs, qf, vis_lo, vis_hi, m0, l0, m1, l1, acc);
   if (g < nrows) {
     float* p = part(g);
-    if (c == 0) { p[0] = has0 ? m0 : -INFINITY; p[1] = has0 ? l0 : 0.f; }
+    if (c == 0) { p[0] = m0; p[1] = l0; }
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<float2*>(p + 2 + 8 * j + 2 * c) =
-          has0 ? make_float2(acc[j][0], acc[j][1]) : make_float2(0.f, 0.f);
+    for (int j = 0; j < 8; ++j) *reinterpret_cast<float2*>(p + 2 + 8 * j + 2 * c) = make_float2(acc[j][0], acc[j][1]);
   }
   if (g + 8 < nrows) {
     float* p = part(g + 8);
-    if (c == 0) { p[0] = has1 ? m1 : -INFINITY; p[1] = has1 ? l1 : 0.f; }
+    if (c == 0) { p[0] = m1; p[1] = l1; }
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<float2*>(p + 2 + 8 * j + 2 * c) =
-          has1 ? make_float2(acc[j][2], acc[j][3]) : make_float2(0.f, 0.f);
+    for (int j = 0; j < 8; ++j) *reinterpret_cast<float2*>(p + 2 + 8 * j + 2 * c) = make_float2(acc[j][2], acc[j][3]);
   }
 }

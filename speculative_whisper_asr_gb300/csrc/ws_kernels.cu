@@ -101,20 +101,22 @@ __global__ void embed_draft_kernel(int K1, const int32_t* req_ids, const int32_t
 // y = (x - mean) / sqrt(var + 1e-5) * g + b over each row, fp32 statistics.
 // group_skip > 0: output row o reads input row (o / (G-1)) * G + o % (G-1) + 1
 // (drops row 0 of every group of G rows: the drafter's anchor row).
-// One warp (one CTA) per row (ln_row_warp).
+// One warp per row (ln_row_warp), four rows per CTA; bf16 rows are stored
+// four values (8 bytes) at a time.
 template <typename T>
-__global__ void __launch_bounds__(32) layernorm_kernel(int M, int d, const float* x, int ldx, const T* g,
-                                                       const T* b, T* y, int ldy, int group_skip) {
+__global__ void __launch_bounds__(128) layernorm_kernel(int M, int d, const float* x, int ldx, const T* g,
+                                                        const T* b, T* y, int ldy, int group_skip) {
   pdl_trigger();
   // gain and bias are weights: bring this lane's groups into L1 before the
   // dependency wait, so the normalisation does not wait on L2 after the
   // reductions
-  for (int k = 4 * (int)threadIdx.x; k < d; k += 128) {
+  const int lane = threadIdx.x & 31;
+  for (int k = 4 * lane; k < d; k += 128) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(g + k));
     asm volatile("prefetch.global.L1 [%0];" ::"l"(b + k));
   }
   pdl_wait();
-  const int o = blockIdx.x;
+  const int o = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (o >= M) return;
   int src = o;
   if (group_skip > 0) {
@@ -123,7 +125,15 @@ __global__ void __launch_bounds__(32) layernorm_kernel(int M, int d, const float
   }
   T* yr = y + (size_t)o * ldy;
   ln_row_warp(x + (size_t)src * ldx, d, g, b, sizeof(T) == 2, [&](int k, float a0, float a1, float a2, float a3) {
-    yr[k] = from_f<T>(a0); yr[k + 1] = from_f<T>(a1); yr[k + 2] = from_f<T>(a2); yr[k + 3] = from_f<T>(a3);
+    if constexpr (sizeof(T) == 2) {
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(a0, a1), h1 = __floats2bfloat162_rn(a2, a3);
+      uint2 w;
+      w.x = *reinterpret_cast<uint32_t*>(&h0);
+      w.y = *reinterpret_cast<uint32_t*>(&h1);
+      *reinterpret_cast<uint2*>(yr + k) = w;
+    } else {
+      yr[k] = from_f<T>(a0); yr[k + 1] = from_f<T>(a1); yr[k + 2] = from_f<T>(a2); yr[k + 3] = from_f<T>(a3);
+    }
   });
 }
 
@@ -804,7 +814,7 @@ cudaError_t launch_layernorm(int M, int d, const float* x, int ldx, const T* g, 
                              int group_skip, cudaStream_t s, bool pdl) {
   if (M <= 0) return cudaSuccess;
   cudaLaunchAttribute at[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(32), 0, s, pdl, at);
+  cudaLaunchConfig_t cfg = make_cfg(dim3((M + 3) / 4), dim3(128), 0, s, pdl, at);
   ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, layernorm_kernel<T>, M, d, x, ldx, g, b, y, ldy, group_skip);
 }
