@@ -220,14 +220,16 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_
 // warp gw = blockIdx.x * SW + w takes the contiguous range [gw * U / GW,
 // (gw + 1) * U / GW) of the U units (GW = all warps), so it streams one
 // (request, head)'s chunks in key order and reloads its query fragments only
-// when the head changes.  Each warp owns two 16 KB slots and stages its next
-// chunk's K and V boxes by TMA while it computes the current one, so every
-// SM keeps several chunks in flight; a slot's mbarrier has one consumer,
-// which takes its phases in order.  A unit's chunk partials are merged in
+// when the head changes.  Each warp owns NSLOT 16 KB slots and keeps the K
+// and V boxes of its next NSLOT - 1 chunks in flight by TMA while it computes
+// the current one (two slots and six warps per SM measured faster than four
+// slots and three warps: per-warp compute, not latency, bounds it); a slot's
+// mbarrier has one consumer, which takes its phases in order.  A unit's chunk partials are merged in
 // registers and stored once; a second kernel (attn_fold_kernel) folds each
 // row's group partials in group order.
 constexpr int SW = 2;                        // warps per CTA
-constexpr int STREAM_SMEM = SW * 2 * CHUNK_BYTES + 1024;
+constexpr int NSLOT = 2;                     // TMA slots per warp: the next chunk lands while one is computed
+constexpr int STREAM_SMEM = SW * NSLOT * CHUNK_BYTES + 1024;
 
 // MODE < 0: the mode is a.mode (one compiled copy serves self- and cross-attention)
 template <int MODE>
@@ -276,33 +278,16 @@ __device__ __forceinline__ bool stage_unit(const AttnArgs& a, const CUtensorMap*
 }
 
 // Chunks per partial of the streaming variant: a warp merges the partials of
-// STREAM_GROUP consecutive 64-key chunks of one (request, head) in registers
-// (in chunk order) and writes one partial per group, which the fold kernel
-// folds in group order.  The grouping depends only on the chunk index, so a
-// row's result does not depend on the batch or the grid.
-constexpr int STREAM_GROUP = 4;
-
-__device__ __forceinline__ void merge_partial(float& M, float& L, float* A, float m, float l, const float* a) {
-  if (!(l > 0.f)) return;
-  if (!(L > 0.f)) {
-    M = m;
-    L = l;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) A[k] = a[k];
-    return;
-  }
-  const float Mn = fmaxf(M, m), cr = expf(M - Mn), cn = expf(m - Mn);
-  L = L * cr + l * cn;
-#pragma unroll
-  for (int k = 0; k < 16; ++k) A[k] = A[k] * cr + a[k] * cn;
-  M = Mn;
-}
+// ATTN_GROUP consecutive 64-key chunks of one (request, head) in registers
+// (attn_merge, chunk order) and writes one partial per group, which the fold
+// kernel folds in group order; the cluster variant groups the same way.
+constexpr int STREAM_GROUP = ATTN_GROUP;
 
 template <int MODE>
 __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_constant__ CUtensorMap tmKV, AttnArgs a,
                                                                const bf16* kv_base) {
   extern __shared__ uint8_t dsm_s[];
-  __shared__ __align__(8) uint64_t bar[SW][2];
+  __shared__ __align__(8) uint64_t bar[SW][NSLOT];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_s) + 1023) & ~uintptr_t(1023));
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int heads = a.d / WS_DH, H = a.H, ns = a.n_split;
@@ -310,32 +295,45 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
   const int mode = MODE >= 0 ? MODE : a.mode;
   const int total = a.n_req * heads * ng;                     // units: (request, head, group)
   const int gw = blockIdx.x * SW + w, GW = gridDim.x * SW;
-  uint8_t* slot_mem[2] = {base + (2 * w) * CHUNK_BYTES, base + (2 * w + 1) * CHUNK_BYTES};
-  if (lane == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[w][0])) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[w][1])) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
+  uint8_t* slots = base + w * NSLOT * CHUNK_BYTES;
+  if (lane < NSLOT) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[w][lane])) : "memory");
+  if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncwarp();
   pdl_trigger();
   // Acoustic K/V, frame counts and request ids were all written before this
   // library call began (the first kernel of every call releases its
   // dependents only after its own dependency wait), so cross-attention
-  // stages its first chunk before waiting on the previous kernel; only the
+  // stages its first chunks before waiting on the previous kernel; only the
   // queries depend on it.  Self-attention reads cache rows this call wrote.
   if (mode == MODE_SELF) pdl_wait();
-  // The warp walks the chunks of its units [u_beg, u_end) in order; chunk
-  // (u, sp) is staged into slot `cur` while the previous one is computed.
+  // The warp walks the chunks of its units [u_beg, u_end) in order; walk
+  // chunk k lives in slot k % NSLOT.
   const int u_beg = (int)((long long)gw * total / GW), u_end = (int)((long long)(gw + 1) * total / GW);
   auto sp_first = [&](int u) { return (u % ng) * STREAM_GROUP; };
   auto sp_end = [&](int u) { return min(ns, sp_first(u) + STREAM_GROUP); };
   auto flat = [&](int u, int sp) { return (u / ng) * ns + sp; };     // (request, head) * ns + chunk
-  // loaded[b]: slot b holds a requested (not yet consumed) copy; uses[b]: phases issued on bar[w][b]
-  bool loaded[2] = {false, false};
-  uint32_t uses[2] = {0u, 0u};
-  if (lane == 0 && u_beg < u_end)
-    loaded[0] = stage_unit<MODE>(a, &tmKV, kv_base, flat(u_beg, sp_first(u_beg)), slot_mem[0], &bar[w][0]);
-  loaded[0] = __shfl_sync(0xffffffffu, loaded[0], 0);
+  // loaded[b]: slot b holds a requested, not yet consumed copy; uses[b]: phases consumed on bar[w][b]
+  bool loaded[NSLOT];
+  uint32_t uses[NSLOT];
+#pragma unroll
+  for (int b = 0; b < NSLOT; ++b) { loaded[b] = false; uses[b] = 0u; }
+  int lu = u_beg, lsp = u_beg < u_end ? sp_first(u_beg) : 0, staged = 0;   // next walk chunk to stage
+  auto stage_next = [&]() {
+    if (lu >= u_end) return;
+    const int sl = staged % NSLOT;
+    bool ok = false;
+    if (lane == 0) ok = stage_unit<MODE>(a, &tmKV, kv_base, flat(lu, lsp), slots + sl * CHUNK_BYTES, &bar[w][sl]);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+#pragma unroll
+    for (int b = 0; b < NSLOT; ++b)
+      if (b == sl) loaded[b] = ok;
+    ++staged;
+    if (++lsp >= sp_end(lu)) {
+      ++lu;
+      if (lu < u_end) lsp = sp_first(lu);
+    }
+  };
+  for (int k = 0; k < NSLOT - 1; ++k) stage_next();
   if (mode == MODE_CROSS) pdl_wait();
   int qi = -1, qh = -1, m = 0;
   uint32_t qf[4][4];
@@ -346,30 +344,28 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
 #pragma unroll
     for (int k = 0; k < 16; ++k) RA0[k] = RA1[k] = 0.f;
     for (int sp = sp_first(u); sp < sp_end(u); ++sp, ++m) {
-      const int cur = m & 1, nxt = cur ^ 1;
-      // prefetch the next chunk of the walk into the other slot
-      int un = u, spn = sp + 1;
-      if (spn >= sp_end(u)) { un = u + 1; spn = un < u_end ? sp_first(un) : 0; }
-      bool ln = false;
-      if (lane == 0 && un < u_end) ln = stage_unit<MODE>(a, &tmKV, kv_base, flat(un, spn), slot_mem[nxt], &bar[w][nxt]);
-      ln = __shfl_sync(0xffffffffu, ln, 0);
+      stage_next();                 // walk chunk m + NSLOT - 1 into the slot chunk m - 1 used
+      const int cur = m % NSLOT;
+      bool have = false;
+      uint32_t use = 0u;
+#pragma unroll
+      for (int b = 0; b < NSLOT; ++b)
+        if (b == cur) { have = loaded[b]; use = uses[b]; }
       int k_lo, nk, Lr, nrow;
       unit_range<MODE>(a, i, sp, k_lo, nk, Lr, nrow);
-      if (loaded[cur] && (i != qi || head != qh)) {      // query fragments while the chunk lands
+      if (have && (i != qi || head != qh)) {      // query fragments while the chunk lands
         attn_q_frags(reinterpret_cast<const bf16*>(a.Q), a.d, i * H, H, head * WS_DH, qf);
         qi = i;
         qh = head;
       }
-      if (loaded[cur]) {
-        const bool ok = mbar_wait(&bar[w][cur], uses[cur] & 1u);
-        if (!ok) {               // both slots' copies are waited for (bounded) below
+      if (have) {
+        const bool ok = mbar_wait(&bar[w][cur], use & 1u);
+        if (!ok) {               // every slot's copy is waited for (bounded) below
           if (lane == 0) atomicOr(a.status, WS_ST_TIMEOUT);
           stop = true;
-          loaded[nxt] = ln;
           break;
         }
-        ++uses[cur];
-        uint8_t* Ks = slot_mem[cur];
+        uint8_t* Ks = slots + cur * CHUNK_BYTES;
         uint8_t* Vs = Ks + CHUNK_BYTES / 2;
         for (int idx = nk * 8 + lane; idx < WS_XCHUNK * 8; idx += 32)   // finite values beyond the keys
           *reinterpret_cast<uint4*>(Vs + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -388,12 +384,16 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
           a0[2 * j] = acc[j][0]; a0[2 * j + 1] = acc[j][1];
           a1[2 * j] = acc[j][2]; a1[2 * j + 1] = acc[j][3];
         }
-        merge_partial(RM0, RL0, RA0, m0, l0, a0);
-        merge_partial(RM1, RL1, RA1, m1, l1, a1);
+        attn_merge<16>(RM0, RL0, RA0, m0, l0, a0);
+        attn_merge<16>(RM1, RL1, RA1, m1, l1, a1);
       }
-      __syncwarp();                 // the slot is free for the chunk after next
-      loaded[cur] = false;
-      loaded[nxt] = ln;
+      __syncwarp();                 // the slot is free for the walk chunk m + NSLOT
+#pragma unroll
+      for (int b = 0; b < NSLOT; ++b)
+        if (b == cur) {
+          if (loaded[b]) ++uses[b];
+          loaded[b] = false;
+        }
     }
     if (stop) break;
     // the group's partial of rows g and g + 8
@@ -412,7 +412,8 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
     }
   }
   // copies still requested (an early stop) land before exit (bounded)
-  for (int b = 0; b < 2; ++b)
+#pragma unroll
+  for (int b = 0; b < NSLOT; ++b)
     if (loaded[b] && lane == 0 && !mbar_wait(&bar[w][b], uses[b] & 1u)) atomicOr(a.status, WS_ST_TIMEOUT);
   __syncwarp();
 }
@@ -445,7 +446,7 @@ __global__ void __launch_bounds__(512) attn_fold_kernel(AttnArgs a) {
 // global memory, and rows bit-identical to the streaming variant's.
 constexpr int CW = 4;                                     // warps (chunks) per CTA
 constexpr int CL_MAX = 8;                                 // CTAs per cluster (portable size)
-constexpr int CLUSTER_SMEM = CW * CHUNK_BYTES + CW * MAXR * PART * 4 + 1024;
+constexpr int CLUSTER_SMEM = CW * CHUNK_BYTES + (CW + 1) * MAXR * PART * 4 + 1024;
 
 template <int MODE>
 __global__ void __launch_bounds__(CW * 32) attn_cluster_kernel(const __grid_constant__ CUtensorMap tmKV, AttnArgs a,
@@ -509,11 +510,32 @@ __global__ void __launch_bounds__(CW * 32) attn_cluster_kernel(const __grid_cons
       }
     }
   }
-  cl.sync();                        // every chunk partial of the cluster is written
+  // This CTA's four chunks are one group (CW == ATTN_GROUP): merge their
+  // partials row by row in chunk order (attn_merge, as the streaming variant
+  // does in registers), then fold the cluster's groups through DSMEM with
+  // the fold kernel's arithmetic.
+  static_assert(CW == ATTN_GROUP, "a CTA's chunks form one partial group");
+  __syncthreads();                  // the CTA's chunk partials are written
+  float* gparts = parts + CW * MAXR * PART;                       // [MAXR][PART] group partials
+  for (int j = w; j < H; j += CW) {
+    float GM = -INFINITY, GL = 0.f, GA[2] = {0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < CW; ++k) {
+      if (rank * CW + k >= ns) break;
+      const float* p = parts + (k * MAXR + j) * PART;
+      const float2 av = *reinterpret_cast<const float2*>(p + 2 + 2 * lane);
+      const float aa[2] = {av.x, av.y};
+      attn_merge<2>(GM, GL, GA, p[0], p[1], aa);
+    }
+    float* q = gparts + j * PART;
+    if (lane == 0) { q[0] = GM; q[1] = GL; }
+    q[2 + 2 * lane] = GA[0];
+    q[3 + 2 * lane] = GA[1];
+  }
+  cl.sync();                        // every group partial of the cluster is written
   for (int j = rank * CW + w; j < H; j += C * CW) {
     float o0, o1;
-    attn_fold_row_of<false>(
-        [&](int s) { return cl.map_shared_rank(parts, s / CW) + ((s % CW) * MAXR + j) * PART; }, ns, o0, o1);
+    attn_fold_row_of<false>([&](int g) { return cl.map_shared_rank(gparts, g) + j * PART; }, C, o0, o1);
     bf16* o = reinterpret_cast<bf16*>(a.O) + ((size_t)i * H + j) * a.d + head * WS_DH + 2 * lane;
     o[0] = __float2bfloat16_rn(o0);
     o[1] = __float2bfloat16_rn(o1);
@@ -562,7 +584,7 @@ template <int MODE>
 cudaError_t launch_stream(const AttnArgs& a, int n, int heads, const CUtensorMap& map, const void* kv_base,
                           cudaStream_t s, bool pdl) {
   const int total = n * heads * ((a.n_split + STREAM_GROUP - 1) / STREAM_GROUP);
-  const int cap = 3 * (g_attn_sms > 0 ? g_attn_sms : 148);       // three CTAs (six warps) per SM
+  const int cap = 3 * (g_attn_sms > 0 ? g_attn_sms : 148);       // three CTAs per SM
   const int ctas = (total + SW - 1) / SW;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas < cap ? ctas : cap);

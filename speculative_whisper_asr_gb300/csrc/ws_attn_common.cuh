@@ -79,6 +79,36 @@ __device__ __forceinline__ void row_subtile(RowState& st, const float* q, const 
 // order are those of the sequential fold: M = max_s m_s, then den, n0, n1
 // accumulate over s = 0, 1, ... with weights exp(m_s - M), skipping empty
 // splits.
+// Chunks per partial group: the partials of ATTN_GROUP consecutive 64-key
+// chunks of a row are merged in chunk order (attn_merge), and the group
+// partials are folded in group order (attn_fold_row_of).  Every bf16
+// attention kernel of the batched and one-cluster paths does exactly this,
+// so a row's result does not depend on how many requests share the call.
+constexpr int ATTN_GROUP = 4;
+
+// Merge one chunk partial (m, l, a[K]) into the running group partial (M, L,
+// A[K]); empty chunks (l = 0) are skipped and the first non-empty chunk is
+// taken as is.  Explicit FMAs fix the rounding in every kernel.
+template <int K>
+__device__ __forceinline__ void attn_merge(float& M, float& L, float* A, float m, float l, const float* a) {
+  if (!(l > 0.f)) return;
+  if (!(L > 0.f)) {
+    M = m;
+    L = l;
+#pragma unroll
+    for (int k = 0; k < K; ++k) A[k] = a[k];
+    return;
+  }
+  // the larger of M and m keeps weight exp(0) = 1: one exponential per merge
+  const bool up = m > M;
+  const float e = expf(up ? M - m : m - M);
+  const float cr = up ? e : 1.0f, cn = up ? 1.0f : e;
+  L = fmaf(L, cr, __fmul_rn(l, cn));
+#pragma unroll
+  for (int k = 0; k < K; ++k) A[k] = fmaf(A[k], cr, __fmul_rn(a[k], cn));
+  M = up ? m : M;
+}
+
 template <bool GLOBAL>
 __device__ __forceinline__ float fold_ld(const float* p) { return GLOBAL ? __ldcg(p) : *p; }
 template <bool GLOBAL>

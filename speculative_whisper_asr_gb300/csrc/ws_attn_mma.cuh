@@ -62,11 +62,12 @@ __device__ __forceinline__ void attn_q_frags(const bf16* q, int ldq, int q_row0,
   }
 }
 
-// The chunk's partial in registers: lane (g = lane / 4, c = lane % 4) holds
+// The chunk's partial in registers (HILO: P enters P V as bf16 hi + lo,
+// ~16 mantissa bits; else as one bf16 value): lane (g = lane / 4, c = lane % 4) holds
 // rows g and g + 8: (m0, l0) and acc[j][0..1] (dims 8j + 2c, + 1) for row g,
 // (m1, l1) and acc[j][2..3] for row g + 8.  A row with no visible key has
 // m = -inf, l = 0 and zero values.
-template <bool SWZ>
+template <bool SWZ, bool HILO = true>
 __device__ __forceinline__ void attn_chunk_regs(const uint8_t* Ks, const uint8_t* Vs, const uint32_t qf[4][4],
                                                 uint64_t vis_lo, uint64_t vis_hi, float& om0, float& ol0, float& om1,
                                                 float& ol1, float acc[8][4]) {
@@ -145,9 +146,9 @@ __device__ __forceinline__ void attn_chunk_regs(const uint8_t* Ks, const uint8_t
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(vb + kv_off<SWZ>(key, chunk), b0, b1, b2, b3);
       mma_bf16_16816(acc[j2], ph, b0, b1);
-      mma_bf16_16816(acc[j2], pl, b0, b1);
+      if (HILO) mma_bf16_16816(acc[j2], pl, b0, b1);
       mma_bf16_16816(acc[j2 + 1], ph, b2, b3);
-      mma_bf16_16816(acc[j2 + 1], pl, b2, b3);
+      if (HILO) mma_bf16_16816(acc[j2 + 1], pl, b2, b3);
     }
   }
   const bool has0 = vis_lo != 0ull, has1 = vis_hi != 0ull;
