@@ -226,60 +226,98 @@ __device__ __forceinline__ float scaled(const float* z, int v, float T, const ui
 }
 
 struct RowStat { float m, S; };
-// max and sum of exp(z/T - max) over a row (FP32, fixed order per thread chunk).
+// max and sum of exp(z/T - max) over a row (FP32).  Each thread takes ids
+// tid, tid + 256, ... with four loads in flight (four partial maxima / sums,
+// combined in a fixed order), then the block reduces in a fixed order.
 __device__ RowStat row_stat(const float* z, int V, float T, const uint32_t* sup, float* sh) {
-  float m = -INFINITY;
-  for (int v = threadIdx.x; v < V; v += SNT) m = fmaxf(m, scaled(z, v, T, sup));
-  m = block_max<SNT>(m, sh);
-  float s = 0.0f;
-  for (int v = threadIdx.x; v < V; v += SNT) s += expf(scaled(z, v, T, sup) - m);
-  s = block_sum<SNT>(s, sh);
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  int v = threadIdx.x;
+  for (; v + 3 * SNT < V; v += 4 * SNT) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m4[q] = fmaxf(m4[q], scaled(z, v + q * SNT, T, sup));
+  }
+  for (; v < V; v += SNT) m4[0] = fmaxf(m4[0], scaled(z, v, T, sup));
+  float m = block_max<SNT>(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), sh);
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  v = threadIdx.x;
+  for (; v + 3 * SNT < V; v += 4 * SNT) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s4[q] += expf(scaled(z, v + q * SNT, T, sup) - m);
+  }
+  for (; v < V; v += SNT) s4[0] += expf(scaled(z, v, T, sup) - m);
+  const float s = block_sum<SNT>((s4[0] + s4[1]) + (s4[2] + s4[3]), sh);
   RowStat r; r.m = m; r.S = s;
   return r;
 }
 
+__device__ __forceinline__ double warp_sum_d(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
 // Inverse CDF over non-negative weights w(v), v = 0..V-1 in ascending id
-// order: the smallest v whose running sum exceeds u * sum(w).  Each thread
-// owns a contiguous chunk; chunk sums are prefixed in thread order.
+// order: the smallest v whose running sum exceeds u * sum(w).  Warp k owns
+// the contiguous ids [k * seg, (k + 1) * seg); its lanes read them 32 at a
+// time (coalesced, four weights in flight per lane) for the segment's sum;
+// segment sums are prefixed in warp order; the warp whose segment holds the
+// target then scans it 32 ids at a time (an inclusive warp scan per step).
 template <class WF>
 __device__ int block_inverse_cdf(WF w, int V, float u) {
   // The weights are FP32 probabilities; their running sums are kept in FP64
   // so that the drawn id depends on the weights, not on the summation order.
+  constexpr int NWARP = SNT / 32;
   __shared__ int found;
-  __shared__ double shd[SNT + 1];
-  const int C = (V + SNT - 1) / SNT;
-  const int lo = threadIdx.x * C, hi = min(V, lo + C);
-  double s = 0.0;
-  for (int v = lo; v < hi; ++v) s += (double)w(v);
+  __shared__ double shd[NWARP + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = (V + NWARP - 1) / NWARP;
+  const int lo = warp * seg, hi = min(V, lo + seg);
+  double s4[4] = {0.0, 0.0, 0.0, 0.0};
+  int v = lo + lane;
+  for (; v + 96 < hi; v += 128) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s4[q] += (double)w(v + 32 * q);
+  }
+  for (; v < hi; v += 32) s4[0] += (double)w(v);
+  const double s = warp_sum_d((s4[0] + s4[1]) + (s4[2] + s4[3]));
   __syncthreads();
-  shd[threadIdx.x] = s;
+  if (lane == 0) shd[warp] = s;
   if (threadIdx.x == 0) found = -1;
   __syncthreads();
   if (threadIdx.x == 0) {
     double run = 0.0;
-    for (int t = 0; t < SNT; ++t) { double c = shd[t]; shd[t] = run; run += c; }
-    shd[SNT] = run;
+    for (int t = 0; t < NWARP; ++t) { double c = shd[t]; shd[t] = run; run += c; }
+    shd[NWARP] = run;
   }
   __syncthreads();
-  const double total = shd[SNT];
+  const double total = shd[NWARP];
   const double target = (double)u * total;
-  const double pre = shd[threadIdx.x];
-  const double nxt = threadIdx.x + 1 < SNT ? shd[threadIdx.x + 1] : total;
+  const double pre = shd[warp];
+  const double nxt = warp + 1 < NWARP ? shd[warp + 1] : total;
   if (s > 0.0 && pre <= target && target < nxt) {
     double run = pre;
     int tok = -1, last = -1;
-    for (int v = lo; v < hi; ++v) {
-      const float wv = w(v);
-      if (wv > 0.0f) last = v;
-      run += (double)wv;
-      if (run > target) { tok = v; break; }
+    for (int v0 = lo; v0 < hi; v0 += 32) {
+      const int vv = v0 + lane;
+      const float wv = vv < hi ? w(vv) : 0.0f;
+      double x = (double)wv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, vv < hi && run + x > target);
+      const unsigned pos = __ballot_sync(0xffffffffu, wv > 0.0f);
+      if (pos) last = v0 + 31 - __clz(pos);
+      if (hit) { tok = v0 + __ffs(hit) - 1; break; }
+      run += __shfl_sync(0xffffffffu, x, 31);
     }
-    atomicMax(&found, tok >= 0 ? tok : last);
+    if (lane == 0) atomicMax(&found, tok >= 0 ? tok : last);
   }
   __syncthreads();
   if (found < 0) {   // rounding pushed the target past the end: last id with weight
     if (threadIdx.x == 0) {
-      for (int v = V - 1; v >= 0; --v) if (w(v) > 0.0f) { found = v; break; }
+      for (int vb = V - 1; vb >= 0; --vb) if (w(vb) > 0.0f) { found = vb; break; }
       if (found < 0) found = 0;
     }
     __syncthreads();
