@@ -69,7 +69,7 @@ typedef struct {
   int32_t d_model;         /* width d; multiple of 128 */
   int32_t n_heads;         /* d_model / n_heads must be 64 */
   int32_t d_ff;            /* FFN width; multiple of 128 */
-  int32_t vocab;           /* V */
+  int32_t vocab;           /* V (even, at most 65,536) */
   int32_t max_pos;         /* decoder context (learned positions), <= 448 */
   int32_t drafter_layers;  /* 0 (no drafter) or 2 */
   int32_t n_hist;          /* history layers (1..8) */

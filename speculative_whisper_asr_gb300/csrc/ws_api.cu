@@ -163,7 +163,7 @@ const char* check_desc(const ws_model_desc* d) {
   if (d->d_model < 128 || d->d_model % 128 != 0 || d->d_model > 2048) return "d_model must be a multiple of 128, <= 2048";
   if (d->n_heads < 1 || d->d_model / d->n_heads != WS_DH || d->d_model % d->n_heads) return "d_model / n_heads must be 64";
   if (d->d_ff < 128 || d->d_ff % 128 != 0) return "d_ff must be a multiple of 128";
-  if (d->vocab < 2 || d->vocab % 2 != 0) return "vocab must be even and >= 2";
+  if (d->vocab < 2 || d->vocab % 2 != 0 || d->vocab > 65536) return "vocab must be even, 2..65536";
   if (d->max_pos < 1 || d->max_pos > 4096) return "max_pos out of range";
   if (d->drafter_layers < 0 || d->drafter_layers > 8) return "drafter_layers out of range";
   if (d->K < 1 || d->K > 15) return "K must be 1..15";

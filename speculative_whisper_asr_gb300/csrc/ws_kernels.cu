@@ -224,25 +224,39 @@ __device__ __forceinline__ bool suppressed(const uint32_t* sup, int v) {
 __device__ __forceinline__ float scaled(const float* z, int v, float T, const uint32_t* sup) {
   return suppressed(sup, v) ? -INFINITY : z[v] / T;
 }
+// The same for an already loaded logit value zv of id v.
+__device__ __forceinline__ float scaled_val(float zv, int v, float T, const uint32_t* sup) {
+  return suppressed(sup, v) ? -INFINITY : zv / T;
+}
 
 struct RowStat { float m, S; };
 // max and sum of exp(z/T - max) over a row (FP32).  Each thread takes ids
-// tid, tid + 256, ... with four loads in flight (four partial maxima / sums,
-// combined in a fixed order), then the block reduces in a fixed order.
+// tid, tid + 256, ... with sixteen loads in flight (the row streams from
+// HBM at microseconds of latency): four partial maxima / sums combined in a
+// fixed order, then the block reduces in a fixed order.  The maximum is
+// taken over the raw logits and divided once: a correctly rounded division
+// by T > 0 is monotone, so max(z) / T equals max(z / T) exactly.
+constexpr int RS_DEPTH = 16;
 __device__ RowStat row_stat(const float* z, int V, float T, const uint32_t* sup, float* sh) {
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   int v = threadIdx.x;
-  for (; v + 3 * SNT < V; v += 4 * SNT) {
+  for (; v + (RS_DEPTH - 1) * SNT < V; v += RS_DEPTH * SNT) {
+    float zz[RS_DEPTH];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) m4[q] = fmaxf(m4[q], scaled(z, v + q * SNT, T, sup));
+    for (int q = 0; q < RS_DEPTH; ++q) zz[q] = __ldg(z + v + q * SNT);      // all loads first
+#pragma unroll
+    for (int q = 0; q < RS_DEPTH; ++q) m4[q & 3] = fmaxf(m4[q & 3], suppressed(sup, v + q * SNT) ? -INFINITY : zz[q]);
   }
-  for (; v < V; v += SNT) m4[0] = fmaxf(m4[0], scaled(z, v, T, sup));
-  float m = block_max<SNT>(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), sh);
+  for (; v < V; v += SNT) m4[0] = fmaxf(m4[0], suppressed(sup, v) ? -INFINITY : z[v]);
+  const float m = block_max<SNT>(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), sh) / T;
   float s4[4] = {0.f, 0.f, 0.f, 0.f};
   v = threadIdx.x;
-  for (; v + 3 * SNT < V; v += 4 * SNT) {
+  for (; v + (RS_DEPTH - 1) * SNT < V; v += RS_DEPTH * SNT) {
+    float zz[RS_DEPTH];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) s4[q] += expf(scaled(z, v + q * SNT, T, sup) - m);
+    for (int q = 0; q < RS_DEPTH; ++q) zz[q] = __ldg(z + v + q * SNT);
+#pragma unroll
+    for (int q = 0; q < RS_DEPTH; ++q) s4[q & 3] += expf(scaled_val(zz[q], v + q * SNT, T, sup) - m);
   }
   for (; v < V; v += SNT) s4[0] += expf(scaled(z, v, T, sup) - m);
   const float s = block_sum<SNT>((s4[0] + s4[1]) + (s4[2] + s4[3]), sh);
@@ -256,30 +270,76 @@ __device__ __forceinline__ double warp_sum_d(double x) {
   return x;
 }
 
+// Float-float sums: TwoSum (Knuth) keeps the rounding error of every FP32
+// addition, so a 32-value sum is exact to ~2^-48 relative without FP64
+// arithmetic (which runs far slower than FP32 on this part).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+__device__ __forceinline__ void warp_sum_ff(float& hi, float& lo) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    float sum, err;
+    two_sum(hi, h2, sum, err);
+    hi = sum;
+    lo = (lo + l2) + err;
+  }
+}
+
 // Inverse CDF over non-negative weights w(v), v = 0..V-1 in ascending id
 // order: the smallest v whose running sum exceeds u * sum(w).  Warp k owns
-// the contiguous ids [k * seg, (k + 1) * seg); its lanes read them 32 at a
-// time (coalesced, four weights in flight per lane) for the segment's sum;
-// segment sums are prefixed in warp order; the warp whose segment holds the
-// target then scans it 32 ids at a time (an inclusive warp scan per step).
+// the contiguous ids [k * seg, (k + 1) * seg), seg a multiple of 32; its
+// lanes read them one 32-id row at a time (coalesced, eight rows in flight)
+// and keep every row's sum (float-float, stored as FP64) in shared memory.
+// Segment sums are prefixed in warp order; the warp whose segment holds the
+// target finds the row from the row sums (a lane scan over contiguous row
+// ranges, FP64), then the id inside the row with an inclusive float-float
+// warp scan, so only that one row is read twice.
+constexpr int CDF_ROWS = 256;      // rows per warp: V <= 8 * 256 * 32 = 65,536
+// rsum_base: the caller's shared scratch of (SNT / 32) * CDF_ROWS doubles (one per kernel).
 template <class WF>
-__device__ int block_inverse_cdf(WF w, int V, float u) {
-  // The weights are FP32 probabilities; their running sums are kept in FP64
-  // so that the drawn id depends on the weights, not on the summation order.
+__device__ int block_inverse_cdf(WF w, int V, float u, double* rsum_base) {
+  // The weights are FP32 probabilities; their running sums are kept exact
+  // (float-float rows, FP64 across rows) so that the drawn id depends on the
+  // weights, not on the summation order.
   constexpr int NWARP = SNT / 32;
   __shared__ int found;
   __shared__ double shd[NWARP + 1];
+  double (*rsum)[CDF_ROWS] = reinterpret_cast<double (*)[CDF_ROWS]>(rsum_base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = (V + NWARP - 1) / NWARP;
+  const int seg = ((V + NWARP - 1) / NWARP + 31) & ~31;
+  const int nrow = min(seg / 32, CDF_ROWS);
   const int lo = warp * seg, hi = min(V, lo + seg);
-  double s4[4] = {0.0, 0.0, 0.0, 0.0};
-  int v = lo + lane;
-  for (; v + 96 < hi; v += 128) {
+  for (int k0 = 0; k0 < nrow; k0 += 8) {
+    float wv[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) s4[q] += (double)w(v + 32 * q);
+    for (int q = 0; q < 8; ++q) {
+      const int v = lo + 32 * (k0 + q) + lane;
+      wv[q] = (k0 + q < nrow && v < hi) ? w(v) : 0.0f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float rh = wv[q], rl = 0.0f;
+      warp_sum_ff(rh, rl);
+      if (lane == 0 && k0 + q < nrow) rsum[warp][k0 + q] = (double)rh + (double)rl;
+    }
   }
-  for (; v < hi; v += 32) s4[0] += (double)w(v);
-  const double s = warp_sum_d((s4[0] + s4[1]) + (s4[2] + s4[3]));
+  __syncwarp();
+  // lane l owns rows [l * rpl, (l + 1) * rpl): its sum in FP64, then the segment's
+  const int rpl = (nrow + 31) / 32;
+  const int r0 = lane * rpl, r1 = min(nrow, r0 + rpl);
+  double own = 0.0;
+  for (int k = r0; k < r1; ++k) own += rsum[warp][k];
+  double incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const double s = __shfl_sync(0xffffffffu, incl, 31);
   __syncthreads();
   if (lane == 0) shd[warp] = s;
   if (threadIdx.x == 0) found = -1;
@@ -295,24 +355,55 @@ __device__ int block_inverse_cdf(WF w, int V, float u) {
   const double pre = shd[warp];
   const double nxt = warp + 1 < NWARP ? shd[warp + 1] : total;
   if (s > 0.0 && pre <= target && target < nxt) {
-    double run = pre;
-    int tok = -1, last = -1;
-    for (int v0 = lo; v0 < hi; v0 += 32) {
-      const int vv = v0 + lane;
-      const float wv = vv < hi ? w(vv) : 0.0f;
-      double x = (double)wv;
+    double ex = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) ex = 0.0;
+    const unsigned hitl = __ballot_sync(0xffffffffu, own > 0.0 && pre + incl > target);
+    int row = -1;
+    double before = 0.0;
+    if (hitl) {
+      const int L = __ffs(hitl) - 1;
+      if (lane == L) {
+        double run = pre + ex;
+        for (int k = r0; k < r1; ++k) {
+          const double c = rsum[warp][k];
+          if (c > 0.0 && run + c > target) { row = k; break; }
+          run += c;
+        }
+        before = run;
+      }
+      row = __shfl_sync(0xffffffffu, row, L);
+      before = __shfl_sync(0xffffffffu, before, L);
+    }
+    int tok = -1;
+    if (row >= 0) {
+      const int v = lo + 32 * row + lane;
+      const float wv = v < hi ? w(v) : 0.0f;
+      float xh = wv, xl = 0.0f;              // inclusive float-float scan of the row
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const float yh = __shfl_up_sync(0xffffffffu, xh, o), yl = __shfl_up_sync(0xffffffffu, xl, o);
+        if (lane >= o) {
+          float sum, err;
+          two_sum(xh, yh, sum, err);
+          xh = sum;
+          xl = (xl + yl) + err;
+        }
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, vv < hi && run + x > target);
-      const unsigned pos = __ballot_sync(0xffffffffu, wv > 0.0f);
-      if (pos) last = v0 + 31 - __clz(pos);
-      if (hit) { tok = v0 + __ffs(hit) - 1; break; }
-      run += __shfl_sync(0xffffffffu, x, 31);
+      const unsigned hit = __ballot_sync(0xffffffffu, v < hi && before + ((double)xh + (double)xl) > target);
+      const unsigned posw = __ballot_sync(0xffffffffu, wv > 0.0f);
+      tok = hit ? lo + 32 * row + __ffs(hit) - 1 : (posw ? lo + 32 * row + 31 - __clz(posw) : -1);
     }
-    if (lane == 0) atomicMax(&found, tok >= 0 ? tok : last);
+    if (tok < 0) {   // rounding left the target past the rows: last row with weight, its last id
+      int last_row = -1;
+      for (int k = nrow - 1; k >= 0; --k)
+        if (rsum[warp][k] > 0.0) { last_row = k; break; }
+      if (last_row >= 0) {
+        const int v = lo + 32 * last_row + lane;
+        const unsigned posw = __ballot_sync(0xffffffffu, v < hi && w(v) > 0.0f);
+        if (posw) tok = lo + 32 * last_row + 31 - __clz(posw);
+      }
+    }
+    if (lane == 0 && tok >= 0) atomicMax(&found, tok);
   }
   __syncthreads();
   if (found < 0) {   // rounding pushed the target past the end: last id with weight
@@ -333,6 +424,7 @@ __global__ void __launch_bounds__(SNT) sample_rows_kernel(int rows, const int32_
                                                           long long row_stride, int V, float T, uint64_t seed,
                                                           uint64_t rnd, const uint32_t* sup, int32_t* out,
                                                           int out_stride, int out_col0) {
+  __shared__ double cdf_scratch[(SNT / 32) * CDF_ROWS];
   __shared__ float sh[SNT + 8];
   pdl_wait();
   const int i = blockIdx.x / rows, r = blockIdx.x - i * rows;
@@ -340,7 +432,7 @@ __global__ void __launch_bounds__(SNT) sample_rows_kernel(int rows, const int32_
   const float* z = logits + ((long long)i * rows + r) * row_stride;
   RowStat st = row_stat(z, V, T, sup, sh);
   const float u = ws_uniform(seed, (uint32_t)slot, rnd, (uint32_t)(r + 1), 0u);
-  int tok = block_inverse_cdf([&](int v) { return expf(scaled(z, v, T, sup) - st.m) / st.S; }, V, u);
+  int tok = block_inverse_cdf([&](int v) { return expf(scaled(z, v, T, sup) - st.m) / st.S; }, V, u, cdf_scratch);
   pdl_trigger();
   if (threadIdx.x == 0) out[(size_t)i * out_stride + out_col0 + r] = tok;
 }
@@ -561,6 +653,7 @@ __global__ void __launch_bounds__(128) window_attn_kernel(int H, const int32_t* 
 // ------------------------------------------------------------------ acceptance
 // One CTA per request.  Whisper-Flash §3.1 / Appendix A.1 / A.4.
 __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
+  __shared__ double cdf_scratch[(SNT / 32) * CDF_ROWS];
   __shared__ float sh[SNT + 8];
   __shared__ int s_emit[17];
   __shared__ int s_ne, s_a, s_stop;
@@ -674,8 +767,9 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
       rs = block_sum<SNT>(rs, sh);
       const float u2 = ws_uniform(A.seed, (uint32_t)slot, A.round, (uint32_t)j, 2u);
       int tok;
-      if (rs > 0.0f) tok = block_inverse_cdf(resid, P.V, u2);
-      else tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m) / sp.S; }, P.V, u2);
+      if (rs > 0.0f) tok = block_inverse_cdf(resid, P.V, u2, cdf_scratch);
+      else tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m) / sp.S; }, P.V, u2,
+                                   cdf_scratch);
       if (threadIdx.x == 0) { s_emit[s_ne++] = tok; s_stop = 2; }
       __syncthreads();
       break;
@@ -687,7 +781,8 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
       RowStat sp;
       sp.m = ps.x; sp.S = ps.y;
       const float u2 = ws_uniform(A.seed, (uint32_t)slot, A.round, (uint32_t)(n_prop + 1), 2u);
-      int tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m) / sp.S; }, P.V, u2);
+      int tok = block_inverse_cdf([&](int v) { return expf(scaled(zp, v, T, P.suppress) - sp.m) / sp.S; }, P.V, u2,
+                                  cdf_scratch);
       if (threadIdx.x == 0) s_emit[s_ne++] = tok;
     }
     __syncthreads();
