@@ -59,7 +59,7 @@ def test_query_workspace_sizes(B):
 
 
 @pytest.mark.parametrize("bad", [dict(d_model=100), dict(n_heads=5), dict(K=0), dict(K=16),
-                                 dict(max_block=3), dict(dtype=7), dict(eos_id=10 ** 6), dict(vocab=51867),
+                                 dict(max_block=3), dict(dtype=7), dict(eos_id=10 ** 6), dict(vocab=51867), dict(vocab=65538),
                                  dict(hist_layers=(0, 9)), dict(max_frames=0), dict(gemm=9)])
 def test_invalid_descriptions_rejected(B, bad):
     assert B.ws_query_workspace(_desc(B, synth.TINY, **bad)) == 0
