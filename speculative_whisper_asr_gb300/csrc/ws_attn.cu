@@ -222,14 +222,16 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, uint64_
 // (request, head)'s chunks in key order and reloads its query fragments only
 // when the head changes.  Each warp owns NSLOT 16 KB slots and keeps the K
 // and V boxes of its next NSLOT - 1 chunks in flight by TMA while it computes
-// the current one (two slots and six warps per SM measured faster than four
-// slots and three warps: per-warp compute, not latency, bounds it); a slot's
+// the current one (two slots per warp measured faster than four slots with
+// half the warps: per-warp compute, not latency, bounds it; seven warps in
+// one CTA per SM fill the shared memory); a slot's
 // mbarrier has one consumer, which takes its phases in order.  A unit's chunk partials are merged in
 // registers and stored once; a second kernel (attn_fold_kernel) folds each
 // row's group partials in group order.
-constexpr int SW = 2;                        // warps per CTA
+constexpr int SW = 7;                        // warps per CTA, one CTA per SM (7 x 32 KB of slots)
 constexpr int NSLOT = 2;                     // TMA slots per warp: the next chunk lands while one is computed
 constexpr int STREAM_SMEM = SW * NSLOT * CHUNK_BYTES + 1024;
+static_assert(STREAM_SMEM <= 227 * 1024, "streaming slots exceed the shared memory of one CTA");
 
 // MODE < 0: the mode is a.mode (one compiled copy serves self- and cross-attention)
 template <int MODE>
@@ -377,7 +379,10 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
           return self_key_mask(k_lo, nk, Lr, tree_anc(a.tree, j));
         };
         float m0, l0, m1, l1, acc[8][4];
-        attn_chunk_regs<true>(Ks, Vs, qf, vis(g), vis(g + 8), m0, l0, m1, l1, acc);
+        if (mode == MODE_CROSS && nk == WS_XCHUNK)      // a full acoustic chunk: no mask (rows >= H are not stored)
+          attn_chunk_regs<true, true, true>(Ks, Vs, qf, 0ull, 0ull, m0, l0, m1, l1, acc);
+        else
+          attn_chunk_regs<true>(Ks, Vs, qf, vis(g), vis(g + 8), m0, l0, m1, l1, acc);
         float a0[16], a1[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -584,7 +589,7 @@ template <int MODE>
 cudaError_t launch_stream(const AttnArgs& a, int n, int heads, const CUtensorMap& map, const void* kv_base,
                           cudaStream_t s, bool pdl) {
   const int total = n * heads * ((a.n_split + STREAM_GROUP - 1) / STREAM_GROUP);
-  const int cap = 3 * (g_attn_sms > 0 ? g_attn_sms : 148);       // three CTAs per SM
+  const int cap = g_attn_sms > 0 ? g_attn_sms : 148;             // one CTA per SM
   const int ctas = (total + SW - 1) / SW;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas < cap ? ctas : cap);

@@ -66,8 +66,11 @@ __device__ __forceinline__ void attn_q_frags(const bf16* q, int ldq, int q_row0,
 // ~16 mantissa bits; else as one bf16 value): lane (g = lane / 4, c = lane % 4) holds
 // rows g and g + 8: (m0, l0) and acc[j][0..1] (dims 8j + 2c, + 1) for row g,
 // (m1, l1) and acc[j][2..3] for row g + 8.  A row with no visible key has
-// m = -inf, l = 0 and zero values.
-template <bool SWZ, bool HILO = true>
+// m = -inf, l = 0 and zero values.  DENSE: every key of the chunk is
+// visible to every row (the masks are not read); the rows' arithmetic is
+// then exactly that of all-ones masks, and rows the caller does not store
+// may hold any finite values.
+template <bool SWZ, bool HILO = true, bool DENSE = false>
 __device__ __forceinline__ void attn_chunk_regs(const uint8_t* Ks, const uint8_t* Vs, const uint32_t qf[4][4],
                                                 uint64_t vis_lo, uint64_t vis_hi, float& om0, float& ol0, float& om1,
                                                 float& ol1, float acc[8][4]) {
@@ -97,8 +100,8 @@ __device__ __forceinline__ void attn_chunk_regs(const uint8_t* Ks, const uint8_t
       const int key = 8 * j + 2 * c + e;
       sc[j][e] *= 0.125f;                      // 1/sqrt(64)
       sc[j][2 + e] *= 0.125f;
-      if ((vis_lo >> key) & 1ull) m0 = fmaxf(m0, sc[j][e]);
-      if ((vis_hi >> key) & 1ull) m1 = fmaxf(m1, sc[j][2 + e]);
+      if (DENSE || ((vis_lo >> key) & 1ull)) m0 = fmaxf(m0, sc[j][e]);
+      if (DENSE || ((vis_hi >> key) & 1ull)) m1 = fmaxf(m1, sc[j][2 + e]);
     }
   }
   m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
@@ -111,8 +114,8 @@ __device__ __forceinline__ void attn_chunk_regs(const uint8_t* Ks, const uint8_t
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int key = 8 * j + 2 * c + e;
-      const float p0 = ((vis_lo >> key) & 1ull) ? expf(sc[j][e] - m0) : 0.f;
-      const float p1 = ((vis_hi >> key) & 1ull) ? expf(sc[j][2 + e] - m1) : 0.f;
+      const float p0 = (DENSE || ((vis_lo >> key) & 1ull)) ? expf(sc[j][e] - m0) : 0.f;
+      const float p1 = (DENSE || ((vis_hi >> key) & 1ull)) ? expf(sc[j][2 + e] - m1) : 0.f;
       sc[j][e] = p0;
       sc[j][2 + e] = p1;
       l0 += p0;
@@ -151,7 +154,7 @@ __device__ __forceinline__ void attn_chunk_regs(const uint8_t* Ks, const uint8_t
       if (HILO) mma_bf16_16816(acc[j2 + 1], pl, b2, b3);
     }
   }
-  const bool has0 = vis_lo != 0ull, has1 = vis_hi != 0ull;
+  const bool has0 = DENSE || vis_lo != 0ull, has1 = DENSE || vis_hi != 0ull;
   om0 = has0 ? m0 : -INFINITY;
   ol0 = has0 ? l0 : 0.f;
   om1 = has1 ? m1 : -INFINITY;
