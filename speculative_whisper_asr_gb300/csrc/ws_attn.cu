@@ -379,8 +379,10 @@ __global__ void __launch_bounds__(SW * 32) attn_stream_kernel(const __grid_const
           return self_key_mask(k_lo, nk, Lr, tree_anc(a.tree, j));
         };
         float m0, l0, m1, l1, acc[8][4];
-        if (mode == MODE_CROSS && nk == WS_XCHUNK)      // a full acoustic chunk: no mask (rows >= H are not stored)
-          attn_chunk_regs<true, true, true>(Ks, Vs, qf, 0ull, 0ull, m0, l0, m1, l1, acc);
+        // a full chunk that every valid row sees whole (acoustic frames, or
+        // cache rows before the block): each mask is all ones or empty
+        if (nk == WS_XCHUNK && (mode == MODE_CROSS || k_lo + WS_XCHUNK <= Lr))
+          attn_chunk_regs<true, true, true>(Ks, Vs, qf, vis(g), vis(g + 8), m0, l0, m1, l1, acc);
         else
           attn_chunk_regs<true>(Ks, Vs, qf, vis(g), vis(g + 8), m0, l0, m1, l1, acc);
         float a0[16], a1[16];

@@ -66,10 +66,9 @@ __device__ __forceinline__ void attn_q_frags(const bf16* q, int ldq, int q_row0,
 // ~16 mantissa bits; else as one bf16 value): lane (g = lane / 4, c = lane % 4) holds
 // rows g and g + 8: (m0, l0) and acc[j][0..1] (dims 8j + 2c, + 1) for row g,
 // (m1, l1) and acc[j][2..3] for row g + 8.  A row with no visible key has
-// m = -inf, l = 0 and zero values.  DENSE: every key of the chunk is
-// visible to every row (the masks are not read); the rows' arithmetic is
-// then exactly that of all-ones masks, and rows the caller does not store
-// may hold any finite values.
+// m = -inf, l = 0 and zero values.  DENSE: each row's mask is either all
+// ones or empty, so the per-key tests are skipped; every row's result is
+// exactly what the general path gives for the same masks.
 template <bool SWZ, bool HILO = true, bool DENSE = false>
 __device__ __forceinline__ void attn_chunk_regs(const uint8_t* Ks, const uint8_t* Vs, const uint32_t qf[4][4],
                                                 uint64_t vis_lo, uint64_t vis_hi, float& om0, float& ol0, float& om1,
@@ -154,7 +153,7 @@ __device__ __forceinline__ void attn_chunk_regs(const uint8_t* Ks, const uint8_t
       if (HILO) mma_bf16_16816(acc[j2 + 1], pl, b2, b3);
     }
   }
-  const bool has0 = DENSE || vis_lo != 0ull, has1 = DENSE || vis_hi != 0ull;
+  const bool has0 = vis_lo != 0ull, has1 = vis_hi != 0ull;
   om0 = has0 ? m0 : -INFINITY;
   ol0 = has0 ? l0 : 0.f;
   om1 = has1 ? m1 : -INFINITY;
