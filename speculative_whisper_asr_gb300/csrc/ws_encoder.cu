@@ -81,7 +81,7 @@ size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 const char* check_enc_desc(const ws_encoder_desc* d) {
   if (!d) return "null encoder description";
   if (d->n_layers < 1 || d->n_layers > 128) return "n_layers out of range";
-  if (d->d_model < 128 || d->d_model % 128 != 0 || d->d_model > 4096) return "d_model must be a multiple of 128, <= 4096";
+  if (d->d_model < 128 || d->d_model % 128 != 0 || d->d_model > 2048) return "d_model must be a multiple of 128, <= 2048";
   if (d->n_heads < 1 || d->d_model % d->n_heads != 0 || d->d_model / d->n_heads != WS_DH) return "d_model / n_heads must be 64";
   if (d->d_ff < 128 || d->d_ff % 128 != 0) return "d_ff must be a multiple of 128";
   if (d->n_mels < 1 || d->n_mels > 1024) return "n_mels out of range";

@@ -553,19 +553,47 @@ __global__ void __launch_bounds__(PERSIST_THREADS, 1)
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
       }
+      const int n = ti.tile_f * BM + row;
+      // Residual epilogue on tiles of 64 or 128 tokens: the residual values
+      // of this warp's column groups do not depend on the MMAs, so they are
+      // read before the accumulator wait instead of one round trip per group
+      // after it (the stores of a group would otherwise hold back the next
+      // group's loads: both address the residual rows).
+      constexpr bool PRE = KIND == EPI_RESID && BN >= 64 && BN <= 128;
+      constexpr int NPG = PRE ? BN / 32 : 1;
+      float xpre[NPG][16];
+      if (PRE) {
+#pragma unroll
+        for (int q = 0; q < NPG; ++q)
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int r = ti.t0 + half * 16 + 32 * q + c;
+            xpre[q][c] = (r < ti.M && n < p.N) ? __ldcg(e.resid + (size_t)r * e.ldr + n) : 0.0f;
+          }
+      }
       const uint32_t acc = local & 1u;
       const bool ok = mbar_wait(&acc_full[acc], (local >> 1) & 1u);
       if (!ok) { if (lane == 0) atomicOr(p.status, WS_ST_TIMEOUT); break; }
       tc_fence_after();
       const uint32_t taddr = tmem + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
-      const int n = ti.tile_f * BM + row;
+      if constexpr (PRE) {
+#pragma unroll
+        for (int q = 0; q < NPG; ++q) {
+          const int c0 = half * 16 + 32 * q;
+          if (ti.t0 + c0 >= ti.M) break;
+          float v[16];
+          tmem_ld16(taddr + (uint32_t)c0, v);
+          fast_epilogue16(kind, e, p.N, ti.t0 + c0, ti.M, n, ti.z, v, tok_tab, c0, xpre[q]);
+        }
+      } else {
 #pragma unroll 1
-      for (int c0 = half * 16; c0 < BN; c0 += 32) {
-        if (ti.t0 + c0 >= ti.M) break;
-        float v[16];
-        tmem_ld16(taddr + (uint32_t)c0, v);
-        if (fast) fast_epilogue16(kind, e, p.N, ti.t0 + c0, ti.M, n, ti.z, v, tok_tab, c0);
-        else epi_columns16(kind, e, p.N, ti.t0 + c0, n, ti.M, ti.z, v);
+        for (int c0 = half * 16; c0 < BN; c0 += 32) {
+          if (ti.t0 + c0 >= ti.M) break;
+          float v[16];
+          tmem_ld16(taddr + (uint32_t)c0, v);
+          if (fast) fast_epilogue16(kind, e, p.N, ti.t0 + c0, ti.M, n, ti.z, v, tok_tab, c0);
+          else epi_columns16(kind, e, p.N, ti.t0 + c0, n, ti.M, ti.z, v);
+        }
       }
       tc_fence_before();
       __syncwarp();

@@ -116,6 +116,28 @@ __device__ __forceinline__ void ln_rows_warp(const float* const* xs, int nr, int
       }
     }
   }
+  // One row (the layer-norm kernel): gains and biases of this lane's groups
+  // are loaded while the reductions run and all before the first output is
+  // written, since out stores to global memory the compiler cannot tell
+  // apart from g and b (each group's loads would otherwise wait behind the
+  // previous stores).  Several rows (a GEMM normalising its operand from
+  // shared memory): loaded per group, which keeps the registers down.
+  constexpr bool HOIST = NR == 1;
+  uint2 gq[MAXV], bq[MAXV];
+  float4 gf[MAXV], bf[MAXV];
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int k = 4 * lane + 128 * i;
+    if (HOIST && i < nv && k >= k_lo && k < k_hi) {
+      if (g_bf16) {
+        gq[i] = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(g) + (k - g_off));
+        bq[i] = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(b) + (k - g_off));
+      } else {
+        gf[i] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + (k - g_off));
+        bf[i] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(b) + (k - g_off));
+      }
+    }
+  }
   float mean[NR], rstd[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
@@ -153,20 +175,25 @@ __device__ __forceinline__ void ln_rows_warp(const float* const* xs, int nr, int
     const int k = 4 * lane + 128 * i;
     if (i < nv && k >= k_lo && k < k_hi) {
       float gg[4], bv[4];
+      if (!HOIST) {
+        if (g_bf16) {
+          gq[i] = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(g) + (k - g_off));
+          bq[i] = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(b) + (k - g_off));
+        } else {
+          gf[i] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + (k - g_off));
+          bf[i] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(b) + (k - g_off));
+        }
+      }
       if (g_bf16) {
-        const uint2 gq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(g) + (k - g_off));
-        const uint2 bq = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(b) + (k - g_off));
-        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.x));
-        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq.y));
-        const float2 b01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.x));
-        const float2 b23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq.y));
+        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq[i].x));
+        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gq[i].y));
+        const float2 b01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq[i].x));
+        const float2 b23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bq[i].y));
         gg[0] = g01.x; gg[1] = g01.y; gg[2] = g23.x; gg[3] = g23.y;
         bv[0] = b01.x; bv[1] = b01.y; bv[2] = b23.x; bv[3] = b23.y;
       } else {
-        const float4 gq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + (k - g_off));
-        const float4 bq = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(b) + (k - g_off));
-        gg[0] = gq.x; gg[1] = gq.y; gg[2] = gq.z; gg[3] = gq.w;
-        bv[0] = bq.x; bv[1] = bq.y; bv[2] = bq.z; bv[3] = bq.w;
+        gg[0] = gf[i].x; gg[1] = gf[i].y; gg[2] = gf[i].z; gg[3] = gf[i].w;
+        bv[0] = bf[i].x; bv[1] = bf[i].y; bv[2] = bf[i].z; bv[3] = bf[i].w;
       }
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
@@ -178,11 +205,11 @@ __device__ __forceinline__ void ln_rows_warp(const float* const* xs, int nr, int
   }
 }
 
-template <bool CG = false, class Out>
+template <bool CG = false, int MAXV = 16, class Out>
 __device__ __forceinline__ void ln_row_warp(const float* x, int d, const void* g, const void* b, bool g_bf16,
                                             Out out) {
   const float* xs[1] = {x};
-  ln_rows_warp<CG, 1, 16>(xs, 1, d, g, b, g_bf16,
+  ln_rows_warp<CG, 1, MAXV>(xs, 1, d, g, b, g_bf16,
                           [&](int, int k, float v0, float v1, float v2, float v3) { out(k, v0, v1, v2, v3); });
 }
 

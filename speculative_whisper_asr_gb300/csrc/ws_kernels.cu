@@ -102,8 +102,9 @@ __global__ void embed_draft_kernel(int K1, const int32_t* req_ids, const int32_t
 // group_skip > 0: output row o reads input row (o / (G-1)) * G + o % (G-1) + 1
 // (drops row 0 of every group of G rows: the drafter's anchor row).
 // One warp per row (ln_row_warp), four rows per CTA; bf16 rows are stored
-// four values (8 bytes) at a time.
-template <typename T>
+// four values (8 bytes) at a time.  MAXV: register groups of 128 features
+// (d <= 128 * MAXV).
+template <typename T, int MAXV>
 __global__ void __launch_bounds__(128) layernorm_kernel(int M, int d, const float* x, int ldx, const T* g,
                                                         const T* b, T* y, int ldy, int group_skip) {
   pdl_trigger();
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(128) layernorm_kernel(int M, int d, const floa
     src = (o / G1) * group_skip + (o % G1) + 1;
   }
   T* yr = y + (size_t)o * ldy;
-  ln_row_warp(x + (size_t)src * ldx, d, g, b, sizeof(T) == 2, [&](int k, float a0, float a1, float a2, float a3) {
+  ln_row_warp<false, MAXV>(x + (size_t)src * ldx, d, g, b, sizeof(T) == 2, [&](int k, float a0, float a1, float a2, float a3) {
     if constexpr (sizeof(T) == 2) {
       __nv_bfloat162 h0 = __floats2bfloat162_rn(a0, a1), h1 = __floats2bfloat162_rn(a2, a3);
       uint2 w;
@@ -946,10 +947,12 @@ template <typename T>
 cudaError_t launch_layernorm(int M, int d, const float* x, int ldx, const T* g, const T* b, T* y, int ldy,
                              int group_skip, cudaStream_t s, bool pdl) {
   if (M <= 0) return cudaSuccess;
+  if (d % 128 != 0 || d > 2048) return cudaErrorInvalidValue;
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3((M + 3) / 4), dim3(128), 0, s, pdl, at);
   ws_count_launches(1);
-  return cudaLaunchKernelEx(&cfg, layernorm_kernel<T>, M, d, x, ldx, g, b, y, ldy, group_skip);
+  return cudaLaunchKernelEx(&cfg, d <= 1280 ? layernorm_kernel<T, 10> : layernorm_kernel<T, 16>, M, d, x, ldx, g, b, y,
+                            ldy, group_skip);
 }
 cudaError_t launch_argmax_init(int M, unsigned long long* keys, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute at[1];
