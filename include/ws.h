@@ -421,10 +421,12 @@ void ws_free(ws_ctx* ctx);
 typedef struct ws_enc ws_enc;
 
 typedef struct {
-  int32_t n_layers, d_model, n_heads, d_ff;   /* large-v3: 32, 1280, 20, 5120 */
-  int32_t n_mels;                             /* 128 (large-v3), 80 (tiny) */
-  int32_t n_frames;                           /* output positions F (1500 for 30 s); input 2F mel frames */
-  int32_t max_batch;                          /* windows per ws_encode call */
+  int32_t n_layers, d_model, n_heads, d_ff;   /* large-v3: 32, 1280, 20, 5120; n_layers 1..128, d_model a
+                                                 multiple of 128 up to 2048 with 64 per head, d_ff a
+                                                 multiple of 128 */
+  int32_t n_mels;                             /* 128 (large-v3), 80 (tiny); 1..1024 */
+  int32_t n_frames;                           /* output positions F (1500 for 30 s); input 2F mel frames; <= 16384 */
+  int32_t max_batch;                          /* windows per ws_encode call; 1..256 */
 } ws_encoder_desc;
 
 /* Workspace bytes for the encoder (weights, repacked convolutions, position

@@ -100,3 +100,27 @@ def test_product_path_does_not_import_oracle():
         if fn.endswith(".py"):
             src = open(os.path.join(ROOT, "oracle", fn)).read()
             assert "speculative_whisper_asr_gb300" not in src, fn
+
+
+def _enc_desc(B, **kw):
+    s = synth.ENC_LARGE_V3
+    args = dict(n_layers=s.n_layers, d_model=s.d_model, n_heads=s.n_heads, d_ff=s.d_ff, n_mels=s.n_mels,
+                n_frames=s.n_frames, max_batch=16)
+    args.update(kw)
+    return B.make_encoder_desc(**args)
+
+
+def test_encoder_workspace_size():
+    """Large-v3 encoder, 16 windows: 0.64 G bf16 weights plus the activations
+    of 24,000 rows (a few GB), well inside one GPU."""
+    from speculative_whisper_asr_gb300 import binding as B
+    n = B.ws_encoder_workspace(_enc_desc(B))
+    assert 1.0e9 < n < 8.0e9, n
+
+
+@pytest.mark.parametrize("bad", [dict(d_model=100), dict(d_model=2176, n_heads=34), dict(n_heads=7),
+                                 dict(d_ff=100), dict(n_layers=0), dict(n_mels=0), dict(n_frames=0),
+                                 dict(max_batch=0)])
+def test_invalid_encoder_descriptions_rejected(bad):
+    from speculative_whisper_asr_gb300 import binding as B
+    assert B.ws_encoder_workspace(_enc_desc(B, **bad)) == 0
