@@ -138,6 +138,58 @@ __global__ void __launch_bounds__(128) layernorm_kernel(int M, int d, const floa
   });
 }
 
+// Many rows (the encoder's 1500 per window): gain and bias are staged in
+// shared memory once per CTA, and each warp normalises LN_RPW consecutive
+// rows two at a time (both rows' loads in one memory round trip), with the
+// same per-row arithmetic as layernorm_kernel.
+constexpr int LN_RPW = 4;
+constexpr int LN_MANY = 4096;     // rows from which a call takes this kernel
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(128) layernorm_rows_kernel(int M, int d, const float* x, int ldx, const T* g,
+                                                             const T* b, T* y, int ldy, int group_skip) {
+  __shared__ __align__(16) T gb[2][128 * MAXV];
+  pdl_trigger();
+  constexpr int PER = 8 / sizeof(T);             // elements per 8-byte copy
+  for (int i = threadIdx.x * PER; i < d; i += 128 * PER) {
+    *reinterpret_cast<uint2*>(&gb[0][i]) = *reinterpret_cast<const uint2*>(g + i);
+    *reinterpret_cast<uint2*>(&gb[1][i]) = *reinterpret_cast<const uint2*>(b + i);
+  }
+  __syncthreads();
+  pdl_wait();
+  const int o0 = (blockIdx.x * 4 + (threadIdx.x >> 5)) * LN_RPW;
+  for (int j = 0; j < LN_RPW; j += 2) {
+    const int oa = o0 + j;
+    if (oa >= M) break;
+    const int nr = min(2, M - oa);
+    const float* xs[2];
+    T* ys[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int o = oa + (r < nr ? r : 0);
+      int src = o;
+      if (group_skip > 0) {
+        const int G1 = group_skip - 1;
+        src = (o / G1) * group_skip + (o % G1) + 1;
+      }
+      xs[r] = x + (size_t)src * ldx;
+      ys[r] = y + (size_t)o * ldy;
+    }
+    ln_rows_warp<false, 2, MAXV>(xs, nr, d, gb[0], gb[1], sizeof(T) == 2,
+                                 [&](int r, int k, float a0, float a1, float a2, float a3) {
+      T* yr = ys[r];
+      if constexpr (sizeof(T) == 2) {
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(a0, a1), h1 = __floats2bfloat162_rn(a2, a3);
+        uint2 w;
+        w.x = *reinterpret_cast<uint32_t*>(&h0);
+        w.y = *reinterpret_cast<uint32_t*>(&h1);
+        *reinterpret_cast<uint2*>(yr + k) = w;
+      } else {
+        yr[k] = from_f<T>(a0); yr[k + 1] = from_f<T>(a1); yr[k + 2] = from_f<T>(a2); yr[k + 3] = from_f<T>(a3);
+      }
+    });
+  }
+}
+
 // ------------------------------------------------------------------ argmax
 __global__ void argmax_init_kernel(int M, unsigned long long* keys) {
   pdl_wait();
@@ -949,6 +1001,12 @@ cudaError_t launch_layernorm(int M, int d, const float* x, int ldx, const T* g, 
   if (M <= 0) return cudaSuccess;
   if (d % 128 != 0 || d > 2048) return cudaErrorInvalidValue;
   cudaLaunchAttribute at[1];
+  if (M >= LN_MANY) {
+    cudaLaunchConfig_t cfg = make_cfg(dim3((M + 4 * LN_RPW - 1) / (4 * LN_RPW)), dim3(128), 0, s, pdl, at);
+    ws_count_launches(1);
+    return cudaLaunchKernelEx(&cfg, d <= 1280 ? layernorm_rows_kernel<T, 10> : layernorm_rows_kernel<T, 16>, M, d, x,
+                              ldx, g, b, y, ldy, group_skip);
+  }
   cudaLaunchConfig_t cfg = make_cfg(dim3((M + 3) / 4), dim3(128), 0, s, pdl, at);
   ws_count_launches(1);
   return cudaLaunchKernelEx(&cfg, d <= 1280 ? layernorm_kernel<T, 10> : layernorm_kernel<T, 16>, M, d, x, ldx, g, b, y,
