@@ -121,21 +121,24 @@ __device__ __forceinline__ void epi_columns16(int kind, const Epi& e, int N, int
   const int lane = threadIdx.x & 31;
   const int mc = min(M, t + c_hi), m0 = t + c_lo;     // rows m0 <= r < mc
   if (kind == EPI_LOGITS) {
+    const bool ok = n < N;
+    const bool sup = ok && e.suppress && ((e.suppress[n >> 5] >> (n & 31)) & 1u);   // one lookup per feature
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int r = t + c;
-      unsigned long long key = 0ull;
-      if (r >= m0 && r < mc && n < N) {
-        const float y = epi_logit(e, n, v[c]);
-        if (e.logits) e.logits[(long long)r * e.ldl + n] = y;
-        key = argmax_key(y, n);
-      }
+      if (r < m0 || r >= mc) continue;              // the same row for every lane
+      const float y = ok && !sup ? v[c] : -INFINITY;
+      if (ok && e.logits) e.logits[(long long)r * e.ldl + n] = y;
+      if (e.amax) {
+        // The warp's largest value, then the lowest lane holding it (the
+        // lanes' ids are consecutive): for finite and infinite logits this is
+        // the key a reduction of (value, id) keys gives, -0 tying with +0.
+        float m = y;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-        key = other > key ? other : key;
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const unsigned hit = __ballot_sync(0xffffffffu, ok && y == m);
+        if (hit && lane == __ffs(hit) - 1) atomicMax(e.amax + r, argmax_key(m, n));
       }
-      if (lane == 0 && key != 0ull && e.amax) atomicMax(e.amax + r, key);
     }
     return;
   }
