@@ -815,9 +815,27 @@ __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
         float qv = expf(scaled(zq, v, T, P.suppress) - sq.m) / sq.S;
         return fmaxf(pv - qv, 0.0f);
       };
-      float rs = 0.0f;
-      for (int v = threadIdx.x; v < P.V; v += SNT) rs += resid(v);
-      rs = block_sum<SNT>(rs, sh);
+      // its mass (only whether it is positive matters): eight ids of both
+      // rows loaded at once per thread, since the rows stream from HBM
+      float r4[4] = {0.f, 0.f, 0.f, 0.f};
+      int v = threadIdx.x;
+      for (; v + 7 * SNT < P.V; v += 8 * SNT) {
+        float zpv[8], zqv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          zpv[q] = __ldg(zp + v + q * SNT);
+          zqv[q] = __ldg(zq + v + q * SNT);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int vq = v + q * SNT;
+          const float pv = expf(scaled_val(zpv[q], vq, T, P.suppress) - sp.m) / sp.S;
+          const float qv = expf(scaled_val(zqv[q], vq, T, P.suppress) - sq.m) / sq.S;
+          r4[q & 3] += fmaxf(pv - qv, 0.0f);
+        }
+      }
+      for (; v < P.V; v += SNT) r4[0] += resid(v);
+      const float rs = block_sum<SNT>((r4[0] + r4[1]) + (r4[2] + r4[3]), sh);
       const float u2 = ws_uniform(A.seed, (uint32_t)slot, A.round, (uint32_t)j, 2u);
       int tok;
       if (rs > 0.0f) tok = block_inverse_cdf(resid, P.V, u2, cdf_scratch);
