@@ -344,48 +344,55 @@ __device__ __forceinline__ void warp_sum_ff(float& hi, float& lo) {
 
 // Inverse CDF over non-negative weights w(v), v = 0..V-1 in ascending id
 // order: the smallest v whose running sum exceeds u * sum(w).  Warp k owns
-// the contiguous ids [k * seg, (k + 1) * seg), seg a multiple of 32; its
-// lanes read them one 32-id row at a time (coalesced, eight rows in flight)
-// and keep every row's sum (float-float, stored as FP64) in shared memory.
-// Segment sums are prefixed in warp order; the warp whose segment holds the
-// target finds the row from the row sums (a lane scan over contiguous row
-// ranges, FP64), then the id inside the row with an inclusive float-float
-// warp scan, so only that one row is read twice.
-constexpr int CDF_ROWS = 256;      // rows per warp: V <= 8 * 256 * 32 = 65,536
-// rsum_base: the caller's shared scratch of (SNT / 32) * CDF_ROWS doubles (one per kernel).
+// the contiguous ids [k * seg, (k + 1) * seg), seg a multiple of 256: 256-id
+// super-rows of eight coalesced 32-id rows.  Each lane sums its eight ids of
+// a super-row with TwoSum and the warp combines the lanes (float-float), so
+// every super-row's sum is exact to ~2^-48 and is kept (as FP64) in shared
+// memory; sixteen ids per lane are in flight.  Segment sums are prefixed in
+// warp order; the warp whose segment holds the target finds the super-row
+// from the sums (one per lane, FP64 scan), reloads its eight rows to find the
+// row, then the id inside the row with an inclusive float-float warp scan.
+constexpr int CDF_SUPER = 8;        // 32-id rows per super-row
+constexpr int CDF_SROWS = 32;       // super-rows per warp: V <= 8 * 32 * 256 = 65,536
+// rsum_base: the caller's shared scratch of (SNT / 32) * CDF_SROWS doubles (one per kernel).
 template <class WF>
 __device__ int block_inverse_cdf(WF w, int V, float u, double* rsum_base) {
-  // The weights are FP32 probabilities; their running sums are kept exact
-  // (float-float rows, FP64 across rows) so that the drawn id depends on the
-  // weights, not on the summation order.
-  constexpr int NWARP = SNT / 32;
+  // The weights are FP32 probabilities; their running sums are kept exact so
+  // that the drawn id depends on the weights, not on the summation order.
+  constexpr int NWARP = SNT / 32, SR = CDF_SUPER * 32;
   __shared__ int found;
   __shared__ double shd[NWARP + 1];
-  double (*rsum)[CDF_ROWS] = reinterpret_cast<double (*)[CDF_ROWS]>(rsum_base);
+  double (*rsum)[CDF_SROWS] = reinterpret_cast<double (*)[CDF_SROWS]>(rsum_base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = ((V + NWARP - 1) / NWARP + 31) & ~31;
-  const int nrow = min(seg / 32, CDF_ROWS);
+  const int seg = ((V + NWARP - 1) / NWARP + SR - 1) / SR * SR;
+  const int nsr = min(seg / SR, CDF_SROWS);
   const int lo = warp * seg, hi = min(V, lo + seg);
-  for (int k0 = 0; k0 < nrow; k0 += 8) {
-    float wv[8];
+  for (int s0 = 0; s0 < nsr; s0 += 2) {
+    float wv[2][CDF_SUPER];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int v = lo + 32 * (k0 + q) + lane;
-      wv[q] = (k0 + q < nrow && v < hi) ? w(v) : 0.0f;
-    }
+    for (int p = 0; p < 2; ++p)
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float rh = wv[q], rl = 0.0f;
-      warp_sum_ff(rh, rl);
-      if (lane == 0 && k0 + q < nrow) rsum[warp][k0 + q] = (double)rh + (double)rl;
+      for (int q = 0; q < CDF_SUPER; ++q) {
+        const int v = lo + SR * (s0 + p) + 32 * q + lane;
+        wv[p][q] = (s0 + p < nsr && v < hi) ? w(v) : 0.0f;
+      }
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      float h = 0.0f, l = 0.0f;
+#pragma unroll
+      for (int q = 0; q < CDF_SUPER; ++q) {
+        float sm, er;
+        two_sum(h, wv[p][q], sm, er);
+        h = sm;
+        l += er;
+      }
+      warp_sum_ff(h, l);
+      if (lane == 0 && s0 + p < nsr) rsum[warp][s0 + p] = (double)h + (double)l;
     }
   }
   __syncwarp();
-  // lane l owns rows [l * rpl, (l + 1) * rpl): its sum in FP64, then the segment's
-  const int rpl = (nrow + 31) / 32;
-  const int r0 = lane * rpl, r1 = min(nrow, r0 + rpl);
-  double own = 0.0;
-  for (int k = r0; k < r1; ++k) own += rsum[warp][k];
+  // lane l owns super-row l: its sum in FP64, then the segment's
+  const double own = lane < nsr ? rsum[warp][lane] : 0.0;
   double incl = own;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -410,50 +417,62 @@ __device__ int block_inverse_cdf(WF w, int V, float u, double* rsum_base) {
   if (s > 0.0 && pre <= target && target < nxt) {
     double ex = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane == 0) ex = 0.0;
-    const unsigned hitl = __ballot_sync(0xffffffffu, own > 0.0 && pre + incl > target);
-    int row = -1;
-    double before = 0.0;
-    if (hitl) {
-      const int L = __ffs(hitl) - 1;
-      if (lane == L) {
-        double run = pre + ex;
-        for (int k = r0; k < r1; ++k) {
-          const double c = rsum[warp][k];
-          if (c > 0.0 && run + c > target) { row = k; break; }
-          run += c;
-        }
-        before = run;
-      }
-      row = __shfl_sync(0xffffffffu, row, L);
-      before = __shfl_sync(0xffffffffu, before, L);
-    }
+    const unsigned hits = __ballot_sync(0xffffffffu, own > 0.0 && pre + incl > target);
     int tok = -1;
-    if (row >= 0) {
-      const int v = lo + 32 * row + lane;
-      const float wv = v < hi ? w(v) : 0.0f;
-      float xh = wv, xl = 0.0f;              // inclusive float-float scan of the row
+    if (hits) {
+      const int sr = __ffs(hits) - 1;
+      double before = pre + __shfl_sync(0xffffffffu, ex, sr);
+      const int base = lo + SR * sr;
+      float wv[CDF_SUPER];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float yh = __shfl_up_sync(0xffffffffu, xh, o), yl = __shfl_up_sync(0xffffffffu, xl, o);
-        if (lane >= o) {
-          float sum, err;
-          two_sum(xh, yh, sum, err);
-          xh = sum;
-          xl = (xl + yl) + err;
+      for (int q = 0; q < CDF_SUPER; ++q) {
+        const int v = base + 32 * q + lane;
+        wv[q] = v < hi ? w(v) : 0.0f;
+      }
+      // the super-row's rows in order (exact sums, the same in every lane);
+      // if rounding leaves the target past them: the last row with weight
+      int row = -1, lrow = -1;
+      float rw = 0.0f, lrw = 0.0f;
+#pragma unroll
+      for (int q = 0; q < CDF_SUPER; ++q) {
+        float h = wv[q], l = 0.0f;
+        warp_sum_ff(h, l);
+        const double c = (double)h + (double)l;
+        if (c > 0.0) { lrow = q; lrw = wv[q]; }
+        if (row < 0) {
+          if (c > 0.0 && before + c > target) { row = q; rw = wv[q]; }
+          else before += c;
         }
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, v < hi && before + ((double)xh + (double)xl) > target);
-      const unsigned posw = __ballot_sync(0xffffffffu, wv > 0.0f);
-      tok = hit ? lo + 32 * row + __ffs(hit) - 1 : (posw ? lo + 32 * row + 31 - __clz(posw) : -1);
+      const bool past = row < 0;
+      if (past) { row = lrow; rw = lrw; }
+      if (row >= 0) {
+        const int v = base + 32 * row + lane;
+        float xh = rw, xl = 0.0f;              // inclusive float-float scan of the row
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float yh = __shfl_up_sync(0xffffffffu, xh, o), yl = __shfl_up_sync(0xffffffffu, xl, o);
+          if (lane >= o) {
+            float sum, err;
+            two_sum(xh, yh, sum, err);
+            xh = sum;
+            xl = (xl + yl) + err;
+          }
+        }
+        const unsigned hit =
+            __ballot_sync(0xffffffffu, !past && v < hi && before + ((double)xh + (double)xl) > target);
+        const unsigned posw = __ballot_sync(0xffffffffu, rw > 0.0f);
+        tok = hit ? base + 32 * row + __ffs(hit) - 1 : (posw ? base + 32 * row + 31 - __clz(posw) : -1);
+      }
     }
-    if (tok < 0) {   // rounding left the target past the rows: last row with weight, its last id
-      int last_row = -1;
-      for (int k = nrow - 1; k >= 0; --k)
-        if (rsum[warp][k] > 0.0) { last_row = k; break; }
-      if (last_row >= 0) {
-        const int v = lo + 32 * last_row + lane;
-        const unsigned posw = __ballot_sync(0xffffffffu, v < hi && w(v) > 0.0f);
-        if (posw) tok = lo + 32 * last_row + 31 - __clz(posw);
+    if (tok < 0) {   // rounding left the target past the rows: last id with weight in the segment
+      for (int k = nsr - 1; k >= 0 && tok < 0; --k) {
+        if (!(rsum[warp][k] > 0.0)) continue;
+        for (int q = CDF_SUPER - 1; q >= 0 && tok < 0; --q) {
+          const int v = lo + SR * k + 32 * q + lane;
+          const unsigned posw = __ballot_sync(0xffffffffu, v < hi && w(v) > 0.0f);
+          if (posw) tok = lo + SR * k + 32 * q + 31 - __clz(posw);
+        }
       }
     }
     if (lane == 0 && tok >= 0) atomicMax(&found, tok);
@@ -477,7 +496,7 @@ __global__ void __launch_bounds__(SNT) sample_rows_kernel(int rows, const int32_
                                                           long long row_stride, int V, float T, uint64_t seed,
                                                           uint64_t rnd, const uint32_t* sup, int32_t* out,
                                                           int out_stride, int out_col0) {
-  __shared__ double cdf_scratch[(SNT / 32) * CDF_ROWS];
+  __shared__ double cdf_scratch[(SNT / 32) * CDF_SROWS];
   __shared__ float sh[SNT + 8];
   pdl_wait();
   const int i = blockIdx.x / rows, r = blockIdx.x - i * rows;
@@ -706,7 +725,7 @@ __global__ void __launch_bounds__(128) window_attn_kernel(int H, const int32_t* 
 // ------------------------------------------------------------------ acceptance
 // One CTA per request.  Whisper-Flash §3.1 / Appendix A.1 / A.4.
 __global__ void __launch_bounds__(SNT) accept_kernel(AcceptParams P) {
-  __shared__ double cdf_scratch[(SNT / 32) * CDF_ROWS];
+  __shared__ double cdf_scratch[(SNT / 32) * CDF_SROWS];
   __shared__ float sh[SNT + 8];
   __shared__ int s_emit[17];
   __shared__ int s_ne, s_a, s_stop;
