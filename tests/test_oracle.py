@@ -476,6 +476,46 @@ def _grid_uniform(n):
     return (np.arange(n) + 0.5) / n
 
 
+def test_inverse_cdf_and_fp32_softmax_by_hand():
+    """Sampling helpers pinned by hand and by brute force: the inverse CDF
+    returns the smallest id whose running sum exceeds u * total (zero-weight
+    ids are never drawn, u = 0 gives the first id with weight); the FP32
+    softmax at temperature T equals torch's float64 softmax of z / T within
+    FP32 rounding and gives suppressed ids probability zero."""
+    w = np.array([0.0, 1.0, 0.0, 2.0, 0.0])
+    # running sums 0, 1, 1, 3, 3: by hand
+    assert M.sample_inverse_cdf(w, 0.0) == 1
+    assert M.sample_inverse_cdf(w, 0.3) == 1          # 0.9 < 1
+    assert M.sample_inverse_cdf(w, 1 / 3 + 1e-9) == 3
+    assert M.sample_inverse_cdf(w, 0.999999) == 3
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        n = int(rng.integers(1, 40))
+        ww = rng.random(n) * (rng.random(n) < 0.6)
+        if ww.sum() == 0:
+            ww[int(rng.integers(0, n))] = 1.0
+        u = float(rng.random())
+        tgt = u * ww.sum()
+        run, want = 0.0, None
+        for v in range(n):                             # brute force: first id past the target
+            run += ww[v]
+            if run > tgt:
+                want = v
+                break
+        assert M.sample_inverse_cdf(ww, u) == want
+        assert ww[want] > 0
+    z = rng.normal(size=300).astype(np.float32)
+    sup = [0, 7, 299]
+    for T in (0.7, 1.0, 1.5):
+        p = M.probs_fp32(z, T, sup)
+        assert p.dtype == np.float32 and np.all(p[sup] == 0)
+        zz = torch.tensor(z.astype(np.float64) / T)
+        zz[sup] = -math.inf
+        ref = torch.softmax(zz, 0).numpy()
+        np.testing.assert_allclose(p, ref, rtol=2e-6, atol=1e-9)
+        assert abs(float(p.astype(np.float64).sum()) - 1.0) < 1e-5
+
+
 def test_rejection_rule_preserves_target_distribution_exactly():
     """Quadrature over the acceptance and residual uniforms: the first
     emitted token's distribution equals p (Leviathan et al. / Chen et al.,
